@@ -1,0 +1,123 @@
+/*
+ * gdn_oracle.h -- fp64 CPU oracle for the Gated DeltaNet mixer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This oracle is the slow, plain definition that the
+ * CUDA library is checked against.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load it.  It shares no code, header, table or
+ * helper with the CUDA path, and the CUDA path never calls it.
+ *
+ * What it computes (sources):
+ *  - The recurrent state: one matrix per value head, updated in place once per
+ *    token, fixed size, never re-allocated.  TandemLLM "Architecture" (v0.14.2)
+ *    section 8.1, table of layer kinds (48 Gated DeltaNet layers, fp32 state of
+ *    48 heads x 128 x 128 plus a 4-wide convolution tail per layer);
+ *    "Serving A Research Architecture On CPU", the constant-state section
+ *    (rank-1 update of a fixed [d, d] matrix per head, no allocation in the loop).
+ *  - The gated delta rule for one token, a block and a tree: TandemLLM
+ *    "Architecture" (v0.11.1), "The parts" diagram, recurrent-layer kernels box.
+ *    The pages name the rule but print no equation; the recurrence used is the
+ *    published Gated DeltaNet update (Yang, Kautz & Hatamizadeh, "Gated Delta
+ *    Networks: Improving Mamba2 with Delta Rule", 2024, eq. for S_t):
+ *        S <- alpha * S * (I - beta * k k^T) + beta * v k^T,   o = S q
+ *    with q, k L2-normalised per key head and a 4-tap causal depthwise
+ *    convolution + SiLU in front of q, k, v.
+ *  - Tree verify and commit: "Architecture" (v0.14.2) section 8.3 and the
+ *    v0.11.1 round sequence diagram: a tree of up to 32 draft nodes is verified
+ *    in one pass, each node's state branched from its parent's, and the state of
+ *    the accepted root-to-node path is then kept exactly.
+ *
+ * Layouts (row-major, all dense):
+ *   qkv    bf16 [.., C_qkv] with C_qkv = 2*Hk*dk + Hv*dv, channels [q | k | v],
+ *          q and k head-major (key head g occupies channels g*dk .. g*dk+dk-1).
+ *   alpha, beta  fp32 [.., Hv]
+ *   state  fp64 [Hv, dv, dk]   (row i of S_h is contiguous over the key index j)
+ *   out    fp64 [.., Hv, dv]
+ *   conv   x bf16 [.., C], w bf16 [C, W], tail bf16 [W, C] oldest first, W = 4.
+ * Value head h reads key head h / (Hv / Hk).
+ *
+ * Error behaviour: functions that validate (tree / path checks) return 0 or a
+ * negative code; the numeric functions assume valid arguments (test code).
+ */
+#ifndef GDN_ORACLE_H
+#define GDN_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- bf16 storage conversion -------------------------------------------- */
+double   orc_bf16_to_f64(uint16_t h);
+uint16_t orc_f64_to_bf16(double x);           /* round to nearest, ties to even */
+void     orc_bf16_to_f64_n(const uint16_t* h, double* out, int64_t n);
+void     orc_f64_to_bf16_n(const double* x, uint16_t* out, int64_t n);
+
+/* ---- short causal convolution + SiLU ------------------------------------ */
+double orc_silu(double z);
+
+/* Linear run: per sequence b, inputs x[b, 0..T-1, :] follow the history held in
+ * tail[b] (W inputs, oldest first).  y[b,t,c] = SiLU(sum_j w[c][j] * u_j) where
+ * u_{W-1} is x[b,t,c] and u_{W-1-m} is the m-th earlier input.  tail[b] is
+ * replaced by the last W inputs of (tail ++ x).  y is fp64 (not rounded). */
+void orc_conv_linear(int B, int T, int C, int W, const uint16_t* x,
+                     const uint16_t* w, uint16_t* tail, double* y);
+
+/* Tree run (one sequence): node n's earlier inputs are its ancestors' inputs,
+ * nearest first, and then the committed tail.  tail is not modified. */
+void orc_conv_tree(int N, int C, int W, const int32_t* parents, const uint16_t* x,
+                   const uint16_t* w, const uint16_t* tail, double* y);
+
+/* ---- tree bookkeeping ---------------------------------------------------- */
+/* 0 if parents[] describes one tree rooted at node 0 (parents[0] == -1 and
+ * 0 <= parents[i] < i for i > 0); negative otherwise.  depth[n] (optional)
+ * gets the number of nodes on the root..n path (root depth 1). */
+int orc_tree_check(int N, const int32_t* parents, int32_t* depth);
+/* Root-to-node path of `node`; returns its length. */
+int orc_root_path(int N, const int32_t* parents, int node, int32_t* path);
+/* 0 if path[0..L-1] is a root-to-node path of the tree, negative otherwise. */
+int orc_path_check(int N, const int32_t* parents, const int32_t* path, int L);
+
+/* ---- gated delta rule ---------------------------------------------------- */
+/* out = x / sqrt(sum x^2 + eps) */
+void orc_l2norm(const double* x, int n, double eps, double* out);
+
+/* One token on one value head, row form (S is dv x dk, row-major):
+ *   a_i = s_i . k ;  s_i <- alpha*s_i + beta*(v_i - alpha*a_i) * k
+ * then o = S_new q computed as a plain matrix-vector product. */
+void orc_delta_token(int dk, int dv, double* S, const double* k, const double* v,
+                     const double* q, double alpha, double beta, double* o);
+
+/* The same token written as the textbook matrix product, with explicit dk x dk
+ * and dv x dk temporaries:  S <- alpha * S (I - beta k k^T) + beta v k^T. */
+void orc_delta_token_matrix(int dk, int dv, double* S, const double* k,
+                            const double* v, const double* q, double alpha,
+                            double beta, double* o);
+
+/* T sequential tokens for B independent sequences.
+ * qkv bf16 [B,T,C_qkv]; alpha, beta fp32 [B,T,Hv]; state fp64 [B,Hv,dv,dk]
+ * (in/out); out fp64 [B,T,Hv,dv].  normalize != 0 applies the L2 norm to q, k
+ * (eps = 1e-6); q is then multiplied by q_scale. */
+void orc_decode(int B, int T, int Hk, int Hv, int dk, int dv, const uint16_t* qkv,
+                const float* alpha, const float* beta, double* state, double* out,
+                double q_scale, int normalize);
+
+/* Tree verify (one sequence): node n's state is the committed state advanced
+ * through the root..n path; out[n] is that node's output.  Computed by replaying
+ * each node's root path from the committed state (state is not modified). */
+void orc_tree_verify(int N, int Hk, int Hv, int dk, int dv, const int32_t* parents,
+                     const uint16_t* qkv, const float* alpha, const float* beta,
+                     const double* state, double* out, double q_scale, int normalize);
+
+/* Commit: advance state through the accepted path's nodes, in order.  If
+ * x_tree is not NULL, tail [W, C] becomes the last W inputs of
+ * (tail ++ x_tree[path[0]] ++ ... ++ x_tree[path[L-1]]). */
+void orc_commit(int N, int Hk, int Hv, int dk, int dv, const int32_t* parents,
+                const int32_t* path, int L, const uint16_t* qkv, const float* alpha,
+                const float* beta, const uint16_t* x_tree, int W, double* state,
+                uint16_t* tail, int normalize);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
