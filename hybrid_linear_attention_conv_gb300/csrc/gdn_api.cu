@@ -1,0 +1,353 @@
+// gdn_api.cu -- host side of the C ABI declared in include/gdn.h: argument
+// validation, tree bookkeeping and kernel launches.  Every check runs before
+// anything is enqueued, so a failing call leaves all buffers untouched and
+// the stream unchanged.  Unsupported shapes are refused with an error code
+// rather than run (the lesson of the hardcoded head-size bug in "Serving A
+// Research Architecture On CPU").  Nothing here allocates device memory.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "gdn_internal.h"
+
+using namespace gdn;
+
+namespace {
+
+thread_local std::string t_error;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_error = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(GDN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool head_size_ok(int d) { return d == 32 || d == 64 || d == 128; }
+
+int check_shape(const gdn_shape* s, bool need_single) {
+    if (s == nullptr) return fail(GDN_ERR_INVALID_ARG, "shape is NULL");
+    if (s->B < 0 || s->Hk < 1 || s->Hv < 1)
+        return fail(GDN_ERR_UNSUPPORTED_SHAPE, "bad head counts / batch: B=%d Hk=%d Hv=%d", s->B,
+                    s->Hk, s->Hv);
+    if (s->Hv % s->Hk != 0)
+        return fail(GDN_ERR_UNSUPPORTED_SHAPE, "Hv=%d is not a multiple of Hk=%d", s->Hv, s->Hk);
+    if (!head_size_ok(s->dk) || !head_size_ok(s->dv))
+        return fail(GDN_ERR_UNSUPPORTED_SHAPE, "head sizes dk=%d dv=%d not in {32, 64, 128}", s->dk,
+                    s->dv);
+    if (s->Hv > 65535 || s->B > 65535)
+        return fail(GDN_ERR_UNSUPPORTED_SHAPE, "B=%d / Hv=%d exceed the grid limit 65535", s->B, s->Hv);
+    if (need_single && s->B != 1)
+        return fail(GDN_ERR_UNSUPPORTED_SHAPE, "this call takes one sequence (B=%d)", s->B);
+    return GDN_OK;
+}
+
+int packed_channels(const gdn_shape* s) { return 2 * s->Hk * s->dk + s->Hv * s->dv; }
+
+int check_flags(uint32_t flags) {
+    if (flags & ~(GDN_NORMALIZE_QK | GDN_OUT_BF16))
+        return fail(GDN_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
+    return GDN_OK;
+}
+
+int check_ptr(const void* p, const char* name, bool required = true) {
+    if (p == nullptr) {
+        if (required) return fail(GDN_ERR_INVALID_ARG, "%s is NULL", name);
+        return GDN_OK;
+    }
+    if (!aligned16(p)) return fail(GDN_ERR_MISALIGNED, "%s (%p) is not 16-byte aligned", name, p);
+    return GDN_OK;
+}
+
+// Parent array -> OK or GDN_ERR_BAD_PARENTS (one tree rooted at node 0).
+int check_parents(int N, const int32_t* parents) {
+    if (parents == nullptr) return fail(GDN_ERR_INVALID_ARG, "parents is NULL");
+    if (N < 1 || N > GDN_MAX_TREE_NODES)
+        return fail(GDN_ERR_BAD_PARENTS, "tree size N=%d outside [1, %d]", N, GDN_MAX_TREE_NODES);
+    if (parents[0] != -1) return fail(GDN_ERR_BAD_PARENTS, "parents[0]=%d, the root must be -1", parents[0]);
+    for (int i = 1; i < N; ++i)
+        if (parents[i] < 0 || parents[i] >= i)
+            return fail(GDN_ERR_BAD_PARENTS, "parents[%d]=%d, need 0 <= parent < %d", i, parents[i], i);
+    return GDN_OK;
+}
+
+// Depth-first preorder walk with branch-state slots (see TreeStep).
+int schedule_tree(int N, const int32_t* parents, TreeStep* steps, int* n_slots) {
+    std::vector<std::vector<int>> children(N);
+    for (int i = 1; i < N; ++i) children[parents[i]].push_back(i);
+    std::vector<int> order;
+    order.reserve(N);
+    std::vector<int> stack{0};
+    while (!stack.empty()) {
+        const int n = stack.back();
+        stack.pop_back();
+        order.push_back(n);
+        for (int c = (int)children[n].size() - 1; c >= 0; --c) stack.push_back(children[n][c]);
+    }
+    std::vector<int> slot_of(N, -1);
+    int depth = 0, max_depth = 0, prev = -1;
+    for (int k = 0; k < N; ++k) {
+        const int n = order[k];
+        int restore = -1;
+        if (n != 0) {
+            const int par = parents[n];
+            if (prev != par) {
+                restore = slot_of[par];
+                if (restore < 0) return fail(GDN_ERR_BAD_PARENTS, "internal: no saved state for node %d", par);
+            }
+            if (slot_of[par] >= 0 && n == children[par].back()) {
+                if (slot_of[par] != depth - 1)
+                    return fail(GDN_ERR_BAD_PARENTS, "internal: slot stack out of order at node %d", n);
+                depth -= 1;
+            }
+        }
+        int save = -1;
+        if (children[n].size() >= 2) {
+            save = depth++;
+            slot_of[n] = save;
+            if (depth > max_depth) max_depth = depth;
+        }
+        if (max_depth > GDN_MAX_TREE_SLOTS)
+            return fail(GDN_ERR_DEPTH_EXCEEDED,
+                        "tree keeps %d branch states at once (more than %d nested branching nodes)",
+                        max_depth, GDN_MAX_TREE_SLOTS);
+        steps[k].node = (int8_t)n;
+        steps[k].restore = (int8_t)restore;
+        steps[k].save = (int8_t)save;
+        steps[k].pad = 0;
+        prev = n;
+    }
+    *n_slots = max_depth;
+    return GDN_OK;
+}
+
+int check_path(int N, const int32_t* parents, const int32_t* path, int L) {
+    if (L < 0) return fail(GDN_ERR_INVALID_ARG, "path length L=%d < 0", L);
+    if (L == 0) return GDN_OK;
+    if (path == nullptr) return fail(GDN_ERR_INVALID_ARG, "path is NULL");
+    for (int i = 0; i < L; ++i)
+        if (path[i] < 0 || path[i] >= N) return fail(GDN_ERR_BAD_PATH, "path[%d]=%d outside [0, %d)", i, path[i], N);
+    if (parents[path[0]] != -1) return fail(GDN_ERR_BAD_PATH, "path[0]=%d is not the root", path[0]);
+    for (int i = 1; i < L; ++i)
+        if (parents[path[i]] != path[i - 1])
+            return fail(GDN_ERR_BAD_PATH, "path[%d]=%d is not a child of path[%d]=%d", i, path[i], i - 1,
+                        path[i - 1]);
+    return GDN_OK;
+}
+
+int sm_count() {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+// Rows of one head per CTA for decode: the widest (fewest CTAs, most loads in
+// flight per thread) that still gives every SM a few CTAs.
+int decode_rows_per_cta(int B, int Hv, int dv) {
+    const long heads = (long)B * Hv;
+    const long want = 4L * sm_count();
+    for (int rows = 128; rows > 32; rows /= 2) {
+        if (dv % rows != 0) continue;
+        if (heads * (dv / rows) >= want) return rows;
+    }
+    return 32;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_abi_version(void) { return GDN_ABI_VERSION; }
+
+const char* gdn_last_error(void) { return t_error.c_str(); }
+
+size_t gdn_state_bytes(const gdn_shape* s) {
+    if (check_shape(s, false) != GDN_OK) return 0;
+    return (size_t)s->B * s->Hv * s->dv * s->dk * sizeof(float);
+}
+
+int gdn_tree_root_path(int32_t N, const int32_t* parents, int32_t node, int32_t* path, int32_t cap) {
+    int rc = check_parents(N, parents);
+    if (rc != GDN_OK) return rc;
+    if (node < 0 || node >= N) return fail(GDN_ERR_INVALID_ARG, "node %d outside [0, %d)", node, N);
+    if (path == nullptr) return fail(GDN_ERR_INVALID_ARG, "path is NULL");
+    int len = 0;
+    for (int m = node; m >= 0; m = parents[m]) ++len;
+    if (len > cap) return fail(GDN_ERR_INVALID_ARG, "path of length %d does not fit cap=%d", len, cap);
+    int pos = len - 1;
+    for (int m = node; m >= 0; m = parents[m]) path[pos--] = m;
+    return len;
+}
+
+int gdn_conv_step(int32_t B, int32_t T, int32_t C, const int32_t* parents, const gdn_bf16* x,
+                  const gdn_bf16* w, gdn_bf16* tail, gdn_bf16* y, uint32_t flags, void* stream) {
+    int rc;
+    if ((rc = check_flags(flags)) != GDN_OK) return rc;
+    if (B < 0 || T < 0 || C < 0) return fail(GDN_ERR_INVALID_ARG, "negative size B=%d T=%d C=%d", B, T, C);
+    if (C % 8 != 0) return fail(GDN_ERR_UNSUPPORTED_SHAPE, "channels C=%d not a multiple of 8", C);
+    if (B > 65535) return fail(GDN_ERR_UNSUPPORTED_SHAPE, "B=%d exceeds 65535", B);
+    if (parents != nullptr && (rc = check_parents(T, parents)) != GDN_OK) return rc;
+    if (B == 0 || T == 0 || C == 0) return GDN_OK;  // nothing to do; pointers may be NULL
+    if ((rc = check_ptr(x, "x")) || (rc = check_ptr(w, "w")) || (rc = check_ptr(tail, "tail")) ||
+        (rc = check_ptr(y, "y")))
+        return rc;
+    ConvParams p{};
+    p.x = x;
+    p.w = w;
+    p.tail = tail;
+    p.y = y;
+    p.B = B;
+    p.T = T;
+    p.C = C;
+    p.tree = parents != nullptr;
+    if (p.tree) {
+        for (int n = 0; n < T; ++n) {
+            int a = n, tail_slot = GDN_CONV_W - 1;
+            for (int m = 0; m < GDN_CONV_W - 1; ++m) {
+                if (a >= 0) a = parents[a];
+                if (a >= 0) {
+                    p.anc[n][m] = (int8_t)a;
+                } else {
+                    p.anc[n][m] = (int8_t)(-1 - tail_slot);
+                    tail_slot -= 1;
+                }
+            }
+        }
+    }
+    cudaError_t e = launch_conv(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "conv launch");
+}
+
+int gdn_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const float* alpha,
+                    const float* beta, float* state, void* out, float q_scale, uint32_t flags,
+                    void* stream) {
+    int rc;
+    if ((rc = check_shape(shape, false)) != GDN_OK) return rc;
+    if ((rc = check_flags(flags)) != GDN_OK) return rc;
+    if (T < 0) return fail(GDN_ERR_INVALID_ARG, "T=%d < 0", T);
+    if (shape->B == 0 || T == 0) return GDN_OK;  // nothing to do; pointers may be NULL
+    if ((rc = check_ptr(qkv, "qkv")) || (rc = check_ptr(alpha, "alpha")) || (rc = check_ptr(beta, "beta")) ||
+        (rc = check_ptr(state, "state")) || (rc = check_ptr(out, "out", false)))
+        return rc;
+    DecodeParams p{};
+    p.qkv = qkv;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.state = state;
+    p.out = out;
+    p.B = shape->B;
+    p.T = T;
+    p.Tsrc = T;
+    p.Hk = shape->Hk;
+    p.Hv = shape->Hv;
+    p.dv = shape->dv;
+    p.group = shape->Hv / shape->Hk;
+    p.C = packed_channels(shape);
+    p.q_scale = q_scale;
+    p.normalize = (flags & GDN_NORMALIZE_QK) != 0;
+    p.out_bf16 = (flags & GDN_OUT_BF16) != 0;
+    const int rows = decode_rows_per_cta(shape->B, shape->Hv, shape->dv);
+    cudaError_t e = launch_decode(p, shape->dk, rows, 0, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "decode launch");
+}
+
+int gdn_tree_verify(const gdn_shape* shape, int32_t N, const int32_t* parents, const gdn_bf16* qkv,
+                    const float* alpha, const float* beta, const float* state, void* out,
+                    float q_scale, uint32_t flags, void* stream) {
+    int rc;
+    if ((rc = check_shape(shape, true)) != GDN_OK) return rc;
+    if ((rc = check_flags(flags)) != GDN_OK) return rc;
+    if ((rc = check_parents(N, parents)) != GDN_OK) return rc;
+    if ((rc = check_ptr(qkv, "qkv")) || (rc = check_ptr(alpha, "alpha")) || (rc = check_ptr(beta, "beta")) ||
+        (rc = check_ptr(state, "state")) || (rc = check_ptr(out, "out")))
+        return rc;
+    TreeParams p{};
+    if ((rc = schedule_tree(N, parents, p.steps, &p.n_slots)) != GDN_OK) return rc;
+    p.qkv = qkv;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.state = state;
+    p.out = out;
+    p.N = N;
+    p.Hk = shape->Hk;
+    p.Hv = shape->Hv;
+    p.dv = shape->dv;
+    p.group = shape->Hv / shape->Hk;
+    p.C = packed_channels(shape);
+    p.q_scale = q_scale;
+    p.normalize = (flags & GDN_NORMALIZE_QK) != 0;
+    p.out_bf16 = (flags & GDN_OUT_BF16) != 0;
+    cudaError_t e = launch_tree(p, shape->dk, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "tree verify launch");
+}
+
+int gdn_commit_path(const gdn_shape* shape, int32_t N, const int32_t* parents, const int32_t* path,
+                    int32_t L, const gdn_bf16* qkv, const float* alpha, const float* beta,
+                    const gdn_bf16* x_tree, float* state, gdn_bf16* tail, uint32_t flags,
+                    void* stream) {
+    int rc;
+    if ((rc = check_shape(shape, true)) != GDN_OK) return rc;
+    if (flags & GDN_OUT_BF16) return fail(GDN_ERR_INVALID_ARG, "commit writes no output; GDN_OUT_BF16 not allowed");
+    if ((rc = check_flags(flags)) != GDN_OK) return rc;
+    if ((rc = check_parents(N, parents)) != GDN_OK) return rc;
+    if ((rc = check_path(N, parents, path, L)) != GDN_OK) return rc;
+    if ((rc = check_ptr(qkv, "qkv")) || (rc = check_ptr(alpha, "alpha")) || (rc = check_ptr(beta, "beta")) ||
+        (rc = check_ptr(state, "state")) || (rc = check_ptr(x_tree, "x_tree", false)))
+        return rc;
+    if (x_tree != nullptr && (rc = check_ptr(tail, "tail")) != GDN_OK) return rc;
+    if (L == 0) return GDN_OK;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    DecodeParams p{};
+    p.qkv = qkv;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.state = state;
+    p.out = nullptr;
+    p.B = 1;
+    p.T = L;
+    p.Tsrc = N;
+    p.Hk = shape->Hk;
+    p.Hv = shape->Hv;
+    p.dv = shape->dv;
+    p.group = shape->Hv / shape->Hk;
+    p.C = packed_channels(shape);
+    p.q_scale = 1.0f;
+    p.normalize = (flags & GDN_NORMALIZE_QK) != 0;
+    p.out_bf16 = 0;
+    for (int i = 0; i < L; ++i) p.tok[i] = path[i];
+    const int rows = decode_rows_per_cta(1, shape->Hv, shape->dv);
+    cudaError_t e = launch_decode(p, shape->dk, rows, 1, st);
+    if (e != cudaSuccess) return cuda_fail(e, "commit launch");
+    if (x_tree != nullptr) {
+        TailParams tp{};
+        tp.x_tree = x_tree;
+        tp.tail = tail;
+        tp.C = p.C;
+        tp.L = L;
+        for (int i = 0; i < L; ++i) tp.path[i] = path[i];
+        e = launch_commit_tail(tp, st);
+        if (e != cudaSuccess) return cuda_fail(e, "commit tail launch");
+    }
+    return GDN_OK;
+}
+
+}  // extern "C"

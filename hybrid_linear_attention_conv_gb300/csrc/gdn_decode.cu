@@ -1,0 +1,184 @@
+// gdn_decode.cu -- decode, commit and tree-verify kernels (sm_103a).
+//
+// Decode / commit: one CTA owns 32*R rows of one value head of one sequence.
+// Its rows of the state are loaded into registers once, advanced through all
+// T tokens, and stored once: the state crosses HBM exactly twice per call,
+// whatever T is (the recurrent state is updated in place and never grows --
+// "Serving A Research Architecture On CPU", constant-state section).  Loads and
+// stores use the streaming cache hint, since a batched decode touches each
+// state exactly once per step and it should not evict the activations from L2.
+//
+// Tree verify: one CTA owns 32 rows of one value head and walks the draft
+// tree depth-first.  The current node's rows stay in registers; the rows of a
+// node with two or more children are parked in shared memory until its last
+// child starts (host-computed slots).  The committed state is read once and
+// node states never reach HBM (TandemLLM "Architecture" v0.14.2 section 8.3:
+// each draft node's state branches from its parent's and the whole tree is
+// verified in one pass).
+#include <cuda_runtime.h>
+
+#include "gdn_internal.h"
+#include "gdn_step.cuh"
+
+namespace gdn {
+
+constexpr int kThreads = 256;        // 8 warps = 32 row groups of 8 lanes
+constexpr int kRowsPerPass = 32;
+
+template <int DK, int R, bool GATHER>
+__global__ void __launch_bounds__(kThreads)
+gdn_decode_kernel(const __grid_constant__ DecodeParams p) {
+    constexpr int V = DK / 32;
+    const int lane8 = threadIdx.x & 7;
+    const int rg = threadIdx.x >> 3;
+    const int h = blockIdx.y;
+    const int b = blockIdx.z;
+    const int g = h / p.group;
+    const int row0 = blockIdx.x * (kRowsPerPass * R) + rg;
+    float* S = p.state + ((size_t)b * p.Hv + h) * (size_t)p.dv * DK;
+
+    float4 s[R][V];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < V; ++m)
+            s[r][m] = __ldcs(reinterpret_cast<const float4*>(
+                S + (size_t)(row0 + kRowsPerPass * r) * DK + 32 * m + 4 * lane8));
+
+    const bool normalize = p.normalize != 0;
+    const bool out_bf16 = p.out_bf16 != 0;
+    for (int t = 0; t < p.T; ++t) {
+        const int tok = GATHER ? p.tok[t] : t;
+        const size_t trow = (size_t)b * p.Tsrc + tok;
+        const uint16_t* row = p.qkv + trow * (size_t)p.C;
+        TokenKQ<V> kq;
+        token_kq<V>(row + g * DK, row + (size_t)p.Hk * DK + g * DK, lane8, p.q_scale,
+                    normalize, kq);
+        const float alpha = p.alpha[trow * p.Hv + h];
+        const float beta = p.beta[trow * p.Hv + h];
+        const uint16_t* vrow = row + (size_t)2 * p.Hk * DK + (size_t)h * p.dv;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int i = row0 + kRowsPerPass * r;
+            const float v_i = __uint_as_float((uint32_t)vrow[i] << 16);
+            const float o = row_step<V>(s[r], kq, v_i, alpha, beta);
+            if (p.out != nullptr && lane8 == 0)
+                store_out(p.out, (((size_t)b * p.T + t) * p.Hv + h) * p.dv + i, o, out_bf16);
+        }
+    }
+
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < V; ++m)
+            __stcs(reinterpret_cast<float4*>(S + (size_t)(row0 + kRowsPerPass * r) * DK + 32 * m +
+                                             4 * lane8),
+                   s[r][m]);
+}
+
+template <int DK>
+__global__ void __launch_bounds__(kThreads)
+gdn_tree_kernel(const __grid_constant__ TreeParams p) {
+    constexpr int V = DK / 32;
+    extern __shared__ float4 slots[];  // [n_slots][32 row groups][V][8 lanes]
+    const int lane8 = threadIdx.x & 7;
+    const int rg = threadIdx.x >> 3;
+    const int h = blockIdx.y;
+    const int g = h / p.group;
+    const int row = blockIdx.x * kRowsPerPass + rg;
+    const float* S = p.state + (size_t)h * p.dv * DK + (size_t)row * DK;
+
+    float4 s[V];
+#pragma unroll
+    for (int m = 0; m < V; ++m) s[m] = __ldg(reinterpret_cast<const float4*>(S + 32 * m + 4 * lane8));
+
+    const bool normalize = p.normalize != 0;
+    const bool out_bf16 = p.out_bf16 != 0;
+    for (int step = 0; step < p.N; ++step) {
+        const TreeStep st = p.steps[step];
+        if (st.restore >= 0) {
+#pragma unroll
+            for (int m = 0; m < V; ++m) s[m] = slots[((st.restore * kRowsPerPass + rg) * V + m) * 8 + lane8];
+        }
+        const int node = st.node;
+        const uint16_t* qkv_row = p.qkv + (size_t)node * p.C;
+        TokenKQ<V> kq;
+        token_kq<V>(qkv_row + g * DK, qkv_row + (size_t)p.Hk * DK + g * DK, lane8, p.q_scale,
+                    normalize, kq);
+        const float alpha = p.alpha[(size_t)node * p.Hv + h];
+        const float beta = p.beta[(size_t)node * p.Hv + h];
+        const float v_i =
+            __uint_as_float((uint32_t)qkv_row[(size_t)2 * p.Hk * DK + (size_t)h * p.dv + row] << 16);
+        const float o = row_step<V>(s, kq, v_i, alpha, beta);
+        if (lane8 == 0) store_out(p.out, ((size_t)node * p.Hv + h) * p.dv + row, o, out_bf16);
+        if (st.save >= 0) {
+#pragma unroll
+            for (int m = 0; m < V; ++m) slots[((st.save * kRowsPerPass + rg) * V + m) * 8 + lane8] = s[m];
+        }
+    }
+}
+
+template <int DK, int R, bool GATHER>
+static cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
+    dim3 grid(p.dv / (kRowsPerPass * R), p.Hv, p.B);
+    gdn_decode_kernel<DK, R, GATHER><<<grid, kThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <int DK, bool GATHER>
+static cudaError_t launch_decode_r(const DecodeParams& p, int rows_per_cta, cudaStream_t s) {
+    switch (rows_per_cta) {
+        case 32: return launch_decode_t<DK, 1, GATHER>(p, s);
+        case 64: return launch_decode_t<DK, 2, GATHER>(p, s);
+        case 128: return launch_decode_t<DK, 4, GATHER>(p, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int gather,
+                          cudaStream_t s) {
+    if (gather) {
+        // commit replays short paths: one row pass per CTA keeps the grid wide
+        switch (dk) {
+            case 32: return launch_decode_r<32, true>(p, rows_per_cta, s);
+            case 64: return launch_decode_r<64, true>(p, rows_per_cta, s);
+            case 128: return launch_decode_r<128, true>(p, rows_per_cta, s);
+        }
+    } else {
+        switch (dk) {
+            case 32: return launch_decode_r<32, false>(p, rows_per_cta, s);
+            case 64: return launch_decode_r<64, false>(p, rows_per_cta, s);
+            case 128: return launch_decode_r<128, false>(p, rows_per_cta, s);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <int DK>
+static cudaError_t launch_tree_t(const TreeParams& p, cudaStream_t s) {
+    const size_t smem = (size_t)p.n_slots * kRowsPerPass * DK * sizeof(float);
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        const int max_smem = GDN_MAX_TREE_SLOTS * kRowsPerPass * DK * (int)sizeof(float);
+        cudaError_t e = cudaFuncSetAttribute(gdn_tree_kernel<DK>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    dim3 grid(p.dv / kRowsPerPass, p.Hv, 1);
+    gdn_tree_kernel<DK><<<grid, kThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tree(const TreeParams& p, int dk, cudaStream_t s) {
+    switch (dk) {
+        case 32: return launch_tree_t<32>(p, s);
+        case 64: return launch_tree_t<64>(p, s);
+        case 128: return launch_tree_t<128>(p, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace gdn

@@ -1,0 +1,77 @@
+// gdn_internal.h -- launch parameters shared by the host API and the kernels.
+// Host validation (gdn_api.cu) fills these; the kernels (gdn_decode.cu,
+// gdn_conv.cu, gdn_prefill.cu) consume them.  Nothing here is part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gdn.h"
+
+namespace gdn {
+
+// Decode / commit: T sequential tokens per sequence, optionally gathered
+// through an index map (commit replays a tree path).
+struct DecodeParams {
+    const uint16_t* qkv;   // bf16 [B, Tsrc, C]
+    const float* alpha;    // [B, Tsrc, Hv]
+    const float* beta;     // [B, Tsrc, Hv]
+    float* state;          // [B, Hv, dv, dk]
+    void* out;             // [B, T, Hv, dv] or nullptr
+    int B, T, Tsrc, Hk, Hv, dv, group;  // group = Hv / Hk
+    int C;                 // packed row length
+    float q_scale;
+    int normalize;
+    int out_bf16;
+    int32_t tok[GDN_MAX_TREE_NODES];  // gather map when used (commit)
+};
+
+// One step of the tree walk, computed on the host (depth-first preorder).
+struct TreeStep {
+    int8_t node;      // node processed at this step
+    int8_t restore;   // slot holding the parent's state, or -1 (registers)
+    int8_t save;      // slot to keep this node's state in, or -1
+    int8_t pad;
+};
+
+struct TreeParams {
+    const uint16_t* qkv;   // bf16 [N, C]
+    const float* alpha;    // [N, Hv]
+    const float* beta;     // [N, Hv]
+    const float* state;    // [Hv, dv, dk] read only
+    void* out;             // [N, Hv, dv]
+    int N, Hk, Hv, dv, group, C;
+    float q_scale;
+    int normalize;
+    int out_bf16;
+    int n_slots;
+    TreeStep steps[GDN_MAX_TREE_NODES];
+};
+
+struct ConvParams {
+    const uint16_t* x;     // [B, T, C]
+    const uint16_t* w;     // [C, 4]
+    uint16_t* tail;        // [B, 4, C]
+    uint16_t* y;           // [B, T, C]
+    int B, T, C;
+    int tree;              // 0: linear run, 1: tree (ancestor table below)
+    // tree mode: for node n, source of its m-th earlier input (m = 1..3):
+    // >= 0 a node index, < 0 tail slot (-1 - s).
+    int8_t anc[GDN_MAX_TREE_NODES][3];
+};
+
+struct TailParams {
+    const uint16_t* x_tree;  // [N, C]
+    uint16_t* tail;          // [4, C]
+    int C, L;
+    int32_t path[GDN_MAX_TREE_NODES];
+};
+
+// Launchers (return the cudaError_t of the launch).
+cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int gather,
+                          cudaStream_t s);
+cudaError_t launch_tree(const TreeParams& p, int dk, cudaStream_t s);
+cudaError_t launch_conv(const ConvParams& p, cudaStream_t s);
+cudaError_t launch_commit_tail(const TailParams& p, cudaStream_t s);
+
+}  // namespace gdn

@@ -1,0 +1,155 @@
+// gdn_step.cuh -- the one per-row gated delta-rule step used by every kernel
+// that advances a state token by token (decode, commit, tree verify).
+//
+// Because decode, commit and tree verify all call these functions with the
+// same lane layout, a committed path's state equals a linear decode of that
+// path bit for bit, and a tree node's output equals the decode output of the
+// last token of its root path.  The speculative round needs exactly that
+// (TandemLLM "Architecture" v0.11.1: a model whose verify rows equal its decode
+// rows bit for bit can speculate with no change to its greedy text).  All
+// floating-point operations use explicit round-to-nearest intrinsics so that no
+// compiler contraction can differ between call sites.
+//
+// Layout: a row of the state (dk fp32 values) is owned by a group of 8 lanes;
+// lane l of the group holds float4 number m at columns 32*m + 4*l, for
+// m = 0 .. dk/32 - 1.  A warp therefore covers 4 rows, and each load/store
+// instruction of a warp touches 4 x 128 contiguous bytes.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace gdn {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+constexpr float kNormEps = 1e-6f;
+
+// Sum over the 8 lanes of a row group (xor butterfly: every lane of the group
+// ends with the same bits, since a + b == b + a exactly).
+__device__ __forceinline__ float group_sum8(float x) {
+    x = __fadd_rn(x, __shfl_xor_sync(kFullMask, x, 4));
+    x = __fadd_rn(x, __shfl_xor_sync(kFullMask, x, 2));
+    x = __fadd_rn(x, __shfl_xor_sync(kFullMask, x, 1));
+    return x;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// This lane's V*4 elements of a dk-long bf16 head vector.
+template <int V>
+__device__ __forceinline__ void load_head_vec(const uint16_t* head, int lane8, float (&x)[V][4]) {
+#pragma unroll
+    for (int m = 0; m < V; ++m) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(head + 32 * m + 4 * lane8);
+        x[m][0] = bf16_lo(raw.x);
+        x[m][1] = bf16_hi(raw.x);
+        x[m][2] = bf16_lo(raw.y);
+        x[m][3] = bf16_hi(raw.y);
+    }
+}
+
+// Dot product of this lane's slice with another, reduced over the row group.
+// Per float4 a short fma chain, then a fixed pairwise tree over the float4s.
+template <int V>
+__device__ __forceinline__ float lane_dot(const float (&a)[V][4], const float (&b)[V][4]) {
+    float part[V];
+#pragma unroll
+    for (int m = 0; m < V; ++m) {
+        float acc = __fmul_rn(a[m][0], b[m][0]);
+        acc = __fmaf_rn(a[m][1], b[m][1], acc);
+        acc = __fmaf_rn(a[m][2], b[m][2], acc);
+        acc = __fmaf_rn(a[m][3], b[m][3], acc);
+        part[m] = acc;
+    }
+#pragma unroll
+    for (int w = 1; w < V; w *= 2)
+#pragma unroll
+        for (int m = 0; m + w < V; m += 2 * w) part[m] = __fadd_rn(part[m], part[m + w]);
+    return group_sum8(part[0]);
+}
+
+template <int V>
+__device__ __forceinline__ float lane_dot4(const float4 (&s)[V], const float (&b)[V][4]) {
+    float part[V];
+#pragma unroll
+    for (int m = 0; m < V; ++m) {
+        float acc = __fmul_rn(s[m].x, b[m][0]);
+        acc = __fmaf_rn(s[m].y, b[m][1], acc);
+        acc = __fmaf_rn(s[m].z, b[m][2], acc);
+        acc = __fmaf_rn(s[m].w, b[m][3], acc);
+        part[m] = acc;
+    }
+#pragma unroll
+    for (int w = 1; w < V; w *= 2)
+#pragma unroll
+        for (int m = 0; m + w < V; m += 2 * w) part[m] = __fadd_rn(part[m], part[m + w]);
+    return part[0];
+}
+
+// q^ = scale * q / sqrt(|q|^2 + eps) (or scale * q without normalisation).
+template <int V>
+__device__ __forceinline__ void normalize_vec(float (&x)[V][4], float scale, bool normalize) {
+    float inv = scale;
+    if (normalize) {
+        const float ss = lane_dot<V>(x, x);
+        inv = __fmul_rn(rsqrtf(__fadd_rn(ss, kNormEps)), scale);
+    }
+#pragma unroll
+    for (int m = 0; m < V; ++m)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[m][e] = __fmul_rn(x[m][e], inv);
+}
+
+// Per-token key-head vectors of one row group: normalised q, k and k.q.
+template <int V>
+struct TokenKQ {
+    float k[V][4];
+    float q[V][4];
+    float kq;
+};
+
+template <int V>
+__device__ __forceinline__ void token_kq(const uint16_t* q_head, const uint16_t* k_head,
+                                         int lane8, float q_scale, bool normalize,
+                                         TokenKQ<V>& t) {
+    load_head_vec<V>(k_head, lane8, t.k);
+    load_head_vec<V>(q_head, lane8, t.q);
+    normalize_vec<V>(t.k, 1.0f, normalize);
+    normalize_vec<V>(t.q, q_scale, normalize);
+    t.kq = lane_dot<V>(t.k, t.q);
+}
+
+// One token on one state row s (this lane's slice), in place:
+//   a = s.k, c = s.q  (row-group sums),  u = beta * (v_i - alpha * a),
+//   o_i = alpha * c + u * (k.q),         s <- alpha * s + u * k.
+// This is row i of S <- alpha S (I - beta k k^T) + beta v k^T followed by
+// o = S q (expand S_new q = alpha S q + u (k.q)).  Returns o_i in every lane.
+template <int V>
+__device__ __forceinline__ float row_step(float4 (&s)[V], const TokenKQ<V>& t, float v_i,
+                                          float alpha, float beta) {
+    const float a_part = lane_dot4<V>(s, t.k);
+    const float c_part = lane_dot4<V>(s, t.q);
+    const float a = group_sum8(a_part);
+    const float c = group_sum8(c_part);
+    const float u = __fmul_rn(beta, __fmaf_rn(-alpha, a, v_i));
+    const float o = __fmaf_rn(alpha, c, __fmul_rn(u, t.kq));
+#pragma unroll
+    for (int m = 0; m < V; ++m) {
+        s[m].x = __fmaf_rn(u, t.k[m][0], __fmul_rn(alpha, s[m].x));
+        s[m].y = __fmaf_rn(u, t.k[m][1], __fmul_rn(alpha, s[m].y));
+        s[m].z = __fmaf_rn(u, t.k[m][2], __fmul_rn(alpha, s[m].z));
+        s[m].w = __fmaf_rn(u, t.k[m][3], __fmul_rn(alpha, s[m].w));
+    }
+    return o;
+}
+
+__device__ __forceinline__ void store_out(void* out, size_t idx, float o, bool as_bf16) {
+    if (as_bf16) {
+        reinterpret_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(o);
+    } else {
+        reinterpret_cast<float*>(out)[idx] = o;
+    }
+}
+
+}  // namespace gdn

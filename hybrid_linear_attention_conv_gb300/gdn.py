@@ -1,0 +1,286 @@
+"""Thin Python binding over ``libgdn.so`` (the C ABI in ``include/gdn.h``).
+
+Argument marshalling only: tensors are checked for device, dtype, shape and
+contiguity, and their ``data_ptr()`` plus the current CUDA stream are passed to
+the C entry point of the same name.  Every step of the computation runs in the
+library's CUDA kernels; there is no CPU fallback, and a missing library is an
+error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgdn.so")
+
+GDN_CONV_W = 4
+GDN_MAX_TREE_NODES = 64
+GDN_MAX_TREE_SLOTS = 8
+GDN_NORMALIZE_QK = 0x1
+GDN_OUT_BF16 = 0x2
+
+STATUS = {
+    0: "GDN_OK",
+    -1: "GDN_ERR_INVALID_ARG",
+    -2: "GDN_ERR_UNSUPPORTED_SHAPE",
+    -3: "GDN_ERR_BAD_PARENTS",
+    -4: "GDN_ERR_BAD_PATH",
+    -5: "GDN_ERR_DEPTH_EXCEEDED",
+    -6: "GDN_ERR_MISALIGNED",
+    -7: "GDN_ERR_CUDA",
+    -8: "GDN_ERR_TIMEOUT",
+    -9: "GDN_ERR_WORKSPACE",
+}
+
+# Every symbol include/gdn.h declares.
+EXPORTS = [
+    "gdn_abi_version",
+    "gdn_last_error",
+    "gdn_state_bytes",
+    "gdn_tree_root_path",
+    "gdn_conv_step",
+    "gdn_decode_step",
+    "gdn_tree_verify",
+    "gdn_commit_path",
+    "gdn_prefill_workspace_bytes",
+    "gdn_chunk_prefill",
+]
+
+
+class GdnError(RuntimeError):
+    def __init__(self, code: int, fn: str, msg: str):
+        super().__init__(f"{fn} -> {STATUS.get(code, code)}: {msg}")
+        self.code = code
+
+
+class gdn_shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("Hk", ctypes.c_int32), ("Hv", ctypes.c_int32),
+                ("dk", ctypes.c_int32), ("dv", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load the shared library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build() "
+                               "(the CUDA library is required; there is no fallback)")
+        lib = ctypes.CDLL(path)
+        P, I32, U32, F, SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_float,
+                              ctypes.c_size_t)
+        SH = ctypes.POINTER(gdn_shape)
+        sig = {
+            "gdn_abi_version": (ctypes.c_int, []),
+            "gdn_last_error": (ctypes.c_char_p, []),
+            "gdn_state_bytes": (SZ, [SH]),
+            "gdn_tree_root_path": (ctypes.c_int, [I32, P, I32, P, I32]),
+            "gdn_conv_step": (ctypes.c_int, [I32, I32, I32, P, P, P, P, P, U32, P]),
+            "gdn_decode_step": (ctypes.c_int, [SH, I32, P, P, P, P, P, F, U32, P]),
+            "gdn_tree_verify": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, F, U32, P]),
+            "gdn_commit_path": (ctypes.c_int, [SH, I32, P, P, I32, P, P, P, P, P, P, U32, P]),
+            "gdn_prefill_workspace_bytes": (SZ, [SH, I32, I32]),
+            "gdn_chunk_prefill": (ctypes.c_int, [SH, I32, I32, P, P, P, P, P, P, SZ, F, U32, P]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def last_error() -> str:
+    return load().gdn_last_error().decode()
+
+
+def _check(rc: int, fn: str):
+    if rc != 0:
+        raise GdnError(rc, fn, last_error())
+
+
+def _shape(B, Hk, Hv, dk, dv) -> gdn_shape:
+    return gdn_shape(int(B), int(Hk), int(Hv), int(dk), int(dv))
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _dev(t: torch.Tensor | None, dtype, name: str, shape=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _host_i32(a, name):
+    if a is None:
+        return None, None
+    arr = np.ascontiguousarray(a, dtype=np.int32)
+    return arr, arr.ctypes.data_as(ctypes.c_void_p)
+
+
+def packed_channels(Hk, Hv, dk, dv) -> int:
+    """Length of a packed [q | k | v] row."""
+    return 2 * Hk * dk + Hv * dv
+
+
+def _flags(normalize: bool, out_bf16: bool) -> int:
+    return (GDN_NORMALIZE_QK if normalize else 0) | (GDN_OUT_BF16 if out_bf16 else 0)
+
+
+# ---------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------
+def abi_version() -> int:
+    return load().gdn_abi_version()
+
+
+def state_bytes(B, Hk, Hv, dk, dv) -> int:
+    sh = _shape(B, Hk, Hv, dk, dv)
+    return load().gdn_state_bytes(ctypes.byref(sh))
+
+
+def tree_root_path(parents, node: int) -> np.ndarray:
+    par, pp = _host_i32(parents, "parents")
+    path = np.zeros(max(len(par), 1), np.int32)
+    n = load().gdn_tree_root_path(len(par), pp, int(node), path.ctypes.data_as(ctypes.c_void_p),
+                                  len(path))
+    if n < 0:
+        _check(n, "gdn_tree_root_path")
+    return path[:n].copy()
+
+
+def conv_step(x: torch.Tensor, w: torch.Tensor, tail: torch.Tensor, y: torch.Tensor | None = None,
+              parents=None) -> torch.Tensor:
+    """x bf16 [B,T,C], w bf16 [C,4], tail bf16 [B,4,C] (updated in place in linear mode)."""
+    B, T, C = x.shape
+    if y is None:
+        y = torch.empty_like(x)
+    par, pp = _host_i32(parents, "parents")
+    rc = load().gdn_conv_step(B, T, C, pp, _dev(x, torch.bfloat16, "x"),
+                              _dev(w, torch.bfloat16, "w", (C, GDN_CONV_W)),
+                              _dev(tail, torch.bfloat16, "tail", (B, GDN_CONV_W, C)),
+                              _dev(y, torch.bfloat16, "y", (B, T, C)), 0, _stream())
+    _check(rc, "gdn_conv_step")
+    return y
+
+
+def decode_step(qkv, alpha, beta, state, Hk, Hv, dk, dv, out=None, q_scale=1.0, normalize=True,
+                out_bf16=False) -> torch.Tensor:
+    """qkv bf16 [B,T,C], alpha/beta fp32 [B,T,Hv], state fp32 [B,Hv,dv,dk] (in place)."""
+    B, T, C = qkv.shape
+    if out is None:
+        out = torch.empty((B, T, Hv, dv), dtype=torch.bfloat16 if out_bf16 else torch.float32,
+                          device=qkv.device)
+    sh = _shape(B, Hk, Hv, dk, dv)
+    rc = load().gdn_decode_step(ctypes.byref(sh), T,
+                                _dev(qkv, torch.bfloat16, "qkv", (B, T, packed_channels(Hk, Hv, dk, dv))),
+                                _dev(alpha, torch.float32, "alpha", (B, T, Hv)),
+                                _dev(beta, torch.float32, "beta", (B, T, Hv)),
+                                _dev(state, torch.float32, "state", (B, Hv, dv, dk)),
+                                _dev(out, torch.bfloat16 if out_bf16 else torch.float32, "out",
+                                     (B, T, Hv, dv)),
+                                float(q_scale), _flags(normalize, out_bf16), _stream())
+    _check(rc, "gdn_decode_step")
+    return out
+
+
+def tree_verify(parents, qkv, alpha, beta, state, Hk, Hv, dk, dv, out=None, q_scale=1.0,
+                normalize=True, out_bf16=False) -> torch.Tensor:
+    """qkv bf16 [N,C], alpha/beta fp32 [N,Hv], state fp32 [Hv,dv,dk] (read only)."""
+    par, pp = _host_i32(parents, "parents")
+    N = len(par)
+    if out is None:
+        out = torch.empty((N, Hv, dv), dtype=torch.bfloat16 if out_bf16 else torch.float32,
+                          device=qkv.device)
+    sh = _shape(1, Hk, Hv, dk, dv)
+    rc = load().gdn_tree_verify(ctypes.byref(sh), N, pp,
+                                _dev(qkv, torch.bfloat16, "qkv", (N, packed_channels(Hk, Hv, dk, dv))),
+                                _dev(alpha, torch.float32, "alpha", (N, Hv)),
+                                _dev(beta, torch.float32, "beta", (N, Hv)),
+                                _dev(state, torch.float32, "state", (Hv, dv, dk)),
+                                _dev(out, torch.bfloat16 if out_bf16 else torch.float32, "out",
+                                     (N, Hv, dv)),
+                                float(q_scale), _flags(normalize, out_bf16), _stream())
+    _check(rc, "gdn_tree_verify")
+    return out
+
+
+def commit_path(parents, path, qkv, alpha, beta, state, Hk, Hv, dk, dv, x_tree=None, tail=None,
+                normalize=True) -> None:
+    """Replays `path` through the step in place on state [Hv,dv,dk]; updates tail [4,C]."""
+    par, pp = _host_i32(parents, "parents")
+    pa, ppa = _host_i32(path, "path")
+    N = len(par)
+    sh = _shape(1, Hk, Hv, dk, dv)
+    rc = load().gdn_commit_path(ctypes.byref(sh), N, pp, ppa, len(pa),
+                                _dev(qkv, torch.bfloat16, "qkv", (N, packed_channels(Hk, Hv, dk, dv))),
+                                _dev(alpha, torch.float32, "alpha", (N, Hv)),
+                                _dev(beta, torch.float32, "beta", (N, Hv)),
+                                _dev(x_tree, torch.bfloat16, "x_tree", (N, packed_channels(Hk, Hv, dk, dv))),
+                                _dev(state, torch.float32, "state", (Hv, dv, dk)),
+                                _dev(tail, torch.bfloat16, "tail", (GDN_CONV_W, packed_channels(Hk, Hv, dk, dv))), _flags(normalize, False),
+                                _stream())
+    _check(rc, "gdn_commit_path")
+
+
+def prefill_workspace_bytes(T, Hk, Hv, dk, dv, chunk=64) -> int:
+    sh = _shape(1, Hk, Hv, dk, dv)
+    return load().gdn_prefill_workspace_bytes(ctypes.byref(sh), int(T), int(chunk))
+
+
+def chunk_prefill(qkv, alpha, beta, state, Hk, Hv, dk, dv, out=None, workspace=None, chunk=64,
+                  q_scale=1.0, normalize=True, out_bf16=False) -> torch.Tensor:
+    """qkv bf16 [T,C], alpha/beta fp32 [T,Hv], state fp32 [Hv,dv,dk] (S_0 in, S_T out)."""
+    T = qkv.shape[0]
+    if out is None:
+        out = torch.empty((T, Hv, dv), dtype=torch.bfloat16 if out_bf16 else torch.float32,
+                          device=qkv.device)
+    ws_bytes = prefill_workspace_bytes(T, Hk, Hv, dk, dv, chunk)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=qkv.device)
+    sh = _shape(1, Hk, Hv, dk, dv)
+    rc = load().gdn_chunk_prefill(ctypes.byref(sh), T, int(chunk),
+                                  _dev(qkv, torch.bfloat16, "qkv", (T, packed_channels(Hk, Hv, dk, dv))),
+                                  _dev(alpha, torch.float32, "alpha", (T, Hv)),
+                                  _dev(beta, torch.float32, "beta", (T, Hv)),
+                                  _dev(state, torch.float32, "state", (Hv, dv, dk)),
+                                  _dev(out, torch.bfloat16 if out_bf16 else torch.float32, "out",
+                                       (T, Hv, dv)),
+                                  _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+                                  float(q_scale), _flags(normalize, out_bf16), _stream())
+    _check(rc, "gdn_chunk_prefill")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# conversions between the generator's numpy arrays and device tensors
+# ---------------------------------------------------------------------------
+def bf16_tensor(bits: np.ndarray, device="cuda") -> torch.Tensor:
+    """Raw bf16 bits (uint16 numpy) -> bf16 tensor on `device`."""
+    t = torch.from_numpy(np.ascontiguousarray(bits, np.uint16).view(np.int16))
+    return t.view(torch.bfloat16).to(device)
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> raw bits as uint16 numpy."""
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)

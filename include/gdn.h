@@ -1,0 +1,222 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) Gated DeltaNet mixer library.
+ *
+ * The library runs the recurrent mixer of a hybrid DeltaNet/attention decoder on
+ * one GPU: the short causal convolution in front of it, decode of one or more
+ * tokens, speculative tree verify, commit of the accepted path, and chunked
+ * prefill.  Sources for what each call computes:
+ *
+ *  - Layer and state: TandemLLM "Architecture" (v0.14.2) section 8.1, table of
+ *    layer kinds: 48 Gated DeltaNet layers, each keeping per sequence an fp32
+ *    state of 48 heads x 128 x 128 (3.15 MB) and a 4-wide convolution tail
+ *    (80 KB); the state is fixed-size and has no inverse.
+ *  - Recurrence: the pages name "the gated delta rule for one token, a block, a
+ *    tree" (TandemLLM "Architecture" v0.11.1, "The parts" diagram) but print no
+ *    equation.  The update is the published Gated DeltaNet rule (Yang, Kautz &
+ *    Hatamizadeh 2024): per value head h and token t,
+ *        S_h <- alpha * S_h (I - beta k k^T) + beta v k^T,   o = S_h q
+ *    with q, k the L2-normalised key-head vectors (eps 1e-6) after a 4-tap
+ *    causal depthwise convolution + SiLU over the q/k/v channels.
+ *  - In-place, constant-size state with no allocation inside the decode loop:
+ *    "Serving A Research Architecture On CPU", section on the constant-state
+ *    guarantee.  This library never allocates or frees device memory; every
+ *    buffer is owned by the caller.
+ *  - Tree verify and commit: "Architecture" (v0.14.2) section 8.3 and the
+ *    round sequence diagram of v0.11.1: a draft tree of up to 32 nodes is
+ *    verified in one pass with each node's state branched from its parent's;
+ *    the accepted root-to-node path's state is then committed exactly.
+ *  - Refusing unsupported shapes loudly instead of corrupting memory: "Serving
+ *    A Research Architecture On CPU", the hardcoded-head-size bug.
+ *
+ * Conventions for every call
+ *  - Tensor pointers are DEVICE pointers to caller-owned, dense, row-major
+ *    memory, unless marked "host".  Layouts are given per argument.
+ *  - bf16 tensors are raw bfloat16 bit patterns (gdn_bf16).
+ *  - Packed activations: one token's row holds C_qkv = 2*Hk*dk + Hv*dv channels
+ *    ordered [q | k | v]; q and k are key-head-major (key head g in channels
+ *    g*dk .. g*dk+dk-1 of its block), v is value-head-major.
+ *  - Value head h reads key head h / (Hv / Hk).
+ *  - State S_h is dv x dk fp32, row i contiguous over the key index:
+ *    state[b][h][i][j].
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t, NULL = the
+ *    legacy default stream).  Host arrays (parents, path) are read before the
+ *    call returns and may be reused at once.
+ *  - Return value: GDN_OK (0) or a negative gdn_status.  A call that fails
+ *    validation enqueues nothing and leaves every buffer untouched.
+ *    gdn_last_error() returns a message for the calling thread's last failure.
+ *  - Supported shapes: dk, dv in {32, 64, 128}; Hk >= 1; Hv a multiple of Hk;
+ *    B >= 0; token counts >= 0 (0 is a no-op).  Device pointers must be 16-byte
+ *    aligned (GDN_ERR_MISALIGNED otherwise).
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDN_ABI_VERSION 1
+
+/* Taps of the causal depthwise convolution; the tail keeps this many inputs. */
+#define GDN_CONV_W 4
+/* Largest draft tree accepted by tree verify / commit / tree-mode conv. */
+#define GDN_MAX_TREE_NODES 64
+/* Largest number of branch states a tree verify keeps at once (nested nodes
+ * with two or more children on one root path). */
+#define GDN_MAX_TREE_SLOTS 8
+
+typedef uint16_t gdn_bf16;
+
+typedef struct gdn_shape {
+    int32_t B;   /* sequences in the batch */
+    int32_t Hk;  /* key heads (q and k) */
+    int32_t Hv;  /* value heads (v, state, output) */
+    int32_t dk;  /* key head size: state columns */
+    int32_t dv;  /* value head size: state rows */
+} gdn_shape;
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = -1,       /* null pointer, negative count, bad flag */
+    GDN_ERR_UNSUPPORTED_SHAPE = -2, /* head sizes / head counts not supported */
+    GDN_ERR_BAD_PARENTS = -3,       /* parent array is not one tree rooted at 0 */
+    GDN_ERR_BAD_PATH = -4,          /* path is not a root-to-node path */
+    GDN_ERR_DEPTH_EXCEEDED = -5,    /* tree needs more than GDN_MAX_TREE_SLOTS */
+    GDN_ERR_MISALIGNED = -6,        /* device pointer not 16-byte aligned */
+    GDN_ERR_CUDA = -7,              /* a CUDA runtime call failed */
+    GDN_ERR_TIMEOUT = -8,           /* a bounded device wait gave up */
+    GDN_ERR_WORKSPACE = -9          /* workspace missing or too small */
+} gdn_status;
+
+/* flags */
+#define GDN_NORMALIZE_QK 0x1u  /* L2-normalise q and k per key head (eps 1e-6) */
+#define GDN_OUT_BF16 0x2u      /* outputs stored as bf16 (RNE) instead of fp32 */
+
+/* ABI version of the loaded library (GDN_ABI_VERSION it was built with). */
+int gdn_abi_version(void);
+
+/* Message for the calling thread's most recent failed call ("" if none). */
+const char* gdn_last_error(void);
+
+/* Bytes of fp32 state for the shape: B * Hv * dv * dk * 4 (0 on a bad shape). */
+size_t gdn_state_bytes(const gdn_shape* shape);
+
+/* Host-only tree bookkeeping, the same code the tree calls validate with.
+ * Writes the root-to-node path of `node` (root first) into path[0..cap-1] and
+ * returns its length, or a negative gdn_status for a bad tree, node or cap. */
+int gdn_tree_root_path(int32_t N, const int32_t* parents, int32_t node, int32_t* path,
+                       int32_t cap);
+
+/*
+ * gdn_conv_step -- 4-tap causal depthwise convolution + SiLU.
+ *   y[b,t,c] = SiLU( sum_{j=0..3} w[c][j] * u_j ),   u_3 = x[b,t,c] (newest),
+ *   u_{3-m} = the m-th earlier input of that token's history.
+ * Linear mode (parents == NULL): the history of token t is x[b,0..t-1] after
+ *   tail[b]; on return tail[b] holds the last 4 inputs of (tail[b] ++ x[b]).
+ * Tree mode (parents != NULL, host int32[T]; T = N draft nodes): the history
+ *   of node n is its ancestors' inputs, nearest first, then tail[b]; the tail
+ *   is read only.  All B sequences share the tree.
+ *   B, T, C   sequences, tokens (or nodes), channels; C % 8 == 0.
+ *   x         bf16 [B, T, C]  pre-conv inputs.
+ *   w         bf16 [C, 4]     taps, oldest input first.
+ *   tail      bf16 [B, 4, C]  the last four inputs, oldest first (in/out in
+ *                             linear mode, read-only in tree mode).
+ *   y         bf16 [B, T, C]  output (fp32 math, rounded to nearest even).
+ * Source: the per-layer 4-wide convolution tail, "Architecture" (v0.14.2)
+ * section 8.1; short convolution rings carried between steps, "Serving A
+ * Research Architecture On CPU" (engine design).
+ */
+int gdn_conv_step(int32_t B, int32_t T, int32_t C, const int32_t* parents,
+                  const gdn_bf16* x, const gdn_bf16* w, gdn_bf16* tail, gdn_bf16* y,
+                  uint32_t flags, void* stream);
+
+/*
+ * gdn_decode_step -- T sequential tokens of the gated delta rule, in place.
+ * For each sequence b, token t, value head h (key head g = h / (Hv/Hk)):
+ *   q^ = q_scale * q / |q|,  k^ = k / |k|   (if GDN_NORMALIZE_QK),
+ *   S_h <- alpha S_h (I - beta k^ k^T) + beta v k^T,   out = S_h q^.
+ * The state is read from HBM once and written once per call, whatever T.
+ *   qkv     bf16 [B, T, C_qkv]   packed post-conv activations.
+ *   alpha   fp32 [B, T, Hv]      decay, beta fp32 [B, T, Hv] write strength.
+ *   state   fp32 [B, Hv, dv, dk] in/out.
+ *   out     [B, T, Hv, dv] fp32, or bf16 with GDN_OUT_BF16; may be NULL.
+ * Source: "Architecture" (v0.11.1) "The parts" (one token, a block);
+ * "Architecture" (v0.14.2) section 8.3 (decode without speculation).
+ */
+int gdn_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv,
+                    const float* alpha, const float* beta, float* state, void* out,
+                    float q_scale, uint32_t flags, void* stream);
+
+/*
+ * gdn_tree_verify -- outputs of every node of a draft tree in one pass.
+ * Node n's state is the committed state advanced through the root..n path
+ * (each node branches from its parent's state); out[n] = S_n q^_n.  The
+ * committed state is read once and NOT modified; node states never reach HBM.
+ *   shape->B must be 1.  N in [1, GDN_MAX_TREE_NODES].
+ *   parents host int32 [N]: parents[0] == -1 (the root follows the committed
+ *           state), 0 <= parents[n] < n otherwise.
+ *   qkv     bf16 [N, C_qkv]; alpha, beta fp32 [N, Hv].
+ *   state   fp32 [Hv, dv, dk] read only.
+ *   out     [N, Hv, dv] fp32 (or bf16 with GDN_OUT_BF16).
+ * A node's output equals, bit for bit, the output gdn_decode_step gives for
+ * the last token of that node's root path (same step arithmetic).
+ * Source: "Architecture" (v0.14.2) section 8.3 and the v0.11.1 round diagram
+ * (verify the whole tree in one pass, trees of up to 32 nodes).
+ */
+int gdn_tree_verify(const gdn_shape* shape, int32_t N, const int32_t* parents,
+                    const gdn_bf16* qkv, const float* alpha, const float* beta,
+                    const float* state, void* out, float q_scale, uint32_t flags,
+                    void* stream);
+
+/*
+ * gdn_commit_path -- keep the accepted path's state: replay path[0..L-1]
+ * (a root-to-node path of the tree) through the step, in place.  The result
+ * equals, bit for bit, gdn_decode_step over the path's gathered inputs.
+ *   shape->B must be 1.  parents host int32 [N]; path host int32 [L], L >= 0
+ *   (L == 0 leaves everything unchanged).
+ *   qkv, alpha, beta  the tree's inputs as given to gdn_tree_verify.
+ *   x_tree  bf16 [N, C_qkv] the tree's pre-conv inputs, or NULL.
+ *   state   fp32 [Hv, dv, dk] in/out.
+ *   tail    bf16 [4, C_qkv]: when x_tree != NULL, replaced by the last four
+ *           inputs of (tail ++ x_tree[path[0]] ++ ... ++ x_tree[path[L-1]]).
+ * Source: "Architecture" (v0.14.2) section 8.3 (commit the state of the
+ * accepted path), v0.11.1 round diagram (commit KV rows and recurrent state).
+ */
+int gdn_commit_path(const gdn_shape* shape, int32_t N, const int32_t* parents,
+                    const int32_t* path, int32_t L, const gdn_bf16* qkv,
+                    const float* alpha, const float* beta, const gdn_bf16* x_tree,
+                    float* state, gdn_bf16* tail, uint32_t flags, void* stream);
+
+/*
+ * gdn_prefill_workspace_bytes -- device workspace gdn_chunk_prefill needs for
+ * T tokens in chunks of `chunk` (0 on a bad shape).
+ */
+size_t gdn_prefill_workspace_bytes(const gdn_shape* shape, int32_t T, int32_t chunk);
+
+/*
+ * gdn_chunk_prefill -- T tokens of one sequence by the chunk-parallel (WY/UT)
+ * form of the same recurrence, on tensor cores.  Mathematically identical to
+ * gdn_decode_step over the T tokens; rounding differs (fp32 accumulation of
+ * bf16 products in a different order).
+ *   shape->B must be 1.  chunk == 64.  T >= 0 (a ragged last chunk is masked).
+ *   qkv bf16 [T, C_qkv]; alpha, beta fp32 [T, Hv];
+ *   state fp32 [Hv, dv, dk] in: S_0, out: S_T;  out [T, Hv, dv] fp32 / bf16.
+ *   workspace  device, >= gdn_prefill_workspace_bytes(), 256-byte aligned.
+ * Source: "Architecture" (v0.11.1) "The parts" (the rule over a block);
+ * chunk-parallel versus sequential evaluation of the recurrence, "Serving A
+ * Research Architecture On CPU" (third exactness layer).  Chunk form: Yang et
+ * al. 2024, "Parallelizing Linear Transformers with the Delta Rule over
+ * Sequence Length", with the gated extension of "Gated Delta Networks".
+ */
+int gdn_chunk_prefill(const gdn_shape* shape, int32_t T, int32_t chunk,
+                      const gdn_bf16* qkv, const float* alpha, const float* beta,
+                      float* state, void* out, void* workspace, size_t workspace_bytes,
+                      float q_scale, uint32_t flags, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDN_H */

@@ -1,0 +1,170 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+symbol include/gdn.h declares, validates its arguments before touching the
+device, and its host-side tree bookkeeping matches the oracle bit for bit.
+
+Every call here is made with arguments that fail validation (or with host-only
+entry points), so no kernel is ever launched from these tests."""
+import ctypes
+import itertools
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from hybrid_linear_attention_conv_gb300 import build as gbuild
+from hybrid_linear_attention_conv_gb300 import gdn
+from hybrid_linear_attention_conv_gb300 import inputs as gen
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return gdn.load()
+
+
+def _header_symbols():
+    txt = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_0-9]+)\s*\(", txt)))
+
+
+def test_exports_every_declared_symbol(lib):
+    syms = _header_symbols()
+    assert sorted(gdn.EXPORTS) == syms
+    for s in syms:
+        assert hasattr(lib, s), s
+    # the symbols are real dynamic exports of the .so (nm -D)
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", gdn.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r" T (gdn_\w+)", out))
+    assert set(syms) <= exported
+
+
+def test_abi_version(lib):
+    assert gdn.abi_version() == 1
+
+
+def test_state_bytes(lib):
+    assert gdn.state_bytes(1, 16, 48, 128, 128) == 48 * 128 * 128 * 4 == 3145728
+    assert gdn.state_bytes(64, 16, 48, 128, 128) == 64 * 3145728
+    assert gdn.state_bytes(1, 16, 48, 100, 128) == 0  # unsupported head size
+
+
+def _sh(B=1, Hk=16, Hv=48, dk=128, dv=128):
+    return gdn.gdn_shape(B, Hk, Hv, dk, dv)
+
+
+FAKE = 0x10000  # aligned, never dereferenced: every call below fails validation first
+
+
+def test_decode_validation(lib):
+    P = ctypes.c_void_p
+    cases = [
+        (_sh(dk=100), 1, FAKE, -2),
+        (_sh(dv=48), 1, FAKE, -2),
+        (_sh(Hk=5), 1, FAKE, -2),           # 48 % 5 != 0
+        (_sh(B=-1), 1, FAKE, -2),
+        (_sh(), -3, FAKE, -1),
+        (_sh(), 1, FAKE + 2, -6),           # misaligned qkv
+    ]
+    for sh, T, qkv, want in cases:
+        rc = lib.gdn_decode_step(ctypes.byref(sh), T, P(qkv), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                                 1.0, 1, None)
+        assert rc == want, (sh.dk, sh.dv, sh.Hk, T, gdn.last_error())
+        assert gdn.last_error()
+    # null state
+    rc = lib.gdn_decode_step(ctypes.byref(_sh()), 1, P(FAKE), P(FAKE), P(FAKE), None, None, 1.0, 1, None)
+    assert rc == -1
+    # unknown flag
+    rc = lib.gdn_decode_step(ctypes.byref(_sh()), 1, P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, 1.0,
+                             0x80, None)
+    assert rc == -1
+
+
+def test_conv_validation(lib):
+    P = ctypes.c_void_p
+    assert lib.gdn_conv_step(1, 1, 100, None, P(FAKE), P(FAKE), P(FAKE), P(FAKE), 0, None) == -2
+    assert lib.gdn_conv_step(1, -1, 128, None, P(FAKE), P(FAKE), P(FAKE), P(FAKE), 0, None) == -1
+    assert lib.gdn_conv_step(1, 1, 128, None, P(FAKE), P(FAKE + 8), P(FAKE), P(FAKE), 0, None) == -6
+    bad = np.array([-1, 0, 5], np.int32)
+    assert lib.gdn_conv_step(1, 3, 128, bad.ctypes.data_as(P), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 0,
+                             None) == -3
+
+
+def _tree_call(lib, parents, sh=None, N=None):
+    P = ctypes.c_void_p
+    par = np.ascontiguousarray(parents, np.int32)
+    sh = sh or _sh()
+    return lib.gdn_tree_verify(ctypes.byref(sh), len(par) if N is None else N, par.ctypes.data_as(P),
+                               P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1.0, 1, None)
+
+
+def test_tree_validation(lib):
+    assert _tree_call(lib, [0, 0]) == -3                  # root must be -1
+    assert _tree_call(lib, [-1, 1]) == -3                 # parent must precede
+    assert _tree_call(lib, [-1, 0, -1]) == -3             # a second root
+    assert _tree_call(lib, [-1] + [0] * 64) == -3         # N = 65 > 64
+    assert _tree_call(lib, [-1], N=0) == -3
+    assert _tree_call(lib, [-1, 0], sh=_sh(B=2)) == -2    # one sequence only
+
+
+def _nested_branch_tree(levels):
+    """A spine where every spine node also has a leaf child: `levels` nested
+    branching nodes on the deepest root path."""
+    parents = [-1]
+    spine = 0
+    for _ in range(levels):
+        parents.append(spine)          # next spine node (first child)
+        nxt = len(parents) - 1
+        parents.append(spine)          # a leaf sibling (second child)
+        spine = nxt
+    return np.array(parents, np.int32)
+
+
+def test_tree_depth_exceeded(lib):
+    # 9 nested branching nodes need 9 parked states: refused before any launch
+    parents = _nested_branch_tree(9)
+    assert _tree_call(lib, parents) == -5
+    assert "branch" in gdn.last_error()
+
+
+def test_commit_validation(lib):
+    P = ctypes.c_void_p
+    parents = np.array([-1, 0, 0, 1, 3], np.int32)
+
+    def call(path, sh=None):
+        pa = np.ascontiguousarray(path, np.int32)
+        return lib.gdn_commit_path(ctypes.byref(sh or _sh()), len(parents), parents.ctypes.data_as(P),
+                                   pa.ctypes.data_as(P) if pa.size else None, len(pa), P(FAKE), P(FAKE),
+                                   P(FAKE), None, P(FAKE + 4), None, 1, None)
+
+    assert call([1, 3]) == -4          # does not start at the root
+    assert call([0, 2, 3]) == -4       # 3 is not a child of 2
+    assert call([0, 7]) == -4          # out of range
+    assert call([0, 1, 3], sh=_sh(dk=96)) == -2
+    assert call([0, 1, 3]) == -6       # valid path, misaligned state pointer
+
+
+def test_root_path_matches_oracle_brute_force(lib):
+    """Bit-exact bookkeeping: every node of every tree with up to 7 nodes."""
+    for N in range(1, 8):
+        for tail in itertools.product(*[range(i) for i in range(1, N)]):
+            parents = np.array((-1,) + tail, np.int32)
+            for n in range(N):
+                assert np.array_equal(gdn.tree_root_path(parents, n), oracle.root_path(parents, n))
+    for seed in range(10):
+        parents = gen.random_tree(seed, 64, 20)
+        for n in range(64):
+            assert np.array_equal(gdn.tree_root_path(parents, n), oracle.root_path(parents, n))
+
+
+def test_root_path_rejects(lib):
+    with pytest.raises(gdn.GdnError):
+        gdn.tree_root_path(np.array([-1, 2, 0], np.int32), 1)
+    with pytest.raises(gdn.GdnError):
+        gdn.tree_root_path(np.array([-1, 0], np.int32), 5)

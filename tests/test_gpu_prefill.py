@@ -1,0 +1,101 @@
+"""GPU parity for chunked prefill against the sequential fp64 oracle.
+
+The chunk form rounds differently from the sequential recurrence (the same
+mathematics accumulated in another order), so parity is the stated tolerance,
+not bits.  At the full 8,192-token size the oracle runs on sampled key heads
+(each with the value heads that read it): the heads are independent, so a
+sampled head's outputs and state are exactly what the full oracle would give."""
+import numpy as np
+import pytest
+import torch
+
+from gdn_testutil import assert_out_close, assert_state_close, bf16, f32, gdn, gen, host, oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from hybrid_linear_attention_conv_gb300 import build
+    build.build()
+    gdn.load()
+
+
+def _slice_key_head(qkv, shape, g):
+    """Packed rows of one key head g and its value heads, as a (Hk=1) problem."""
+    Hk, dk, dv = shape.Hk, shape.dk, shape.dv
+    grp = shape.Hv // Hk
+    q = qkv[..., g * dk:(g + 1) * dk]
+    k = qkv[..., Hk * dk + g * dk: Hk * dk + (g + 1) * dk]
+    v = qkv[..., 2 * Hk * dk + g * grp * dv: 2 * Hk * dk + (g + 1) * grp * dv]
+    return np.ascontiguousarray(np.concatenate([q, k, v], axis=-1)), slice(g * grp, (g + 1) * grp)
+
+
+def _run(shape, T, seed, heads=None, **kw):
+    d = gen.decode_inputs(seed, shape.with_batch(1), T, tag="prefill")
+    st = f32(d["state"][0])
+    out = gdn.chunk_prefill(bf16(d["qkv"][0]), f32(d["alpha"][0]), f32(d["beta"][0]), st, shape.Hk,
+                            shape.Hv, shape.dk, shape.dv, **kw)
+    torch.cuda.synchronize()
+    out_h, st_h = host(out), host(st)
+    if heads is None:
+        out_ref, st_ref = oracle.prefill(d["qkv"], d["alpha"], d["beta"], d["state"], shape.Hk, shape.Hv,
+                                         shape.dk, shape.dv, q_scale=kw.get("q_scale", 1.0))
+        return out_h, st_h, out_ref[0], st_ref[0]
+    grp = shape.Hv // shape.Hk
+    outs, sts, refs_o, refs_s = [], [], [], []
+    for g in heads:
+        qkv_g, hs = _slice_key_head(d["qkv"], shape, g)
+        o_ref, s_ref = oracle.prefill(qkv_g, d["alpha"][..., hs], d["beta"][..., hs], d["state"][:, hs],
+                                      1, grp, shape.dk, shape.dv, q_scale=kw.get("q_scale", 1.0))
+        outs.append(out_h[:, hs])
+        sts.append(st_h[hs])
+        refs_o.append(o_ref[0])
+        refs_s.append(s_ref[0])
+    return (np.concatenate(outs, 1), np.concatenate(sts, 0), np.concatenate(refs_o, 1),
+            np.concatenate(refs_s, 0))
+
+
+@pytest.mark.parametrize("shape,T", [(gen.TINY, 64), (gen.TINY, 300), (gen.QWEN_27B, 129),
+                                     (gen.Shape(1, 2, 4, 64, 64), 1), (gen.Shape(1, 1, 2, 128, 128), 511)])
+def test_prefill_small_vs_oracle(shape, T):
+    out, st, out_ref, st_ref = _run(shape, T, 40 + T)
+    assert_out_close(out, out_ref)
+    assert_state_close(st, st_ref)
+
+
+def test_prefill_27b_8192_sampled_heads():
+    """1 sequence, 8,192 tokens, 27B head shape, chunk 64; key heads 0 and 13."""
+    out, st, out_ref, st_ref = _run(gen.QWEN_27B, 8192, 0, heads=[0, 13])
+    assert_out_close(out, out_ref)
+    assert_state_close(st, st_ref)
+
+
+def test_prefill_zero_tokens_keeps_state():
+    shape = gen.TINY
+    d = gen.decode_inputs(1, shape, 1)
+    st = f32(d["state"][0])
+    before = st.clone()
+    qkv = torch.empty((0, shape.C), dtype=torch.bfloat16, device="cuda")
+    e = torch.empty((0, shape.Hv), dtype=torch.float32, device="cuda")
+    gdn.chunk_prefill(qkv, e, e, st, shape.Hk, shape.Hv, shape.dk, shape.dv)
+    torch.cuda.synchronize()
+    assert torch.equal(st, before)
+
+
+def test_prefill_then_decode_continues():
+    """Prefill leaves a state that decode continues from (prompt then one token)."""
+    shape = gen.QWEN_27B
+    T = 200
+    d = gen.decode_inputs(9, shape, T + 1, tag="pd")
+    st = f32(d["state"][0])
+    gdn.chunk_prefill(bf16(d["qkv"][0, :T]), f32(d["alpha"][0, :T]), f32(d["beta"][0, :T]), st, shape.Hk,
+                      shape.Hv, shape.dk, shape.dv)
+    st_b = st[None].contiguous()
+    out = gdn.decode_step(bf16(d["qkv"][:, T:]), f32(d["alpha"][:, T:]), f32(d["beta"][:, T:]), st_b,
+                          shape.Hk, shape.Hv, shape.dk, shape.dv)
+    torch.cuda.synchronize()
+    out_ref, st_ref = oracle.decode(d["qkv"], d["alpha"], d["beta"], d["state"], shape.Hk, shape.Hv,
+                                    shape.dk, shape.dv)
+    assert_out_close(host(out)[0, 0], out_ref[0, T])
+    assert_state_close(host(st_b)[0], st_ref[0])

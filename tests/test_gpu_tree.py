@@ -1,0 +1,202 @@
+"""GPU parity for speculative tree verify and commit.
+
+* tree outputs vs the oracle's root-path replay (tolerance);
+* the committed state vs the oracle (tolerance);
+* bit-exact GPU vs GPU: a node's verify output == decode of its root path,
+  the committed state == decode of the accepted path, and the conv tail is
+  exactly the last four inputs."""
+import numpy as np
+import pytest
+import torch
+
+from gdn_testutil import (assert_out_close, assert_state_close, bf16, f32, gdn, gen, host, oracle,
+                          oracle_conv_then_round)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from hybrid_linear_attention_conv_gb300 import build
+    build.build()
+    gdn.load()
+
+
+def _tree_case(shape, N, seed, max_depth=8, parents=None):
+    s1 = shape.with_batch(1)
+    if parents is None:
+        parents = gen.random_tree(seed, N, max_depth)
+    d = gen.decode_inputs(seed, s1, N, tag="tree")
+    return parents, {"qkv": d["qkv"][0], "alpha": d["alpha"][0], "beta": d["beta"][0],
+                     "state": d["state"][0]}
+
+
+def _verify(shape, parents, d, **kw):
+    st = f32(d["state"])
+    before = st.clone()
+    out = gdn.tree_verify(parents, bf16(d["qkv"]), f32(d["alpha"]), f32(d["beta"]), st, shape.Hk,
+                          shape.Hv, shape.dk, shape.dv, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(st, before), "tree verify must not write the committed state"
+    return out
+
+
+def _path_decode(shape, d, path):
+    """GPU linear decode of the gathered path inputs: (outputs, final state)."""
+    st = f32(d["state"][None])
+    out = gdn.decode_step(bf16(d["qkv"][None, path]), f32(d["alpha"][None, path]),
+                          f32(d["beta"][None, path]), st, shape.Hk, shape.Hv, shape.dk, shape.dv)
+    torch.cuda.synchronize()
+    return out[0], st[0]
+
+
+@pytest.mark.parametrize("shape", [gen.TINY, gen.QWEN_27B])
+def test_tree_verify_vs_oracle(shape):
+    parents, d = _tree_case(shape, 32, 1)
+    out = _verify(shape, parents, d)
+    ref = oracle.tree_verify(parents, d["qkv"], d["alpha"], d["beta"], d["state"], shape.Hk, shape.Hv,
+                             shape.dk, shape.dv)
+    assert_out_close(host(out), ref)
+
+
+def test_tree_verify_outputs_equal_decode_bitwise():
+    shape = gen.QWEN_27B
+    parents, d = _tree_case(shape, 32, 2)
+    out = _verify(shape, parents, d)
+    for n in range(32):
+        path = gdn.tree_root_path(parents, n)
+        o, _ = _path_decode(shape, d, path)
+        assert torch.equal(out[n], o[-1]), f"node {n}"
+
+
+@pytest.mark.parametrize("parents", [
+    np.array([-1], np.int32),                                  # a single node
+    np.arange(-1, 63, dtype=np.int32),                         # a 64-long chain (no branch states)
+    np.array([-1] + [0] * 31, np.int32),                       # a star: 31 children of the root
+])
+def test_tree_verify_degenerate_shapes(parents):
+    shape = gen.Shape(1, 2, 4, 64, 64)
+    _, d = _tree_case(shape, len(parents), 3, parents=parents)
+    out = _verify(shape, parents, d)
+    ref = oracle.tree_verify(parents, d["qkv"], d["alpha"], d["beta"], d["state"], shape.Hk, shape.Hv,
+                             shape.dk, shape.dv)
+    assert_out_close(host(out), ref)
+
+
+def _nested_branch_tree(levels):
+    parents = [-1]
+    spine = 0
+    for _ in range(levels):
+        parents.append(spine)
+        nxt = len(parents) - 1
+        parents.append(spine)
+        spine = nxt
+    return np.array(parents, np.int32)
+
+
+def test_tree_verify_max_branch_states():
+    """Exactly GDN_MAX_TREE_SLOTS nested branching nodes is accepted and correct."""
+    shape = gen.Shape(1, 2, 4, 128, 128)
+    parents = _nested_branch_tree(gdn.GDN_MAX_TREE_SLOTS)
+    _, d = _tree_case(shape, len(parents), 4, parents=parents)
+    out = _verify(shape, parents, d)
+    ref = oracle.tree_verify(parents, d["qkv"], d["alpha"], d["beta"], d["state"], shape.Hk, shape.Hv,
+                             shape.dk, shape.dv)
+    assert_out_close(host(out), ref)
+
+
+def test_tree_verify_bf16_out_and_scale():
+    shape = gen.Shape(1, 2, 6, 64, 64)
+    parents, d = _tree_case(shape, 20, 5)
+    out = _verify(shape, parents, d, q_scale=0.5, out_bf16=True)
+    ref = oracle.tree_verify(parents, d["qkv"], d["alpha"], d["beta"], d["state"], shape.Hk, shape.Hv,
+                             shape.dk, shape.dv, q_scale=0.5)
+    got = gen.bf16_bits_to_f32(host(out)).astype(np.float64)
+    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-3)
+
+
+@pytest.mark.parametrize("shape", [gen.TINY, gen.QWEN_27B])
+def test_commit_vs_oracle_and_decode_bitwise(shape):
+    N = 32
+    parents, d = _tree_case(shape, N, 6)
+    c = gen.conv_inputs(6, 1, N, shape.C)
+    leaf = gen.random_leaf(6, parents)
+    path = gdn.tree_root_path(parents, leaf)
+    assert np.array_equal(path, oracle.root_path(parents, leaf))
+    st = f32(d["state"])
+    tail = bf16(c["tail"][0])
+    gdn.commit_path(parents, path, bf16(d["qkv"]), f32(d["alpha"]), f32(d["beta"]), st, shape.Hk,
+                    shape.Hv, shape.dk, shape.dv, x_tree=bf16(c["x"][0]), tail=tail)
+    torch.cuda.synchronize()
+    st_ref, tail_ref = oracle.commit(parents, path, d["qkv"], d["alpha"], d["beta"], d["state"],
+                                     shape.Hk, shape.Hv, shape.dk, shape.dv, x_tree=c["x"][0],
+                                     tail=c["tail"][0])
+    assert_state_close(host(st), st_ref)
+    assert np.array_equal(host(tail), tail_ref)
+    _, st_dec = _path_decode(shape, d, path)
+    assert torch.equal(st, st_dec), "commit must equal the linear decode of the path bit for bit"
+
+
+def test_commit_every_prefix_length():
+    shape = gen.Shape(1, 2, 4, 64, 64)
+    parents = np.arange(-1, 11, dtype=np.int32)  # chain of 12
+    _, d = _tree_case(shape, 12, 7, parents=parents)
+    c = gen.conv_inputs(7, 1, 12, shape.C)
+    for L in range(0, 13):
+        path = np.arange(L, dtype=np.int32)
+        st = f32(d["state"])
+        tail = bf16(c["tail"][0])
+        gdn.commit_path(parents, path, bf16(d["qkv"]), f32(d["alpha"]), f32(d["beta"]), st, shape.Hk,
+                        shape.Hv, shape.dk, shape.dv, x_tree=bf16(c["x"][0]), tail=tail)
+        torch.cuda.synchronize()
+        st_ref, tail_ref = oracle.commit(parents, path, d["qkv"], d["alpha"], d["beta"], d["state"],
+                                         shape.Hk, shape.Hv, shape.dk, shape.dv, x_tree=c["x"][0],
+                                         tail=c["tail"][0])
+        assert np.array_equal(host(tail), tail_ref), L
+        if L == 0:
+            assert np.array_equal(host(st), d["state"])
+        else:
+            assert_state_close(host(st), st_ref)
+
+
+def test_speculative_round_end_to_end():
+    """One round at the 27B shape: tree conv -> verify -> commit (state and
+    tail), compared with the oracle's conv + verify + commit, and the commit
+    compared bitwise with conv + decode of the accepted path from scratch."""
+    shape = gen.QWEN_27B
+    N = 32
+    parents = gen.random_tree(8, N, 8)
+    c = gen.conv_inputs(8, 1, N, shape.C)
+    d = gen.decode_inputs(8, shape, N, tag="round")
+    w = bf16(c["w"])
+    tail = bf16(c["tail"])
+    x_tree = bf16(c["x"])
+    y_tree = gdn.conv_step(x_tree, w, tail, parents=parents)
+    st = f32(d["state"][0])
+    al, be = f32(d["alpha"][0]), f32(d["beta"][0])
+    out = gdn.tree_verify(parents, y_tree[0], al, be, st, shape.Hk, shape.Hv, shape.dk, shape.dv)
+    leaf = gen.random_leaf(8, parents)
+    path = gdn.tree_root_path(parents, leaf)
+    gdn.commit_path(parents, path, y_tree[0], al, be, st, shape.Hk, shape.Hv, shape.dk, shape.dv,
+                    x_tree=x_tree[0], tail=tail[0])
+    torch.cuda.synchronize()
+
+    y_ref = oracle.f64_to_bf16(oracle.conv_tree(parents, c["x"][0], c["w"], c["tail"][0]))
+    out_ref = oracle.tree_verify(parents, y_ref, d["alpha"][0], d["beta"][0], d["state"][0], shape.Hk,
+                                 shape.Hv, shape.dk, shape.dv)
+    st_ref, tail_ref = oracle.commit(parents, path, y_ref, d["alpha"][0], d["beta"][0], d["state"][0],
+                                     shape.Hk, shape.Hv, shape.dk, shape.dv, x_tree=c["x"][0],
+                                     tail=c["tail"][0])
+    assert_out_close(host(out), out_ref)
+    assert_state_close(host(st), st_ref)
+    assert np.array_equal(host(tail[0]), tail_ref)
+
+    # the same tokens decoded linearly from the pre-round state and tail
+    tail2 = bf16(c["tail"])
+    y_lin = gdn.conv_step(bf16(c["x"][:, path]), w, tail2)
+    st2 = f32(d["state"][0:1])
+    gdn.decode_step(y_lin, f32(d["alpha"][:, path]), f32(d["beta"][:, path]), st2, shape.Hk, shape.Hv,
+                    shape.dk, shape.dv)
+    torch.cuda.synchronize()
+    assert torch.equal(st2[0], st)
+    assert torch.equal(tail2[0], tail[0])
