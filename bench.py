@@ -205,7 +205,8 @@ class Batched:
     name = "batched"
     L, B = 48, 64
 
-    def __init__(self, device, seed: int, n_sets: int):
+    def __init__(self, device, seed: int, n_sets: int, layers: int = 48):
+        self.L = layers
         import torch
         from hybrid_linear_attention_conv_gb300 import gdn
         self.torch, self.gdn = torch, gdn
@@ -287,14 +288,16 @@ class Batched:
                 raise RuntimeError(self.gdn.last_error())
         self.h_out.copy_(self.out, non_blocking=True)
 
-    @classmethod
-    def config(cls) -> dict:
-        return {"workload": "batched decode over all 48 GDN layers: batch 64 sequences, 27B head "
+    def config(self=None) -> dict:
+        L = Batched.L if self is None else self.L
+        B = Batched.B
+        sb = L * B * HV * DV * DK * 4
+        return {"workload": f"batched decode over {L} GDN layers: batch {B} sequences, 27B head "
                             "shape (16 key / 48 value heads x 128), independent fp32 states, one token "
                             "per sequence per layer (conv + delta step)",
-                "layers": cls.L, "batch": cls.B, "Hk": HK, "Hv": HV, "dk": DK, "dv": DV,
-                "state_bytes": cls.L * cls.B * HV * DV * DK * 4,
-                "l2": "inputs larger than L2: 9.66 GB of state streamed per step",
+                "layers": L, "batch": B, "Hk": HK, "Hv": HV, "dk": DK, "dv": DV,
+                "state_bytes": sb,
+                "l2": f"inputs larger than L2: {sb / 1e9:.2f} GB of state streamed per step",
                 "launch": "eager, CUDA events between kernels"}
 
 
@@ -338,7 +341,7 @@ def run_ours(args) -> dict | None:
     __graft_entry__.build()
 
     peaks, peaks_kind = load_peaks()
-    wl = Batched(device, seed=1234 + rank, n_sets=min(4, args.steps + args.warmup))
+    wl = Batched(device, seed=1234 + rank, n_sets=min(4, args.steps + args.warmup), layers=args.layers)
     torch.cuda.synchronize()
 
     for i in range(args.warmup):
@@ -465,6 +468,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["batched"], default="batched")
+    ap.add_argument("--layers", type=int, default=48,
+                    help="GDN layers in the batched workload (48 = the 27B model; fewer only for "
+                         "profiling small cases)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
