@@ -174,6 +174,33 @@ int decode_rows_per_cta(int B, int Hv, int dv) {
 
 }  // namespace
 
+namespace gdn {
+
+int cuda_error(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+
+int check_prefill_args(const gdn_shape* shape, int T, int chunk, const void* qkv, const void* alpha,
+                       const void* beta, const void* state, const void* out, const void* workspace,
+                       size_t workspace_bytes, uint32_t flags) {
+    int rc;
+    if ((rc = check_shape(shape, true)) != GDN_OK) return rc;
+    if ((rc = check_flags(flags)) != GDN_OK) return rc;
+    if (chunk != 64) return fail(GDN_ERR_INVALID_ARG, "chunk=%d, only 64 is supported", chunk);
+    if (T < 0) return fail(GDN_ERR_INVALID_ARG, "T=%d < 0", T);
+    if (T == 0) return GDN_OK;  // nothing to do; pointers may be NULL
+    if ((rc = check_ptr(qkv, "qkv")) || (rc = check_ptr(alpha, "alpha")) || (rc = check_ptr(beta, "beta")) ||
+        (rc = check_ptr(state, "state")) || (rc = check_ptr(out, "out")))
+        return rc;
+    if (workspace == nullptr) return fail(GDN_ERR_WORKSPACE, "workspace is NULL");
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(GDN_ERR_MISALIGNED, "workspace (%p) is not 256-byte aligned", workspace);
+    const size_t need = gdn_prefill_workspace_bytes(shape, T, chunk);
+    if (workspace_bytes < need)
+        return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", workspace_bytes, need);
+    return GDN_OK;
+}
+
+}  // namespace gdn
+
 extern "C" {
 
 int gdn_abi_version(void) { return GDN_ABI_VERSION; }

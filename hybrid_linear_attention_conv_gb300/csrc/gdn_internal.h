@@ -67,6 +67,13 @@ struct TailParams {
     int32_t path[GDN_MAX_TREE_NODES];
 };
 
+// Host validation shared by the entry points (gdn_api.cu).  Both record a
+// message for gdn_last_error() and return a gdn_status.
+int check_prefill_args(const gdn_shape* shape, int T, int chunk, const void* qkv, const void* alpha,
+                       const void* beta, const void* state, const void* out, const void* workspace,
+                       size_t workspace_bytes, uint32_t flags);
+int cuda_error(cudaError_t e, const char* what);
+
 // Launchers (return the cudaError_t of the launch).
 cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int gather,
                           cudaStream_t s);

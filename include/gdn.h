@@ -192,19 +192,26 @@ int gdn_commit_path(const gdn_shape* shape, int32_t N, const int32_t* parents,
 
 /*
  * gdn_prefill_workspace_bytes -- device workspace gdn_chunk_prefill needs for
- * T tokens in chunks of `chunk` (0 on a bad shape).
+ * T tokens in chunks of `chunk` (0 on a bad shape or chunk).  The workspace
+ * holds the call's status word (int32 at offset 0).
  */
 size_t gdn_prefill_workspace_bytes(const gdn_shape* shape, int32_t T, int32_t chunk);
 
 /*
  * gdn_chunk_prefill -- T tokens of one sequence by the chunk-parallel (WY/UT)
- * form of the same recurrence, on tensor cores.  Mathematically identical to
- * gdn_decode_step over the T tokens; rounding differs (fp32 accumulation of
- * bf16 products in a different order).
+ * form of the same recurrence, on the tcgen05 tensor cores.  Mathematically
+ * identical to gdn_decode_step over the T tokens; rounding differs (bf16
+ * operand splits with fp32 accumulation, in another order).
  *   shape->B must be 1.  chunk == 64.  T >= 0 (a ragged last chunk is masked).
  *   qkv bf16 [T, C_qkv]; alpha, beta fp32 [T, Hv];
  *   state fp32 [Hv, dv, dk] in: S_0, out: S_T;  out [T, Hv, dv] fp32 / bf16.
- *   workspace  device, >= gdn_prefill_workspace_bytes(), 256-byte aligned.
+ *   workspace  device, >= gdn_prefill_workspace_bytes(), 256-byte aligned,
+ *              caller-owned.  Its int32 at offset 0 is reset to 0 by the call
+ *              and set non-zero on the device if a bounded tensor-core wait gave
+ *              up (read it after the stream has synchronised; non-zero means
+ *              the results are invalid, as for GDN_ERR_TIMEOUT).
+ * The chunk form runs for dk = dv = 128 (the 27B layer's heads); narrower
+ * heads run the same recurrence token by token on the GPU.
  * Source: "Architecture" (v0.11.1) "The parts" (the rule over a block);
  * chunk-parallel versus sequential evaluation of the recurrence, "Serving A
  * Research Architecture On CPU" (third exactness layer).  Chunk form: Yang et

@@ -34,9 +34,13 @@ def _slice_key_head(qkv, shape, g):
 def _run(shape, T, seed, heads=None, **kw):
     d = gen.decode_inputs(seed, shape.with_batch(1), T, tag="prefill")
     st = f32(d["state"][0])
+    ws = torch.full((gdn.prefill_workspace_bytes(T, shape.Hk, shape.Hv, shape.dk, shape.dv),), 7,
+                    dtype=torch.uint8, device="cuda")
     out = gdn.chunk_prefill(bf16(d["qkv"][0]), f32(d["alpha"][0]), f32(d["beta"][0]), st, shape.Hk,
-                            shape.Hv, shape.dk, shape.dv, **kw)
+                            shape.Hv, shape.dk, shape.dv, workspace=ws, **kw)
     torch.cuda.synchronize()
+    if T > 0:
+        assert int(ws[:4].view(torch.int32).item()) == 0, "a bounded tensor-core wait gave up"
     out_h, st_h = host(out), host(st)
     if heads is None:
         out_ref, st_ref = oracle.prefill(d["qkv"], d["alpha"], d["beta"], d["state"], shape.Hk, shape.Hv,
@@ -57,7 +61,9 @@ def _run(shape, T, seed, heads=None, **kw):
 
 
 @pytest.mark.parametrize("shape,T", [(gen.TINY, 64), (gen.TINY, 300), (gen.QWEN_27B, 129),
-                                     (gen.Shape(1, 2, 4, 64, 64), 1), (gen.Shape(1, 1, 2, 128, 128), 511)])
+                                     (gen.Shape(1, 2, 4, 64, 64), 1), (gen.Shape(1, 1, 2, 128, 128), 511),
+                                     (gen.Shape(1, 1, 3, 128, 128), 1), (gen.Shape(1, 1, 3, 128, 128), 64),
+                                     (gen.Shape(1, 2, 2, 128, 128), 65), (gen.QWEN_27B, 1000)])
 def test_prefill_small_vs_oracle(shape, T):
     out, st, out_ref, st_ref = _run(shape, T, 40 + T)
     assert_out_close(out, out_ref)
@@ -68,6 +74,18 @@ def test_prefill_27b_8192_sampled_heads():
     """1 sequence, 8,192 tokens, 27B head shape, chunk 64; key heads 0 and 13."""
     out, st, out_ref, st_ref = _run(gen.QWEN_27B, 8192, 0, heads=[0, 13])
     assert_out_close(out, out_ref)
+    assert_state_close(st, st_ref)
+
+
+def test_prefill_options_27b():
+    """q scale and bf16 outputs on the tensor-core path."""
+    shape = gen.Shape(1, 2, 6, 128, 128)
+    out, st, out_ref, st_ref = _run(shape, 200, 3, q_scale=0.25)
+    assert_out_close(out, out_ref)
+    assert_state_close(st, st_ref)
+    out, st, out_ref, st_ref = _run(shape, 150, 4, out_bf16=True)
+    got = gen.bf16_bits_to_f32(out).astype(np.float64)
+    assert np.all(np.abs(got - out_ref) <= np.abs(out_ref) * 2.0 ** -8 + 1e-3)
     assert_state_close(st, st_ref)
 
 
