@@ -10,11 +10,15 @@ Prints ONE JSON line (rank 0).  The metric is GDN state updates per second
 Workloads (27B head shape: 16 key heads, 48 value heads, d = 128):
   batched  (default) one step = conv + decode of one token for 64 sequences in
            each of 48 GDN layers (independent fp32 states, 9.66 GB).
-  decode1  one step = conv + decode of one token, one layer, batch 1 (L2
-           flushed between steps, as the other layers would evict the state).
+  decode1  one step = conv + decode of one token, one layer, batch 1; L2 is
+           flushed between steps (the other layers evict the state in a real
+           decode) and the flush is outside the timed intervals.
   tree     one step = tree conv + verify of a 32-node draft tree + commit of a
-           random root-to-leaf path, one layer.
+           random root-to-leaf path, one layer (L2 flushed between steps).
   prefill  one step = chunked prefill of 8,192 tokens, one layer.
+
+Timing: CUDA events on the launching stream after every kernel of a step, so
+the same timed region gives the step time and each kernel's launch duration.
 
 Multi-GPU: the path shards without any exchange (sequences, layers and heads
 are independent), so N ranks run N independent replicas; value = all ranks'
@@ -39,12 +43,16 @@ if ROOT not in sys.path:
 
 METRIC = "GDN state-updates/sec (head·tokens/s) and achieved HBM GB/s vs GB300 peak"
 UNIT = "head·tokens/s"
-FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "sm_max_mhz": 2070.0}
 NOMINAL_HBM_GBS = 8000.0
+SMS = 152               # GB300 streaming multiprocessors
+FP32_LANES_PER_SM = 128  # fp32 FMA lanes per SM
 
 # 27B head shape
 HK, HV, DK, DV = 16, 48, 128, 128
 C_QKV = 2 * HK * DK + HV * DV
+CHUNK = 64
 
 
 # ---------------------------------------------------------------------------
@@ -56,6 +64,11 @@ def load_peaks() -> tuple[dict, str]:
         with open(path) as f:
             return json.load(f), "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+def fp32_alu_peak_tflops(sm_mhz: float) -> float:
+    """FP32 CUDA-core peak: SMs x fp32 lanes x 2 flops (FMA) x clock."""
+    return SMS * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
 
 
 def dist_env() -> tuple[int, int, int]:
@@ -179,16 +192,11 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-# workloads
+# algorithmic work per launch (what the roofline divides by)
 # ---------------------------------------------------------------------------
-DECODE_SOURCES = ["hybrid_linear_attention_conv_gb300/csrc/gdn_decode.cu",
-                  "hybrid_linear_attention_conv_gb300/csrc/gdn_step.cuh",
-                  "hybrid_linear_attention_conv_gb300/csrc/gdn_internal.h"]
-
-
 def decode_bytes_per_launch(B: int, T: int = 1) -> int:
-    """Algorithmic HBM bytes of one decode launch: the state read and written
-    once, q/k/v read once (bf16), alpha/beta read (fp32), outputs written (fp32)."""
+    """HBM bytes of one decode launch: the state read and written once, q/k/v
+    read once (bf16), alpha/beta read (fp32), outputs written (fp32)."""
     state = B * HV * DV * DK * 4 * 2
     act = B * T * C_QKV * 2 + B * T * HV * 4 * 2 + B * T * HV * DV * 4
     return state + act
@@ -199,94 +207,195 @@ def conv_bytes_per_launch(B: int, T: int = 1) -> int:
     return B * T * C_QKV * 2 + C_QKV * 4 * 2 + 2 * B * 4 * C_QKV * 2 + B * T * C_QKV * 2
 
 
-class Batched:
+def step_flops_per_head_token() -> int:
+    """fp32 flops of one state update of one head: s.k and s.q (2 x 2d per
+    row), alpha s + u k (2d per row), the row scalars u and o (5 per row)."""
+    return DV * (6 * DK + 5)
+
+
+def prefill_flops(T: int) -> int:
+    """Algorithmic flops of the chunk form over T tokens (chunk 64): per value
+    head and chunk, S k and S q (2 x 2.64.d.d), T X and P U (2 x 2.64.64.d),
+    the state update (2.d.d.64) and the triangular solve (64^3/3); per key head
+    and chunk, K K^T and Q K^T (2 x 2.64.64.d)."""
+    n = (T + CHUNK - 1) // CHUNK
+    per_v = 2 * 2 * CHUNK * DV * DK + 2 * 2 * CHUNK * CHUNK * DV + 2 * DV * DK * CHUNK + CHUNK ** 3 // 3
+    per_k = 2 * 2 * CHUNK * CHUNK * DK
+    return n * (HV * per_v + HK * per_k)
+
+
+def prefill_bytes(T: int) -> int:
+    """q, k, v read once (bf16), alpha/beta read, outputs written (fp32), the
+    state read and written once."""
+    return T * C_QKV * 2 + T * HV * 8 + T * HV * DV * 4 + 2 * HV * DV * DK * 4
+
+
+DECODE_SOURCES = ["hybrid_linear_attention_conv_gb300/csrc/gdn_decode.cu",
+                  "hybrid_linear_attention_conv_gb300/csrc/gdn_step.cuh",
+                  "hybrid_linear_attention_conv_gb300/csrc/gdn_internal.h"]
+PREFILL_SOURCES = ["hybrid_linear_attention_conv_gb300/csrc/gdn_prefill.cu",
+                   "hybrid_linear_attention_conv_gb300/csrc/gdn_tc.cuh",
+                   "hybrid_linear_attention_conv_gb300/csrc/gdn_internal.h"]
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+class Recorder:
+    """CUDA events recorded on the launching stream after every kernel."""
+
+    def __init__(self, torch, stream, marks_per_step: int, steps: int):
+        self.stream = stream
+        self.events = [[torch.cuda.Event(enable_timing=True) for _ in range(marks_per_step + 1)]
+                       for _ in range(steps)]
+        self.names = [[None] * (marks_per_step + 1) for _ in range(steps)]
+        self.i = -1
+        self.k = 0
+
+    def begin(self, i: int):
+        """Start the next timed step (`i` is the workload's own step number)."""
+        self.i, self.k = self.i + 1, 0
+        self.events[self.i][0].record(self.stream)
+
+    def mark(self, name: str):
+        self.k += 1
+        self.names[self.i][self.k] = name
+        self.events[self.i][self.k].record(self.stream)
+
+    def step_ms(self) -> list:
+        return [ev[0].elapsed_time(ev[-1]) for ev in self.events]
+
+    def kernel_ms(self, name: str) -> list:
+        out = []
+        for ev, nm in zip(self.events, self.names):
+            for k in range(1, len(ev)):
+                if nm[k] == name:
+                    out.append(ev[k - 1].elapsed_time(ev[k]))
+        return out
+
+
+def _call(fn, args, gdn):
+    rc = fn(*args)
+    if rc != 0:
+        raise RuntimeError(f"{fn.__name__} failed: {gdn.last_error()}")
+
+
+class Workload:
+    """Common plumbing: device inputs, the stream, optional L2 flush."""
+
+    flush = False
+    launches_per_step = 0
+    units_per_step = 0
+
+    @property
+    def marks_per_step(self) -> int:
+        """CUDA events recorded per step after the first (one per marked call)."""
+        return self.launches_per_step
+
+    def __init__(self, device, seed: int):
+        import torch
+        from hybrid_linear_attention_conv_gb300 import gdn
+        self.torch, self.gdn, self.lib = torch, gdn, gdn.load()
+        self.device = device
+        self.gen = torch.Generator(device=device)
+        self.gen.manual_seed(seed)
+        self.stream = torch.cuda.current_stream()
+        self.sp = ctypes.c_void_p(self.stream.cuda_stream)
+        self.flush_buf = None
+        if self.flush:
+            # 256 MB > the 129 MB L2: writing it evicts the previous step's lines
+            self.flush_buf = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=device)
+
+    def randn(self, shape, scale=1.0, dtype=None):
+        t = self.torch.randn(shape, generator=self.gen, device=self.device)
+        if scale != 1.0:
+            t.mul_(scale)
+        return t.to(dtype) if dtype is not None else t
+
+    def gates(self, shape):
+        torch = self.torch
+        a = 0.9 + 0.1 * torch.rand(shape, generator=self.gen, device=self.device)
+        b = torch.sigmoid(torch.randn(shape, generator=self.gen, device=self.device))
+        return a, b
+
+    def pre_step(self):
+        if self.flush_buf is not None:
+            self.flush_buf.zero_()
+
+    def e2e_copy(self, dst, src):
+        dst.copy_(src, non_blocking=True)
+
+
+class Batched(Workload):
     """48 GDN layers x 64 sequences, one token per sequence per layer."""
 
     name = "batched"
     L, B = 48, 64
 
-    def __init__(self, device, seed: int, n_sets: int, layers: int = 48):
+    def __init__(self, device, seed: int, steps: int, layers: int = 48):
+        super().__init__(device, seed)
         self.L = layers
-        import torch
-        from hybrid_linear_attention_conv_gb300 import gdn
-        self.torch, self.gdn = torch, gdn
-        self.lib = gdn.load()
+        torch, gdn = self.torch, self.gdn
         L, B = self.L, self.B
-        g = torch.Generator(device=device)
-        g.manual_seed(seed)
         bf = torch.bfloat16
-        self.state = torch.randn((L, B, HV, DV, DK), generator=g, device=device, dtype=torch.float32)
-        self.state.mul_(0.1)
-        self.w = (0.5 * torch.randn((L, C_QKV, 4), generator=g, device=device)).to(bf)
-        self.tail = torch.randn((L, B, 4, C_QKV), generator=g, device=device).to(bf)
-        self.n_sets = n_sets
-        self.x = torch.randn((n_sets, L, B, 1, C_QKV), generator=g, device=device).to(bf)
-        self.alpha = 0.9 + 0.1 * torch.rand((n_sets, L, B, 1, HV), generator=g, device=device)
-        self.beta = torch.sigmoid(torch.randn((n_sets, L, B, 1, HV), generator=g, device=device))
+        self.state = self.randn((L, B, HV, DV, DK), 0.1)
+        self.w = self.randn((L, C_QKV, 4), 0.5, bf)
+        self.tail = self.randn((L, B, 4, C_QKV), 1.0, bf)
+        self.n_sets = min(4, steps)
+        self.x = self.randn((self.n_sets, L, B, 1, C_QKV), 1.0, bf)
+        self.alpha, self.beta = self.gates((self.n_sets, L, B, 1, HV))
         self.y = torch.empty((B, 1, C_QKV), dtype=bf, device=device)
         self.out = torch.empty((L, B, 1, HV, DV), dtype=torch.float32, device=device)
         self.shape = gdn.gdn_shape(B, HK, HV, DK, DV)
-        self.stream = torch.cuda.current_stream()
-        sp = ctypes.c_void_p(self.stream.cuda_stream)
         P = ctypes.c_void_p
         self.args = []
-        for s in range(n_sets):
+        for s in range(self.n_sets):
             per = []
             for l in range(L):
                 conv = (B, 1, C_QKV, None, P(self.x[s, l].data_ptr()), P(self.w[l].data_ptr()),
-                        P(self.tail[l].data_ptr()), P(self.y.data_ptr()), 0, sp)
+                        P(self.tail[l].data_ptr()), P(self.y.data_ptr()), 0, self.sp)
                 dec = (ctypes.byref(self.shape), 1, P(self.y.data_ptr()), P(self.alpha[s, l].data_ptr()),
                        P(self.beta[s, l].data_ptr()), P(self.state[l].data_ptr()),
-                       P(self.out[l].data_ptr()), 1.0, gdn.GDN_NORMALIZE_QK, sp)
+                       P(self.out[l].data_ptr()), 1.0, gdn.GDN_NORMALIZE_QK, self.sp)
                 per.append((conv, dec))
             self.args.append(per)
         self.launches_per_step = 2 * L
-        self.units_per_step = L * B * HV  # head.tokens
+        self.units_per_step = L * B * HV
         self.dominant = "gdn_decode_kernel"
-        self.dominant_bytes = decode_bytes_per_launch(B)
+        self.dominant_sources = DECODE_SOURCES
+        self.bound = "hbm"
+        self.dominant_work = decode_bytes_per_launch(B)
         self.step_bytes = L * (decode_bytes_per_launch(B) + conv_bytes_per_launch(B))
 
-    def step(self, i: int, events=None):
-        """Enqueue step i; events (list of 2L+1) are recorded around each kernel."""
-        lib = self.lib
-        conv_fn, dec_fn = lib.gdn_conv_step, lib.gdn_decode_step
-        if events is not None:
-            events[0].record(self.stream)
-        for l, (conv, dec) in enumerate(self.args[i % self.n_sets]):
-            rc = conv_fn(*conv)
-            if events is not None:
-                events[2 * l + 1].record(self.stream)
-            rc |= dec_fn(*dec)
-            if events is not None:
-                events[2 * l + 2].record(self.stream)
-            if rc != 0:
-                raise RuntimeError(f"gdn call failed: {self.gdn.last_error()}")
+    def step(self, i: int, rec: Recorder | None = None):
+        lib, gdn = self.lib, self.gdn
+        if rec:
+            rec.begin(i)
+        for conv, dec in self.args[i % self.n_sets]:
+            _call(lib.gdn_conv_step, conv, gdn)
+            if rec:
+                rec.mark("gdn_conv_kernel")
+            _call(lib.gdn_decode_step, dec, gdn)
+            if rec:
+                rec.mark("gdn_decode_kernel")
 
-    def dominant_ms(self, events) -> list:
-        """Durations of the decode launches of one instrumented step."""
-        return [events[2 * l + 1].elapsed_time(events[2 * l + 2]) for l in range(self.L)]
-
-    # end-to-end: inputs from pinned host memory, outputs back to the host
     def e2e_setup(self):
         torch = self.torch
-        self.h_x = torch.empty(self.x[0].shape, dtype=self.x.dtype, pin_memory=True)
-        self.h_x.copy_(self.x[0])
-        self.h_a = torch.empty(self.alpha[0].shape, dtype=torch.float32, pin_memory=True)
-        self.h_a.copy_(self.alpha[0])
-        self.h_b = torch.empty(self.beta[0].shape, dtype=torch.float32, pin_memory=True)
-        self.h_b.copy_(self.beta[0])
+        self.h_x = self.x[0].cpu().pin_memory()
+        self.h_a = self.alpha[0].cpu().pin_memory()
+        self.h_b = self.beta[0].cpu().pin_memory()
         self.h_out = torch.empty(self.out.shape, dtype=torch.float32, pin_memory=True)
-        self.e2e_h2d = (self.h_x.numel() * 2 + self.h_a.numel() * 4 + self.h_b.numel() * 4)
+        self.e2e_h2d = self.h_x.numel() * 2 + self.h_a.numel() * 4 + self.h_b.numel() * 4
         self.e2e_d2h = self.h_out.numel() * 4
 
     def e2e_step(self, i: int):
-        self.x[0].copy_(self.h_x, non_blocking=True)
-        self.alpha[0].copy_(self.h_a, non_blocking=True)
-        self.beta[0].copy_(self.h_b, non_blocking=True)
+        self.e2e_copy(self.x[0], self.h_x)
+        self.e2e_copy(self.alpha[0], self.h_a)
+        self.e2e_copy(self.beta[0], self.h_b)
         for conv, dec in self.args[0]:
-            if self.lib.gdn_conv_step(*conv) | self.lib.gdn_decode_step(*dec):
-                raise RuntimeError(self.gdn.last_error())
-        self.h_out.copy_(self.out, non_blocking=True)
+            _call(self.lib.gdn_conv_step, conv, self.gdn)
+            _call(self.lib.gdn_decode_step, dec, self.gdn)
+        self.e2e_copy(self.h_out, self.out)
 
     def config(self=None) -> dict:
         L = Batched.L if self is None else self.L
@@ -295,34 +404,310 @@ class Batched:
         return {"workload": f"batched decode over {L} GDN layers: batch {B} sequences, 27B head "
                             "shape (16 key / 48 value heads x 128), independent fp32 states, one token "
                             "per sequence per layer (conv + delta step)",
-                "layers": L, "batch": B, "Hk": HK, "Hv": HV, "dk": DK, "dv": DV,
-                "state_bytes": sb,
+                "layers": L, "batch": B, "Hk": HK, "Hv": HV, "dk": DK, "dv": DV, "state_bytes": sb,
                 "l2": f"inputs larger than L2: {sb / 1e9:.2f} GB of state streamed per step",
-                "launch": "eager, CUDA events between kernels"}
+                "launch": "eager, CUDA events after every kernel"}
 
 
-def cpu_oracle_sample(seconds: float = 10.0) -> dict:
-    """The oracle as it stands: conv + decode of one sequence, one layer, one
-    token (48 head.tokens) at the 27B shape, repeated for about `seconds`."""
-    import numpy as np
-    import oracle
-    from hybrid_linear_attention_conv_gb300 import inputs as gen
-    s = gen.QWEN_27B
-    c = gen.conv_inputs(0, 1, 1, s.C)
-    d = gen.decode_inputs(0, s, 1)
-    state = d["state"].astype(np.float64)
-    n = 0
+class Decode1(Workload):
+    """One layer, batch 1: conv + decode of one token per step."""
+
+    name = "decode1"
+    flush = True
+
+    def __init__(self, device, seed: int, steps: int):
+        super().__init__(device, seed)
+        torch, gdn = self.torch, self.gdn
+        bf = torch.bfloat16
+        self.n = steps
+        self.state = self.randn((1, HV, DV, DK), 0.1)
+        self.w = self.randn((C_QKV, 4), 0.5, bf)
+        self.tail = self.randn((1, 4, C_QKV), 1.0, bf)
+        self.x = self.randn((self.n, 1, 1, C_QKV), 1.0, bf)
+        self.alpha, self.beta = self.gates((self.n, 1, 1, HV))
+        self.y = torch.empty((1, 1, C_QKV), dtype=bf, device=device)
+        self.out = torch.empty((self.n, 1, 1, HV, DV), dtype=torch.float32, device=device)
+        self.shape = gdn.gdn_shape(1, HK, HV, DK, DV)
+        self.launches_per_step = 2
+        self.units_per_step = HV
+        self.dominant = "gdn_decode_kernel"
+        self.dominant_sources = DECODE_SOURCES
+        self.bound = "hbm"
+        self.dominant_work = decode_bytes_per_launch(1)
+        self.step_bytes = decode_bytes_per_launch(1) + conv_bytes_per_launch(1)
+
+    def _args(self, s):
+        P = ctypes.c_void_p
+        conv = (1, 1, C_QKV, None, P(self.x[s].data_ptr()), P(self.w.data_ptr()), P(self.tail.data_ptr()),
+                P(self.y.data_ptr()), 0, self.sp)
+        dec = (ctypes.byref(self.shape), 1, P(self.y.data_ptr()), P(self.alpha[s].data_ptr()),
+               P(self.beta[s].data_ptr()), P(self.state.data_ptr()), P(self.out[s].data_ptr()), 1.0,
+               self.gdn.GDN_NORMALIZE_QK, self.sp)
+        return conv, dec
+
+    def step(self, i: int, rec: Recorder | None = None):
+        conv, dec = self._args(i % self.n)
+        if rec:
+            rec.begin(i)
+        _call(self.lib.gdn_conv_step, conv, self.gdn)
+        if rec:
+            rec.mark("gdn_conv_kernel")
+        _call(self.lib.gdn_decode_step, dec, self.gdn)
+        if rec:
+            rec.mark("gdn_decode_kernel")
+
+    def e2e_setup(self):
+        self.h_x = self.x[0].cpu().pin_memory()
+        self.h_a = self.alpha[0].cpu().pin_memory()
+        self.h_b = self.beta[0].cpu().pin_memory()
+        self.h_out = self.torch.empty(self.out[0].shape, dtype=self.torch.float32, pin_memory=True)
+        self.e2e_h2d = self.h_x.numel() * 2 + self.h_a.numel() * 4 + self.h_b.numel() * 4
+        self.e2e_d2h = self.h_out.numel() * 4
+
+    def e2e_step(self, i: int):
+        self.e2e_copy(self.x[0], self.h_x)
+        self.e2e_copy(self.alpha[0], self.h_a)
+        self.e2e_copy(self.beta[0], self.h_b)
+        conv, dec = self._args(0)
+        _call(self.lib.gdn_conv_step, conv, self.gdn)
+        _call(self.lib.gdn_decode_step, dec, self.gdn)
+        self.e2e_copy(self.h_out, self.out[0])
+
+    @staticmethod
+    def config() -> dict:
+        return {"workload": "27B-shape single-token decode, one layer: batch 1, 16 key / 48 value heads "
+                            "x 128, fp32 state 3.15 MB, bf16 inputs, 4-tap bf16 conv tail over 10,240 "
+                            "channels (conv + delta step per token)",
+                "layers": 1, "batch": 1, "Hk": HK, "Hv": HV, "dk": DK, "dv": DV,
+                "l2": "L2 flushed (256 MB write) before every step, outside the timed intervals",
+                "launch": "eager, CUDA events around the step's kernels"}
+
+
+class Tree(Workload):
+    """One speculative round on one layer: tree conv, verify, commit."""
+
+    name = "tree"
+    flush = True
+    N = 32
+
+    def __init__(self, device, seed: int, steps: int):
+        super().__init__(device, seed)
+        import numpy as np
+        from hybrid_linear_attention_conv_gb300 import inputs as gen
+        torch, gdn = self.torch, self.gdn
+        bf = torch.bfloat16
+        N = self.N
+        self.parents = np.ascontiguousarray(gen.random_tree(seed, N, 8), np.int32)
+        self.path = np.ascontiguousarray(gdn.tree_root_path(self.parents, gen.random_leaf(seed, self.parents)),
+                                         np.int32)
+        self.n_sets = min(8, steps)
+        self.state = self.randn((HV, DV, DK), 0.1)
+        self.w = self.randn((C_QKV, 4), 0.5, bf)
+        self.tail = self.randn((1, 4, C_QKV), 1.0, bf)
+        self.x = self.randn((self.n_sets, 1, N, C_QKV), 1.0, bf)
+        self.alpha, self.beta = self.gates((self.n_sets, N, HV))
+        self.y = torch.empty((1, N, C_QKV), dtype=bf, device=device)
+        self.out = torch.empty((N, HV, DV), dtype=torch.float32, device=device)
+        self.shape = gdn.gdn_shape(1, HK, HV, DK, DV)
+        self.launches_per_step = 4  # tree conv, verify, commit replay, commit tail
+        self.tree_marks = 3          # conv, verify, commit (its two launches together)
+        self.units_per_step = (N + len(self.path)) * HV
+        self.dominant = "gdn_tree_kernel"
+        self.dominant_sources = DECODE_SOURCES
+        self.bound = "alu"
+        self.dominant_work = N * HV * step_flops_per_head_token()
+        self.step_bytes = (2 * conv_bytes_per_launch(1, N) + HV * DV * DK * 4 +
+                           N * (C_QKV * 2 + HV * 8 + HV * DV * 4) + 2 * HV * DV * DK * 4)
+
+    @property
+    def marks_per_step(self) -> int:
+        return self.tree_marks
+
+    def _run(self, s, rec=None):
+        P = ctypes.c_void_p
+        lib, gdn = self.lib, self.gdn
+        pp = self.parents.ctypes.data_as(P)
+        _call(lib.gdn_conv_step, (1, self.N, C_QKV, pp, P(self.x[s].data_ptr()), P(self.w.data_ptr()),
+                                  P(self.tail.data_ptr()), P(self.y.data_ptr()), 0, self.sp), gdn)
+        if rec:
+            rec.mark("gdn_conv_kernel")
+        _call(lib.gdn_tree_verify, (ctypes.byref(self.shape), self.N, pp, P(self.y.data_ptr()),
+                                    P(self.alpha[s].data_ptr()), P(self.beta[s].data_ptr()),
+                                    P(self.state.data_ptr()), P(self.out.data_ptr()), 1.0,
+                                    gdn.GDN_NORMALIZE_QK, self.sp), gdn)
+        if rec:
+            rec.mark("gdn_tree_kernel")
+        _call(lib.gdn_commit_path, (ctypes.byref(self.shape), self.N, pp, self.path.ctypes.data_as(P),
+                                    len(self.path), P(self.y.data_ptr()), P(self.alpha[s].data_ptr()),
+                                    P(self.beta[s].data_ptr()), P(self.x[s].data_ptr()),
+                                    P(self.state.data_ptr()), P(self.tail.data_ptr()),
+                                    gdn.GDN_NORMALIZE_QK, self.sp), gdn)
+        if rec:
+            rec.mark("commit")  # replay + tail update (two launches)
+
+    def step(self, i: int, rec: Recorder | None = None):
+        if rec:
+            rec.begin(i)
+        self._run(i % self.n_sets, rec)
+
+    def e2e_setup(self):
+        self.h_x = self.x[0].cpu().pin_memory()
+        self.h_a = self.alpha[0].cpu().pin_memory()
+        self.h_b = self.beta[0].cpu().pin_memory()
+        self.h_out = self.torch.empty(self.out.shape, dtype=self.torch.float32, pin_memory=True)
+        self.e2e_h2d = self.h_x.numel() * 2 + self.h_a.numel() * 4 + self.h_b.numel() * 4
+        self.e2e_d2h = self.h_out.numel() * 4
+
+    def e2e_step(self, i: int):
+        self.e2e_copy(self.x[0], self.h_x)
+        self.e2e_copy(self.alpha[0], self.h_a)
+        self.e2e_copy(self.beta[0], self.h_b)
+        self._run(0)
+        self.e2e_copy(self.h_out, self.out)
+
+    def config(self=None) -> dict:
+        L = None if self is None else len(self.path)
+        return {"workload": "tree verify + commit, 27B head shape, one layer: random 32-node draft tree "
+                            "(depth <= 8, branching 1-4), state branched per node from its parent, random "
+                            "root-to-leaf path committed (tree conv + verify + commit per step)",
+                "nodes": Tree.N, "path_len": L, "Hk": HK, "Hv": HV, "dk": DK, "dv": DV,
+                "units": "head.tokens = (verified nodes + committed tokens) x 48 value heads",
+                "l2": "L2 flushed (256 MB write) before every step, outside the timed intervals",
+                "launch": "eager, CUDA events around the step's kernels"}
+
+
+class Prefill(Workload):
+    """Chunked prefill of 8,192 tokens, one layer."""
+
+    name = "prefill"
+    T = 8192
+
+    def __init__(self, device, seed: int, steps: int):
+        super().__init__(device, seed)
+        torch, gdn = self.torch, self.gdn
+        T = self.T
+        self.state = self.randn((HV, DV, DK), 0.1)
+        self.qkv = self.randn((T, C_QKV), 1.0, torch.bfloat16)
+        self.alpha, self.beta = self.gates((T, HV))
+        self.out = torch.empty((T, HV, DV), dtype=torch.float32, device=device)
+        nbytes = gdn.prefill_workspace_bytes(T, HK, HV, DK, DV)
+        self.ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+        self.shape = gdn.gdn_shape(1, HK, HV, DK, DV)
+        self.launches_per_step = 1
+        self.units_per_step = T * HV
+        self.dominant = "gdn_prefill_tc_kernel"
+        self.dominant_sources = PREFILL_SOURCES
+        self.bound = "tensor"
+        self.dominant_work = prefill_flops(T)
+        self.step_bytes = prefill_bytes(T)
+
+    def _args(self):
+        P = ctypes.c_void_p
+        return (ctypes.byref(self.shape), self.T, CHUNK, P(self.qkv.data_ptr()), P(self.alpha.data_ptr()),
+                P(self.beta.data_ptr()), P(self.state.data_ptr()), P(self.out.data_ptr()),
+                P(self.ws.data_ptr()), self.ws.numel(), 1.0, self.gdn.GDN_NORMALIZE_QK, self.sp)
+
+    def step(self, i: int, rec: Recorder | None = None):
+        if rec:
+            rec.begin(i)
+        _call(self.lib.gdn_chunk_prefill, self._args(), self.gdn)
+        if rec:
+            rec.mark("gdn_prefill_tc_kernel")
+
+    def check_status(self):
+        st = int(self.ws[:4].view(self.torch.int32).item())
+        if st != 0:
+            raise RuntimeError("prefill reported a tensor-core wait timeout")
+
+    def e2e_setup(self):
+        self.h_qkv = self.qkv.cpu().pin_memory()
+        self.h_a = self.alpha.cpu().pin_memory()
+        self.h_b = self.beta.cpu().pin_memory()
+        self.h_out = self.torch.empty(self.out.shape, dtype=self.torch.float32, pin_memory=True)
+        self.e2e_h2d = self.h_qkv.numel() * 2 + self.h_a.numel() * 4 + self.h_b.numel() * 4
+        self.e2e_d2h = self.h_out.numel() * 4
+
+    def e2e_step(self, i: int):
+        self.e2e_copy(self.qkv, self.h_qkv)
+        self.e2e_copy(self.alpha, self.h_a)
+        self.e2e_copy(self.beta, self.h_b)
+        _call(self.lib.gdn_chunk_prefill, self._args(), self.gdn)
+        self.e2e_copy(self.h_out, self.out)
+
+    @staticmethod
+    def config() -> dict:
+        return {"workload": "chunked prefill: 1 sequence, 8,192 tokens, 27B head shape, chunk 64, bf16 "
+                            "q/k/v, fp32 alpha/beta/state, WY/UT chunk form on tcgen05 tensor cores",
+                "tokens": Prefill.T, "chunk": CHUNK, "Hk": HK, "Hv": HV, "dk": DK, "dv": DV,
+                "l2": "inputs larger than L2: 168 MB of q/k/v read and 201 MB of outputs per step",
+                "launch": "eager, CUDA events around the launch"}
+
+
+WORKLOADS = {"batched": Batched, "decode1": Decode1, "tree": Tree, "prefill": Prefill}
+DEFAULT_STEPS = {"batched": 100, "decode1": 1000, "tree": 200, "prefill": 20}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+class OracleSample:
+    """A bounded sample of a workload run by the fp64 C oracle as it stands."""
+
+    def __init__(self, workload: str):
+        import numpy as np
+        import oracle
+        from hybrid_linear_attention_conv_gb300 import inputs as gen
+        oracle.build()
+        self.np, self.oracle, self.gen = np, oracle, gen
+        self.workload = workload
+        s = self.s = gen.QWEN_27B
+        if workload in ("batched", "decode1"):
+            self.c = gen.conv_inputs(0, 1, 1, s.C)
+            self.d = gen.decode_inputs(0, s, 1)
+            self.state = self.d["state"].astype(np.float64)
+            self.units = s.Hv
+            self.desc = "conv + decode of 1 sequence x 1 layer x 1 token (48 head.tokens)"
+        elif workload == "tree":
+            self.parents = gen.random_tree(0, 32, 8)
+            self.c = gen.conv_inputs(0, 1, 32, s.C)
+            self.d = gen.decode_inputs(0, s, 32, tag="tree")
+            self.path = oracle.root_path(self.parents, gen.random_leaf(0, self.parents))
+            self.units = (32 + len(self.path)) * s.Hv
+            self.desc = (f"tree conv + verify (32 nodes, root-path replay) + commit ({len(self.path)} "
+                         f"tokens) of one layer")
+        else:
+            self.Ts = 128
+            self.d = gen.decode_inputs(0, s, self.Ts, tag="prefill")
+            self.units = self.Ts * s.Hv
+            self.desc = f"sequential prefill of {self.Ts} of the 8,192 tokens, all 48 value heads"
+
+    def run_once(self) -> int:
+        o, s, d = self.oracle, self.s, self.d
+        if self.workload in ("batched", "decode1"):
+            y, _ = o.conv_linear(self.c["x"], self.c["w"], self.c["tail"])
+            _, self.state = o.decode(o.f64_to_bf16(y), d["alpha"], d["beta"], self.state, s.Hk, s.Hv, s.dk, s.dv)
+        elif self.workload == "tree":
+            y = o.f64_to_bf16(o.conv_tree(self.parents, self.c["x"][0], self.c["w"], self.c["tail"][0]))
+            o.tree_verify(self.parents, y, d["alpha"][0], d["beta"][0], d["state"][0], s.Hk, s.Hv, s.dk, s.dv)
+            o.commit(self.parents, self.path, y, d["alpha"][0], d["beta"][0], d["state"][0], s.Hk, s.Hv,
+                     s.dk, s.dv, x_tree=self.c["x"][0], tail=self.c["tail"][0])
+        else:
+            o.prefill(d["qkv"], d["alpha"], d["beta"], d["state"], s.Hk, s.Hv, s.dk, s.dv)
+        return self.units
+
+
+def cpu_oracle_sample(workload: str, seconds: float) -> dict:
+    smp = OracleSample(workload)
+    n, units = 0, 0
     t0 = time.perf_counter()
     while True:
-        y, _ = oracle.conv_linear(c["x"], c["w"], c["tail"])
-        _, state = oracle.decode(oracle.f64_to_bf16(y), d["alpha"], d["beta"], state, s.Hk, s.Hv, s.dk, s.dv)
+        units += smp.run_once()
         n += 1
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    return {"value": n * s.Hv / el, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n} x (conv + decode of 1 sequence x 1 layer x 1 token, 48 value heads, 27B "
-                      f"head shape), fp64 C oracle, single thread, {el:.1f} s"}
+    return {"value": units / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} x ({smp.desc}), 27B head shape, fp64 C oracle, single thread, {el:.1f} s"}
 
 
 # ---------------------------------------------------------------------------
@@ -341,56 +726,83 @@ def run_ours(args) -> dict | None:
     __graft_entry__.build()
 
     peaks, peaks_kind = load_peaks()
-    wl = Batched(device, seed=1234 + rank, n_sets=min(4, args.steps + args.warmup), layers=args.layers)
+    cls = WORKLOADS[args.workload]
+    if cls is Batched:
+        wl = Batched(device, 1234 + rank, args.steps + args.warmup, layers=args.layers)
+    else:
+        wl = cls(device, 1234 + rank, args.steps + args.warmup)
     torch.cuda.synchronize()
 
     for i in range(args.warmup):
+        wl.pre_step()
         wl.step(i)
     torch.cuda.synchronize()
 
-    # timed region: K steps, an event after every kernel
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(wl.launches_per_step + 1)]
-           for _ in range(args.steps)]
+    rec = Recorder(torch, wl.stream, wl.marks_per_step, args.steps)
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.2)
     barrier(world)
     torch.cuda.synchronize()
     for i in range(args.steps):
-        wl.step(args.warmup + i, evs[i])
+        wl.pre_step()
+        wl.step(args.warmup + i, rec)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
-    step_ms = [evs[i][0].elapsed_time(evs[i][-1]) for i in range(args.steps)]
-    total_s = evs[0][0].elapsed_time(evs[-1][-1]) / 1e3
-    dom_ms = [d for i in range(args.steps) for d in wl.dominant_ms(evs[i])]
+    if hasattr(wl, "check_status"):
+        wl.check_status()
+    step_ms = rec.step_ms()
+    total_s = sum(step_ms) / 1e3
+    dom_ms = rec.kernel_ms(wl.dominant)
     agg = aggregate(wl.units_per_step * args.steps, total_s, world, device)
 
     # end-to-end through the API with host buffers
     wl.e2e_setup()
     for i in range(2):
+        wl.pre_step()
         wl.e2e_step(i)
     torch.cuda.synchronize()
     barrier(world)
-    t0 = time.perf_counter()
+    # each step: host->device copies of the step's inputs (pinned), the C-ABI
+    # calls, the device->host copy of the outputs; timed by events on the stream
+    e2e_total = 0.0
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
     for i in range(args.steps):
+        wl.pre_step()
+        e0.record()
         wl.e2e_step(i)
-    e1.record()
-    torch.cuda.synchronize()
-    e2e_s = max(e0.elapsed_time(e1) / 1e3, time.perf_counter() - t0)
-    e2e = aggregate(wl.units_per_step * args.steps, e2e_s, world, device)
+        e1.record()
+        e1.synchronize()
+        e2e_total += e0.elapsed_time(e1) / 1e3
+    e2e = aggregate(wl.units_per_step * args.steps, e2e_total, world, device)
 
     if rank != 0:
         return None
 
     dom_avg_s = statistics.mean(dom_ms) / 1e3
-    achieved = wl.dominant_bytes / dom_avg_s / 1e9
-    peak = float(peaks["hbm_gbs"])
-    traffic = ncu_traffic(wl.dominant, DECODE_SOURCES)
+    if wl.bound == "hbm":
+        achieved = wl.dominant_work / dom_avg_s / 1e9
+        peak, unit = float(peaks["hbm_gbs"]), "GB/s"
+        peak_kind = peaks_kind
+    elif wl.bound == "tensor":
+        achieved = wl.dominant_work / dom_avg_s / 1e12
+        peak, unit = float(peaks["bf16_tflops"]), "TFLOP/s"
+        peak_kind = f"{peaks_kind} bf16 dense (burst), algorithmic flops only"
+    else:
+        achieved = wl.dominant_work / dom_avg_s / 1e12
+        mhz = float(peaks.get("sm_max_mhz", 2070.0))
+        peak, unit = fp32_alu_peak_tflops(mhz), "TFLOP/s"
+        peak_kind = f"derived fp32 FMA peak: {SMS} SMs x {FP32_LANES_PER_SM} lanes x 2 x {mhz:.0f} MHz"
+    traffic = ncu_traffic(wl.dominant, wl.dominant_sources)
     step_gbs = wl.step_bytes * args.steps / total_s / 1e9
+    roof = {"bound": wl.bound, "kernel": wl.dominant, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "peak_kind": peak_kind, "avg_launch_us": dom_avg_s * 1e6,
+            "work_per_launch": wl.dominant_work,
+            "work_unit": "bytes" if wl.bound == "hbm" else "flops", "traffic": traffic}
+    if wl.bound == "hbm":
+        roof["frac_nominal_8tbs"] = achieved / NOMINAL_HBM_GBS
     line = {
         "metric": METRIC,
         "value": agg["value"],
@@ -406,20 +818,15 @@ def run_ours(args) -> dict | None:
         "data": "synthetic (seeded device RNG; 27B head shape, random-init states)",
         "config": wl.config(),
         "hbm_gbs_step": step_gbs,
-        "hbm_frac_step": step_gbs / peak,
-        "hbm_frac_step_nominal_8tbs": step_gbs / NOMINAL_HBM_GBS,
-        "roofline": {"bound": "hbm", "kernel": wl.dominant, "achieved": achieved, "peak": peak,
-                     "unit": "GB/s", "frac": achieved / peak, "peak_kind": peaks_kind,
-                     "frac_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
-                     "bytes_per_launch": wl.dominant_bytes, "avg_launch_us": dom_avg_s * 1e6,
-                     "traffic": traffic},
+        "hbm_frac_step": step_gbs / float(peaks["hbm_gbs"]),
+        "roofline": roof,
         "clocks": clk,
         "e2e": {"value": e2e["value"], "unit": UNIT, "h2d_bytes_per_step": wl.e2e_h2d,
-                "d2h_bytes_per_step": wl.e2e_d2h, "ms_per_step": e2e_s * 1e3 / args.steps},
+                "d2h_bytes_per_step": wl.e2e_d2h, "ms_per_step": e2e_total * 1e3 / args.steps},
         "gpu_launches": wl.launches_per_step * args.steps,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_oracle_sample(args.cpu_seconds)
+        line["cpu_baseline"] = cpu_oracle_sample(args.workload, args.cpu_seconds)
     return line
 
 
@@ -427,35 +834,23 @@ def run_reference(args) -> dict | None:
     rank, world, _ = dist_env()
     if rank != 0:
         return None
-    import numpy as np
-    import oracle
-    from hybrid_linear_attention_conv_gb300 import inputs as gen
-    oracle.build()
-    s = gen.QWEN_27B
-    c = gen.conv_inputs(0, 1, 1, s.C)
-    d = gen.decode_inputs(0, s, 1)
-    state = d["state"].astype(np.float64)
-
-    def one():
-        nonlocal state
-        y, _ = oracle.conv_linear(c["x"], c["w"], c["tail"])
-        _, state = oracle.decode(oracle.f64_to_bf16(y), d["alpha"], d["beta"], state, s.Hk, s.Hv, s.dk, s.dv)
-
+    smp = OracleSample(args.workload)
     for _ in range(args.warmup):
-        one()
+        smp.run_once()
+    units = 0
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        one()
+        units += smp.run_once()
     el = time.perf_counter() - t0
-    value = args.steps * s.Hv / el
-    sample = (f"each step: conv + decode of 1 sequence x 1 layer x 1 token (48 head.tokens) of the "
-              f"batched workload, fp64 C oracle, single thread")
+    value = units / el
+    sample = f"each step: {smp.desc}, 27B head shape, fp64 C oracle, single thread"
+    cfg = WORKLOADS[args.workload].config()
     return {
         "impl": "reference",
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": Batched.config(),
+        "config": cfg,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -464,16 +859,18 @@ def run_reference(args) -> dict | None:
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["batched"], default="batched")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="batched")
     ap.add_argument("--layers", type=int, default=48,
                     help="GDN layers in the batched workload (48 = the 27B model; fewer only for "
                          "profiling small cases)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
+    if args.steps is None:
+        args.steps = DEFAULT_STEPS[args.workload]
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line is not None:
