@@ -92,7 +92,33 @@ __global__ void __launch_bounds__(kConvThreads) gdn_conv_kernel(const __grid_con
         }
     }
 
-    if (!p.tree) {
+    if (!p.tree && gridDim.y == 1) {
+        // The whole run in one pass (T <= kConvTok, e.g. a decode step): a
+        // window of the four most recent inputs starts as the tail, every
+        // load is issued up front, and the new tail is the final window.
+        Vec8 h0 = load8(tb), h1 = load8(tb + C), h2 = load8(tb + 2 * C), h3 = load8(tb + 3 * C);
+        Vec8 xn = p.T > 0 ? load8(xb) : h3;
+        for (int t = 0; t < p.T; ++t) {
+            h0 = h1;
+            h1 = h2;
+            h2 = h3;
+            h3 = xn;
+            if (t + 1 < p.T) xn = load8(xb + (size_t)(t + 1) * C);
+            store_y(yb + (size_t)t * C, w, h0, h1, h2, h3);
+        }
+        auto put = [&](uint16_t* dst, const Vec8& v) {
+            uint4 o;
+            o.x = pack2(v.v[0], v.v[1]);
+            o.y = pack2(v.v[2], v.v[3]);
+            o.z = pack2(v.v[4], v.v[5]);
+            o.w = pack2(v.v[6], v.v[7]);
+            *reinterpret_cast<uint4*>(dst) = o;
+        };
+        put(tb, h0);
+        put(tb + C, h1);
+        put(tb + 2 * C, h2);
+        put(tb + 3 * C, h3);
+    } else if (!p.tree) {
         // inputs before token t0: t < 0 reads tail slot 4 + t
         const int t0 = blockIdx.y * kConvTok;
         const int t1 = min(p.T, t0 + kConvTok);

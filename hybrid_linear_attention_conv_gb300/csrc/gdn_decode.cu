@@ -76,24 +76,96 @@ gdn_decode_kernel(const __grid_constant__ DecodeParams p) {
                    s[r][m]);
 }
 
+// Shared-memory staging of the tree's inputs for one CTA (after the slots):
+// q and k of this CTA's key head for every node, this CTA's 32 rows of v, and
+// alpha/beta -- loaded once, all loads in flight together, before the walk.
+// Per node, the normalised k and q in the lane layout of TokenKQ plus k.q,
+// computed once per CTA (by one row group per node, with token_kq itself).
+template <int DK>
+__host__ __device__ constexpr size_t tree_kq_bytes(int N) {
+    return (size_t)N * (8 * 2 * (DK / 32) * 4 * 4 + 16);
+}
+
+template <int DK>
+__host__ __device__ constexpr size_t tree_stage_bytes(int N) {
+    return tree_kq_bytes<DK>(N) + (size_t)N * (kRowsPerPass * 2 + 2 * 4);
+}
+
 template <int DK>
 __global__ void __launch_bounds__(kThreads)
 gdn_tree_kernel(const __grid_constant__ TreeParams p) {
     constexpr int V = DK / 32;
-    extern __shared__ float4 slots[];  // [n_slots][32 row groups][V][8 lanes]
+    extern __shared__ float4 smem4[];
+    float4* slots = smem4;  // [n_slots][32 row groups][V][8 lanes]
+    uint8_t* stage = reinterpret_cast<uint8_t*>(smem4) + (size_t)p.n_slots * kRowsPerPass * DK * sizeof(float);
+    float4* s_kq = reinterpret_cast<float4*>(stage);                                   // per-node records
+    uint16_t* s_v = reinterpret_cast<uint16_t*>(stage + tree_kq_bytes<DK>(p.N));        // [N][32]
+    float* s_ab = reinterpret_cast<float*>(s_v + (size_t)p.N * kRowsPerPass);            // [N][alpha, beta]
     const int lane8 = threadIdx.x & 7;
     const int rg = threadIdx.x >> 3;
     const int h = blockIdx.y;
     const int g = h / p.group;
-    const int row = blockIdx.x * kRowsPerPass + rg;
-    const float* S = p.state + (size_t)h * p.dv * DK + (size_t)row * DK;
+    const int row0 = blockIdx.x * kRowsPerPass;
+    const int row = row0 + rg;
+    // node n's record in s_kq: [V float4 of k, V float4 of q][8 lanes], then k.q
+    constexpr int KQ_REC = 8 * 2 * V + 1;  // float4 units
 
+    {
+        for (int idx = threadIdx.x; idx < p.N * (kRowsPerPass / 8); idx += kThreads) {
+            const int n = idx / (kRowsPerPass / 8), c = idx % (kRowsPerPass / 8);
+            const uint16_t* src = p.qkv + (size_t)n * p.C + (size_t)2 * p.Hk * DK + (size_t)h * p.dv + row0 + c * 8;
+            *reinterpret_cast<uint4*>(s_v + (size_t)n * kRowsPerPass + c * 8) =
+                __ldg(reinterpret_cast<const uint4*>(src));
+        }
+        for (int n = threadIdx.x; n < p.N; n += kThreads) {
+            s_ab[2 * n] = p.alpha[(size_t)n * p.Hv + h];
+            s_ab[2 * n + 1] = p.beta[(size_t)n * p.Hv + h];
+        }
+    }
+    const float* S = p.state + (size_t)h * p.dv * DK + (size_t)row * DK;
     float4 s[V];
 #pragma unroll
     for (int m = 0; m < V; ++m) s[m] = __ldg(reinterpret_cast<const float4*>(S + 32 * m + 4 * lane8));
+    __syncthreads();
 
     const bool normalize = p.normalize != 0;
     const bool out_bf16 = p.out_bf16 != 0;
+    // The key-head vectors do not depend on the state: row group n computes
+    // node n's with the same token_kq every decode row group runs (so the bits
+    // match decode), and the walk reads them back.
+    // token_kq reduces with full-warp shuffles, so the loop is warp-uniform:
+    // all four row groups of a warp iterate together (on a clamped node when
+    // they run past N) and only the groups with a real node write.
+    for (int n0 = rg & ~3; n0 < p.N; n0 += kRowsPerPass) {
+        const int n = n0 + (rg & 3);
+        const bool real = n < p.N;
+        TokenKQ<V> t;
+        const uint16_t* qkv_row = p.qkv + (size_t)(real ? n : p.N - 1) * p.C;
+        token_kq<V>(qkv_row + (size_t)g * DK, qkv_row + (size_t)p.Hk * DK + (size_t)g * DK, lane8, p.q_scale,
+                    normalize, t);
+        if (real) {
+            float4* rec = s_kq + (size_t)n * KQ_REC + lane8;
+#pragma unroll
+            for (int m = 0; m < V; ++m) {
+                rec[8 * m] = make_float4(t.k[m][0], t.k[m][1], t.k[m][2], t.k[m][3]);
+                rec[8 * (V + m)] = make_float4(t.q[m][0], t.q[m][1], t.q[m][2], t.q[m][3]);
+            }
+            if (lane8 == 0) s_kq[(size_t)n * KQ_REC + 8 * 2 * V] = make_float4(t.kq, 0.f, 0.f, 0.f);
+        }
+    }
+    __syncthreads();
+    auto fetch = [&](int n, TokenKQ<V>& t) {
+        const float4* rec = s_kq + (size_t)n * KQ_REC + lane8;
+#pragma unroll
+        for (int m = 0; m < V; ++m) {
+            const float4 a = rec[8 * m], b = rec[8 * (V + m)];
+            t.k[m][0] = a.x; t.k[m][1] = a.y; t.k[m][2] = a.z; t.k[m][3] = a.w;
+            t.q[m][0] = b.x; t.q[m][1] = b.y; t.q[m][2] = b.z; t.q[m][3] = b.w;
+        }
+        t.kq = s_kq[(size_t)n * KQ_REC + 8 * 2 * V].x;
+    };
+    TokenKQ<V> cur, nxt;
+    fetch(p.steps[0].node, cur);
     for (int step = 0; step < p.N; ++step) {
         const TreeStep st = p.steps[step];
         if (st.restore >= 0) {
@@ -101,20 +173,17 @@ gdn_tree_kernel(const __grid_constant__ TreeParams p) {
             for (int m = 0; m < V; ++m) s[m] = slots[((st.restore * kRowsPerPass + rg) * V + m) * 8 + lane8];
         }
         const int node = st.node;
-        const uint16_t* qkv_row = p.qkv + (size_t)node * p.C;
-        TokenKQ<V> kq;
-        token_kq<V>(qkv_row + g * DK, qkv_row + (size_t)p.Hk * DK + g * DK, lane8, p.q_scale,
-                    normalize, kq);
-        const float alpha = p.alpha[(size_t)node * p.Hv + h];
-        const float beta = p.beta[(size_t)node * p.Hv + h];
-        const float v_i =
-            __uint_as_float((uint32_t)qkv_row[(size_t)2 * p.Hk * DK + (size_t)h * p.dv + row] << 16);
-        const float o = row_step<V>(s, kq, v_i, alpha, beta);
+        if (step + 1 < p.N) fetch(p.steps[step + 1].node, nxt);
+        const float alpha = s_ab[2 * node];
+        const float beta = s_ab[2 * node + 1];
+        const float v_i = __uint_as_float((uint32_t)s_v[(size_t)node * kRowsPerPass + rg] << 16);
+        const float o = row_step<V>(s, cur, v_i, alpha, beta);
         if (lane8 == 0) store_out(p.out, ((size_t)node * p.Hv + h) * p.dv + row, o, out_bf16);
         if (st.save >= 0) {
 #pragma unroll
             for (int m = 0; m < V; ++m) slots[((st.save * kRowsPerPass + rg) * V + m) * 8 + lane8] = s[m];
         }
+        cur = nxt;
     }
 }
 
@@ -156,12 +225,13 @@ cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int g
 
 template <int DK>
 static cudaError_t launch_tree_t(const TreeParams& p, cudaStream_t s) {
-    const size_t smem = (size_t)p.n_slots * kRowsPerPass * DK * sizeof(float);
+    const size_t smem = (size_t)p.n_slots * kRowsPerPass * DK * sizeof(float) + tree_stage_bytes<DK>(p.N);
     static bool configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured[dev]) {
-        const int max_smem = GDN_MAX_TREE_SLOTS * kRowsPerPass * DK * (int)sizeof(float);
+        const int max_smem = GDN_MAX_TREE_SLOTS * kRowsPerPass * DK * (int)sizeof(float) +
+                             (int)tree_stage_bytes<DK>(GDN_MAX_TREE_NODES);
         cudaError_t e = cudaFuncSetAttribute(gdn_tree_kernel<DK>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
         if (e != cudaSuccess) return e;

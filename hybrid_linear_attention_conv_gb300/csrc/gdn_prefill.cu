@@ -62,8 +62,10 @@ constexpr uint32_t OFF_X_LO = 180224;
 constexpr uint32_t OFF_U_HI = 196608;   // U^T   [128 i][64 s]    A of U^T P^T
 constexpr uint32_t OFF_U_LO = 212992;
 constexpr uint32_t OFF_L = 196608;      // L fp32 [64][64] (aliases U^T, used before it)
-constexpr uint32_t OFF_SCAL = 229376;   // alpha, beta, log gamma, r_k, r_q: 5 x 64 fp32
-constexpr uint32_t OFF_MISC = OFF_SCAL + 5 * 64 * 4;  // mbarrier, TMEM base, abort flag
+constexpr uint32_t OFF_TF = 212992;     // T fp32 [64][64] while it is solved (aliases U^T lo)
+constexpr uint32_t OFF_R = 131072;      // block-solve scratch fp32 [16][48] (aliases T hi)
+constexpr uint32_t OFF_SCAL = 229376;   // per-token scalars: 9 x 64 fp32 (see kernel)
+constexpr uint32_t OFF_MISC = OFF_SCAL + 9 * 64 * 4;  // mbarrier, TMEM base, abort flag
 constexpr uint32_t kPrefillSmem = OFF_MISC + 32;
 
 // TMEM columns (fp32 accumulators, 128 lanes each).
@@ -91,6 +93,51 @@ struct PrefillParams {
 
 __device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
+// One block row BI of the blocked triangular inverse (T zero above its block
+// diagonal, blocks left of BI already final): with W = 16 BI,
+//   R = L[W:W+16][0:W] T[0:W][0:W],   T[W:W+16][0:W] = -T[W:W+16][W:W+16] R.
+// Trip counts are compile-time, so the sums unroll with independent chains.
+template <int BI>
+__device__ __forceinline__ void block_row_solve(const float* sL, float* Tf, float* R, int tid) {
+    constexpr int W = 16 * BI;
+    constexpr int PER = 16 * W / kPrefillThreads;  // elements per thread
+    float acc[PER];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) acc[k] = 0.f;
+#pragma unroll
+    for (int q = 0; q < W; ++q) {
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int e = tid + k * kPrefillThreads;
+            const int r = e / W, cj = e % W;
+            acc[k] = __fmaf_rn(sL[(W + r) * kChunk + q], Tf[q * kChunk + cj], acc[k]);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        const int e = tid + k * kPrefillThreads;
+        R[(e / W) * 48 + e % W] = acc[k];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < PER; ++k) acc[k] = 0.f;
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int e = tid + k * kPrefillThreads;
+            const int r = e / W, cj = e % W;
+            acc[k] = __fmaf_rn(Tf[(W + r) * kChunk + W + m], R[m * 48 + cj], acc[k]);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        const int e = tid + k * kPrefillThreads;
+        Tf[(W + e / W) * kChunk + e % W] = -acc[k];
+    }
+    __syncthreads();
+}
+
 __global__ void __launch_bounds__(kPrefillThreads, 1)
 gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
     extern __shared__ __align__(1024) uint8_t sm[];
@@ -100,9 +147,13 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
     const int g = h / p.group;
     float* s_alpha = reinterpret_cast<float*>(sm + OFF_SCAL);
     float* s_beta = s_alpha + 64;
-    float* s_lg = s_alpha + 128;
-    float* s_rk = s_alpha + 192;
-    float* s_rq = s_alpha + 256;
+    float* s_lg = s_alpha + 128;   // log2 gamma_t (prefix sums of log2 alpha)
+    float* s_rk = s_alpha + 192;   // r_k,t
+    float* s_rq = s_alpha + 256;   // q_scale r_q,t
+    float* s_gk = s_alpha + 320;   // gamma_t r_k,t
+    float* s_gq = s_alpha + 384;   // gamma_t q_scale r_q,t
+    float* s_ck = s_alpha + 448;   // (gamma_C / gamma_t) r_k,t
+    float* s_brk = s_alpha + 512;  // beta_t r_k,t
     uint64_t* bar_ptr = reinterpret_cast<uint64_t*>(sm + OFF_MISC);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_MISC + 8);
     int* abort_flag = reinterpret_cast<int*>(sm + OFF_MISC + 12);
@@ -159,42 +210,26 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
 
         // ---- A: stage the chunk's inputs ---------------------------------
         {
-            // thread t' loads row t' of [K;Q] (t' < 64: k_t, else q_t) and its norm
-            const int t = tid & 63;
-            const bool is_q = tid >= 64;
-            const bool valid = t < n;
-            const uint16_t* src = p.qkv + (size_t)(t0 + t) * C + (is_q ? 0 : (size_t)p.Hk * kD) + (size_t)g * kD;
-            float ss = 0.f;
+            // [K;Q] rows into the K-major core layout and v rows row-major,
+            // all as asynchronous 16-byte copies (zero-filled past the end)
 #pragma unroll 4
-            for (int kb = 0; kb < 16; ++kb) {
-                uint4 w = make_uint4(0, 0, 0, 0);
-                if (valid) w = __ldg(reinterpret_cast<const uint4*>(src + kb * 8));
-                const uint16_t* e = reinterpret_cast<const uint16_t*>(&w);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float x = bf16_to_f(e[j]);
-                    ss = __fmaf_rn(x, x, ss);
-                }
-                *reinterpret_cast<uint4*>(sm + OFF_KQ + core_off(tid, kb * 8, kD)) = w;
-                if (!is_q) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        *reinterpret_cast<uint16_t*>(sm + OFF_KT + core_off(kb * 8 + j, t, kChunk)) = e[j];
-                }
+            for (int idx = tid; idx < 2 * kChunk * 16; idx += kPrefillThreads) {
+                const int r = idx >> 4, kb = idx & 15;
+                const int t = r & 63;
+                const bool ok = t < n;
+                const uint16_t* src = p.qkv + (size_t)(t0 + (ok ? t : 0)) * C +
+                                      (r >= 64 ? 0 : (size_t)p.Hk * kD) + (size_t)g * kD + kb * 8;
+                cp_async16(sbase + OFF_KQ + core_off(r, kb * 8, kD), src, ok);
             }
-            const float r = p.normalize ? rsqrtf(__fadd_rn(ss, 1e-6f)) : 1.0f;
-            if (is_q) s_rq[t] = __fmul_rn(r, p.q_scale);
-            else s_rk[t] = r;
-            // v rows of this value head (plain row-major)
-#pragma unroll 2
-            for (int e = tid; e < kChunk * 16; e += kPrefillThreads) {
-                const int tt = e >> 4, kb = e & 15;
-                uint4 w = make_uint4(0, 0, 0, 0);
-                if (tt < n)
-                    w = __ldg(reinterpret_cast<const uint4*>(p.qkv + (size_t)(t0 + tt) * C + (size_t)2 * p.Hk * kD +
-                                                             (size_t)h * kD + kb * 8));
-                *reinterpret_cast<uint4*>(sm + OFF_V + tt * 256 + kb * 16) = w;
+#pragma unroll 4
+            for (int idx = tid; idx < kChunk * 16; idx += kPrefillThreads) {
+                const int t = idx >> 4, kb = idx & 15;
+                const bool ok = t < n;
+                const uint16_t* src =
+                    p.qkv + (size_t)(t0 + (ok ? t : 0)) * C + (size_t)2 * p.Hk * kD + (size_t)h * kD + kb * 8;
+                cp_async16(sbase + OFF_V + t * 256 + kb * 16, src, ok);
             }
+            cp_async_commit_wait_all();
             if (tid < kChunk) {
                 const bool ok = tid < n;
                 s_alpha[tid] = ok ? p.alpha[(size_t)(t0 + tid) * p.Hv + h] : 1.0f;
@@ -202,11 +237,38 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
             }
         }
         __syncthreads();
+        {
+            // norm of row tid of [K;Q]
+            float ss = 0.f;
+#pragma unroll 4
+            for (int kb = 0; kb < 16; ++kb) {
+                const uint4 w = *reinterpret_cast<const uint4*>(sm + OFF_KQ + core_off(tid, kb * 8, kD));
+                const uint16_t* e = reinterpret_cast<const uint16_t*>(&w);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float x = bf16_to_f(e[j]);
+                    ss = __fmaf_rn(x, x, ss);
+                }
+            }
+            const float r = p.normalize ? rsqrtf(__fadd_rn(ss, 1e-6f)) : 1.0f;
+            if (tid >= 64) s_rq[tid - 64] = __fmul_rn(r, p.q_scale);
+            else s_rk[tid] = r;
+            // K^T: each warp transposes 32 of the 128 8x8 core matrices of K
+            const int lane = tid & 31;
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int q = warp * 32 + it * 4 + (lane >> 3);  // core matrix (tb, jb) = (q / 16, q % 16)
+                const int tb = q >> 4, jb = q & 15;
+                const uint32_t src = sbase + OFF_KQ + tb * (kD * 16) + jb * 128 + (lane & 7) * 16;
+                const uint32_t dst = sbase + OFF_KT + jb * (kChunk * 16) + tb * 128 + (lane & 7) * 16;
+                transpose_8x8x4(src, dst);
+            }
+        }
         if (warp == 0) {
-            // log gamma: inclusive prefix sum of log(alpha) (two tokens per lane)
+            // log2 gamma: inclusive prefix sum of log2(alpha) (two tokens per lane)
             const int l = tid;
-            const float a0 = logf(fmaxf(s_alpha[2 * l], 1e-30f));
-            const float a1 = logf(fmaxf(s_alpha[2 * l + 1], 1e-30f));
+            const float a0 = log2f(fmaxf(s_alpha[2 * l], 1e-30f));
+            const float a1 = log2f(fmaxf(s_alpha[2 * l + 1], 1e-30f));
             const float pair = __fadd_rn(a0, a1);
             float incl = pair;
 #pragma unroll
@@ -217,6 +279,15 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
             const float excl = __fsub_rn(incl, pair);
             s_lg[2 * l] = __fadd_rn(excl, a0);
             s_lg[2 * l + 1] = incl;
+        }
+        __syncthreads();
+        if (tid < kChunk) {
+            const float lg = s_lg[tid];
+            const float gam = exp2f(lg);
+            s_gk[tid] = __fmul_rn(gam, s_rk[tid]);
+            s_gq[tid] = __fmul_rn(gam, s_rq[tid]);
+            s_ck[tid] = __fmul_rn(exp2f(__fsub_rn(s_lg[kChunk - 1], lg)), s_rk[tid]);
+            s_brk[tid] = __fmul_rn(s_beta[tid], s_rk[tid]);
         }
         fence_async_smem();
         fence_before_sync();
@@ -245,37 +316,28 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
         {
             const int t = tid & 63;
             const float lg_t = s_lg[t];
+            const float f = tid < 64 ? s_brk[t] : s_rq[t];
 #pragma unroll 1
             for (int s0 = 0; s0 < kChunk; s0 += 16) {
                 float a[16];
                 tmem_ld16(trow + COL_G + s0, a);
-                if (tid < 64) {
-                    // L row t (strictly lower), fp32 for the solve
-                    const float f = __fmul_rn(s_beta[t], s_rk[t]);
-                    float lrow[16];
+                float row[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int s = s0 + j;
-                        const float ratio = expf(__fsub_rn(lg_t, s_lg[s]));
-                        lrow[j] = (s < t) ? __fmul_rn(__fmul_rn(f, __fmul_rn(s_rk[s], ratio)), a[j]) : 0.f;
-                    }
+                for (int j = 0; j < 16; ++j) {
+                    const int sj = s0 + j;
+                    const float ratio = exp2f(__fsub_rn(lg_t, s_lg[sj]));  // gamma_t / gamma_s
+                    const float v = __fmul_rn(__fmul_rn(f, __fmul_rn(s_rk[sj], ratio)), a[j]);
+                    // L: strictly lower (rows of K); P: lower incl. diagonal (rows of Q)
+                    row[j] = (tid < 64 ? sj < t : sj <= t) ? v : 0.f;
+                }
+                if (tid < 64) {
                     float4* dst = reinterpret_cast<float4*>(sm + OFF_L + (t * kChunk + s0) * 4);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        dst[q] = make_float4(lrow[4 * q], lrow[4 * q + 1], lrow[4 * q + 2], lrow[4 * q + 3]);
+                    for (int q = 0; q < 4; ++q) dst[q] = make_float4(row[4 * q], row[4 * q + 1], row[4 * q + 2], row[4 * q + 3]);
                 } else {
-                    // P row t (lower incl. diagonal), split for the B operand
-                    const float f = s_rq[t];
-                    float prow[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int s = s0 + j;
-                        const float ratio = expf(__fsub_rn(lg_t, s_lg[s]));
-                        prow[j] = (s <= t) ? __fmul_rn(__fmul_rn(f, __fmul_rn(s_rk[s], ratio)), a[j]) : 0.f;
-                    }
-                    store_split8(sm + OFF_P_HI + core_off(t, s0, kChunk), sm + OFF_P_LO + core_off(t, s0, kChunk), prow);
+                    store_split8(sm + OFF_P_HI + core_off(t, s0, kChunk), sm + OFF_P_LO + core_off(t, s0, kChunk), row);
                     store_split8(sm + OFF_P_HI + core_off(t, s0 + 8, kChunk),
-                                 sm + OFF_P_LO + core_off(t, s0 + 8, kChunk), prow + 8);
+                                 sm + OFF_P_LO + core_off(t, s0 + 8, kChunk), row + 8);
                 }
             }
             // thread i: X^T[i][s] = beta_s (v_s[i] - gamma_s r_k,s (S k_s)[i])
@@ -287,9 +349,8 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
                 tmem_ld16(trow + COL_KQ + s0, ks);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const int s = s0 + j;
-                    const float gk = __fmul_rn(expf(s_lg[s]), s_rk[s]);
-                    x[j] = __fmul_rn(s_beta[s], __fmaf_rn(-gk, ks[j], bf16_to_f(vcol[s * kD])));
+                    const int sj = s0 + j;
+                    x[j] = __fmul_rn(s_beta[sj], __fmaf_rn(-s_gk[sj], ks[j], bf16_to_f(vcol[sj * kD])));
                 }
                 store_split8(sm + OFF_X_HI + core_off(i, s0, kChunk), sm + OFF_X_LO + core_off(i, s0, kChunk), x);
                 store_split8(sm + OFF_X_HI + core_off(i, s0 + 8, kChunk), sm + OFF_X_LO + core_off(i, s0 + 8, kChunk),
@@ -301,40 +362,55 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
                 float qs[16];
                 tmem_ld16(trow + COL_O + s0, qs);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) qs[j] = __fmul_rn(qs[j], __fmul_rn(expf(s_lg[s0 + j]), s_rq[s0 + j]));
+                for (int j = 0; j < 16; ++j) qs[j] = __fmul_rn(qs[j], s_gq[s0 + j]);
                 tmem_st16(trow + COL_O + s0, qs);
             }
             tmem_wait_st();
         }
         __syncthreads();
 
-        // ---- D: T = (I + L)^-1, column c per thread (threads 0..63) --------
-        if (tid < kChunk) {
-            const int cc = tid;
-            const float4* L4 = reinterpret_cast<const float4*>(sm + OFF_L);
-            float col[kChunk];
+        // ---- D: T = (I + L)^-1, blocked by 16 --------------------------
+        {
+            const float* sL = reinterpret_cast<const float*>(sm + OFF_L);
+            float* Tf = reinterpret_cast<float*>(sm + OFF_TF);
+            float* R = reinterpret_cast<float*>(sm + OFF_R);
+            const int lane = tid & 31;
+            // zero T, so every sum below can run over whole 16-blocks
+            {
+                float4* z = reinterpret_cast<float4*>(Tf);
 #pragma unroll
-            for (int t = 0; t < kChunk; ++t) col[t] = (t == cc) ? 1.f : 0.f;
-#pragma unroll
-            for (int t = 1; t < kChunk; ++t) {
-                float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-#pragma unroll
-                for (int s4 = 0; s4 < (t + 3) / 4; ++s4) {
-                    const float4 l = L4[t * 16 + s4];
-                    acc0 = __fmaf_rn(l.x, col[4 * s4], acc0);
-                    if (4 * s4 + 1 < t) acc1 = __fmaf_rn(l.y, col[4 * s4 + 1], acc1);
-                    if (4 * s4 + 2 < t) acc2 = __fmaf_rn(l.z, col[4 * s4 + 2], acc2);
-                    if (4 * s4 + 3 < t) acc3 = __fmaf_rn(l.w, col[4 * s4 + 3], acc3);
-                }
-                const float v = -__fadd_rn(__fadd_rn(acc0, acc1), __fadd_rn(acc2, acc3));
-                if (t > cc) col[t] = v;
+                for (int q = 0; q < kChunk * kChunk / 4 / kPrefillThreads; ++q)
+                    z[tid + q * kPrefillThreads] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
+            __syncthreads();
+            // diagonal blocks: warp w inverts block w column by column (lane = column)
+            if (lane < 16) {
+                const int b = warp * 16, cc = lane;
+                float x[16];
 #pragma unroll
-            for (int t = 0; t < kChunk; ++t) {
-                __nv_bfloat16 hi, lo;
-                split_bf16(col[t], hi, lo);
-                *reinterpret_cast<__nv_bfloat16*>(sm + OFF_T_HI + core_off(t, cc, kChunk)) = hi;
-                *reinterpret_cast<__nv_bfloat16*>(sm + OFF_T_LO + core_off(t, cc, kChunk)) = lo;
+                for (int r = 0; r < 16; ++r) x[r] = (r == cc) ? 1.f : 0.f;
+#pragma unroll
+                for (int r = 1; r < 16; ++r) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int q = 0; q < r; ++q) acc = __fmaf_rn(sL[(b + r) * kChunk + b + q], x[q], acc);
+                    if (r > cc) x[r] = -acc;
+                }
+#pragma unroll
+                for (int r = 0; r < 16; ++r) Tf[(b + r) * kChunk + b + cc] = x[r];
+            }
+            __syncthreads();
+            // block rows 1..3: T[I][:I] = -T_II (L[I][:I] T[:I][:I])
+            block_row_solve<1>(sL, Tf, R, tid);
+            block_row_solve<2>(sL, Tf, R, tid);
+            block_row_solve<3>(sL, Tf, R, tid);
+            // T -> bf16 hi/lo B-operand tiles (rows t, K = s)
+            for (int e = tid; e < kChunk * 8; e += kPrefillThreads) {
+                const int t = e >> 3, s0 = (e & 7) * 8;
+                const float4 a = *reinterpret_cast<const float4*>(Tf + t * kChunk + s0);
+                const float4 b = *reinterpret_cast<const float4*>(Tf + t * kChunk + s0 + 4);
+                const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                store_split8(sm + OFF_T_HI + core_off(t, s0, kChunk), sm + OFF_T_LO + core_off(t, s0, kChunk), v);
             }
         }
         fence_async_smem();
@@ -366,8 +442,7 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
                 float u[16], uh[16];
                 tmem_ld16(trow + COL_U + s0, u);
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    uh[j] = __fmul_rn(u[j], __fmul_rn(expf(__fsub_rn(lg_c, s_lg[s0 + j])), s_rk[s0 + j]));
+                for (int j = 0; j < 16; ++j) uh[j] = __fmul_rn(u[j], s_ck[s0 + j]);
                 store_split8(sm + OFF_X_HI + core_off(i, s0, kChunk), sm + OFF_X_LO + core_off(i, s0, kChunk), uh);
                 store_split8(sm + OFF_X_HI + core_off(i, s0 + 8, kChunk), sm + OFF_X_LO + core_off(i, s0 + 8, kChunk),
                              uh + 8);
@@ -375,7 +450,7 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
                 store_split8(sm + OFF_U_HI + core_off(i, s0 + 8, kChunk), sm + OFF_U_LO + core_off(i, s0 + 8, kChunk),
                              u + 8);
             }
-            const float gamma_c = expf(lg_c);
+            const float gamma_c = exp2f(lg_c);
 #pragma unroll 1
             for (int c0 = 0; c0 < kD; c0 += 16) {
                 float sv[16];

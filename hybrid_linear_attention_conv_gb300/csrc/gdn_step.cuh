@@ -10,6 +10,9 @@
 // floating-point operations use explicit round-to-nearest intrinsics so that no
 // compiler contraction can differ between call sites.
 //
+// The row arithmetic runs on the packed fp32x2 pipe (fma.rn.f32x2 etc.), which
+// rounds every element exactly as the scalar instruction would.
+//
 // Layout: a row of the state (dk fp32 values) is owned by a group of 8 lanes;
 // lane l of the group holds float4 number m at columns 32*m + 4*l, for
 // m = 0 .. dk/32 - 1.  A warp therefore covers 4 rows, and each load/store
@@ -69,22 +72,25 @@ __device__ __forceinline__ float lane_dot(const float (&a)[V][4], const float (&
     return group_sum8(part[0]);
 }
 
+// Dot product of this lane's slice of a state row with a vector slice, on the
+// packed fp32x2 pipe: two float2 accumulators (even and odd float4s), each a
+// short fma2 chain, then summed in a fixed order.
 template <int V>
 __device__ __forceinline__ float lane_dot4(const float4 (&s)[V], const float (&b)[V][4]) {
-    float part[V];
+    float2 acc[2];
 #pragma unroll
-    for (int m = 0; m < V; ++m) {
-        float acc = __fmul_rn(s[m].x, b[m][0]);
-        acc = __fmaf_rn(s[m].y, b[m][1], acc);
-        acc = __fmaf_rn(s[m].z, b[m][2], acc);
-        acc = __fmaf_rn(s[m].w, b[m][3], acc);
-        part[m] = acc;
+    for (int m = 0; m < V && m < 2; ++m) {
+        acc[m] = __fmul2_rn(make_float2(s[m].x, s[m].y), make_float2(b[m][0], b[m][1]));
+        acc[m] = __ffma2_rn(make_float2(s[m].z, s[m].w), make_float2(b[m][2], b[m][3]), acc[m]);
     }
 #pragma unroll
-    for (int w = 1; w < V; w *= 2)
-#pragma unroll
-        for (int m = 0; m + w < V; m += 2 * w) part[m] = __fadd_rn(part[m], part[m + w]);
-    return part[0];
+    for (int m = 2; m < V; ++m) {
+        acc[m & 1] = __ffma2_rn(make_float2(s[m].x, s[m].y), make_float2(b[m][0], b[m][1]), acc[m & 1]);
+        acc[m & 1] = __ffma2_rn(make_float2(s[m].z, s[m].w), make_float2(b[m][2], b[m][3]), acc[m & 1]);
+    }
+    float2 t = acc[0];
+    if (V > 1) t = __fadd2_rn(acc[0], acc[1]);
+    return __fadd_rn(t.x, t.y);
 }
 
 // q^ = scale * q / sqrt(|q|^2 + eps) (or scale * q without normalisation).
@@ -134,12 +140,12 @@ __device__ __forceinline__ float row_step(float4 (&s)[V], const TokenKQ<V>& t, f
     const float c = group_sum8(c_part);
     const float u = __fmul_rn(beta, __fmaf_rn(-alpha, a, v_i));
     const float o = __fmaf_rn(alpha, c, __fmul_rn(u, t.kq));
+    const float2 uu = make_float2(u, u), aa = make_float2(alpha, alpha);
 #pragma unroll
     for (int m = 0; m < V; ++m) {
-        s[m].x = __fmaf_rn(u, t.k[m][0], __fmul_rn(alpha, s[m].x));
-        s[m].y = __fmaf_rn(u, t.k[m][1], __fmul_rn(alpha, s[m].y));
-        s[m].z = __fmaf_rn(u, t.k[m][2], __fmul_rn(alpha, s[m].z));
-        s[m].w = __fmaf_rn(u, t.k[m][3], __fmul_rn(alpha, s[m].w));
+        const float2 lo = __ffma2_rn(uu, make_float2(t.k[m][0], t.k[m][1]), __fmul2_rn(aa, make_float2(s[m].x, s[m].y)));
+        const float2 hi = __ffma2_rn(uu, make_float2(t.k[m][2], t.k[m][3]), __fmul2_rn(aa, make_float2(s[m].z, s[m].w)));
+        s[m] = make_float4(lo.x, lo.y, hi.x, hi.y);
     }
     return o;
 }

@@ -152,5 +152,27 @@ __device__ __forceinline__ void store_split8(uint8_t* hi_dst, uint8_t* lo_dst, c
         make_uint4(pack_bf16(l[0], l[1]), pack_bf16(l[2], l[3]), pack_bf16(l[4], l[5]), pack_bf16(l[6], l[7]));
 }
 
+// Asynchronous 16-byte global -> shared copy; zero-fills when !valid.
+__device__ __forceinline__ void cp_async16(uint32_t dst_saddr, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_saddr), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// Transpose four 8x8 b16 matrices: lane l gives row (l & 7) of matrix (l >> 3)
+// of the source (src) and of the destination (dst).
+__device__ __forceinline__ void transpose_8x8x4(uint32_t src, uint32_t dst) {
+    uint32_t r0, r1, r2, r3;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(src));
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(r0), "r"(r1),
+                 "r"(r2), "r"(r3)
+                 : "memory");
+}
+
 }  // namespace tc
 }  // namespace gdn

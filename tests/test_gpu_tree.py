@@ -73,6 +73,7 @@ def test_tree_verify_outputs_equal_decode_bitwise():
     np.array([-1], np.int32),                                  # a single node
     np.arange(-1, 63, dtype=np.int32),                         # a 64-long chain (no branch states)
     np.array([-1] + [0] * 31, np.int32),                       # a star: 31 children of the root
+    np.array([-1, 0, 0, 1, 1, 2, 3, 3, 4, 6, 6, 9, 10], np.int32),  # 13 nodes (not a multiple of 4)
 ])
 def test_tree_verify_degenerate_shapes(parents):
     shape = gen.Shape(1, 2, 4, 64, 64)
