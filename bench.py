@@ -207,6 +207,16 @@ def conv_bytes_per_launch(B: int, T: int = 1) -> int:
     return B * T * C_QKV * 2 + C_QKV * 4 * 2 + 2 * B * 4 * C_QKV * 2 + B * T * C_QKV * 2
 
 
+def fused_bytes_per_launch(B: int, T: int = 1) -> int:
+    """HBM bytes of one fused conv + decode launch: the state read and written
+    once, x read (bf16), the last three tail inputs read and the four-input
+    tail written (bf16), the taps, alpha/beta (fp32) and the outputs (fp32)."""
+    state = B * HV * DV * DK * 4 * 2
+    conv = B * T * C_QKV * 2 + B * 3 * C_QKV * 2 + B * 4 * C_QKV * 2 + C_QKV * 4 * 2
+    gates_out = B * T * HV * 4 * 2 + B * T * HV * DV * 4
+    return state + conv + gates_out
+
+
 def step_flops_per_head_token() -> int:
     """fp32 flops of one state update of one head: s.k and s.q (2 x 2d per
     row), alpha s + u k (2d per row), the row scalars u and o (5 per row)."""
@@ -344,7 +354,6 @@ class Batched(Workload):
         self.n_sets = min(4, steps)
         self.x = self.randn((self.n_sets, L, B, 1, C_QKV), 1.0, bf)
         self.alpha, self.beta = self.gates((self.n_sets, L, B, 1, HV))
-        self.y = torch.empty((B, 1, C_QKV), dtype=bf, device=device)
         self.out = torch.empty((L, B, 1, HV, DV), dtype=torch.float32, device=device)
         self.shape = gdn.gdn_shape(B, HK, HV, DK, DV)
         P = ctypes.c_void_p
@@ -352,32 +361,28 @@ class Batched(Workload):
         for s in range(self.n_sets):
             per = []
             for l in range(L):
-                conv = (B, 1, C_QKV, None, P(self.x[s, l].data_ptr()), P(self.w[l].data_ptr()),
-                        P(self.tail[l].data_ptr()), P(self.y.data_ptr()), 0, self.sp)
-                dec = (ctypes.byref(self.shape), 1, P(self.y.data_ptr()), P(self.alpha[s, l].data_ptr()),
-                       P(self.beta[s, l].data_ptr()), P(self.state[l].data_ptr()),
-                       P(self.out[l].data_ptr()), 1.0, gdn.GDN_NORMALIZE_QK, self.sp)
-                per.append((conv, dec))
+                tl = P(self.tail[l].data_ptr())
+                per.append((ctypes.byref(self.shape), 1, P(self.x[s, l].data_ptr()), P(self.w[l].data_ptr()), tl,
+                            tl, P(self.alpha[s, l].data_ptr()), P(self.beta[s, l].data_ptr()),
+                            P(self.state[l].data_ptr()), P(self.out[l].data_ptr()), 1.0, gdn.GDN_NORMALIZE_QK,
+                            self.sp))
             self.args.append(per)
-        self.launches_per_step = 2 * L
+        self.launches_per_step = L
         self.units_per_step = L * B * HV
-        self.dominant = "gdn_decode_kernel"
+        self.dominant = "gdn_conv_decode_kernel"
         self.dominant_sources = DECODE_SOURCES
         self.bound = "hbm"
-        self.dominant_work = decode_bytes_per_launch(B)
-        self.step_bytes = L * (decode_bytes_per_launch(B) + conv_bytes_per_launch(B))
+        self.dominant_work = fused_bytes_per_launch(B)
+        self.step_bytes = L * fused_bytes_per_launch(B)
 
     def step(self, i: int, rec: Recorder | None = None):
         lib, gdn = self.lib, self.gdn
         if rec:
             rec.begin(i)
-        for conv, dec in self.args[i % self.n_sets]:
-            _call(lib.gdn_conv_step, conv, gdn)
+        for args in self.args[i % self.n_sets]:
+            _call(lib.gdn_conv_decode_step, args, gdn)
             if rec:
-                rec.mark("gdn_conv_kernel")
-            _call(lib.gdn_decode_step, dec, gdn)
-            if rec:
-                rec.mark("gdn_decode_kernel")
+                rec.mark("gdn_conv_decode_kernel")
 
     def e2e_setup(self):
         torch = self.torch
@@ -392,9 +397,8 @@ class Batched(Workload):
         self.e2e_copy(self.x[0], self.h_x)
         self.e2e_copy(self.alpha[0], self.h_a)
         self.e2e_copy(self.beta[0], self.h_b)
-        for conv, dec in self.args[0]:
-            _call(self.lib.gdn_conv_step, conv, self.gdn)
-            _call(self.lib.gdn_decode_step, dec, self.gdn)
+        for args in self.args[0]:
+            _call(self.lib.gdn_conv_decode_step, args, self.gdn)
         self.e2e_copy(self.h_out, self.out)
 
     def config(self=None) -> dict:
@@ -403,7 +407,7 @@ class Batched(Workload):
         sb = L * B * HV * DV * DK * 4
         return {"workload": f"batched decode over {L} GDN layers: batch {B} sequences, 27B head "
                             "shape (16 key / 48 value heads x 128), independent fp32 states, one token "
-                            "per sequence per layer (conv + delta step)",
+                            "per sequence per layer (fused conv + delta step, one launch per layer)",
                 "layers": L, "batch": B, "Hk": HK, "Hv": HV, "dk": DK, "dv": DV, "state_bytes": sb,
                 "l2": f"inputs larger than L2: {sb / 1e9:.2f} GB of state streamed per step",
                 "launch": "eager, CUDA events after every kernel"}
@@ -422,39 +426,35 @@ class Decode1(Workload):
         self.n = steps
         self.state = self.randn((1, HV, DV, DK), 0.1)
         self.w = self.randn((C_QKV, 4), 0.5, bf)
-        self.tail = self.randn((1, 4, C_QKV), 1.0, bf)
+        self.tails = [self.randn((1, 4, C_QKV), 1.0, bf), torch.empty((1, 4, C_QKV), dtype=bf, device=device)]
         self.x = self.randn((self.n, 1, 1, C_QKV), 1.0, bf)
         self.alpha, self.beta = self.gates((self.n, 1, 1, HV))
-        self.y = torch.empty((1, 1, C_QKV), dtype=bf, device=device)
         self.out = torch.empty((self.n, 1, 1, HV, DV), dtype=torch.float32, device=device)
         self.shape = gdn.gdn_shape(1, HK, HV, DK, DV)
-        self.launches_per_step = 2
+        self.launches_per_step = 1
         self.units_per_step = HV
-        self.dominant = "gdn_decode_kernel"
+        self.dominant = "gdn_conv_decode_kernel"
         self.dominant_sources = DECODE_SOURCES
         self.bound = "hbm"
-        self.dominant_work = decode_bytes_per_launch(1)
-        self.step_bytes = decode_bytes_per_launch(1) + conv_bytes_per_launch(1)
+        self.dominant_work = fused_bytes_per_launch(1)
+        self.step_bytes = fused_bytes_per_launch(1)
+        self.k = 0  # ping-pong position of the conv tail
 
     def _args(self, s):
         P = ctypes.c_void_p
-        conv = (1, 1, C_QKV, None, P(self.x[s].data_ptr()), P(self.w.data_ptr()), P(self.tail.data_ptr()),
-                P(self.y.data_ptr()), 0, self.sp)
-        dec = (ctypes.byref(self.shape), 1, P(self.y.data_ptr()), P(self.alpha[s].data_ptr()),
-               P(self.beta[s].data_ptr()), P(self.state.data_ptr()), P(self.out[s].data_ptr()), 1.0,
-               self.gdn.GDN_NORMALIZE_QK, self.sp)
-        return conv, dec
+        tin, tout = self.tails[self.k % 2], self.tails[(self.k + 1) % 2]
+        self.k += 1
+        return (ctypes.byref(self.shape), 1, P(self.x[s].data_ptr()), P(self.w.data_ptr()), P(tin.data_ptr()),
+                P(tout.data_ptr()), P(self.alpha[s].data_ptr()), P(self.beta[s].data_ptr()),
+                P(self.state.data_ptr()), P(self.out[s].data_ptr()), 1.0, self.gdn.GDN_NORMALIZE_QK, self.sp)
 
     def step(self, i: int, rec: Recorder | None = None):
-        conv, dec = self._args(i % self.n)
+        args = self._args(i % self.n)
         if rec:
             rec.begin(i)
-        _call(self.lib.gdn_conv_step, conv, self.gdn)
+        _call(self.lib.gdn_conv_decode_step, args, self.gdn)
         if rec:
-            rec.mark("gdn_conv_kernel")
-        _call(self.lib.gdn_decode_step, dec, self.gdn)
-        if rec:
-            rec.mark("gdn_decode_kernel")
+            rec.mark("gdn_conv_decode_kernel")
 
     def e2e_setup(self):
         self.h_x = self.x[0].cpu().pin_memory()
@@ -468,16 +468,15 @@ class Decode1(Workload):
         self.e2e_copy(self.x[0], self.h_x)
         self.e2e_copy(self.alpha[0], self.h_a)
         self.e2e_copy(self.beta[0], self.h_b)
-        conv, dec = self._args(0)
-        _call(self.lib.gdn_conv_step, conv, self.gdn)
-        _call(self.lib.gdn_decode_step, dec, self.gdn)
+        _call(self.lib.gdn_conv_decode_step, self._args(0), self.gdn)
         self.e2e_copy(self.h_out, self.out[0])
 
     @staticmethod
     def config() -> dict:
         return {"workload": "27B-shape single-token decode, one layer: batch 1, 16 key / 48 value heads "
                             "x 128, fp32 state 3.15 MB, bf16 inputs, 4-tap bf16 conv tail over 10,240 "
-                            "channels (conv + delta step per token)",
+                            "channels (fused conv + delta step per token; conv tail ping-ponged "
+                            "between two buffers)",
                 "layers": 1, "batch": 1, "Hk": HK, "Hv": HV, "dk": DK, "dv": DV,
                 "l2": "L2 flushed (256 MB write) before every step, outside the timed intervals",
                 "launch": "eager, CUDA events around the step's kernels"}

@@ -297,6 +297,65 @@ int gdn_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, cons
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "decode launch");
 }
 
+int gdn_conv_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* x, const gdn_bf16* w,
+                         const gdn_bf16* tail_in, gdn_bf16* tail_out, const float* alpha, const float* beta,
+                         float* state, void* out, float q_scale, uint32_t flags, void* stream) {
+    int rc;
+    if ((rc = check_shape(shape, false)) != GDN_OK) return rc;
+    if ((rc = check_flags(flags)) != GDN_OK) return rc;
+    if (T < 0) return fail(GDN_ERR_INVALID_ARG, "T=%d < 0", T);
+    if (T > kFusedMaxTokens)
+        return fail(GDN_ERR_UNSUPPORTED_SHAPE, "T=%d tokens, the fused step takes at most %d", T, kFusedMaxTokens);
+    const int group = shape->Hv / shape->Hk;
+    const int CC = 2 * shape->dk + group * shape->dv;
+    if ((long)T * CC * 2 > kFusedMaxSmem)
+        return fail(GDN_ERR_UNSUPPORTED_SHAPE, "T=%d x %d channels per key-head group exceed the fused step's "
+                    "%d-byte staging", T, CC, kFusedMaxSmem);
+    if (shape->B == 0 || T == 0) return GDN_OK;  // nothing to do; pointers may be NULL
+    if ((rc = check_ptr(x, "x")) || (rc = check_ptr(w, "w")) || (rc = check_ptr(tail_in, "tail_in")) ||
+        (rc = check_ptr(tail_out, "tail_out")) || (rc = check_ptr(alpha, "alpha")) ||
+        (rc = check_ptr(beta, "beta")) || (rc = check_ptr(state, "state")) || (rc = check_ptr(out, "out", false)))
+        return rc;
+    const int C = packed_channels(shape);
+    const size_t tail_bytes = (size_t)shape->B * GDN_CONV_W * C * 2;
+    const uintptr_t ti = reinterpret_cast<uintptr_t>(tail_in), to = reinterpret_cast<uintptr_t>(tail_out);
+    if (ti != to && (ti < to + tail_bytes && to < ti + tail_bytes))
+        return fail(GDN_ERR_INVALID_ARG, "tail_in and tail_out overlap without being equal");
+    ConvDecodeParams p{};
+    p.x = x;
+    p.w = w;
+    p.tail_in = tail_in;
+    p.tail_out = tail_out;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.state = state;
+    p.out = out;
+    p.B = shape->B;
+    p.T = T;
+    p.Hk = shape->Hk;
+    p.Hv = shape->Hv;
+    p.dv = shape->dv;
+    p.group = group;
+    p.C = C;
+    p.CC = CC;
+    p.q_scale = q_scale;
+    p.normalize = (flags & GDN_NORMALIZE_QK) != 0;
+    p.out_bf16 = (flags & GDN_OUT_BF16) != 0;
+    // Rows of each value head per CTA: all of them when the tail is updated in
+    // place (one writer per tail entry); with distinct tails, split the rows
+    // until every SM has a few CTAs.
+    int row_blocks = 1;
+    if (ti != to) {
+        const long want = 4L * sm_count();
+        while (row_blocks < 4 && shape->dv / (row_blocks * 2) >= 32 &&
+               (long)shape->Hk * shape->B * row_blocks < want)
+            row_blocks *= 2;
+    }
+    p.row_blocks = row_blocks;
+    cudaError_t e = launch_conv_decode(p, shape->dk, shape->dv / row_blocks, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "conv+decode launch");
+}
+
 int gdn_tree_verify(const gdn_shape* shape, int32_t N, const int32_t* parents, const gdn_bf16* qkv,
                     const float* alpha, const float* beta, const float* state, void* out,
                     float q_scale, uint32_t flags, void* stream) {

@@ -17,6 +17,7 @@
 // verified in one pass).
 #include <cuda_runtime.h>
 
+#include "gdn_conv.cuh"
 #include "gdn_internal.h"
 #include "gdn_step.cuh"
 
@@ -185,6 +186,126 @@ gdn_tree_kernel(const __grid_constant__ TreeParams p) {
         }
         cur = nxt;
     }
+}
+
+// Fused conv + decode.  A CTA owns one key-head group (its q and k channels
+// and the v channels of the group's value heads) of one sequence, and 32*R
+// rows of each of those value heads.  It runs the conv for the group's
+// channels into shared memory (rounded to bf16 exactly as gdn_conv_step
+// stores it), then advances each value head's rows through the T tokens with
+// the shared step.  Every tail entry is written by one CTA only (row block 0);
+// with several row blocks the tail is read from tail_in and written to a
+// distinct tail_out, so no CTA reads an entry another CTA has overwritten.
+template <int DK, int R>
+__global__ void __launch_bounds__(kThreads)
+gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
+    constexpr int V = DK / 32;
+    extern __shared__ uint4 smem_y[];
+    uint16_t* ys = reinterpret_cast<uint16_t*>(smem_y);  // [T][CC] bf16 conv outputs
+    const int lane8 = threadIdx.x & 7;
+    const int rg = threadIdx.x >> 3;
+    const int g = blockIdx.x / p.row_blocks;
+    const int rb = blockIdx.x % p.row_blocks;
+    const int b = blockIdx.y;
+    const size_t C = (size_t)p.C;
+    const int CC = p.CC;
+    const int row0 = rb * (kRowsPerPass * R) + rg;
+    auto state_of = [&](int j) { return p.state + ((size_t)b * p.Hv + g * p.group + j) * (size_t)p.dv * DK; };
+
+    // ---- conv of this group's channels (8 per thread)
+    for (int cv = threadIdx.x; cv < CC / 8; cv += kThreads) {
+        const int c = cv * 8;
+        const int gc = c < DK ? g * DK + c
+                     : c < 2 * DK ? p.Hk * DK + g * DK + (c - DK)
+                     : 2 * p.Hk * DK + g * p.group * p.dv + (c - 2 * DK);
+        float w[8][4];
+        load_taps8(p.w + (size_t)gc * GDN_CONV_W, w);
+        const uint16_t* tb = p.tail_in + (size_t)b * GDN_CONV_W * C + gc;
+        const uint16_t* xb = p.x + (size_t)b * p.T * C + gc;
+        // tail[0] is shifted out by the first token (T >= 1), so it is not read
+        Vec8 h1 = load8(tb + C), h2 = load8(tb + 2 * C), h3 = load8(tb + 3 * C);
+        Vec8 h0 = h1;
+        for (int t = 0; t < p.T; ++t) {
+            h0 = h1;
+            h1 = h2;
+            h2 = h3;
+            h3 = load8(xb + (size_t)t * C);
+            store_y(ys + (size_t)t * CC + c, w, h0, h1, h2, h3);
+        }
+        if (rb == 0) {
+            uint16_t* to = p.tail_out + (size_t)b * GDN_CONV_W * C + gc;
+            put8(to, h0);
+            put8(to + C, h1);
+            put8(to + 2 * C, h2);
+            put8(to + 3 * C, h3);
+        }
+    }
+    __syncthreads();
+
+    // ---- the group's value heads, one after another
+    const bool normalize = p.normalize != 0;
+    const bool out_bf16 = p.out_bf16 != 0;
+    for (int j = 0; j < p.group; ++j) {
+        const int h = g * p.group + j;
+        float* S = state_of(j);
+        float4 s[R][V];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < V; ++m)
+                s[r][m] = __ldcs(reinterpret_cast<const float4*>(
+                    S + (size_t)(row0 + kRowsPerPass * r) * DK + 32 * m + 4 * lane8));
+        for (int t = 0; t < p.T; ++t) {
+            const uint16_t* yt = ys + (size_t)t * CC;
+            TokenKQ<V> kq;
+            token_kq<V>(yt, yt + DK, lane8, p.q_scale, normalize, kq);
+            const size_t trow = (size_t)b * p.T + t;
+            const float alpha = p.alpha[trow * p.Hv + h];
+            const float beta = p.beta[trow * p.Hv + h];
+            const uint16_t* vrow = yt + 2 * DK + j * p.dv;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int i = row0 + kRowsPerPass * r;
+                const float v_i = __uint_as_float((uint32_t)vrow[i] << 16);
+                const float o = row_step<V>(s[r], kq, v_i, alpha, beta);
+                if (p.out != nullptr && lane8 == 0)
+                    store_out(p.out, ((trow * p.Hv) + h) * p.dv + i, o, out_bf16);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < V; ++m)
+                __stcs(reinterpret_cast<float4*>(S + (size_t)(row0 + kRowsPerPass * r) * DK + 32 * m + 4 * lane8),
+                       s[r][m]);
+    }
+}
+
+template <int DK, int R>
+static cudaError_t launch_conv_decode_t(const ConvDecodeParams& p, cudaStream_t s) {
+    dim3 grid(p.Hk * p.row_blocks, p.B, 1);
+    const size_t smem = (size_t)p.T * p.CC * 2;
+    gdn_conv_decode_kernel<DK, R><<<grid, kThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <int DK>
+static cudaError_t launch_conv_decode_r(const ConvDecodeParams& p, int rows_per_cta, cudaStream_t s) {
+    switch (rows_per_cta) {
+        case 32: return launch_conv_decode_t<DK, 1>(p, s);
+        case 64: return launch_conv_decode_t<DK, 2>(p, s);
+        case 128: return launch_conv_decode_t<DK, 4>(p, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_conv_decode(const ConvDecodeParams& p, int dk, int rows_per_cta, cudaStream_t s) {
+    switch (dk) {
+        case 32: return launch_conv_decode_r<32>(p, rows_per_cta, s);
+        case 64: return launch_conv_decode_r<64>(p, rows_per_cta, s);
+        case 128: return launch_conv_decode_r<128>(p, rows_per_cta, s);
+    }
+    return cudaErrorInvalidValue;
 }
 
 template <int DK, int R, bool GATHER>

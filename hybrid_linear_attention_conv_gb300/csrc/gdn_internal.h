@@ -60,6 +60,24 @@ struct ConvParams {
     int8_t anc[GDN_MAX_TREE_NODES][3];
 };
 
+// Fused conv + decode: one CTA per (key-head group, row block, sequence).
+struct ConvDecodeParams {
+    const uint16_t* x;        // [B, T, C] pre-conv inputs
+    const uint16_t* w;        // [C, 4]
+    const uint16_t* tail_in;  // [B, 4, C]
+    uint16_t* tail_out;       // [B, 4, C] (equal to tail_in when row_blocks == 1)
+    const float* alpha;       // [B, T, Hv]
+    const float* beta;        // [B, T, Hv]
+    float* state;             // [B, Hv, dv, dk]
+    void* out;                // [B, T, Hv, dv] or nullptr
+    int B, T, Hk, Hv, dv, group, C;
+    int CC;                   // channels of one key-head group: 2 dk + group dv
+    int row_blocks;           // CTAs along the value rows of one group
+    float q_scale;
+    int normalize;
+    int out_bf16;
+};
+
 struct TailParams {
     const uint16_t* x_tree;  // [N, C]
     uint16_t* tail;          // [4, C]
@@ -78,6 +96,9 @@ int cuda_error(cudaError_t e, const char* what);
 cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int gather,
                           cudaStream_t s);
 cudaError_t launch_tree(const TreeParams& p, int dk, cudaStream_t s);
+cudaError_t launch_conv_decode(const ConvDecodeParams& p, int dk, int rows_per_cta, cudaStream_t s);
+constexpr int kFusedMaxTokens = 16;
+constexpr int kFusedMaxSmem = 48 * 1024;
 cudaError_t launch_conv(const ConvParams& p, cudaStream_t s);
 cudaError_t launch_commit_tail(const TailParams& p, cudaStream_t s);
 

@@ -45,6 +45,7 @@ EXPORTS = [
     "gdn_tree_root_path",
     "gdn_conv_step",
     "gdn_decode_step",
+    "gdn_conv_decode_step",
     "gdn_tree_verify",
     "gdn_commit_path",
     "gdn_prefill_workspace_bytes",
@@ -87,6 +88,7 @@ def load(path: str = LIB_PATH):
             "gdn_tree_root_path": (ctypes.c_int, [I32, P, I32, P, I32]),
             "gdn_conv_step": (ctypes.c_int, [I32, I32, I32, P, P, P, P, P, U32, P]),
             "gdn_decode_step": (ctypes.c_int, [SH, I32, P, P, P, P, P, F, U32, P]),
+            "gdn_conv_decode_step": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, P, F, U32, P]),
             "gdn_tree_verify": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, F, U32, P]),
             "gdn_commit_path": (ctypes.c_int, [SH, I32, P, P, I32, P, P, P, P, P, P, U32, P]),
             "gdn_prefill_workspace_bytes": (SZ, [SH, I32, I32]),
@@ -201,6 +203,32 @@ def decode_step(qkv, alpha, beta, state, Hk, Hv, dk, dv, out=None, q_scale=1.0, 
                                      (B, T, Hv, dv)),
                                 float(q_scale), _flags(normalize, out_bf16), _stream())
     _check(rc, "gdn_decode_step")
+    return out
+
+
+def conv_decode_step(x, w, tail_in, alpha, beta, state, Hk, Hv, dk, dv, tail_out=None, out=None,
+                     q_scale=1.0, normalize=True, out_bf16=False) -> torch.Tensor:
+    """Fused conv + decode.  x bf16 [B,T,C] pre-conv, w bf16 [C,4], tail_in bf16
+    [B,4,C]; tail_out defaults to tail_in (in place).  Returns out [B,T,Hv,dv]."""
+    B, T, C = x.shape
+    if tail_out is None:
+        tail_out = tail_in
+    if out is None:
+        out = torch.empty((B, T, Hv, dv), dtype=torch.bfloat16 if out_bf16 else torch.float32,
+                          device=x.device)
+    sh = _shape(B, Hk, Hv, dk, dv)
+    C_ = packed_channels(Hk, Hv, dk, dv)
+    rc = load().gdn_conv_decode_step(ctypes.byref(sh), T, _dev(x, torch.bfloat16, "x", (B, T, C_)),
+                                     _dev(w, torch.bfloat16, "w", (C_, GDN_CONV_W)),
+                                     _dev(tail_in, torch.bfloat16, "tail_in", (B, GDN_CONV_W, C_)),
+                                     _dev(tail_out, torch.bfloat16, "tail_out", (B, GDN_CONV_W, C_)),
+                                     _dev(alpha, torch.float32, "alpha", (B, T, Hv)),
+                                     _dev(beta, torch.float32, "beta", (B, T, Hv)),
+                                     _dev(state, torch.float32, "state", (B, Hv, dv, dk)),
+                                     _dev(out, torch.bfloat16 if out_bf16 else torch.float32, "out",
+                                          (B, T, Hv, dv)),
+                                     float(q_scale), _flags(normalize, out_bf16), _stream())
+    _check(rc, "gdn_conv_decode_step")
     return out
 
 

@@ -151,6 +151,29 @@ int gdn_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv,
                     float q_scale, uint32_t flags, void* stream);
 
 /*
+ * gdn_conv_decode_step -- gdn_conv_step (linear mode) followed by
+ * gdn_decode_step on its output, in one launch: the conv output never
+ * reaches HBM.  Results (out, state, the new tail) are identical, bit for
+ * bit, to the two separate calls.
+ *   T          1 .. 16 tokens per sequence (0 is a no-op); T * (2 dk +
+ *              (Hv/Hk) dv) * 2 bytes must not exceed 48 KB.
+ *   x          bf16 [B, T, C_qkv] pre-conv inputs (packed [q | k | v]).
+ *   w          bf16 [C_qkv, 4] conv taps.
+ *   tail_in    bf16 [B, 4, C_qkv] the last four inputs before this call.
+ *   tail_out   bf16 [B, 4, C_qkv] receives the last four inputs after it.
+ *              It may be tail_in itself (updated in place); a distinct
+ *              buffer (ping-pong between calls) lets small batches spread
+ *              each head's rows over more CTAs.  Partial overlap is refused.
+ *   alpha, beta, state, out, q_scale, flags: as for gdn_decode_step.
+ * Source: the per-layer decode step of "Architecture" (v0.14.2) section 8.1
+ * (conv tail + recurrent state per layer) and section 8.3 (decode loop).
+ */
+int gdn_conv_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* x, const gdn_bf16* w,
+                         const gdn_bf16* tail_in, gdn_bf16* tail_out, const float* alpha,
+                         const float* beta, float* state, void* out, float q_scale, uint32_t flags,
+                         void* stream);
+
+/*
  * gdn_tree_verify -- outputs of every node of a draft tree in one pass.
  * Node n's state is the committed state advanced through the root..n path
  * (each node branches from its parent's state); out[n] = S_n q^_n.  The

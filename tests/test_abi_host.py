@@ -168,3 +168,16 @@ def test_root_path_rejects(lib):
         gdn.tree_root_path(np.array([-1, 2, 0], np.int32), 1)
     with pytest.raises(gdn.GdnError):
         gdn.tree_root_path(np.array([-1, 0], np.int32), 5)
+
+
+def test_conv_decode_validation(lib):
+    P = ctypes.c_void_p
+    sh = _sh(B=2)
+    args = lambda T, ti, to: (ctypes.byref(sh), T, P(FAKE), P(FAKE), P(ti), P(to), P(FAKE), P(FAKE), P(FAKE), None,
+                              1.0, 1, None)
+    assert lib.gdn_conv_decode_step(*args(17, FAKE, FAKE)) == -2   # more than 16 tokens
+    assert lib.gdn_conv_decode_step(*args(1, FAKE, FAKE + 16)) == -1  # overlapping tails
+    assert lib.gdn_conv_decode_step(*args(1, FAKE, FAKE + 8)) == -6   # misaligned tail_out
+    big = gdn.gdn_shape(1, 1, 16, 128, 128)  # 2*128 + 16*128 channels x 16 tokens > 48 KB staging
+    assert lib.gdn_conv_decode_step(ctypes.byref(big), 16, P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                                     P(FAKE), None, 1.0, 1, None) == -2

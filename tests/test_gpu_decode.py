@@ -225,3 +225,54 @@ def test_conv_decode_pipeline(shape):
     assert np.array_equal(host(tail), tail_ref)
     assert_out_close(host(out), out_ref)
     assert_state_close(host(st), st_ref)
+
+
+# ---------------------------------------------------------------------------
+# fused conv + decode == conv_step then decode_step, bit for bit
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("shape,T,pingpong", [
+    (gen.QWEN_27B.with_batch(4), 1, False),
+    (gen.QWEN_27B.with_batch(1), 1, True),      # distinct tails: rows split over CTAs
+    (gen.QWEN_27B.with_batch(2), 3, True),
+    (gen.TINY, 16, False),
+    (gen.Shape(3, 2, 4, 32, 64), 2, True),      # dk != dv
+    (gen.Shape(2, 1, 3, 64, 128), 5, False),
+])
+def test_conv_decode_fused_equals_unfused(shape, T, pingpong):
+    c = gen.conv_inputs(31 + T, shape.B, T, shape.C)
+    d = gen.decode_inputs(31 + T, shape, T, tag="fused")
+    w = bf16(c["w"])
+    # unfused
+    tail_a = bf16(c["tail"])
+    y = gdn.conv_step(bf16(c["x"]), w, tail_a)
+    st_a = f32(d["state"])
+    out_a = gdn.decode_step(y, f32(d["alpha"]), f32(d["beta"]), st_a, shape.Hk, shape.Hv, shape.dk, shape.dv)
+    # fused
+    tail_in = bf16(c["tail"])
+    tail_out = torch.zeros_like(tail_in) if pingpong else None
+    st_b = f32(d["state"])
+    out_b = gdn.conv_decode_step(bf16(c["x"]), w, tail_in, f32(d["alpha"]), f32(d["beta"]), st_b, shape.Hk,
+                                 shape.Hv, shape.dk, shape.dv, tail_out=tail_out)
+    torch.cuda.synchronize()
+    assert torch.equal(out_a, out_b)
+    assert torch.equal(st_a, st_b)
+    assert torch.equal(tail_a, tail_out if pingpong else tail_in)
+    if pingpong:
+        assert np.array_equal(host(tail_in), c["tail"]), "tail_in must be read only"
+
+
+def test_conv_decode_fused_vs_oracle_27b():
+    shape = gen.QWEN_27B.with_batch(2)
+    c = gen.conv_inputs(5, 2, 1, shape.C)
+    d = gen.decode_inputs(5, shape, 1, tag="fusedo")
+    tail = bf16(c["tail"])
+    st = f32(d["state"])
+    out = gdn.conv_decode_step(bf16(c["x"]), bf16(c["w"]), tail, f32(d["alpha"]), f32(d["beta"]), st, shape.Hk,
+                               shape.Hv, shape.dk, shape.dv)
+    torch.cuda.synchronize()
+    y_ref, tail_ref = oracle_conv_then_round(c["x"], c["w"], c["tail"])
+    out_ref, st_ref = oracle.decode(y_ref, d["alpha"], d["beta"], d["state"], shape.Hk, shape.Hv, shape.dk,
+                                    shape.dv)
+    assert np.array_equal(host(tail), tail_ref)
+    assert_out_close(host(out), out_ref)
+    assert_state_close(host(st), st_ref)
