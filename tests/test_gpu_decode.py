@@ -276,3 +276,26 @@ def test_conv_decode_fused_vs_oracle_27b():
     assert np.array_equal(host(tail), tail_ref)
     assert_out_close(host(out), out_ref)
     assert_state_close(host(st), st_ref)
+
+
+@pytest.mark.parametrize("T,pingpong", [(1, False), (2, True)])
+def test_conv_decode_full_batch_equals_unfused(T, pingpong):
+    """Batch 64 at the 27B shape (the batched decode config): the fused step
+    equals conv_step then decode_step bit for bit."""
+    shape = gen.QWEN_27B.with_batch(64)
+    c = gen.conv_inputs(71 + T, shape.B, T, shape.C)
+    d = gen.decode_inputs(71 + T, shape, T, tag="stream")
+    w = bf16(c["w"])
+    tail_a = bf16(c["tail"])
+    y = gdn.conv_step(bf16(c["x"]), w, tail_a)
+    st_a = f32(d["state"])
+    out_a = gdn.decode_step(y, f32(d["alpha"]), f32(d["beta"]), st_a, shape.Hk, shape.Hv, shape.dk, shape.dv)
+    tail_in = bf16(c["tail"])
+    tail_out = torch.zeros_like(tail_in) if pingpong else None
+    st_b = f32(d["state"])
+    out_b = gdn.conv_decode_step(bf16(c["x"]), w, tail_in, f32(d["alpha"]), f32(d["beta"]), st_b, shape.Hk,
+                                 shape.Hv, shape.dk, shape.dv, tail_out=tail_out)
+    torch.cuda.synchronize()
+    assert torch.equal(out_a, out_b)
+    assert torch.equal(st_a, st_b)
+    assert torch.equal(tail_a, tail_out if pingpong else tail_in)
