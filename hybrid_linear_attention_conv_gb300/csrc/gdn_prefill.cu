@@ -45,7 +45,7 @@ using namespace gdn::tc;
 
 constexpr int kChunk = 64;
 constexpr int kD = 128;
-constexpr int kPrefillThreads = 128;
+constexpr int kPrefillThreads = 256;  // two warpgroups over the same 128 TMEM lanes
 
 // Shared memory map (bytes).
 constexpr uint32_t OFF_S_HI = 0;        // S hi  [128 i][128 j]   A of S [K;Q]^T
@@ -157,25 +157,32 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
     uint64_t* bar_ptr = reinterpret_cast<uint64_t*>(sm + OFF_MISC);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_MISC + 8);
     int* abort_flag = reinterpret_cast<int*>(sm + OFF_MISC + 12);
+    uint64_t* barg_ptr = reinterpret_cast<uint64_t*>(sm + OFF_MISC + 16);
     const uint32_t sbase = smem_u32(sm);
-    const uint32_t bar = smem_u32(bar_ptr);
+    const uint32_t bar = smem_u32(bar_ptr);    // every MMA batch except [K;Q] K^T
+    const uint32_t barg = smem_u32(barg_ptr);  // [K;Q] K^T, so L and T need not wait for S [K;Q]^T
 
     if (warp == 0) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     if (tid == 0) {
         mbar_init(bar, 1);
+        mbar_init(barg, 1);
         *abort_flag = 0;
     }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);  // this thread's lane
-    uint32_t parity = 0;
+    // Thread tid owns TMEM lane / state row i = tid % 128; the two warpgroups
+    // (wg = tid / 128) split every row's columns in halves.
+    const int i_row = tid & 127;
+    const int wg = tid >> 7;
+    const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // this thread's lane
+    uint32_t parity = 0, parity_g = 0;
 
     // wait for the tensor cores; on a timeout every thread leaves the chunk loop
-    auto wait_mma = [&]() -> bool {
-        const bool ok = mbar_wait(bar, parity, kWaitLimitNs);
-        if (ok) parity ^= 1u;  // on a timeout keep the phase, to drain it below
+    auto wait_on = [&](uint32_t b, uint32_t& par) -> bool {
+        const bool ok = mbar_wait(b, par, kWaitLimitNs);
+        if (ok) par ^= 1u;  // on a timeout keep the phase, to drain it below
         else atomicOr(abort_flag, 1);
         __syncthreads();
         fence_after_sync();
@@ -183,9 +190,9 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
     };
 
     // ---- prologue: state row i -> TMEM lane i and the bf16 hi/lo operand tiles
-    float* srow = p.state + ((size_t)h * kD + tid) * kD;
+    float* srow = p.state + ((size_t)h * kD + i_row) * kD;
 #pragma unroll 1
-    for (int c0 = 0; c0 < kD; c0 += 16) {
+    for (int c0 = wg * 64; c0 < wg * 64 + 64; c0 += 16) {
         float v[16];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -196,40 +203,50 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
             v[4 * q + 3] = f.w;
         }
         tmem_st16(trow + COL_S + c0, v);
-        store_split8(sm + OFF_S_HI + core_off(tid, c0, kD), sm + OFF_S_LO + core_off(tid, c0, kD), v);
-        store_split8(sm + OFF_S_HI + core_off(tid, c0 + 8, kD), sm + OFF_S_LO + core_off(tid, c0 + 8, kD), v + 8);
+        store_split8(sm + OFF_S_HI + core_off(i_row, c0, kD), sm + OFF_S_LO + core_off(i_row, c0, kD), v);
+        store_split8(sm + OFF_S_HI + core_off(i_row, c0 + 8, kD), sm + OFF_S_LO + core_off(i_row, c0 + 8, kD), v + 8);
     }
     tmem_wait_st();
 
     const int nchunks = (p.T + kChunk - 1) / kChunk;
     const size_t C = (size_t)p.C;
+    // [K;Q] rows into the K-major core layout and v rows row-major, as
+    // asynchronous 16-byte copies (zero-filled past the last token)
+    auto issue_kq = [&](int t0, int n) {
+#pragma unroll 4
+        for (int idx = tid; idx < 2 * kChunk * 16; idx += kPrefillThreads) {
+            const int r = idx >> 4, kb = idx & 15;
+            const int t = r & 63;
+            const bool ok = t < n;
+            const uint16_t* src = p.qkv + (size_t)(t0 + (ok ? t : 0)) * C + (r >= 64 ? 0 : (size_t)p.Hk * kD) +
+                                  (size_t)g * kD + kb * 8;
+            cp_async16(sbase + OFF_KQ + core_off(r, kb * 8, kD), src, ok);
+        }
+    };
+    auto issue_v = [&](int t0, int n) {
+#pragma unroll 4
+        for (int idx = tid; idx < kChunk * 16; idx += kPrefillThreads) {
+            const int t = idx >> 4, kb = idx & 15;
+            const bool ok = t < n;
+            const uint16_t* src =
+                p.qkv + (size_t)(t0 + (ok ? t : 0)) * C + (size_t)2 * p.Hk * kD + (size_t)h * kD + kb * 8;
+            cp_async16(sbase + OFF_V + t * 256 + kb * 16, src, ok);
+        }
+    };
 #pragma unroll 1
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = c * kChunk;
         const int n = min(kChunk, p.T - t0);
 
         // ---- A: stage the chunk's inputs ---------------------------------
+        // ([K;Q] and v of chunk c > 0 were prefetched during chunk c - 1)
         {
-            // [K;Q] rows into the K-major core layout and v rows row-major,
-            // all as asynchronous 16-byte copies (zero-filled past the end)
-#pragma unroll 4
-            for (int idx = tid; idx < 2 * kChunk * 16; idx += kPrefillThreads) {
-                const int r = idx >> 4, kb = idx & 15;
-                const int t = r & 63;
-                const bool ok = t < n;
-                const uint16_t* src = p.qkv + (size_t)(t0 + (ok ? t : 0)) * C +
-                                      (r >= 64 ? 0 : (size_t)p.Hk * kD) + (size_t)g * kD + kb * 8;
-                cp_async16(sbase + OFF_KQ + core_off(r, kb * 8, kD), src, ok);
+            if (c == 0) {
+                issue_kq(t0, n);
+                issue_v(t0, n);
+                cp_async_commit();
             }
-#pragma unroll 4
-            for (int idx = tid; idx < kChunk * 16; idx += kPrefillThreads) {
-                const int t = idx >> 4, kb = idx & 15;
-                const bool ok = t < n;
-                const uint16_t* src =
-                    p.qkv + (size_t)(t0 + (ok ? t : 0)) * C + (size_t)2 * p.Hk * kD + (size_t)h * kD + kb * 8;
-                cp_async16(sbase + OFF_V + t * 256 + kb * 16, src, ok);
-            }
-            cp_async_commit_wait_all();
+            cp_async_wait_all();
             if (tid < kChunk) {
                 const bool ok = tid < n;
                 s_alpha[tid] = ok ? p.alpha[(size_t)(t0 + tid) * p.Hv + h] : 1.0f;
@@ -237,7 +254,7 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
             }
         }
         __syncthreads();
-        {
+        if (tid < 128) {
             // norm of row tid of [K;Q]
             float ss = 0.f;
 #pragma unroll 4
@@ -253,11 +270,13 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
             const float r = p.normalize ? rsqrtf(__fadd_rn(ss, 1e-6f)) : 1.0f;
             if (tid >= 64) s_rq[tid - 64] = __fmul_rn(r, p.q_scale);
             else s_rk[tid] = r;
-            // K^T: each warp transposes 32 of the 128 8x8 core matrices of K
+        }
+        {
+            // K^T: each warp transposes 16 of the 128 8x8 core matrices of K
             const int lane = tid & 31;
 #pragma unroll
-            for (int it = 0; it < 8; ++it) {
-                const int q = warp * 32 + it * 4 + (lane >> 3);  // core matrix (tb, jb) = (q / 16, q % 16)
+            for (int it = 0; it < 4; ++it) {
+                const int q = warp * 16 + it * 4 + (lane >> 3);  // core matrix (tb, jb) = (q / 16, q % 16)
                 const int tb = q >> 4, jb = q & 15;
                 const uint32_t src = sbase + OFF_KQ + tb * (kD * 16) + jb * 128 + (lane & 7) * 16;
                 const uint32_t dst = sbase + OFF_KT + jb * (kChunk * 16) + tb * 128 + (lane & 7) * 16;
@@ -302,6 +321,7 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
             for (int ks = 0; ks < kD / 16; ++ks)
                 mma_bf16(tmem + COL_G, smem_desc(sbase + OFF_KQ + ks * 256, kD * 16),
                          smem_desc(sbase + OFF_KQ + ks * 256, kD * 16), id_g, ks > 0);
+            mma_commit(barg);
 #pragma unroll 1
             for (int pass = 0; pass < 2; ++pass)
 #pragma unroll 1
@@ -310,15 +330,16 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
                              smem_desc(sbase + OFF_KQ + ks * 256, kD * 16), id_kq, (pass > 0 || ks > 0));
             mma_commit(bar);
         }
-        if (!wait_mma()) break;
+        if (!wait_on(barg, parity_g)) break;
 
-        // ---- C: L, P, X^T and the scaled Q S^T ----------------------------
+        // ---- C: L and P (from [K;Q] K^T), then the T solve, while S [K;Q]^T runs
         {
-            const int t = tid & 63;
+            const int t = i_row & 63;
+            const bool krow = i_row < 64;
             const float lg_t = s_lg[t];
-            const float f = tid < 64 ? s_brk[t] : s_rq[t];
+            const float f = krow ? s_brk[t] : s_rq[t];
 #pragma unroll 1
-            for (int s0 = 0; s0 < kChunk; s0 += 16) {
+            for (int s0 = wg * 32; s0 < wg * 32 + 32; s0 += 16) {
                 float a[16];
                 tmem_ld16(trow + COL_G + s0, a);
                 float row[16];
@@ -328,9 +349,9 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
                     const float ratio = exp2f(__fsub_rn(lg_t, s_lg[sj]));  // gamma_t / gamma_s
                     const float v = __fmul_rn(__fmul_rn(f, __fmul_rn(s_rk[sj], ratio)), a[j]);
                     // L: strictly lower (rows of K); P: lower incl. diagonal (rows of Q)
-                    row[j] = (tid < 64 ? sj < t : sj <= t) ? v : 0.f;
+                    row[j] = (krow ? sj < t : sj <= t) ? v : 0.f;
                 }
-                if (tid < 64) {
+                if (krow) {
                     float4* dst = reinterpret_cast<float4*>(sm + OFF_L + (t * kChunk + s0) * 4);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) dst[q] = make_float4(row[4 * q], row[4 * q + 1], row[4 * q + 2], row[4 * q + 3]);
@@ -340,32 +361,6 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
                                  sm + OFF_P_LO + core_off(t, s0 + 8, kChunk), row + 8);
                 }
             }
-            // thread i: X^T[i][s] = beta_s (v_s[i] - gamma_s r_k,s (S k_s)[i])
-            const int i = tid;
-            const uint16_t* vcol = reinterpret_cast<const uint16_t*>(sm + OFF_V) + i;
-#pragma unroll 1
-            for (int s0 = 0; s0 < kChunk; s0 += 16) {
-                float ks[16], x[16];
-                tmem_ld16(trow + COL_KQ + s0, ks);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int sj = s0 + j;
-                    x[j] = __fmul_rn(s_beta[sj], __fmaf_rn(-s_gk[sj], ks[j], bf16_to_f(vcol[sj * kD])));
-                }
-                store_split8(sm + OFF_X_HI + core_off(i, s0, kChunk), sm + OFF_X_LO + core_off(i, s0, kChunk), x);
-                store_split8(sm + OFF_X_HI + core_off(i, s0 + 8, kChunk), sm + OFF_X_LO + core_off(i, s0 + 8, kChunk),
-                             x + 8);
-            }
-            // scaled (S q_t)[i] * gamma_t r_q,t, written back as the start of O^T
-#pragma unroll 1
-            for (int s0 = 0; s0 < kChunk; s0 += 16) {
-                float qs[16];
-                tmem_ld16(trow + COL_O + s0, qs);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) qs[j] = __fmul_rn(qs[j], s_gq[s0 + j]);
-                tmem_st16(trow + COL_O + s0, qs);
-            }
-            tmem_wait_st();
         }
         __syncthreads();
 
@@ -383,8 +378,8 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
                     z[tid + q * kPrefillThreads] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
             __syncthreads();
-            // diagonal blocks: warp w inverts block w column by column (lane = column)
-            if (lane < 16) {
+            // diagonal blocks: warp w < 4 inverts block w column by column (lane = column)
+            if (warp < 4 && lane < 16) {
                 const int b = warp * 16, cc = lane;
                 float x[16];
 #pragma unroll
@@ -417,6 +412,52 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
         fence_before_sync();
         __syncthreads();
 
+        if (!wait_on(bar, parity)) break;
+        // S [K;Q]^T has read [K;Q]: prefetch the next chunk's rows behind it
+        if (c + 1 < nchunks) {
+            issue_kq(t0 + kChunk, min(kChunk, p.T - t0 - kChunk));
+            cp_async_commit();
+        }
+
+        // ---- C2: X^T and the scaled Q S^T --------------------------------
+        {
+            // thread i: X^T[i][s] = beta_s (v_s[i] - gamma_s r_k,s (S k_s)[i])
+            const int i = i_row;
+            const uint16_t* vcol = reinterpret_cast<const uint16_t*>(sm + OFF_V) + i;
+#pragma unroll 1
+            for (int s0 = wg * 32; s0 < wg * 32 + 32; s0 += 16) {
+                float ks[16], x[16];
+                tmem_ld16(trow + COL_KQ + s0, ks);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int sj = s0 + j;
+                    x[j] = __fmul_rn(s_beta[sj], __fmaf_rn(-s_gk[sj], ks[j], bf16_to_f(vcol[sj * kD])));
+                }
+                store_split8(sm + OFF_X_HI + core_off(i, s0, kChunk), sm + OFF_X_LO + core_off(i, s0, kChunk), x);
+                store_split8(sm + OFF_X_HI + core_off(i, s0 + 8, kChunk), sm + OFF_X_LO + core_off(i, s0 + 8, kChunk),
+                             x + 8);
+            }
+            // scaled (S q_t)[i] * gamma_t r_q,t, written back as the start of O^T
+#pragma unroll 1
+            for (int s0 = wg * 32; s0 < wg * 32 + 32; s0 += 16) {
+                float qs[16];
+                tmem_ld16(trow + COL_O + s0, qs);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) qs[j] = __fmul_rn(qs[j], s_gq[s0 + j]);
+                tmem_st16(trow + COL_O + s0, qs);
+            }
+            tmem_wait_st();
+        }
+        __syncthreads();
+        // X^T has read this chunk's v rows: prefetch the next chunk's
+        if (c + 1 < nchunks) {
+            issue_v(t0 + kChunk, min(kChunk, p.T - t0 - kChunk));
+            cp_async_commit();
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+
         // ---- E: U^T = X^T T^T (3 passes) ----------------------------------
         if (tid == 0) {
             fence_after_sync();
@@ -431,14 +472,14 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
                              smem_desc(sbase + b_off[pass] + ks * 256, kChunk * 16), id, (pass > 0 || ks > 0));
             mma_commit(bar);
         }
-        if (!wait_mma()) break;
+        if (!wait_on(bar, parity)) break;
 
         // ---- F: Uhat^T and U^T operands; S <- gamma_C S -------------------
         {
-            const int i = tid;
+            const int i = i_row;
             const float lg_c = s_lg[kChunk - 1];
 #pragma unroll 1
-            for (int s0 = 0; s0 < kChunk; s0 += 16) {
+            for (int s0 = wg * 32; s0 < wg * 32 + 32; s0 += 16) {
                 float u[16], uh[16];
                 tmem_ld16(trow + COL_U + s0, u);
 #pragma unroll
@@ -452,7 +493,7 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
             }
             const float gamma_c = exp2f(lg_c);
 #pragma unroll 1
-            for (int c0 = 0; c0 < kD; c0 += 16) {
+            for (int c0 = wg * 64; c0 < wg * 64 + 64; c0 += 16) {
                 float sv[16];
                 tmem_ld16(trow + COL_S + c0, sv);
 #pragma unroll
@@ -486,15 +527,15 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
                              smem_desc(sbase + b_off[pass] + ks * 256, kChunk * 16), id_o, 1u);
             mma_commit(bar);
         }
-        if (!wait_mma()) break;
+        if (!wait_on(bar, parity)) break;
 
         // ---- H: outputs, next chunk's S operands, final state -------------
         {
-            const int i = tid;
+            const int i = i_row;
             const size_t ostride = (size_t)p.Hv * kD;
             const size_t obase = (size_t)t0 * ostride + (size_t)h * kD + i;
 #pragma unroll 1
-            for (int s0 = 0; s0 < kChunk; s0 += 16) {
+            for (int s0 = wg * 32; s0 < wg * 32 + 32; s0 += 16) {
                 float o[16];
                 tmem_ld16(trow + COL_O + s0, o);
 #pragma unroll
@@ -508,7 +549,7 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
             }
             const bool last = (c == nchunks - 1);
 #pragma unroll 1
-            for (int c0 = 0; c0 < kD; c0 += 16) {
+            for (int c0 = wg * 64; c0 < wg * 64 + 64; c0 += 16) {
                 float sv[16];
                 tmem_ld16(trow + COL_S + c0, sv);
                 if (last) {
@@ -528,6 +569,7 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
         __syncthreads();
     }
 
+    cp_async_wait_all();  // no prefetch may still be writing shared memory at exit
     if (*abort_flag != 0) {
         if (tid == 0) atomicExch(p.status, 1);
         // give in-flight tensor-core work one more bounded chance to drain

@@ -158,9 +158,8 @@ __device__ __forceinline__ void cp_async16(uint32_t dst_saddr, const void* src, 
                  "r"(valid ? 16 : 0)
                  : "memory");
 }
-__device__ __forceinline__ void cp_async_commit_wait_all() {
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // Transpose four 8x8 b16 matrices: lane l gives row (l & 7) of matrix (l >> 3)
 // of the source (src) and of the destination (dst).
