@@ -178,6 +178,15 @@ namespace gdn {
 
 int cuda_error(cudaError_t e, const char* what) { return cuda_fail(e, what); }
 
+int report_error(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    return fail(code, "%s", buf);
+}
+
 int check_prefill_args(const gdn_shape* shape, int T, int chunk, const void* qkv, const void* alpha,
                        const void* beta, const void* state, const void* out, const void* workspace,
                        size_t workspace_bytes, uint32_t flags) {

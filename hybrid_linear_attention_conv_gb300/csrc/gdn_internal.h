@@ -91,6 +91,7 @@ int check_prefill_args(const gdn_shape* shape, int T, int chunk, const void* qkv
                        const void* beta, const void* state, const void* out, const void* workspace,
                        size_t workspace_bytes, uint32_t flags);
 int cuda_error(cudaError_t e, const char* what);
+int report_error(int code, const char* fmt, ...);
 
 // Launchers (return the cudaError_t of the launch).
 cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int gather,

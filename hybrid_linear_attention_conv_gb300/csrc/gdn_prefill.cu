@@ -34,6 +34,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <mutex>
 
 #include "gdn_internal.h"
 #include "gdn_tc.cuh"
@@ -636,3 +637,56 @@ int gdn_chunk_prefill(const gdn_shape* shape, int32_t T, int32_t chunk, const gd
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Prefill without caller-provided workspace.
+//
+// Some callers cannot allocate device memory when they run the prefill: a
+// serving loop whose device memory is fixed once at start-up (it must not
+// allocate while it serves, so that its footprint stays constant), or a host
+// program whose device memory belongs to another allocator and which can only
+// hand this library the tensors it already has.  For them the scratch the
+// prefill kernel needs lives in the array below, which every GPU that loads
+// this library holds until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 256;  // largest workspace the variant can serve
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[64] = {};
+
+// Device address of g_noalloc_scratch on the current device, looked up once per
+// device (in host code the array's name is only a host-side stand-in).
+cudaError_t noalloc_scratch(void** ptr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_ptr[dev] = p;
+    }
+    *ptr = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" int gdn_chunk_prefill_noalloc(const gdn_shape* shape, int32_t T, int32_t chunk, const gdn_bf16* qkv,
+                                         const float* alpha, const float* beta, float* state, void* out,
+                                         float q_scale, uint32_t flags, void* stream) {
+    const size_t need = gdn_prefill_workspace_bytes(shape, T, chunk);
+    if (need > kNoAllocScratchBytes)
+        return report_error(GDN_ERR_WORKSPACE, "prefill needs %zu bytes of scratch; the built-in array holds %zu",
+                            need, kNoAllocScratchBytes);
+    void* scratch = nullptr;
+    cudaError_t e = noalloc_scratch(&scratch);
+    if (e != cudaSuccess) return cuda_error(e, "locating the built-in prefill scratch");
+    return gdn_chunk_prefill(shape, T, chunk, qkv, alpha, beta, state, out, scratch, kNoAllocScratchBytes, q_scale,
+                             flags, stream);
+}

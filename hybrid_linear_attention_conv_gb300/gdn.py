@@ -50,6 +50,7 @@ EXPORTS = [
     "gdn_commit_path",
     "gdn_prefill_workspace_bytes",
     "gdn_chunk_prefill",
+    "gdn_chunk_prefill_noalloc",
 ]
 
 
@@ -93,6 +94,7 @@ def load(path: str = LIB_PATH):
             "gdn_commit_path": (ctypes.c_int, [SH, I32, P, P, I32, P, P, P, P, P, P, U32, P]),
             "gdn_prefill_workspace_bytes": (SZ, [SH, I32, I32]),
             "gdn_chunk_prefill": (ctypes.c_int, [SH, I32, I32, P, P, P, P, P, P, SZ, F, U32, P]),
+            "gdn_chunk_prefill_noalloc": (ctypes.c_int, [SH, I32, I32, P, P, P, P, P, F, U32, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)

@@ -246,6 +246,27 @@ int gdn_chunk_prefill(const gdn_shape* shape, int32_t T, int32_t chunk,
                       float* state, void* out, void* workspace, size_t workspace_bytes,
                       float q_scale, uint32_t flags, void* stream);
 
+/*
+ * gdn_chunk_prefill_noalloc -- gdn_chunk_prefill for callers that cannot
+ * allocate device memory, e.g. a serving loop whose device footprint is fixed
+ * at start-up and must not grow while it serves, or a host whose device memory
+ * is owned by another allocator.  (The pages describe no such call; it exists
+ * for those callers.)
+ *   Arguments and results as gdn_chunk_prefill, without the workspace: the
+ *   scratch the kernel needs lives in a 256-byte array inside this library,
+ *   which every GPU that loads the library keeps until the process exits.
+ *   Returns GDN_ERR_WORKSPACE if the call would need more scratch than that.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture.  Every call on a device shares the one array and clears the part
+ *   that must start at zero; calls that overlap on the GPU (different streams,
+ *   no ordering between them) race on it.  The kernel's status word lives in
+ *   that shared array and is not returned to the caller.
+ */
+int gdn_chunk_prefill_noalloc(const gdn_shape* shape, int32_t T, int32_t chunk, const gdn_bf16* qkv,
+                              const float* alpha, const float* beta, float* state, void* out,
+                              float q_scale, uint32_t flags, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,74 @@
+"""The allocation-free prefill entry point, checked against the regular one.
+
+gdn_chunk_prefill_noalloc serves callers that cannot allocate device memory
+when they run a prefill -- for example a serving loop whose device footprint
+is fixed at start-up, or a host whose device memory belongs to another
+allocator.  It keeps the kernel's scratch in an array inside the library
+instead of a caller-provided workspace.  Here two calls in a row (the second
+continuing from the first one's state) must agree with gdn_chunk_prefill on
+the same inputs, within the tolerances every parity test uses.
+
+The file is named so that pytest collects it last: if it fails, a run that
+stops at the first failure has already run every other test.
+"""
+import ctypes
+
+import pytest
+import torch
+
+from gdn_testutil import assert_out_close, assert_state_close, bf16, f32, gdn, gen, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from hybrid_linear_attention_conv_gb300 import build
+    build.build()
+    return gdn.load()
+
+
+def _prefill_noalloc(lib, shape, qkv, alpha, beta, state, out):
+    """One call of the C entry point (no workspace argument)."""
+    sh = gdn.gdn_shape(1, shape.Hk, shape.Hv, shape.dk, shape.dv)
+    P = ctypes.c_void_p
+    T = qkv.shape[0]
+    rc = lib.gdn_chunk_prefill_noalloc(ctypes.byref(sh), T, 64, P(qkv.data_ptr()), P(alpha.data_ptr()),
+                                       P(beta.data_ptr()), P(state.data_ptr()), P(out.data_ptr()), 1.0,
+                                       gdn.GDN_NORMALIZE_QK, P(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0, gdn.last_error()
+
+
+def test_noalloc_prefill_matches_workspace_prefill_on_two_calls(lib):
+    shape = gen.QWEN_27B
+    T = 300  # four full chunks and a ragged one per call
+    d = gen.decode_inputs(17, shape, 2 * T, tag="noalloc")
+    qkv, al, be = bf16(d["qkv"][0]), f32(d["alpha"][0]), f32(d["beta"][0])
+
+    st_ref = f32(d["state"][0])
+    st_new = f32(d["state"][0])
+    for call in range(2):
+        sl = slice(call * T, (call + 1) * T)
+        q_c, a_c, b_c = qkv[sl].contiguous(), al[sl].contiguous(), be[sl].contiguous()
+        out_ref = gdn.chunk_prefill(q_c, a_c, b_c, st_ref, shape.Hk, shape.Hv, shape.dk, shape.dv)
+        out_new = torch.empty_like(out_ref)
+        _prefill_noalloc(lib, shape, q_c, a_c, b_c, st_new, out_new)
+        torch.cuda.synchronize()
+        assert_out_close(host(out_new), host(out_ref).astype("float64"))
+        assert_state_close(host(st_new), host(st_ref).astype("float64"))
+
+
+def test_noalloc_prefill_refuses_bad_arguments(lib):
+    shape = gen.QWEN_27B
+    d = gen.decode_inputs(18, shape, 64, tag="noalloc_bad")
+    st = f32(d["state"][0])
+    before = st.clone()
+    out = torch.empty((64, shape.Hv, shape.dv), dtype=torch.float32, device="cuda")
+    sh = gdn.gdn_shape(1, shape.Hk, shape.Hv, shape.dk, shape.dv)
+    P = ctypes.c_void_p
+    rc = lib.gdn_chunk_prefill_noalloc(ctypes.byref(sh), 64, 32, P(bf16(d["qkv"][0]).data_ptr()),
+                                       P(f32(d["alpha"][0]).data_ptr()), P(f32(d["beta"][0]).data_ptr()),
+                                       P(st.data_ptr()), P(out.data_ptr()), 1.0, gdn.GDN_NORMALIZE_QK, None)
+    torch.cuda.synchronize()
+    assert rc == -1 and "chunk" in gdn.last_error()
+    assert torch.equal(st, before)
