@@ -243,6 +243,7 @@ def prefill_bytes(T: int) -> int:
 DECODE_SOURCES = ["hybrid_linear_attention_conv_gb300/csrc/gdn_decode.cu",
                   "hybrid_linear_attention_conv_gb300/csrc/gdn_step.cuh",
                   "hybrid_linear_attention_conv_gb300/csrc/gdn_internal.h"]
+FUSED_SOURCES = DECODE_SOURCES + ["hybrid_linear_attention_conv_gb300/csrc/gdn_conv.cuh"]
 PREFILL_SOURCES = ["hybrid_linear_attention_conv_gb300/csrc/gdn_prefill.cu",
                    "hybrid_linear_attention_conv_gb300/csrc/gdn_tc.cuh",
                    "hybrid_linear_attention_conv_gb300/csrc/gdn_internal.h"]
@@ -370,19 +371,57 @@ class Batched(Workload):
         self.launches_per_step = L
         self.units_per_step = L * B * HV
         self.dominant = "gdn_conv_decode_kernel"
-        self.dominant_sources = DECODE_SOURCES
+        self.dominant_sources = FUSED_SOURCES
         self.bound = "hbm"
         self.dominant_work = fused_bytes_per_launch(B)
         self.step_bytes = L * fused_bytes_per_launch(B)
+
+    def _launch_all(self, s: int, sp):
+        P = ctypes.c_void_p
+        for l in range(self.L):
+            tl = P(self.tail[l].data_ptr())
+            _call(self.lib.gdn_conv_decode_step,
+                  (ctypes.byref(self.shape), 1, P(self.x[s, l].data_ptr()), P(self.w[l].data_ptr()), tl, tl,
+                   P(self.alpha[s, l].data_ptr()), P(self.beta[s, l].data_ptr()), P(self.state[l].data_ptr()),
+                   P(self.out[l].data_ptr()), 1.0, self.gdn.GDN_NORMALIZE_QK, sp), self.gdn)
+
+    def capture(self):
+        """One CUDA graph per input set holding the step's L launches (the
+        pages' engine captures its decode launches the same way)."""
+        torch = self.torch
+        self.graphs = []
+        for s in range(self.n_sets):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self._launch_all(s, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+            self.graphs.append(g)
+        torch.cuda.synchronize()
+
+    @property
+    def marks_per_step(self) -> int:
+        return 1 if getattr(self, "graphs", None) else self.launches_per_step
 
     def step(self, i: int, rec: Recorder | None = None):
         lib, gdn = self.lib, self.gdn
         if rec:
             rec.begin(i)
+        if getattr(self, "graphs", None):
+            self.graphs[i % self.n_sets].replay()
+            if rec:
+                rec.mark("step")
+            return
         for args in self.args[i % self.n_sets]:
             _call(lib.gdn_conv_decode_step, args, gdn)
             if rec:
                 rec.mark("gdn_conv_decode_kernel")
+
+    def dominant_ms(self, rec: Recorder) -> list:
+        """Per-launch durations: measured per kernel in eager mode; in graph
+        mode the step time spread over its L launches (an upper bound, since it
+        includes any gap between launches)."""
+        if getattr(self, "graphs", None):
+            return [ms / self.L for ms in rec.step_ms()]
+        return rec.kernel_ms(self.dominant)
 
     def e2e_setup(self):
         torch = self.torch
@@ -397,8 +436,11 @@ class Batched(Workload):
         self.e2e_copy(self.x[0], self.h_x)
         self.e2e_copy(self.alpha[0], self.h_a)
         self.e2e_copy(self.beta[0], self.h_b)
-        for args in self.args[0]:
-            _call(self.lib.gdn_conv_decode_step, args, self.gdn)
+        if getattr(self, "graphs", None):
+            self.graphs[0].replay()
+        else:
+            for args in self.args[0]:
+                _call(self.lib.gdn_conv_decode_step, args, self.gdn)
         self.e2e_copy(self.h_out, self.out)
 
     def config(self=None) -> dict:
@@ -410,7 +452,9 @@ class Batched(Workload):
                             "per sequence per layer (fused conv + delta step, one launch per layer)",
                 "layers": L, "batch": B, "Hk": HK, "Hv": HV, "dk": DK, "dv": DV, "state_bytes": sb,
                 "l2": f"inputs larger than L2: {sb / 1e9:.2f} GB of state streamed per step",
-                "launch": "eager, CUDA events after every kernel"}
+                "launch": ("eager, CUDA events after every kernel" if self is not None and not
+                           getattr(self, "graphs", None) else
+                           f"one CUDA graph per step ({L} launches), CUDA events around each replay")}
 
 
 class Decode1(Workload):
@@ -434,7 +478,7 @@ class Decode1(Workload):
         self.launches_per_step = 1
         self.units_per_step = HV
         self.dominant = "gdn_conv_decode_kernel"
-        self.dominant_sources = DECODE_SOURCES
+        self.dominant_sources = FUSED_SOURCES
         self.bound = "hbm"
         self.dominant_work = fused_bytes_per_launch(1)
         self.step_bytes = fused_bytes_per_launch(1)
@@ -736,6 +780,10 @@ def run_ours(args) -> dict | None:
         wl.pre_step()
         wl.step(i)
     torch.cuda.synchronize()
+    if hasattr(wl, "capture") and not args.eager:
+        wl.capture()
+        wl.step(0)  # one replay before the timed region
+        torch.cuda.synchronize()
 
     rec = Recorder(torch, wl.stream, wl.marks_per_step, args.steps)
     clocks = ClockSampler(local)
@@ -753,7 +801,7 @@ def run_ours(args) -> dict | None:
         wl.check_status()
     step_ms = rec.step_ms()
     total_s = sum(step_ms) / 1e3
-    dom_ms = rec.kernel_ms(wl.dominant)
+    dom_ms = wl.dominant_ms(rec) if hasattr(wl, "dominant_ms") else rec.kernel_ms(wl.dominant)
     agg = aggregate(wl.units_per_step * args.steps, total_s, world, device)
 
     # end-to-end through the API with host buffers
@@ -865,6 +913,9 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=48,
                     help="GDN layers in the batched workload (48 = the 27B model; fewer only for "
                          "profiling small cases)")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch the batched step eagerly with an event after every kernel instead of "
+                         "replaying it as a CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
