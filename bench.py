@@ -2,7 +2,7 @@
 """Benchmark of the Gated DeltaNet mixer hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload batched|decode1|tree|prefill]
+                    [--workload batched|decode1|tree|treebatch|prefill]
 
 Prints ONE JSON line (rank 0).  The metric is GDN state updates per second
 (head.tokens/s) with the achieved HBM bandwidth against the measured peak.
@@ -619,6 +619,74 @@ class Tree(Workload):
                 "launch": "eager, CUDA events around the step's kernels"}
 
 
+class TreeBatch(Workload):
+    """Joint verify of 8 sequences' draft trees (32 nodes each, own shapes) in one launch."""
+
+    name = "treebatch"
+    flush = True
+    B, N = 8, 32
+
+    def __init__(self, device, seed: int, steps: int):
+        super().__init__(device, seed)
+        import numpy as np
+        from hybrid_linear_attention_conv_gb300 import inputs as gen
+        torch, gdn = self.torch, self.gdn
+        B, N = self.B, self.N
+        self.parents = np.ascontiguousarray(np.stack([gen.random_tree(seed + b, N, 8) for b in range(B)]), np.int32)
+        self.counts = np.full(B, N, np.int32)
+        self.n_sets = min(8, steps)
+        self.state = self.randn((B, HV, DV, DK), 0.1)
+        self.qkv = self.randn((self.n_sets, B, N, C_QKV), 1.0, torch.bfloat16)
+        self.alpha, self.beta = self.gates((self.n_sets, B, N, HV))
+        self.out = torch.empty((B, N, HV, DV), dtype=torch.float32, device=device)
+        self.shape = gdn.gdn_shape(B, HK, HV, DK, DV)
+        self.launches_per_step = 1
+        self.units_per_step = B * N * HV
+        self.dominant = "gdn_tree_kernel"
+        self.dominant_sources = DECODE_SOURCES
+        self.bound = "alu"
+        self.dominant_work = B * N * HV * step_flops_per_head_token()
+        self.step_bytes = B * (HV * DV * DK * 4 + N * (C_QKV * 2 + HV * 8 + HV * DV * 4))
+
+    def _args(self, s):
+        P = ctypes.c_void_p
+        return (ctypes.byref(self.shape), self.N, self.counts.ctypes.data_as(P), self.parents.ctypes.data_as(P),
+                P(self.qkv[s].data_ptr()), P(self.alpha[s].data_ptr()), P(self.beta[s].data_ptr()),
+                P(self.state.data_ptr()), P(self.out.data_ptr()), 1.0, self.gdn.GDN_NORMALIZE_QK, self.sp)
+
+    def step(self, i: int, rec: Recorder | None = None):
+        args = self._args(i % self.n_sets)
+        if rec:
+            rec.begin(i)
+        _call(self.lib.gdn_tree_verify_batched, args, self.gdn)
+        if rec:
+            rec.mark("gdn_tree_kernel")
+
+    def e2e_setup(self):
+        self.h_qkv = self.qkv[0].cpu().pin_memory()
+        self.h_a = self.alpha[0].cpu().pin_memory()
+        self.h_b = self.beta[0].cpu().pin_memory()
+        self.h_out = self.torch.empty(self.out.shape, dtype=self.torch.float32, pin_memory=True)
+        self.e2e_h2d = self.h_qkv.numel() * 2 + self.h_a.numel() * 4 + self.h_b.numel() * 4
+        self.e2e_d2h = self.h_out.numel() * 4
+
+    def e2e_step(self, i: int):
+        self.e2e_copy(self.qkv[0], self.h_qkv)
+        self.e2e_copy(self.alpha[0], self.h_a)
+        self.e2e_copy(self.beta[0], self.h_b)
+        _call(self.lib.gdn_tree_verify_batched, self._args(0), self.gdn)
+        self.e2e_copy(self.h_out, self.out)
+
+    @staticmethod
+    def config() -> dict:
+        return {"workload": "joint tree verify of 8 sequences, 27B head shape, one layer: a random 32-node "
+                            "draft tree per sequence (depth <= 8, branching 1-4, own shape), each sequence's "
+                            "own state, all trees in one launch",
+                "sequences": TreeBatch.B, "nodes": TreeBatch.N, "Hk": HK, "Hv": HV, "dk": DK, "dv": DV,
+                "l2": "L2 flushed (256 MB write) before every step, outside the timed intervals",
+                "launch": "eager, CUDA events around the launch"}
+
+
 class Prefill(Workload):
     """Chunked prefill of 8,192 tokens, one layer."""
 
@@ -686,8 +754,8 @@ class Prefill(Workload):
                 "launch": "eager, CUDA events around the launch"}
 
 
-WORKLOADS = {"batched": Batched, "decode1": Decode1, "tree": Tree, "prefill": Prefill}
-DEFAULT_STEPS = {"batched": 100, "decode1": 1000, "tree": 200, "prefill": 20}
+WORKLOADS = {"batched": Batched, "decode1": Decode1, "tree": Tree, "treebatch": TreeBatch, "prefill": Prefill}
+DEFAULT_STEPS = {"batched": 100, "decode1": 1000, "tree": 200, "treebatch": 200, "prefill": 20}
 
 
 # ---------------------------------------------------------------------------
@@ -710,14 +778,18 @@ class OracleSample:
             self.state = self.d["state"].astype(np.float64)
             self.units = s.Hv
             self.desc = "conv + decode of 1 sequence x 1 layer x 1 token (48 head.tokens)"
-        elif workload == "tree":
+        elif workload in ("tree", "treebatch"):
             self.parents = gen.random_tree(0, 32, 8)
             self.c = gen.conv_inputs(0, 1, 32, s.C)
             self.d = gen.decode_inputs(0, s, 32, tag="tree")
             self.path = oracle.root_path(self.parents, gen.random_leaf(0, self.parents))
-            self.units = (32 + len(self.path)) * s.Hv
-            self.desc = (f"tree conv + verify (32 nodes, root-path replay) + commit ({len(self.path)} "
-                         f"tokens) of one layer")
+            if workload == "tree":
+                self.units = (32 + len(self.path)) * s.Hv
+                self.desc = (f"tree conv + verify (32 nodes, root-path replay) + commit ({len(self.path)} "
+                             f"tokens) of one layer")
+            else:
+                self.units = 32 * s.Hv
+                self.desc = "tree conv + verify of one sequence's 32-node tree (root-path replay), one layer"
         else:
             self.Ts = 128
             self.d = gen.decode_inputs(0, s, self.Ts, tag="prefill")
@@ -732,6 +804,8 @@ class OracleSample:
         elif self.workload == "tree":
             y = o.f64_to_bf16(o.conv_tree(self.parents, self.c["x"][0], self.c["w"], self.c["tail"][0]))
             o.tree_verify(self.parents, y, d["alpha"][0], d["beta"][0], d["state"][0], s.Hk, s.Hv, s.dk, s.dv)
+            if self.workload == "treebatch":
+                return self.units
             o.commit(self.parents, self.path, y, d["alpha"][0], d["beta"][0], d["state"][0], s.Hk, s.Hv,
                      s.dk, s.dv, x_tree=self.c["x"][0], tail=self.c["tail"][0])
         else:

@@ -376,13 +376,15 @@ int gdn_tree_verify(const gdn_shape* shape, int32_t N, const int32_t* parents, c
         (rc = check_ptr(state, "state")) || (rc = check_ptr(out, "out")))
         return rc;
     TreeParams p{};
-    if ((rc = schedule_tree(N, parents, p.steps, &p.n_slots)) != GDN_OK) return rc;
+    if ((rc = schedule_tree(N, parents, p.steps[0], &p.n_slots)) != GDN_OK) return rc;
     p.qkv = qkv;
     p.alpha = alpha;
     p.beta = beta;
     p.state = state;
     p.out = out;
-    p.N = N;
+    p.B = 1;
+    p.Nmax = N;
+    p.N[0] = N;
     p.Hk = shape->Hk;
     p.Hv = shape->Hv;
     p.dv = shape->dv;
@@ -393,6 +395,56 @@ int gdn_tree_verify(const gdn_shape* shape, int32_t N, const int32_t* parents, c
     p.out_bf16 = (flags & GDN_OUT_BF16) != 0;
     cudaError_t e = launch_tree(p, shape->dk, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "tree verify launch");
+}
+
+int gdn_tree_verify_batched(const gdn_shape* shape, int32_t N, const int32_t* counts, const int32_t* parents,
+                            const gdn_bf16* qkv, const float* alpha, const float* beta, const float* state,
+                            void* out, float q_scale, uint32_t flags, void* stream) {
+    int rc;
+    if ((rc = check_shape(shape, false)) != GDN_OK) return rc;
+    if ((rc = check_flags(flags)) != GDN_OK) return rc;
+    if (shape->B < 1 || shape->B > kMaxTreeBatch)
+        return fail(GDN_ERR_UNSUPPORTED_SHAPE, "B=%d trees, one call verifies 1 .. %d", shape->B, kMaxTreeBatch);
+    if (N < 1 || N > GDN_MAX_TREE_NODES)
+        return fail(GDN_ERR_BAD_PARENTS, "node capacity N=%d outside [1, %d]", N, GDN_MAX_TREE_NODES);
+    if (counts == nullptr || parents == nullptr) return fail(GDN_ERR_INVALID_ARG, "counts / parents is NULL");
+    if ((rc = check_ptr(qkv, "qkv")) || (rc = check_ptr(alpha, "alpha")) || (rc = check_ptr(beta, "beta")) ||
+        (rc = check_ptr(state, "state")) || (rc = check_ptr(out, "out")))
+        return rc;
+    static thread_local TreeParamsBatch p;  // 8 KB of schedules: kept off the stack
+    p = TreeParamsBatch{};
+    for (int b = 0; b < shape->B; ++b) {
+        if (counts[b] < 1 || counts[b] > N)
+            return fail(GDN_ERR_BAD_PARENTS, "tree %d has %d nodes, need 1 .. %d", b, counts[b], N);
+        if ((rc = check_parents(counts[b], parents + (size_t)b * N)) != GDN_OK) {
+            const std::string why = t_error;
+            return fail(rc, "tree %d: %s", b, why.c_str());
+        }
+        int slots = 0;
+        if ((rc = schedule_tree(counts[b], parents + (size_t)b * N, p.steps[b], &slots)) != GDN_OK) {
+            const std::string why = t_error;
+            return fail(rc, "tree %d: %s", b, why.c_str());
+        }
+        p.N[b] = counts[b];
+        if (slots > p.n_slots) p.n_slots = slots;
+    }
+    p.qkv = qkv;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.state = state;
+    p.out = out;
+    p.B = shape->B;
+    p.Nmax = N;
+    p.Hk = shape->Hk;
+    p.Hv = shape->Hv;
+    p.dv = shape->dv;
+    p.group = shape->Hv / shape->Hk;
+    p.C = packed_channels(shape);
+    p.q_scale = q_scale;
+    p.normalize = (flags & GDN_NORMALIZE_QK) != 0;
+    p.out_bf16 = (flags & GDN_OUT_BF16) != 0;
+    cudaError_t e = launch_tree(p, shape->dk, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "batched tree verify launch");
 }
 
 int gdn_commit_path(const gdn_shape* shape, int32_t N, const int32_t* parents, const int32_t* path,

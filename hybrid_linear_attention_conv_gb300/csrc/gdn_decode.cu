@@ -92,16 +92,22 @@ __host__ __device__ constexpr size_t tree_stage_bytes(int N) {
     return tree_kq_bytes<DK>(N) + (size_t)N * (kRowsPerPass * 2 + 2 * 4);
 }
 
-template <int DK>
+template <int DK, int MB>
 __global__ void __launch_bounds__(kThreads)
-gdn_tree_kernel(const __grid_constant__ TreeParams p) {
+gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     constexpr int V = DK / 32;
+    const int tree = blockIdx.z;          // sequence b: its own tree and state
+    const int N = p.N[tree];
+    const TreeStep* steps = p.steps[tree];
+    const uint16_t* qkv = p.qkv + (size_t)tree * p.Nmax * p.C;
+    const float* alpha_b = p.alpha + (size_t)tree * p.Nmax * p.Hv;
+    const float* beta_b = p.beta + (size_t)tree * p.Nmax * p.Hv;
     extern __shared__ float4 smem4[];
     float4* slots = smem4;  // [n_slots][32 row groups][V][8 lanes]
     uint8_t* stage = reinterpret_cast<uint8_t*>(smem4) + (size_t)p.n_slots * kRowsPerPass * DK * sizeof(float);
     float4* s_kq = reinterpret_cast<float4*>(stage);                                   // per-node records
-    uint16_t* s_v = reinterpret_cast<uint16_t*>(stage + tree_kq_bytes<DK>(p.N));        // [N][32]
-    float* s_ab = reinterpret_cast<float*>(s_v + (size_t)p.N * kRowsPerPass);            // [N][alpha, beta]
+    uint16_t* s_v = reinterpret_cast<uint16_t*>(stage + tree_kq_bytes<DK>(p.Nmax));        // [N][32]
+    float* s_ab = reinterpret_cast<float*>(s_v + (size_t)p.Nmax * kRowsPerPass);            // [N][alpha, beta]
     const int lane8 = threadIdx.x & 7;
     const int rg = threadIdx.x >> 3;
     const int h = blockIdx.y;
@@ -112,18 +118,18 @@ gdn_tree_kernel(const __grid_constant__ TreeParams p) {
     constexpr int KQ_REC = 8 * 2 * V + 1;  // float4 units
 
     {
-        for (int idx = threadIdx.x; idx < p.N * (kRowsPerPass / 8); idx += kThreads) {
+        for (int idx = threadIdx.x; idx < N * (kRowsPerPass / 8); idx += kThreads) {
             const int n = idx / (kRowsPerPass / 8), c = idx % (kRowsPerPass / 8);
-            const uint16_t* src = p.qkv + (size_t)n * p.C + (size_t)2 * p.Hk * DK + (size_t)h * p.dv + row0 + c * 8;
+            const uint16_t* src = qkv + (size_t)n * p.C + (size_t)2 * p.Hk * DK + (size_t)h * p.dv + row0 + c * 8;
             *reinterpret_cast<uint4*>(s_v + (size_t)n * kRowsPerPass + c * 8) =
                 __ldg(reinterpret_cast<const uint4*>(src));
         }
-        for (int n = threadIdx.x; n < p.N; n += kThreads) {
-            s_ab[2 * n] = p.alpha[(size_t)n * p.Hv + h];
-            s_ab[2 * n + 1] = p.beta[(size_t)n * p.Hv + h];
+        for (int n = threadIdx.x; n < N; n += kThreads) {
+            s_ab[2 * n] = alpha_b[(size_t)n * p.Hv + h];
+            s_ab[2 * n + 1] = beta_b[(size_t)n * p.Hv + h];
         }
     }
-    const float* S = p.state + (size_t)h * p.dv * DK + (size_t)row * DK;
+    const float* S = p.state + ((size_t)tree * p.Hv + h) * p.dv * DK + (size_t)row * DK;
     float4 s[V];
 #pragma unroll
     for (int m = 0; m < V; ++m) s[m] = __ldg(reinterpret_cast<const float4*>(S + 32 * m + 4 * lane8));
@@ -137,11 +143,11 @@ gdn_tree_kernel(const __grid_constant__ TreeParams p) {
     // token_kq reduces with full-warp shuffles, so the loop is warp-uniform:
     // all four row groups of a warp iterate together (on a clamped node when
     // they run past N) and only the groups with a real node write.
-    for (int n0 = rg & ~3; n0 < p.N; n0 += kRowsPerPass) {
+    for (int n0 = rg & ~3; n0 < N; n0 += kRowsPerPass) {
         const int n = n0 + (rg & 3);
-        const bool real = n < p.N;
+        const bool real = n < N;
         TokenKQ<V> t;
-        const uint16_t* qkv_row = p.qkv + (size_t)(real ? n : p.N - 1) * p.C;
+        const uint16_t* qkv_row = qkv + (size_t)(real ? n : N - 1) * p.C;
         token_kq<V>(qkv_row + (size_t)g * DK, qkv_row + (size_t)p.Hk * DK + (size_t)g * DK, lane8, p.q_scale,
                     normalize, t);
         if (real) {
@@ -166,20 +172,20 @@ gdn_tree_kernel(const __grid_constant__ TreeParams p) {
         t.kq = s_kq[(size_t)n * KQ_REC + 8 * 2 * V].x;
     };
     TokenKQ<V> cur, nxt;
-    fetch(p.steps[0].node, cur);
-    for (int step = 0; step < p.N; ++step) {
-        const TreeStep st = p.steps[step];
+    fetch(steps[0].node, cur);
+    for (int step = 0; step < N; ++step) {
+        const TreeStep st = steps[step];
         if (st.restore >= 0) {
 #pragma unroll
             for (int m = 0; m < V; ++m) s[m] = slots[((st.restore * kRowsPerPass + rg) * V + m) * 8 + lane8];
         }
         const int node = st.node;
-        if (step + 1 < p.N) fetch(p.steps[step + 1].node, nxt);
+        if (step + 1 < N) fetch(steps[step + 1].node, nxt);
         const float alpha = s_ab[2 * node];
         const float beta = s_ab[2 * node + 1];
         const float v_i = __uint_as_float((uint32_t)s_v[(size_t)node * kRowsPerPass + rg] << 16);
         const float o = row_step<V>(s, cur, v_i, alpha, beta);
-        if (lane8 == 0) store_out(p.out, ((size_t)node * p.Hv + h) * p.dv + row, o, out_bf16);
+        if (lane8 == 0) store_out(p.out, (((size_t)tree * p.Nmax + node) * p.Hv + h) * p.dv + row, o, out_bf16);
         if (st.save >= 0) {
 #pragma unroll
             for (int m = 0; m < V; ++m) slots[((st.save * kRowsPerPass + rg) * V + m) * 8 + lane8] = s[m];
@@ -344,32 +350,35 @@ cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int g
     return cudaErrorInvalidValue;
 }
 
-template <int DK>
-static cudaError_t launch_tree_t(const TreeParams& p, cudaStream_t s) {
-    const size_t smem = (size_t)p.n_slots * kRowsPerPass * DK * sizeof(float) + tree_stage_bytes<DK>(p.N);
+template <int DK, int MB>
+static cudaError_t launch_tree_t(const TreeParamsT<MB>& p, cudaStream_t s) {
+    const size_t smem = (size_t)p.n_slots * kRowsPerPass * DK * sizeof(float) + tree_stage_bytes<DK>(p.Nmax);
     static bool configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured[dev]) {
         const int max_smem = GDN_MAX_TREE_SLOTS * kRowsPerPass * DK * (int)sizeof(float) +
                              (int)tree_stage_bytes<DK>(GDN_MAX_TREE_NODES);
-        cudaError_t e = cudaFuncSetAttribute(gdn_tree_kernel<DK>,
+        cudaError_t e = cudaFuncSetAttribute(gdn_tree_kernel<DK, MB>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    dim3 grid(p.dv / kRowsPerPass, p.Hv, 1);
-    gdn_tree_kernel<DK><<<grid, kThreads, smem, s>>>(p);
+    dim3 grid(p.dv / kRowsPerPass, p.Hv, p.B);
+    gdn_tree_kernel<DK, MB><<<grid, kThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_tree(const TreeParams& p, int dk, cudaStream_t s) {
+template <int MB>
+cudaError_t launch_tree(const TreeParamsT<MB>& p, int dk, cudaStream_t s) {
     switch (dk) {
-        case 32: return launch_tree_t<32>(p, s);
-        case 64: return launch_tree_t<64>(p, s);
-        case 128: return launch_tree_t<128>(p, s);
+        case 32: return launch_tree_t<32, MB>(p, s);
+        case 64: return launch_tree_t<64, MB>(p, s);
+        case 128: return launch_tree_t<128, MB>(p, s);
     }
     return cudaErrorInvalidValue;
 }
+template cudaError_t launch_tree<1>(const TreeParamsT<1>&, int, cudaStream_t);
+template cudaError_t launch_tree<kMaxTreeBatch>(const TreeParamsT<kMaxTreeBatch>&, int, cudaStream_t);
 
 }  // namespace gdn

@@ -34,19 +34,25 @@ struct TreeStep {
     int8_t pad;
 };
 
-struct TreeParams {
-    const uint16_t* qkv;   // bf16 [N, C]
-    const float* alpha;    // [N, Hv]
-    const float* beta;     // [N, Hv]
-    const float* state;    // [Hv, dv, dk] read only
-    void* out;             // [N, Hv, dv]
-    int N, Hk, Hv, dv, group, C;
+// Tree verify over up to MB trees (one per sequence) in one launch.
+template <int MB>
+struct TreeParamsT {
+    const uint16_t* qkv;   // bf16 [B, Nmax, C]
+    const float* alpha;    // [B, Nmax, Hv]
+    const float* beta;     // [B, Nmax, Hv]
+    const float* state;    // [B, Hv, dv, dk] read only
+    void* out;             // [B, Nmax, Hv, dv]
+    int B, Nmax, Hk, Hv, dv, group, C;
     float q_scale;
     int normalize;
     int out_bf16;
-    int n_slots;
-    TreeStep steps[GDN_MAX_TREE_NODES];
+    int n_slots;           // largest number of branch states any tree needs
+    int N[MB];             // nodes of tree b
+    TreeStep steps[MB][GDN_MAX_TREE_NODES];
 };
+constexpr int kMaxTreeBatch = 32;
+using TreeParams = TreeParamsT<1>;
+using TreeParamsBatch = TreeParamsT<kMaxTreeBatch>;
 
 struct ConvParams {
     const uint16_t* x;     // [B, T, C]
@@ -96,7 +102,8 @@ int report_error(int code, const char* fmt, ...);
 // Launchers (return the cudaError_t of the launch).
 cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int gather,
                           cudaStream_t s);
-cudaError_t launch_tree(const TreeParams& p, int dk, cudaStream_t s);
+template <int MB>
+cudaError_t launch_tree(const TreeParamsT<MB>& p, int dk, cudaStream_t s);
 cudaError_t launch_conv_decode(const ConvDecodeParams& p, int dk, int rows_per_cta, cudaStream_t s);
 constexpr int kFusedMaxTokens = 16;
 constexpr int kFusedMaxSmem = 48 * 1024;

@@ -47,6 +47,7 @@ EXPORTS = [
     "gdn_decode_step",
     "gdn_conv_decode_step",
     "gdn_tree_verify",
+    "gdn_tree_verify_batched",
     "gdn_commit_path",
     "gdn_prefill_workspace_bytes",
     "gdn_chunk_prefill",
@@ -91,6 +92,7 @@ def load(path: str = LIB_PATH):
             "gdn_decode_step": (ctypes.c_int, [SH, I32, P, P, P, P, P, F, U32, P]),
             "gdn_conv_decode_step": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, P, F, U32, P]),
             "gdn_tree_verify": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, F, U32, P]),
+            "gdn_tree_verify_batched": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, F, U32, P]),
             "gdn_commit_path": (ctypes.c_int, [SH, I32, P, P, I32, P, P, P, P, P, P, U32, P]),
             "gdn_prefill_workspace_bytes": (SZ, [SH, I32, I32]),
             "gdn_chunk_prefill": (ctypes.c_int, [SH, I32, I32, P, P, P, P, P, P, SZ, F, U32, P]),
@@ -252,6 +254,28 @@ def tree_verify(parents, qkv, alpha, beta, state, Hk, Hv, dk, dv, out=None, q_sc
                                      (N, Hv, dv)),
                                 float(q_scale), _flags(normalize, out_bf16), _stream())
     _check(rc, "gdn_tree_verify")
+    return out
+
+
+def tree_verify_batched(counts, parents, qkv, alpha, beta, state, Hk, Hv, dk, dv, out=None, q_scale=1.0,
+                        normalize=True, out_bf16=False) -> torch.Tensor:
+    """B trees in one launch.  counts [B], parents [B,N] (host), qkv bf16 [B,N,C],
+    alpha/beta fp32 [B,N,Hv], state fp32 [B,Hv,dv,dk] (read only) -> out [B,N,Hv,dv]."""
+    cnt, pc = _host_i32(counts, "counts")
+    par, pp = _host_i32(parents, "parents")
+    B, N = par.shape
+    if out is None:
+        out = torch.empty((B, N, Hv, dv), dtype=torch.bfloat16 if out_bf16 else torch.float32,
+                          device=qkv.device)
+    sh = _shape(B, Hk, Hv, dk, dv)
+    rc = load().gdn_tree_verify_batched(
+        ctypes.byref(sh), N, pc, pp,
+        _dev(qkv, torch.bfloat16, "qkv", (B, N, packed_channels(Hk, Hv, dk, dv))),
+        _dev(alpha, torch.float32, "alpha", (B, N, Hv)), _dev(beta, torch.float32, "beta", (B, N, Hv)),
+        _dev(state, torch.float32, "state", (B, Hv, dv, dk)),
+        _dev(out, torch.bfloat16 if out_bf16 else torch.float32, "out", (B, N, Hv, dv)),
+        float(q_scale), _flags(normalize, out_bf16), _stream())
+    _check(rc, "gdn_tree_verify_batched")
     return out
 
 

@@ -195,6 +195,26 @@ int gdn_tree_verify(const gdn_shape* shape, int32_t N, const int32_t* parents,
                     void* stream);
 
 /*
+ * gdn_tree_verify_batched -- gdn_tree_verify for B sequences in one launch,
+ * each with its own draft tree (own size and shape) and its own state.
+ *   shape->B  trees, 1 .. 32.   N  node capacity per tree, 1 .. 64.
+ *   counts    host int32 [B]: nodes of tree b, 1 .. N.
+ *   parents   host int32 [B, N]: tree b's parent array in parents[b*N ..],
+ *             as for gdn_tree_verify; entries past counts[b] are ignored.
+ *   qkv       bf16 [B, N, C_qkv]; alpha, beta fp32 [B, N, Hv].
+ *   state     fp32 [B, Hv, dv, dk] read only.
+ *   out       [B, N, Hv, dv] fp32 (or bf16); rows past counts[b] are not written.
+ * Each tree's outputs equal, bit for bit, gdn_tree_verify of that tree alone.
+ * Source: "Architecture" (v0.14.2) section 8.5 and v0.11.1 "One request, one
+ * engine": with several sequences held over one copy of the weights, the
+ * trees of concurrent requests are verified in one joint pass.
+ */
+int gdn_tree_verify_batched(const gdn_shape* shape, int32_t N, const int32_t* counts,
+                            const int32_t* parents, const gdn_bf16* qkv, const float* alpha,
+                            const float* beta, const float* state, void* out, float q_scale,
+                            uint32_t flags, void* stream);
+
+/*
  * gdn_commit_path -- keep the accepted path's state: replay path[0..L-1]
  * (a root-to-node path of the tree) through the step, in place.  The result
  * equals, bit for bit, gdn_decode_step over the path's gathered inputs.

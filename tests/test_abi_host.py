@@ -181,3 +181,22 @@ def test_conv_decode_validation(lib):
     big = gdn.gdn_shape(1, 1, 16, 128, 128)  # 2*128 + 16*128 channels x 16 tokens > 48 KB staging
     assert lib.gdn_conv_decode_step(ctypes.byref(big), 16, P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
                                      P(FAKE), None, 1.0, 1, None) == -2
+
+
+def test_tree_verify_batched_validation(lib):
+    P = ctypes.c_void_p
+
+    def call(B, N, counts, parents):
+        c = np.ascontiguousarray(counts, np.int32)
+        pa = np.ascontiguousarray(parents, np.int32)
+        sh = _sh(B=B)
+        return lib.gdn_tree_verify_batched(ctypes.byref(sh), N, c.ctypes.data_as(P), pa.ctypes.data_as(P),
+                                           P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1.0, 1, None)
+
+    ok_tree = [-1, 0, 0, 1]
+    assert call(33, 4, [4] * 33, ok_tree * 33) == -2            # more than 32 trees
+    assert call(2, 4, [4, 0], ok_tree * 2) == -3                 # an empty tree
+    assert call(2, 4, [4, 5], ok_tree * 2) == -3                 # more nodes than the capacity
+    assert call(3, 4, [4, 4, 3], ok_tree + ok_tree + [-1, 2, 0, 9]) == -3  # tree 2: parent after child
+    assert "tree 2" in gdn.last_error()
+    assert call(2, 65, [1, 1], [-1] * 130) == -3                 # capacity above 64

@@ -201,3 +201,41 @@ def test_speculative_round_end_to_end():
     torch.cuda.synchronize()
     assert torch.equal(st2[0], st)
     assert torch.equal(tail2[0], tail[0])
+
+
+# ---------------------------------------------------------------------------
+# joint verify of several sequences' trees (different sizes and shapes)
+# ---------------------------------------------------------------------------
+def _pad_parents(trees, N):
+    out = np.full((len(trees), N), -7, np.int32)  # junk past each tree's size
+    for b, t in enumerate(trees):
+        out[b, :len(t)] = t
+    return out
+
+
+@pytest.mark.parametrize("shape", [gen.QWEN_27B, gen.Shape(1, 2, 4, 64, 64)])
+def test_tree_verify_batched_equals_single_and_oracle(shape):
+    N = 32
+    trees = [gen.random_tree(40, 32, 8), np.array([-1], np.int32), gen.random_tree(41, 13, 5),
+             gen.random_tree(42, 20, 8), np.arange(-1, 6, dtype=np.int32)]
+    B = len(trees)
+    counts = np.array([len(t) for t in trees], np.int32)
+    parents = _pad_parents(trees, N)
+    d = gen.decode_inputs(43, shape.with_batch(B), N, tag="treeb")
+    st = f32(d["state"])
+    before = st.clone()
+    out = torch.full((B, N, shape.Hv, shape.dv), float("nan"), device="cuda")
+    gdn.tree_verify_batched(counts, parents, bf16(d["qkv"]), f32(d["alpha"]), f32(d["beta"]), st, shape.Hk,
+                            shape.Hv, shape.dk, shape.dv, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(st, before), "verify must not write the committed states"
+    for b, t in enumerate(trees):
+        n = len(t)
+        assert torch.isnan(out[b, n:]).all(), "rows past the tree's size must stay untouched"
+        single = gdn.tree_verify(t, bf16(d["qkv"][b, :n]), f32(d["alpha"][b, :n]), f32(d["beta"][b, :n]),
+                                 f32(d["state"][b]), shape.Hk, shape.Hv, shape.dk, shape.dv)
+        torch.cuda.synchronize()
+        assert torch.equal(out[b, :n], single), f"tree {b}"
+        ref = oracle.tree_verify(t, d["qkv"][b, :n], d["alpha"][b, :n], d["beta"][b, :n], d["state"][b], shape.Hk,
+                                 shape.Hv, shape.dk, shape.dv)
+        assert_out_close(host(out[b, :n]), ref)
