@@ -191,3 +191,13 @@ def random_leaf(seed: int, parents) -> int:
     leaves = np.nonzero(~has_child)[0]
     u = uniform(seed, "leaf", 1)[0]
     return int(leaves[min(int(u * len(leaves)), len(leaves) - 1)])
+
+
+def kda_inputs(seed: int, shape: Shape, T: int, tag: str = "kda") -> dict:
+    """As decode_inputs, with alpha fp32 [B,T,Hv,dk]: one decay per key channel,
+    each ~ U(0.9, 1.0)."""
+    d = decode_inputs(seed, shape, T, tag=tag)
+    n = shape.B * T * shape.Hv * shape.dk
+    d["alpha"] = (0.9 + 0.1 * uniform(seed, tag + ".alpha_vec", n)).astype(np.float32).reshape(
+        shape.B, T, shape.Hv, shape.dk)
+    return d

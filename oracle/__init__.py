@@ -64,6 +64,9 @@ def _load():
             "orc_decode": (None, [I, I, I, I, I, I, P, P, P, P, P, D, I]),
             "orc_tree_verify": (None, [I, I, I, I, I, P, P, P, P, P, P, D, I]),
             "orc_commit": (None, [I, I, I, I, I, P, P, I, P, P, P, P, I, P, P, I]),
+            "orc_kda_token": (None, [I, I, P, P, P, P, P, D, P]),
+            "orc_kda_token_matrix": (None, [I, I, P, P, P, P, P, D, P]),
+            "orc_kda_decode": (None, [I, I, I, I, I, I, P, P, P, P, P, D, I]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -232,3 +235,31 @@ def prefill(qkv, alpha, beta, state, Hk, Hv, dk, dv, q_scale=1.0, normalize=True
     """Chunked prefill's definition: the plain sequential recurrence over all T
     tokens of one sequence (the chunk form is an exact reorganisation of it)."""
     return decode(qkv, alpha, beta, state, Hk, Hv, dk, dv, q_scale, normalize)
+
+
+# --------------------------------------------------------------------------
+# KDA variant (a decay per key channel)
+# --------------------------------------------------------------------------
+def kda_token(S, k, v, q, alpha, beta, matrix_form=False):
+    """One KDA token, one head: alpha is a vector of dk decays.  Returns (S_new, o)."""
+    S = _c(S, np.float64).copy()
+    k, v, q, a = (_c(x, np.float64) for x in (k, v, q, alpha))
+    dv, dk = S.shape
+    o = np.empty(dv, np.float64)
+    fn = _load().orc_kda_token_matrix if matrix_form else _load().orc_kda_token
+    fn(dk, dv, _ptr(S), _ptr(k), _ptr(v), _ptr(q), _ptr(a), float(beta), _ptr(o))
+    return S, o
+
+
+def kda_decode(qkv, alpha, beta, state, Hk, Hv, dk, dv, q_scale=1.0, normalize=True):
+    """qkv bf16 [B,T,C], alpha f32 [B,T,Hv,dk], beta f32 [B,T,Hv], state [B,Hv,dv,dk]."""
+    qkv = _c(qkv, np.uint16)
+    alpha = _c(alpha, np.float32)
+    beta = _c(beta, np.float32)
+    st = _c(state, np.float64).copy()
+    B, T = qkv.shape[0], qkv.shape[1]
+    assert alpha.shape == (B, T, Hv, dk)
+    out = np.empty((B, T, Hv, dv), np.float64)
+    _load().orc_kda_decode(B, T, Hk, Hv, dk, dv, _ptr(qkv), _ptr(alpha), _ptr(beta), _ptr(st), _ptr(out),
+                           float(q_scale), int(bool(normalize)))
+    return out, st

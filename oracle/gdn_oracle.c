@@ -325,3 +325,76 @@ void orc_commit(int N, int Hk, int Hv, int dk, int dv, const int32_t* parents,
     free(k);
     free(q);
 }
+
+/* ------------------------------------------------------------------------ */
+/* KDA variant                                                                */
+/* ------------------------------------------------------------------------ */
+
+void orc_kda_token(int dk, int dv, double* S, const double* k, const double* v,
+                   const double* q, const double* alpha, double beta, double* o) {
+    for (int i = 0; i < dv; ++i) {
+        double* s = S + (size_t)i * dk;
+        for (int j = 0; j < dk; ++j) s[j] *= alpha[j];      /* s' = a o s */
+        double a = 0.0;
+        for (int j = 0; j < dk; ++j) a += s[j] * k[j];
+        double u = beta * (v[i] - a);
+        for (int j = 0; j < dk; ++j) s[j] += u * k[j];
+    }
+    for (int i = 0; i < dv; ++i) {
+        const double* s = S + (size_t)i * dk;
+        double acc = 0.0;
+        for (int j = 0; j < dk; ++j) acc += s[j] * q[j];
+        o[i] = acc;
+    }
+}
+
+void orc_kda_token_matrix(int dk, int dv, double* S, const double* k, const double* v,
+                          const double* q, const double* alpha, double beta, double* o) {
+    /* D A with D = diag(alpha), A = I - beta k k^T: (D A)[a][b] = alpha[a] A[a][b] */
+    double* DA = (double*)malloc(sizeof(double) * (size_t)dk * dk);
+    double* R = (double*)malloc(sizeof(double) * (size_t)dv * dk);
+    for (int a = 0; a < dk; ++a)
+        for (int b = 0; b < dk; ++b)
+            DA[(size_t)a * dk + b] = alpha[a] * ((a == b ? 1.0 : 0.0) - beta * k[a] * k[b]);
+    /* R = S (D A) + beta v k^T */
+    for (int i = 0; i < dv; ++i)
+        for (int b = 0; b < dk; ++b) {
+            double acc = 0.0;
+            for (int a = 0; a < dk; ++a) acc += S[(size_t)i * dk + a] * DA[(size_t)a * dk + b];
+            R[(size_t)i * dk + b] = acc + beta * v[i] * k[b];
+        }
+    memcpy(S, R, sizeof(double) * (size_t)dv * dk);
+    for (int i = 0; i < dv; ++i) {
+        double acc = 0.0;
+        for (int j = 0; j < dk; ++j) acc += S[(size_t)i * dk + j] * q[j];
+        o[i] = acc;
+    }
+    free(R);
+    free(DA);
+}
+
+void orc_kda_decode(int B, int T, int Hk, int Hv, int dk, int dv, const uint16_t* qkv,
+                    const float* alpha, const float* beta, double* state, double* out,
+                    double q_scale, int normalize) {
+    const size_t C = (size_t)2 * Hk * dk + (size_t)Hv * dv;
+    const int group = Hv / Hk;
+    double* q = (double*)malloc(sizeof(double) * (size_t)dk);
+    double* k = (double*)malloc(sizeof(double) * (size_t)dk);
+    double* v = (double*)malloc(sizeof(double) * (size_t)dv);
+    double* a = (double*)malloc(sizeof(double) * (size_t)dk);
+    for (int b = 0; b < B; ++b)
+        for (int t = 0; t < T; ++t) {
+            const size_t tok = (size_t)b * T + t;
+            for (int h = 0; h < Hv; ++h) {
+                token_vectors(Hk, dk, dv, qkv + tok * C, h / group, h, q_scale, normalize, q, k, v);
+                for (int j = 0; j < dk; ++j) a[j] = (double)alpha[(tok * Hv + h) * dk + j];
+                double* S = state + ((size_t)b * Hv + h) * (size_t)dv * dk;
+                orc_kda_token(dk, dv, S, k, v, q, a, (double)beta[tok * Hv + h],
+                              out + (tok * Hv + h) * dv);
+            }
+        }
+    free(a);
+    free(v);
+    free(k);
+    free(q);
+}

@@ -117,6 +117,23 @@ void orc_commit(int N, int Hk, int Hv, int dk, int dv, const int32_t* parents,
                 const float* beta, const uint16_t* x_tree, int W, double* state,
                 uint16_t* tail, int normalize);
 
+/* ---- KDA variant: a decay per key channel ---------------------------------
+ * Kimi Delta Attention is listed, with a CPU reference, in the module index of
+ * the metrale_model_arch API page (Modules: glm5next_kda, kimi_k3); the page
+ * prints no update rule.  Read here as the gated delta rule with the scalar
+ * decay replaced by a diagonal one on the key dimension:
+ *     S <- (S diag(a)) (I - beta k k^T) + beta v k^T,   o = S q
+ * with a = alpha[0..dk-1].  Row form: s' = a o s (elementwise);
+ * s <- s' + beta (v_i - s'.k) k.  Then o = S_new q as a plain product. */
+void orc_kda_token(int dk, int dv, double* S, const double* k, const double* v,
+                   const double* q, const double* alpha, double beta, double* o);
+void orc_kda_token_matrix(int dk, int dv, double* S, const double* k, const double* v,
+                          const double* q, const double* alpha, double beta, double* o);
+/* As orc_decode, with alpha fp32 [B,T,Hv,dk] (one decay per key channel). */
+void orc_kda_decode(int B, int T, int Hk, int Hv, int dk, int dv, const uint16_t* qkv,
+                    const float* alpha, const float* beta, double* state, double* out,
+                    double q_scale, int normalize);
+
 #ifdef __cplusplus
 }
 #endif

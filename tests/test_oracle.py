@@ -418,3 +418,98 @@ def test_sequential_oracle_matches_chunk_form(Tn, chunk):
     out_c, st_c = _chunk_form(d["qkv"], d["alpha"], d["beta"], d["state"], 2, 4, 16, 16, chunk)
     np.testing.assert_allclose(out[0], out_c, rtol=0, atol=1e-12)
     np.testing.assert_allclose(st[0], st_c, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# KDA variant: a decay per key channel
+# ---------------------------------------------------------------------------
+def _kda_textbook(S, k, v, q, alpha, beta):
+    dk = len(k)
+    S1 = S @ np.diag(alpha) @ (np.eye(dk) - beta * np.outer(k, k)) + beta * np.outer(v, k)
+    return S1, S1 @ q
+
+
+@pytest.mark.parametrize("dk,dv", [(5, 3), (3, 7), (32, 32)])
+def test_kda_row_form_vs_matrix_forms(dk, dv):
+    n = gen.normal(11, f"kda{dk}{dv}", dv * dk + 2 * dk + dv)
+    S = n[: dv * dk].reshape(dv, dk)
+    k = n[dv * dk: dv * dk + dk]
+    k = k / np.linalg.norm(k)
+    q = n[dv * dk + dk: dv * dk + 2 * dk]
+    v = n[dv * dk + 2 * dk:]
+    a = 0.8 + 0.2 * gen.uniform(11, f"kdaa{dk}", dk)
+    S_row, o_row = oracle.kda_token(S, k, v, q, a, 0.7)
+    S_mat, o_mat = oracle.kda_token(S, k, v, q, a, 0.7, matrix_form=True)
+    S_np, o_np = _kda_textbook(S, k, v, q, a, 0.7)
+    np.testing.assert_allclose(S_row, S_np, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(S_mat, S_np, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(o_row, o_np, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(o_mat, o_np, rtol=0, atol=1e-12)
+
+
+def test_kda_invariants():
+    dk, dv = 16, 12
+    n = gen.normal(12, "kdainv", dv * dk + 2 * dk + dv)
+    S = n[: dv * dk].reshape(dv, dk)
+    k = n[dv * dk: dv * dk + dk]
+    k = k / np.linalg.norm(k)
+    q = n[dv * dk + dk: dv * dk + 2 * dk]
+    v = n[dv * dk + 2 * dk:]
+    a = 0.8 + 0.2 * gen.uniform(12, "kdaa", dk)
+    # beta = 0: every column decays by its own gate
+    S1, o = oracle.kda_token(S, k, v, q, a, 0.0)
+    np.testing.assert_allclose(S1, S * a[None, :], rtol=1e-15, atol=0)
+    np.testing.assert_allclose(o, (S * a[None, :]) @ q, rtol=0, atol=1e-13)
+    # a gate of zero on a channel wipes that column before the write
+    a0 = a.copy()
+    a0[3] = 0.0
+    S1, _ = oracle.kda_token(S, k, v, q, a0, 0.5)
+    S_np, _ = _kda_textbook(S, k, v, q, a0, 0.5)
+    np.testing.assert_allclose(S1, S_np, rtol=0, atol=1e-13)
+    # all gates 1, beta 1, unit k: the new state maps k to v
+    S1, _ = oracle.kda_token(S, k, v, q, np.ones(dk), 1.0)
+    np.testing.assert_allclose(S1 @ k, v, rtol=0, atol=1e-13)
+    # the decay comes first, the delta step second: read at k, the new state
+    # moves beta of the way from the decayed read to v; read at any x
+    # orthogonal to k, it is the decayed state alone.  Together these fix the
+    # whole map, so they also catch the decay applied after the projection.
+    beta = 0.35
+    S1, _ = oracle.kda_token(S, k, v, q, a, beta)
+    np.testing.assert_allclose(S1 @ k, (1 - beta) * ((S * a[None, :]) @ k) + beta * v, rtol=0, atol=1e-13)
+    for t in range(3):
+        x = gen.normal(12, f"kdaperp{t}", dk)
+        x = x - (x @ k) * k
+        np.testing.assert_allclose(S1 @ x, (S * a[None, :]) @ x, rtol=0, atol=1e-13)
+
+
+def test_kda_with_equal_gates_is_gdn():
+    """The same decay on every channel reduces KDA to the scalar-gated rule."""
+    s = gen.Shape(2, 2, 4, 16, 8)
+    d = gen.decode_inputs(13, s, 5, tag="kdagdn")
+    a_vec = np.repeat(d["alpha"][..., None], s.dk, axis=-1)
+    out_g, st_g = oracle.decode(d["qkv"], d["alpha"], d["beta"], d["state"], s.Hk, s.Hv, s.dk, s.dv)
+    out_k, st_k = oracle.kda_decode(d["qkv"], a_vec, d["beta"], d["state"], s.Hk, s.Hv, s.dk, s.dv)
+    np.testing.assert_allclose(out_k, out_g, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(st_k, st_g, rtol=0, atol=1e-13)
+
+
+def test_kda_decode_vs_textbook():
+    s = gen.Shape(2, 1, 3, 8, 6)
+    T = 4
+    d = gen.kda_inputs(14, s, T)
+    out, st = oracle.kda_decode(d["qkv"], d["alpha"], d["beta"], d["state"], s.Hk, s.Hv, s.dk, s.dv)
+    qkv = gen.bf16_bits_to_f32(d["qkv"]).astype(np.float64)
+    S = d["state"].astype(np.float64).copy()
+    for b in range(s.B):
+        for t in range(T):
+            row = qkv[b, t]
+            q = row[: s.dk]
+            k = row[s.dk: 2 * s.dk]
+            q = q / math.sqrt(q @ q + 1e-6)
+            k = k / math.sqrt(k @ k + 1e-6)
+            for h in range(s.Hv):
+                v = row[2 * s.dk + h * s.dv: 2 * s.dk + (h + 1) * s.dv]
+                S[b, h], o = _kda_textbook(S[b, h], k, v, q, d["alpha"][b, t, h].astype(np.float64),
+                                           float(d["beta"][b, t, h]))
+                np.testing.assert_allclose(out[b, t, h], o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(st, S, rtol=0, atol=1e-12)
