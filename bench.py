@@ -217,6 +217,12 @@ def fused_bytes_per_launch(B: int, T: int = 1) -> int:
     return state + conv + gates_out
 
 
+def kda_fused_bytes_per_launch(B: int, T: int = 1) -> int:
+    """As fused_bytes_per_launch with a decay per key channel: alpha is dk
+    fp32 values per head and token instead of one."""
+    return fused_bytes_per_launch(B, T) + B * T * HV * (DK - 1) * 4
+
+
 def step_flops_per_head_token() -> int:
     """fp32 flops of one state update of one head: s.k and s.q (2 x 2d per
     row), alpha s + u k (2d per row), the row scalars u and o (5 per row)."""
@@ -341,6 +347,7 @@ class Batched(Workload):
     """48 GDN layers x 64 sequences, one token per sequence per layer."""
 
     name = "batched"
+    kda = False
     L, B = 48, 64
 
     def __init__(self, device, seed: int, steps: int, layers: int = 48):
@@ -355,6 +362,10 @@ class Batched(Workload):
         self.n_sets = min(4, steps)
         self.x = self.randn((self.n_sets, L, B, 1, C_QKV), 1.0, bf)
         self.alpha, self.beta = self.gates((self.n_sets, L, B, 1, HV))
+        if self.kda:
+            self.alpha = 0.9 + 0.1 * torch.rand((self.n_sets, L, B, 1, HV, DK), generator=self.gen,
+                                                device=device)
+        self.fn = self.lib.gdn_kda_conv_decode_step if self.kda else self.lib.gdn_conv_decode_step
         self.out = torch.empty((L, B, 1, HV, DV), dtype=torch.float32, device=device)
         self.shape = gdn.gdn_shape(B, HK, HV, DK, DV)
         P = ctypes.c_void_p
@@ -370,17 +381,18 @@ class Batched(Workload):
             self.args.append(per)
         self.launches_per_step = L
         self.units_per_step = L * B * HV
-        self.dominant = "gdn_conv_decode_kernel"
+        self.dominant = "gdn_conv_decode_kernel[kda]" if self.kda else "gdn_conv_decode_kernel"
         self.dominant_sources = FUSED_SOURCES
         self.bound = "hbm"
-        self.dominant_work = fused_bytes_per_launch(B)
-        self.step_bytes = L * fused_bytes_per_launch(B)
+        per_launch = kda_fused_bytes_per_launch(B) if self.kda else fused_bytes_per_launch(B)
+        self.dominant_work = per_launch
+        self.step_bytes = L * per_launch
 
     def _launch_all(self, s: int, sp):
         P = ctypes.c_void_p
         for l in range(self.L):
             tl = P(self.tail[l].data_ptr())
-            _call(self.lib.gdn_conv_decode_step,
+            _call(self.fn,
                   (ctypes.byref(self.shape), 1, P(self.x[s, l].data_ptr()), P(self.w[l].data_ptr()), tl, tl,
                    P(self.alpha[s, l].data_ptr()), P(self.beta[s, l].data_ptr()), P(self.state[l].data_ptr()),
                    P(self.out[l].data_ptr()), 1.0, self.gdn.GDN_NORMALIZE_QK, sp), self.gdn)
@@ -411,9 +423,9 @@ class Batched(Workload):
                 rec.mark("step")
             return
         for args in self.args[i % self.n_sets]:
-            _call(lib.gdn_conv_decode_step, args, gdn)
+            _call(self.fn, args, gdn)
             if rec:
-                rec.mark("gdn_conv_decode_kernel")
+                rec.mark(self.dominant)
 
     def dominant_ms(self, rec: Recorder) -> list:
         """Per-launch durations: measured per kernel in eager mode; in graph
@@ -440,7 +452,7 @@ class Batched(Workload):
             self.graphs[0].replay()
         else:
             for args in self.args[0]:
-                _call(self.lib.gdn_conv_decode_step, args, self.gdn)
+                _call(self.fn, args, self.gdn)
         self.e2e_copy(self.h_out, self.out)
 
     def config(self=None) -> dict:
@@ -455,6 +467,21 @@ class Batched(Workload):
                 "launch": ("eager, CUDA events after every kernel" if self is not None and not
                            getattr(self, "graphs", None) else
                            f"one CUDA graph per step ({L} launches), CUDA events around each replay")}
+
+
+class KdaBatched(Batched):
+    """The batched decode with the KDA step: a decay per key channel."""
+
+    name = "kdabatch"
+    kda = True
+
+    def config(self=None) -> dict:
+        L = Batched.L if self is None else self.L
+        cfg = Batched.config(self)
+        cfg["workload"] = (f"batched KDA decode over {L} layers: batch {Batched.B} sequences, 27B head shape "
+                           "(16 key / 48 value heads x 128), a decay per key channel (alpha [B, Hv, 128] "
+                           "fp32), fused conv + KDA step, one launch per layer")
+        return cfg
 
 
 class Decode1(Workload):
@@ -754,8 +781,9 @@ class Prefill(Workload):
                 "launch": "eager, CUDA events around the launch"}
 
 
-WORKLOADS = {"batched": Batched, "decode1": Decode1, "tree": Tree, "treebatch": TreeBatch, "prefill": Prefill}
-DEFAULT_STEPS = {"batched": 100, "decode1": 1000, "tree": 200, "treebatch": 200, "prefill": 20}
+WORKLOADS = {"batched": Batched, "kdabatch": KdaBatched, "decode1": Decode1, "tree": Tree, "treebatch": TreeBatch,
+             "prefill": Prefill}
+DEFAULT_STEPS = {"batched": 100, "kdabatch": 100, "decode1": 1000, "tree": 200, "treebatch": 200, "prefill": 20}
 
 
 # ---------------------------------------------------------------------------
@@ -772,12 +800,13 @@ class OracleSample:
         self.np, self.oracle, self.gen = np, oracle, gen
         self.workload = workload
         s = self.s = gen.QWEN_27B
-        if workload in ("batched", "decode1"):
+        if workload in ("batched", "decode1", "kdabatch"):
             self.c = gen.conv_inputs(0, 1, 1, s.C)
-            self.d = gen.decode_inputs(0, s, 1)
+            self.d = gen.kda_inputs(0, s, 1) if workload == "kdabatch" else gen.decode_inputs(0, s, 1)
             self.state = self.d["state"].astype(np.float64)
             self.units = s.Hv
-            self.desc = "conv + decode of 1 sequence x 1 layer x 1 token (48 head.tokens)"
+            step = "KDA decode" if workload == "kdabatch" else "decode"
+            self.desc = f"conv + {step} of 1 sequence x 1 layer x 1 token (48 head.tokens)"
         elif workload in ("tree", "treebatch"):
             self.parents = gen.random_tree(0, 32, 8)
             self.c = gen.conv_inputs(0, 1, 32, s.C)
@@ -798,9 +827,10 @@ class OracleSample:
 
     def run_once(self) -> int:
         o, s, d = self.oracle, self.s, self.d
-        if self.workload in ("batched", "decode1"):
+        if self.workload in ("batched", "decode1", "kdabatch"):
             y, _ = o.conv_linear(self.c["x"], self.c["w"], self.c["tail"])
-            _, self.state = o.decode(o.f64_to_bf16(y), d["alpha"], d["beta"], self.state, s.Hk, s.Hv, s.dk, s.dv)
+            step = o.kda_decode if self.workload == "kdabatch" else o.decode
+            _, self.state = step(o.f64_to_bf16(y), d["alpha"], d["beta"], self.state, s.Hk, s.Hv, s.dk, s.dv)
         elif self.workload == "tree":
             y = o.f64_to_bf16(o.conv_tree(self.parents, self.c["x"][0], self.c["w"], self.c["tail"][0]))
             o.tree_verify(self.parents, y, d["alpha"][0], d["beta"][0], d["state"][0], s.Hk, s.Hv, s.dk, s.dv)
@@ -844,8 +874,8 @@ def run_ours(args) -> dict | None:
 
     peaks, peaks_kind = load_peaks()
     cls = WORKLOADS[args.workload]
-    if cls is Batched:
-        wl = Batched(device, 1234 + rank, args.steps + args.warmup, layers=args.layers)
+    if issubclass(cls, Batched):
+        wl = cls(device, 1234 + rank, args.steps + args.warmup, layers=args.layers)
     else:
         wl = cls(device, 1234 + rank, args.steps + args.warmup)
     torch.cuda.synchronize()

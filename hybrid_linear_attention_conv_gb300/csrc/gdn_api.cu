@@ -273,9 +273,10 @@ int gdn_conv_step(int32_t B, int32_t T, int32_t C, const int32_t* parents, const
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "conv launch");
 }
 
-int gdn_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const float* alpha,
-                    const float* beta, float* state, void* out, float q_scale, uint32_t flags,
-                    void* stream) {
+// The decode step with a decay per head (kda = false) or per key channel.
+static int decode_impl(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const float* alpha,
+                       const float* beta, float* state, void* out, float q_scale, uint32_t flags,
+                       void* stream, bool kda) {
     int rc;
     if ((rc = check_shape(shape, false)) != GDN_OK) return rc;
     if ((rc = check_flags(flags)) != GDN_OK) return rc;
@@ -302,13 +303,25 @@ int gdn_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, cons
     p.normalize = (flags & GDN_NORMALIZE_QK) != 0;
     p.out_bf16 = (flags & GDN_OUT_BF16) != 0;
     const int rows = decode_rows_per_cta(shape->B, shape->Hv, shape->dv);
-    cudaError_t e = launch_decode(p, shape->dk, rows, 0, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "decode launch");
+    cudaError_t e = launch_decode(p, shape->dk, rows, 0, kda, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, kda ? "KDA decode launch" : "decode launch");
 }
 
-int gdn_conv_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* x, const gdn_bf16* w,
-                         const gdn_bf16* tail_in, gdn_bf16* tail_out, const float* alpha, const float* beta,
-                         float* state, void* out, float q_scale, uint32_t flags, void* stream) {
+int gdn_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const float* alpha,
+                    const float* beta, float* state, void* out, float q_scale, uint32_t flags,
+                    void* stream) {
+    return decode_impl(shape, T, qkv, alpha, beta, state, out, q_scale, flags, stream, false);
+}
+
+int gdn_kda_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const float* alpha,
+                        const float* beta, float* state, void* out, float q_scale, uint32_t flags,
+                        void* stream) {
+    return decode_impl(shape, T, qkv, alpha, beta, state, out, q_scale, flags, stream, true);
+}
+
+static int conv_decode_impl(const gdn_shape* shape, int32_t T, const gdn_bf16* x, const gdn_bf16* w,
+                            const gdn_bf16* tail_in, gdn_bf16* tail_out, const float* alpha, const float* beta,
+                            float* state, void* out, float q_scale, uint32_t flags, void* stream, bool kda) {
     int rc;
     if ((rc = check_shape(shape, false)) != GDN_OK) return rc;
     if ((rc = check_flags(flags)) != GDN_OK) return rc;
@@ -317,9 +330,11 @@ int gdn_conv_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* x, c
         return fail(GDN_ERR_UNSUPPORTED_SHAPE, "T=%d tokens, the fused step takes at most %d", T, kFusedMaxTokens);
     const int group = shape->Hv / shape->Hk;
     const int CC = 2 * shape->dk + group * shape->dv;
-    if ((long)T * CC * 2 > kFusedMaxSmem)
-        return fail(GDN_ERR_UNSUPPORTED_SHAPE, "T=%d x %d channels per key-head group exceed the fused step's "
-                    "%d-byte staging", T, CC, kFusedMaxSmem);
+    // staged per token: the group's conv outputs (bf16) and, for KDA, its decay vectors (fp32)
+    const long per_token = (long)CC * 2 + (kda ? (long)group * shape->dk * 4 : 0);
+    if ((long)T * per_token > kFusedMaxSmem)
+        return fail(GDN_ERR_UNSUPPORTED_SHAPE, "T=%d x %ld staged bytes per key-head group exceed the fused "
+                    "step's %d-byte staging", T, per_token, kFusedMaxSmem);
     if (shape->B == 0 || T == 0) return GDN_OK;  // nothing to do; pointers may be NULL
     if ((rc = check_ptr(x, "x")) || (rc = check_ptr(w, "w")) || (rc = check_ptr(tail_in, "tail_in")) ||
         (rc = check_ptr(tail_out, "tail_out")) || (rc = check_ptr(alpha, "alpha")) ||
@@ -361,8 +376,23 @@ int gdn_conv_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* x, c
             row_blocks *= 2;
     }
     p.row_blocks = row_blocks;
-    cudaError_t e = launch_conv_decode(p, shape->dk, shape->dv / row_blocks, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "conv+decode launch");
+    cudaError_t e =
+        launch_conv_decode(p, shape->dk, shape->dv / row_blocks, kda, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, kda ? "conv+KDA decode launch" : "conv+decode launch");
+}
+
+int gdn_conv_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* x, const gdn_bf16* w,
+                         const gdn_bf16* tail_in, gdn_bf16* tail_out, const float* alpha, const float* beta,
+                         float* state, void* out, float q_scale, uint32_t flags, void* stream) {
+    return conv_decode_impl(shape, T, x, w, tail_in, tail_out, alpha, beta, state, out, q_scale, flags, stream,
+                            false);
+}
+
+int gdn_kda_conv_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* x, const gdn_bf16* w,
+                             const gdn_bf16* tail_in, gdn_bf16* tail_out, const float* alpha, const float* beta,
+                             float* state, void* out, float q_scale, uint32_t flags, void* stream) {
+    return conv_decode_impl(shape, T, x, w, tail_in, tail_out, alpha, beta, state, out, q_scale, flags, stream,
+                            true);
 }
 
 int gdn_tree_verify(const gdn_shape* shape, int32_t N, const int32_t* parents, const gdn_bf16* qkv,
@@ -482,7 +512,7 @@ int gdn_commit_path(const gdn_shape* shape, int32_t N, const int32_t* parents, c
     p.out_bf16 = 0;
     for (int i = 0; i < L; ++i) p.tok[i] = path[i];
     const int rows = decode_rows_per_cta(1, shape->Hv, shape->dv);
-    cudaError_t e = launch_decode(p, shape->dk, rows, 1, st);
+    cudaError_t e = launch_decode(p, shape->dk, rows, 1, false, st);
     if (e != cudaSuccess) return cuda_fail(e, "commit launch");
     if (x_tree != nullptr) {
         TailParams tp{};

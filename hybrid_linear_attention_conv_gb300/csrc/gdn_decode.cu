@@ -26,8 +26,9 @@ namespace gdn {
 constexpr int kThreads = 256;        // 8 warps = 32 row groups of 8 lanes
 constexpr int kRowsPerPass = 32;
 
-template <int DK, int R, bool GATHER>
-__global__ void __launch_bounds__(kThreads)
+// KDA selects a decay per key channel: alpha is then [B, Tsrc, Hv, dk].
+template <int DK, int R, bool GATHER, bool KDA>
+__global__ void __launch_bounds__(kThreads, 2)
 gdn_decode_kernel(const __grid_constant__ DecodeParams p) {
     constexpr int V = DK / 32;
     const int lane8 = threadIdx.x & 7;
@@ -46,23 +47,41 @@ gdn_decode_kernel(const __grid_constant__ DecodeParams p) {
             s[r][m] = __ldcs(reinterpret_cast<const float4*>(
                 S + (size_t)(row0 + kRowsPerPass * r) * DK + 32 * m + 4 * lane8));
 
+    // KDA: each token's decay vector, staged in shared memory (two buffers, so
+    // one barrier per token separates a buffer's readers from its next writer)
+    __shared__ float4 s_gate[KDA ? 2 : 1][KDA ? DK / 4 : 1];
     const bool normalize = p.normalize != 0;
     const bool out_bf16 = p.out_bf16 != 0;
     for (int t = 0; t < p.T; ++t) {
         const int tok = GATHER ? p.tok[t] : t;
         const size_t trow = (size_t)b * p.Tsrc + tok;
+        if constexpr (KDA) {
+            if (threadIdx.x < DK / 4)
+                s_gate[t & 1][threadIdx.x] =
+                    __ldg(reinterpret_cast<const float4*>(p.alpha + (trow * p.Hv + h) * DK) + threadIdx.x);
+            __syncthreads();
+        }
         const uint16_t* row = p.qkv + trow * (size_t)p.C;
         TokenKQ<V> kq;
         token_kq<V>(row + g * DK, row + (size_t)p.Hk * DK + g * DK, lane8, p.q_scale,
                     normalize, kq);
-        const float alpha = p.alpha[trow * p.Hv + h];
+        float alpha = 0.0f;
+        if constexpr (!KDA) alpha = p.alpha[trow * p.Hv + h];
         const float beta = p.beta[trow * p.Hv + h];
         const uint16_t* vrow = row + (size_t)2 * p.Hk * DK + (size_t)h * p.dv;
+        if constexpr (KDA) {
+            float4 g[V];
+            load_gate_smem<V>(s_gate[t & 1], lane8, g);
+#pragma unroll
+            for (int r = 0; r < R; ++r) kda_decay<V>(s[r], g);
+        }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const int i = row0 + kRowsPerPass * r;
             const float v_i = __uint_as_float((uint32_t)vrow[i] << 16);
-            const float o = row_step<V>(s[r], kq, v_i, alpha, beta);
+            float o;
+            if constexpr (KDA) o = delta_row_step<V>(s[r], kq, v_i, beta);
+            else o = row_step<V>(s[r], kq, v_i, alpha, beta);
             if (p.out != nullptr && lane8 == 0)
                 store_out(p.out, (((size_t)b * p.T + t) * p.Hv + h) * p.dv + i, o, out_bf16);
         }
@@ -202,12 +221,14 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
 // the shared step.  Every tail entry is written by one CTA only (row block 0);
 // with several row blocks the tail is read from tail_in and written to a
 // distinct tail_out, so no CTA reads an entry another CTA has overwritten.
-template <int DK, int R>
-__global__ void __launch_bounds__(kThreads)
+template <int DK, int R, bool KDA>
+__global__ void __launch_bounds__(kThreads, 2)
 gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
     constexpr int V = DK / 32;
     extern __shared__ uint4 smem_y[];
     uint16_t* ys = reinterpret_cast<uint16_t*>(smem_y);  // [T][CC] bf16 conv outputs
+    // KDA: the group's decay vectors [T][group][DK] fp32, after the conv outputs
+    float4* gs = reinterpret_cast<float4*>(ys + (size_t)p.T * p.CC);
     const int lane8 = threadIdx.x & 7;
     const int rg = threadIdx.x >> 3;
     const int g = blockIdx.x / p.row_blocks;
@@ -217,6 +238,19 @@ gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
     const int CC = p.CC;
     const int row0 = rb * (kRowsPerPass * R) + rg;
     auto state_of = [&](int j) { return p.state + ((size_t)b * p.Hv + g * p.group + j) * (size_t)p.dv * DK; };
+
+    // KDA: the group's decay vectors [T][group][DK] go to shared memory after
+    // the conv outputs; the first kThreads float4s are loaded before the conv
+    // so that their latency overlaps it.
+    constexpr int G4 = DK / 4;  // float4s of one decay vector
+    const int n_gate4 = KDA ? p.T * p.group * G4 : 0;
+    auto gate_src = [&](int idx) {
+        const int tj = idx / G4, c4 = idx % G4;
+        const int t = tj / p.group, j = tj % p.group;
+        return reinterpret_cast<const float4*>(p.alpha + (((size_t)b * p.T + t) * p.Hv + g * p.group + j) * DK) + c4;
+    };
+    float4 gate_first = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (KDA && threadIdx.x < n_gate4) gate_first = __ldg(gate_src(threadIdx.x));
 
     // ---- conv of this group's channels (8 per thread)
     for (int cv = threadIdx.x; cv < CC / 8; cv += kThreads) {
@@ -246,6 +280,10 @@ gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
             put8(to + 3 * C, h3);
         }
     }
+    if constexpr (KDA) {
+        if (threadIdx.x < n_gate4) gs[threadIdx.x] = gate_first;
+        for (int idx = threadIdx.x + kThreads; idx < n_gate4; idx += kThreads) gs[idx] = __ldg(gate_src(idx));
+    }
     __syncthreads();
 
     // ---- the group's value heads, one after another
@@ -266,14 +304,23 @@ gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
             TokenKQ<V> kq;
             token_kq<V>(yt, yt + DK, lane8, p.q_scale, normalize, kq);
             const size_t trow = (size_t)b * p.T + t;
-            const float alpha = p.alpha[trow * p.Hv + h];
+            float alpha = 0.0f;
+            if constexpr (!KDA) alpha = p.alpha[trow * p.Hv + h];
             const float beta = p.beta[trow * p.Hv + h];
             const uint16_t* vrow = yt + 2 * DK + j * p.dv;
+            if constexpr (KDA) {
+                float4 g[V];
+                load_gate_smem<V>(gs + ((size_t)t * p.group + j) * (DK / 4), lane8, g);
+#pragma unroll
+                for (int r = 0; r < R; ++r) kda_decay<V>(s[r], g);
+            }
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const int i = row0 + kRowsPerPass * r;
                 const float v_i = __uint_as_float((uint32_t)vrow[i] << 16);
-                const float o = row_step<V>(s[r], kq, v_i, alpha, beta);
+                float o;
+                if constexpr (KDA) o = delta_row_step<V>(s[r], kq, v_i, beta);
+                else o = row_step<V>(s[r], kq, v_i, alpha, beta);
                 if (p.out != nullptr && lane8 == 0)
                     store_out(p.out, ((trow * p.Hv) + h) * p.dv + i, o, out_bf16);
             }
@@ -287,67 +334,73 @@ gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
     }
 }
 
-template <int DK, int R>
+template <int DK, int R, bool KDA>
 static cudaError_t launch_conv_decode_t(const ConvDecodeParams& p, cudaStream_t s) {
     dim3 grid(p.Hk * p.row_blocks, p.B, 1);
-    const size_t smem = (size_t)p.T * p.CC * 2;
-    gdn_conv_decode_kernel<DK, R><<<grid, kThreads, smem, s>>>(p);
+    const size_t smem = (size_t)p.T * p.CC * 2 + (KDA ? (size_t)p.T * p.group * DK * 4 : 0);
+    gdn_conv_decode_kernel<DK, R, KDA><<<grid, kThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 
-template <int DK>
+template <int DK, bool KDA>
 static cudaError_t launch_conv_decode_r(const ConvDecodeParams& p, int rows_per_cta, cudaStream_t s) {
     switch (rows_per_cta) {
-        case 32: return launch_conv_decode_t<DK, 1>(p, s);
-        case 64: return launch_conv_decode_t<DK, 2>(p, s);
-        case 128: return launch_conv_decode_t<DK, 4>(p, s);
+        case 32: return launch_conv_decode_t<DK, 1, KDA>(p, s);
+        case 64: return launch_conv_decode_t<DK, 2, KDA>(p, s);
+        case 128: return launch_conv_decode_t<DK, 4, KDA>(p, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
-cudaError_t launch_conv_decode(const ConvDecodeParams& p, int dk, int rows_per_cta, cudaStream_t s) {
+template <bool KDA>
+static cudaError_t launch_conv_decode_k(const ConvDecodeParams& p, int dk, int rows_per_cta, cudaStream_t s) {
     switch (dk) {
-        case 32: return launch_conv_decode_r<32>(p, rows_per_cta, s);
-        case 64: return launch_conv_decode_r<64>(p, rows_per_cta, s);
-        case 128: return launch_conv_decode_r<128>(p, rows_per_cta, s);
+        case 32: return launch_conv_decode_r<32, KDA>(p, rows_per_cta, s);
+        case 64: return launch_conv_decode_r<64, KDA>(p, rows_per_cta, s);
+        case 128: return launch_conv_decode_r<128, KDA>(p, rows_per_cta, s);
     }
     return cudaErrorInvalidValue;
 }
 
-template <int DK, int R, bool GATHER>
+cudaError_t launch_conv_decode(const ConvDecodeParams& p, int dk, int rows_per_cta, bool kda, cudaStream_t s) {
+    return kda ? launch_conv_decode_k<true>(p, dk, rows_per_cta, s)
+               : launch_conv_decode_k<false>(p, dk, rows_per_cta, s);
+}
+
+template <int DK, int R, bool GATHER, bool KDA>
 static cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
     dim3 grid(p.dv / (kRowsPerPass * R), p.Hv, p.B);
-    gdn_decode_kernel<DK, R, GATHER><<<grid, kThreads, 0, s>>>(p);
+    gdn_decode_kernel<DK, R, GATHER, KDA><<<grid, kThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 
-template <int DK, bool GATHER>
+template <int DK, bool GATHER, bool KDA>
 static cudaError_t launch_decode_r(const DecodeParams& p, int rows_per_cta, cudaStream_t s) {
     switch (rows_per_cta) {
-        case 32: return launch_decode_t<DK, 1, GATHER>(p, s);
-        case 64: return launch_decode_t<DK, 2, GATHER>(p, s);
-        case 128: return launch_decode_t<DK, 4, GATHER>(p, s);
+        case 32: return launch_decode_t<DK, 1, GATHER, KDA>(p, s);
+        case 64: return launch_decode_t<DK, 2, GATHER, KDA>(p, s);
+        case 128: return launch_decode_t<DK, 4, GATHER, KDA>(p, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
-cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int gather,
-                          cudaStream_t s) {
-    if (gather) {
-        // commit replays short paths: one row pass per CTA keeps the grid wide
-        switch (dk) {
-            case 32: return launch_decode_r<32, true>(p, rows_per_cta, s);
-            case 64: return launch_decode_r<64, true>(p, rows_per_cta, s);
-            case 128: return launch_decode_r<128, true>(p, rows_per_cta, s);
-        }
-    } else {
-        switch (dk) {
-            case 32: return launch_decode_r<32, false>(p, rows_per_cta, s);
-            case 64: return launch_decode_r<64, false>(p, rows_per_cta, s);
-            case 128: return launch_decode_r<128, false>(p, rows_per_cta, s);
-        }
+template <bool GATHER, bool KDA>
+static cudaError_t launch_decode_k(const DecodeParams& p, int dk, int rows_per_cta, cudaStream_t s) {
+    switch (dk) {
+        case 32: return launch_decode_r<32, GATHER, KDA>(p, rows_per_cta, s);
+        case 64: return launch_decode_r<64, GATHER, KDA>(p, rows_per_cta, s);
+        case 128: return launch_decode_r<128, GATHER, KDA>(p, rows_per_cta, s);
     }
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int gather, bool kda,
+                          cudaStream_t s) {
+    // commit (gather) replays short paths: one row pass per CTA keeps the grid wide
+    if (gather) return kda ? launch_decode_k<true, true>(p, dk, rows_per_cta, s)
+                           : launch_decode_k<true, false>(p, dk, rows_per_cta, s);
+    return kda ? launch_decode_k<false, true>(p, dk, rows_per_cta, s)
+               : launch_decode_k<false, false>(p, dk, rows_per_cta, s);
 }
 
 template <int DK, int MB>

@@ -14,7 +14,7 @@ namespace gdn {
 // through an index map (commit replays a tree path).
 struct DecodeParams {
     const uint16_t* qkv;   // bf16 [B, Tsrc, C]
-    const float* alpha;    // [B, Tsrc, Hv]
+    const float* alpha;    // [B, Tsrc, Hv], or [B, Tsrc, Hv, dk] for KDA
     const float* beta;     // [B, Tsrc, Hv]
     float* state;          // [B, Hv, dv, dk]
     void* out;             // [B, T, Hv, dv] or nullptr
@@ -72,7 +72,7 @@ struct ConvDecodeParams {
     const uint16_t* w;        // [C, 4]
     const uint16_t* tail_in;  // [B, 4, C]
     uint16_t* tail_out;       // [B, 4, C] (equal to tail_in when row_blocks == 1)
-    const float* alpha;       // [B, T, Hv]
+    const float* alpha;       // [B, T, Hv], or [B, T, Hv, dk] for KDA
     const float* beta;        // [B, T, Hv]
     float* state;             // [B, Hv, dv, dk]
     void* out;                // [B, T, Hv, dv] or nullptr
@@ -100,11 +100,12 @@ int cuda_error(cudaError_t e, const char* what);
 int report_error(int code, const char* fmt, ...);
 
 // Launchers (return the cudaError_t of the launch).
-cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int gather,
+// kda: a decay per key channel (alpha [.., Hv, dk]) instead of one per head.
+cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int gather, bool kda,
                           cudaStream_t s);
 template <int MB>
 cudaError_t launch_tree(const TreeParamsT<MB>& p, int dk, cudaStream_t s);
-cudaError_t launch_conv_decode(const ConvDecodeParams& p, int dk, int rows_per_cta, cudaStream_t s);
+cudaError_t launch_conv_decode(const ConvDecodeParams& p, int dk, int rows_per_cta, bool kda, cudaStream_t s);
 constexpr int kFusedMaxTokens = 16;
 constexpr int kFusedMaxSmem = 48 * 1024;
 cudaError_t launch_conv(const ConvParams& p, cudaStream_t s);

@@ -150,6 +150,58 @@ __device__ __forceinline__ float row_step(float4 (&s)[V], const TokenKQ<V>& t, f
     return o;
 }
 
+// One KDA token on one state row (a decay per key channel, Kimi Delta
+// Attention): row i of S <- (S diag(g)) (I - beta k k^T) + beta v k^T, then
+// o = S q.  The decay comes first, s' = g o s; then on s'
+//   a = s'.k, c = s'.q,  u = beta * (v_i - a),  o_i = c + u * (k.q),
+//   s <- s' + u * k.
+// With g equal on every channel this is the same map as row_step; the
+// rounding order differs (the decay is applied before the dot products).
+// KDA (Kimi Delta Attention) replaces the scalar decay by one per key channel:
+// row i of S <- (S diag(g)) (I - beta k k^T) + beta v k^T, then o = S q.  The
+// decay comes first, s' = g o s (kda_decay, applied to all of a thread's rows
+// before their delta steps, so that the decay slice is live only briefly);
+// then on s' (delta_row_step)
+//   a = s'.k, c = s'.q,  u = beta * (v_i - a),  o_i = c + u * (k.q),
+//   s <- s' + u * k.
+// With g equal on every channel this is the same map as row_step; the
+// rounding order differs (the decay is applied before the dot products).
+
+// This lane's slice of a decay vector (dk fp32) staged in shared memory.
+template <int V>
+__device__ __forceinline__ void load_gate_smem(const float4* gate, int lane8, float4 (&g)[V]) {
+#pragma unroll
+    for (int m = 0; m < V; ++m) g[m] = gate[8 * m + lane8];
+}
+
+template <int V>
+__device__ __forceinline__ void kda_decay(float4 (&s)[V], const float4 (&g)[V]) {
+#pragma unroll
+    for (int m = 0; m < V; ++m) {
+        const float2 lo = __fmul2_rn(make_float2(g[m].x, g[m].y), make_float2(s[m].x, s[m].y));
+        const float2 hi = __fmul2_rn(make_float2(g[m].z, g[m].w), make_float2(s[m].z, s[m].w));
+        s[m] = make_float4(lo.x, lo.y, hi.x, hi.y);
+    }
+}
+
+template <int V>
+__device__ __forceinline__ float delta_row_step(float4 (&s)[V], const TokenKQ<V>& t, float v_i, float beta) {
+    const float a_part = lane_dot4<V>(s, t.k);
+    const float c_part = lane_dot4<V>(s, t.q);
+    const float a = group_sum8(a_part);
+    const float c = group_sum8(c_part);
+    const float u = __fmul_rn(beta, __fsub_rn(v_i, a));
+    const float o = __fmaf_rn(u, t.kq, c);
+    const float2 uu = make_float2(u, u);
+#pragma unroll
+    for (int m = 0; m < V; ++m) {
+        const float2 lo = __ffma2_rn(uu, make_float2(t.k[m][0], t.k[m][1]), make_float2(s[m].x, s[m].y));
+        const float2 hi = __ffma2_rn(uu, make_float2(t.k[m][2], t.k[m][3]), make_float2(s[m].z, s[m].w));
+        s[m] = make_float4(lo.x, lo.y, hi.x, hi.y);
+    }
+    return o;
+}
+
 __device__ __forceinline__ void store_out(void* out, size_t idx, float o, bool as_bf16) {
     if (as_bf16) {
         reinterpret_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(o);

@@ -46,6 +46,8 @@ EXPORTS = [
     "gdn_conv_step",
     "gdn_decode_step",
     "gdn_conv_decode_step",
+    "gdn_kda_decode_step",
+    "gdn_kda_conv_decode_step",
     "gdn_tree_verify",
     "gdn_tree_verify_batched",
     "gdn_commit_path",
@@ -91,6 +93,8 @@ def load(path: str = LIB_PATH):
             "gdn_conv_step": (ctypes.c_int, [I32, I32, I32, P, P, P, P, P, U32, P]),
             "gdn_decode_step": (ctypes.c_int, [SH, I32, P, P, P, P, P, F, U32, P]),
             "gdn_conv_decode_step": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, P, F, U32, P]),
+            "gdn_kda_decode_step": (ctypes.c_int, [SH, I32, P, P, P, P, P, F, U32, P]),
+            "gdn_kda_conv_decode_step": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, P, F, U32, P]),
             "gdn_tree_verify": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, F, U32, P]),
             "gdn_tree_verify_batched": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, F, U32, P]),
             "gdn_commit_path": (ctypes.c_int, [SH, I32, P, P, I32, P, P, P, P, P, P, U32, P]),
@@ -190,30 +194,39 @@ def conv_step(x: torch.Tensor, w: torch.Tensor, tail: torch.Tensor, y: torch.Ten
     return y
 
 
-def decode_step(qkv, alpha, beta, state, Hk, Hv, dk, dv, out=None, q_scale=1.0, normalize=True,
-                out_bf16=False) -> torch.Tensor:
-    """qkv bf16 [B,T,C], alpha/beta fp32 [B,T,Hv], state fp32 [B,Hv,dv,dk] (in place)."""
+def _decode(fn, qkv, alpha, beta, state, Hk, Hv, dk, dv, out, q_scale, normalize, out_bf16, gate_shape):
     B, T, C = qkv.shape
     if out is None:
         out = torch.empty((B, T, Hv, dv), dtype=torch.bfloat16 if out_bf16 else torch.float32,
                           device=qkv.device)
     sh = _shape(B, Hk, Hv, dk, dv)
-    rc = load().gdn_decode_step(ctypes.byref(sh), T,
-                                _dev(qkv, torch.bfloat16, "qkv", (B, T, packed_channels(Hk, Hv, dk, dv))),
-                                _dev(alpha, torch.float32, "alpha", (B, T, Hv)),
-                                _dev(beta, torch.float32, "beta", (B, T, Hv)),
-                                _dev(state, torch.float32, "state", (B, Hv, dv, dk)),
-                                _dev(out, torch.bfloat16 if out_bf16 else torch.float32, "out",
-                                     (B, T, Hv, dv)),
-                                float(q_scale), _flags(normalize, out_bf16), _stream())
-    _check(rc, "gdn_decode_step")
+    rc = getattr(load(), fn)(ctypes.byref(sh), T,
+                             _dev(qkv, torch.bfloat16, "qkv", (B, T, packed_channels(Hk, Hv, dk, dv))),
+                             _dev(alpha, torch.float32, "alpha", gate_shape(B, T)),
+                             _dev(beta, torch.float32, "beta", (B, T, Hv)),
+                             _dev(state, torch.float32, "state", (B, Hv, dv, dk)),
+                             _dev(out, torch.bfloat16 if out_bf16 else torch.float32, "out", (B, T, Hv, dv)),
+                             float(q_scale), _flags(normalize, out_bf16), _stream())
+    _check(rc, fn)
     return out
 
 
-def conv_decode_step(x, w, tail_in, alpha, beta, state, Hk, Hv, dk, dv, tail_out=None, out=None,
-                     q_scale=1.0, normalize=True, out_bf16=False) -> torch.Tensor:
-    """Fused conv + decode.  x bf16 [B,T,C] pre-conv, w bf16 [C,4], tail_in bf16
-    [B,4,C]; tail_out defaults to tail_in (in place).  Returns out [B,T,Hv,dv]."""
+def decode_step(qkv, alpha, beta, state, Hk, Hv, dk, dv, out=None, q_scale=1.0, normalize=True,
+                out_bf16=False) -> torch.Tensor:
+    """qkv bf16 [B,T,C], alpha/beta fp32 [B,T,Hv], state fp32 [B,Hv,dv,dk] (in place)."""
+    return _decode("gdn_decode_step", qkv, alpha, beta, state, Hk, Hv, dk, dv, out, q_scale, normalize,
+                   out_bf16, lambda B, T: (B, T, Hv))
+
+
+def kda_decode_step(qkv, alpha, beta, state, Hk, Hv, dk, dv, out=None, q_scale=1.0, normalize=True,
+                    out_bf16=False) -> torch.Tensor:
+    """KDA: alpha fp32 [B,T,Hv,dk] (a decay per key channel); the rest as decode_step."""
+    return _decode("gdn_kda_decode_step", qkv, alpha, beta, state, Hk, Hv, dk, dv, out, q_scale, normalize,
+                   out_bf16, lambda B, T: (B, T, Hv, dk))
+
+
+def _conv_decode(fn, x, w, tail_in, alpha, beta, state, Hk, Hv, dk, dv, tail_out, out, q_scale, normalize,
+                 out_bf16, gate_shape):
     B, T, C = x.shape
     if tail_out is None:
         tail_out = tail_in
@@ -222,18 +235,32 @@ def conv_decode_step(x, w, tail_in, alpha, beta, state, Hk, Hv, dk, dv, tail_out
                           device=x.device)
     sh = _shape(B, Hk, Hv, dk, dv)
     C_ = packed_channels(Hk, Hv, dk, dv)
-    rc = load().gdn_conv_decode_step(ctypes.byref(sh), T, _dev(x, torch.bfloat16, "x", (B, T, C_)),
-                                     _dev(w, torch.bfloat16, "w", (C_, GDN_CONV_W)),
-                                     _dev(tail_in, torch.bfloat16, "tail_in", (B, GDN_CONV_W, C_)),
-                                     _dev(tail_out, torch.bfloat16, "tail_out", (B, GDN_CONV_W, C_)),
-                                     _dev(alpha, torch.float32, "alpha", (B, T, Hv)),
-                                     _dev(beta, torch.float32, "beta", (B, T, Hv)),
-                                     _dev(state, torch.float32, "state", (B, Hv, dv, dk)),
-                                     _dev(out, torch.bfloat16 if out_bf16 else torch.float32, "out",
-                                          (B, T, Hv, dv)),
-                                     float(q_scale), _flags(normalize, out_bf16), _stream())
-    _check(rc, "gdn_conv_decode_step")
+    rc = getattr(load(), fn)(ctypes.byref(sh), T, _dev(x, torch.bfloat16, "x", (B, T, C_)),
+                             _dev(w, torch.bfloat16, "w", (C_, GDN_CONV_W)),
+                             _dev(tail_in, torch.bfloat16, "tail_in", (B, GDN_CONV_W, C_)),
+                             _dev(tail_out, torch.bfloat16, "tail_out", (B, GDN_CONV_W, C_)),
+                             _dev(alpha, torch.float32, "alpha", gate_shape(B, T)),
+                             _dev(beta, torch.float32, "beta", (B, T, Hv)),
+                             _dev(state, torch.float32, "state", (B, Hv, dv, dk)),
+                             _dev(out, torch.bfloat16 if out_bf16 else torch.float32, "out", (B, T, Hv, dv)),
+                             float(q_scale), _flags(normalize, out_bf16), _stream())
+    _check(rc, fn)
     return out
+
+
+def conv_decode_step(x, w, tail_in, alpha, beta, state, Hk, Hv, dk, dv, tail_out=None, out=None,
+                     q_scale=1.0, normalize=True, out_bf16=False) -> torch.Tensor:
+    """Fused conv + decode.  x bf16 [B,T,C] pre-conv, w bf16 [C,4], tail_in bf16
+    [B,4,C]; tail_out defaults to tail_in (in place).  Returns out [B,T,Hv,dv]."""
+    return _conv_decode("gdn_conv_decode_step", x, w, tail_in, alpha, beta, state, Hk, Hv, dk, dv, tail_out,
+                        out, q_scale, normalize, out_bf16, lambda B, T: (B, T, Hv))
+
+
+def kda_conv_decode_step(x, w, tail_in, alpha, beta, state, Hk, Hv, dk, dv, tail_out=None, out=None,
+                         q_scale=1.0, normalize=True, out_bf16=False) -> torch.Tensor:
+    """Fused conv + KDA decode: alpha fp32 [B,T,Hv,dk]; the rest as conv_decode_step."""
+    return _conv_decode("gdn_kda_conv_decode_step", x, w, tail_in, alpha, beta, state, Hk, Hv, dk, dv,
+                        tail_out, out, q_scale, normalize, out_bf16, lambda B, T: (B, T, Hv, dk))
 
 
 def tree_verify(parents, qkv, alpha, beta, state, Hk, Hv, dk, dv, out=None, q_scale=1.0,

@@ -174,6 +174,35 @@ int gdn_conv_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* x, c
                          void* stream);
 
 /*
+ * gdn_kda_decode_step -- gdn_decode_step with a decay per key channel (KDA,
+ * Kimi Delta Attention) instead of one per head:
+ *   S_h <- (S_h diag(a)) (I - beta k^ k^T) + beta v k^T,   out = S_h q^,
+ * with a = alpha[b, t, h, 0 .. dk-1] (column j of S, the j-th key channel,
+ * decays by a[j]).  With a[j] equal for all j this is gdn_decode_step's map;
+ * rounding differs (the decay is applied before the dot products).
+ *   alpha   fp32 [B, T, Hv, dk]; every other argument as for gdn_decode_step.
+ * Source: the metrale_model_arch API page lists a KDA mixer with a CPU
+ * reference (module index: glm5next_kda, glm5next_kda_ref, kimi_k3) and prints
+ * no update rule; the rule above is the gated delta rule of "Architecture"
+ * (v0.11.1) "The parts" with its scalar decay made diagonal on the key side.
+ */
+int gdn_kda_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv,
+                        const float* alpha, const float* beta, float* state, void* out,
+                        float q_scale, uint32_t flags, void* stream);
+
+/*
+ * gdn_kda_conv_decode_step -- gdn_conv_decode_step with the KDA step of
+ * gdn_kda_decode_step: conv + SiLU, L2-norm and the per-channel-decay delta
+ * step in one launch.  Results equal, bit for bit, gdn_conv_step followed by
+ * gdn_kda_decode_step.  alpha fp32 [B, T, Hv, dk]; every other argument and
+ * limit as for gdn_conv_decode_step.
+ */
+int gdn_kda_conv_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* x,
+                             const gdn_bf16* w, const gdn_bf16* tail_in, gdn_bf16* tail_out,
+                             const float* alpha, const float* beta, float* state, void* out,
+                             float q_scale, uint32_t flags, void* stream);
+
+/*
  * gdn_tree_verify -- outputs of every node of a draft tree in one pass.
  * Node n's state is the committed state advanced through the root..n path
  * (each node branches from its parent's state); out[n] = S_n q^_n.  The

@@ -62,8 +62,10 @@ def _sh(B=1, Hk=16, Hv=48, dk=128, dv=128):
 FAKE = 0x10000  # aligned, never dereferenced: every call below fails validation first
 
 
-def test_decode_validation(lib):
+@pytest.mark.parametrize("fn", ["gdn_decode_step", "gdn_kda_decode_step"])
+def test_decode_validation(lib, fn):
     P = ctypes.c_void_p
+    step = getattr(lib, fn)
     cases = [
         (_sh(dk=100), 1, FAKE, -2),
         (_sh(dv=48), 1, FAKE, -2),
@@ -73,15 +75,15 @@ def test_decode_validation(lib):
         (_sh(), 1, FAKE + 2, -6),           # misaligned qkv
     ]
     for sh, T, qkv, want in cases:
-        rc = lib.gdn_decode_step(ctypes.byref(sh), T, P(qkv), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+        rc = step(ctypes.byref(sh), T, P(qkv), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
                                  1.0, 1, None)
         assert rc == want, (sh.dk, sh.dv, sh.Hk, T, gdn.last_error())
         assert gdn.last_error()
     # null state
-    rc = lib.gdn_decode_step(ctypes.byref(_sh()), 1, P(FAKE), P(FAKE), P(FAKE), None, None, 1.0, 1, None)
+    rc = step(ctypes.byref(_sh()), 1, P(FAKE), P(FAKE), P(FAKE), None, None, 1.0, 1, None)
     assert rc == -1
     # unknown flag
-    rc = lib.gdn_decode_step(ctypes.byref(_sh()), 1, P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, 1.0,
+    rc = step(ctypes.byref(_sh()), 1, P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, 1.0,
                              0x80, None)
     assert rc == -1
 
@@ -170,16 +172,18 @@ def test_root_path_rejects(lib):
         gdn.tree_root_path(np.array([-1, 0], np.int32), 5)
 
 
-def test_conv_decode_validation(lib):
+@pytest.mark.parametrize("fn", ["gdn_conv_decode_step", "gdn_kda_conv_decode_step"])
+def test_conv_decode_validation(lib, fn):
     P = ctypes.c_void_p
+    step = getattr(lib, fn)
     sh = _sh(B=2)
     args = lambda T, ti, to: (ctypes.byref(sh), T, P(FAKE), P(FAKE), P(ti), P(to), P(FAKE), P(FAKE), P(FAKE), None,
                               1.0, 1, None)
-    assert lib.gdn_conv_decode_step(*args(17, FAKE, FAKE)) == -2   # more than 16 tokens
-    assert lib.gdn_conv_decode_step(*args(1, FAKE, FAKE + 16)) == -1  # overlapping tails
-    assert lib.gdn_conv_decode_step(*args(1, FAKE, FAKE + 8)) == -6   # misaligned tail_out
+    assert step(*args(17, FAKE, FAKE)) == -2   # more than 16 tokens
+    assert step(*args(1, FAKE, FAKE + 16)) == -1  # overlapping tails
+    assert step(*args(1, FAKE, FAKE + 8)) == -6   # misaligned tail_out
     big = gdn.gdn_shape(1, 1, 16, 128, 128)  # 2*128 + 16*128 channels x 16 tokens > 48 KB staging
-    assert lib.gdn_conv_decode_step(ctypes.byref(big), 16, P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+    assert step(ctypes.byref(big), 16, P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
                                      P(FAKE), None, 1.0, 1, None) == -2
 
 

@@ -79,6 +79,8 @@ def test_work_formulas():
                                                + 16 * 4 * 64 * 64 * 128)
     assert bench.prefill_flops(65) == 2 * bench.prefill_flops(64)
     assert bench.fp32_alu_peak_tflops(2070.0) == pytest.approx(152 * 128 * 2 * 2.07e9 / 1e12)
+    # KDA: alpha carries 128 fp32 decays per head.token instead of one
+    assert bench.kda_fused_bytes_per_launch(64) - bench.fused_bytes_per_launch(64) == 64 * 48 * 127 * 4
 
 
 def test_peaks_present_or_fallback():
@@ -87,7 +89,7 @@ def test_peaks_present_or_fallback():
     assert peaks["hbm_gbs"] > 1000 and peaks["bf16_tflops"] > 100
 
 
-@pytest.mark.parametrize("workload", ["batched", "tree"])
+@pytest.mark.parametrize("workload", ["batched", "tree", "kdabatch"])
 def test_reference_arm_line(workload):
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
                           "--workload", workload, "--steps", "2", "--warmup", "3"],
