@@ -67,6 +67,13 @@ def _load():
             "orc_kda_token": (None, [I, I, P, P, P, P, P, D, P]),
             "orc_kda_token_matrix": (None, [I, I, P, P, P, P, P, D, P]),
             "orc_kda_decode": (None, [I, I, I, I, I, I, P, P, P, P, P, D, I]),
+            "orc_fnv1a64": (ctypes.c_uint64, [P, ctypes.c_size_t]),
+            "orc_mix64": (ctypes.c_uint64, [ctypes.c_uint64]),
+            "orc_snapshot_checksum": (ctypes.c_uint64, [P, ctypes.c_size_t]),
+            "orc_snapshot_signature": (ctypes.c_uint64, [I, I, I, I, I]),
+            "orc_snapshot_bytes": (ctypes.c_size_t, [I, I, I, I, I]),
+            "orc_snapshot_save": (None, [I, I, I, I, I, I, I, P, P, P]),
+            "orc_snapshot_restore": (I, [I, I, I, I, I, I, I, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -263,3 +270,49 @@ def kda_decode(qkv, alpha, beta, state, Hk, Hv, dk, dv, q_scale=1.0, normalize=T
     _load().orc_kda_decode(B, T, Hk, Hv, dk, dv, _ptr(qkv), _ptr(alpha), _ptr(beta), _ptr(st), _ptr(out),
                            float(q_scale), int(bool(normalize)))
     return out, st
+
+
+# --------------------------------------------------------------------------
+# state snapshot / restore
+# --------------------------------------------------------------------------
+def fnv1a64(data: bytes) -> int:
+    buf = np.frombuffer(bytes(data), np.uint8).copy() if len(data) else np.zeros(1, np.uint8)
+    return int(_load().orc_fnv1a64(_ptr(buf), len(data)))
+
+
+def mix64(z: int) -> int:
+    return int(_load().orc_mix64(ctypes.c_uint64(z & 0xFFFFFFFFFFFFFFFF)))
+
+
+def snapshot_checksum(payload) -> int:
+    payload = np.ascontiguousarray(np.frombuffer(bytes(payload), np.uint8) if isinstance(payload, (bytes, bytearray))
+                                   else payload).view(np.uint8)
+    return int(_load().orc_snapshot_checksum(_ptr(payload), payload.size))
+
+
+def snapshot_signature(layers, Hk, Hv, dk, dv) -> int:
+    return int(_load().orc_snapshot_signature(layers, Hk, Hv, dk, dv))
+
+
+def snapshot_bytes(layers, Hk, Hv, dk, dv) -> int:
+    return int(_load().orc_snapshot_bytes(layers, Hk, Hv, dk, dv))
+
+
+def snapshot_save(state, tail, seq, Hk, Hv, dk, dv) -> np.ndarray:
+    """state fp32 [L,B,Hv,dv,dk], tail bf16 bits [L,B,4,C]: the blob of sequence seq (uint8)."""
+    state = _c(state, np.float32)
+    tail = _c(tail, np.uint16)
+    L, B = state.shape[0], state.shape[1]
+    blob = np.zeros(snapshot_bytes(L, Hk, Hv, dk, dv), np.uint8)
+    _load().orc_snapshot_save(L, B, Hk, Hv, dk, dv, int(seq), _ptr(state), _ptr(tail), _ptr(blob))
+    return blob
+
+
+def snapshot_restore(blob, state, tail, seq, Hk, Hv, dk, dv):
+    """Restore sequence seq in copies of state/tail; returns (rc, state, tail)."""
+    blob = np.ascontiguousarray(blob, np.uint8)
+    st = _c(state, np.float32).copy()
+    tl = _c(tail, np.uint16).copy()
+    rc = _load().orc_snapshot_restore(st.shape[0], st.shape[1], Hk, Hv, dk, dv, int(seq), _ptr(blob), _ptr(st),
+                                      _ptr(tl))
+    return int(rc), st, tl

@@ -10,6 +10,7 @@
 #include "gdn_oracle.h"
 
 #include <math.h>
+#include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -397,4 +398,131 @@ void orc_kda_decode(int B, int T, int Hk, int Hv, int dk, int dv, const uint16_t
     free(v);
     free(k);
     free(q);
+}
+
+/* ------------------------------------------------------------------------ */
+/* state snapshot / restore                                                   */
+/* ------------------------------------------------------------------------ */
+
+uint64_t orc_fnv1a64(const uint8_t* p, size_t n) {
+    uint64_t h = 0xcbf29ce484222325ULL;
+    for (size_t i = 0; i < n; ++i) {
+        h ^= (uint64_t)p[i];
+        h *= 0x100000001b3ULL;
+    }
+    return h;
+}
+
+uint64_t orc_mix64(uint64_t z) {
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ULL;
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebULL;
+    return z ^ (z >> 31);
+}
+
+uint64_t orc_snapshot_checksum(const uint8_t* payload, size_t bytes) {
+    uint64_t sum = 0;
+    for (size_t i = 0; i < bytes / 4; ++i) {
+        const uint64_t w = (uint64_t)payload[4 * i] | ((uint64_t)payload[4 * i + 1] << 8) |
+                           ((uint64_t)payload[4 * i + 2] << 16) | ((uint64_t)payload[4 * i + 3] << 24);
+        sum += orc_mix64(((uint64_t)i << 32) | w);
+    }
+    return sum;
+}
+
+static int snap_channels(int Hk, int Hv, int dk, int dv) { return 2 * Hk * dk + Hv * dv; }
+
+uint64_t orc_snapshot_signature(int layers, int Hk, int Hv, int dk, int dv) {
+    char text[256];
+    int n = snprintf(text, sizeof text, "gdn-snapshot/1;layers=%d;state:f32[%d,%d,%d];tail:bf16[4,%d]", layers,
+                     Hv, dv, dk, snap_channels(Hk, Hv, dk, dv));
+    return orc_fnv1a64((const uint8_t*)text, (size_t)n);
+}
+
+static size_t snap_state_bytes(int Hv, int dk, int dv) { return (size_t)Hv * dv * dk * 4; }
+static size_t snap_tail_bytes(int Hk, int Hv, int dk, int dv) {
+    return (size_t)4 * snap_channels(Hk, Hv, dk, dv) * 2;
+}
+
+size_t orc_snapshot_bytes(int layers, int Hk, int Hv, int dk, int dv) {
+    return 64 + (size_t)layers * (snap_state_bytes(Hv, dk, dv) + snap_tail_bytes(Hk, Hv, dk, dv));
+}
+
+static void put_u32(uint8_t* p, uint32_t v) {
+    for (int i = 0; i < 4; ++i) p[i] = (uint8_t)(v >> (8 * i));
+}
+static void put_u64(uint8_t* p, uint64_t v) {
+    for (int i = 0; i < 8; ++i) p[i] = (uint8_t)(v >> (8 * i));
+}
+static uint32_t get_u32(const uint8_t* p) {
+    uint32_t v = 0;
+    for (int i = 0; i < 4; ++i) v |= (uint32_t)p[i] << (8 * i);
+    return v;
+}
+static uint64_t get_u64(const uint8_t* p) {
+    uint64_t v = 0;
+    for (int i = 0; i < 8; ++i) v |= (uint64_t)p[i] << (8 * i);
+    return v;
+}
+
+/* fp32 and bf16 values are stored as their little-endian bit patterns */
+static void put_f32(uint8_t* p, float f) {
+    uint32_t bits;
+    memcpy(&bits, &f, 4);
+    put_u32(p, bits);
+}
+
+static void write_header(uint8_t* h, int layers, int Hk, int Hv, int dk, int dv, uint64_t checksum) {
+    memcpy(h, "GDNSNAP1", 8);
+    put_u32(h + 8, 1);
+    put_u32(h + 12, (uint32_t)layers);
+    put_u32(h + 16, (uint32_t)Hk);
+    put_u32(h + 20, (uint32_t)Hv);
+    put_u32(h + 24, (uint32_t)dk);
+    put_u32(h + 28, (uint32_t)dv);
+    put_u64(h + 32, orc_snapshot_signature(layers, Hk, Hv, dk, dv));
+    put_u64(h + 40, orc_snapshot_bytes(layers, Hk, Hv, dk, dv) - 64);
+    put_u64(h + 48, checksum);
+    put_u64(h + 56, 0);
+}
+
+void orc_snapshot_save(int layers, int B, int Hk, int Hv, int dk, int dv, int seq, const float* state,
+                       const uint16_t* tail, uint8_t* blob) {
+    const size_t S = (size_t)Hv * dv * dk;           /* state values of one sequence */
+    const size_t TL = (size_t)4 * snap_channels(Hk, Hv, dk, dv);  /* tail values of one sequence */
+    uint8_t* p = blob + 64;
+    for (int l = 0; l < layers; ++l) {
+        const float* st = state + ((size_t)l * B + seq) * S;
+        for (size_t i = 0; i < S; ++i, p += 4) put_f32(p, st[i]);
+        const uint16_t* tl = tail + ((size_t)l * B + seq) * TL;
+        for (size_t i = 0; i < TL; ++i, p += 2) {
+            p[0] = (uint8_t)(tl[i] & 0xff);
+            p[1] = (uint8_t)(tl[i] >> 8);
+        }
+    }
+    const size_t payload = orc_snapshot_bytes(layers, Hk, Hv, dk, dv) - 64;
+    write_header(blob, layers, Hk, Hv, dk, dv, orc_snapshot_checksum(blob + 64, payload));
+}
+
+int orc_snapshot_restore(int layers, int B, int Hk, int Hv, int dk, int dv, int seq, const uint8_t* blob,
+                         float* state, uint16_t* tail) {
+    const size_t payload = orc_snapshot_bytes(layers, Hk, Hv, dk, dv) - 64;
+    if (memcmp(blob, "GDNSNAP1", 8) != 0 || get_u32(blob + 8) != 1 || get_u32(blob + 12) != (uint32_t)layers ||
+        get_u32(blob + 16) != (uint32_t)Hk || get_u32(blob + 20) != (uint32_t)Hv ||
+        get_u32(blob + 24) != (uint32_t)dk || get_u32(blob + 28) != (uint32_t)dv ||
+        get_u64(blob + 32) != orc_snapshot_signature(layers, Hk, Hv, dk, dv) || get_u64(blob + 40) != payload)
+        return 1;
+    if (orc_snapshot_checksum(blob + 64, payload) != get_u64(blob + 48)) return 2;
+    const size_t S = (size_t)Hv * dv * dk;
+    const size_t TL = (size_t)4 * snap_channels(Hk, Hv, dk, dv);
+    const uint8_t* p = blob + 64;
+    for (int l = 0; l < layers; ++l) {
+        float* st = state + ((size_t)l * B + seq) * S;
+        for (size_t i = 0; i < S; ++i, p += 4) {
+            const uint32_t bits = get_u32(p);
+            memcpy(&st[i], &bits, 4);
+        }
+        uint16_t* tl = tail + ((size_t)l * B + seq) * TL;
+        for (size_t i = 0; i < TL; ++i, p += 2) tl[i] = (uint16_t)(p[0] | (p[1] << 8));
+    }
+    return 0;
 }

@@ -41,6 +41,7 @@
 #ifndef GDN_ORACLE_H
 #define GDN_ORACLE_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -133,6 +134,38 @@ void orc_kda_token_matrix(int dk, int dv, double* S, const double* k, const doub
 void orc_kda_decode(int B, int T, int Hk, int Hv, int dk, int dv, const uint16_t* qkv,
                     const float* alpha, const float* beta, double* state, double* out,
                     double q_scale, int normalize);
+
+/* ---- state snapshot / restore ----------------------------------------------
+ * A cache restores a sequence's recurrent state exactly ("Architecture"
+ * v0.14.2, section 8.1: the state has absorbed every token and has no inverse,
+ * so it is restored from a cache); a signature over section names, shapes and
+ * dtypes refuses a restore across models (section "ModelState: sections and
+ * views").  Blob format (little-endian):
+ *   header, 64 bytes: magic "GDNSNAP1" | u32 version 1 | u32 layers |
+ *     i32 Hk, Hv, dk, dv | u64 signature | u64 payload bytes | u64 checksum |
+ *     u64 0
+ *   payload: for each layer l in order, the sequence's state [Hv][dv][dk] fp32
+ *     then its conv tail [4][C] bf16, C = 2 Hk dk + Hv dv.
+ * signature = FNV-1a 64 (Fowler, Noll, Vo; offset basis 0xcbf29ce484222325,
+ *   prime 0x100000001b3) of the text
+ *   "gdn-snapshot/1;layers=<L>;state:f32[<Hv>,<dv>,<dk>];tail:bf16[4,<C>]".
+ * checksum = sum over the payload's 32-bit words w_i (i = 0, 1, ...) of
+ *   mix64((i << 32) | w_i), modulo 2^64, where mix64 is the output function
+ *   of Steele, Lea & Flood's SplitMix64 (shift 30, multiply
+ *   0xbf58476d1ce4e5b9, shift 27, multiply 0x94d049bb133111eb, shift 31). */
+uint64_t orc_fnv1a64(const uint8_t* p, size_t n);
+uint64_t orc_mix64(uint64_t z);
+uint64_t orc_snapshot_checksum(const uint8_t* payload, size_t bytes);
+uint64_t orc_snapshot_signature(int layers, int Hk, int Hv, int dk, int dv);
+size_t orc_snapshot_bytes(int layers, int Hk, int Hv, int dk, int dv);
+/* state [layers][B][Hv][dv][dk], tail [layers][B][4][C]; seq in [0, B). */
+void orc_snapshot_save(int layers, int B, int Hk, int Hv, int dk, int dv, int seq, const float* state,
+                       const uint16_t* tail, uint8_t* blob);
+/* Returns 0 and writes sequence seq's sections; 1 if the header does not
+ * match (magic, version, layers, shape, signature, payload size); 2 if the
+ * payload's checksum does not match.  Nothing is written unless 0. */
+int orc_snapshot_restore(int layers, int B, int Hk, int Hv, int dk, int dv, int seq, const uint8_t* blob,
+                         float* state, uint16_t* tail);
 
 #ifdef __cplusplus
 }

@@ -513,3 +513,97 @@ def test_kda_decode_vs_textbook():
                                            float(d["beta"][b, t, h]))
                 np.testing.assert_allclose(out[b, t, h], o, rtol=0, atol=1e-12)
     np.testing.assert_allclose(st, S, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# state snapshot / restore
+# ---------------------------------------------------------------------------
+def test_fnv1a64_published_vectors():
+    # test vectors of the FNV-1a 64-bit hash (Fowler, Noll, Vo)
+    assert oracle.fnv1a64(b"") == 0xCBF29CE484222325
+    assert oracle.fnv1a64(b"a") == 0xAF63DC4C8601EC8C
+    assert oracle.fnv1a64(b"foobar") == 0x85944171F73967E8
+
+
+def test_mix64_is_splitmix64_output():
+    # SplitMix64 seeded with 0: output n is mix64(n * golden gamma); its first
+    # outputs are published with the generator
+    g = 0x9E3779B97F4A7C15
+    assert oracle.mix64(g) == 0xE220A8397B1DCDAF
+    assert oracle.mix64(2 * g % 2 ** 64) == 0x6E789E6AA1B965F4
+    assert oracle.mix64(3 * g % 2 ** 64) == 0x06C45D188009454F
+    # and the seeded generator module's own implementation agrees
+    z = np.array([5, 2 ** 63 + 7, 0xDEADBEEF], np.uint64)
+    assert [oracle.mix64(int(x)) for x in z] == [int(v) for v in gen._mix64(z)]
+
+
+def test_snapshot_checksum_special_cases():
+    assert oracle.snapshot_checksum(b"") == 0
+    # one word: mix64 of the little-endian word at index 0
+    assert oracle.snapshot_checksum(bytes([1, 0, 0, 0])) == oracle.mix64(1)
+    assert oracle.snapshot_checksum(bytes([0x78, 0x56, 0x34, 0x12])) == oracle.mix64(0x12345678)
+    # two words: the second is keyed by its index in the high half
+    two = bytes([3, 0, 0, 0, 9, 0, 0, 0])
+    assert oracle.snapshot_checksum(two) == (oracle.mix64(3) + oracle.mix64((1 << 32) | 9)) % 2 ** 64
+    # position matters: swapping two different words changes the sum
+    assert oracle.snapshot_checksum(bytes([9, 0, 0, 0, 3, 0, 0, 0])) != oracle.snapshot_checksum(two)
+    # changing one word moves the sum by exactly that word's term
+    p = gen.uniform(3, "ck", 64)
+    raw = bytearray(np.asarray(p * 2 ** 32, np.uint64).astype(np.uint32).tobytes())
+    base = oracle.snapshot_checksum(raw)
+    w_old = int.from_bytes(raw[20:24], "little")
+    raw[20:24] = (w_old ^ 0x10).to_bytes(4, "little")
+    delta = oracle.mix64((5 << 32) | (w_old ^ 0x10)) - oracle.mix64((5 << 32) | w_old)
+    assert oracle.snapshot_checksum(raw) == (base + delta) % 2 ** 64
+
+
+def _snap_arrays(seed, L, B, s):
+    st = gen.normal(seed, "snap.state", L * B * s.Hv * s.dv * s.dk).astype(np.float32).reshape(L, B, s.Hv, s.dv, s.dk)
+    tl = gen.normal_bf16(seed, "snap.tail", L * B * 4 * s.C).reshape(L, B, 4, s.C)
+    return st, tl
+
+
+def test_snapshot_format_and_round_trip():
+    s = gen.Shape(1, 2, 4, 32, 64)
+    L, B, seq = 3, 4, 2
+    st, tl = _snap_arrays(5, L, B, s)
+    blob = oracle.snapshot_save(st, tl, seq, s.Hk, s.Hv, s.dk, s.dv)
+    assert blob.size == 64 + L * (s.Hv * s.dv * s.dk * 4 + 4 * s.C * 2)
+    h = blob[:64].tobytes()
+    assert h[:8] == b"GDNSNAP1"
+    assert [int.from_bytes(h[o:o + 4], "little") for o in range(8, 32, 4)] == [1, L, s.Hk, s.Hv, s.dk, s.dv]
+    text = f"gdn-snapshot/1;layers={L};state:f32[{s.Hv},{s.dv},{s.dk}];tail:bf16[4,{s.C}]".encode()
+    assert int.from_bytes(h[32:40], "little") == oracle.fnv1a64(text)
+    assert int.from_bytes(h[40:48], "little") == blob.size - 64
+    assert int.from_bytes(h[56:64], "little") == 0
+    # the payload is each layer's raw state bytes then raw tail bytes, in layer order
+    want = b"".join(st[l, seq].tobytes() + tl[l, seq].tobytes() for l in range(L))
+    assert blob[64:].tobytes() == want
+    assert int.from_bytes(h[48:56], "little") == oracle.snapshot_checksum(want)
+    # restore into other arrays: only sequence seq changes, bit for bit
+    st0, tl0 = _snap_arrays(6, L, B, s)
+    rc, st1, tl1 = oracle.snapshot_restore(blob, st0, tl0, seq, s.Hk, s.Hv, s.dk, s.dv)
+    assert rc == 0
+    assert st1[:, seq].tobytes() == st[:, seq].tobytes() and np.array_equal(tl1[:, seq], tl[:, seq])
+    others = [b for b in range(B) if b != seq]
+    assert np.array_equal(st1[:, others], st0[:, others]) and np.array_equal(tl1[:, others], tl0[:, others])
+
+
+def test_snapshot_restore_refusals():
+    s = gen.Shape(1, 2, 4, 32, 32)
+    L, B = 2, 2
+    st, tl = _snap_arrays(7, L, B, s)
+    blob = oracle.snapshot_save(st, tl, 1, s.Hk, s.Hv, s.dk, s.dv)
+    st0, tl0 = np.zeros_like(st), np.zeros_like(tl)
+    bad = blob.copy()
+    bad[64 + 1000] ^= 1                                  # one payload bit
+    rc, st1, tl1 = oracle.snapshot_restore(bad, st0, tl0, 1, s.Hk, s.Hv, s.dk, s.dv)
+    assert rc == 2 and not st1.any() and not tl1.any()
+    bad = blob.copy()
+    bad[0] ^= 1                                          # magic
+    assert oracle.snapshot_restore(bad, st0, tl0, 1, s.Hk, s.Hv, s.dk, s.dv)[0] == 1
+    # another model's shape: the signature and shape fields refuse it
+    assert oracle.snapshot_restore(blob, np.zeros((L, B, 4, 64, 16), np.float32),
+                                   np.zeros((L, B, 4, 2 * 2 * 16 + 4 * 64), np.uint16), 1, 2, 4, 16, 64)[0] == 1
+    assert oracle.snapshot_signature(2, 2, 4, 32, 32) != oracle.snapshot_signature(3, 2, 4, 32, 32)
+    assert oracle.snapshot_signature(2, 2, 4, 32, 32) != oracle.snapshot_signature(2, 1, 4, 32, 32)
