@@ -421,10 +421,10 @@ uint64_t orc_mix64(uint64_t z) {
 
 uint64_t orc_snapshot_checksum(const uint8_t* payload, size_t bytes) {
     uint64_t sum = 0;
-    for (size_t i = 0; i < bytes / 4; ++i) {
-        const uint64_t w = (uint64_t)payload[4 * i] | ((uint64_t)payload[4 * i + 1] << 8) |
-                           ((uint64_t)payload[4 * i + 2] << 16) | ((uint64_t)payload[4 * i + 3] << 24);
-        sum += orc_mix64(((uint64_t)i << 32) | w);
+    for (size_t j = 0; j < bytes / 8; ++j) {
+        uint64_t d = 0;
+        for (int b = 0; b < 8; ++b) d |= (uint64_t)payload[8 * j + b] << (8 * b);
+        sum += orc_mix64(d + (uint64_t)(j + 1) * 0x9e3779b97f4a7c15ULL);
     }
     return sum;
 }

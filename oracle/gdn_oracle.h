@@ -149,10 +149,12 @@ void orc_kda_decode(int B, int T, int Hk, int Hv, int dk, int dv, const uint16_t
  * signature = FNV-1a 64 (Fowler, Noll, Vo; offset basis 0xcbf29ce484222325,
  *   prime 0x100000001b3) of the text
  *   "gdn-snapshot/1;layers=<L>;state:f32[<Hv>,<dv>,<dk>];tail:bf16[4,<C>]".
- * checksum = sum over the payload's 32-bit words w_i (i = 0, 1, ...) of
- *   mix64((i << 32) | w_i), modulo 2^64, where mix64 is the output function
- *   of Steele, Lea & Flood's SplitMix64 (shift 30, multiply
- *   0xbf58476d1ce4e5b9, shift 27, multiply 0x94d049bb133111eb, shift 31). */
+ * checksum = sum over the payload's little-endian 64-bit words d_j
+ *   (j = 0, 1, ...) of mix64(d_j + (j + 1) * 0x9e3779b97f4a7c15), modulo
+ *   2^64, where mix64 is the output function of Steele, Lea & Flood's
+ *   SplitMix64 (shift 30, multiply 0xbf58476d1ce4e5b9, shift 27, multiply
+ *   0x94d049bb133111eb, shift 31) and 0x9e3779b97f4a7c15 its increment: for
+ *   an all-zero payload the terms are the generator's outputs from seed 0. */
 uint64_t orc_fnv1a64(const uint8_t* p, size_t n);
 uint64_t orc_mix64(uint64_t z);
 uint64_t orc_snapshot_checksum(const uint8_t* payload, size_t bytes);

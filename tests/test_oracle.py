@@ -538,22 +538,26 @@ def test_mix64_is_splitmix64_output():
 
 
 def test_snapshot_checksum_special_cases():
+    g = 0x9E3779B97F4A7C15
     assert oracle.snapshot_checksum(b"") == 0
-    # one word: mix64 of the little-endian word at index 0
-    assert oracle.snapshot_checksum(bytes([1, 0, 0, 0])) == oracle.mix64(1)
-    assert oracle.snapshot_checksum(bytes([0x78, 0x56, 0x34, 0x12])) == oracle.mix64(0x12345678)
-    # two words: the second is keyed by its index in the high half
-    two = bytes([3, 0, 0, 0, 9, 0, 0, 0])
-    assert oracle.snapshot_checksum(two) == (oracle.mix64(3) + oracle.mix64((1 << 32) | 9)) % 2 ** 64
+    # all-zero payloads: the terms are SplitMix64's published outputs from seed 0
+    assert oracle.snapshot_checksum(bytes(8)) == 0xE220A8397B1DCDAF
+    assert oracle.snapshot_checksum(bytes(16)) == (0xE220A8397B1DCDAF + 0x6E789E6AA1B965F4) % 2 ** 64
+    # one word: mix64 of the little-endian word plus the increment
+    one = bytes([0x08, 0x07, 0x06, 0x05, 0x04, 0x03, 0x02, 0x01])
+    assert oracle.snapshot_checksum(one) == oracle.mix64(0x0102030405060708 + g)
+    # two words: the second is keyed by index 2
+    two = bytes([3] + [0] * 7 + [9] + [0] * 7)
+    assert oracle.snapshot_checksum(two) == (oracle.mix64(3 + g) + oracle.mix64(9 + 2 * g)) % 2 ** 64
     # position matters: swapping two different words changes the sum
-    assert oracle.snapshot_checksum(bytes([9, 0, 0, 0, 3, 0, 0, 0])) != oracle.snapshot_checksum(two)
+    assert oracle.snapshot_checksum(bytes([9] + [0] * 7 + [3] + [0] * 7)) != oracle.snapshot_checksum(two)
     # changing one word moves the sum by exactly that word's term
     p = gen.uniform(3, "ck", 64)
     raw = bytearray(np.asarray(p * 2 ** 32, np.uint64).astype(np.uint32).tobytes())
     base = oracle.snapshot_checksum(raw)
-    w_old = int.from_bytes(raw[20:24], "little")
-    raw[20:24] = (w_old ^ 0x10).to_bytes(4, "little")
-    delta = oracle.mix64((5 << 32) | (w_old ^ 0x10)) - oracle.mix64((5 << 32) | w_old)
+    d_old = int.from_bytes(raw[40:48], "little")
+    raw[40:48] = (d_old ^ 0x10).to_bytes(8, "little")
+    delta = oracle.mix64(((d_old ^ 0x10) + 6 * g) % 2 ** 64) - oracle.mix64((d_old + 6 * g) % 2 ** 64)
     assert oracle.snapshot_checksum(raw) == (base + delta) % 2 ** 64
 
 
