@@ -714,6 +714,107 @@ class TreeBatch(Workload):
                 "launch": "eager, CUDA events around the launch"}
 
 
+SNAPSHOT_SOURCES = ["hybrid_linear_attention_conv_gb300/csrc/gdn_snapshot.cu",
+                    "hybrid_linear_attention_conv_gb300/csrc/gdn_internal.h"]
+
+
+def snapshot_payload_bytes(layers: int = 48) -> int:
+    """One sequence's sections over all layers: fp32 state + bf16 conv tail."""
+    return layers * (HV * DV * DK * 4 + 4 * C_QKV * 2)
+
+
+class Snapshot(Workload):
+    """Snapshot one sequence's recurrent sections (48 layers) and restore them."""
+
+    name = "snapshot"
+    flush = True
+    L, B = 48, 64
+    metric = "state snapshot save + restore throughput (one sequence, every layer, bit-exact)"
+    unit = "GB/s"
+    dtype = "u8"  # raw bytes: fp32 and bf16 bit patterns copied as they are
+
+    def __init__(self, device, seed: int, steps: int, layers: int = 48, seqs: int = 64):
+        super().__init__(device, seed)
+        torch, gdn = self.torch, self.gdn
+        self.L, self.B = layers, seqs
+        L, B = self.L, self.B
+        self.state = self.randn((L, B, HV, DV, DK), 0.1)
+        self.tail = self.randn((L, B, 4, C_QKV), 1.0, torch.bfloat16)
+        self.shape = gdn.gdn_shape(B, HK, HV, DK, DV)
+        self.nbytes = gdn.snapshot_bytes(L, HK, HV, DK, DV)
+        self.payload = snapshot_payload_bytes(L)
+        self.blob = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+        self.ws = torch.zeros(256, dtype=torch.uint8, device=device)
+        self.launches_per_step = 3       # gather; verify, scatter
+        # algorithmic bytes: save reads and writes the payload, restore reads and writes it
+        self.units_per_step = 4 * self.payload / 1e9
+        self.dominant = "save"                          # the save call: workspace reset + gather kernel
+        self.traffic_key = "gdn_snapshot_gather_kernel"
+        self.dominant_sources = SNAPSHOT_SOURCES
+        self.bound = "hbm"
+        self.dominant_work = 2 * self.payload + 64
+        self.step_bytes = 4 * self.payload
+
+    @property
+    def marks_per_step(self) -> int:
+        return 2
+
+    def _save(self, seq, blob):
+        P = ctypes.c_void_p
+        _call(self.lib.gdn_snapshot_save,
+              (ctypes.byref(self.shape), self.L, seq, P(self.state.data_ptr()), self.state.stride(0),
+               P(self.tail.data_ptr()), self.tail.stride(0), P(blob.data_ptr()), blob.numel(),
+               P(self.ws.data_ptr()), 256, self.sp), self.gdn)
+
+    def _restore(self, seq, blob):
+        P = ctypes.c_void_p
+        _call(self.lib.gdn_snapshot_restore,
+              (ctypes.byref(self.shape), self.L, seq, P(blob.data_ptr()), blob.numel(), P(self.state.data_ptr()),
+               self.state.stride(0), P(self.tail.data_ptr()), self.tail.stride(0), P(self.ws.data_ptr()), 256,
+               self.sp), self.gdn)
+
+    def step(self, i: int, rec: Recorder | None = None):
+        seq = i % self.B
+        if rec:
+            rec.begin(i)
+        self._save(seq, self.blob)
+        if rec:
+            rec.mark("save")
+        self._restore(seq, self.blob)
+        if rec:
+            rec.mark("restore")
+
+    def check_status(self):
+        status = int(self.ws[:4].view(self.torch.int32).item())
+        if status != 0:
+            raise RuntimeError(f"snapshot restore refused the blob (status {status})")
+
+    def e2e_setup(self):
+        # the blob lives in pinned host memory: the kernels write and read it there
+        self.h_blob = self.torch.empty(self.nbytes, dtype=self.torch.uint8, pin_memory=True)
+        self.e2e_h2d = self.nbytes
+        self.e2e_d2h = self.nbytes
+
+    def e2e_step(self, i: int):
+        seq = i % self.B
+        self._save(seq, self.h_blob)
+        self._restore(seq, self.h_blob)
+
+    def config(self=None) -> dict:
+        L = Snapshot.L if self is None else self.L
+        B = Snapshot.B if self is None else self.B
+        return {"workload": f"snapshot of one sequence's recurrent sections over {L} layers (fp32 state "
+                            f"48 x 128 x 128 + bf16 conv tail 4 x 10,240 per layer) out of {B} sequences held "
+                            "in HBM, into a device blob, then a verified restore of it",
+                "layers": L, "sequences": B, "blob_bytes": snapshot_payload_bytes(L) + 64,
+                "units": "algorithmic GB: payload read + written by save, read + written by restore",
+                "l2": "L2 flushed (256 MB write) before every step, outside the timed intervals",
+                "launch": "eager; CUDA events after the save call (workspace reset, gather) and after the "
+                          "restore call (reset, verify, scatter); the roofline times the save call",
+                "e2e": "the blob in pinned host memory instead, written and read by the kernels over the "
+                       "host link"}
+
+
 class Prefill(Workload):
     """Chunked prefill of 8,192 tokens, one layer."""
 
@@ -782,8 +883,9 @@ class Prefill(Workload):
 
 
 WORKLOADS = {"batched": Batched, "kdabatch": KdaBatched, "decode1": Decode1, "tree": Tree, "treebatch": TreeBatch,
-             "prefill": Prefill}
-DEFAULT_STEPS = {"batched": 100, "kdabatch": 100, "decode1": 1000, "tree": 200, "treebatch": 200, "prefill": 20}
+             "prefill": Prefill, "snapshot": Snapshot}
+DEFAULT_STEPS = {"batched": 100, "kdabatch": 100, "decode1": 1000, "tree": 200, "treebatch": 200, "prefill": 20,
+                 "snapshot": 50}
 
 
 # ---------------------------------------------------------------------------
@@ -819,14 +921,22 @@ class OracleSample:
             else:
                 self.units = 32 * s.Hv
                 self.desc = "tree conv + verify of one sequence's 32-node tree (root-path replay), one layer"
+        elif workload == "snapshot":
+            self.Ls = 4
+            n_st = self.Ls * s.Hv * s.dv * s.dk
+            self.snap_state = gen.normal(0, "snapshot.state", n_st).astype(np.float32).reshape(
+                self.Ls, 1, s.Hv, s.dv, s.dk)
+            self.snap_tail = gen.normal_bf16(0, "snapshot.tail", self.Ls * 4 * s.C).reshape(self.Ls, 1, 4, s.C)
+            self.units = 4 * snapshot_payload_bytes(self.Ls) / 1e9
+            self.desc = f"snapshot save + verified restore of one sequence over {self.Ls} of the 48 layers"
         else:
             self.Ts = 128
             self.d = gen.decode_inputs(0, s, self.Ts, tag="prefill")
             self.units = self.Ts * s.Hv
             self.desc = f"sequential prefill of {self.Ts} of the 8,192 tokens, all 48 value heads"
 
-    def run_once(self) -> int:
-        o, s, d = self.oracle, self.s, self.d
+    def run_once(self) -> float:
+        o, s, d = self.oracle, self.s, getattr(self, "d", None)
         if self.workload in ("batched", "decode1", "kdabatch"):
             y, _ = o.conv_linear(self.c["x"], self.c["w"], self.c["tail"])
             step = o.kda_decode if self.workload == "kdabatch" else o.decode
@@ -838,6 +948,10 @@ class OracleSample:
                 return self.units
             o.commit(self.parents, self.path, y, d["alpha"][0], d["beta"][0], d["state"][0], s.Hk, s.Hv,
                      s.dk, s.dv, x_tree=self.c["x"][0], tail=self.c["tail"][0])
+        elif self.workload == "snapshot":
+            blob = o.snapshot_save(self.snap_state, self.snap_tail, 0, s.Hk, s.Hv, s.dk, s.dv)
+            rc, _, _ = o.snapshot_restore(blob, self.snap_state, self.snap_tail, 0, s.Hk, s.Hv, s.dk, s.dv)
+            assert rc == 0
         else:
             o.prefill(d["qkv"], d["alpha"], d["beta"], d["state"], s.Hk, s.Hv, s.dk, s.dv)
         return self.units
@@ -845,7 +959,7 @@ class OracleSample:
 
 def cpu_oracle_sample(workload: str, seconds: float) -> dict:
     smp = OracleSample(workload)
-    n, units = 0, 0
+    n, units = 0, 0.0
     t0 = time.perf_counter()
     while True:
         units += smp.run_once()
@@ -853,7 +967,7 @@ def cpu_oracle_sample(workload: str, seconds: float) -> dict:
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    return {"value": units / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": units / el, "unit": getattr(WORKLOADS[workload], "unit", UNIT), "cores": 1, "kind": "oracle",
             "sample": f"{n} x ({smp.desc}), 27B head shape, fp64 C oracle, single thread, {el:.1f} s"}
 
 
@@ -876,6 +990,8 @@ def run_ours(args) -> dict | None:
     cls = WORKLOADS[args.workload]
     if issubclass(cls, Batched):
         wl = cls(device, 1234 + rank, args.steps + args.warmup, layers=args.layers)
+    elif cls is Snapshot:
+        wl = cls(device, 1234 + rank, args.steps + args.warmup, layers=args.layers, seqs=args.seqs)
     else:
         wl = cls(device, 1234 + rank, args.steps + args.warmup)
     torch.cuda.synchronize()
@@ -946,7 +1062,7 @@ def run_ours(args) -> dict | None:
         mhz = float(peaks.get("sm_max_mhz", 2070.0))
         peak, unit = fp32_alu_peak_tflops(mhz), "TFLOP/s"
         peak_kind = f"derived fp32 FMA peak: {SMS} SMs x {FP32_LANES_PER_SM} lanes x 2 x {mhz:.0f} MHz"
-    traffic = ncu_traffic(wl.dominant, wl.dominant_sources)
+    traffic = ncu_traffic(getattr(wl, "traffic_key", wl.dominant), wl.dominant_sources)
     step_gbs = wl.step_bytes * args.steps / total_s / 1e9
     roof = {"bound": wl.bound, "kernel": wl.dominant, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": achieved / peak, "peak_kind": peak_kind, "avg_launch_us": dom_avg_s * 1e6,
@@ -954,10 +1070,11 @@ def run_ours(args) -> dict | None:
             "work_unit": "bytes" if wl.bound == "hbm" else "flops", "traffic": traffic}
     if wl.bound == "hbm":
         roof["frac_nominal_8tbs"] = achieved / NOMINAL_HBM_GBS
+    metric, unit_v = getattr(wl, "metric", METRIC), getattr(wl, "unit", UNIT)
     line = {
-        "metric": METRIC,
+        "metric": metric,
         "value": agg["value"],
-        "unit": UNIT,
+        "unit": unit_v,
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
@@ -965,14 +1082,14 @@ def run_ours(args) -> dict | None:
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": getattr(wl, "dtype", "f32"),
         "data": "synthetic (seeded device RNG; 27B head shape, random-init states)",
         "config": wl.config(),
         "hbm_gbs_step": step_gbs,
         "hbm_frac_step": step_gbs / float(peaks["hbm_gbs"]),
         "roofline": roof,
         "clocks": clk,
-        "e2e": {"value": e2e["value"], "unit": UNIT, "h2d_bytes_per_step": wl.e2e_h2d,
+        "e2e": {"value": e2e["value"], "unit": unit_v, "h2d_bytes_per_step": wl.e2e_h2d,
                 "d2h_bytes_per_step": wl.e2e_d2h, "ms_per_step": e2e_total * 1e3 / args.steps},
         "gpu_launches": wl.launches_per_step * args.steps,
     }
@@ -995,15 +1112,17 @@ def run_reference(args) -> dict | None:
     el = time.perf_counter() - t0
     value = units / el
     sample = f"each step: {smp.desc}, 27B head shape, fp64 C oracle, single thread"
-    cfg = WORKLOADS[args.workload].config()
+    cls = WORKLOADS[args.workload]
+    cfg = cls.config()
+    metric, unit = getattr(cls, "metric", METRIC), getattr(cls, "unit", UNIT)
     return {
         "impl": "reference",
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": getattr(cls, "dtype", "f64"), "data": "synthetic",
         "config": cfg,
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
-        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
 
@@ -1017,6 +1136,8 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=48,
                     help="GDN layers in the batched workload (48 = the 27B model; fewer only for "
                          "profiling small cases)")
+    ap.add_argument("--seqs", type=int, default=64,
+                    help="sequences held in HBM by the snapshot workload (fewer only for profiling small cases)")
     ap.add_argument("--eager", action="store_true",
                     help="launch the batched step eagerly with an event after every kernel instead of "
                          "replaying it as a CUDA graph")

@@ -19,7 +19,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgdn.so")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 
-SOURCES = ["gdn_api.cu", "gdn_decode.cu", "gdn_conv.cu", "gdn_prefill.cu"]
+SOURCES = ["gdn_api.cu", "gdn_decode.cu", "gdn_conv.cu", "gdn_prefill.cu", "gdn_snapshot.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
               "-I", INCLUDE, "-I", CSRC] + ARCH

@@ -178,6 +178,12 @@ namespace gdn {
 
 int cuda_error(cudaError_t e, const char* what) { return cuda_fail(e, what); }
 
+int check_shape_arg(const gdn_shape* s, bool need_single) { return check_shape(s, need_single); }
+
+int check_pointer(const void* p, const char* name) { return check_ptr(p, name); }
+
+int device_sm_count() { return sm_count(); }
+
 int report_error(int code, const char* fmt, ...) {
     char buf[512];
     va_list ap;

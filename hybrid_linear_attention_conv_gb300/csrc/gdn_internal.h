@@ -98,6 +98,9 @@ int check_prefill_args(const gdn_shape* shape, int T, int chunk, const void* qkv
                        size_t workspace_bytes, uint32_t flags);
 int cuda_error(cudaError_t e, const char* what);
 int report_error(int code, const char* fmt, ...);
+int check_shape_arg(const gdn_shape* s, bool need_single);  // head sizes, Hv % Hk, grid limits
+int check_pointer(const void* p, const char* name);          // non-NULL and 16-byte aligned
+int device_sm_count();                                        // SMs of the current device (cached)
 
 // Launchers (return the cudaError_t of the launch).
 // kda: a decay per key channel (alpha [.., Hv, dk]) instead of one per head.

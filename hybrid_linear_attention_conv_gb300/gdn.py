@@ -54,6 +54,10 @@ EXPORTS = [
     "gdn_prefill_workspace_bytes",
     "gdn_chunk_prefill",
     "gdn_chunk_prefill_noalloc",
+    "gdn_snapshot_bytes",
+    "gdn_snapshot_signature",
+    "gdn_snapshot_save",
+    "gdn_snapshot_restore",
 ]
 
 
@@ -84,6 +88,7 @@ def load(path: str = LIB_PATH):
         lib = ctypes.CDLL(path)
         P, I32, U32, F, SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_float,
                               ctypes.c_size_t)
+        I64 = ctypes.c_int64
         SH = ctypes.POINTER(gdn_shape)
         sig = {
             "gdn_abi_version": (ctypes.c_int, []),
@@ -101,6 +106,10 @@ def load(path: str = LIB_PATH):
             "gdn_prefill_workspace_bytes": (SZ, [SH, I32, I32]),
             "gdn_chunk_prefill": (ctypes.c_int, [SH, I32, I32, P, P, P, P, P, P, SZ, F, U32, P]),
             "gdn_chunk_prefill_noalloc": (ctypes.c_int, [SH, I32, I32, P, P, P, P, P, F, U32, P]),
+            "gdn_snapshot_bytes": (SZ, [SH, I32]),
+            "gdn_snapshot_signature": (ctypes.c_uint64, [SH, I32]),
+            "gdn_snapshot_save": (ctypes.c_int, [SH, I32, I32, P, I64, P, I64, P, SZ, P, SZ, P]),
+            "gdn_snapshot_restore": (ctypes.c_int, [SH, I32, I32, P, SZ, P, I64, P, I64, P, SZ, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -351,6 +360,99 @@ def chunk_prefill(qkv, alpha, beta, state, Hk, Hv, dk, dv, out=None, workspace=N
                                   float(q_scale), _flags(normalize, out_bf16), _stream())
     _check(rc, "gdn_chunk_prefill")
     return out
+
+
+# ---------------------------------------------------------------------------
+# snapshot / restore of one sequence's recurrent sections
+# ---------------------------------------------------------------------------
+SNAPSHOT_WORKSPACE_BYTES = 256
+SNAPSHOT_STATUS = {0: "ok", 1: "header does not match this shape (magic/version/layers/shape/signature/size)",
+                   2: "payload checksum does not match"}
+
+
+def snapshot_bytes(layers, Hk, Hv, dk, dv) -> int:
+    return int(load().gdn_snapshot_bytes(ctypes.byref(_shape(1, Hk, Hv, dk, dv)), int(layers)))
+
+
+def snapshot_signature(layers, Hk, Hv, dk, dv) -> int:
+    return int(load().gdn_snapshot_signature(ctypes.byref(_shape(1, Hk, Hv, dk, dv)), int(layers)))
+
+
+def _layered(t: torch.Tensor, dtype, name: str, inner) -> tuple[ctypes.c_void_p, int]:
+    """A [layers, *inner] CUDA tensor whose layers may be strided apart but are
+    each contiguous: (pointer, layer stride in elements)."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape[1:]) != tuple(inner):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected (layers, {', '.join(map(str, inner))})")
+    if not t[0].is_contiguous():
+        raise ValueError(f"each layer of {name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr()), int(t.stride(0))
+
+
+def _blob(t: torch.Tensor, name: str) -> ctypes.c_void_p:
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.uint8 or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous uint8 tensor")
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be device memory or pinned host memory")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def snapshot_save(state, tail, seq, Hk, Hv, dk, dv, dst=None, workspace=None, host=False) -> torch.Tensor:
+    """Blob of sequence `seq` from state fp32 [L,B,Hv,dv,dk] and tail bf16
+    [L,B,4,C].  dst: a uint8 tensor (device, or pinned host) of at least
+    snapshot_bytes(); by default a new device tensor (pinned host with host=True)."""
+    L, B = state.shape[0], state.shape[1]
+    C = packed_channels(Hk, Hv, dk, dv)
+    sp, ss = _layered(state, torch.float32, "state", (B, Hv, dv, dk))
+    tp, ts = _layered(tail, torch.bfloat16, "tail", (B, 4, C))
+    n = snapshot_bytes(L, Hk, Hv, dk, dv)
+    if dst is None:
+        dst = (torch.empty(n, dtype=torch.uint8, pin_memory=True) if host
+               else torch.empty(n, dtype=torch.uint8, device=state.device))
+    if workspace is None:
+        workspace = torch.empty(SNAPSHOT_WORKSPACE_BYTES, dtype=torch.uint8, device=state.device)
+    rc = load().gdn_snapshot_save(ctypes.byref(_shape(B, Hk, Hv, dk, dv)), L, int(seq), sp, ss, tp, ts,
+                                  _blob(dst, "dst"), dst.numel(), _dev(workspace, torch.uint8, "workspace"),
+                                  workspace.numel(), _stream())
+    _check(rc, "gdn_snapshot_save")
+    return dst
+
+
+def snapshot_restore(src, state, tail, seq, Hk, Hv, dk, dv, workspace=None, check=True) -> int:
+    """Verify the blob `src` and write it into sequence `seq` of state/tail.
+    With check=True, synchronise and raise GdnError when the device refused
+    the blob (nothing is written then); return the status word (0 = done)."""
+    L, B = state.shape[0], state.shape[1]
+    C = packed_channels(Hk, Hv, dk, dv)
+    sp, ss = _layered(state, torch.float32, "state", (B, Hv, dv, dk))
+    tp, ts = _layered(tail, torch.bfloat16, "tail", (B, 4, C))
+    if workspace is None:
+        workspace = torch.empty(SNAPSHOT_WORKSPACE_BYTES, dtype=torch.uint8, device=state.device)
+    rc = load().gdn_snapshot_restore(ctypes.byref(_shape(B, Hk, Hv, dk, dv)), L, int(seq), _blob(src, "src"),
+                                     src.numel(), sp, ss, tp, ts, _dev(workspace, torch.uint8, "workspace"),
+                                     workspace.numel(), _stream())
+    _check(rc, "gdn_snapshot_restore")
+    if not check:
+        return 0
+    torch.cuda.current_stream().synchronize()
+    status = int(workspace[:4].view(torch.int32).item())
+    if status != 0:
+        raise GdnError(-100 - status, "gdn_snapshot_restore", SNAPSHOT_STATUS.get(status, str(status)))
+    return status
+
+
+def write_snapshot_file(blob: torch.Tensor, path: str) -> None:
+    """Write a blob to a file as it is (the format carries its own header)."""
+    blob.detach().cpu().numpy().tofile(path)
+
+
+def read_snapshot_file(path: str, pinned: bool = True) -> torch.Tensor:
+    """Read a blob file into (pinned) host memory, ready for snapshot_restore."""
+    t = torch.from_numpy(np.fromfile(path, dtype=np.uint8))
+    return t.pin_memory() if pinned else t
 
 
 # ---------------------------------------------------------------------------

@@ -316,6 +316,59 @@ int gdn_chunk_prefill_noalloc(const gdn_shape* shape, int32_t T, int32_t chunk, 
                               const float* alpha, const float* beta, float* state, void* out,
                               float q_scale, uint32_t flags, void* stream);
 
+/*
+ * ---- Snapshot and restore of one sequence's recurrent sections -------------
+ * A cache restores a sequence's state exactly: the recurrent state has
+ * absorbed every token and cannot be undone, so it is restored rather than
+ * recomputed ("Architecture" v0.14.2 section 8.1), and a signature over the
+ * sections' names, shapes and dtypes refuses a restore across models (same
+ * page, "ModelState: sections and views").  The sections of a sequence are,
+ * for each of `layers` layers in order, its fp32 state [Hv, dv, dk] and its
+ * bf16 conv tail [4, C_qkv].
+ *
+ * Blob (little-endian), gdn_snapshot_bytes() long:
+ *   bytes  0..63  header: "GDNSNAP1" | u32 version 1 | u32 layers |
+ *                 i32 Hk, Hv, dk, dv | u64 signature | u64 payload bytes |
+ *                 u64 checksum | u64 0
+ *   bytes 64..    payload: layer 0 state, layer 0 tail, layer 1 state, ...
+ *                 (raw bits: the restore is bit-exact).
+ *   signature  FNV-1a 64 of the text
+ *              "gdn-snapshot/1;layers=<L>;state:f32[<Hv>,<dv>,<dk>];tail:bf16[4,<C>]".
+ *   checksum   sum over the payload's 64-bit words d_j (j = 0, 1, ...) of
+ *              mix64(d_j + (j + 1) * 0x9e3779b97f4a7c15) modulo 2^64, mix64
+ *              being SplitMix64's output function and the constant its
+ *              increment.
+ *
+ * Arrays: layer l's state is at state + l * state_layer_stride (fp32
+ * elements), laid out [B, Hv, dv, dk]; its tail at tail + l *
+ * tail_layer_stride (bf16 elements), [B, 4, C_qkv]; strides are multiples of
+ * 16 bytes and at least one layer's array (any value when layers == 1).
+ * `seq` in [0, shape->B) picks the sequence.  The blob may be device memory
+ * or pinned host memory mapped into the device's address space (the kernels
+ * read and write it directly); pageable host memory is refused.
+ * workspace  device, >= 256 bytes, 256-byte aligned, caller-owned.  Its int32
+ * at offset 0 is the call's status (read it after the stream synchronises):
+ *   0  done;  1  restore refused: the blob's header (magic, version, layers,
+ *   shape, signature, size) is not this shape's;  2  restore refused: the
+ *   payload's checksum does not match the header's.  A refused restore writes
+ *   nothing.
+ */
+size_t gdn_snapshot_bytes(const gdn_shape* shape, int32_t layers);       /* 0 on a bad shape */
+uint64_t gdn_snapshot_signature(const gdn_shape* shape, int32_t layers); /* 0 on a bad shape */
+
+/* gdn_snapshot_save -- write sequence seq's sections into the blob dst. */
+int gdn_snapshot_save(const gdn_shape* shape, int32_t layers, int32_t seq, const float* state,
+                      int64_t state_layer_stride, const gdn_bf16* tail, int64_t tail_layer_stride,
+                      void* dst, size_t dst_bytes, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
+/* gdn_snapshot_restore -- verify the blob src (header and checksum, on the
+ * device) and, only if it verifies, write it into sequence seq's sections. */
+int gdn_snapshot_restore(const gdn_shape* shape, int32_t layers, int32_t seq, const void* src,
+                         size_t src_bytes, float* state, int64_t state_layer_stride, gdn_bf16* tail,
+                         int64_t tail_layer_stride, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
 #ifdef __cplusplus
 }
 #endif

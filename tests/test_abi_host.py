@@ -204,3 +204,44 @@ def test_tree_verify_batched_validation(lib):
     assert call(3, 4, [4, 4, 3], ok_tree + ok_tree + [-1, 2, 0, 9]) == -3  # tree 2: parent after child
     assert "tree 2" in gdn.last_error()
     assert call(2, 65, [1, 1], [-1] * 130) == -3                 # capacity above 64
+
+
+# ---------------------------------------------------------------------------
+# snapshot / restore (host side: sizes, signature, refusals)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("L,shape", [(1, (2, 4, 32, 32)), (48, (16, 48, 128, 128)), (3, (2, 4, 32, 64))])
+def test_snapshot_sizes_and_signature_match_oracle(lib, L, shape):
+    Hk, Hv, dk, dv = shape
+    assert gdn.snapshot_bytes(L, Hk, Hv, dk, dv) == oracle.snapshot_bytes(L, Hk, Hv, dk, dv)
+    assert gdn.snapshot_signature(L, Hk, Hv, dk, dv) == oracle.snapshot_signature(L, Hk, Hv, dk, dv)
+
+
+def test_snapshot_validation(lib):
+    P = ctypes.c_void_p
+    sh = _sh(B=4)
+    need = gdn.snapshot_bytes(2, sh.Hk, sh.Hv, sh.dk, sh.dv)
+    s_el = 4 * sh.Hv * sh.dv * sh.dk
+    t_el = 4 * 4 * (2 * sh.Hk * sh.dk + sh.Hv * sh.dv)
+
+    def save(L=2, seq=1, ss=s_el, ts=t_el, dst=FAKE, n=need, ws=FAKE, wsn=256, shape=sh):
+        return lib.gdn_snapshot_save(ctypes.byref(shape), L, seq, P(FAKE), ss, P(FAKE), ts, P(dst), n, P(ws), wsn,
+                                     None)
+
+    def restore(L=2, seq=1, ss=s_el, ts=t_el, src=FAKE, n=need, ws=FAKE, wsn=256):
+        return lib.gdn_snapshot_restore(ctypes.byref(sh), L, seq, P(src), n, P(FAKE), ss, P(FAKE), ts, P(ws), wsn,
+                                        None)
+
+    assert save(L=0) == -1
+    assert save(seq=4) == -1 and "seq" in gdn.last_error()
+    assert save(seq=-1) == -1
+    assert save(ss=s_el - 4) == -1                      # layers would overlap
+    assert save(ts=t_el + 4) == -6                      # 8 bytes: not a multiple of 16
+    assert save(n=need - 1) == -1 and "needs" in gdn.last_error()
+    assert save(dst=FAKE + 8) == -6
+    assert save(ws=0) == -9
+    assert save(ws=FAKE + 16) == -6
+    assert save(wsn=255) == -9
+    assert save(shape=_sh(dk=100)) == -2
+    assert restore(n=need - 16) == -1
+    assert restore(seq=9) == -1
+    assert gdn.snapshot_bytes(1, 2, 4, 100, 32) == 0    # bad shape
