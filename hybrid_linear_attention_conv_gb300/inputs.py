@@ -201,3 +201,23 @@ def kda_inputs(seed: int, shape: Shape, T: int, tag: str = "kda") -> dict:
     d["alpha"] = (0.9 + 0.1 * uniform(seed, tag + ".alpha_vec", n)).astype(np.float32).reshape(
         shape.B, T, shape.Hv, shape.dk)
     return d
+
+
+def layer_inputs(seed: int, shape: Shape, T: int, tag: str = "layer") -> dict:
+    """Inputs of the layer's decode step around the mixer: pre-conv x, taps and
+    tail (as conv_inputs), the gate projections a, b bf16 [B,T,Hv] ~ N(0, 1),
+    the per-head parameters A_log = log(U(1, 16)) and dt_bias = the inverse
+    softplus of dt, log-uniform in [1e-3, 1e-1] (the published initialisation),
+    the output-gate projection z bf16 [B,T,Hv,dv] ~ N(0, 1), the norm weight
+    w fp32 [dv] ~ N(1, 0.1^2) and the fp32 state [B,Hv,dv,dk] ~ N(0, 0.1^2)."""
+    B, Hv, dv = shape.B, shape.Hv, shape.dv
+    d = conv_inputs(seed, B, T, shape.C, tag=tag + ".conv")
+    d["a"] = normal_bf16(seed, tag + ".a", (B, T, Hv))
+    d["b"] = normal_bf16(seed, tag + ".b", (B, T, Hv))
+    d["A_log"] = np.log(1.0 + 15.0 * uniform(seed, tag + ".A", Hv)).astype(np.float32)
+    dt = np.exp(np.log(1e-3) + (np.log(1e-1) - np.log(1e-3)) * uniform(seed, tag + ".dt", Hv))
+    d["dt_bias"] = (dt + np.log(-np.expm1(-dt))).astype(np.float32)
+    d["z"] = normal_bf16(seed, tag + ".z", (B, T, Hv, dv))
+    d["norm_w"] = (1.0 + 0.1 * normal(seed, tag + ".w", dv)).astype(np.float32)
+    d["state"] = normal_f32(seed, tag + ".state", (B, Hv, dv, shape.dk), 0.1)
+    return d

@@ -67,6 +67,11 @@ def _load():
             "orc_kda_token": (None, [I, I, P, P, P, P, P, D, P]),
             "orc_kda_token_matrix": (None, [I, I, P, P, P, P, P, D, P]),
             "orc_kda_decode": (None, [I, I, I, I, I, I, P, P, P, P, P, D, I]),
+            "orc_softplus": (D, [D]),
+            "orc_sigmoid": (D, [D]),
+            "orc_gates": (None, [I, I, P, P, P, P, P, P]),
+            "orc_gated_rmsnorm": (None, [I, P, P, P, D, P]),
+            "orc_layer_decode": (None, [I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, D, P, P, P, D, I]),
             "orc_fnv1a64": (ctypes.c_uint64, [P, ctypes.c_size_t]),
             "orc_mix64": (ctypes.c_uint64, [ctypes.c_uint64]),
             "orc_snapshot_checksum": (ctypes.c_uint64, [P, ctypes.c_size_t]),
@@ -316,3 +321,52 @@ def snapshot_restore(blob, state, tail, seq, Hk, Hv, dk, dv):
     rc = _load().orc_snapshot_restore(st.shape[0], st.shape[1], Hk, Hv, dk, dv, int(seq), _ptr(blob), _ptr(st),
                                       _ptr(tl))
     return int(rc), st, tl
+
+
+# --------------------------------------------------------------------------
+# gate front end and gated-norm output
+# --------------------------------------------------------------------------
+def softplus(x: float) -> float:
+    return float(_load().orc_softplus(float(x)))
+
+
+def sigmoid(x: float) -> float:
+    return float(_load().orc_sigmoid(float(x)))
+
+
+def gates_from_projections(a, b, A_log, dt_bias):
+    """a, b bf16 bits [..., Hv]; A_log, dt_bias fp32 [Hv] -> (alpha, beta) fp64 [..., Hv]."""
+    a = _c(a, np.uint16)
+    b = _c(b, np.uint16)
+    Hv = a.shape[-1]
+    n = a.size // Hv
+    al = np.empty(a.shape, np.float64)
+    be = np.empty(a.shape, np.float64)
+    _load().orc_gates(n, Hv, _ptr(a), _ptr(b), _ptr(_c(A_log, np.float32)), _ptr(_c(dt_bias, np.float32)),
+                      _ptr(al), _ptr(be))
+    return al, be
+
+
+def gated_rmsnorm(o, z, w, eps=1e-6):
+    """o fp64 [dv], z bf16 bits [dv], w fp32 [dv] -> y fp64 [dv]."""
+    o = _c(o, np.float64)
+    y = np.empty(o.size, np.float64)
+    _load().orc_gated_rmsnorm(o.size, _ptr(o), _ptr(_c(z, np.uint16)), _ptr(_c(w, np.float32)), float(eps),
+                              _ptr(y))
+    return y
+
+
+def layer_decode(x, conv_w, tail, a, b, A_log, dt_bias, z, norm_w, state, Hk, Hv, dk, dv, eps=1e-6,
+                 q_scale=1.0, normalize=True):
+    """The layer's decode step.  Returns (o, y, state, tail); inputs are not modified."""
+    x = _c(x, np.uint16)
+    B, T, C = x.shape
+    tl = _c(tail, np.uint16).copy()
+    st = _c(state, np.float64).copy()
+    o = np.empty((B, T, Hv, dv), np.float64)
+    y = np.empty((B, T, Hv, dv), np.float64)
+    _load().orc_layer_decode(B, T, Hk, Hv, dk, dv, _ptr(x), _ptr(_c(conv_w, np.uint16)), _ptr(tl),
+                             _ptr(_c(a, np.uint16)), _ptr(_c(b, np.uint16)), _ptr(_c(A_log, np.float32)),
+                             _ptr(_c(dt_bias, np.float32)), _ptr(_c(z, np.uint16)), _ptr(_c(norm_w, np.float32)),
+                             float(eps), _ptr(st), _ptr(o), _ptr(y), float(q_scale), int(bool(normalize)))
+    return o, y, st, tl

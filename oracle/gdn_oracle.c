@@ -526,3 +526,63 @@ int orc_snapshot_restore(int layers, int B, int Hk, int Hv, int dk, int dv, int 
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* gate front end and gated-norm output                                       */
+/* ------------------------------------------------------------------------ */
+
+double orc_softplus(double x) { return (x > 0.0 ? x : 0.0) + log1p(exp(-fabs(x))); }
+
+double orc_sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+void orc_gates(int n, int Hv, const uint16_t* a, const uint16_t* b, const float* A_log, const float* dt_bias,
+               double* alpha, double* beta) {
+    for (int t = 0; t < n; ++t)
+        for (int h = 0; h < Hv; ++h) {
+            const size_t i = (size_t)t * Hv + h;
+            const double dt = orc_softplus(orc_bf16_to_f64(a[i]) + (double)dt_bias[h]);
+            alpha[i] = exp(-exp((double)A_log[h]) * dt);
+            beta[i] = orc_sigmoid(orc_bf16_to_f64(b[i]));
+        }
+}
+
+void orc_gated_rmsnorm(int dv, const double* o, const uint16_t* z, const float* w, double eps, double* y) {
+    double ss = 0.0;
+    for (int i = 0; i < dv; ++i) ss += o[i] * o[i];
+    const double inv = 1.0 / sqrt(ss / dv + eps);
+    for (int i = 0; i < dv; ++i) y[i] = o[i] * inv * (double)w[i] * orc_silu(orc_bf16_to_f64(z[i]));
+}
+
+void orc_layer_decode(int B, int T, int Hk, int Hv, int dk, int dv, const uint16_t* x, const uint16_t* conv_w,
+                      uint16_t* tail, const uint16_t* a, const uint16_t* b, const float* A_log,
+                      const float* dt_bias, const uint16_t* z, const float* norm_w, double eps, double* state,
+                      double* o, double* y, double q_scale, int normalize) {
+    const size_t C = (size_t)2 * Hk * dk + (size_t)Hv * dv;
+    const int group = Hv / Hk;
+    const size_t n = (size_t)B * T;
+    double* yc = (double*)malloc(sizeof(double) * n * C);
+    uint16_t* qkv = (uint16_t*)malloc(sizeof(uint16_t) * n * C);
+    double* alpha = (double*)malloc(sizeof(double) * n * Hv);
+    double* beta = (double*)malloc(sizeof(double) * n * Hv);
+    double* q = (double*)malloc(sizeof(double) * (size_t)dk);
+    double* k = (double*)malloc(sizeof(double) * (size_t)dk);
+    double* v = (double*)malloc(sizeof(double) * (size_t)dv);
+    orc_conv_linear(B, T, (int)C, 4, x, conv_w, tail, yc);
+    orc_f64_to_bf16_n(yc, qkv, (int64_t)(n * C));       /* the conv output is stored as bf16 */
+    orc_gates((int)n, Hv, a, b, A_log, dt_bias, alpha, beta);
+    for (size_t tok = 0; tok < n; ++tok)
+        for (int h = 0; h < Hv; ++h) {
+            token_vectors(Hk, dk, dv, qkv + tok * C, h / group, h, q_scale, normalize, q, k, v);
+            double* S = state + ((tok / T) * Hv + h) * (size_t)dv * dk;
+            double* oh = o + (tok * Hv + h) * dv;
+            orc_delta_token(dk, dv, S, k, v, q, alpha[tok * Hv + h], beta[tok * Hv + h], oh);
+            orc_gated_rmsnorm(dv, oh, z + (tok * Hv + h) * dv, norm_w, eps, y + (tok * Hv + h) * dv);
+        }
+    free(v);
+    free(k);
+    free(q);
+    free(beta);
+    free(alpha);
+    free(qkv);
+    free(yc);
+}

@@ -135,6 +135,33 @@ void orc_kda_decode(int B, int T, int Hk, int Hv, int dk, int dv, const uint16_t
                     const float* alpha, const float* beta, double* state, double* out,
                     double q_scale, int normalize);
 
+/* ---- gate front end and gated-norm output (the layer around the mixer) -----
+ * The pages name the layer but print neither step; both are read from the
+ * published Gated DeltaNet layer (Yang, Kautz & Hatamizadeh 2024, as shipped
+ * with the Qwen3-Next models): per value head h, from bf16 projections a, b
+ * and fp32 parameters A_log[h], dt_bias[h]:
+ *     alpha = exp(-exp(A_log[h]) * softplus(a + dt_bias[h])),
+ *     beta  = sigmoid(b),
+ * and after the mixer, with bf16 projection z [dv] and fp32 weight w [dv]:
+ *     y_i = o_i / sqrt(mean_i(o_i^2) + eps) * w_i * SiLU(z_i).
+ * softplus(x) = log(1 + e^x), evaluated as max(x, 0) + log1p(e^-|x|). */
+double orc_softplus(double x);
+double orc_sigmoid(double x);
+/* a, b bf16 [n, Hv]; alpha, beta fp64 [n, Hv]. */
+void orc_gates(int n, int Hv, const uint16_t* a, const uint16_t* b, const float* A_log, const float* dt_bias,
+               double* alpha, double* beta);
+void orc_gated_rmsnorm(int dv, const double* o, const uint16_t* z, const float* w, double eps, double* y);
+/* The whole decode step of one layer for T tokens of B sequences:
+ * conv + SiLU (tail in/out, conv output rounded to bf16 as stored), gates
+ * from a/b, L2-norm, the delta step (state in/out), o = S q, then y.
+ *   x bf16 [B,T,C]; conv_w bf16 [C,4]; tail bf16 [B,4,C] in/out;
+ *   a, b bf16 [B,T,Hv]; A_log, dt_bias fp32 [Hv]; z bf16 [B,T,Hv,dv];
+ *   norm_w fp32 [dv]; state fp64 [B,Hv,dv,dk]; o, y fp64 [B,T,Hv,dv]. */
+void orc_layer_decode(int B, int T, int Hk, int Hv, int dk, int dv, const uint16_t* x, const uint16_t* conv_w,
+                      uint16_t* tail, const uint16_t* a, const uint16_t* b, const float* A_log,
+                      const float* dt_bias, const uint16_t* z, const float* norm_w, double eps, double* state,
+                      double* o, double* y, double q_scale, int normalize);
+
 /* ---- state snapshot / restore ----------------------------------------------
  * A cache restores a sequence's recurrent state exactly ("Architecture"
  * v0.14.2, section 8.1: the state has absorbed every token and has no inverse,

@@ -611,3 +611,86 @@ def test_snapshot_restore_refusals():
                                    np.zeros((L, B, 4, 2 * 2 * 16 + 4 * 64), np.uint16), 1, 2, 4, 16, 64)[0] == 1
     assert oracle.snapshot_signature(2, 2, 4, 32, 32) != oracle.snapshot_signature(3, 2, 4, 32, 32)
     assert oracle.snapshot_signature(2, 2, 4, 32, 32) != oracle.snapshot_signature(2, 1, 4, 32, 32)
+
+
+# ---------------------------------------------------------------------------
+# gate front end and gated-norm output
+# ---------------------------------------------------------------------------
+def test_softplus_and_sigmoid_closed_forms():
+    assert oracle.softplus(0.0) == pytest.approx(math.log(2.0), rel=0, abs=1e-16)
+    for x in (-40.0, -3.5, -0.25, 0.7, 5.0, 40.0):
+        # softplus(x) - softplus(-x) = x; sigmoid(x) + sigmoid(-x) = 1
+        assert oracle.softplus(x) - oracle.softplus(-x) == pytest.approx(x, rel=0, abs=1e-13)
+        assert oracle.sigmoid(x) + oracle.sigmoid(-x) == pytest.approx(1.0, rel=0, abs=1e-15)
+        # d/dx softplus = sigmoid (central difference)
+        h = 1e-5
+        assert (oracle.softplus(x + h) - oracle.softplus(x - h)) / (2 * h) == pytest.approx(oracle.sigmoid(x),
+                                                                                            abs=1e-9)
+    assert oracle.softplus(-40.0) == pytest.approx(math.exp(-40.0), rel=1e-12)
+    assert oracle.sigmoid(0.0) == 0.5
+
+
+def test_gates_special_values_and_power_form():
+    Hv = 4
+    bf = gen.f32_to_bf16_bits
+    a = bf(np.array([[0.0, 0.0, 1.5, -2.0]], np.float32))
+    b = bf(np.array([[0.0, 2.0, -1.0, 0.5]], np.float32))
+    A_log = np.array([0.0, math.log(2.0), 0.3, 1.7], np.float32)
+    dt_bias = np.array([0.0, 0.0, -4.0, 0.25], np.float32)
+    al, be = oracle.gates_from_projections(a, b, A_log, dt_bias)
+    assert al[0, 0] == pytest.approx(0.5, abs=1e-15)        # exp(-1 * ln 2)
+    # A_log = ln 2 rounded to fp32: alpha = 2^-(e^A_log), about 1/4
+    assert al[0, 1] == pytest.approx(2.0 ** -math.exp(float(A_log[1])), rel=1e-15)
+    assert be[0, 0] == 0.5
+    # alpha = (1 + e^(a + dt_bias)) ^ (-e^A_log); beta = 1 / (1 + e^-b)
+    av = gen.bf16_bits_to_f32(a).astype(np.float64)[0]
+    bv = gen.bf16_bits_to_f32(b).astype(np.float64)[0]
+    for h in range(Hv):
+        x = av[h] + float(dt_bias[h])
+        assert al[0, h] == pytest.approx((1.0 + math.exp(x)) ** (-math.exp(float(A_log[h]))), rel=1e-13)
+        assert be[0, h] == pytest.approx(1.0 / (1.0 + math.exp(-bv[h])), rel=1e-15)
+
+
+def test_gated_rmsnorm_invariants():
+    dv = 16
+    o = gen.normal(21, "rms.o", dv)
+    z = gen.normal_bf16(21, "rms.z", (dv,))
+    w = (1.0 + 0.1 * gen.normal(21, "rms.w", dv)).astype(np.float32)
+    zf = gen.bf16_bits_to_f32(z).astype(np.float64)
+    g = w.astype(np.float64) * zf / (1.0 + np.exp(-zf))            # w * SiLU(z)
+    y = oracle.gated_rmsnorm(o, z, w, eps=0.0)
+    # with eps = 0: y / (w SiLU(z)) has unit root-mean-square and o's direction
+    r = y / g
+    assert np.sqrt(np.mean(r ** 2)) == pytest.approx(1.0, abs=1e-13)
+    np.testing.assert_allclose(r * np.linalg.norm(o) / math.sqrt(dv), o, rtol=1e-12, atol=0)
+    # scale invariance, and eps acting as an additive floor on the mean square
+    np.testing.assert_allclose(oracle.gated_rmsnorm(7.5 * o, z, w, eps=0.0), y, rtol=1e-13, atol=0)
+    c = np.full(dv, 0.01)
+    y_c = oracle.gated_rmsnorm(c, z, w, eps=1e-4)
+    np.testing.assert_allclose(y_c, 0.01 / math.sqrt(1e-4 + 1e-4) * g, rtol=1e-13, atol=0)
+    # SiLU(0) = 0
+    assert np.all(oracle.gated_rmsnorm(o, np.zeros(dv, np.uint16), w) == 0.0)
+
+
+def test_layer_decode_is_conv_gates_decode_norm():
+    """The composed oracle equals its parts: the pinned conv, the pinned decode
+    (fed the gates rounded to fp32, hence the 1e-6 slack) and the norm."""
+    s = gen.Shape(2, 2, 4, 32, 32)
+    T = 3
+    d = gen.layer_inputs(22, s, T)
+    o, y, st, tl = oracle.layer_decode(d["x"], d["w"], d["tail"], d["a"], d["b"], d["A_log"], d["dt_bias"], d["z"],
+                                       d["norm_w"], d["state"], s.Hk, s.Hv, s.dk, s.dv)
+    yc, tail_ref = oracle.conv_linear(d["x"], d["w"], d["tail"])
+    assert np.array_equal(tl, tail_ref)
+    al, be = oracle.gates_from_projections(d["a"], d["b"], d["A_log"], d["dt_bias"])
+    o_ref, st_ref = oracle.decode(oracle.f64_to_bf16(yc), al.astype(np.float32), be.astype(np.float32), d["state"],
+                                  s.Hk, s.Hv, s.dk, s.dv)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-6)
+    np.testing.assert_allclose(st, st_ref, rtol=0, atol=1e-6)
+    for b_ in range(s.B):
+        for t in range(T):
+            for h in range(s.Hv):
+                np.testing.assert_array_equal(y[b_, t, h], oracle.gated_rmsnorm(o[b_, t, h], d["z"][b_, t, h],
+                                                                                d["norm_w"]))
+    # the gates the recipe draws decay (some heads strongly: A up to 16, dt up to 0.1)
+    assert 0.0 < al.min() and al.max() < 1.0
