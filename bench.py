@@ -30,6 +30,7 @@ import argparse
 import ctypes
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -368,17 +369,8 @@ class Batched(Workload):
         self.fn = self.lib.gdn_kda_conv_decode_step if self.kda else self.lib.gdn_conv_decode_step
         self.out = torch.empty((L, B, 1, HV, DV), dtype=torch.float32, device=device)
         self.shape = gdn.gdn_shape(B, HK, HV, DK, DV)
-        P = ctypes.c_void_p
-        self.args = []
-        for s in range(self.n_sets):
-            per = []
-            for l in range(L):
-                tl = P(self.tail[l].data_ptr())
-                per.append((ctypes.byref(self.shape), 1, P(self.x[s, l].data_ptr()), P(self.w[l].data_ptr()), tl,
-                            tl, P(self.alpha[s, l].data_ptr()), P(self.beta[s, l].data_ptr()),
-                            P(self.state[l].data_ptr()), P(self.out[l].data_ptr()), 1.0, gdn.GDN_NORMALIZE_QK,
-                            self.sp))
-            self.args.append(per)
+        self._extra_inputs()
+        self.args = [[self._args(s, l, self.sp) for l in range(L)] for s in range(self.n_sets)]
         self.launches_per_step = L
         self.units_per_step = L * B * HV
         self.dominant = "gdn_conv_decode_kernel[kda]" if self.kda else "gdn_conv_decode_kernel"
@@ -388,14 +380,20 @@ class Batched(Workload):
         self.dominant_work = per_launch
         self.step_bytes = L * per_launch
 
-    def _launch_all(self, s: int, sp):
+    def _extra_inputs(self):
+        """Inputs beyond the fused step's (the layer step's projections and parameters)."""
+
+    def _args(self, s: int, l: int, sp):
+        """C-ABI arguments of layer l's launch with input set s on stream sp."""
         P = ctypes.c_void_p
+        tl = P(self.tail[l].data_ptr())
+        return (ctypes.byref(self.shape), 1, P(self.x[s, l].data_ptr()), P(self.w[l].data_ptr()), tl, tl,
+                P(self.alpha[s, l].data_ptr()), P(self.beta[s, l].data_ptr()), P(self.state[l].data_ptr()),
+                P(self.out[l].data_ptr()), 1.0, self.gdn.GDN_NORMALIZE_QK, sp)
+
+    def _launch_all(self, s: int, sp):
         for l in range(self.L):
-            tl = P(self.tail[l].data_ptr())
-            _call(self.fn,
-                  (ctypes.byref(self.shape), 1, P(self.x[s, l].data_ptr()), P(self.w[l].data_ptr()), tl, tl,
-                   P(self.alpha[s, l].data_ptr()), P(self.beta[s, l].data_ptr()), P(self.state[l].data_ptr()),
-                   P(self.out[l].data_ptr()), 1.0, self.gdn.GDN_NORMALIZE_QK, sp), self.gdn)
+            _call(self.fn, self._args(s, l, sp), self.gdn)
 
     def capture(self):
         """One CUDA graph per input set holding the step's L launches (the
@@ -469,6 +467,81 @@ class Batched(Workload):
                            f"one CUDA graph per step ({L} launches), CUDA events around each replay")}
 
 
+def layer_bytes_per_launch(B: int, T: int = 1) -> int:
+    """HBM bytes of one layer decode launch: the fused step's bytes without the
+    fp32 gates and outputs, plus the a/b projections (bf16), the per-head
+    parameters, z (bf16), the norm weight and y (bf16)."""
+    state = B * HV * DV * DK * 4 * 2
+    conv = B * T * C_QKV * 2 + B * 3 * C_QKV * 2 + B * 4 * C_QKV * 2 + C_QKV * 4 * 2
+    around = B * T * HV * 2 * 2 + HV * 4 * 2 + B * T * HV * DV * 2 + DV * 4 + B * T * HV * DV * 2
+    return state + conv + around
+
+
+class LayerBatched(Batched):
+    """The batched decode through the layer step: gates from projections in
+    front, gated RMS norm after, y in bf16 (one launch per layer)."""
+
+    name = "layer"
+
+    def _extra_inputs(self):
+        torch = self.torch
+        L, B, bf = self.L, self.B, torch.bfloat16
+        self.fn = self.lib.gdn_layer_decode_step
+        self.a = self.randn((self.n_sets, L, B, 1, HV), 1.0, bf)
+        self.b = self.randn((self.n_sets, L, B, 1, HV), 1.0, bf)
+        self.A_log = torch.log(1.0 + 15.0 * torch.rand((L, HV), generator=self.gen, device=self.device))
+        dt = torch.exp(math.log(1e-3) + (math.log(1e-1) - math.log(1e-3)) *
+                       torch.rand((L, HV), generator=self.gen, device=self.device))
+        self.dt_bias = dt + torch.log(-torch.expm1(-dt))
+        self.z = self.randn((self.n_sets, L, B, 1, HV, DV), 1.0, bf)
+        self.norm_w = 1.0 + 0.1 * torch.randn((L, DV), generator=self.gen, device=self.device)
+        self.y = torch.empty((L, B, 1, HV, DV), dtype=bf, device=self.device)
+
+    def __init__(self, device, seed: int, steps: int, layers: int = 48):
+        super().__init__(device, seed, steps, layers)
+        self.dominant = "gdn_conv_decode_kernel[layer]"
+        self.dominant_work = layer_bytes_per_launch(self.B)
+        self.step_bytes = self.L * self.dominant_work
+
+    def _args(self, s: int, l: int, sp):
+        P = ctypes.c_void_p
+        tl = P(self.tail[l].data_ptr())
+        return (ctypes.byref(self.shape), 1, P(self.x[s, l].data_ptr()), P(self.w[l].data_ptr()), tl, tl,
+                P(self.a[s, l].data_ptr()), P(self.b[s, l].data_ptr()), P(self.A_log[l].data_ptr()),
+                P(self.dt_bias[l].data_ptr()), P(self.z[s, l].data_ptr()), P(self.norm_w[l].data_ptr()), 1e-6,
+                P(self.state[l].data_ptr()), None, P(self.y[l].data_ptr()), 1.0, self.gdn.GDN_NORMALIZE_QK, sp)
+
+    def e2e_setup(self):
+        torch = self.torch
+        self.h_x = self.x[0].cpu().pin_memory()
+        self.h_a = self.a[0].cpu().pin_memory()
+        self.h_b = self.b[0].cpu().pin_memory()
+        self.h_z = self.z[0].cpu().pin_memory()
+        self.h_y = torch.empty(self.y.shape, dtype=torch.bfloat16, pin_memory=True)
+        self.e2e_h2d = (self.h_x.numel() + self.h_a.numel() + self.h_b.numel() + self.h_z.numel()) * 2
+        self.e2e_d2h = self.h_y.numel() * 2
+
+    def e2e_step(self, i: int):
+        self.e2e_copy(self.x[0], self.h_x)
+        self.e2e_copy(self.a[0], self.h_a)
+        self.e2e_copy(self.b[0], self.h_b)
+        self.e2e_copy(self.z[0], self.h_z)
+        if getattr(self, "graphs", None):
+            self.graphs[0].replay()
+        else:
+            for args in self.args[0]:
+                _call(self.fn, args, self.gdn)
+        self.e2e_copy(self.h_y, self.y)
+
+    def config(self=None) -> dict:
+        L = Batched.L if self is None else self.L
+        cfg = Batched.config(self)
+        cfg["workload"] = (f"batched layer decode over {L} GDN layers: batch {Batched.B} sequences, 27B head "
+                           "shape; per layer one launch of conv + SiLU, gates from the a/b projections "
+                           "(A_log, dt_bias), L2-norm, the delta step and the gated RMS norm with z; y in bf16")
+        return cfg
+
+
 class KdaBatched(Batched):
     """The batched decode with the KDA step: a decay per key channel."""
 
@@ -505,6 +578,7 @@ class Decode1(Workload):
         self.launches_per_step = 1
         self.units_per_step = HV
         self.dominant = "gdn_conv_decode_kernel"
+        self.traffic_key = "gdn_conv_decode_kernel[b1]"
         self.dominant_sources = FUSED_SOURCES
         self.bound = "hbm"
         self.dominant_work = fused_bytes_per_launch(1)
@@ -882,9 +956,9 @@ class Prefill(Workload):
                 "launch": "eager, CUDA events around the launch"}
 
 
-WORKLOADS = {"batched": Batched, "kdabatch": KdaBatched, "decode1": Decode1, "tree": Tree, "treebatch": TreeBatch,
+WORKLOADS = {"batched": Batched, "kdabatch": KdaBatched, "layer": LayerBatched, "decode1": Decode1, "tree": Tree, "treebatch": TreeBatch,
              "prefill": Prefill, "snapshot": Snapshot}
-DEFAULT_STEPS = {"batched": 100, "kdabatch": 100, "decode1": 1000, "tree": 200, "treebatch": 200, "prefill": 20,
+DEFAULT_STEPS = {"batched": 100, "kdabatch": 100, "layer": 100, "decode1": 1000, "tree": 200, "treebatch": 200, "prefill": 20,
                  "snapshot": 50}
 
 
@@ -921,6 +995,11 @@ class OracleSample:
             else:
                 self.units = 32 * s.Hv
                 self.desc = "tree conv + verify of one sequence's 32-node tree (root-path replay), one layer"
+        elif workload == "layer":
+            self.d = gen.layer_inputs(0, s, 1)
+            self.state = self.d["state"].astype(np.float64)
+            self.units = s.Hv
+            self.desc = "the layer decode step (conv, gates, delta step, gated norm) of 1 sequence x 1 layer x 1 token"
         elif workload == "snapshot":
             self.Ls = 4
             n_st = self.Ls * s.Hv * s.dv * s.dk
@@ -948,6 +1027,9 @@ class OracleSample:
                 return self.units
             o.commit(self.parents, self.path, y, d["alpha"][0], d["beta"][0], d["state"][0], s.Hk, s.Hv,
                      s.dk, s.dv, x_tree=self.c["x"][0], tail=self.c["tail"][0])
+        elif self.workload == "layer":
+            _, _, self.state, _ = o.layer_decode(d["x"], d["w"], d["tail"], d["a"], d["b"], d["A_log"], d["dt_bias"],
+                                                 d["z"], d["norm_w"], self.state, s.Hk, s.Hv, s.dk, s.dv)
         elif self.workload == "snapshot":
             blob = o.snapshot_save(self.snap_state, self.snap_tail, 0, s.Hk, s.Hv, s.dk, s.dv)
             rc, _, _ = o.snapshot_restore(blob, self.snap_state, self.snap_tail, 0, s.Hk, s.Hv, s.dk, s.dv)

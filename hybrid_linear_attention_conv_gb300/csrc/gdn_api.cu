@@ -325,9 +325,13 @@ int gdn_kda_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, 
     return decode_impl(shape, T, qkv, alpha, beta, state, out, q_scale, flags, stream, true);
 }
 
+// The fused step: kind 0 plain, 1 KDA, 2 the layer step (gates from the
+// projections in `layer`, alpha/beta unused; gated-norm output to layer->y).
 static int conv_decode_impl(const gdn_shape* shape, int32_t T, const gdn_bf16* x, const gdn_bf16* w,
                             const gdn_bf16* tail_in, gdn_bf16* tail_out, const float* alpha, const float* beta,
-                            float* state, void* out, float q_scale, uint32_t flags, void* stream, bool kda) {
+                            float* state, void* out, float q_scale, uint32_t flags, void* stream, int kind,
+                            const LayerParams* layer = nullptr) {
+    const bool kda = kind == 1;
     int rc;
     if ((rc = check_shape(shape, false)) != GDN_OK) return rc;
     if ((rc = check_flags(flags)) != GDN_OK) return rc;
@@ -337,15 +341,16 @@ static int conv_decode_impl(const gdn_shape* shape, int32_t T, const gdn_bf16* x
     const int group = shape->Hv / shape->Hk;
     const int CC = 2 * shape->dk + group * shape->dv;
     // staged per token: the group's conv outputs (bf16) and, for KDA, its decay vectors (fp32)
-    const long per_token = (long)CC * 2 + (kda ? (long)group * shape->dk * 4 : 0);
+    const long per_token = (long)CC * 2 + (kda ? (long)group * shape->dk * 4 : 0) + (kind == 2 ? (long)group * 8 : 0);
     if ((long)T * per_token > kFusedMaxSmem)
         return fail(GDN_ERR_UNSUPPORTED_SHAPE, "T=%d x %ld staged bytes per key-head group exceed the fused "
                     "step's %d-byte staging", T, per_token, kFusedMaxSmem);
     if (shape->B == 0 || T == 0) return GDN_OK;  // nothing to do; pointers may be NULL
     if ((rc = check_ptr(x, "x")) || (rc = check_ptr(w, "w")) || (rc = check_ptr(tail_in, "tail_in")) ||
-        (rc = check_ptr(tail_out, "tail_out")) || (rc = check_ptr(alpha, "alpha")) ||
-        (rc = check_ptr(beta, "beta")) || (rc = check_ptr(state, "state")) || (rc = check_ptr(out, "out", false)))
+        (rc = check_ptr(tail_out, "tail_out")) || (rc = check_ptr(state, "state")) ||
+        (rc = check_ptr(out, "out", false)))
         return rc;
+    if (kind != 2 && ((rc = check_ptr(alpha, "alpha")) || (rc = check_ptr(beta, "beta")))) return rc;
     const int C = packed_channels(shape);
     const size_t tail_bytes = (size_t)shape->B * GDN_CONV_W * C * 2;
     const uintptr_t ti = reinterpret_cast<uintptr_t>(tail_in), to = reinterpret_cast<uintptr_t>(tail_out);
@@ -374,8 +379,9 @@ static int conv_decode_impl(const gdn_shape* shape, int32_t T, const gdn_bf16* x
     // Rows of each value head per CTA: all of them when the tail is updated in
     // place (one writer per tail entry); with distinct tails, split the rows
     // until every SM has a few CTAs.
+    if (layer != nullptr) p.layer = *layer;
     int row_blocks = 1;
-    if (ti != to) {
+    if (ti != to && kind != 2) {  // the layer step's norm needs every row of a head in one CTA
         const long want = 4L * sm_count();
         while (row_blocks < 4 && shape->dv / (row_blocks * 2) >= 32 &&
                (long)shape->Hk * shape->B * row_blocks < want)
@@ -383,22 +389,76 @@ static int conv_decode_impl(const gdn_shape* shape, int32_t T, const gdn_bf16* x
     }
     p.row_blocks = row_blocks;
     cudaError_t e =
-        launch_conv_decode(p, shape->dk, shape->dv / row_blocks, kda, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? GDN_OK : cuda_fail(e, kda ? "conv+KDA decode launch" : "conv+decode launch");
+        launch_conv_decode(p, shape->dk, shape->dv / row_blocks, kind, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GDN_OK
+                            : cuda_fail(e, kind == 1 ? "conv+KDA decode launch"
+                                                     : kind == 2 ? "layer decode launch" : "conv+decode launch");
 }
 
 int gdn_conv_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* x, const gdn_bf16* w,
                          const gdn_bf16* tail_in, gdn_bf16* tail_out, const float* alpha, const float* beta,
                          float* state, void* out, float q_scale, uint32_t flags, void* stream) {
     return conv_decode_impl(shape, T, x, w, tail_in, tail_out, alpha, beta, state, out, q_scale, flags, stream,
-                            false);
+                            0);
 }
 
 int gdn_kda_conv_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* x, const gdn_bf16* w,
                              const gdn_bf16* tail_in, gdn_bf16* tail_out, const float* alpha, const float* beta,
                              float* state, void* out, float q_scale, uint32_t flags, void* stream) {
     return conv_decode_impl(shape, T, x, w, tail_in, tail_out, alpha, beta, state, out, q_scale, flags, stream,
-                            true);
+                            1);
+}
+
+int gdn_layer_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* x, const gdn_bf16* conv_w,
+                          const gdn_bf16* tail_in, gdn_bf16* tail_out, const gdn_bf16* a, const gdn_bf16* b,
+                          const float* A_log, const float* dt_bias, const gdn_bf16* z, const float* norm_w,
+                          float norm_eps, float* state, float* o, gdn_bf16* y, float q_scale, uint32_t flags,
+                          void* stream) {
+    int rc;
+    if ((rc = check_shape(shape, false)) != GDN_OK) return rc;
+    if (flags & GDN_OUT_BF16)
+        return fail(GDN_ERR_INVALID_ARG, "the layer step writes y in bf16 and o in fp32; GDN_OUT_BF16 not allowed");
+    if (!(norm_eps >= 0.0f) || norm_eps > 1.0f)
+        return fail(GDN_ERR_INVALID_ARG, "norm_eps=%g outside [0, 1]", (double)norm_eps);
+    if (T < 0) return fail(GDN_ERR_INVALID_ARG, "T=%d < 0", T);
+    if (shape->B == 0 || T == 0) return GDN_OK;  // nothing to do; pointers may be NULL
+    if ((rc = check_ptr(a, "a")) || (rc = check_ptr(b, "b")) || (rc = check_ptr(A_log, "A_log")) ||
+        (rc = check_ptr(dt_bias, "dt_bias")) || (rc = check_ptr(z, "z")) || (rc = check_ptr(norm_w, "norm_w")) ||
+        (rc = check_ptr(y, "y")))
+        return rc;
+    LayerParams lp{};
+    lp.a = a;
+    lp.b = b;
+    lp.A_log = A_log;
+    lp.dt_bias = dt_bias;
+    lp.z = z;
+    lp.norm_w = norm_w;
+    lp.y = y;
+    lp.norm_eps = norm_eps;
+    return conv_decode_impl(shape, T, x, conv_w, tail_in, tail_out, nullptr, nullptr, state, o, q_scale, flags,
+                            stream, 2, &lp);
+}
+
+int gdn_gates(int64_t n, int32_t Hv, const gdn_bf16* a, const gdn_bf16* b, const float* A_log,
+              const float* dt_bias, float* alpha, float* beta, void* stream) {
+    int rc;
+    if (n < 0 || Hv < 1) return fail(GDN_ERR_INVALID_ARG, "n=%lld tokens, Hv=%d heads", (long long)n, Hv);
+    if (n == 0) return GDN_OK;
+    if ((rc = check_ptr(a, "a")) || (rc = check_ptr(b, "b")) || (rc = check_ptr(A_log, "A_log")) ||
+        (rc = check_ptr(dt_bias, "dt_bias")) || (rc = check_ptr(alpha, "alpha")) || (rc = check_ptr(beta, "beta")))
+        return rc;
+    if (n * (int64_t)Hv > (int64_t)1 << 38) return fail(GDN_ERR_INVALID_ARG, "n * Hv above 2^38");
+    GatesParams p{};
+    p.a = a;
+    p.b = b;
+    p.A_log = A_log;
+    p.dt_bias = dt_bias;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.n = n;
+    p.Hv = Hv;
+    cudaError_t e = launch_gates(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gates launch");
 }
 
 int gdn_tree_verify(const gdn_shape* shape, int32_t N, const int32_t* parents, const gdn_bf16* qkv,

@@ -18,6 +18,7 @@
 #include <cuda_runtime.h>
 
 #include "gdn_conv.cuh"
+#include "gdn_gates.cuh"
 #include "gdn_internal.h"
 #include "gdn_step.cuh"
 
@@ -75,6 +76,7 @@ gdn_decode_kernel(const __grid_constant__ DecodeParams p) {
 #pragma unroll
             for (int r = 0; r < R; ++r) kda_decay<V>(s[r], g);
         }
+        float my_o = 0.0f;  // lane l < R of a row group stores row r = l (all lanes hold the same o)
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const int i = row0 + kRowsPerPass * r;
@@ -82,9 +84,10 @@ gdn_decode_kernel(const __grid_constant__ DecodeParams p) {
             float o;
             if constexpr (KDA) o = delta_row_step<V>(s[r], kq, v_i, beta);
             else o = row_step<V>(s[r], kq, v_i, alpha, beta);
-            if (p.out != nullptr && lane8 == 0)
-                store_out(p.out, (((size_t)b * p.T + t) * p.Hv + h) * p.dv + i, o, out_bf16);
+            if (lane8 == r) my_o = o;
         }
+        if (p.out != nullptr && lane8 < R)
+            store_out(p.out, (((size_t)b * p.T + t) * p.Hv + h) * p.dv + row0 + kRowsPerPass * lane8, my_o, out_bf16);
     }
 
 #pragma unroll
@@ -221,9 +224,15 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
 // the shared step.  Every tail entry is written by one CTA only (row block 0);
 // with several row blocks the tail is read from tail_in and written to a
 // distinct tail_out, so no CTA reads an entry another CTA has overwritten.
-template <int DK, int R, bool KDA>
+// KIND 0: the step as it is; 1: KDA (a decay per key channel); 2: the layer
+// step -- gates computed from the token's projections in front, and the
+// gated RMS norm of each head's output after (the CTA holds all the head's
+// rows: one value-row block).
+template <int DK, int R, int KIND>
 __global__ void __launch_bounds__(kThreads, 2)
 gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
+    constexpr bool KDA = KIND == 1;
+    constexpr bool LAYER = KIND == 2;
     constexpr int V = DK / 32;
     extern __shared__ uint4 smem_y[];
     uint16_t* ys = reinterpret_cast<uint16_t*>(smem_y);  // [T][CC] bf16 conv outputs
@@ -284,11 +293,50 @@ gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
         if (threadIdx.x < n_gate4) gs[threadIdx.x] = gate_first;
         for (int idx = threadIdx.x + kThreads; idx < n_gate4; idx += kThreads) gs[idx] = __ldg(gate_src(idx));
     }
+    // layer: the group's (alpha, beta) per token and head, [T][group], computed once
+    float2* s_ab = reinterpret_cast<float2*>(ys + (size_t)p.T * p.CC);
+    if constexpr (LAYER) {
+        for (int idx = threadIdx.x; idx < p.T * p.group; idx += kThreads) {
+            const int t = idx / p.group, h = g * p.group + idx % p.group;
+            const size_t ti = ((size_t)b * p.T + t) * p.Hv + h;
+            float al, be;
+            gate_pair(bf16_bits_to_float(p.layer.a[ti]), bf16_bits_to_float(p.layer.b[ti]), p.layer.A_log[h],
+                      p.layer.dt_bias[h], al, be);
+            s_ab[idx] = make_float2(al, be);
+        }
+    }
+    // the row this lane writes outputs for: lane l < R of a row group takes
+    // row r = l (every lane of the group holds the same o bits)
+    const int my_row = row0 + kRowsPerPass * (lane8 < R ? lane8 : 0);
+    float my_w = 0.0f;
+    if constexpr (LAYER) my_w = p.layer.norm_w[my_row];
     __syncthreads();
 
     // ---- the group's value heads, one after another
     const bool normalize = p.normalize != 0;
     const bool out_bf16 = p.out_bf16 != 0;
+    // layer: per-warp sums of o^2 (two buffers).  A head's norm needs every
+    // warp's sum, i.e. a barrier; the last token's epilogue is deferred until
+    // the next head's state loads are in flight, so that the barrier wait
+    // overlaps them.
+    __shared__ float red[LAYER ? 2 : 1][kThreads / 32];
+    int red_buf = 0;
+    bool pend = false;      // an epilogue waiting for its barrier
+    float pend_o = 0.0f;    // this lane's o for it
+    size_t pend_at = 0;     // where its y goes
+    int pend_buf = 0;
+    auto finish_pending = [&]() {
+        __syncthreads();
+        float tot = red[pend_buf][0];
+#pragma unroll
+        for (int w = 1; w < kThreads / 32; ++w) tot = __fadd_rn(tot, red[pend_buf][w]);
+        const float inv_rms = rsqrtf(__fadd_rn(__fmul_rn(tot, 1.0f / (float)(kRowsPerPass * R)), p.layer.norm_eps));
+        if (lane8 < R) {
+            const float yv = gated_norm_out(pend_o, inv_rms, my_w, bf16_bits_to_float(p.layer.z[pend_at]));
+            reinterpret_cast<__nv_bfloat16*>(p.layer.y)[pend_at] = __float2bfloat16_rn(yv);
+        }
+        pend = false;
+    };
     for (int j = 0; j < p.group; ++j) {
         const int h = g * p.group + j;
         float* S = state_of(j);
@@ -299,14 +347,23 @@ gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
             for (int m = 0; m < V; ++m)
                 s[r][m] = __ldcs(reinterpret_cast<const float4*>(
                     S + (size_t)(row0 + kRowsPerPass * r) * DK + 32 * m + 4 * lane8));
+        if constexpr (LAYER) {
+            if (pend) finish_pending();  // the previous head's last token, behind these loads
+        }
         for (int t = 0; t < p.T; ++t) {
             const uint16_t* yt = ys + (size_t)t * CC;
             TokenKQ<V> kq;
             token_kq<V>(yt, yt + DK, lane8, p.q_scale, normalize, kq);
             const size_t trow = (size_t)b * p.T + t;
-            float alpha = 0.0f;
-            if constexpr (!KDA) alpha = p.alpha[trow * p.Hv + h];
-            const float beta = p.beta[trow * p.Hv + h];
+            float alpha = 0.0f, beta;
+            if constexpr (LAYER) {
+                const float2 ab = s_ab[t * p.group + j];
+                alpha = ab.x;
+                beta = ab.y;
+            } else {
+                if constexpr (!KDA) alpha = p.alpha[trow * p.Hv + h];
+                beta = p.beta[trow * p.Hv + h];
+            }
             const uint16_t* vrow = yt + 2 * DK + j * p.dv;
             if constexpr (KDA) {
                 float4 g[V];
@@ -314,6 +371,7 @@ gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
 #pragma unroll
                 for (int r = 0; r < R; ++r) kda_decay<V>(s[r], g);
             }
+            float o_r[R];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const int i = row0 + kRowsPerPass * r;
@@ -321,8 +379,29 @@ gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
                 float o;
                 if constexpr (KDA) o = delta_row_step<V>(s[r], kq, v_i, beta);
                 else o = row_step<V>(s[r], kq, v_i, alpha, beta);
-                if (p.out != nullptr && lane8 == 0)
-                    store_out(p.out, ((trow * p.Hv) + h) * p.dv + i, o, out_bf16);
+                o_r[r] = o;
+            }
+            float my_o = o_r[0];
+#pragma unroll
+            for (int r = 1; r < R; ++r)
+                if (lane8 == r) my_o = o_r[r];  // compile-time indices: o_r stays in registers
+            if (p.out != nullptr && lane8 < R) store_out(p.out, ((trow * p.Hv) + h) * p.dv + my_row, my_o, out_bf16);
+            if constexpr (LAYER) {
+                // mean of o^2 over the head's dv rows: this thread's rows in
+                // order, the warp's four row groups (xor butterfly: the same
+                // bits in every lane), then the eight warps in order
+                float ss = __fmul_rn(o_r[0], o_r[0]);
+#pragma unroll
+                for (int r = 1; r < R; ++r) ss = __fmaf_rn(o_r[r], o_r[r], ss);
+                ss = __fadd_rn(ss, __shfl_xor_sync(kFullMask, ss, 8));
+                ss = __fadd_rn(ss, __shfl_xor_sync(kFullMask, ss, 16));
+                if ((threadIdx.x & 31) == 0) red[red_buf][threadIdx.x >> 5] = ss;
+                pend = true;
+                pend_o = my_o;
+                pend_at = ((trow * p.Hv) + h) * p.dv + my_row;
+                pend_buf = red_buf;
+                red_buf ^= 1;
+                if (t + 1 < p.T) finish_pending();  // nothing to overlap within a head's tokens
             }
         }
 #pragma unroll
@@ -332,39 +411,65 @@ gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
                 __stcs(reinterpret_cast<float4*>(S + (size_t)(row0 + kRowsPerPass * r) * DK + 32 * m + 4 * lane8),
                        s[r][m]);
     }
+    if constexpr (LAYER) {
+        if (pend) finish_pending();
+    }
 }
 
-template <int DK, int R, bool KDA>
+template <int DK, int R, int KIND>
 static cudaError_t launch_conv_decode_t(const ConvDecodeParams& p, cudaStream_t s) {
     dim3 grid(p.Hk * p.row_blocks, p.B, 1);
-    const size_t smem = (size_t)p.T * p.CC * 2 + (KDA ? (size_t)p.T * p.group * DK * 4 : 0);
-    gdn_conv_decode_kernel<DK, R, KDA><<<grid, kThreads, smem, s>>>(p);
+    const size_t smem = (size_t)p.T * p.CC * 2 + (KIND == 1 ? (size_t)p.T * p.group * DK * 4 : 0) +
+                        (KIND == 2 ? (size_t)p.T * p.group * 8 : 0);
+    gdn_conv_decode_kernel<DK, R, KIND><<<grid, kThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 
-template <int DK, bool KDA>
+template <int DK, int KIND>
 static cudaError_t launch_conv_decode_r(const ConvDecodeParams& p, int rows_per_cta, cudaStream_t s) {
     switch (rows_per_cta) {
-        case 32: return launch_conv_decode_t<DK, 1, KDA>(p, s);
-        case 64: return launch_conv_decode_t<DK, 2, KDA>(p, s);
-        case 128: return launch_conv_decode_t<DK, 4, KDA>(p, s);
+        case 32: return launch_conv_decode_t<DK, 1, KIND>(p, s);
+        case 64: return launch_conv_decode_t<DK, 2, KIND>(p, s);
+        case 128: return launch_conv_decode_t<DK, 4, KIND>(p, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
-template <bool KDA>
+template <int KIND>
 static cudaError_t launch_conv_decode_k(const ConvDecodeParams& p, int dk, int rows_per_cta, cudaStream_t s) {
     switch (dk) {
-        case 32: return launch_conv_decode_r<32, KDA>(p, rows_per_cta, s);
-        case 64: return launch_conv_decode_r<64, KDA>(p, rows_per_cta, s);
-        case 128: return launch_conv_decode_r<128, KDA>(p, rows_per_cta, s);
+        case 32: return launch_conv_decode_r<32, KIND>(p, rows_per_cta, s);
+        case 64: return launch_conv_decode_r<64, KIND>(p, rows_per_cta, s);
+        case 128: return launch_conv_decode_r<128, KIND>(p, rows_per_cta, s);
     }
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_conv_decode(const ConvDecodeParams& p, int dk, int rows_per_cta, bool kda, cudaStream_t s) {
-    return kda ? launch_conv_decode_k<true>(p, dk, rows_per_cta, s)
-               : launch_conv_decode_k<false>(p, dk, rows_per_cta, s);
+cudaError_t launch_conv_decode(const ConvDecodeParams& p, int dk, int rows_per_cta, int kind, cudaStream_t s) {
+    switch (kind) {
+        case 0: return launch_conv_decode_k<0>(p, dk, rows_per_cta, s);
+        case 1: return launch_conv_decode_k<1>(p, dk, rows_per_cta, s);
+        case 2: return launch_conv_decode_k<2>(p, dk, rows_per_cta, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+// Gates from projections for n tokens x Hv heads (one thread per pair).
+__global__ void __launch_bounds__(kThreads) gdn_gates_kernel(const __grid_constant__ GatesParams p) {
+    const int64_t idx = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    if (idx >= p.n * p.Hv) return;
+    const int h = (int)(idx % p.Hv);
+    float alpha, beta;
+    gate_pair(bf16_bits_to_float(p.a[idx]), bf16_bits_to_float(p.b[idx]), p.A_log[h], p.dt_bias[h], alpha, beta);
+    p.alpha[idx] = alpha;
+    p.beta[idx] = beta;
+}
+
+cudaError_t launch_gates(const GatesParams& p, cudaStream_t s) {
+    const int64_t n = p.n * p.Hv;
+    const unsigned blocks = (unsigned)((n + kThreads - 1) / kThreads);
+    gdn_gates_kernel<<<blocks, kThreads, 0, s>>>(p);
+    return cudaGetLastError();
 }
 
 template <int DK, int R, bool GATHER, bool KDA>

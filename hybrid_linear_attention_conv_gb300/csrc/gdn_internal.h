@@ -67,6 +67,29 @@ struct ConvParams {
 };
 
 // Fused conv + decode: one CTA per (key-head group, row block, sequence).
+// The layer step's extra inputs around the mixer (gdn_layer_decode_step).
+struct LayerParams {
+    const uint16_t* a;       // bf16 [B, T, Hv] decay projection
+    const uint16_t* b;       // bf16 [B, T, Hv] write-strength projection
+    const float* A_log;      // [Hv]
+    const float* dt_bias;    // [Hv]
+    const uint16_t* z;       // bf16 [B, T, Hv, dv] output-gate projection
+    const float* norm_w;     // [dv]
+    uint16_t* y;             // bf16 [B, T, Hv, dv]
+    float norm_eps;
+};
+
+struct GatesParams {
+    const uint16_t* a;
+    const uint16_t* b;
+    const float* A_log;
+    const float* dt_bias;
+    float* alpha;            // [n, Hv]
+    float* beta;
+    int64_t n;               // tokens
+    int Hv;
+};
+
 struct ConvDecodeParams {
     const uint16_t* x;        // [B, T, C] pre-conv inputs
     const uint16_t* w;        // [C, 4]
@@ -82,6 +105,7 @@ struct ConvDecodeParams {
     float q_scale;
     int normalize;
     int out_bf16;
+    LayerParams layer;        // the layer step only (gates from projections, gated-norm output)
 };
 
 struct TailParams {
@@ -108,7 +132,9 @@ cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int g
                           cudaStream_t s);
 template <int MB>
 cudaError_t launch_tree(const TreeParamsT<MB>& p, int dk, cudaStream_t s);
-cudaError_t launch_conv_decode(const ConvDecodeParams& p, int dk, int rows_per_cta, bool kda, cudaStream_t s);
+// kind: 0 the plain step, 1 KDA, 2 the layer step (gates in front, gated norm after)
+cudaError_t launch_conv_decode(const ConvDecodeParams& p, int dk, int rows_per_cta, int kind, cudaStream_t s);
+cudaError_t launch_gates(const GatesParams& p, cudaStream_t s);
 constexpr int kFusedMaxTokens = 16;
 constexpr int kFusedMaxSmem = 48 * 1024;
 cudaError_t launch_conv(const ConvParams& p, cudaStream_t s);

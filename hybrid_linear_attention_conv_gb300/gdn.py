@@ -48,6 +48,8 @@ EXPORTS = [
     "gdn_conv_decode_step",
     "gdn_kda_decode_step",
     "gdn_kda_conv_decode_step",
+    "gdn_layer_decode_step",
+    "gdn_gates",
     "gdn_tree_verify",
     "gdn_tree_verify_batched",
     "gdn_commit_path",
@@ -100,6 +102,9 @@ def load(path: str = LIB_PATH):
             "gdn_conv_decode_step": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, P, F, U32, P]),
             "gdn_kda_decode_step": (ctypes.c_int, [SH, I32, P, P, P, P, P, F, U32, P]),
             "gdn_kda_conv_decode_step": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, P, F, U32, P]),
+            "gdn_layer_decode_step": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, P, P, P, F, P, P, P, F, U32,
+                                                     P]),
+            "gdn_gates": (ctypes.c_int, [I64, I32, P, P, P, P, P, P, P]),
             "gdn_tree_verify": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, F, U32, P]),
             "gdn_tree_verify_batched": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, F, U32, P]),
             "gdn_commit_path": (ctypes.c_int, [SH, I32, P, P, I32, P, P, P, P, P, P, U32, P]),
@@ -270,6 +275,44 @@ def kda_conv_decode_step(x, w, tail_in, alpha, beta, state, Hk, Hv, dk, dv, tail
     """Fused conv + KDA decode: alpha fp32 [B,T,Hv,dk]; the rest as conv_decode_step."""
     return _conv_decode("gdn_kda_conv_decode_step", x, w, tail_in, alpha, beta, state, Hk, Hv, dk, dv,
                         tail_out, out, q_scale, normalize, out_bf16, lambda B, T: (B, T, Hv, dk))
+
+
+def layer_decode_step(x, conv_w, tail_in, a, b, A_log, dt_bias, z, norm_w, state, Hk, Hv, dk, dv, tail_out=None,
+                      y=None, o=None, norm_eps=1e-6, q_scale=1.0, normalize=True) -> torch.Tensor:
+    """The layer's decode step: x bf16 [B,T,C] pre-conv, conv_w bf16 [C,4], tail_in bf16 [B,4,C],
+    a/b bf16 [B,T,Hv], A_log/dt_bias fp32 [Hv], z bf16 [B,T,Hv,dv], norm_w fp32 [dv],
+    state fp32 [B,Hv,dv,dk] (in place).  Returns y bf16 [B,T,Hv,dv]; o (fp32, pre-norm) if given."""
+    B, T, C = x.shape
+    if tail_out is None:
+        tail_out = tail_in
+    if y is None:
+        y = torch.empty((B, T, Hv, dv), dtype=torch.bfloat16, device=x.device)
+    C_ = packed_channels(Hk, Hv, dk, dv)
+    rc = load().gdn_layer_decode_step(
+        ctypes.byref(_shape(B, Hk, Hv, dk, dv)), T, _dev(x, torch.bfloat16, "x", (B, T, C_)),
+        _dev(conv_w, torch.bfloat16, "conv_w", (C_, GDN_CONV_W)),
+        _dev(tail_in, torch.bfloat16, "tail_in", (B, GDN_CONV_W, C_)),
+        _dev(tail_out, torch.bfloat16, "tail_out", (B, GDN_CONV_W, C_)),
+        _dev(a, torch.bfloat16, "a", (B, T, Hv)), _dev(b, torch.bfloat16, "b", (B, T, Hv)),
+        _dev(A_log, torch.float32, "A_log", (Hv,)), _dev(dt_bias, torch.float32, "dt_bias", (Hv,)),
+        _dev(z, torch.bfloat16, "z", (B, T, Hv, dv)), _dev(norm_w, torch.float32, "norm_w", (dv,)), float(norm_eps),
+        _dev(state, torch.float32, "state", (B, Hv, dv, dk)), _dev(o, torch.float32, "o", (B, T, Hv, dv)),
+        _dev(y, torch.bfloat16, "y", (B, T, Hv, dv)), float(q_scale), _flags(normalize, False), _stream())
+    _check(rc, "gdn_layer_decode_step")
+    return y
+
+
+def gates(a, b, A_log, dt_bias):
+    """a, b bf16 [..., Hv]; A_log, dt_bias fp32 [Hv] -> (alpha, beta) fp32 [..., Hv]."""
+    Hv = a.shape[-1]
+    n = a.numel() // Hv
+    alpha = torch.empty(a.shape, dtype=torch.float32, device=a.device)
+    beta = torch.empty(a.shape, dtype=torch.float32, device=a.device)
+    rc = load().gdn_gates(n, Hv, _dev(a, torch.bfloat16, "a"), _dev(b, torch.bfloat16, "b", tuple(a.shape)),
+                          _dev(A_log, torch.float32, "A_log", (Hv,)), _dev(dt_bias, torch.float32, "dt_bias", (Hv,)),
+                          _dev(alpha, torch.float32, "alpha"), _dev(beta, torch.float32, "beta"), _stream())
+    _check(rc, "gdn_gates")
+    return alpha, beta
 
 
 def tree_verify(parents, qkv, alpha, beta, state, Hk, Hv, dk, dv, out=None, q_scale=1.0,

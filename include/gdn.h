@@ -203,6 +203,44 @@ int gdn_kda_conv_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* 
                              float q_scale, uint32_t flags, void* stream);
 
 /*
+ * gdn_layer_decode_step -- the layer's whole decode step around the mixer, in
+ * one launch: conv + SiLU and L2-norm as in gdn_conv_decode_step, the gates
+ * computed from the token's projections, the delta step, and the gated RMS
+ * norm of each head's output:
+ *   alpha = exp(-exp(A_log[h]) * softplus(a + dt_bias[h])),  beta = sigmoid(b),
+ *   o = S_h q^ (after the update),
+ *   y_i = o_i / sqrt(mean_i(o_i^2) + norm_eps) * norm_w[i] * SiLU(z_i).
+ *   x, conv_w, tail_in, tail_out, state, q_scale, T: as gdn_conv_decode_step
+ *               (T * (2 dk + (Hv/Hk) dv) * 2 bytes <= 48 KB).
+ *   a, b        bf16 [B, T, Hv] the decay and write-strength projections.
+ *   A_log, dt_bias  fp32 [Hv] per-head parameters.
+ *   z           bf16 [B, T, Hv, dv] the output-gate projection.
+ *   norm_w      fp32 [dv] the norm weight (shared by the heads); norm_eps in [0, 1].
+ *   o           fp32 [B, T, Hv, dv] the mixer outputs before the norm, or NULL.
+ *   y           bf16 [B, T, Hv, dv] the layer's mixer output.
+ *   flags       GDN_NORMALIZE_QK only.
+ * o equals, bit for bit, gdn_gates followed by gdn_conv_decode_step.
+ * Source: the pages name the layer but print neither the gates nor the
+ * output norm ("Architecture" v0.14.2 section 8.1; v0.11.1 "The parts"); both
+ * follow the published Gated DeltaNet layer (Yang, Kautz & Hatamizadeh 2024,
+ * as shipped with the Qwen3-Next models).
+ */
+int gdn_layer_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* x,
+                          const gdn_bf16* conv_w, const gdn_bf16* tail_in, gdn_bf16* tail_out,
+                          const gdn_bf16* a, const gdn_bf16* b, const float* A_log,
+                          const float* dt_bias, const gdn_bf16* z, const float* norm_w,
+                          float norm_eps, float* state, float* o, gdn_bf16* y, float q_scale,
+                          uint32_t flags, void* stream);
+
+/*
+ * gdn_gates -- the gates of gdn_layer_decode_step alone, for n tokens:
+ *   a, b bf16 [n, Hv] -> alpha, beta fp32 [n, Hv] (A_log, dt_bias fp32 [Hv]).
+ * Same arithmetic, same bits as inside the layer step.
+ */
+int gdn_gates(int64_t n, int32_t Hv, const gdn_bf16* a, const gdn_bf16* b, const float* A_log,
+              const float* dt_bias, float* alpha, float* beta, void* stream);
+
+/*
  * gdn_tree_verify -- outputs of every node of a draft tree in one pass.
  * Node n's state is the committed state advanced through the root..n path
  * (each node branches from its parent's state); out[n] = S_n q^_n.  The

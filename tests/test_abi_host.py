@@ -245,3 +245,28 @@ def test_snapshot_validation(lib):
     assert restore(n=need - 16) == -1
     assert restore(seq=9) == -1
     assert gdn.snapshot_bytes(1, 2, 4, 100, 32) == 0    # bad shape
+
+
+def test_layer_step_and_gates_validation(lib):
+    P = ctypes.c_void_p
+    sh = _sh(B=2)
+
+    def layer(T=1, flags=1, eps=1e-6, a=FAKE, y=FAKE, shape=sh, tail_out=FAKE):
+        return lib.gdn_layer_decode_step(ctypes.byref(shape), T, P(FAKE), P(FAKE), P(FAKE), P(tail_out), P(a),
+                                         P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), eps, P(FAKE), None, P(y), 1.0,
+                                         flags, None)
+
+    assert layer(flags=1 | 2) == -1 and "GDN_OUT_BF16" in gdn.last_error()
+    assert layer(eps=-1.0) == -1
+    assert layer(eps=float("nan")) == -1
+    assert layer(T=-1) == -1
+    assert layer(T=17) == -2                          # the fused step's token limit
+    assert layer(a=FAKE + 2) == -6
+    assert layer(y=0) == -1
+    assert layer(tail_out=FAKE + 16) == -1            # overlapping tails
+    assert layer(shape=_sh(dv=48)) == -2
+    assert layer(T=0) == 0                            # no-op
+    assert lib.gdn_gates(-1, 4, P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), None) == -1
+    assert lib.gdn_gates(4, 0, P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), None) == -1
+    assert lib.gdn_gates(4, 4, P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE + 4), P(FAKE), None) == -6
+    assert lib.gdn_gates(0, 4, None, None, None, None, None, None, None) == 0

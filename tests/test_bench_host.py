@@ -81,6 +81,10 @@ def test_work_formulas():
     assert bench.fp32_alu_peak_tflops(2070.0) == pytest.approx(152 * 128 * 2 * 2.07e9 / 1e12)
     # KDA: alpha carries 128 fp32 decays per head.token instead of one
     assert bench.kda_fused_bytes_per_launch(64) - bench.fused_bytes_per_launch(64) == 64 * 48 * 127 * 4
+    # the layer step: the fused bytes with bf16 gate projections and y instead of fp32 gates and outputs,
+    # plus z, the per-head parameters and the norm weight
+    assert bench.layer_bytes_per_launch(64) == (bench.fused_bytes_per_launch(64) - 64 * 48 * (8 + 128 * 4)
+                                                + 64 * 48 * 4 + 48 * 8 + 2 * 64 * 48 * 128 * 2 + 128 * 4)
     # snapshot payload of one sequence: 48 layers x (fp32 state + bf16 tail)
     assert bench.snapshot_payload_bytes(48) == 48 * (48 * 128 * 128 * 4 + 4 * 10240 * 2) == 154_927_104
 
@@ -91,7 +95,7 @@ def test_peaks_present_or_fallback():
     assert peaks["hbm_gbs"] > 1000 and peaks["bf16_tflops"] > 100
 
 
-@pytest.mark.parametrize("workload", ["batched", "tree", "kdabatch", "snapshot"])
+@pytest.mark.parametrize("workload", ["batched", "tree", "kdabatch", "snapshot", "layer"])
 def test_reference_arm_line(workload):
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
                           "--workload", workload, "--steps", "2", "--warmup", "3"],
