@@ -195,7 +195,7 @@ int report_error(int code, const char* fmt, ...) {
 
 int check_prefill_args(const gdn_shape* shape, int T, int chunk, const void* qkv, const void* alpha,
                        const void* beta, const void* state, const void* out, const void* workspace,
-                       size_t workspace_bytes, uint32_t flags) {
+                       size_t workspace_bytes, uint32_t flags, bool records) {
     int rc;
     if ((rc = check_shape(shape, true)) != GDN_OK) return rc;
     if ((rc = check_flags(flags)) != GDN_OK) return rc;
@@ -208,7 +208,8 @@ int check_prefill_args(const gdn_shape* shape, int T, int chunk, const void* qkv
     if (workspace == nullptr) return fail(GDN_ERR_WORKSPACE, "workspace is NULL");
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return fail(GDN_ERR_MISALIGNED, "workspace (%p) is not 256-byte aligned", workspace);
-    const size_t need = gdn_prefill_workspace_bytes(shape, T, chunk);
+    // with records: the pre-pass records as well as the status word
+    const size_t need = records ? gdn_prefill_workspace_bytes(shape, T, chunk) : 256;
     if (workspace_bytes < need)
         return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", workspace_bytes, need);
     return GDN_OK;

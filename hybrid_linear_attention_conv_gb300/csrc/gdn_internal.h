@@ -119,7 +119,7 @@ struct TailParams {
 // message for gdn_last_error() and return a gdn_status.
 int check_prefill_args(const gdn_shape* shape, int T, int chunk, const void* qkv, const void* alpha,
                        const void* beta, const void* state, const void* out, const void* workspace,
-                       size_t workspace_bytes, uint32_t flags);
+                       size_t workspace_bytes, uint32_t flags, bool records = true);
 int cuda_error(cudaError_t e, const char* what);
 int report_error(int code, const char* fmt, ...);
 int check_shape_arg(const gdn_shape* s, bool need_single);  // head sizes, Hv % Hk, grid limits

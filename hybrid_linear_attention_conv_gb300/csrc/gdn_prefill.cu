@@ -139,8 +139,288 @@ __device__ __forceinline__ void block_row_solve(const float* sL, float* Tf, floa
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kPrefillThreads, 1)
+// ---------------------------------------------------------------------------
+// Chunk-local steps, shared by the pre-pass kernel and the self-contained
+// prefill kernel (the same code, so both produce the same bits).
+// ---------------------------------------------------------------------------
+
+// r_k,t = 1/|k_t| and q_scale r_q,t from the staged [K;Q] rows (threads 0..127).
+__device__ __forceinline__ void kq_norms(const uint8_t* kq_tile, float* s_rk, float* s_rq, int tid, bool normalize,
+                                         float q_scale) {
+    if (tid < 128) {
+        float ss = 0.f;
+#pragma unroll 4
+        for (int kb = 0; kb < 16; ++kb) {
+            const uint4 w = *reinterpret_cast<const uint4*>(kq_tile + core_off(tid, kb * 8, kD));
+            const uint16_t* e = reinterpret_cast<const uint16_t*>(&w);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float x = bf16_to_f(e[j]);
+                ss = __fmaf_rn(x, x, ss);
+            }
+        }
+        const float r = normalize ? rsqrtf(__fadd_rn(ss, 1e-6f)) : 1.0f;
+        if (tid >= 64) s_rq[tid - 64] = __fmul_rn(r, q_scale);
+        else s_rk[tid] = r;
+    }
+}
+
+// log2 gamma_t: inclusive prefix sum of log2(alpha) over the chunk (warp 0,
+// two tokens per lane).
+__device__ __forceinline__ void log2_gamma_scan(const float* s_alpha, float* s_lg, int tid) {
+    if (tid < 32) {
+        const int l = tid;
+        const float a0 = log2f(fmaxf(s_alpha[2 * l], 1e-30f));
+        const float a1 = log2f(fmaxf(s_alpha[2 * l + 1], 1e-30f));
+        const float pair = __fadd_rn(a0, a1);
+        float incl = pair;
+#pragma unroll
+        for (int o = 1; o < 32; o *= 2) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (l >= o) incl = __fadd_rn(incl, y);
+        }
+        const float excl = __fsub_rn(incl, pair);
+        s_lg[2 * l] = __fadd_rn(excl, a0);
+        s_lg[2 * l + 1] = incl;
+    }
+}
+
+// Per-token products of the chunk form (threads 0..63).
+__device__ __forceinline__ void chunk_scalars(const float* s_lg, const float* s_rk, const float* s_rq,
+                                              const float* s_beta, float* s_gk, float* s_gq, float* s_ck,
+                                              float* s_brk, int tid) {
+    if (tid < kChunk) {
+        const float lg = s_lg[tid];
+        const float gam = exp2f(lg);
+        s_gk[tid] = __fmul_rn(gam, s_rk[tid]);
+        s_gq[tid] = __fmul_rn(gam, s_rq[tid]);
+        s_ck[tid] = __fmul_rn(exp2f(__fsub_rn(s_lg[kChunk - 1], lg)), s_rk[tid]);
+        s_brk[tid] = __fmul_rn(s_beta[tid], s_rk[tid]);
+    }
+}
+
+// L (strictly lower, fp32 [64][64]) and P (lower with the diagonal, bf16 hi/lo
+// B-operand tiles) from the [K;Q] K^T accumulator: thread i_row holds row
+// i_row of it (K rows 0..63 give L, Q rows 64..127 give P); warpgroup wg takes
+// columns 32 wg .. 32 wg + 31.
+__device__ __forceinline__ void form_l_p(uint32_t g_cols, int i_row, int wg, const float* s_lg, const float* s_brk,
+                                         const float* s_rq, const float* s_rk, float* sL, uint8_t* p_hi,
+                                         uint8_t* p_lo) {
+    const int t = i_row & 63;
+    const bool krow = i_row < 64;
+    const float lg_t = s_lg[t];
+    const float f = krow ? s_brk[t] : s_rq[t];
+#pragma unroll 1
+    for (int s0 = wg * 32; s0 < wg * 32 + 32; s0 += 16) {
+        float a[16];
+        tmem_ld16(g_cols + s0, a);
+        float row[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int sj = s0 + j;
+            const float ratio = exp2f(__fsub_rn(lg_t, s_lg[sj]));  // gamma_t / gamma_s
+            const float v = __fmul_rn(__fmul_rn(f, __fmul_rn(s_rk[sj], ratio)), a[j]);
+            // L: strictly lower (rows of K); P: lower incl. diagonal (rows of Q)
+            row[j] = (krow ? sj < t : sj <= t) ? v : 0.f;
+        }
+        if (krow) {
+            float4* dst = reinterpret_cast<float4*>(sL + t * kChunk + s0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[q] = make_float4(row[4 * q], row[4 * q + 1], row[4 * q + 2], row[4 * q + 3]);
+        } else {
+            store_split8(p_hi + core_off(t, s0, kChunk), p_lo + core_off(t, s0, kChunk), row);
+            store_split8(p_hi + core_off(t, s0 + 8, kChunk), p_lo + core_off(t, s0 + 8, kChunk), row + 8);
+        }
+    }
+}
+
+// T = (I + L)^-1, blocked by 16, into bf16 hi/lo B-operand tiles (all
+// kPrefillThreads threads; contains barriers).  Tf and R are fp32 scratch.
+__device__ __forceinline__ void solve_t(const float* sL, float* Tf, float* R, uint8_t* t_hi, uint8_t* t_lo, int tid) {
+    const int warp = tid >> 5, lane = tid & 31;
+    // zero T, so every sum below can run over whole 16-blocks
+    {
+        float4* z = reinterpret_cast<float4*>(Tf);
+#pragma unroll
+        for (int q = 0; q < kChunk * kChunk / 4 / kPrefillThreads; ++q)
+            z[tid + q * kPrefillThreads] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncthreads();
+    // diagonal blocks: warp w < 4 inverts block w column by column (lane = column)
+    if (warp < 4 && lane < 16) {
+        const int b = warp * 16, cc = lane;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) x[r] = (r == cc) ? 1.f : 0.f;
+#pragma unroll
+        for (int r = 1; r < 16; ++r) {
+            float acc = 0.f;
+#pragma unroll
+            for (int q = 0; q < r; ++q) acc = __fmaf_rn(sL[(b + r) * kChunk + b + q], x[q], acc);
+            if (r > cc) x[r] = -acc;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Tf[(b + r) * kChunk + b + cc] = x[r];
+    }
+    __syncthreads();
+    // block rows 1..3: T[I][:I] = -T_II (L[I][:I] T[:I][:I])
+    block_row_solve<1>(sL, Tf, R, tid);
+    block_row_solve<2>(sL, Tf, R, tid);
+    block_row_solve<3>(sL, Tf, R, tid);
+    // T -> bf16 hi/lo B-operand tiles (rows t, K = s)
+    for (int e = tid; e < kChunk * 8; e += kPrefillThreads) {
+        const int t = e >> 3, s0 = (e & 7) * 8;
+        const float4 a = *reinterpret_cast<const float4*>(Tf + t * kChunk + s0);
+        const float4 b = *reinterpret_cast<const float4*>(Tf + t * kChunk + s0 + 4);
+        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        store_split8(t_hi + core_off(t, s0, kChunk), t_lo + core_off(t, s0, kChunk), v);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Pre-pass: the chunk-local part of every chunk, all chunks in parallel.
+// T, P and the per-token scalars depend only on the chunk's own q, k, alpha
+// and beta, not on the state, so they need not sit on the chunk-to-chunk
+// chain of the main kernel.  One CTA per (chunk, key head): [K;Q] K^T once,
+// then for each of the key head's value heads its L, P, T and scalars, written
+// to a per-(chunk, value head) record in the workspace in the layout the main
+// kernel copies into shared memory as it is.
+// ---------------------------------------------------------------------------
+constexpr uint32_t REC_TILES = 0;        // T hi, T lo, P hi, P lo: 4 x 8192 B, as OFF_T_HI .. OFF_P_LO
+constexpr uint32_t REC_SCAL = 32768;     // beta, log2 gamma, gamma r_k, gamma q_scale r_q, (gamma_C/gamma) r_k
+constexpr uint32_t kRecBytes = REC_SCAL + 5 * 64 * 4;
+constexpr uint32_t kRecBase = 256;       // records start after the status word
+
+constexpr uint32_t Q_OFF_KQ = 0;         // [K;Q] 32 KB
+constexpr uint32_t Q_OFF_TILES = 32768;  // T hi, T lo, P hi, P lo (the record's tiles)
+constexpr uint32_t Q_OFF_L = 65536;      // L fp32 16 KB
+constexpr uint32_t Q_OFF_TF = 81920;     // T fp32 16 KB
+constexpr uint32_t Q_OFF_R = 98304;      // block-solve scratch 3 KB
+constexpr uint32_t Q_OFF_SCAL = 101376;  // 9 x 64 fp32
+constexpr uint32_t Q_OFF_MISC = Q_OFF_SCAL + 9 * 64 * 4;
+constexpr uint32_t kPrepSmem = Q_OFF_MISC + 32;
+constexpr uint32_t kPrepTmemCols = 64;
+
+__global__ void __launch_bounds__(kPrefillThreads, 2)
+gdn_prefill_prep_kernel(const __grid_constant__ PrefillParams p) {
+    extern __shared__ __align__(1024) uint8_t sm[];
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int c = blockIdx.x;
+    const int g = blockIdx.y;
+    float* s_alpha = reinterpret_cast<float*>(sm + Q_OFF_SCAL);
+    float* s_beta = s_alpha + 64;
+    float* s_lg = s_alpha + 128;
+    float* s_rk = s_alpha + 192;
+    float* s_rq = s_alpha + 256;
+    float* s_gk = s_alpha + 320;
+    float* s_gq = s_alpha + 384;
+    float* s_ck = s_alpha + 448;
+    float* s_brk = s_alpha + 512;
+    uint64_t* bar_ptr = reinterpret_cast<uint64_t*>(sm + Q_OFF_MISC);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Q_OFF_MISC + 8);
+    int* abort_flag = reinterpret_cast<int*>(sm + Q_OFF_MISC + 12);
+    const uint32_t sbase = smem_u32(sm);
+    const uint32_t bar = smem_u32(bar_ptr);
+    const int t0 = c * kChunk;
+    const int n = min(kChunk, p.T - t0);
+    const size_t C = (size_t)p.C;
+
+    if (warp == 0) tmem_alloc(smem_u32(tmem_slot), kPrepTmemCols);
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        *abort_flag = 0;
+    }
+    // [K;Q] rows of the chunk (zero-filled past the last token)
+    for (int idx = tid; idx < 2 * kChunk * 16; idx += kPrefillThreads) {
+        const int r = idx >> 4, kb = idx & 15;
+        const int t = r & 63;
+        const bool ok = t < n;
+        const uint16_t* src = p.qkv + (size_t)(t0 + (ok ? t : 0)) * C + (r >= 64 ? 0 : (size_t)p.Hk * kD) +
+                              (size_t)g * kD + kb * 8;
+        cp_async16(sbase + Q_OFF_KQ + core_off(r, kb * 8, kD), src, ok);
+    }
+    cp_async_commit();
+    cp_async_wait_all();
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const int i_row = tid & 127;
+    const int wg = tid >> 7;
+    const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+
+    if (tid == 0) {
+        constexpr uint32_t id_g = idesc_bf16(128, 64);
+#pragma unroll 1
+        for (int ks = 0; ks < kD / 16; ++ks)
+            mma_bf16(tmem, smem_desc(sbase + Q_OFF_KQ + ks * 256, kD * 16),
+                     smem_desc(sbase + Q_OFF_KQ + ks * 256, kD * 16), id_g, ks > 0);
+        mma_commit(bar);
+    }
+    kq_norms(sm + Q_OFF_KQ, s_rk, s_rq, tid, p.normalize != 0, p.q_scale);
+    const bool ok = mbar_wait(bar, 0, kWaitLimitNs);
+    if (!ok) atomicOr(abort_flag, 1);
+    __syncthreads();
+    fence_after_sync();
+
+    if (*abort_flag == 0) {
+#pragma unroll 1
+        for (int j = 0; j < p.group; ++j) {
+            const int h = g * p.group + j;
+            if (tid < kChunk) {
+                const bool in = tid < n;
+                s_alpha[tid] = in ? p.alpha[(size_t)(t0 + tid) * p.Hv + h] : 1.0f;
+                s_beta[tid] = in ? p.beta[(size_t)(t0 + tid) * p.Hv + h] : 0.0f;
+            }
+            __syncthreads();
+            log2_gamma_scan(s_alpha, s_lg, tid);
+            __syncthreads();
+            chunk_scalars(s_lg, s_rk, s_rq, s_beta, s_gk, s_gq, s_ck, s_brk, tid);
+            __syncthreads();
+            form_l_p(trow, i_row, wg, s_lg, s_brk, s_rq, s_rk, reinterpret_cast<float*>(sm + Q_OFF_L),
+                     sm + Q_OFF_TILES + 16384, sm + Q_OFF_TILES + 24576);
+            __syncthreads();
+            solve_t(reinterpret_cast<const float*>(sm + Q_OFF_L), reinterpret_cast<float*>(sm + Q_OFF_TF),
+                    reinterpret_cast<float*>(sm + Q_OFF_R), sm + Q_OFF_TILES, sm + Q_OFF_TILES + 8192, tid);
+            __syncthreads();
+            // the record of (chunk c, value head h)
+            uint8_t* rec = reinterpret_cast<uint8_t*>(p.status) + kRecBase + ((size_t)c * p.Hv + h) * kRecBytes;
+            for (int v = tid; v < 32768 / 16; v += kPrefillThreads)
+                reinterpret_cast<uint4*>(rec + REC_TILES)[v] = reinterpret_cast<const uint4*>(sm + Q_OFF_TILES)[v];
+            if (tid < 5 * 16) {
+                const float* src[5] = {s_beta, s_lg, s_gk, s_gq, s_ck};
+                reinterpret_cast<uint4*>(rec + REC_SCAL)[tid] =
+                    reinterpret_cast<const uint4*>(src[tid >> 4])[tid & 15];
+            }
+            __syncthreads();
+        }
+    }
+    if (*abort_flag != 0 && tid == 0) atomicExch(p.status, 1);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
+}
+
+// The chain over chunks.  PREP: T, P and the per-token scalars come from the
+// pre-pass records (prefetched one chunk ahead); otherwise they are computed
+// here between the chunk's MMAs (the self-contained form, which needs no
+// workspace beyond the status word).
+// Threads of the chain kernel: with PREP four warpgroups share the 128 TMEM
+// lanes (each takes a quarter of every row's columns, halving the epilogues);
+// the self-contained form keeps two (its solve is written for 256 threads).
+template <bool PREP>
+__host__ __device__ constexpr int chain_threads() { return PREP ? 512 : kPrefillThreads; }
+
+template <bool PREP>
+__global__ void __launch_bounds__(chain_threads<PREP>(), 1)
 gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
+    constexpr int NT = chain_threads<PREP>();
+    constexpr int NWG = NT / 128;      // warpgroups
+    constexpr int CW = kChunk / NWG;   // columns of a 64-wide tile per warpgroup
+    constexpr int CS = kD / NWG;       // columns of the state per warpgroup
     extern __shared__ __align__(1024) uint8_t sm[];
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -173,8 +453,8 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    // Thread tid owns TMEM lane / state row i = tid % 128; the two warpgroups
-    // (wg = tid / 128) split every row's columns in halves.
+    // Thread tid owns TMEM lane / state row i = tid % 128; the warpgroups
+    // (wg = tid / 128) split every row's columns.
     const int i_row = tid & 127;
     const int wg = tid >> 7;
     const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // this thread's lane
@@ -193,7 +473,7 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
     // ---- prologue: state row i -> TMEM lane i and the bf16 hi/lo operand tiles
     float* srow = p.state + ((size_t)h * kD + i_row) * kD;
 #pragma unroll 1
-    for (int c0 = wg * 64; c0 < wg * 64 + 64; c0 += 16) {
+    for (int c0 = wg * CS; c0 < wg * CS + CS; c0 += 16) {
         float v[16];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -215,7 +495,7 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
     // asynchronous 16-byte copies (zero-filled past the last token)
     auto issue_kq = [&](int t0, int n) {
 #pragma unroll 4
-        for (int idx = tid; idx < 2 * kChunk * 16; idx += kPrefillThreads) {
+        for (int idx = tid; idx < 2 * kChunk * 16; idx += NT) {
             const int r = idx >> 4, kb = idx & 15;
             const int t = r & 63;
             const bool ok = t < n;
@@ -226,12 +506,26 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
     };
     auto issue_v = [&](int t0, int n) {
 #pragma unroll 4
-        for (int idx = tid; idx < kChunk * 16; idx += kPrefillThreads) {
+        for (int idx = tid; idx < kChunk * 16; idx += NT) {
             const int t = idx >> 4, kb = idx & 15;
             const bool ok = t < n;
             const uint16_t* src =
                 p.qkv + (size_t)(t0 + (ok ? t : 0)) * C + (size_t)2 * p.Hk * kD + (size_t)h * kD + kb * 8;
             cp_async16(sbase + OFF_V + t * 256 + kb * 16, src, ok);
+        }
+    };
+    // PREP: chunk cc's record (T and P tiles, per-token scalars) into place
+    auto issue_rec = [&](int cc) {
+        const uint8_t* rec =
+            reinterpret_cast<const uint8_t*>(p.status) + kRecBase + ((size_t)cc * p.Hv + h) * kRecBytes;
+#pragma unroll 4
+        for (int v = tid; v < 32768 / 16; v += NT)
+            cp_async16(sbase + OFF_T_HI + v * 16, rec + REC_TILES + v * 16, true);
+        if (tid < 5 * 16) {
+            // beta, log2 gamma, gamma r_k, gamma q_scale r_q, (gamma_C/gamma) r_k
+            const int a = tid >> 4, q = tid & 15;
+            const int at = a < 2 ? 64 * (a + 1) : 256 + 64 * (a - 1);  // s_beta, s_lg, s_gk, s_gq, s_ck
+            cp_async16(sbase + OFF_SCAL + at * 4 + q * 16, rec + REC_SCAL + a * 256 + q * 16, true);
         }
     };
 #pragma unroll 1
@@ -245,69 +539,35 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
             if (c == 0) {
                 issue_kq(t0, n);
                 issue_v(t0, n);
+                if (PREP) issue_rec(0);
                 cp_async_commit();
             }
             cp_async_wait_all();
-            if (tid < kChunk) {
+            if (!PREP && tid < kChunk) {
                 const bool ok = tid < n;
                 s_alpha[tid] = ok ? p.alpha[(size_t)(t0 + tid) * p.Hv + h] : 1.0f;
                 s_beta[tid] = ok ? p.beta[(size_t)(t0 + tid) * p.Hv + h] : 0.0f;
             }
         }
         __syncthreads();
-        if (tid < 128) {
-            // norm of row tid of [K;Q]
-            float ss = 0.f;
-#pragma unroll 4
-            for (int kb = 0; kb < 16; ++kb) {
-                const uint4 w = *reinterpret_cast<const uint4*>(sm + OFF_KQ + core_off(tid, kb * 8, kD));
-                const uint16_t* e = reinterpret_cast<const uint16_t*>(&w);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float x = bf16_to_f(e[j]);
-                    ss = __fmaf_rn(x, x, ss);
-                }
-            }
-            const float r = p.normalize ? rsqrtf(__fadd_rn(ss, 1e-6f)) : 1.0f;
-            if (tid >= 64) s_rq[tid - 64] = __fmul_rn(r, p.q_scale);
-            else s_rk[tid] = r;
-        }
+        if (!PREP) kq_norms(sm + OFF_KQ, s_rk, s_rq, tid, p.normalize != 0, p.q_scale);
         {
             // K^T: each warp transposes 16 of the 128 8x8 core matrices of K
             const int lane = tid & 31;
 #pragma unroll
-            for (int it = 0; it < 4; ++it) {
-                const int q = warp * 16 + it * 4 + (lane >> 3);  // core matrix (tb, jb) = (q / 16, q % 16)
+            for (int it = 0; it < 128 / (NT / 32) / 4; ++it) {
+                // core matrix (tb, jb) = (q / 16, q % 16); each warp takes 128 / (NT / 32) of them
+                const int q = warp * (128 / (NT / 32)) + it * 4 + (lane >> 3);
                 const int tb = q >> 4, jb = q & 15;
                 const uint32_t src = sbase + OFF_KQ + tb * (kD * 16) + jb * 128 + (lane & 7) * 16;
                 const uint32_t dst = sbase + OFF_KT + jb * (kChunk * 16) + tb * 128 + (lane & 7) * 16;
                 transpose_8x8x4(src, dst);
             }
         }
-        if (warp == 0) {
-            // log2 gamma: inclusive prefix sum of log2(alpha) (two tokens per lane)
-            const int l = tid;
-            const float a0 = log2f(fmaxf(s_alpha[2 * l], 1e-30f));
-            const float a1 = log2f(fmaxf(s_alpha[2 * l + 1], 1e-30f));
-            const float pair = __fadd_rn(a0, a1);
-            float incl = pair;
-#pragma unroll
-            for (int o = 1; o < 32; o *= 2) {
-                const float y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (l >= o) incl = __fadd_rn(incl, y);
-            }
-            const float excl = __fsub_rn(incl, pair);
-            s_lg[2 * l] = __fadd_rn(excl, a0);
-            s_lg[2 * l + 1] = incl;
-        }
-        __syncthreads();
-        if (tid < kChunk) {
-            const float lg = s_lg[tid];
-            const float gam = exp2f(lg);
-            s_gk[tid] = __fmul_rn(gam, s_rk[tid]);
-            s_gq[tid] = __fmul_rn(gam, s_rq[tid]);
-            s_ck[tid] = __fmul_rn(exp2f(__fsub_rn(s_lg[kChunk - 1], lg)), s_rk[tid]);
-            s_brk[tid] = __fmul_rn(s_beta[tid], s_rk[tid]);
+        if (!PREP) {
+            log2_gamma_scan(s_alpha, s_lg, tid);
+            __syncthreads();
+            chunk_scalars(s_lg, s_rk, s_rq, s_beta, s_gk, s_gq, s_ck, s_brk, tid);
         }
         fence_async_smem();
         fence_before_sync();
@@ -318,11 +578,13 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
             fence_after_sync();
             constexpr uint32_t id_g = idesc_bf16(128, 64);
             constexpr uint32_t id_kq = idesc_bf16(128, 128);
+            if (!PREP) {
 #pragma unroll 1
-            for (int ks = 0; ks < kD / 16; ++ks)
-                mma_bf16(tmem + COL_G, smem_desc(sbase + OFF_KQ + ks * 256, kD * 16),
-                         smem_desc(sbase + OFF_KQ + ks * 256, kD * 16), id_g, ks > 0);
-            mma_commit(barg);
+                for (int ks = 0; ks < kD / 16; ++ks)
+                    mma_bf16(tmem + COL_G, smem_desc(sbase + OFF_KQ + ks * 256, kD * 16),
+                             smem_desc(sbase + OFF_KQ + ks * 256, kD * 16), id_g, ks > 0);
+                mma_commit(barg);
+            }
 #pragma unroll 1
             for (int pass = 0; pass < 2; ++pass)
 #pragma unroll 1
@@ -331,87 +593,19 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
                              smem_desc(sbase + OFF_KQ + ks * 256, kD * 16), id_kq, (pass > 0 || ks > 0));
             mma_commit(bar);
         }
-        if (!wait_on(barg, parity_g)) break;
-
-        // ---- C: L and P (from [K;Q] K^T), then the T solve, while S [K;Q]^T runs
-        {
-            const int t = i_row & 63;
-            const bool krow = i_row < 64;
-            const float lg_t = s_lg[t];
-            const float f = krow ? s_brk[t] : s_rq[t];
-#pragma unroll 1
-            for (int s0 = wg * 32; s0 < wg * 32 + 32; s0 += 16) {
-                float a[16];
-                tmem_ld16(trow + COL_G + s0, a);
-                float row[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int sj = s0 + j;
-                    const float ratio = exp2f(__fsub_rn(lg_t, s_lg[sj]));  // gamma_t / gamma_s
-                    const float v = __fmul_rn(__fmul_rn(f, __fmul_rn(s_rk[sj], ratio)), a[j]);
-                    // L: strictly lower (rows of K); P: lower incl. diagonal (rows of Q)
-                    row[j] = (krow ? sj < t : sj <= t) ? v : 0.f;
-                }
-                if (krow) {
-                    float4* dst = reinterpret_cast<float4*>(sm + OFF_L + (t * kChunk + s0) * 4);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) dst[q] = make_float4(row[4 * q], row[4 * q + 1], row[4 * q + 2], row[4 * q + 3]);
-                } else {
-                    store_split8(sm + OFF_P_HI + core_off(t, s0, kChunk), sm + OFF_P_LO + core_off(t, s0, kChunk), row);
-                    store_split8(sm + OFF_P_HI + core_off(t, s0 + 8, kChunk),
-                                 sm + OFF_P_LO + core_off(t, s0 + 8, kChunk), row + 8);
-                }
-            }
-        }
-        __syncthreads();
-
-        // ---- D: T = (I + L)^-1, blocked by 16 --------------------------
-        {
-            const float* sL = reinterpret_cast<const float*>(sm + OFF_L);
-            float* Tf = reinterpret_cast<float*>(sm + OFF_TF);
-            float* R = reinterpret_cast<float*>(sm + OFF_R);
-            const int lane = tid & 31;
-            // zero T, so every sum below can run over whole 16-blocks
-            {
-                float4* z = reinterpret_cast<float4*>(Tf);
-#pragma unroll
-                for (int q = 0; q < kChunk * kChunk / 4 / kPrefillThreads; ++q)
-                    z[tid + q * kPrefillThreads] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+        if (!PREP) {
+            if (!wait_on(barg, parity_g)) break;
+            // ---- C: L and P (from [K;Q] K^T), then the T solve, while S [K;Q]^T runs
+            form_l_p(trow + COL_G, i_row, wg, s_lg, s_brk, s_rq, s_rk, reinterpret_cast<float*>(sm + OFF_L),
+                     sm + OFF_P_HI, sm + OFF_P_LO);
             __syncthreads();
-            // diagonal blocks: warp w < 4 inverts block w column by column (lane = column)
-            if (warp < 4 && lane < 16) {
-                const int b = warp * 16, cc = lane;
-                float x[16];
-#pragma unroll
-                for (int r = 0; r < 16; ++r) x[r] = (r == cc) ? 1.f : 0.f;
-#pragma unroll
-                for (int r = 1; r < 16; ++r) {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int q = 0; q < r; ++q) acc = __fmaf_rn(sL[(b + r) * kChunk + b + q], x[q], acc);
-                    if (r > cc) x[r] = -acc;
-                }
-#pragma unroll
-                for (int r = 0; r < 16; ++r) Tf[(b + r) * kChunk + b + cc] = x[r];
-            }
+            // ---- D: T = (I + L)^-1, blocked by 16 --------------------------
+            solve_t(reinterpret_cast<const float*>(sm + OFF_L), reinterpret_cast<float*>(sm + OFF_TF),
+                    reinterpret_cast<float*>(sm + OFF_R), sm + OFF_T_HI, sm + OFF_T_LO, tid);
+            fence_async_smem();
+            fence_before_sync();
             __syncthreads();
-            // block rows 1..3: T[I][:I] = -T_II (L[I][:I] T[:I][:I])
-            block_row_solve<1>(sL, Tf, R, tid);
-            block_row_solve<2>(sL, Tf, R, tid);
-            block_row_solve<3>(sL, Tf, R, tid);
-            // T -> bf16 hi/lo B-operand tiles (rows t, K = s)
-            for (int e = tid; e < kChunk * 8; e += kPrefillThreads) {
-                const int t = e >> 3, s0 = (e & 7) * 8;
-                const float4 a = *reinterpret_cast<const float4*>(Tf + t * kChunk + s0);
-                const float4 b = *reinterpret_cast<const float4*>(Tf + t * kChunk + s0 + 4);
-                const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-                store_split8(sm + OFF_T_HI + core_off(t, s0, kChunk), sm + OFF_T_LO + core_off(t, s0, kChunk), v);
-            }
         }
-        fence_async_smem();
-        fence_before_sync();
-        __syncthreads();
 
         if (!wait_on(bar, parity)) break;
         // S [K;Q]^T has read [K;Q]: prefetch the next chunk's rows behind it
@@ -426,7 +620,7 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
             const int i = i_row;
             const uint16_t* vcol = reinterpret_cast<const uint16_t*>(sm + OFF_V) + i;
 #pragma unroll 1
-            for (int s0 = wg * 32; s0 < wg * 32 + 32; s0 += 16) {
+            for (int s0 = wg * CW; s0 < wg * CW + CW; s0 += 16) {
                 float ks[16], x[16];
                 tmem_ld16(trow + COL_KQ + s0, ks);
 #pragma unroll
@@ -440,7 +634,7 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
             }
             // scaled (S q_t)[i] * gamma_t r_q,t, written back as the start of O^T
 #pragma unroll 1
-            for (int s0 = wg * 32; s0 < wg * 32 + 32; s0 += 16) {
+            for (int s0 = wg * CW; s0 < wg * CW + CW; s0 += 16) {
                 float qs[16];
                 tmem_ld16(trow + COL_O + s0, qs);
 #pragma unroll
@@ -480,7 +674,7 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
             const int i = i_row;
             const float lg_c = s_lg[kChunk - 1];
 #pragma unroll 1
-            for (int s0 = wg * 32; s0 < wg * 32 + 32; s0 += 16) {
+            for (int s0 = wg * CW; s0 < wg * CW + CW; s0 += 16) {
                 float u[16], uh[16];
                 tmem_ld16(trow + COL_U + s0, u);
 #pragma unroll
@@ -494,7 +688,7 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
             }
             const float gamma_c = exp2f(lg_c);
 #pragma unroll 1
-            for (int c0 = wg * 64; c0 < wg * 64 + 64; c0 += 16) {
+            for (int c0 = wg * CS; c0 < wg * CS + CS; c0 += 16) {
                 float sv[16];
                 tmem_ld16(trow + COL_S + c0, sv);
 #pragma unroll
@@ -531,12 +725,17 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
         if (!wait_on(bar, parity)) break;
 
         // ---- H: outputs, next chunk's S operands, final state -------------
+        // (E and G have read T and P, F the scalars: prefetch the next record)
+        if (PREP && c + 1 < nchunks) {
+            issue_rec(c + 1);
+            cp_async_commit();
+        }
         {
             const int i = i_row;
             const size_t ostride = (size_t)p.Hv * kD;
             const size_t obase = (size_t)t0 * ostride + (size_t)h * kD + i;
 #pragma unroll 1
-            for (int s0 = wg * 32; s0 < wg * 32 + 32; s0 += 16) {
+            for (int s0 = wg * CW; s0 < wg * CW + CW; s0 += 16) {
                 float o[16];
                 tmem_ld16(trow + COL_O + s0, o);
 #pragma unroll
@@ -550,7 +749,7 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
             }
             const bool last = (c == nchunks - 1);
 #pragma unroll 1
-            for (int c0 = wg * 64; c0 < wg * 64 + 64; c0 += 16) {
+            for (int c0 = wg * CS; c0 < wg * CS + CS; c0 += 16) {
                 float sv[16];
                 tmem_ld16(trow + COL_S + c0, sv);
                 if (last) {
@@ -587,11 +786,21 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
 
 using namespace gdn;
 
+namespace {
+int launch_prefill(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const float* alpha, const float* beta,
+                   float* state, void* out, void* workspace, float q_scale, uint32_t flags, cudaStream_t st,
+                   bool prep);
+}  // namespace
+
 extern "C" {
 
 size_t gdn_prefill_workspace_bytes(const gdn_shape* shape, int32_t T, int32_t chunk) {
     if (shape == nullptr || T < 0 || chunk != kChunk) return 0;
-    return 256;  // status word (int32 at offset 0), padded
+    // the status word (int32 at offset 0, padded), then for 128-wide heads one
+    // pre-pass record per (chunk, value head)
+    if (shape->dk != kD || shape->dv != kD || shape->Hv < 1) return kRecBase;
+    const size_t nchunks = ((size_t)T + kChunk - 1) / kChunk;
+    return kRecBase + nchunks * (size_t)shape->Hv * kRecBytes;
 }
 
 int gdn_chunk_prefill(const gdn_shape* shape, int32_t T, int32_t chunk, const gdn_bf16* qkv,
@@ -607,12 +816,32 @@ int gdn_chunk_prefill(const gdn_shape* shape, int32_t T, int32_t chunk, const gd
         // narrower heads: the same recurrence token by token on the GPU
         return gdn_decode_step(shape, T, qkv, alpha, beta, state, out, q_scale, flags, stream);
     }
+    return launch_prefill(shape, T, qkv, alpha, beta, state, out, workspace, q_scale, flags, st, true);
+}
+
+}  // extern "C"
+
+namespace {
+
+// The chunk-form launch(es): with `prep`, the pre-pass over all chunks then the
+// chain reading its records (the workspace holds them); without, the
+// self-contained chain (the workspace holds only the status word).
+int launch_prefill(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const float* alpha, const float* beta,
+                   float* state, void* out, void* workspace, float q_scale, uint32_t flags, cudaStream_t st,
+                   bool prep) {
     static bool configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
+    cudaError_t e;
     if (dev >= 0 && dev < 64 && !configured[dev]) {
-        e = cudaFuncSetAttribute(gdn_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(gdn_prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kPrefillSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gdn_prefill_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kPrefillSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gdn_prefill_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kPrepSmem);
         if (e != cudaSuccess) return cuda_error(e, "prefill smem attribute");
         configured[dev] = true;
     }
@@ -631,12 +860,18 @@ int gdn_chunk_prefill(const gdn_shape* shape, int32_t T, int32_t chunk, const gd
     p.q_scale = q_scale;
     p.normalize = (flags & GDN_NORMALIZE_QK) != 0;
     p.out_bf16 = (flags & GDN_OUT_BF16) != 0;
-    gdn_prefill_tc_kernel<<<shape->Hv, kPrefillThreads, kPrefillSmem, st>>>(p);
+    if (prep) {
+        const dim3 grid((unsigned)((T + kChunk - 1) / kChunk), (unsigned)shape->Hk);
+        gdn_prefill_prep_kernel<<<grid, kPrefillThreads, kPrepSmem, st>>>(p);
+        gdn_prefill_tc_kernel<true><<<shape->Hv, chain_threads<true>(), kPrefillSmem, st>>>(p);
+    } else {
+        gdn_prefill_tc_kernel<false><<<shape->Hv, chain_threads<false>(), kPrefillSmem, st>>>(p);
+    }
     e = cudaGetLastError();
     return e == cudaSuccess ? GDN_OK : cuda_error(e, "prefill launch");
 }
 
-}  // extern "C"
+}  // namespace
 
 // ---------------------------------------------------------------------------
 // Prefill without caller-provided workspace.
@@ -680,13 +915,21 @@ cudaError_t noalloc_scratch(void** ptr) {
 extern "C" int gdn_chunk_prefill_noalloc(const gdn_shape* shape, int32_t T, int32_t chunk, const gdn_bf16* qkv,
                                          const float* alpha, const float* beta, float* state, void* out,
                                          float q_scale, uint32_t flags, void* stream) {
-    const size_t need = gdn_prefill_workspace_bytes(shape, T, chunk);
+    // the self-contained chain needs only the status word
+    const size_t need = kRecBase;
     if (need > kNoAllocScratchBytes)
         return report_error(GDN_ERR_WORKSPACE, "prefill needs %zu bytes of scratch; the built-in array holds %zu",
                             need, kNoAllocScratchBytes);
     void* scratch = nullptr;
     cudaError_t e = noalloc_scratch(&scratch);
     if (e != cudaSuccess) return cuda_error(e, "locating the built-in prefill scratch");
-    return gdn_chunk_prefill(shape, T, chunk, qkv, alpha, beta, state, out, scratch, kNoAllocScratchBytes, q_scale,
-                             flags, stream);
+    int rc = check_prefill_args(shape, T, chunk, qkv, alpha, beta, state, out, scratch, kNoAllocScratchBytes, flags,
+                                false);
+    if (rc != GDN_OK || T == 0) return rc;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    e = cudaMemsetAsync(scratch, 0, 16, st);
+    if (e != cudaSuccess) return cuda_error(e, "prefill status reset");
+    if (shape->dk != kD || shape->dv != kD)
+        return gdn_decode_step(shape, T, qkv, alpha, beta, state, out, q_scale, flags, stream);
+    return launch_prefill(shape, T, qkv, alpha, beta, state, out, scratch, q_scale, flags, st, false);
 }

@@ -303,7 +303,10 @@ int gdn_commit_path(const gdn_shape* shape, int32_t N, const int32_t* parents,
 /*
  * gdn_prefill_workspace_bytes -- device workspace gdn_chunk_prefill needs for
  * T tokens in chunks of `chunk` (0 on a bad shape or chunk).  The workspace
- * holds the call's status word (int32 at offset 0).
+ * holds the call's status word (int32 at offset 0, padded to 256 bytes) and,
+ * for 128-wide heads, one 34,048-byte pre-pass record per (chunk, value
+ * head): 256 + ceil(T / 64) * Hv * 34,048 bytes (209 MB at T = 8,192 with 48
+ * value heads).
  */
 size_t gdn_prefill_workspace_bytes(const gdn_shape* shape, int32_t T, int32_t chunk);
 
@@ -321,7 +324,10 @@ size_t gdn_prefill_workspace_bytes(const gdn_shape* shape, int32_t T, int32_t ch
  *              up (read it after the stream has synchronised; non-zero means
  *              the results are invalid, as for GDN_ERR_TIMEOUT).
  * The chunk form runs for dk = dv = 128 (the 27B layer's heads); narrower
- * heads run the same recurrence token by token on the GPU.
+ * heads run the same recurrence token by token on the GPU.  It is two
+ * launches: a pre-pass computing every chunk's state-independent part (the
+ * inverse T = (I + L)^-1, the masked Q K^T and the per-token decays) into the
+ * workspace, all chunks in parallel, then the chain over chunks per head.
  * Source: "Architecture" (v0.11.1) "The parts" (the rule over a block);
  * chunk-parallel versus sequential evaluation of the recurrence, "Serving A
  * Research Architecture On CPU" (third exactness layer).  Chunk form: Yang et
@@ -339,10 +345,12 @@ int gdn_chunk_prefill(const gdn_shape* shape, int32_t T, int32_t chunk,
  * at start-up and must not grow while it serves, or a host whose device memory
  * is owned by another allocator.  (The pages describe no such call; it exists
  * for those callers.)
- *   Arguments and results as gdn_chunk_prefill, without the workspace: the
- *   scratch the kernel needs lives in a 256-byte array inside this library,
- *   which every GPU that loads the library keeps until the process exits.
- *   Returns GDN_ERR_WORKSPACE if the call would need more scratch than that.
+ *   Arguments and results as gdn_chunk_prefill (the same bits), without the
+ *   workspace: it runs the single-launch form of the chain that computes each
+ *   chunk's state-independent part itself, so the only scratch it needs is
+ *   the status word, in a 256-byte array inside this library, which every GPU
+ *   that loads the library keeps until the process exits.  Returns
+ *   GDN_ERR_WORKSPACE if the call would need more scratch than that.
  *   The first call on a device looks up the array's device address (once per
  *   device, with that device current); make that first call before any stream
  *   capture.  Every call on a device shares the one array and clears the part

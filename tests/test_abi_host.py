@@ -270,3 +270,15 @@ def test_layer_step_and_gates_validation(lib):
     assert lib.gdn_gates(4, 0, P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), None) == -1
     assert lib.gdn_gates(4, 4, P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE + 4), P(FAKE), None) == -6
     assert lib.gdn_gates(0, 4, None, None, None, None, None, None, None) == 0
+
+
+def test_prefill_workspace_holds_the_prepass_records(lib):
+    P = ctypes.c_void_p
+    sh = gdn.gdn_shape(1, 16, 48, 128, 128)
+    # the status word, then one 34,048-byte record per (chunk of 64, value head)
+    assert gdn.prefill_workspace_bytes(8192, 16, 48, 128, 128) == 256 + 128 * 48 * 34048
+    assert gdn.prefill_workspace_bytes(65, 16, 48, 128, 128) == 256 + 2 * 48 * 34048
+    assert gdn.prefill_workspace_bytes(100, 2, 4, 32, 32) == 256     # narrow heads: no records
+    rc = lib.gdn_chunk_prefill(ctypes.byref(sh), 64, 64, P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE * 256),
+                               256, 1.0, 1, None)
+    assert rc == -9 and "needed" in gdn.last_error()

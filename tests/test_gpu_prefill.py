@@ -117,3 +117,27 @@ def test_prefill_then_decode_continues():
                                     shape.dk, shape.dv)
     assert_out_close(host(out)[0, 0], out_ref[0, T])
     assert_state_close(host(st_b)[0], st_ref[0])
+
+
+@pytest.mark.parametrize("T", [64, 300, 1000])
+def test_prefill_prepass_equals_self_contained_bitwise(T):
+    """The pre-pass path (T, P and the per-token scalars computed for all
+    chunks in parallel, then read by the chain) and the self-contained chain
+    (the same chunk-local steps between the MMAs) give the same bits."""
+    import ctypes
+    shape = gen.QWEN_27B
+    d = gen.decode_inputs(90 + T, shape.with_batch(1), T, tag="prepass")
+    qkv, al, be = bf16(d["qkv"][0]), f32(d["alpha"][0]), f32(d["beta"][0])
+    st_a = f32(d["state"][0])
+    out_a = gdn.chunk_prefill(qkv, al, be, st_a, shape.Hk, shape.Hv, shape.dk, shape.dv)
+    st_b = f32(d["state"][0])
+    out_b = torch.empty_like(out_a)
+    P = ctypes.c_void_p
+    sh = gdn.gdn_shape(1, shape.Hk, shape.Hv, shape.dk, shape.dv)
+    rc = gdn.load().gdn_chunk_prefill_noalloc(ctypes.byref(sh), T, 64, P(qkv.data_ptr()), P(al.data_ptr()),
+                                              P(be.data_ptr()), P(st_b.data_ptr()), P(out_b.data_ptr()), 1.0,
+                                              gdn.GDN_NORMALIZE_QK, P(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0, gdn.last_error()
+    torch.cuda.synchronize()
+    assert torch.equal(out_a, out_b)
+    assert torch.equal(st_a, st_b)
