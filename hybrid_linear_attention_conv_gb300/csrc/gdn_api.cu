@@ -381,14 +381,19 @@ static int conv_decode_impl(const gdn_shape* shape, int32_t T, const gdn_bf16* x
     // place (one writer per tail entry); with distinct tails, split the rows
     // until every SM has a few CTAs.
     if (layer != nullptr) p.layer = *layer;
-    int row_blocks = 1;
-    if (ti != to && kind != 2) {  // the layer step's norm needs every row of a head in one CTA
+    int row_blocks = 1, head_parts = 1;
+    if (ti != to) {
         const long want = 4L * sm_count();
-        while (row_blocks < 4 && shape->dv / (row_blocks * 2) >= 32 &&
-               (long)shape->Hk * shape->B * row_blocks < want)
-            row_blocks *= 2;
+        if (kind != 2) {  // the layer step's norm needs every row of a head in one CTA
+            while (row_blocks < 4 && shape->dv / (row_blocks * 2) >= 32 &&
+                   (long)shape->Hk * shape->B * row_blocks < want)
+                row_blocks *= 2;
+        }
+        // still short of a few CTAs per SM: one value head per CTA
+        if ((long)shape->Hk * shape->B * row_blocks < want) head_parts = group;
     }
     p.row_blocks = row_blocks;
+    p.head_parts = head_parts;
     cudaError_t e =
         launch_conv_decode(p, shape->dk, shape->dv / row_blocks, kind, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GDN_OK

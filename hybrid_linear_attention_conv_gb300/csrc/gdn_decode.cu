@@ -218,11 +218,13 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
 
 // Fused conv + decode.  A CTA owns one key-head group (its q and k channels
 // and the v channels of the group's value heads) of one sequence, and 32*R
-// rows of each of those value heads.  It runs the conv for the group's
-// channels into shared memory (rounded to bf16 exactly as gdn_conv_step
-// stores it), then advances each value head's rows through the T tokens with
-// the shared step.  Every tail entry is written by one CTA only (row block 0);
-// with several row blocks the tail is read from tail_in and written to a
+// rows of each of the group's value heads it runs: all of them, or one each
+// when the heads are split over CTAs (head_parts = group) to widen the grid of
+// a small batch.  It runs the conv for all of the group's channels into shared
+// memory (rounded to bf16 exactly as gdn_conv_step stores it), then advances
+// its value heads' rows through the T tokens with the shared step.  Every tail
+// entry is written by one CTA only (row block 0 of head part 0); with several
+// row blocks or head parts the tail is read from tail_in and written to a
 // distinct tail_out, so no CTA reads an entry another CTA has overwritten.
 // KIND 0: the step as it is; 1: KDA (a decay per key channel); 2: the layer
 // step -- gates computed from the token's projections in front, and the
@@ -240,8 +242,13 @@ gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
     float4* gs = reinterpret_cast<float4*>(ys + (size_t)p.T * p.CC);
     const int lane8 = threadIdx.x & 7;
     const int rg = threadIdx.x >> 3;
-    const int g = blockIdx.x / p.row_blocks;
+    // blockIdx.x = (group g, head part hp, row block rb); a head part runs
+    // group / head_parts of the group's value heads
+    const int g = blockIdx.x / (p.head_parts * p.row_blocks);
+    const int hp = (blockIdx.x / p.row_blocks) % p.head_parts;
     const int rb = blockIdx.x % p.row_blocks;
+    const int nh = p.group / p.head_parts;
+    const int j0 = hp * nh;
     const int b = blockIdx.y;
     const size_t C = (size_t)p.C;
     const int CC = p.CC;
@@ -281,7 +288,7 @@ gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
             h3 = load8(xb + (size_t)t * C);
             store_y(ys + (size_t)t * CC + c, w, h0, h1, h2, h3);
         }
-        if (rb == 0) {
+        if (rb == 0 && hp == 0) {
             uint16_t* to = p.tail_out + (size_t)b * GDN_CONV_W * C + gc;
             put8(to, h0);
             put8(to + C, h1);
@@ -337,7 +344,7 @@ gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
         }
         pend = false;
     };
-    for (int j = 0; j < p.group; ++j) {
+    for (int j = j0; j < j0 + nh; ++j) {
         const int h = g * p.group + j;
         float* S = state_of(j);
         float4 s[R][V];
@@ -418,7 +425,7 @@ gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
 
 template <int DK, int R, int KIND>
 static cudaError_t launch_conv_decode_t(const ConvDecodeParams& p, cudaStream_t s) {
-    dim3 grid(p.Hk * p.row_blocks, p.B, 1);
+    dim3 grid(p.Hk * p.head_parts * p.row_blocks, p.B, 1);
     const size_t smem = (size_t)p.T * p.CC * 2 + (KIND == 1 ? (size_t)p.T * p.group * DK * 4 : 0) +
                         (KIND == 2 ? (size_t)p.T * p.group * 8 : 0);
     gdn_conv_decode_kernel<DK, R, KIND><<<grid, kThreads, smem, s>>>(p);

@@ -102,6 +102,7 @@ struct ConvDecodeParams {
     int B, T, Hk, Hv, dv, group, C;
     int CC;                   // channels of one key-head group: 2 dk + group dv
     int row_blocks;           // CTAs along the value rows of one group
+    int head_parts;           // CTAs along the value heads of one group (1 or group)
     float q_scale;
     int normalize;
     int out_bf16;

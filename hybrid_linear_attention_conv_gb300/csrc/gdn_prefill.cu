@@ -333,7 +333,7 @@ gdn_prefill_prep_kernel(const __grid_constant__ PrefillParams p) {
     }
     // [K;Q] rows of the chunk (zero-filled past the last token)
     for (int idx = tid; idx < 2 * kChunk * 16; idx += kPrefillThreads) {
-        const int r = idx >> 4, kb = idx & 15;
+        const int r = ((idx >> 7) << 3) | (idx & 7), kb = (idx >> 3) & 15;  // 8 rows x 4 chunks per warp
         const int t = r & 63;
         const bool ok = t < n;
         const uint16_t* src = p.qkv + (size_t)(t0 + (ok ? t : 0)) * C + (r >= 64 ? 0 : (size_t)p.Hk * kD) +
@@ -496,7 +496,7 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
     auto issue_kq = [&](int t0, int n) {
 #pragma unroll 4
         for (int idx = tid; idx < 2 * kChunk * 16; idx += NT) {
-            const int r = idx >> 4, kb = idx & 15;
+            const int r = ((idx >> 7) << 3) | (idx & 7), kb = (idx >> 3) & 15;  // 8 rows x 4 chunks per warp
             const int t = r & 63;
             const bool ok = t < n;
             const uint16_t* src = p.qkv + (size_t)(t0 + (ok ? t : 0)) * C + (r >= 64 ? 0 : (size_t)p.Hk * kD) +
@@ -781,6 +781,413 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
+
+// ---------------------------------------------------------------------------
+// The pipelined chain (pre-pass path).  The same chunk form and the same
+// bf16 hi/lo passes as the kernel above, scheduled so that only the steps that
+// carry the state from chunk to chunk sit on the critical path:
+//   S K^T -> X^T -> U^T = X^T T^T -> Uhat^T -> S += Uhat^T K -> S operand split
+// while the output side (S Q^T, its scaling, U^T P^T, the output stores) runs
+// in the shadow of those MMAs.  X^T, Uhat^T and U^T are A operands written by
+// the epilogue threads straight to tensor memory as bf16 pairs; the pre-pass
+// records are double-buffered in shared memory and prefetched a whole chunk
+// ahead; the output accumulator is double-buffered in tensor memory, so that
+// chunk c's outputs are read out while chunk c + 1's S K^T runs.
+// ---------------------------------------------------------------------------
+constexpr int kEpiThreads = 512;    // four epilogue warpgroups over the 128 TMEM lanes
+constexpr int kChainThreads = kEpiThreads + 32;  // and one warp that only issues the MMAs
+constexpr uint32_t kRecStride = 34816;  // a record slot, padded to 1 KB
+
+constexpr uint32_t C_OFF_S_HI = 0;       // S hi  [128 i][128 j]  A of S K^T and S Q^T
+constexpr uint32_t C_OFF_S_LO = 32768;   // S lo
+constexpr uint32_t C_OFF_KQ = 65536;     // [K;Q] [128 t'][128 j] B of S K^T (rows 0..63), S Q^T (64..127)
+constexpr uint32_t C_OFF_KT = 98304;     // K^T   [128 j][64 t]   B of Uhat^T K
+constexpr uint32_t C_OFF_V = 114688;     // V     [64 t][128 i]   plain row-major
+constexpr uint32_t C_OFF_REC = 131072;   // two record slots (T hi/lo, P hi/lo, scalars)
+constexpr uint32_t C_OFF_MISC = C_OFF_REC + 2 * kRecStride;  // mbarriers, TMEM base, abort flag
+constexpr uint32_t kChainSmem = C_OFF_MISC + 128;
+
+// TMEM columns.  The state, S K^T, two output buffers and U^T are fp32
+// accumulators; X^T (later Uhat^T) and U^T as A operands hold bf16 hi in
+// their first 32 columns and lo in the next 32.
+constexpr uint32_t T_S = 0;      // S [i][j]              128 columns
+constexpr uint32_t T_KS = 128;   // (S K^T) [i][t]         64
+constexpr uint32_t T_O = 192;    // (S Q^T), then O^T      2 x 64 (by chunk parity)
+constexpr uint32_t T_U = 320;    // U^T [i][t]             64
+constexpr uint32_t T_XA = 384;   // X^T, then Uhat^T       hi 32 + lo 32 (A operand)
+constexpr uint32_t T_UA = 448;   // U^T                    hi 32 + lo 32 (A operand)
+
+__global__ void __launch_bounds__(kChainThreads, 1)
+gdn_prefill_chain_kernel(const __grid_constant__ PrefillParams p) {
+    constexpr int CW = kChunk / 4;  // columns of a 64-wide tile per warpgroup
+    constexpr int CS = kD / 4;      // columns of the state per warpgroup
+    extern __shared__ __align__(1024) uint8_t sm[];
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const bool issuer = tid == kEpiThreads;    // lane 0 of the MMA warp
+    const bool epi = tid < kEpiThreads;        // an epilogue thread
+    const int h = blockIdx.x;
+    const int g = h / p.group;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C_OFF_MISC);  // 6 mbarriers
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C_OFF_MISC + 96);
+    int* abort_flag = reinterpret_cast<int*>(sm + C_OFF_MISC + 100);
+    const uint32_t sbase = smem_u32(sm);
+    const uint32_t bar_ks = smem_u32(bars + 0);    // S K^T
+    const uint32_t bar_q = smem_u32(bars + 1);     // S Q^T
+    const uint32_t bar_e = smem_u32(bars + 2);     // X^T T^T
+    const uint32_t bar_s = smem_u32(bars + 3);     // state update
+    const uint32_t bar_o = smem_u32(bars + 4);     // U^T P^T
+    const uint32_t bar_fin = smem_u32(bars + 5);   // every MMA issued, before TMEM is freed
+
+    if (warp == 0) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    if (tid == 0) {
+        for (int b = 0; b < 6; ++b) mbar_init(smem_u32(bars + b), 1);
+        *abort_flag = 0;
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const int i = tid & 127;   // TMEM lane = state row
+    const int wg = tid >> 7;   // warpgroup: a quarter of every row's columns
+    const int s0 = wg * CW;
+    const int c0 = wg * CS;
+    const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+
+    // a bounded wait on one of the per-chunk barriers (each completes once per
+    // chunk); a timeout only raises the flag, which every thread checks at the
+    // end of the chunk, so no thread leaves a barrier the others still reach
+    auto wait_mma = [&](uint32_t b, int chunk) {
+        if (!mbar_wait(b, (uint32_t)chunk & 1u, kWaitLimitNs)) atomicOr(abort_flag, 1);
+        __syncwarp();  // the tcgen05.ld that follow are warp-collective
+        fence_after_sync();
+    };
+
+    // ---- prologue: state row i -> TMEM lane i and the bf16 hi/lo operand tiles
+    float* srow = p.state + ((size_t)h * kD + i) * kD;
+#pragma unroll 1
+    for (int cc = c0; cc < (epi ? c0 + CS : c0); cc += 16) {
+        float v[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 f = *reinterpret_cast<const float4*>(srow + cc + 4 * q);
+            v[4 * q] = f.x;
+            v[4 * q + 1] = f.y;
+            v[4 * q + 2] = f.z;
+            v[4 * q + 3] = f.w;
+        }
+        tmem_st16(trow + T_S + cc, v);
+        store_split8(sm + C_OFF_S_HI + core_off(i, cc, kD), sm + C_OFF_S_LO + core_off(i, cc, kD), v);
+        store_split8(sm + C_OFF_S_HI + core_off(i, cc + 8, kD), sm + C_OFF_S_LO + core_off(i, cc + 8, kD), v + 8);
+    }
+    tmem_wait_st();
+
+    const int nchunks = (p.T + kChunk - 1) / kChunk;
+    const size_t C = (size_t)p.C;
+    auto issue_kq = [&](int t0, int n) {
+#pragma unroll 4
+        for (int idx = tid; idx < 2 * kChunk * 16; idx += kEpiThreads) {
+            const int r = ((idx >> 7) << 3) | (idx & 7), kb = (idx >> 3) & 15;  // 8 rows x 4 chunks per warp
+            const int t = r & 63;
+            const bool ok = t < n;
+            const uint16_t* src = p.qkv + (size_t)(t0 + (ok ? t : 0)) * C + (r >= 64 ? 0 : (size_t)p.Hk * kD) +
+                                  (size_t)g * kD + kb * 8;
+            cp_async16(sbase + C_OFF_KQ + core_off(r, kb * 8, kD), src, ok);
+        }
+    };
+    const int lane = tid & 31;
+    auto issue_v = [&](int t0, int n) {
+#pragma unroll 2
+        for (int idx = tid; idx < kChunk * 16; idx += kEpiThreads) {
+            const int t = idx >> 4, kb = idx & 15;
+            const bool ok = t < n;
+            const uint16_t* src =
+                p.qkv + (size_t)(t0 + (ok ? t : 0)) * C + (size_t)2 * p.Hk * kD + (size_t)h * kD + kb * 8;
+            cp_async16(sbase + C_OFF_V + t * 256 + kb * 16, src, ok);
+        }
+    };
+    // chunk cc's record (T and P tiles, scalars) into slot cc & 1
+    auto issue_rec = [&](int cc) {
+        const uint8_t* rec =
+            reinterpret_cast<const uint8_t*>(p.status) + kRecBase + ((size_t)cc * p.Hv + h) * kRecBytes;
+        const uint32_t dst = sbase + C_OFF_REC + (uint32_t)(cc & 1) * kRecStride;
+#pragma unroll 4
+        for (int v = tid; v < (int)(kRecBytes / 16); v += kEpiThreads) cp_async16(dst + v * 16, rec + v * 16, true);
+    };
+    if (epi) {
+        issue_kq(0, min(kChunk, p.T));
+        issue_v(0, min(kChunk, p.T));
+        issue_rec(0);
+    }
+    cp_async_commit();
+    cp_async_wait_all();
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+
+    // Operand descriptors, computed once: an MMA issue is then a 64-bit add
+    // and the instruction (step ks of a K-major tile starts 256 B, i.e. 16
+    // descriptor units, further on).  The issuing thread shares its SM
+    // sub-partition with busy epilogue warps, so its instruction stream must
+    // stay short for the tensor pipe to be fed at its own rate.
+    const uint64_t d_s_hi = smem_desc(sbase + C_OFF_S_HI, kD * 16);
+    const uint64_t d_s_lo = smem_desc(sbase + C_OFF_S_LO, kD * 16);
+    const uint64_t d_k = smem_desc(sbase + C_OFF_KQ, kD * 16);
+    const uint64_t d_q = smem_desc(sbase + C_OFF_KQ + 64 * 16 * 16, kD * 16);
+    const uint64_t d_kt = smem_desc(sbase + C_OFF_KT, kChunk * 16);
+    const uint64_t d_rec0 = smem_desc(sbase + C_OFF_REC + REC_TILES, kChunk * 16);
+    constexpr uint64_t kRecDesc = kRecStride >> 4;  // slot 1 vs slot 0
+    constexpr uint64_t kTLo = 8192 >> 4, kPHi = 16384 >> 4, kPLo = 24576 >> 4;
+
+    const size_t ostride = (size_t)p.Hv * kD;
+    // outputs of chunk cc (its O^T buffer, after U^T P^T completed)
+    auto store_outputs = [&](int cc) {
+        const int t0 = cc * kChunk;
+        const int n = min(kChunk, p.T - t0);
+        float o[16];
+        tmem_ld16(trow + T_O + (uint32_t)(cc & 1) * 64 + s0, o);
+        const size_t obase = (size_t)(t0 + s0) * ostride + (size_t)h * kD + i;
+        if (p.out_bf16) {
+            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + obase;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (s0 + j < n) dst[(size_t)j * ostride] = __float2bfloat16_rn(o[j]);
+        } else if (n == kChunk) {
+            float* dst = reinterpret_cast<float*>(p.out) + obase;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) dst[(size_t)j * ostride] = o[j];
+        } else {
+            float* dst = reinterpret_cast<float*>(p.out) + obase;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (s0 + j < n) dst[(size_t)j * ostride] = o[j];
+        }
+    };
+
+#pragma unroll 1
+    for (int c = 0; c < nchunks; ++c) {
+        const int t0 = c * kChunk;
+        const uint32_t o_col = T_O + (uint32_t)(c & 1) * 64;
+        const uint8_t* rec = sm + C_OFF_REC + (uint32_t)(c & 1) * kRecStride;
+        const float* s_beta = reinterpret_cast<const float*>(rec + REC_SCAL);  // beta_t
+        const float* s_lg = s_beta + 64;   // log2 gamma_t
+        const float* s_gk = s_beta + 128;  // gamma_t r_k,t
+        const float* s_gq = s_beta + 192;  // gamma_t q_scale r_q,t
+        const float* s_ck = s_beta + 256;  // (gamma_C / gamma_t) r_k,t
+        const uint64_t d_rec = d_rec0 + (uint64_t)(c & 1) * kRecDesc;  // T hi of this chunk's record
+
+        // ---- A: K^T from the staged K rows (inputs of chunk c have landed)
+        if (epi) {
+#pragma unroll
+            for (int it = 0; it < 128 / (kEpiThreads / 32) / 4; ++it) {
+                const int q = warp * (128 / (kEpiThreads / 32)) + it * 4 + (lane >> 3);
+                const int tb = q >> 4, jb = q & 15;
+                const uint32_t src = sbase + C_OFF_KQ + tb * (kD * 16) + jb * 128 + (lane & 7) * 16;
+                const uint32_t dst = sbase + C_OFF_KT + jb * (kChunk * 16) + tb * 128 + (lane & 7) * 16;
+                transpose_8x8x4(src, dst);
+            }
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+
+        // ---- B: S K^T (critical), then S Q^T into this chunk's output buffer
+        if (issuer) {
+            fence_after_sync();
+            constexpr uint32_t id = idesc_bf16(128, 64);
+#pragma unroll
+            for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+                for (int ks = 0; ks < kD / 16; ++ks)
+                    mma_bf16(tmem + T_KS, (pass ? d_s_lo : d_s_hi) + 16 * ks, d_k + 16 * ks, id, (pass > 0 || ks > 0));
+            mma_commit(bar_ks);
+#pragma unroll
+            for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+                for (int ks = 0; ks < kD / 16; ++ks)
+                    mma_bf16(tmem + o_col, (pass ? d_s_lo : d_s_hi) + 16 * ks, d_q + 16 * ks, id, (pass > 0 || ks > 0));
+            mma_commit(bar_q);
+        }
+        if (epi) {
+            // in the shadow of S K^T: the previous chunk's outputs, then the
+            // next record into the slot they freed; S <- gamma_C S
+            if (c > 0) {
+                wait_mma(bar_o, c - 1);
+                store_outputs(c - 1);
+            }
+            if (c + 1 < nchunks) {
+                issue_rec(c + 1);
+                cp_async_commit();
+            }
+            {
+                const float gamma_c = exp2f(s_lg[kChunk - 1]);
+                const float2 g2 = make_float2(gamma_c, gamma_c);
+#pragma unroll 1
+                for (int cc = c0; cc < c0 + CS; cc += 16) {
+                    float sv[16];
+                    tmem_ld16(trow + T_S + cc, sv);
+#pragma unroll
+                    for (int j = 0; j < 16; j += 2) {
+                        const float2 r = __fmul2_rn(make_float2(sv[j], sv[j + 1]), g2);
+                        sv[j] = r.x;
+                        sv[j + 1] = r.y;
+                    }
+                    tmem_st16(trow + T_S + cc, sv);
+                }
+            }
+            wait_mma(bar_ks, c);
+
+            // ---- C: X^T[i][s] = beta_s (v_s[i] - gamma_s r_k,s (S k_s)[i]) as the A operand of X^T T^T
+            {
+                const uint16_t* vcol = reinterpret_cast<const uint16_t*>(sm + C_OFF_V) + i;
+                float ks[16], x[16];
+                tmem_ld16(trow + T_KS + s0, ks);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 b4 = reinterpret_cast<const float4*>(s_beta + s0)[q];
+                    const float4 g4 = reinterpret_cast<const float4*>(s_gk + s0)[q];
+                    const int sj = s0 + 4 * q;
+                    const float2 lo = __fmul2_rn(make_float2(b4.x, b4.y),
+                                                 __ffma2_rn(make_float2(-g4.x, -g4.y), make_float2(ks[4 * q], ks[4 * q + 1]),
+                                                            make_float2(bf16_to_f(vcol[sj * kD]), bf16_to_f(vcol[(sj + 1) * kD]))));
+                    const float2 hi = __fmul2_rn(make_float2(b4.z, b4.w),
+                                                 __ffma2_rn(make_float2(-g4.z, -g4.w), make_float2(ks[4 * q + 2], ks[4 * q + 3]),
+                                                            make_float2(bf16_to_f(vcol[(sj + 2) * kD]), bf16_to_f(vcol[(sj + 3) * kD]))));
+                    x[4 * q] = lo.x;
+                    x[4 * q + 1] = lo.y;
+                    x[4 * q + 2] = hi.x;
+                    x[4 * q + 3] = hi.y;
+                }
+                uint32_t hi[8], lo[8];
+                split_pack16(x, hi, lo);
+                tmem_st8(trow + T_XA + s0 / 2, hi);
+                tmem_st8(trow + T_XA + 32 + s0 / 2, lo);
+                tmem_wait_st();  // also covers the S rescale above
+            }
+        }
+        fence_before_sync();
+        __syncthreads();
+
+        // ---- E: U^T = X^T T^T (3 passes: hi.hi, hi.lo, lo.hi)
+        if (issuer) {
+            fence_after_sync();
+            constexpr uint32_t id = idesc_bf16(128, 64);
+#pragma unroll
+            for (int pass = 0; pass < 3; ++pass)  // (X hi, T hi), (X hi, T lo), (X lo, T hi)
+#pragma unroll
+                for (int ks = 0; ks < kChunk / 16; ++ks)
+                    mma_bf16_ts(tmem + T_U, tmem + T_XA + (pass == 2 ? 32 : 0) + ks * 8,
+                                d_rec + (pass == 1 ? kTLo : 0) + 16 * ks, id, (pass > 0 || ks > 0));
+            mma_commit(bar_e);
+        }
+        if (epi) {
+            // X^T has read this chunk's v rows: the next chunk's behind them
+            if (c + 1 < nchunks) {
+                issue_v(t0 + kChunk, min(kChunk, p.T - t0 - kChunk));
+                cp_async_commit();
+            }
+            // in the shadow of X^T T^T: scale S Q^T by gamma_t q_scale r_q,t
+            // (the start of O^T), then the next chunk's [K;Q] rows into the freed tile
+            wait_mma(bar_q, c);
+            {
+                float qs[16];
+                tmem_ld16(trow + o_col + s0, qs);
+                mul16(qs, s_gq + s0);
+                tmem_st16(trow + o_col + s0, qs);
+            }
+            if (c + 1 < nchunks) {
+                issue_kq(t0 + kChunk, min(kChunk, p.T - t0 - kChunk));
+                cp_async_commit();
+            }
+            wait_mma(bar_e, c);
+
+            // ---- F: Uhat^T = U^T diag(gamma_C / gamma r_k) and U^T as A operands
+            {
+                float u[16], uh[16];
+                tmem_ld16(trow + T_U + s0, u);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) uh[j] = u[j];
+                mul16(uh, s_ck + s0);
+                uint32_t hi[8], lo[8];
+                split_pack16(uh, hi, lo);
+                tmem_st8(trow + T_XA + s0 / 2, hi);
+                tmem_st8(trow + T_XA + 32 + s0 / 2, lo);
+                split_pack16(u, hi, lo);
+                tmem_st8(trow + T_UA + s0 / 2, hi);
+                tmem_st8(trow + T_UA + 32 + s0 / 2, lo);
+                tmem_wait_st();  // also covers the O^T scaling above
+            }
+        }
+        fence_before_sync();
+        __syncthreads();
+
+        // ---- G: S += Uhat^T K (2 passes); then O^T += U^T P^T (3 passes)
+        if (issuer) {
+            fence_after_sync();
+            constexpr uint32_t id_s = idesc_bf16(128, 128);
+            constexpr uint32_t id_o = idesc_bf16(128, 64);
+#pragma unroll
+            for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+                for (int ks = 0; ks < kChunk / 16; ++ks)
+                    mma_bf16_ts(tmem + T_S, tmem + T_XA + (pass ? 32 : 0) + ks * 8, d_kt + 16 * ks, id_s, 1u);
+            mma_commit(bar_s);
+#pragma unroll
+            for (int pass = 0; pass < 3; ++pass)  // (U hi, P hi), (U hi, P lo), (U lo, P hi)
+#pragma unroll
+                for (int ks = 0; ks < kChunk / 16; ++ks)
+                    mma_bf16_ts(tmem + o_col, tmem + T_UA + (pass == 2 ? 32 : 0) + ks * 8,
+                                d_rec + (pass == 1 ? kPLo : kPHi) + 16 * ks, id_o, 1u);
+            mma_commit(bar_o);
+        }
+        if (epi) {
+            wait_mma(bar_s, c);
+
+            // ---- H: the next chunk's S operands, or the final state
+            const bool last = (c == nchunks - 1);
+#pragma unroll 1
+            for (int cc = c0; cc < c0 + CS; cc += 16) {
+                float sv[16];
+                tmem_ld16(trow + T_S + cc, sv);
+                if (last) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<float4*>(srow + cc + 4 * q) =
+                            make_float4(sv[4 * q], sv[4 * q + 1], sv[4 * q + 2], sv[4 * q + 3]);
+                } else {
+                    store_split8(sm + C_OFF_S_HI + core_off(i, cc, kD), sm + C_OFF_S_LO + core_off(i, cc, kD), sv);
+                    store_split8(sm + C_OFF_S_HI + core_off(i, cc + 8, kD), sm + C_OFF_S_LO + core_off(i, cc + 8, kD),
+                                 sv + 8);
+                }
+            }
+            cp_async_wait_all();  // the next chunk's [K;Q], v and record
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        if (*abort_flag != 0) break;
+    }
+
+    if (epi && *abort_flag == 0 && nchunks > 0) {
+        wait_mma(bar_o, nchunks - 1);
+        store_outputs(nchunks - 1);
+    }
+    cp_async_wait_all();  // no prefetch may still be writing shared memory at exit
+    // every MMA this CTA issued has completed before TMEM is released
+    fence_before_sync();
+    __syncthreads();
+    if (issuer) {
+        fence_after_sync();
+        mma_commit(bar_fin);
+    }
+    if (!mbar_wait(bar_fin, 0, kWaitLimitNs)) atomicOr(abort_flag, 1);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (*abort_flag != 0 && tid == 0) atomicExch(p.status, 1);
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
 }  // namespace
 }  // namespace gdn
 
@@ -834,8 +1241,8 @@ int launch_prefill(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const
     cudaGetDevice(&dev);
     cudaError_t e;
     if (dev >= 0 && dev < 64 && !configured[dev]) {
-        e = cudaFuncSetAttribute(gdn_prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kPrefillSmem);
+        e = cudaFuncSetAttribute(gdn_prefill_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kChainSmem);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(gdn_prefill_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kPrefillSmem);
@@ -863,7 +1270,7 @@ int launch_prefill(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const
     if (prep) {
         const dim3 grid((unsigned)((T + kChunk - 1) / kChunk), (unsigned)shape->Hk);
         gdn_prefill_prep_kernel<<<grid, kPrefillThreads, kPrepSmem, st>>>(p);
-        gdn_prefill_tc_kernel<true><<<shape->Hv, chain_threads<true>(), kPrefillSmem, st>>>(p);
+        gdn_prefill_chain_kernel<<<shape->Hv, kChainThreads, kChainSmem, st>>>(p);
     } else {
         gdn_prefill_tc_kernel<false><<<shape->Hv, chain_threads<false>(), kPrefillSmem, st>>>(p);
     }

@@ -50,6 +50,18 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
+// The same with A read from tensor memory: an M = 128 x K = 16 bf16 slice is
+// 128 lanes x 8 columns starting at `a_tmem`, column c of a lane holding
+// elements k = 2c (low 16 bits) and 2c + 1 (high 16 bits); the next K slice
+// starts 8 columns on.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
 // Arrive on `bar` once every MMA issued so far by this thread has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -102,6 +114,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
         "r"(__float_as_uint(v[15]))
         : "memory");
 }
+// 8 consecutive 32-bit columns of this thread's TMEM lane (raw words).
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&w)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -116,15 +134,18 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 // Wait for phase `parity` of `bar` to complete; give up after `limit_ns`.
+// Each try_wait may suspend the thread (up to the hint) until the phase
+// completes, so waiting warps do not take issue slots from working ones.
+constexpr uint32_t kSuspendHintNs = 20000;
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     const uint64_t t0 = global_ns();
     while (true) {
         uint32_t ok;
         asm volatile(
-            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
             "selp.u32 %0, 1, 0, p;\n\t}\n"
             : "=r"(ok)
-            : "r"(bar), "r"(parity)
+            : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
             : "memory");
         if (ok) return true;
         if (global_ns() - t0 > limit_ns) return false;
@@ -141,15 +162,48 @@ __device__ __forceinline__ uint32_t pack_bf16(__nv_bfloat16 a, __nv_bfloat16 b) 
     return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
 }
 
+// Split a pair (a, b) into packed bf16 hi and lo words (a in the low 16
+// bits): hi = RNE(x), lo = RNE(x - hi), where x - hi is exact in fp32 -- the
+// same roundings as split_bf16, with paired conversions and one fp32x2 FMA.
+__device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const uint32_t hw = *reinterpret_cast<const uint32_t*>(&h);
+    const float2 r = __ffma2_rn(make_float2(__uint_as_float(hw << 16), __uint_as_float(hw & 0xffff0000u)),
+                                make_float2(-1.0f, -1.0f), make_float2(a, b));
+    const __nv_bfloat162 l = __floats2bfloat162_rn(r.x, r.y);
+    hi = hw;
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 // Split 8 floats and store them as one 16-byte row segment of a hi and a lo tile.
 __device__ __forceinline__ void store_split8(uint8_t* hi_dst, uint8_t* lo_dst, const float* x) {
-    __nv_bfloat16 h[8], l[8];
+    uint32_t h[4], l[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) split_bf16(x[e], h[e], l[e]);
-    *reinterpret_cast<uint4*>(hi_dst) =
-        make_uint4(pack_bf16(h[0], h[1]), pack_bf16(h[2], h[3]), pack_bf16(h[4], h[5]), pack_bf16(h[6], h[7]));
-    *reinterpret_cast<uint4*>(lo_dst) =
-        make_uint4(pack_bf16(l[0], l[1]), pack_bf16(l[2], l[3]), pack_bf16(l[4], l[5]), pack_bf16(l[6], l[7]));
+    for (int e = 0; e < 4; ++e) split_pair(x[2 * e], x[2 * e + 1], h[e], l[e]);
+    *reinterpret_cast<uint4*>(hi_dst) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(lo_dst) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// Split 16 floats into bf16 hi and lo halves packed two per word (element
+// 2e in the low 16 bits), the layout of an A operand slice in tensor memory.
+__device__ __forceinline__ void split_pack16(const float (&x)[16], uint32_t (&hi)[8], uint32_t (&lo)[8]) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) split_pair(x[2 * e], x[2 * e + 1], hi[e], lo[e]);
+}
+
+// x[j] *= f[j] for 16 values on the fp32x2 pipe (each element rounded as the
+// scalar multiply would be); f is 16 floats in shared memory, 16-byte aligned.
+__device__ __forceinline__ void mul16(float (&x)[16], const float* f) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 m = reinterpret_cast<const float4*>(f)[q];
+        const float2 a = __fmul2_rn(make_float2(x[4 * q], x[4 * q + 1]), make_float2(m.x, m.y));
+        const float2 b = __fmul2_rn(make_float2(x[4 * q + 2], x[4 * q + 3]), make_float2(m.z, m.w));
+        x[4 * q] = a.x;
+        x[4 * q + 1] = a.y;
+        x[4 * q + 2] = b.x;
+        x[4 * q + 3] = b.y;
+    }
 }
 
 // Asynchronous 16-byte global -> shared copy; zero-fills when !valid.

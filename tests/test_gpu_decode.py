@@ -232,7 +232,7 @@ def test_conv_decode_pipeline(shape):
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("shape,T,pingpong", [
     (gen.QWEN_27B.with_batch(4), 1, False),
-    (gen.QWEN_27B.with_batch(1), 1, True),      # distinct tails: rows split over CTAs
+    (gen.QWEN_27B.with_batch(1), 1, True),      # distinct tails: rows and heads split over CTAs
     (gen.QWEN_27B.with_batch(2), 3, True),
     (gen.TINY, 16, False),
     (gen.Shape(3, 2, 4, 32, 64), 2, True),      # dk != dv
