@@ -807,15 +807,16 @@ constexpr uint32_t C_OFF_REC = 131072;   // two record slots (T hi/lo, P hi/lo, 
 constexpr uint32_t C_OFF_MISC = C_OFF_REC + 2 * kRecStride;  // mbarriers, TMEM base, abort flag
 constexpr uint32_t kChainSmem = C_OFF_MISC + 128;
 
-// TMEM columns.  The state, S K^T, two output buffers and U^T are fp32
-// accumulators; X^T (later Uhat^T) and U^T as A operands hold bf16 hi in
-// their first 32 columns and lo in the next 32.
-constexpr uint32_t T_S = 0;      // S [i][j]              128 columns
-constexpr uint32_t T_KS = 128;   // (S K^T) [i][t]         64
-constexpr uint32_t T_O = 192;    // (S Q^T), then O^T      2 x 64 (by chunk parity)
-constexpr uint32_t T_U = 320;    // U^T [i][t]             64
-constexpr uint32_t T_XA = 384;   // X^T, then Uhat^T       hi 32 + lo 32 (A operand)
-constexpr uint32_t T_UA = 448;   // U^T                    hi 32 + lo 32 (A operand)
+// TMEM columns.  The state, S [K;Q]^T and U^T are fp32 accumulators; X^T
+// (later Uhat^T) and U^T as A operands hold bf16 hi in their first 32
+// columns and lo in the next 32.  S [K;Q]^T is double-buffered by chunk
+// parity: its S K^T half feeds X^T, its S Q^T half becomes O^T, which is read
+// out while the next chunk runs.  U^T as an A operand overwrites the fp32 U^T
+// it is made from.
+constexpr uint32_t T_S = 0;      // S [i][j]                               128 columns
+constexpr uint32_t T_D = 128;    // [S K^T | S Q^T -> O^T] [i][t], 2 x 128 (by chunk parity)
+constexpr uint32_t T_U = 384;    // U^T fp32, then U^T hi 32 + lo 32      64
+constexpr uint32_t T_XA = 448;   // X^T, then Uhat^T       hi 32 + lo 32  64
 
 __global__ void __launch_bounds__(kChainThreads, 1)
 gdn_prefill_chain_kernel(const __grid_constant__ PrefillParams p) {
@@ -832,8 +833,7 @@ gdn_prefill_chain_kernel(const __grid_constant__ PrefillParams p) {
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C_OFF_MISC + 96);
     int* abort_flag = reinterpret_cast<int*>(sm + C_OFF_MISC + 100);
     const uint32_t sbase = smem_u32(sm);
-    const uint32_t bar_ks = smem_u32(bars + 0);    // S K^T
-    const uint32_t bar_q = smem_u32(bars + 1);     // S Q^T
+    const uint32_t bar_ks = smem_u32(bars + 0);    // S [K;Q]^T
     const uint32_t bar_e = smem_u32(bars + 2);     // X^T T^T
     const uint32_t bar_s = smem_u32(bars + 3);     // state update
     const uint32_t bar_o = smem_u32(bars + 4);     // U^T P^T
@@ -933,7 +933,6 @@ gdn_prefill_chain_kernel(const __grid_constant__ PrefillParams p) {
     const uint64_t d_s_hi = smem_desc(sbase + C_OFF_S_HI, kD * 16);
     const uint64_t d_s_lo = smem_desc(sbase + C_OFF_S_LO, kD * 16);
     const uint64_t d_k = smem_desc(sbase + C_OFF_KQ, kD * 16);
-    const uint64_t d_q = smem_desc(sbase + C_OFF_KQ + 64 * 16 * 16, kD * 16);
     const uint64_t d_kt = smem_desc(sbase + C_OFF_KT, kChunk * 16);
     const uint64_t d_rec0 = smem_desc(sbase + C_OFF_REC + REC_TILES, kChunk * 16);
     constexpr uint64_t kRecDesc = kRecStride >> 4;  // slot 1 vs slot 0
@@ -945,7 +944,7 @@ gdn_prefill_chain_kernel(const __grid_constant__ PrefillParams p) {
         const int t0 = cc * kChunk;
         const int n = min(kChunk, p.T - t0);
         float o[16];
-        tmem_ld16(trow + T_O + (uint32_t)(cc & 1) * 64 + s0, o);
+        tmem_ld16(trow + T_D + (uint32_t)(cc & 1) * 128 + 64 + s0, o);
         const size_t obase = (size_t)(t0 + s0) * ostride + (size_t)h * kD + i;
         if (p.out_bf16) {
             __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + obase;
@@ -967,7 +966,7 @@ gdn_prefill_chain_kernel(const __grid_constant__ PrefillParams p) {
 #pragma unroll 1
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = c * kChunk;
-        const uint32_t o_col = T_O + (uint32_t)(c & 1) * 64;
+        const uint32_t d_col = T_D + (uint32_t)(c & 1) * 128;  // S K^T here, O^T at + 64
         const uint8_t* rec = sm + C_OFF_REC + (uint32_t)(c & 1) * kRecStride;
         const float* s_beta = reinterpret_cast<const float*>(rec + REC_SCAL);  // beta_t
         const float* s_lg = s_beta + 64;   // log2 gamma_t
@@ -991,26 +990,20 @@ gdn_prefill_chain_kernel(const __grid_constant__ PrefillParams p) {
         fence_before_sync();
         __syncthreads();
 
-        // ---- B: S K^T (critical), then S Q^T into this chunk's output buffer
+        // ---- B: S [K;Q]^T (S hi, S lo) into this chunk's buffer
         if (issuer) {
             fence_after_sync();
-            constexpr uint32_t id = idesc_bf16(128, 64);
+            constexpr uint32_t id = idesc_bf16(128, 128);
 #pragma unroll
             for (int pass = 0; pass < 2; ++pass)
 #pragma unroll
                 for (int ks = 0; ks < kD / 16; ++ks)
-                    mma_bf16(tmem + T_KS, (pass ? d_s_lo : d_s_hi) + 16 * ks, d_k + 16 * ks, id, (pass > 0 || ks > 0));
+                    mma_bf16(tmem + d_col, (pass ? d_s_lo : d_s_hi) + 16 * ks, d_k + 16 * ks, id, (pass > 0 || ks > 0));
             mma_commit(bar_ks);
-#pragma unroll
-            for (int pass = 0; pass < 2; ++pass)
-#pragma unroll
-                for (int ks = 0; ks < kD / 16; ++ks)
-                    mma_bf16(tmem + o_col, (pass ? d_s_lo : d_s_hi) + 16 * ks, d_q + 16 * ks, id, (pass > 0 || ks > 0));
-            mma_commit(bar_q);
         }
         if (epi) {
-            // in the shadow of S K^T: the previous chunk's outputs, then the
-            // next record into the slot they freed; S <- gamma_C S
+            // in the shadow of S [K;Q]^T: the previous chunk's outputs, then
+            // the next record into the slot they freed; S <- gamma_C S
             if (c > 0) {
                 wait_mma(bar_o, c - 1);
                 store_outputs(c - 1);
@@ -1041,7 +1034,7 @@ gdn_prefill_chain_kernel(const __grid_constant__ PrefillParams p) {
             {
                 const uint16_t* vcol = reinterpret_cast<const uint16_t*>(sm + C_OFF_V) + i;
                 float ks[16], x[16];
-                tmem_ld16(trow + T_KS + s0, ks);
+                tmem_ld16(trow + d_col + s0, ks);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const float4 b4 = reinterpret_cast<const float4*>(s_beta + s0)[q];
@@ -1087,13 +1080,13 @@ gdn_prefill_chain_kernel(const __grid_constant__ PrefillParams p) {
                 cp_async_commit();
             }
             // in the shadow of X^T T^T: scale S Q^T by gamma_t q_scale r_q,t
-            // (the start of O^T), then the next chunk's [K;Q] rows into the freed tile
-            wait_mma(bar_q, c);
+            // (the start of O^T), then the next chunk's [K;Q] rows into the
+            // tile S [K;Q]^T has read
             {
                 float qs[16];
-                tmem_ld16(trow + o_col + s0, qs);
+                tmem_ld16(trow + d_col + 64 + s0, qs);
                 mul16(qs, s_gq + s0);
-                tmem_st16(trow + o_col + s0, qs);
+                tmem_st16(trow + d_col + 64 + s0, qs);
             }
             if (c + 1 < nchunks) {
                 issue_kq(t0 + kChunk, min(kChunk, p.T - t0 - kChunk));
@@ -1113,8 +1106,11 @@ gdn_prefill_chain_kernel(const __grid_constant__ PrefillParams p) {
                 tmem_st8(trow + T_XA + s0 / 2, hi);
                 tmem_st8(trow + T_XA + 32 + s0 / 2, lo);
                 split_pack16(u, hi, lo);
-                tmem_st8(trow + T_UA + s0 / 2, hi);
-                tmem_st8(trow + T_UA + 32 + s0 / 2, lo);
+                // U^T hi/lo overwrite the fp32 U^T: every epilogue warp has
+                // read its columns first (named barrier 1 over the epilogue warps)
+                asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+                tmem_st8(trow + T_U + s0 / 2, hi);
+                tmem_st8(trow + T_U + 32 + s0 / 2, lo);
                 tmem_wait_st();  // also covers the O^T scaling above
             }
         }
@@ -1136,7 +1132,7 @@ gdn_prefill_chain_kernel(const __grid_constant__ PrefillParams p) {
             for (int pass = 0; pass < 3; ++pass)  // (U hi, P hi), (U hi, P lo), (U lo, P hi)
 #pragma unroll
                 for (int ks = 0; ks < kChunk / 16; ++ks)
-                    mma_bf16_ts(tmem + o_col, tmem + T_UA + (pass == 2 ? 32 : 0) + ks * 8,
+                    mma_bf16_ts(tmem + d_col + 64, tmem + T_U + (pass == 2 ? 32 : 0) + ks * 8,
                                 d_rec + (pass == 1 ? kPLo : kPHi) + 16 * ks, id_o, 1u);
             mma_commit(bar_o);
         }
