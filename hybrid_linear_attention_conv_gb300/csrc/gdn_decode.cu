@@ -111,7 +111,7 @@ __host__ __device__ constexpr size_t tree_kq_bytes(int N) {
 
 template <int DK>
 __host__ __device__ constexpr size_t tree_stage_bytes(int N) {
-    return tree_kq_bytes<DK>(N) + (size_t)N * (kRowsPerPass * 2 + 2 * 4);
+    return tree_kq_bytes<DK>(N) + (size_t)N * (kRowsPerPass * 2 + 2 * 4 + sizeof(TreeStep));
 }
 
 template <int DK, int MB>
@@ -120,7 +120,6 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     constexpr int V = DK / 32;
     const int tree = blockIdx.z;          // sequence b: its own tree and state
     const int N = p.N[tree];
-    const TreeStep* steps = p.steps[tree];
     const uint16_t* qkv = p.qkv + (size_t)tree * p.Nmax * p.C;
     const float* alpha_b = p.alpha + (size_t)tree * p.Nmax * p.Hv;
     const float* beta_b = p.beta + (size_t)tree * p.Nmax * p.Hv;
@@ -130,6 +129,9 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     float4* s_kq = reinterpret_cast<float4*>(stage);                                   // per-node records
     uint16_t* s_v = reinterpret_cast<uint16_t*>(stage + tree_kq_bytes<DK>(p.Nmax));        // [N][32]
     float* s_ab = reinterpret_cast<float*>(s_v + (size_t)p.Nmax * kRowsPerPass);            // [N][alpha, beta]
+    // the walk's schedule, copied out of the parameter block (read once per
+    // step on the walk's dependent chain)
+    TreeStep* steps = reinterpret_cast<TreeStep*>(s_ab + 2 * (size_t)p.Nmax);
     const int lane8 = threadIdx.x & 7;
     const int rg = threadIdx.x >> 3;
     const int h = blockIdx.y;
@@ -149,6 +151,7 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
         for (int n = threadIdx.x; n < N; n += kThreads) {
             s_ab[2 * n] = alpha_b[(size_t)n * p.Hv + h];
             s_ab[2 * n + 1] = beta_b[(size_t)n * p.Hv + h];
+            steps[n] = p.steps[tree][n];
         }
     }
     const float* S = p.state + ((size_t)tree * p.Hv + h) * p.dv * DK + (size_t)row * DK;
@@ -193,9 +196,10 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
         }
         t.kq = s_kq[(size_t)n * KQ_REC + 8 * 2 * V].x;
     };
-    TokenKQ<V> cur, nxt;
-    fetch(steps[0].node, cur);
-    for (int step = 0; step < N; ++step) {
+    // one step of the walk on the node record `cur`, fetching the next
+    // step's record into `nxt` (the loop below alternates the two, so no
+    // record is copied between steps)
+    auto walk_step = [&](int step, const TokenKQ<V>& cur, TokenKQ<V>& nxt) {
         const TreeStep st = steps[step];
         if (st.restore >= 0) {
 #pragma unroll
@@ -212,7 +216,12 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
 #pragma unroll
             for (int m = 0; m < V; ++m) slots[((st.save * kRowsPerPass + rg) * V + m) * 8 + lane8] = s[m];
         }
-        cur = nxt;
+    };
+    TokenKQ<V> ka, kb;
+    fetch(steps[0].node, ka);
+    for (int step = 0; step < N; step += 2) {
+        walk_step(step, ka, kb);
+        if (step + 1 < N) walk_step(step + 1, kb, ka);
     }
 }
 
