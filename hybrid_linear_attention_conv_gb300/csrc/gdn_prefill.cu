@@ -86,6 +86,8 @@ struct PrefillParams {
     float* state;
     void* out;
     int* status;
+    int* ready;         // per (chunk, key head): 1 once the pre-pass record is written (cooperative form)
+    int n_workers;      // pre-pass worker CTAs of the cooperative form
     int T, Hk, Hv, C, group;
     float q_scale;
     int normalize;
@@ -94,12 +96,23 @@ struct PrefillParams {
 
 __device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
+// Barriers over the threads that run a chunk-local step: the whole CTA, or
+// the first N threads of it (named barrier ID) when other warps of the CTA
+// do something else meanwhile.
+struct CtaSync {
+    __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
+template <int ID, int N>
+struct NamedSync {
+    __device__ __forceinline__ void operator()() const { asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(N) : "memory"); }
+};
+
 // One block row BI of the blocked triangular inverse (T zero above its block
 // diagonal, blocks left of BI already final): with W = 16 BI,
 //   R = L[W:W+16][0:W] T[0:W][0:W],   T[W:W+16][0:W] = -T[W:W+16][W:W+16] R.
 // Trip counts are compile-time, so the sums unroll with independent chains.
-template <int BI>
-__device__ __forceinline__ void block_row_solve(const float* sL, float* Tf, float* R, int tid) {
+template <int BI, class Sync>
+__device__ __forceinline__ void block_row_solve(const float* sL, float* Tf, float* R, int tid, Sync sync) {
     constexpr int W = 16 * BI;
     constexpr int PER = 16 * W / kPrefillThreads;  // elements per thread
     float acc[PER];
@@ -119,7 +132,7 @@ __device__ __forceinline__ void block_row_solve(const float* sL, float* Tf, floa
         const int e = tid + k * kPrefillThreads;
         R[(e / W) * 48 + e % W] = acc[k];
     }
-    __syncthreads();
+    sync();
 #pragma unroll
     for (int k = 0; k < PER; ++k) acc[k] = 0.f;
 #pragma unroll
@@ -136,7 +149,7 @@ __device__ __forceinline__ void block_row_solve(const float* sL, float* Tf, floa
         const int e = tid + k * kPrefillThreads;
         Tf[(W + e / W) * kChunk + e % W] = -acc[k];
     }
-    __syncthreads();
+    sync();
 }
 
 // ---------------------------------------------------------------------------
@@ -236,7 +249,9 @@ __device__ __forceinline__ void form_l_p(uint32_t g_cols, int i_row, int wg, con
 
 // T = (I + L)^-1, blocked by 16, into bf16 hi/lo B-operand tiles (all
 // kPrefillThreads threads; contains barriers).  Tf and R are fp32 scratch.
-__device__ __forceinline__ void solve_t(const float* sL, float* Tf, float* R, uint8_t* t_hi, uint8_t* t_lo, int tid) {
+template <class Sync>
+__device__ __forceinline__ void solve_t(const float* sL, float* Tf, float* R, uint8_t* t_hi, uint8_t* t_lo, int tid,
+                                        Sync sync) {
     const int warp = tid >> 5, lane = tid & 31;
     // zero T, so every sum below can run over whole 16-blocks
     {
@@ -245,7 +260,7 @@ __device__ __forceinline__ void solve_t(const float* sL, float* Tf, float* R, ui
         for (int q = 0; q < kChunk * kChunk / 4 / kPrefillThreads; ++q)
             z[tid + q * kPrefillThreads] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    __syncthreads();
+    sync();
     // diagonal blocks: warp w < 4 inverts block w column by column (lane = column)
     if (warp < 4 && lane < 16) {
         const int b = warp * 16, cc = lane;
@@ -262,11 +277,11 @@ __device__ __forceinline__ void solve_t(const float* sL, float* Tf, float* R, ui
 #pragma unroll
         for (int r = 0; r < 16; ++r) Tf[(b + r) * kChunk + b + cc] = x[r];
     }
-    __syncthreads();
+    sync();
     // block rows 1..3: T[I][:I] = -T_II (L[I][:I] T[:I][:I])
-    block_row_solve<1>(sL, Tf, R, tid);
-    block_row_solve<2>(sL, Tf, R, tid);
-    block_row_solve<3>(sL, Tf, R, tid);
+    block_row_solve<1>(sL, Tf, R, tid, sync);
+    block_row_solve<2>(sL, Tf, R, tid, sync);
+    block_row_solve<3>(sL, Tf, R, tid, sync);
     // T -> bf16 hi/lo B-operand tiles (rows t, K = s)
     for (int e = tid; e < kChunk * 8; e += kPrefillThreads) {
         const int t = e >> 3, s0 = (e & 7) * 8;
@@ -301,13 +316,16 @@ constexpr uint32_t Q_OFF_MISC = Q_OFF_SCAL + 9 * 64 * 4;
 constexpr uint32_t kPrepSmem = Q_OFF_MISC + 32;
 constexpr uint32_t kPrepTmemCols = 64;
 
-__global__ void __launch_bounds__(kPrefillThreads, 2)
-gdn_prefill_prep_kernel(const __grid_constant__ PrefillParams p) {
-    extern __shared__ __align__(1024) uint8_t sm[];
-    const int tid = threadIdx.x;
+// One pre-pass item: chunk c of key head g, giving the records of the key
+// head's value heads.  Runs on threads 0 .. kPrefillThreads - 1 of the CTA
+// (tid), `sync` being a barrier over exactly those threads; `tmem` holds
+// kPrepTmemCols columns and `bar` is an mbarrier whose phase of parity
+// `parity` this item's MMA completes.  Returns false (after raising the status
+// word) when the tensor-core wait timed out.
+template <class Sync>
+__device__ bool prep_item(const PrefillParams& p, uint8_t* sm, uint32_t tmem, uint32_t bar, uint32_t parity, int c,
+                          int g, int tid, Sync sync) {
     const int warp = tid >> 5;
-    const int c = blockIdx.x;
-    const int g = blockIdx.y;
     float* s_alpha = reinterpret_cast<float*>(sm + Q_OFF_SCAL);
     float* s_beta = s_alpha + 64;
     float* s_lg = s_alpha + 128;
@@ -317,20 +335,12 @@ gdn_prefill_prep_kernel(const __grid_constant__ PrefillParams p) {
     float* s_gq = s_alpha + 384;
     float* s_ck = s_alpha + 448;
     float* s_brk = s_alpha + 512;
-    uint64_t* bar_ptr = reinterpret_cast<uint64_t*>(sm + Q_OFF_MISC);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Q_OFF_MISC + 8);
     int* abort_flag = reinterpret_cast<int*>(sm + Q_OFF_MISC + 12);
     const uint32_t sbase = smem_u32(sm);
-    const uint32_t bar = smem_u32(bar_ptr);
     const int t0 = c * kChunk;
     const int n = min(kChunk, p.T - t0);
     const size_t C = (size_t)p.C;
 
-    if (warp == 0) tmem_alloc(smem_u32(tmem_slot), kPrepTmemCols);
-    if (tid == 0) {
-        mbar_init(bar, 1);
-        *abort_flag = 0;
-    }
     // [K;Q] rows of the chunk (zero-filled past the last token)
     for (int idx = tid; idx < 2 * kChunk * 16; idx += kPrefillThreads) {
         const int r = ((idx >> 7) << 3) | (idx & 7), kb = (idx >> 3) & 15;  // 8 rows x 4 chunks per warp
@@ -344,9 +354,8 @@ gdn_prefill_prep_kernel(const __grid_constant__ PrefillParams p) {
     cp_async_wait_all();
     fence_async_smem();
     fence_before_sync();
-    __syncthreads();
+    sync();
     fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
     const int i_row = tid & 127;
     const int wg = tid >> 7;
     const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
@@ -360,12 +369,13 @@ gdn_prefill_prep_kernel(const __grid_constant__ PrefillParams p) {
         mma_commit(bar);
     }
     kq_norms(sm + Q_OFF_KQ, s_rk, s_rq, tid, p.normalize != 0, p.q_scale);
-    const bool ok = mbar_wait(bar, 0, kWaitLimitNs);
+    const bool ok = mbar_wait(bar, parity, kWaitLimitNs);
     if (!ok) atomicOr(abort_flag, 1);
-    __syncthreads();
+    sync();
     fence_after_sync();
+    const bool fine = *abort_flag == 0;
 
-    if (*abort_flag == 0) {
+    if (fine) {
 #pragma unroll 1
         for (int j = 0; j < p.group; ++j) {
             const int h = g * p.group + j;
@@ -374,17 +384,17 @@ gdn_prefill_prep_kernel(const __grid_constant__ PrefillParams p) {
                 s_alpha[tid] = in ? p.alpha[(size_t)(t0 + tid) * p.Hv + h] : 1.0f;
                 s_beta[tid] = in ? p.beta[(size_t)(t0 + tid) * p.Hv + h] : 0.0f;
             }
-            __syncthreads();
+            sync();
             log2_gamma_scan(s_alpha, s_lg, tid);
-            __syncthreads();
+            sync();
             chunk_scalars(s_lg, s_rk, s_rq, s_beta, s_gk, s_gq, s_ck, s_brk, tid);
-            __syncthreads();
+            sync();
             form_l_p(trow, i_row, wg, s_lg, s_brk, s_rq, s_rk, reinterpret_cast<float*>(sm + Q_OFF_L),
                      sm + Q_OFF_TILES + 16384, sm + Q_OFF_TILES + 24576);
-            __syncthreads();
+            sync();
             solve_t(reinterpret_cast<const float*>(sm + Q_OFF_L), reinterpret_cast<float*>(sm + Q_OFF_TF),
-                    reinterpret_cast<float*>(sm + Q_OFF_R), sm + Q_OFF_TILES, sm + Q_OFF_TILES + 8192, tid);
-            __syncthreads();
+                    reinterpret_cast<float*>(sm + Q_OFF_R), sm + Q_OFF_TILES, sm + Q_OFF_TILES + 8192, tid, sync);
+            sync();
             // the record of (chunk c, value head h)
             uint8_t* rec = reinterpret_cast<uint8_t*>(p.status) + kRecBase + ((size_t)c * p.Hv + h) * kRecBytes;
             for (int v = tid; v < 32768 / 16; v += kPrefillThreads)
@@ -394,30 +404,49 @@ gdn_prefill_prep_kernel(const __grid_constant__ PrefillParams p) {
                 reinterpret_cast<uint4*>(rec + REC_SCAL)[tid] =
                     reinterpret_cast<const uint4*>(src[tid >> 4])[tid & 15];
             }
-            __syncthreads();
+            sync();
         }
     }
-    if (*abort_flag != 0 && tid == 0) atomicExch(p.status, 1);
+    if (!fine && tid == 0) atomicExch(p.status, 1);
     fence_before_sync();
-    __syncthreads();
+    sync();  // every thread is past the abort flag and the TMEM reads of this item
     fence_after_sync();
-    if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
+    return fine;
 }
 
-// The chain over chunks.  PREP: T, P and the per-token scalars come from the
-// pre-pass records (prefetched one chunk ahead); otherwise they are computed
-// here between the chunk's MMAs (the self-contained form, which needs no
-// workspace beyond the status word).
-// Threads of the chain kernel: with PREP four warpgroups share the 128 TMEM
-// lanes (each takes a quarter of every row's columns, halving the epilogues);
-// the self-contained form keeps two (its solve is written for 256 threads).
-template <bool PREP>
-__host__ __device__ constexpr int chain_threads() { return PREP ? 512 : kPrefillThreads; }
+// TMEM, mbarrier and abort flag of a pre-pass CTA (threads 0 .. kPrefillThreads - 1).
+template <class Sync>
+__device__ uint32_t prep_setup(uint8_t* sm, int tid, Sync sync) {
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Q_OFF_MISC + 8);
+    if ((tid >> 5) == 0) tmem_alloc(smem_u32(tmem_slot), kPrepTmemCols);
+    if (tid == 0) {
+        mbar_init(smem_u32(sm + Q_OFF_MISC), 1);
+        *reinterpret_cast<int*>(sm + Q_OFF_MISC + 12) = 0;
+    }
+    fence_before_sync();
+    sync();
+    fence_after_sync();
+    return *tmem_slot;
+}
 
-template <bool PREP>
-__global__ void __launch_bounds__(chain_threads<PREP>(), 1)
+__global__ void __launch_bounds__(kPrefillThreads, 2)
+gdn_prefill_prep_kernel(const __grid_constant__ PrefillParams p) {
+    extern __shared__ __align__(1024) uint8_t sm[];
+    const int tid = threadIdx.x;
+    const uint32_t tmem = prep_setup(sm, tid, CtaSync{});
+    prep_item(p, sm, tmem, smem_u32(sm + Q_OFF_MISC), 0, blockIdx.x, blockIdx.y, tid, CtaSync{});
+    if ((tid >> 5) == 0) tmem_dealloc(tmem, kPrepTmemCols);
+}
+
+// The self-contained chain over chunks: T, P and the per-token scalars are
+// computed here, between the chunk's MMAs, with the same helper functions as
+// the pre-pass (so the two paths give the same bits).  It needs no workspace
+// beyond the status word, which is what the allocation-free entry point
+// offers.  Two warpgroups share the 128 TMEM lanes (each takes half of every
+// row's columns).
+__global__ void __launch_bounds__(kPrefillThreads, 1)
 gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
-    constexpr int NT = chain_threads<PREP>();
+    constexpr int NT = kPrefillThreads;
     constexpr int NWG = NT / 128;      // warpgroups
     constexpr int CW = kChunk / NWG;   // columns of a 64-wide tile per warpgroup
     constexpr int CS = kD / NWG;       // columns of the state per warpgroup
@@ -514,20 +543,6 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
             cp_async16(sbase + OFF_V + t * 256 + kb * 16, src, ok);
         }
     };
-    // PREP: chunk cc's record (T and P tiles, per-token scalars) into place
-    auto issue_rec = [&](int cc) {
-        const uint8_t* rec =
-            reinterpret_cast<const uint8_t*>(p.status) + kRecBase + ((size_t)cc * p.Hv + h) * kRecBytes;
-#pragma unroll 4
-        for (int v = tid; v < 32768 / 16; v += NT)
-            cp_async16(sbase + OFF_T_HI + v * 16, rec + REC_TILES + v * 16, true);
-        if (tid < 5 * 16) {
-            // beta, log2 gamma, gamma r_k, gamma q_scale r_q, (gamma_C/gamma) r_k
-            const int a = tid >> 4, q = tid & 15;
-            const int at = a < 2 ? 64 * (a + 1) : 256 + 64 * (a - 1);  // s_beta, s_lg, s_gk, s_gq, s_ck
-            cp_async16(sbase + OFF_SCAL + at * 4 + q * 16, rec + REC_SCAL + a * 256 + q * 16, true);
-        }
-    };
 #pragma unroll 1
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = c * kChunk;
@@ -539,18 +554,17 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
             if (c == 0) {
                 issue_kq(t0, n);
                 issue_v(t0, n);
-                if (PREP) issue_rec(0);
                 cp_async_commit();
             }
             cp_async_wait_all();
-            if (!PREP && tid < kChunk) {
+            if (tid < kChunk) {
                 const bool ok = tid < n;
                 s_alpha[tid] = ok ? p.alpha[(size_t)(t0 + tid) * p.Hv + h] : 1.0f;
                 s_beta[tid] = ok ? p.beta[(size_t)(t0 + tid) * p.Hv + h] : 0.0f;
             }
         }
         __syncthreads();
-        if (!PREP) kq_norms(sm + OFF_KQ, s_rk, s_rq, tid, p.normalize != 0, p.q_scale);
+        kq_norms(sm + OFF_KQ, s_rk, s_rq, tid, p.normalize != 0, p.q_scale);
         {
             // K^T: each warp transposes 16 of the 128 8x8 core matrices of K
             const int lane = tid & 31;
@@ -564,11 +578,9 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
                 transpose_8x8x4(src, dst);
             }
         }
-        if (!PREP) {
-            log2_gamma_scan(s_alpha, s_lg, tid);
-            __syncthreads();
-            chunk_scalars(s_lg, s_rk, s_rq, s_beta, s_gk, s_gq, s_ck, s_brk, tid);
-        }
+        log2_gamma_scan(s_alpha, s_lg, tid);
+        __syncthreads();
+        chunk_scalars(s_lg, s_rk, s_rq, s_beta, s_gk, s_gq, s_ck, s_brk, tid);
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
@@ -578,13 +590,11 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
             fence_after_sync();
             constexpr uint32_t id_g = idesc_bf16(128, 64);
             constexpr uint32_t id_kq = idesc_bf16(128, 128);
-            if (!PREP) {
 #pragma unroll 1
-                for (int ks = 0; ks < kD / 16; ++ks)
-                    mma_bf16(tmem + COL_G, smem_desc(sbase + OFF_KQ + ks * 256, kD * 16),
-                             smem_desc(sbase + OFF_KQ + ks * 256, kD * 16), id_g, ks > 0);
-                mma_commit(barg);
-            }
+            for (int ks = 0; ks < kD / 16; ++ks)
+                mma_bf16(tmem + COL_G, smem_desc(sbase + OFF_KQ + ks * 256, kD * 16),
+                         smem_desc(sbase + OFF_KQ + ks * 256, kD * 16), id_g, ks > 0);
+            mma_commit(barg);
 #pragma unroll 1
             for (int pass = 0; pass < 2; ++pass)
 #pragma unroll 1
@@ -593,7 +603,7 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
                              smem_desc(sbase + OFF_KQ + ks * 256, kD * 16), id_kq, (pass > 0 || ks > 0));
             mma_commit(bar);
         }
-        if (!PREP) {
+        {
             if (!wait_on(barg, parity_g)) break;
             // ---- C: L and P (from [K;Q] K^T), then the T solve, while S [K;Q]^T runs
             form_l_p(trow + COL_G, i_row, wg, s_lg, s_brk, s_rq, s_rk, reinterpret_cast<float*>(sm + OFF_L),
@@ -601,7 +611,7 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
             __syncthreads();
             // ---- D: T = (I + L)^-1, blocked by 16 --------------------------
             solve_t(reinterpret_cast<const float*>(sm + OFF_L), reinterpret_cast<float*>(sm + OFF_TF),
-                    reinterpret_cast<float*>(sm + OFF_R), sm + OFF_T_HI, sm + OFF_T_LO, tid);
+                    reinterpret_cast<float*>(sm + OFF_R), sm + OFF_T_HI, sm + OFF_T_LO, tid, CtaSync{});
             fence_async_smem();
             fence_before_sync();
             __syncthreads();
@@ -725,11 +735,6 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
         if (!wait_on(bar, parity)) break;
 
         // ---- H: outputs, next chunk's S operands, final state -------------
-        // (E and G have read T and P, F the scalars: prefetch the next record)
-        if (PREP && c + 1 < nchunks) {
-            issue_rec(c + 1);
-            cp_async_commit();
-        }
         {
             const int i = i_row;
             const size_t ostride = (size_t)p.Hv * kD;
@@ -818,16 +823,29 @@ constexpr uint32_t T_D = 128;    // [S K^T | S Q^T -> O^T] [i][t], 2 x 128 (by c
 constexpr uint32_t T_U = 384;    // U^T fp32, then U^T hi 32 + lo 32      64
 constexpr uint32_t T_XA = 448;   // X^T, then Uhat^T       hi 32 + lo 32  64
 
-__global__ void __launch_bounds__(kChainThreads, 1)
-gdn_prefill_chain_kernel(const __grid_constant__ PrefillParams p) {
+// Wait (bounded) until the pre-pass item `item` has been published.
+__device__ __forceinline__ bool wait_ready(const int* ready, int item) {
+    const uint64_t t0 = global_ns();
+    while (true) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ready + item) : "memory");
+        if (v != 0) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+        __nanosleep(100);
+    }
+}
+
+// The chain of value head h.  READY: the records are produced concurrently
+// by the pre-pass workers of the cooperative kernel, and thread 0 waits for a
+// record's flag before the CTA barrier that precedes its prefetch.
+template <bool READY>
+__device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, int h) {
     constexpr int CW = kChunk / 4;  // columns of a 64-wide tile per warpgroup
     constexpr int CS = kD / 4;      // columns of the state per warpgroup
-    extern __shared__ __align__(1024) uint8_t sm[];
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const bool issuer = tid == kEpiThreads;    // lane 0 of the MMA warp
     const bool epi = tid < kEpiThreads;        // an epilogue thread
-    const int h = blockIdx.x;
     const int g = h / p.group;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C_OFF_MISC);  // 6 mbarriers
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C_OFF_MISC + 96);
@@ -843,6 +861,7 @@ gdn_prefill_chain_kernel(const __grid_constant__ PrefillParams p) {
     if (tid == 0) {
         for (int b = 0; b < 6; ++b) mbar_init(smem_u32(bars + b), 1);
         *abort_flag = 0;
+        if (READY && p.T > 0 && !wait_ready(p.ready, g)) *abort_flag = 1;  // chunk 0's record
     }
     fence_before_sync();
     __syncthreads();
@@ -986,6 +1005,8 @@ gdn_prefill_chain_kernel(const __grid_constant__ PrefillParams p) {
                 transpose_8x8x4(src, dst);
             }
         }
+        // the next chunk's record is prefetched after this barrier
+        if (READY && tid == 0 && c + 1 < nchunks && !wait_ready(p.ready, (c + 1) * p.Hk + g)) atomicOr(abort_flag, 1);
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
@@ -1184,6 +1205,50 @@ gdn_prefill_chain_kernel(const __grid_constant__ PrefillParams p) {
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
+__global__ void __launch_bounds__(kChainThreads, 1)
+gdn_prefill_chain_kernel(const __grid_constant__ PrefillParams p) {
+    extern __shared__ __align__(1024) uint8_t sm[];
+    chain_body<false>(p, sm, blockIdx.x);
+}
+
+// Pre-pass worker w of the cooperative kernel: items (chunk, key head) in
+// chunk order, w, w + n_workers, ...; each is published with a release store
+// of its flag once all of its records are written.
+__device__ __forceinline__ void prep_worker(const PrefillParams& p, uint8_t* sm, int w) {
+    const int tid = threadIdx.x;
+    const NamedSync<2, kPrefillThreads> sync;
+    const uint32_t tmem = prep_setup(sm, tid, sync);
+    const uint32_t bar = smem_u32(sm + Q_OFF_MISC);
+    const int items = ((p.T + kChunk - 1) / kChunk) * p.Hk;
+    uint32_t k = 0;
+#pragma unroll 1
+    for (int item = w; item < items; item += p.n_workers, ++k) {
+        const bool ok = prep_item(p, sm, tmem, bar, k & 1u, item / p.Hk, item % p.Hk, tid, sync);
+        __threadfence();  // this thread's record stores, before the flag
+        sync();
+        if (tid == 0 && ok) asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.ready + item), "r"(1) : "memory");
+        if (!ok) break;
+    }
+    fence_before_sync();
+    sync();
+    fence_after_sync();
+    if ((tid >> 5) == 0) tmem_dealloc(tmem, kPrepTmemCols);
+}
+
+// Pre-pass and chain in one cooperative launch (every CTA resident at once, so
+// a chain may wait for a worker): CTAs 0 .. Hv - 1 run the value heads'
+// chains, the others the pre-pass, so that the records of later chunks are
+// computed while earlier chunks run through the chain.
+__global__ void __launch_bounds__(kChainThreads, 1)
+gdn_prefill_fused_kernel(const __grid_constant__ PrefillParams p) {
+    extern __shared__ __align__(1024) uint8_t sm[];
+    if ((int)blockIdx.x < p.Hv) {
+        chain_body<true>(p, sm, blockIdx.x);
+    } else if ((int)threadIdx.x < kPrefillThreads) {
+        prep_worker(p, sm, blockIdx.x - p.Hv);
+    }
+}
+
 }  // namespace
 }  // namespace gdn
 
@@ -1193,6 +1258,11 @@ namespace {
 int launch_prefill(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const float* alpha, const float* beta,
                    float* state, void* out, void* workspace, float q_scale, uint32_t flags, cudaStream_t st,
                    bool prep);
+// bytes of the ready flags (one int32 per chunk and key head), padded to 16
+size_t ready_bytes(size_t nchunks, int Hk) { return (nchunks * (size_t)Hk * 4 + 15) / 16 * 16; }
+constexpr int kMinWorkers = 8;  // fewest pre-pass workers worth a cooperative launch
+// CTAs of the cooperative kernel the device holds at once (0: no cooperative launch)
+int fused_capacity(int dev);
 }  // namespace
 
 extern "C" {
@@ -1200,10 +1270,11 @@ extern "C" {
 size_t gdn_prefill_workspace_bytes(const gdn_shape* shape, int32_t T, int32_t chunk) {
     if (shape == nullptr || T < 0 || chunk != kChunk) return 0;
     // the status word (int32 at offset 0, padded), then for 128-wide heads one
-    // pre-pass record per (chunk, value head)
+    // pre-pass record per (chunk, value head) and one ready flag (int32) per
+    // (chunk, key head)
     if (shape->dk != kD || shape->dv != kD || shape->Hv < 1) return kRecBase;
     const size_t nchunks = ((size_t)T + kChunk - 1) / kChunk;
-    return kRecBase + nchunks * (size_t)shape->Hv * kRecBytes;
+    return kRecBase + nchunks * (size_t)shape->Hv * kRecBytes + ready_bytes(nchunks, shape->Hk);
 }
 
 int gdn_chunk_prefill(const gdn_shape* shape, int32_t T, int32_t chunk, const gdn_bf16* qkv,
@@ -1219,6 +1290,11 @@ int gdn_chunk_prefill(const gdn_shape* shape, int32_t T, int32_t chunk, const gd
         // narrower heads: the same recurrence token by token on the GPU
         return gdn_decode_step(shape, T, qkv, alpha, beta, state, out, q_scale, flags, stream);
     }
+    // the ready flags start at zero on every call
+    const size_t nchunks = ((size_t)T + kChunk - 1) / kChunk;
+    e = cudaMemsetAsync(static_cast<uint8_t*>(workspace) + kRecBase + nchunks * (size_t)shape->Hv * kRecBytes, 0,
+                        ready_bytes(nchunks, shape->Hk), st);
+    if (e != cudaSuccess) return cuda_error(e, "prefill flag reset");
     return launch_prefill(shape, T, qkv, alpha, beta, state, out, workspace, q_scale, flags, st, true);
 }
 
@@ -1226,9 +1302,28 @@ int gdn_chunk_prefill(const gdn_shape* shape, int32_t T, int32_t chunk, const gd
 
 namespace {
 
-// The chunk-form launch(es): with `prep`, the pre-pass over all chunks then the
-// chain reading its records (the workspace holds them); without, the
-// self-contained chain (the workspace holds only the status word).
+int fused_capacity(int dev) {
+    static int cached[64];
+    static bool known[64];
+    if (dev < 0 || dev >= 64) return 0;
+    if (!known[dev]) {
+        int coop = 0, sms = 0, per_sm = 0;
+        if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess) coop = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gdn_prefill_fused_kernel, kChainThreads,
+                                                          kChainSmem) != cudaSuccess)
+            per_sm = 0;
+        (void)cudaGetLastError();
+        cached[dev] = coop ? sms * per_sm : 0;
+        known[dev] = true;
+    }
+    return cached[dev];
+}
+
+// The chunk-form launch(es): with `prep`, the pre-pass and the chain reading
+// its records (the workspace holds them), as one cooperative kernel where the
+// device allows it; without, the self-contained chain (the workspace holds
+// only the status word).
 int launch_prefill(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const float* alpha, const float* beta,
                    float* state, void* out, void* workspace, float q_scale, uint32_t flags, cudaStream_t st,
                    bool prep) {
@@ -1240,7 +1335,10 @@ int launch_prefill(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const
         e = cudaFuncSetAttribute(gdn_prefill_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kChainSmem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gdn_prefill_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(gdn_prefill_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kChainSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gdn_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kPrefillSmem);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(gdn_prefill_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1264,11 +1362,28 @@ int launch_prefill(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const
     p.normalize = (flags & GDN_NORMALIZE_QK) != 0;
     p.out_bf16 = (flags & GDN_OUT_BF16) != 0;
     if (prep) {
-        const dim3 grid((unsigned)((T + kChunk - 1) / kChunk), (unsigned)shape->Hk);
+        const int nchunks = (T + kChunk - 1) / kChunk;
+        p.ready = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + kRecBase +
+                                         (size_t)nchunks * shape->Hv * kRecBytes);
+        // The cooperative form when the GPU holds a chain CTA per value head
+        // and at least a few pre-pass workers at once; otherwise the pre-pass
+        // over all chunks, then the chain.
+        const int resident = fused_capacity(dev);
+        const int workers = std::min(resident - shape->Hv, nchunks * shape->Hk);
+        if (workers >= kMinWorkers) {
+            p.n_workers = workers;
+            void* args[] = {&p};
+            e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(gdn_prefill_fused_kernel),
+                                            dim3((unsigned)(shape->Hv + workers)), dim3(kChainThreads), args,
+                                            kChainSmem, st);
+            if (e == cudaSuccess) return GDN_OK;
+            (void)cudaGetLastError();  // not launched: take the two-kernel form
+        }
+        const dim3 grid((unsigned)nchunks, (unsigned)shape->Hk);
         gdn_prefill_prep_kernel<<<grid, kPrefillThreads, kPrepSmem, st>>>(p);
         gdn_prefill_chain_kernel<<<shape->Hv, kChainThreads, kChainSmem, st>>>(p);
     } else {
-        gdn_prefill_tc_kernel<false><<<shape->Hv, chain_threads<false>(), kPrefillSmem, st>>>(p);
+        gdn_prefill_tc_kernel<<<shape->Hv, kPrefillThreads, kPrefillSmem, st>>>(p);
     }
     e = cudaGetLastError();
     return e == cudaSuccess ? GDN_OK : cuda_error(e, "prefill launch");
