@@ -906,10 +906,10 @@ class Prefill(Workload):
         nbytes = gdn.prefill_workspace_bytes(T, HK, HV, DK, DV)
         self.ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
         self.shape = gdn.gdn_shape(1, HK, HV, DK, DV)
-        self.launches_per_step = 2       # the pre-pass over all chunks, then the chain
+        self.launches_per_step = 1       # one cooperative launch: pre-pass workers and chains
         self.units_per_step = T * HV
-        self.dominant = "gdn_chunk_prefill"  # the whole call: pre-pass + chain
-        self.traffic_key = "gdn_prefill_tc_kernel"
+        self.dominant = "gdn_chunk_prefill"  # the whole call
+        self.traffic_key = "gdn_prefill_fused_kernel"
         self.dominant_sources = PREFILL_SOURCES
         self.bound = "tensor"
         self.dominant_work = prefill_flops(T)
@@ -917,7 +917,7 @@ class Prefill(Workload):
 
     @property
     def marks_per_step(self) -> int:
-        return 1  # one event after the call (its two launches are timed together)
+        return 1  # one event after the call
 
     def _args(self):
         P = ctypes.c_void_p

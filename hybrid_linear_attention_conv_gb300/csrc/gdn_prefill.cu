@@ -312,7 +312,9 @@ constexpr uint32_t Q_OFF_L = 65536;      // L fp32 16 KB
 constexpr uint32_t Q_OFF_TF = 81920;     // T fp32 16 KB
 constexpr uint32_t Q_OFF_R = 98304;      // block-solve scratch 3 KB
 constexpr uint32_t Q_OFF_SCAL = 101376;  // 9 x 64 fp32
-constexpr uint32_t Q_OFF_MISC = Q_OFF_SCAL + 9 * 64 * 4;
+constexpr uint32_t Q_OFF_AB = Q_OFF_SCAL + 9 * 64 * 4;  // alpha, beta of the group's heads: 2 x 64 x kMaxGroup fp32
+constexpr int kMaxGroup = 8;                             // value heads per key head staged at once
+constexpr uint32_t Q_OFF_MISC = Q_OFF_AB + 2 * 64 * kMaxGroup * 4;
 constexpr uint32_t kPrepSmem = Q_OFF_MISC + 32;
 constexpr uint32_t kPrepTmemCols = 64;
 
@@ -369,6 +371,17 @@ __device__ bool prep_item(const PrefillParams& p, uint8_t* sm, uint32_t tmem, ui
         mma_commit(bar);
     }
     kq_norms(sm + Q_OFF_KQ, s_rk, s_rq, tid, p.normalize != 0, p.q_scale);
+    // alpha and beta of the first kMaxGroup value heads of the group, all
+    // requested at once ([head][token]; padding tokens: alpha 1, beta 0)
+    float* s_ab = reinterpret_cast<float*>(sm + Q_OFF_AB);
+    const int staged = min(p.group, kMaxGroup);
+    for (int idx = tid; idx < staged * kChunk; idx += kPrefillThreads) {
+        const int j = idx / kChunk, t = idx % kChunk;
+        const bool in = t < n;
+        const size_t at = (size_t)(t0 + (in ? t : 0)) * p.Hv + g * p.group + j;
+        s_ab[idx] = in ? p.alpha[at] : 1.0f;
+        s_ab[kMaxGroup * kChunk + idx] = in ? p.beta[at] : 0.0f;
+    }
     const bool ok = mbar_wait(bar, parity, kWaitLimitNs);
     if (!ok) atomicOr(abort_flag, 1);
     sync();
@@ -381,8 +394,13 @@ __device__ bool prep_item(const PrefillParams& p, uint8_t* sm, uint32_t tmem, ui
             const int h = g * p.group + j;
             if (tid < kChunk) {
                 const bool in = tid < n;
-                s_alpha[tid] = in ? p.alpha[(size_t)(t0 + tid) * p.Hv + h] : 1.0f;
-                s_beta[tid] = in ? p.beta[(size_t)(t0 + tid) * p.Hv + h] : 0.0f;
+                if (j < kMaxGroup) {
+                    s_alpha[tid] = s_ab[j * kChunk + tid];
+                    s_beta[tid] = s_ab[kMaxGroup * kChunk + j * kChunk + tid];
+                } else {
+                    s_alpha[tid] = in ? p.alpha[(size_t)(t0 + tid) * p.Hv + h] : 1.0f;
+                    s_beta[tid] = in ? p.beta[(size_t)(t0 + tid) * p.Hv + h] : 0.0f;
+                }
             }
             sync();
             log2_gamma_scan(s_alpha, s_lg, tid);
