@@ -958,7 +958,7 @@ class Prefill(Workload):
                             "q/k/v, fp32 alpha/beta/state, WY/UT chunk form on tcgen05 tensor cores",
                 "tokens": Prefill.T, "chunk": CHUNK, "Hk": HK, "Hv": HV, "dk": DK, "dv": DV,
                 "l2": "inputs larger than L2: 168 MB of q/k/v read and 201 MB of outputs per step",
-                "launch": "eager, CUDA events around the call (status reset, the pre-pass over all chunks, the chain)"}
+                "launch": "eager, CUDA events around the call (status and flag resets, one cooperative launch: pre-pass workers and chains)"}
 
 
 WORKLOADS = {"batched": Batched, "kdabatch": KdaBatched, "layer": LayerBatched, "decode1": Decode1, "tree": Tree, "treebatch": TreeBatch,

@@ -18,15 +18,26 @@
 // agree mathematically but round differently ("Serving A Research Architecture
 // On CPU", third exactness layer).
 //
-// One CTA owns one value head; thread i owns state row i, which is TMEM lane i
-// of every accumulator, so all products are written in the transposed form
-// (value rows as M = 128): S [K;Q]^T, X^T T^T, Uhat^T K and U^T P^T.  The state
-// stays in TMEM as an fp32 accumulator across all chunks and crosses HBM once
-// in and once out.  Operands that are not exact in bf16 (S, X, T, U, P) are
-// split into bf16 hi + lo and multiplied in 2 or 3 passes (hi.hi + hi.lo +
+// A chain CTA owns one value head; thread i owns state row i, which is TMEM
+// lane i of every accumulator, so all products are written in the transposed
+// form (value rows as M = 128): S [K;Q]^T, X^T T^T, Uhat^T K and U^T P^T.  The
+// state stays in TMEM as an fp32 accumulator across all chunks and crosses HBM
+// once in and once out.  Operands that are not exact in bf16 (S, X, T, U, P)
+// are split into bf16 hi + lo and multiplied in 2 or 3 passes (hi.hi + hi.lo +
 // lo.hi) so the result keeps close to fp32 accuracy; q, k, v enter as the raw
 // bf16 inputs (exact) with the norms applied as fp32 scalings.  T is solved
-// on the CUDA cores by column-parallel forward substitution.
+// on the CUDA cores by blocked forward substitution.
+//
+// The kernels in this file:
+//   gdn_prefill_prep_kernel   the pre-pass: T, P and the per-token scalars of
+//                             every (chunk, key head), written as records;
+//   gdn_prefill_chain_kernel  the pipelined chain reading those records;
+//   gdn_prefill_fused_kernel  both in one cooperative launch, the pre-pass
+//                             workers running ahead of the chains (the form
+//                             gdn_chunk_prefill takes where the GPU holds it);
+//   gdn_prefill_tc_kernel     the self-contained chain computing each chunk's
+//                             T and P itself (gdn_chunk_prefill_noalloc).
+// All four use the same chunk-local arithmetic, so they give the same bits.
 //
 // Heads smaller than 128 run the same recurrence token by token with the
 // decode kernel (still on the GPU; the chunk form here is written for the
