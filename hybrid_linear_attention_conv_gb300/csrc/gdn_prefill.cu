@@ -42,8 +42,11 @@
 // Heads smaller than 128 run the same recurrence token by token with the
 // decode kernel (still on the GPU; the chunk form here is written for the
 // 128-wide heads of the 27B layer).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -90,7 +93,12 @@ constexpr uint32_t kTmemCols = 512;
 
 constexpr uint64_t kWaitLimitNs = 200000000ull;  // 0.2 s per tensor-core batch
 
-struct PrefillParams {
+// Kernel parameters.  The two tensor maps describe the packed q/k/v rows
+// [T][C] (bf16) for the chain's TMA loads: 8 x 64 boxes (one 16-byte column
+// of 64 tokens) for K and Q, 128 x 64 boxes for V.
+struct alignas(64) PrefillParams {
+    CUtensorMap tm_kq;
+    CUtensorMap tm_v;
     const uint16_t* qkv;
     const float* alpha;
     const float* beta;
@@ -832,21 +840,32 @@ constexpr int kEpiThreads = 512;    // four epilogue warpgroups over the 128 TME
 constexpr int kChainThreads = kEpiThreads + 32;  // and one warp that only issues the MMAs
 constexpr uint32_t kRecStride = 34816;  // a record slot, padded to 1 KB
 
-constexpr uint32_t C_OFF_S_HI = 0;       // S hi  [128 i][128 j]  A of S K^T and S Q^T
-constexpr uint32_t C_OFF_S_LO = 32768;   // S lo
-constexpr uint32_t C_OFF_KQ = 65536;     // [K;Q] [128 t'][128 j] B of S K^T (rows 0..63), S Q^T (64..127)
-constexpr uint32_t C_OFF_KT = 98304;     // K^T   [128 j][64 t]   B of Uhat^T K
-constexpr uint32_t C_OFF_V = 114688;     // V     [64 t][128 i]   plain row-major
-constexpr uint32_t C_OFF_REC = 131072;   // two record slots (T hi/lo, P hi/lo, scalars)
+// Inputs of a chunk are double-buffered by chunk parity and loaded by the
+// copy engine a whole chunk ahead.  [K;Q] is [16 column blocks][128 rows][8]
+// (K rows 0..63, Q rows 64..127): one TMA box per 16-byte column of K or Q,
+// i.e. K-major core matrices 2,048 B apart along K and 128 B apart along rows.
+constexpr uint32_t C_OFF_KQ = 0;         // [K;Q] x 2   B of S [K;Q]^T
+constexpr uint32_t C_OFF_KT = 65536;     // K^T   [128 j][64 t]   B of Uhat^T K
+constexpr uint32_t C_OFF_V = 81920;      // V     [64 t][128 i] x 2, plain row-major
+constexpr uint32_t C_OFF_REC = 114688;   // two record slots (T hi/lo, P hi/lo, scalars)
+constexpr uint32_t kKqBytes = 32768, kVBytes = 16384;
+constexpr uint32_t kInputTx = kKqBytes + kVBytes + kRecBytes;  // bytes a chunk's inputs bring
 constexpr uint32_t C_OFF_MISC = C_OFF_REC + 2 * kRecStride;  // mbarriers, TMEM base, abort flag
 constexpr uint32_t kChainSmem = C_OFF_MISC + 128;
+// A chain CTA takes all 512 TMEM columns of its SM, so no two may share an SM:
+// its shared memory must exceed half of the 227 KB an SM offers.
+static_assert(kChainSmem > 232448 / 2, "chain CTAs must not fit two to an SM");
 
 // TMEM columns.  The state, S [K;Q]^T and U^T are fp32 accumulators; X^T
 // (later Uhat^T) and U^T as A operands hold bf16 hi in their first 32
 // columns and lo in the next 32.  S [K;Q]^T is double-buffered by chunk
 // parity: its S K^T half feeds X^T, its S Q^T half becomes O^T, which is read
 // out while the next chunk runs.  U^T as an A operand overwrites the fp32 U^T
-// it is made from.
+// it is made from.  Between chunks, the next chunk's S operand (64 columns
+// each = 128 bf16 per lane) has bf16 hi in T_XA, written once the state
+// update has read the Uhat^T there, and lo in the S K^T half of the current
+// chunk's buffer, which the X^T epilogue has consumed (and which the chunk
+// after next rewrites, after the next chunk's MMAs have read it).
 constexpr uint32_t T_S = 0;      // S [i][j]                               128 columns
 constexpr uint32_t T_D = 128;    // [S K^T | S Q^T -> O^T] [i][t], 2 x 128 (by chunk parity)
 constexpr uint32_t T_U = 384;    // U^T fp32, then U^T hi 32 + lo 32      64
@@ -876,7 +895,7 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
     const bool issuer = tid == kEpiThreads;    // lane 0 of the MMA warp
     const bool epi = tid < kEpiThreads;        // an epilogue thread
     const int g = h / p.group;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C_OFF_MISC);  // 6 mbarriers
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C_OFF_MISC);  // 8 mbarriers
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C_OFF_MISC + 96);
     int* abort_flag = reinterpret_cast<int*>(sm + C_OFF_MISC + 100);
     const uint32_t sbase = smem_u32(sm);
@@ -885,10 +904,11 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
     const uint32_t bar_s = smem_u32(bars + 3);     // state update
     const uint32_t bar_o = smem_u32(bars + 4);     // U^T P^T
     const uint32_t bar_fin = smem_u32(bars + 5);   // every MMA issued, before TMEM is freed
+    const uint32_t bar_in0 = smem_u32(bars + 6);   // a chunk's inputs landed in buffer 0 (bar_in0 + 8: buffer 1)
 
     if (warp == 0) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     if (tid == 0) {
-        for (int b = 0; b < 6; ++b) mbar_init(smem_u32(bars + b), 1);
+        for (int b = 0; b < 8; ++b) mbar_init(smem_u32(bars + b), 1);
         *abort_flag = 0;
         if (READY && p.T > 0 && !wait_ready(p.ready, g)) *abort_flag = 1;  // chunk 0's record
     }
@@ -925,62 +945,53 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
             v[4 * q + 3] = f.w;
         }
         tmem_st16(trow + T_S + cc, v);
-        store_split8(sm + C_OFF_S_HI + core_off(i, cc, kD), sm + C_OFF_S_LO + core_off(i, cc, kD), v);
-        store_split8(sm + C_OFF_S_HI + core_off(i, cc + 8, kD), sm + C_OFF_S_LO + core_off(i, cc + 8, kD), v + 8);
+        uint32_t hi[8], lo[8];
+        split_pack16(v, hi, lo);
+        tmem_st8(trow + T_XA + cc / 2, hi);
+        tmem_st8(trow + T_D + 128 + cc / 2, lo);  // chunk 0 reads lo from buffer 1
     }
     tmem_wait_st();
 
     const int nchunks = (p.T + kChunk - 1) / kChunk;
-    const size_t C = (size_t)p.C;
-    auto issue_kq = [&](int t0, int n) {
-#pragma unroll 4
-        for (int idx = tid; idx < 2 * kChunk * 16; idx += kEpiThreads) {
-            const int r = ((idx >> 7) << 3) | (idx & 7), kb = (idx >> 3) & 15;  // 8 rows x 4 chunks per warp
-            const int t = r & 63;
-            const bool ok = t < n;
-            const uint16_t* src = p.qkv + (size_t)(t0 + (ok ? t : 0)) * C + (r >= 64 ? 0 : (size_t)p.Hk * kD) +
-                                  (size_t)g * kD + kb * 8;
-            cp_async16(sbase + C_OFF_KQ + core_off(r, kb * 8, kD), src, ok);
-        }
-    };
     const int lane = tid & 31;
-    auto issue_v = [&](int t0, int n) {
-#pragma unroll 2
-        for (int idx = tid; idx < kChunk * 16; idx += kEpiThreads) {
-            const int t = idx >> 4, kb = idx & 15;
-            const bool ok = t < n;
-            const uint16_t* src =
-                p.qkv + (size_t)(t0 + (ok ? t : 0)) * C + (size_t)2 * p.Hk * kD + (size_t)h * kD + kb * 8;
-            cp_async16(sbase + C_OFF_V + t * 256 + kb * 16, src, ok);
+    // The MMA warp loads chunk cc's inputs into buffer cc & 1 with the copy
+    // engine: 32 TMA boxes for [K;Q] (lane l: K column block l, or Q column
+    // block l - 16), one for V and one bulk copy of the record, all counted
+    // on that buffer's barrier.  Rows past the end of the prompt read as zeros.
+    int in_last = -1;  // MMA warp: the last chunk whose inputs it requested
+    auto issue_inputs = [&](int cc) {
+        in_last = cc;
+        const uint32_t b = bar_in0 + 8u * (uint32_t)(cc & 1);
+        const int t0 = cc * kChunk;
+        if (lane == 0) mbar_arrive_expect_tx(b, kInputTx);
+        __syncwarp();
+        fence_proxy_async_global();
+        const uint32_t kq = sbase + C_OFF_KQ + (uint32_t)(cc & 1) * kKqBytes;
+        const int kb = lane & 15;
+        const int x = (lane < 16 ? p.Hk * kD : 0) + g * kD + kb * 8;
+        tma_load_2d(kq + (uint32_t)kb * 2048u + (lane < 16 ? 0u : 1024u), &p.tm_kq, x, t0, b);
+        if (lane == 0) {
+            tma_load_2d(sbase + C_OFF_V + (uint32_t)(cc & 1) * kVBytes, &p.tm_v, 2 * p.Hk * kD + h * kD, t0, b);
+            const uint8_t* rec =
+                reinterpret_cast<const uint8_t*>(p.status) + kRecBase + ((size_t)cc * p.Hv + h) * kRecBytes;
+            bulk_g2s(sbase + C_OFF_REC + (uint32_t)(cc & 1) * kRecStride, rec, kRecBytes, b);
         }
     };
-    // chunk cc's record (T and P tiles, scalars) into slot cc & 1
-    auto issue_rec = [&](int cc) {
-        const uint8_t* rec =
-            reinterpret_cast<const uint8_t*>(p.status) + kRecBase + ((size_t)cc * p.Hv + h) * kRecBytes;
-        const uint32_t dst = sbase + C_OFF_REC + (uint32_t)(cc & 1) * kRecStride;
-#pragma unroll 4
-        for (int v = tid; v < (int)(kRecBytes / 16); v += kEpiThreads) cp_async16(dst + v * 16, rec + v * 16, true);
+    // every thread that reads a buffer waits for its phase (chunk cc is the
+    // (cc >> 1)-th use of buffer cc & 1)
+    auto wait_inputs = [&](int cc) {
+        if (!mbar_wait(bar_in0 + 8u * (uint32_t)(cc & 1), (uint32_t)(cc >> 1) & 1u, kWaitLimitNs))
+            atomicOr(abort_flag, 1);
     };
-    if (epi) {
-        issue_kq(0, min(kChunk, p.T));
-        issue_v(0, min(kChunk, p.T));
-        issue_rec(0);
-    }
-    cp_async_commit();
-    cp_async_wait_all();
-    fence_async_smem();
-    fence_before_sync();
-    __syncthreads();
+    if (!epi) issue_inputs(0);
 
     // Operand descriptors, computed once: an MMA issue is then a 64-bit add
     // and the instruction (step ks of a K-major tile starts 256 B, i.e. 16
     // descriptor units, further on).  The issuing thread shares its SM
     // sub-partition with busy epilogue warps, so its instruction stream must
     // stay short for the tensor pipe to be fed at its own rate.
-    const uint64_t d_s_hi = smem_desc(sbase + C_OFF_S_HI, kD * 16);
-    const uint64_t d_s_lo = smem_desc(sbase + C_OFF_S_LO, kD * 16);
-    const uint64_t d_k = smem_desc(sbase + C_OFF_KQ, kD * 16);
+    const uint64_t d_kq0 = smem_desc2(sbase + C_OFF_KQ, 2048, 128);  // [K;Q] of buffer 0
+    constexpr uint64_t kKqDesc = kKqBytes >> 4;                    // buffer 1 vs buffer 0
     const uint64_t d_kt = smem_desc(sbase + C_OFF_KT, kChunk * 16);
     const uint64_t d_rec0 = smem_desc(sbase + C_OFF_REC + REC_TILES, kChunk * 16);
     constexpr uint64_t kRecDesc = kRecStride >> 4;  // slot 1 vs slot 0
@@ -1015,6 +1026,7 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = c * kChunk;
         const uint32_t d_col = T_D + (uint32_t)(c & 1) * 128;  // S K^T here, O^T at + 64
+        const uint32_t s_lo = T_D + (uint32_t)((c + 1) & 1) * 128;  // this chunk's S lo operand
         const uint8_t* rec = sm + C_OFF_REC + (uint32_t)(c & 1) * kRecStride;
         const float* s_beta = reinterpret_cast<const float*>(rec + REC_SCAL);  // beta_t
         const float* s_lg = s_beta + 64;   // log2 gamma_t
@@ -1023,13 +1035,15 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
         const float* s_ck = s_beta + 256;  // (gamma_C / gamma_t) r_k,t
         const uint64_t d_rec = d_rec0 + (uint64_t)(c & 1) * kRecDesc;  // T hi of this chunk's record
 
-        // ---- A: K^T from the staged K rows (inputs of chunk c have landed)
+        // ---- A: K^T from the staged K rows, once chunk c's inputs have landed
         if (epi) {
+            wait_inputs(c);
+            const uint32_t kq = sbase + C_OFF_KQ + (uint32_t)(c & 1) * kKqBytes;
 #pragma unroll
             for (int it = 0; it < 128 / (kEpiThreads / 32) / 4; ++it) {
                 const int q = warp * (128 / (kEpiThreads / 32)) + it * 4 + (lane >> 3);
                 const int tb = q >> 4, jb = q & 15;
-                const uint32_t src = sbase + C_OFF_KQ + tb * (kD * 16) + jb * 128 + (lane & 7) * 16;
+                const uint32_t src = kq + jb * 2048 + tb * 128 + (lane & 7) * 16;
                 const uint32_t dst = sbase + C_OFF_KT + jb * (kChunk * 16) + tb * 128 + (lane & 7) * 16;
                 transpose_8x8x4(src, dst);
             }
@@ -1040,7 +1054,7 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
         fence_before_sync();
         __syncthreads();
 
-        // ---- B: S [K;Q]^T (S hi, S lo) into this chunk's buffer
+        // ---- B: S [K;Q]^T (S hi, S lo from tensor memory) into this chunk's buffer
         if (issuer) {
             fence_after_sync();
             constexpr uint32_t id = idesc_bf16(128, 128);
@@ -1048,19 +1062,21 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
             for (int pass = 0; pass < 2; ++pass)
 #pragma unroll
                 for (int ks = 0; ks < kD / 16; ++ks)
-                    mma_bf16(tmem + d_col, (pass ? d_s_lo : d_s_hi) + 16 * ks, d_k + 16 * ks, id, (pass > 0 || ks > 0));
+                    mma_bf16_ts(tmem + d_col, tmem + (pass ? s_lo : T_XA) + ks * 8,
+                                d_kq0 + (uint64_t)(c & 1) * kKqDesc + 256 * ks, id, (pass > 0 || ks > 0));
             mma_commit(bar_ks);
         }
+        // the next chunk's inputs, into the buffer chunk c - 1 used (its record's
+        // P tile is read by U^T P^T of chunk c - 1: wait for that first)
+        if (!epi && c + 1 < nchunks) {
+            if (c > 0 && lane == 0 && !mbar_wait(bar_o, (uint32_t)(c - 1) & 1u, kWaitLimitNs)) atomicOr(abort_flag, 1);
+            issue_inputs(c + 1);
+        }
         if (epi) {
-            // in the shadow of S [K;Q]^T: the previous chunk's outputs, then
-            // the next record into the slot they freed; S <- gamma_C S
+            // in the shadow of S [K;Q]^T: the previous chunk's outputs; S <- gamma_C S
             if (c > 0) {
                 wait_mma(bar_o, c - 1);
                 store_outputs(c - 1);
-            }
-            if (c + 1 < nchunks) {
-                issue_rec(c + 1);
-                cp_async_commit();
             }
             {
                 const float gamma_c = exp2f(s_lg[kChunk - 1]);
@@ -1082,7 +1098,7 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
 
             // ---- C: X^T[i][s] = beta_s (v_s[i] - gamma_s r_k,s (S k_s)[i]) as the A operand of X^T T^T
             {
-                const uint16_t* vcol = reinterpret_cast<const uint16_t*>(sm + C_OFF_V) + i;
+                const uint16_t* vcol = reinterpret_cast<const uint16_t*>(sm + C_OFF_V + (uint32_t)(c & 1) * kVBytes) + i;
                 float ks[16], x[16];
                 tmem_ld16(trow + d_col + s0, ks);
 #pragma unroll
@@ -1124,23 +1140,13 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
             mma_commit(bar_e);
         }
         if (epi) {
-            // X^T has read this chunk's v rows: the next chunk's behind them
-            if (c + 1 < nchunks) {
-                issue_v(t0 + kChunk, min(kChunk, p.T - t0 - kChunk));
-                cp_async_commit();
-            }
             // in the shadow of X^T T^T: scale S Q^T by gamma_t q_scale r_q,t
-            // (the start of O^T), then the next chunk's [K;Q] rows into the
-            // tile S [K;Q]^T has read
+            // (the start of O^T)
             {
                 float qs[16];
                 tmem_ld16(trow + d_col + 64 + s0, qs);
                 mul16(qs, s_gq + s0);
                 tmem_st16(trow + d_col + 64 + s0, qs);
-            }
-            if (c + 1 < nchunks) {
-                issue_kq(t0 + kChunk, min(kChunk, p.T - t0 - kChunk));
-                cp_async_commit();
             }
             wait_mma(bar_e, c);
 
@@ -1189,26 +1195,31 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
         if (epi) {
             wait_mma(bar_s, c);
 
-            // ---- H: the next chunk's S operands, or the final state
+            // ---- H: the next chunk's S operand (hi into T_XA, which the state
+            // update has read; lo into this chunk's consumed S K^T half), or
+            // the final state
             const bool last = (c == nchunks - 1);
-#pragma unroll 1
-            for (int cc = c0; cc < c0 + CS; cc += 16) {
-                float sv[16];
-                tmem_ld16(trow + T_S + cc, sv);
-                if (last) {
+            float sv[2][16];
+            tmem_ld16(trow + T_S + c0, sv[0]);
+            tmem_ld16(trow + T_S + c0 + 16, sv[1]);
+            if (last) {
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        *reinterpret_cast<float4*>(srow + cc + 4 * q) =
-                            make_float4(sv[4 * q], sv[4 * q + 1], sv[4 * q + 2], sv[4 * q + 3]);
-                } else {
-                    store_split8(sm + C_OFF_S_HI + core_off(i, cc, kD), sm + C_OFF_S_LO + core_off(i, cc, kD), sv);
-                    store_split8(sm + C_OFF_S_HI + core_off(i, cc + 8, kD), sm + C_OFF_S_LO + core_off(i, cc + 8, kD),
-                                 sv + 8);
-                }
+                        *reinterpret_cast<float4*>(srow + c0 + 16 * hh + 4 * q) =
+                            make_float4(sv[hh][4 * q], sv[hh][4 * q + 1], sv[hh][4 * q + 2], sv[hh][4 * q + 3]);
+            } else {
+                uint32_t hi[2][8], lo[2][8];
+                split_pack16(sv[0], hi[0], lo[0]);
+                split_pack16(sv[1], hi[1], lo[1]);
+                tmem_st8(trow + T_XA + c0 / 2, hi[0]);
+                tmem_st8(trow + T_XA + c0 / 2 + 8, hi[1]);
+                tmem_st8(trow + d_col + c0 / 2, lo[0]);
+                tmem_st8(trow + d_col + c0 / 2 + 8, lo[1]);
+                tmem_wait_st();
             }
-            cp_async_wait_all();  // the next chunk's [K;Q], v and record
         }
-        fence_async_smem();
         fence_before_sync();
         __syncthreads();
         if (*abort_flag != 0) break;
@@ -1218,7 +1229,15 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
         wait_mma(bar_o, nchunks - 1);
         store_outputs(nchunks - 1);
     }
-    cp_async_wait_all();  // no prefetch may still be writing shared memory at exit
+    if (!epi && lane == 0) {
+        // no copy may still be writing shared memory at exit: wait for the
+        // last requested phase of each input buffer (a completed one returns
+        // at once)
+        for (int cc = in_last; cc >= 0 && cc > in_last - 2; --cc) {
+            if (!mbar_wait(bar_in0 + 8u * (uint32_t)(cc & 1), (uint32_t)(cc >> 1) & 1u, kWaitLimitNs))
+                atomicOr(abort_flag, 1);
+        }
+    }
     // every MMA this CTA issued has completed before TMEM is released
     fence_before_sync();
     __syncthreads();
@@ -1331,6 +1350,42 @@ int gdn_chunk_prefill(const gdn_shape* shape, int32_t T, int32_t chunk, const gd
 
 namespace {
 
+// cuTensorMapEncodeTiled from the driver, looked up once (no link-time
+// dependency on the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        (void)cudaGetLastError();
+    });
+    return fn;
+}
+
+// The chain's tensor maps over the packed rows qkv [T][C] (bf16): 8 x 64
+// boxes for the K and Q columns, 128 x 64 for V.  Returns false if the driver
+// refuses them.
+bool encode_qkv_maps(PrefillParams& p, const void* qkv, int T, int C) {
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)T};
+    const cuuint64_t strides[1] = {(cuuint64_t)C * 2};
+    const cuuint32_t box_kq[2] = {8, (cuuint32_t)kChunk}, box_v[2] = {(cuuint32_t)kD, (cuuint32_t)kChunk};
+    const cuuint32_t unit[2] = {1, 1};
+    void* base = const_cast<void*>(qkv);
+    return enc(&p.tm_kq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box_kq, unit,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
+           enc(&p.tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box_v, unit,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int fused_capacity(int dev) {
     static int cached[64];
     static bool known[64];
@@ -1391,6 +1446,8 @@ int launch_prefill(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const
     p.normalize = (flags & GDN_NORMALIZE_QK) != 0;
     p.out_bf16 = (flags & GDN_OUT_BF16) != 0;
     if (prep) {
+        if (!encode_qkv_maps(p, qkv, T, p.C))
+            return report_error(GDN_ERR_CUDA, "the driver refused the prefill's tensor maps");
         const int nchunks = (T + kChunk - 1) / kChunk;
         p.ready = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + kRecBase +
                                          (size_t)nchunks * shape->Hv * kRecBytes);

@@ -37,6 +37,17 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo) {
     return d;
 }
 
+// The same with both offsets given: `lbo` between core matrices adjacent
+// along K, `sbo` between groups of 8 rows.
+__device__ __forceinline__ uint64_t smem_desc2(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B (K-major), fp32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
@@ -204,6 +215,37 @@ __device__ __forceinline__ void mul16(float (&x)[16], const float* f) {
         x[4 * q + 2] = b.x;
         x[4 * q + 3] = b.y;
     }
+}
+
+// Arrive once on `bar` and announce `bytes` of copy-engine data that will
+// complete on it (the phase completes when both have happened).
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// from global to shared memory by the copy engine, counted on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Tiled TMA load of one box of a 2-D tensor map at element coordinates
+// (x, y) into shared memory, counted on `bar`; rows past the tensor's end
+// read as zeros.  x times the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// Order this thread's earlier generic-proxy view of global memory before its
+// later copy-engine accesses (data another CTA published through a flag).
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // Asynchronous 16-byte global -> shared copy; zero-fills when !valid.
