@@ -234,10 +234,11 @@ __device__ __forceinline__ void chunk_scalars(const float* s_lg, const float* s_
 // L (strictly lower, fp32 [64][64]) and P (lower with the diagonal, bf16 hi/lo
 // B-operand tiles) from the [K;Q] K^T accumulator: thread i_row holds row
 // i_row of it (K rows 0..63 give L, Q rows 64..127 give P); warpgroup wg takes
-// columns 32 wg .. 32 wg + 31.
+// columns 32 wg .. 32 wg + 31.  P goes to fp32 rows at sP32 when that is
+// given, else to the bf16 hi/lo tiles.
 __device__ __forceinline__ void form_l_p(uint32_t g_cols, int i_row, int wg, const float* s_lg, const float* s_brk,
                                          const float* s_rq, const float* s_rk, float* sL, uint8_t* p_hi,
-                                         uint8_t* p_lo) {
+                                         uint8_t* p_lo, float* sP32 = nullptr) {
     const int t = i_row & 63;
     const bool krow = i_row < 64;
     const float lg_t = s_lg[t];
@@ -255,8 +256,8 @@ __device__ __forceinline__ void form_l_p(uint32_t g_cols, int i_row, int wg, con
             // L: strictly lower (rows of K); P: lower incl. diagonal (rows of Q)
             row[j] = (krow ? sj < t : sj <= t) ? v : 0.f;
         }
-        if (krow) {
-            float4* dst = reinterpret_cast<float4*>(sL + t * kChunk + s0);
+        if (krow || sP32 != nullptr) {
+            float4* dst = reinterpret_cast<float4*>((krow ? sL : sP32) + t * kChunk + s0);
 #pragma unroll
             for (int q = 0; q < 4; ++q) dst[q] = make_float4(row[4 * q], row[4 * q + 1], row[4 * q + 2], row[4 * q + 3]);
         } else {
@@ -266,8 +267,9 @@ __device__ __forceinline__ void form_l_p(uint32_t g_cols, int i_row, int wg, con
     }
 }
 
-// T = (I + L)^-1, blocked by 16, into bf16 hi/lo B-operand tiles (all
-// kPrefillThreads threads; contains barriers).  Tf and R are fp32 scratch.
+// T = (I + L)^-1, blocked by 16, into Tf (fp32) and, when t_hi is given, bf16
+// hi/lo B-operand tiles (all kPrefillThreads threads; contains barriers).  R
+// is fp32 scratch.
 template <class Sync>
 __device__ __forceinline__ void solve_t(const float* sL, float* Tf, float* R, uint8_t* t_hi, uint8_t* t_lo, int tid,
                                         Sync sync) {
@@ -302,7 +304,7 @@ __device__ __forceinline__ void solve_t(const float* sL, float* Tf, float* R, ui
     block_row_solve<2>(sL, Tf, R, tid, sync);
     block_row_solve<3>(sL, Tf, R, tid, sync);
     // T -> bf16 hi/lo B-operand tiles (rows t, K = s)
-    for (int e = tid; e < kChunk * 8; e += kPrefillThreads) {
+    for (int e = tid; t_hi != nullptr && e < kChunk * 8; e += kPrefillThreads) {
         const int t = e >> 3, s0 = (e & 7) * 8;
         const float4 a = *reinterpret_cast<const float4*>(Tf + t * kChunk + s0);
         const float4 b = *reinterpret_cast<const float4*>(Tf + t * kChunk + s0 + 4);
@@ -320,33 +322,51 @@ __device__ __forceinline__ void solve_t(const float* sL, float* Tf, float* R, ui
 // to a per-(chunk, value head) record in the workspace in the layout the main
 // kernel copies into shared memory as it is.
 // ---------------------------------------------------------------------------
-constexpr uint32_t REC_TILES = 0;        // T hi, T lo, P hi, P lo: 4 x 8192 B, as OFF_T_HI .. OFF_P_LO
-constexpr uint32_t REC_SCAL = 32768;     // beta, log2 gamma, gamma r_k, gamma q_scale r_q, (gamma_C/gamma) r_k
+constexpr uint32_t REC_W_HI = 0;         // W^T hi [128 j][64 s]  B of X^T W (the state update)
+constexpr uint32_t REC_W_LO = 16384;     // W^T lo
+constexpr uint32_t REC_PT_HI = 32768;    // (P T) hi [64 t][64 s]  B of X^T (P T)^T (the outputs)
+constexpr uint32_t REC_PT_LO = 40960;    // (P T) lo
+constexpr uint32_t REC_SCAL = 49152;     // beta, log2 gamma, gamma r_k, gamma q_scale r_q, (gamma_C/gamma) r_k
 constexpr uint32_t kRecBytes = REC_SCAL + 5 * 64 * 4;
 constexpr uint32_t kRecBase = 256;       // records start after the status word
 
-constexpr uint32_t Q_OFF_KQ = 0;         // [K;Q] 32 KB
-constexpr uint32_t Q_OFF_TILES = 32768;  // T hi, T lo, P hi, P lo (the record's tiles)
-constexpr uint32_t Q_OFF_L = 65536;      // L fp32 16 KB
-constexpr uint32_t Q_OFF_TF = 81920;     // T fp32 16 KB
-constexpr uint32_t Q_OFF_R = 98304;      // block-solve scratch 3 KB
-constexpr uint32_t Q_OFF_SCAL = 101376;  // 9 x 64 fp32
+// Shared memory of one pre-pass pipeline.  Regions whose contents are dead
+// are reused: once [K;Q] K^T and K^T are made, the [K;Q] tile holds P (fp32)
+// and then the P T tiles; once T is solved, L's region holds (diag(c) T)^T.
+constexpr uint32_t Q_OFF_KQ = 0;         // [K;Q] 32 KB (K-major core matrices, 128 rows)
+constexpr uint32_t Q_OFF_P = 0;          // P fp32 16 KB (after [K;Q] is consumed)
+constexpr uint32_t Q_OFF_PT = 16384;     // (P T) hi, lo [64 t][64 s] 2 x 8 KB (copied to the record)
+constexpr uint32_t Q_OFF_KT = 32768;     // K^T [128 j][64 t] 16 KB, A of K^T (diag(c) T)
+constexpr uint32_t Q_OFF_L = 49152;      // L fp32 16 KB
+constexpr uint32_t Q_OFF_CT = 49152;     // (diag(c) T)^T hi, lo [64 s][64 t] 2 x 8 KB (after the solve)
+constexpr uint32_t Q_OFF_TF = 65536;     // T fp32 16 KB
+constexpr uint32_t Q_OFF_R = 81920;      // block-solve scratch 3 KB
+constexpr uint32_t Q_OFF_SCAL = 84992;   // 9 x 64 fp32
 constexpr uint32_t Q_OFF_AB = Q_OFF_SCAL + 9 * 64 * 4;  // alpha, beta of the group's heads: 2 x 64 x kMaxGroup fp32
 constexpr int kMaxGroup = 8;                             // value heads per key head staged at once
-constexpr uint32_t Q_OFF_MISC = Q_OFF_AB + 2 * 64 * kMaxGroup * 4;
+constexpr uint32_t Q_OFF_MISC = Q_OFF_AB + 2 * 64 * kMaxGroup * 4;  // 2 mbarriers, TMEM base, abort flag
 constexpr uint32_t kPrepSmem = Q_OFF_MISC + 32;
-constexpr uint32_t kPrepTmemCols = 64;
+constexpr uint32_t kPrepStride = (kPrepSmem + 1023) / 1024 * 1024;  // one pipeline's share of a worker CTA
+constexpr uint32_t kPrepTmemCols = 128;  // [K;Q] K^T (64 columns), then W^T (64 columns)
 
 // One pre-pass item: chunk c of key head g, giving the records of the key
-// head's value heads.  Runs on threads 0 .. kPrefillThreads - 1 of the CTA
-// (tid), `sync` being a barrier over exactly those threads; `tmem` holds
-// kPrepTmemCols columns and `bar` is an mbarrier whose phase of parity
-// `parity` this item's MMA completes.  Returns false (after raising the status
-// word) when the tensor-core wait timed out.
+// head's value heads.  Per value head, from the chunk's own inputs:
+//   L, P and T = (I + L)^-1 as in the chunk form;
+//   W  = T^T diag(c) K with c_t = (gamma_C / gamma_t) r_k,t (64 x dk), the
+//        state-update factor: S_new = gamma_C S + X^T W;
+//   PT = P T (64 x 64), the output factor: O = diag(gamma r_q) Q S^T + PT X.
+// (With U = T X these are the chunk form's U^T diag(c) K and P U, regrouped
+// so that the chain never forms U.)  W^T = K^T (diag(c) T) runs on tcgen05
+// with K exact in bf16 and diag(c) T split hi + lo; P T runs on the CUDA cores
+// in fp32.  Runs on threads 0 .. kPrefillThreads - 1 of the CTA (tid), `sync`
+// being a barrier over exactly those threads; `tmem` holds kPrepTmemCols
+// columns; `bars` are two mbarriers whose phases this CTA's MMAs complete in
+// turn (`*phase` counts them).  Returns false (after raising the status word)
+// when a tensor-core wait timed out.
 template <class Sync>
-__device__ bool prep_item(const PrefillParams& p, uint8_t* sm, uint32_t tmem, uint32_t bar, uint32_t parity, int c,
+__device__ bool prep_item(const PrefillParams& p, uint8_t* sm, uint32_t tmem, uint32_t bars, uint32_t* phase, int c,
                           int g, int tid, Sync sync) {
-    const int warp = tid >> 5;
+    const int warp = tid >> 5, lane = tid & 31;
     float* s_alpha = reinterpret_cast<float*>(sm + Q_OFF_SCAL);
     float* s_beta = s_alpha + 64;
     float* s_lg = s_alpha + 128;
@@ -356,11 +376,16 @@ __device__ bool prep_item(const PrefillParams& p, uint8_t* sm, uint32_t tmem, ui
     float* s_gq = s_alpha + 384;
     float* s_ck = s_alpha + 448;
     float* s_brk = s_alpha + 512;
-    int* abort_flag = reinterpret_cast<int*>(sm + Q_OFF_MISC + 12);
+    int* abort_flag = reinterpret_cast<int*>(sm + Q_OFF_MISC + 20);
     const uint32_t sbase = smem_u32(sm);
     const int t0 = c * kChunk;
     const int n = min(kChunk, p.T - t0);
     const size_t C = (size_t)p.C;
+    const uint32_t bar_g = bars, bar_w = bars + 8;
+    // a bounded wait for the next phase of one of the two barriers
+    auto wait_mma = [&](uint32_t b, uint32_t ph) {
+        if (!mbar_wait(b, ph & 1u, kWaitLimitNs)) atomicOr(abort_flag, 1);
+    };
 
     // [K;Q] rows of the chunk (zero-filled past the last token)
     for (int idx = tid; idx < 2 * kChunk * 16; idx += kPrefillThreads) {
@@ -387,7 +412,16 @@ __device__ bool prep_item(const PrefillParams& p, uint8_t* sm, uint32_t tmem, ui
         for (int ks = 0; ks < kD / 16; ++ks)
             mma_bf16(tmem, smem_desc(sbase + Q_OFF_KQ + ks * 256, kD * 16),
                      smem_desc(sbase + Q_OFF_KQ + ks * 256, kD * 16), id_g, ks > 0);
-        mma_commit(bar);
+        mma_commit(bar_g);
+    }
+    // K^T (A operand of K^T (diag(c) T)): each warp transposes 16 of the 128
+    // 8 x 8 core matrices of K
+#pragma unroll
+    for (int it = 0; it < 128 / (kPrefillThreads / 32) / 4; ++it) {
+        const int q = warp * (128 / (kPrefillThreads / 32)) + it * 4 + (lane >> 3);
+        const int tb = q >> 4, jb = q & 15;
+        transpose_8x8x4(sbase + Q_OFF_KQ + tb * (kD * 16) + jb * 128 + (lane & 7) * 16,
+                        sbase + Q_OFF_KT + jb * (kChunk * 16) + tb * 128 + (lane & 7) * 16);
     }
     kq_norms(sm + Q_OFF_KQ, s_rk, s_rq, tid, p.normalize != 0, p.q_scale);
     // alpha and beta of the first kMaxGroup value heads of the group, all
@@ -401,48 +435,130 @@ __device__ bool prep_item(const PrefillParams& p, uint8_t* sm, uint32_t tmem, ui
         s_ab[idx] = in ? p.alpha[at] : 1.0f;
         s_ab[kMaxGroup * kChunk + idx] = in ? p.beta[at] : 0.0f;
     }
-    const bool ok = mbar_wait(bar, parity, kWaitLimitNs);
-    if (!ok) atomicOr(abort_flag, 1);
+    wait_mma(bar_g, phase[0]++);
     sync();
     fence_after_sync();
-    const bool fine = *abort_flag == 0;
+    bool fine = *abort_flag == 0;
 
-    if (fine) {
+    const float* sL = reinterpret_cast<const float*>(sm + Q_OFF_L);
+    float* sP = reinterpret_cast<float*>(sm + Q_OFF_P);
+    float* Tf = reinterpret_cast<float*>(sm + Q_OFF_TF);
 #pragma unroll 1
-        for (int j = 0; j < p.group; ++j) {
-            const int h = g * p.group + j;
-            if (tid < kChunk) {
-                const bool in = tid < n;
-                if (j < kMaxGroup) {
-                    s_alpha[tid] = s_ab[j * kChunk + tid];
-                    s_beta[tid] = s_ab[kMaxGroup * kChunk + j * kChunk + tid];
-                } else {
-                    s_alpha[tid] = in ? p.alpha[(size_t)(t0 + tid) * p.Hv + h] : 1.0f;
-                    s_beta[tid] = in ? p.beta[(size_t)(t0 + tid) * p.Hv + h] : 0.0f;
+    for (int j = 0; fine && j < p.group; ++j) {
+        const int h = g * p.group + j;
+        if (tid < kChunk) {
+            const bool in = tid < n;
+            if (j < kMaxGroup) {
+                s_alpha[tid] = s_ab[j * kChunk + tid];
+                s_beta[tid] = s_ab[kMaxGroup * kChunk + j * kChunk + tid];
+            } else {
+                s_alpha[tid] = in ? p.alpha[(size_t)(t0 + tid) * p.Hv + h] : 1.0f;
+                s_beta[tid] = in ? p.beta[(size_t)(t0 + tid) * p.Hv + h] : 0.0f;
+            }
+        }
+        sync();
+        log2_gamma_scan(s_alpha, s_lg, tid);
+        sync();
+        chunk_scalars(s_lg, s_rk, s_rq, s_beta, s_gk, s_gq, s_ck, s_brk, tid);
+        sync();
+        form_l_p(trow, i_row, wg, s_lg, s_brk, s_rq, s_rk, reinterpret_cast<float*>(sm + Q_OFF_L), nullptr, nullptr,
+                 sP);
+        sync();
+        solve_t(sL, Tf, reinterpret_cast<float*>(sm + Q_OFF_R), nullptr, nullptr, tid, sync);
+        sync();
+        // (diag(c) T)^T as the B operand [s][t] of K^T (diag(c) T), hi/lo (a
+        // warp's lanes take consecutive s: conflict-free column reads of T)
+        for (int e = tid; e < kChunk * 8; e += kPrefillThreads) {
+            const int sc = e & 63, tb = (e >> 6) * 8;
+            float v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] = __fmul_rn(s_ck[tb + q], Tf[(tb + q) * kChunk + sc]);
+            store_split8(sm + Q_OFF_CT + core_off(sc, tb, kChunk), sm + Q_OFF_CT + 8192 + core_off(sc, tb, kChunk), v);
+        }
+        fence_async_smem();
+        fence_before_sync();
+        sync();
+        if (tid == 0) {
+            fence_after_sync();
+            constexpr uint32_t id_w = idesc_bf16(128, 64);
+#pragma unroll
+            for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+                for (int ks = 0; ks < kChunk / 16; ++ks)
+                    mma_bf16(tmem + 64, smem_desc(sbase + Q_OFF_KT + ks * 256, kChunk * 16),
+                             smem_desc(sbase + Q_OFF_CT + (pass ? 8192 : 0) + ks * 256, kChunk * 16),
+                             id_w, (pass > 0 || ks > 0));
+            mma_commit(bar_w);
+        }
+        // meanwhile P T on the CUDA cores, a 4 x 4 block per thread, summed
+        // over u in order (the terms with u > t or u < s are exact zeros: P
+        // and T are lower triangular), into hi/lo tiles [t][s]
+        {
+            const int tb = (tid >> 4) * 4, sb = (tid & 15) * 4;
+            float acc[4][4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[r][q] = 0.f;
+#pragma unroll 2
+            for (int u = 0; u < kChunk; u += 4) {
+                float4 pr[4], tr[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) pr[r] = *reinterpret_cast<const float4*>(sP + (tb + r) * kChunk + u);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) tr[r] = *reinterpret_cast<const float4*>(Tf + (u + r) * kChunk + sb);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const float pv[4] = {pr[r].x, pr[r].y, pr[r].z, pr[r].w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float tv[4] = {tr[k].x, tr[k].y, tr[k].z, tr[k].w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) acc[r][q] = __fmaf_rn(pv[k], tv[q], acc[r][q]);
+                    }
                 }
             }
-            sync();
-            log2_gamma_scan(s_alpha, s_lg, tid);
-            sync();
-            chunk_scalars(s_lg, s_rk, s_rq, s_beta, s_gk, s_gq, s_ck, s_brk, tid);
-            sync();
-            form_l_p(trow, i_row, wg, s_lg, s_brk, s_rq, s_rk, reinterpret_cast<float*>(sm + Q_OFF_L),
-                     sm + Q_OFF_TILES + 16384, sm + Q_OFF_TILES + 24576);
-            sync();
-            solve_t(reinterpret_cast<const float*>(sm + Q_OFF_L), reinterpret_cast<float*>(sm + Q_OFF_TF),
-                    reinterpret_cast<float*>(sm + Q_OFF_R), sm + Q_OFF_TILES, sm + Q_OFF_TILES + 8192, tid, sync);
-            sync();
-            // the record of (chunk c, value head h)
-            uint8_t* rec = reinterpret_cast<uint8_t*>(p.status) + kRecBase + ((size_t)c * p.Hv + h) * kRecBytes;
-            for (int v = tid; v < 32768 / 16; v += kPrefillThreads)
-                reinterpret_cast<uint4*>(rec + REC_TILES)[v] = reinterpret_cast<const uint4*>(sm + Q_OFF_TILES)[v];
-            if (tid < 5 * 16) {
-                const float* src[5] = {s_beta, s_lg, s_gk, s_gq, s_ck};
-                reinterpret_cast<uint4*>(rec + REC_SCAL)[tid] =
-                    reinterpret_cast<const uint4*>(src[tid >> 4])[tid & 15];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                uint32_t h0, l0, h1, l1;
+                split_pair(acc[r][0], acc[r][1], h0, l0);
+                split_pair(acc[r][2], acc[r][3], h1, l1);
+                *reinterpret_cast<uint2*>(sm + Q_OFF_PT + core_off(tb + r, sb, kChunk)) = make_uint2(h0, h1);
+                *reinterpret_cast<uint2*>(sm + Q_OFF_PT + 8192 + core_off(tb + r, sb, kChunk)) = make_uint2(l0, l1);
             }
-            sync();
         }
+        wait_mma(bar_w, phase[1]++);
+        sync();
+        fence_after_sync();
+        if (*abort_flag != 0) {
+            fine = false;
+            break;
+        }
+        // the record of (chunk c, value head h): W^T from TMEM (lane j, this
+        // warpgroup's 32 columns s) as hi/lo tiles, P T and the scalars
+        uint8_t* rec = reinterpret_cast<uint8_t*>(p.status) + kRecBase + ((size_t)c * p.Hv + h) * kRecBytes;
+        {
+            float w[2][16];
+            tmem_ld16(trow + 64 + wg * 32, w[0]);
+            tmem_ld16(trow + 64 + wg * 32 + 16, w[1]);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int sc = wg * 32 + hh * 16 + q * 8;
+                    store_split8(rec + REC_W_HI + core_off(i_row, sc, kChunk), rec + REC_W_LO + core_off(i_row, sc, kChunk),
+                                 w[hh] + q * 8);
+                }
+        }
+        for (int v = tid; v < 16384 / 16; v += kPrefillThreads)
+            reinterpret_cast<uint4*>(rec + REC_PT_HI)[v] = reinterpret_cast<const uint4*>(sm + Q_OFF_PT)[v];
+        if (tid < 5 * 16) {
+            const float* src[5] = {s_beta, s_lg, s_gk, s_gq, s_ck};
+            reinterpret_cast<uint4*>(rec + REC_SCAL)[tid] = reinterpret_cast<const uint4*>(src[tid >> 4])[tid & 15];
+        }
+        fence_before_sync();
+        sync();  // every thread is past this head's TMEM reads and tiles
+        fence_after_sync();
     }
     if (!fine && tid == 0) atomicExch(p.status, 1);
     fence_before_sync();
@@ -451,14 +567,15 @@ __device__ bool prep_item(const PrefillParams& p, uint8_t* sm, uint32_t tmem, ui
     return fine;
 }
 
-// TMEM, mbarrier and abort flag of a pre-pass CTA (threads 0 .. kPrefillThreads - 1).
+// TMEM, mbarriers and abort flag of a pre-pass CTA (threads 0 .. kPrefillThreads - 1).
 template <class Sync>
 __device__ uint32_t prep_setup(uint8_t* sm, int tid, Sync sync) {
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Q_OFF_MISC + 8);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Q_OFF_MISC + 16);
     if ((tid >> 5) == 0) tmem_alloc(smem_u32(tmem_slot), kPrepTmemCols);
     if (tid == 0) {
         mbar_init(smem_u32(sm + Q_OFF_MISC), 1);
-        *reinterpret_cast<int*>(sm + Q_OFF_MISC + 12) = 0;
+        mbar_init(smem_u32(sm + Q_OFF_MISC + 8), 1);
+        *reinterpret_cast<int*>(sm + Q_OFF_MISC + 20) = 0;
     }
     fence_before_sync();
     sync();
@@ -471,7 +588,8 @@ gdn_prefill_prep_kernel(const __grid_constant__ PrefillParams p) {
     extern __shared__ __align__(1024) uint8_t sm[];
     const int tid = threadIdx.x;
     const uint32_t tmem = prep_setup(sm, tid, CtaSync{});
-    prep_item(p, sm, tmem, smem_u32(sm + Q_OFF_MISC), 0, blockIdx.x, blockIdx.y, tid, CtaSync{});
+    uint32_t phase[2] = {0, 0};
+    prep_item(p, sm, tmem, smem_u32(sm + Q_OFF_MISC), phase, blockIdx.x, blockIdx.y, tid, CtaSync{});
     if ((tid >> 5) == 0) tmem_dealloc(tmem, kPrepTmemCols);
 }
 
@@ -825,51 +943,52 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
 
 
 // ---------------------------------------------------------------------------
-// The pipelined chain (pre-pass path).  The same chunk form and the same
-// bf16 hi/lo passes as the kernel above, scheduled so that only the steps that
-// carry the state from chunk to chunk sit on the critical path:
-//   S K^T -> X^T -> U^T = X^T T^T -> Uhat^T -> S += Uhat^T K -> S operand split
-// while the output side (S Q^T, its scaling, U^T P^T, the output stores) runs
-// in the shadow of those MMAs.  X^T, Uhat^T and U^T are A operands written by
-// the epilogue threads straight to tensor memory as bf16 pairs; the pre-pass
-// records are double-buffered in shared memory and prefetched a whole chunk
-// ahead; the output accumulator is double-buffered in tensor memory, so that
-// chunk c's outputs are read out while chunk c + 1's S K^T runs.
+// The pipelined chain (pre-pass path).  The chunk form regrouped so that the
+// chain never forms U = T X: with the pre-pass factors W = T^T diag(c) K and
+// PT = P T,
+//   S_new = gamma_C S + X^T W,      O^T = (S Q^T) diag(gamma r_q) + X^T PT^T,
+// so that only S [K;Q]^T -> X^T -> S += X^T W -> the next S operand carry the
+// state from chunk to chunk, while the output side (the S Q^T scaling,
+// X^T PT^T and the output stores) runs in the shadow of those MMAs.  X^T is
+// the A operand of both products, written by the epilogue threads straight
+// to tensor memory as bf16 pairs, as is the S operand of S [K;Q]^T.  A chunk's
+// inputs ([K;Q], v, the record) arrive by the copy engine a whole chunk ahead
+// into double buffers; the output accumulator is double-buffered in tensor
+// memory, so that chunk c's outputs are read out while chunk c + 1 runs.
 // ---------------------------------------------------------------------------
 constexpr int kEpiThreads = 512;    // four epilogue warpgroups over the 128 TMEM lanes
 constexpr int kChainThreads = kEpiThreads + 32;  // and one warp that only issues the MMAs
-constexpr uint32_t kRecStride = 34816;  // a record slot, padded to 1 KB
+constexpr uint32_t kRecStride = (kRecBytes + 1023) / 1024 * 1024;  // a record slot, padded to 1 KB
 
 // Inputs of a chunk are double-buffered by chunk parity and loaded by the
 // copy engine a whole chunk ahead.  [K;Q] is [16 column blocks][128 rows][8]
 // (K rows 0..63, Q rows 64..127): one TMA box per 16-byte column of K or Q,
 // i.e. K-major core matrices 2,048 B apart along K and 128 B apart along rows.
 constexpr uint32_t C_OFF_KQ = 0;         // [K;Q] x 2   B of S [K;Q]^T
-constexpr uint32_t C_OFF_KT = 65536;     // K^T   [128 j][64 t]   B of Uhat^T K
-constexpr uint32_t C_OFF_V = 81920;      // V     [64 t][128 i] x 2, plain row-major
-constexpr uint32_t C_OFF_REC = 114688;   // two record slots (T hi/lo, P hi/lo, scalars)
+constexpr uint32_t C_OFF_V = 65536;      // V     [64 t][128 i] x 2, plain row-major
+constexpr uint32_t C_OFF_REC = 98304;    // two record slots (W^T hi/lo, PT hi/lo, scalars)
 constexpr uint32_t kKqBytes = 32768, kVBytes = 16384;
 constexpr uint32_t kInputTx = kKqBytes + kVBytes + kRecBytes;  // bytes a chunk's inputs bring
 constexpr uint32_t C_OFF_MISC = C_OFF_REC + 2 * kRecStride;  // mbarriers, TMEM base, abort flag
 constexpr uint32_t kChainSmem = C_OFF_MISC + 128;
 // A chain CTA takes all 512 TMEM columns of its SM, so no two may share an SM:
-// its shared memory must exceed half of the 227 KB an SM offers.
+// its shared memory must exceed half of the 227 KB an SM offers.  The
+// cooperative kernel's workers run the pre-pass in the same allocation.
 static_assert(kChainSmem > 232448 / 2, "chain CTAs must not fit two to an SM");
+static_assert(kChainSmem <= 232448 && kPrepStride + kPrepSmem <= kChainSmem, "shared-memory layouts");
 
-// TMEM columns.  The state, S [K;Q]^T and U^T are fp32 accumulators; X^T
-// (later Uhat^T) and U^T as A operands hold bf16 hi in their first 32
-// columns and lo in the next 32.  S [K;Q]^T is double-buffered by chunk
-// parity: its S K^T half feeds X^T, its S Q^T half becomes O^T, which is read
-// out while the next chunk runs.  U^T as an A operand overwrites the fp32 U^T
-// it is made from.  Between chunks, the next chunk's S operand (64 columns
-// each = 128 bf16 per lane) has bf16 hi in T_XA, written once the state
-// update has read the Uhat^T there, and lo in the S K^T half of the current
-// chunk's buffer, which the X^T epilogue has consumed (and which the chunk
-// after next rewrites, after the next chunk's MMAs have read it).
+// TMEM columns.  The state and S [K;Q]^T are fp32 accumulators.  S [K;Q]^T
+// is double-buffered by chunk parity: its S K^T half feeds X^T, its S Q^T
+// half becomes O^T, which is read out while the next chunk runs.  X^T as an A
+// operand holds bf16 hi in its first 32 columns and lo in the next 32.  The S
+// operand of the next chunk (64 columns each = 128 bf16 per lane) has hi in
+// T_SH and lo in the S K^T half of the current chunk's buffer, which the X^T
+// epilogue has consumed (and which the chunk after next rewrites, after the
+// next chunk's MMAs have read it).
 constexpr uint32_t T_S = 0;      // S [i][j]                               128 columns
 constexpr uint32_t T_D = 128;    // [S K^T | S Q^T -> O^T] [i][t], 2 x 128 (by chunk parity)
-constexpr uint32_t T_U = 384;    // U^T fp32, then U^T hi 32 + lo 32      64
-constexpr uint32_t T_XA = 448;   // X^T, then Uhat^T       hi 32 + lo 32  64
+constexpr uint32_t T_SH = 384;   // S hi (the next chunk's operand)        64
+constexpr uint32_t T_XA = 448;   // X^T                    hi 32 + lo 32  64
 
 // Wait (bounded) until the pre-pass item `item` has been published.
 __device__ __forceinline__ bool wait_ready(const int* ready, int item) {
@@ -884,8 +1003,8 @@ __device__ __forceinline__ bool wait_ready(const int* ready, int item) {
 }
 
 // The chain of value head h.  READY: the records are produced concurrently
-// by the pre-pass workers of the cooperative kernel, and thread 0 waits for a
-// record's flag before the CTA barrier that precedes its prefetch.
+// by the pre-pass workers of the cooperative kernel; the MMA warp waits for a
+// record's flag just before it requests the record, a chunk ahead of use.
 template <bool READY>
 __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, int h) {
     constexpr int CW = kChunk / 4;  // columns of a 64-wide tile per warpgroup
@@ -900,9 +1019,8 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
     int* abort_flag = reinterpret_cast<int*>(sm + C_OFF_MISC + 100);
     const uint32_t sbase = smem_u32(sm);
     const uint32_t bar_ks = smem_u32(bars + 0);    // S [K;Q]^T
-    const uint32_t bar_e = smem_u32(bars + 2);     // X^T T^T
-    const uint32_t bar_s = smem_u32(bars + 3);     // state update
-    const uint32_t bar_o = smem_u32(bars + 4);     // U^T P^T
+    const uint32_t bar_s = smem_u32(bars + 3);     // state update X^T W
+    const uint32_t bar_o = smem_u32(bars + 4);     // outputs X^T PT^T
     const uint32_t bar_fin = smem_u32(bars + 5);   // every MMA issued, before TMEM is freed
     const uint32_t bar_in0 = smem_u32(bars + 6);   // a chunk's inputs landed in buffer 0 (bar_in0 + 8: buffer 1)
 
@@ -910,7 +1028,6 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
     if (tid == 0) {
         for (int b = 0; b < 8; ++b) mbar_init(smem_u32(bars + b), 1);
         *abort_flag = 0;
-        if (READY && p.T > 0 && !wait_ready(p.ready, g)) *abort_flag = 1;  // chunk 0's record
     }
     fence_before_sync();
     __syncthreads();
@@ -947,7 +1064,7 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
         tmem_st16(trow + T_S + cc, v);
         uint32_t hi[8], lo[8];
         split_pack16(v, hi, lo);
-        tmem_st8(trow + T_XA + cc / 2, hi);
+        tmem_st8(trow + T_SH + cc / 2, hi);
         tmem_st8(trow + T_D + 128 + cc / 2, lo);  // chunk 0 reads lo from buffer 1
     }
     tmem_wait_st();
@@ -958,24 +1075,43 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
     // engine: 32 TMA boxes for [K;Q] (lane l: K column block l, or Q column
     // block l - 16), one for V and one bulk copy of the record, all counted
     // on that buffer's barrier.  Rows past the end of the prompt read as zeros.
+    // (The barrier expects all of a chunk's bytes when [K;Q] and V are
+    // requested; the record follows later, once its flag is set.)
     int in_last = -1;  // MMA warp: the last chunk whose inputs it requested
-    auto issue_inputs = [&](int cc) {
+    auto issue_kqv = [&](int cc) {
         in_last = cc;
         const uint32_t b = bar_in0 + 8u * (uint32_t)(cc & 1);
         const int t0 = cc * kChunk;
         if (lane == 0) mbar_arrive_expect_tx(b, kInputTx);
         __syncwarp();
-        fence_proxy_async_global();
         const uint32_t kq = sbase + C_OFF_KQ + (uint32_t)(cc & 1) * kKqBytes;
         const int kb = lane & 15;
         const int x = (lane < 16 ? p.Hk * kD : 0) + g * kD + kb * 8;
         tma_load_2d(kq + (uint32_t)kb * 2048u + (lane < 16 ? 0u : 1024u), &p.tm_kq, x, t0, b);
-        if (lane == 0) {
+        if (lane == 0)
             tma_load_2d(sbase + C_OFF_V + (uint32_t)(cc & 1) * kVBytes, &p.tm_v, 2 * p.Hk * kD + h * kD, t0, b);
+    };
+    // whether chunk cc's record is published (READY), without waiting
+    auto record_ready = [&](int cc) -> bool {
+        if (!READY) return true;
+        int v = 0;
+        if (lane == 0) asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.ready + cc * p.Hk + g) : "memory");
+        return __shfl_sync(0xffffffffu, v, 0) != 0;
+    };
+    bool rec_pending = false;  // MMA warp: the next chunk's record is still to be requested
+    auto issue_record = [&](int cc) {
+        if (lane == 0) {
+            if (READY && !wait_ready(p.ready, cc * p.Hk + g)) atomicOr(abort_flag, 1);
+            fence_proxy_async_global();
             const uint8_t* rec =
                 reinterpret_cast<const uint8_t*>(p.status) + kRecBase + ((size_t)cc * p.Hv + h) * kRecBytes;
-            bulk_g2s(sbase + C_OFF_REC + (uint32_t)(cc & 1) * kRecStride, rec, kRecBytes, b);
+            bulk_g2s(sbase + C_OFF_REC + (uint32_t)(cc & 1) * kRecStride, rec, kRecBytes,
+                     bar_in0 + 8u * (uint32_t)(cc & 1));
         }
+    };
+    auto issue_inputs = [&](int cc) {
+        issue_kqv(cc);
+        issue_record(cc);
     };
     // every thread that reads a buffer waits for its phase (chunk cc is the
     // (cc >> 1)-th use of buffer cc & 1)
@@ -992,10 +1128,9 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
     // stay short for the tensor pipe to be fed at its own rate.
     const uint64_t d_kq0 = smem_desc2(sbase + C_OFF_KQ, 2048, 128);  // [K;Q] of buffer 0
     constexpr uint64_t kKqDesc = kKqBytes >> 4;                    // buffer 1 vs buffer 0
-    const uint64_t d_kt = smem_desc(sbase + C_OFF_KT, kChunk * 16);
-    const uint64_t d_rec0 = smem_desc(sbase + C_OFF_REC + REC_TILES, kChunk * 16);
+    const uint64_t d_rec0 = smem_desc(sbase + C_OFF_REC, kChunk * 16);  // record slot 0, 64-wide K-major tiles
     constexpr uint64_t kRecDesc = kRecStride >> 4;  // slot 1 vs slot 0
-    constexpr uint64_t kTLo = 8192 >> 4, kPHi = 16384 >> 4, kPLo = 24576 >> 4;
+    constexpr uint64_t kWHi = REC_W_HI >> 4, kWLo = REC_W_LO >> 4, kPtHi = REC_PT_HI >> 4, kPtLo = REC_PT_LO >> 4;
 
     const size_t ostride = (size_t)p.Hv * kD;
     // outputs of chunk cc (its O^T buffer, after U^T P^T completed)
@@ -1024,7 +1159,6 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
 
 #pragma unroll 1
     for (int c = 0; c < nchunks; ++c) {
-        const int t0 = c * kChunk;
         const uint32_t d_col = T_D + (uint32_t)(c & 1) * 128;  // S K^T here, O^T at + 64
         const uint32_t s_lo = T_D + (uint32_t)((c + 1) & 1) * 128;  // this chunk's S lo operand
         const uint8_t* rec = sm + C_OFF_REC + (uint32_t)(c & 1) * kRecStride;
@@ -1032,25 +1166,10 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
         const float* s_lg = s_beta + 64;   // log2 gamma_t
         const float* s_gk = s_beta + 128;  // gamma_t r_k,t
         const float* s_gq = s_beta + 192;  // gamma_t q_scale r_q,t
-        const float* s_ck = s_beta + 256;  // (gamma_C / gamma_t) r_k,t
-        const uint64_t d_rec = d_rec0 + (uint64_t)(c & 1) * kRecDesc;  // T hi of this chunk's record
+        const uint64_t d_rec = d_rec0 + (uint64_t)(c & 1) * kRecDesc;
 
-        // ---- A: K^T from the staged K rows, once chunk c's inputs have landed
-        if (epi) {
-            wait_inputs(c);
-            const uint32_t kq = sbase + C_OFF_KQ + (uint32_t)(c & 1) * kKqBytes;
-#pragma unroll
-            for (int it = 0; it < 128 / (kEpiThreads / 32) / 4; ++it) {
-                const int q = warp * (128 / (kEpiThreads / 32)) + it * 4 + (lane >> 3);
-                const int tb = q >> 4, jb = q & 15;
-                const uint32_t src = kq + jb * 2048 + tb * 128 + (lane & 7) * 16;
-                const uint32_t dst = sbase + C_OFF_KT + jb * (kChunk * 16) + tb * 128 + (lane & 7) * 16;
-                transpose_8x8x4(src, dst);
-            }
-        }
-        // the next chunk's record is prefetched after this barrier
-        if (READY && tid == 0 && c + 1 < nchunks && !wait_ready(p.ready, (c + 1) * p.Hk + g)) atomicOr(abort_flag, 1);
-        fence_async_smem();
+        // ---- A: chunk c's inputs have landed
+        if (epi) wait_inputs(c);
         fence_before_sync();
         __syncthreads();
 
@@ -1062,22 +1181,22 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
             for (int pass = 0; pass < 2; ++pass)
 #pragma unroll
                 for (int ks = 0; ks < kD / 16; ++ks)
-                    mma_bf16_ts(tmem + d_col, tmem + (pass ? s_lo : T_XA) + ks * 8,
+                    mma_bf16_ts(tmem + d_col, tmem + (pass ? s_lo : T_SH) + ks * 8,
                                 d_kq0 + (uint64_t)(c & 1) * kKqDesc + 256 * ks, id, (pass > 0 || ks > 0));
             mma_commit(bar_ks);
         }
-        // the next chunk's inputs, into the buffer chunk c - 1 used (its record's
-        // P tile is read by U^T P^T of chunk c - 1: wait for that first)
+        // the next chunk's [K;Q] and v, into the buffers chunk c - 1 used (its
+        // record's PT tile is read by chunk c - 1's output MMA: wait for that
+        // first, since the record follows into that slot)
         if (!epi && c + 1 < nchunks) {
             if (c > 0 && lane == 0 && !mbar_wait(bar_o, (uint32_t)(c - 1) & 1u, kWaitLimitNs)) atomicOr(abort_flag, 1);
-            issue_inputs(c + 1);
+            issue_kqv(c + 1);
+            // the record too if it is already published; else after this chunk's MMAs
+            rec_pending = !record_ready(c + 1);
+            if (!rec_pending) issue_record(c + 1);
         }
         if (epi) {
-            // in the shadow of S [K;Q]^T: the previous chunk's outputs; S <- gamma_C S
-            if (c > 0) {
-                wait_mma(bar_o, c - 1);
-                store_outputs(c - 1);
-            }
+            // in the shadow of S [K;Q]^T: S <- gamma_C S
             {
                 const float gamma_c = exp2f(s_lg[kChunk - 1]);
                 const float2 g2 = make_float2(gamma_c, gamma_c);
@@ -1096,7 +1215,8 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
             }
             wait_mma(bar_ks, c);
 
-            // ---- C: X^T[i][s] = beta_s (v_s[i] - gamma_s r_k,s (S k_s)[i]) as the A operand of X^T T^T
+            // ---- C: X^T[i][s] = beta_s (v_s[i] - gamma_s r_k,s (S k_s)[i]) as the A operand
+            // of both X^T W and X^T PT^T; S Q^T scaled by gamma_t q_scale r_q,t (the start of O^T)
             {
                 const uint16_t* vcol = reinterpret_cast<const uint16_t*>(sm + C_OFF_V + (uint32_t)(c & 1) * kVBytes) + i;
                 float ks[16], x[16];
@@ -1121,83 +1241,51 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
                 split_pack16(x, hi, lo);
                 tmem_st8(trow + T_XA + s0 / 2, hi);
                 tmem_st8(trow + T_XA + 32 + s0 / 2, lo);
+                float qs[16];
+                tmem_ld16(trow + d_col + 64 + s0, qs);
+                mul16(qs, s_gq + s0);
+                tmem_st16(trow + d_col + 64 + s0, qs);
                 tmem_wait_st();  // also covers the S rescale above
             }
         }
         fence_before_sync();
         __syncthreads();
 
-        // ---- E: U^T = X^T T^T (3 passes: hi.hi, hi.lo, lo.hi)
-        if (issuer) {
-            fence_after_sync();
-            constexpr uint32_t id = idesc_bf16(128, 64);
-#pragma unroll
-            for (int pass = 0; pass < 3; ++pass)  // (X hi, T hi), (X hi, T lo), (X lo, T hi)
-#pragma unroll
-                for (int ks = 0; ks < kChunk / 16; ++ks)
-                    mma_bf16_ts(tmem + T_U, tmem + T_XA + (pass == 2 ? 32 : 0) + ks * 8,
-                                d_rec + (pass == 1 ? kTLo : 0) + 16 * ks, id, (pass > 0 || ks > 0));
-            mma_commit(bar_e);
-        }
-        if (epi) {
-            // in the shadow of X^T T^T: scale S Q^T by gamma_t q_scale r_q,t
-            // (the start of O^T)
-            {
-                float qs[16];
-                tmem_ld16(trow + d_col + 64 + s0, qs);
-                mul16(qs, s_gq + s0);
-                tmem_st16(trow + d_col + 64 + s0, qs);
-            }
-            wait_mma(bar_e, c);
-
-            // ---- F: Uhat^T = U^T diag(gamma_C / gamma r_k) and U^T as A operands
-            {
-                float u[16], uh[16];
-                tmem_ld16(trow + T_U + s0, u);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) uh[j] = u[j];
-                mul16(uh, s_ck + s0);
-                uint32_t hi[8], lo[8];
-                split_pack16(uh, hi, lo);
-                tmem_st8(trow + T_XA + s0 / 2, hi);
-                tmem_st8(trow + T_XA + 32 + s0 / 2, lo);
-                split_pack16(u, hi, lo);
-                // U^T hi/lo overwrite the fp32 U^T: every epilogue warp has
-                // read its columns first (named barrier 1 over the epilogue warps)
-                asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-                tmem_st8(trow + T_U + s0 / 2, hi);
-                tmem_st8(trow + T_U + 32 + s0 / 2, lo);
-                tmem_wait_st();  // also covers the O^T scaling above
-            }
-        }
-        fence_before_sync();
-        __syncthreads();
-
-        // ---- G: S += Uhat^T K (2 passes); then O^T += U^T P^T (3 passes)
+        // ---- G: S += X^T W (3 passes); then O^T += X^T PT^T (3 passes)
         if (issuer) {
             fence_after_sync();
             constexpr uint32_t id_s = idesc_bf16(128, 128);
             constexpr uint32_t id_o = idesc_bf16(128, 64);
 #pragma unroll
-            for (int pass = 0; pass < 2; ++pass)
+            for (int pass = 0; pass < 3; ++pass)  // (X hi, W hi), (X hi, W lo), (X lo, W hi)
 #pragma unroll
                 for (int ks = 0; ks < kChunk / 16; ++ks)
-                    mma_bf16_ts(tmem + T_S, tmem + T_XA + (pass ? 32 : 0) + ks * 8, d_kt + 16 * ks, id_s, 1u);
+                    mma_bf16_ts(tmem + T_S, tmem + T_XA + (pass == 2 ? 32 : 0) + ks * 8,
+                                d_rec + (pass == 1 ? kWLo : kWHi) + 16 * ks, id_s, 1u);
             mma_commit(bar_s);
 #pragma unroll
-            for (int pass = 0; pass < 3; ++pass)  // (U hi, P hi), (U hi, P lo), (U lo, P hi)
+            for (int pass = 0; pass < 3; ++pass)  // (X hi, PT hi), (X hi, PT lo), (X lo, PT hi)
 #pragma unroll
                 for (int ks = 0; ks < kChunk / 16; ++ks)
-                    mma_bf16_ts(tmem + d_col + 64, tmem + T_U + (pass == 2 ? 32 : 0) + ks * 8,
-                                d_rec + (pass == 1 ? kPLo : kPHi) + 16 * ks, id_o, 1u);
+                    mma_bf16_ts(tmem + d_col + 64, tmem + T_XA + (pass == 2 ? 32 : 0) + ks * 8,
+                                d_rec + (pass == 1 ? kPtLo : kPtHi) + 16 * ks, id_o, 1u);
             mma_commit(bar_o);
         }
+        // the next chunk's record, if it was not published in time above
+        if (!epi && rec_pending) {
+            issue_record(c + 1);
+            rec_pending = false;
+        }
         if (epi) {
+            // in the shadow of the state update: the previous chunk's outputs
+            if (c > 0) {
+                wait_mma(bar_o, c - 1);
+                store_outputs(c - 1);
+            }
             wait_mma(bar_s, c);
 
-            // ---- H: the next chunk's S operand (hi into T_XA, which the state
-            // update has read; lo into this chunk's consumed S K^T half), or
-            // the final state
+            // ---- H: the next chunk's S operand (hi into T_SH; lo into this
+            // chunk's consumed S K^T half), or the final state
             const bool last = (c == nchunks - 1);
             float sv[2][16];
             tmem_ld16(trow + T_S + c0, sv[0]);
@@ -1213,8 +1301,8 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
                 uint32_t hi[2][8], lo[2][8];
                 split_pack16(sv[0], hi[0], lo[0]);
                 split_pack16(sv[1], hi[1], lo[1]);
-                tmem_st8(trow + T_XA + c0 / 2, hi[0]);
-                tmem_st8(trow + T_XA + c0 / 2 + 8, hi[1]);
+                tmem_st8(trow + T_SH + c0 / 2, hi[0]);
+                tmem_st8(trow + T_SH + c0 / 2 + 8, hi[1]);
                 tmem_st8(trow + d_col + c0 / 2, lo[0]);
                 tmem_st8(trow + d_col + c0 / 2 + 8, lo[1]);
                 tmem_wait_st();
@@ -1259,28 +1347,53 @@ gdn_prefill_chain_kernel(const __grid_constant__ PrefillParams p) {
     chain_body<false>(p, sm, blockIdx.x);
 }
 
-// Pre-pass worker w of the cooperative kernel: items (chunk, key head) in
-// chunk order, w, w + n_workers, ...; each is published with a release store
-// of its flag once all of its records are written.
-__device__ __forceinline__ void prep_worker(const PrefillParams& p, uint8_t* sm, int w) {
-    const int tid = threadIdx.x;
-    const NamedSync<2, kPrefillThreads> sync;
-    const uint32_t tmem = prep_setup(sm, tid, sync);
-    const uint32_t bar = smem_u32(sm + Q_OFF_MISC);
+// Pre-pass worker w of the cooperative kernel: two independent pipelines of
+// kPrefillThreads threads (each with its own shared memory, named barrier and
+// 128 TMEM columns of one shared allocation), pipeline q taking the items
+// (chunk, key head) 2w + q, 2w + q + 2 n_workers, ... in chunk order.  Each
+// item is published with a release store of its flag once all of its records
+// are written.
+template <int Q>
+__device__ __forceinline__ void prep_pipeline(const PrefillParams& p, uint8_t* sm, uint32_t tmem, int w) {
+    const int tid = threadIdx.x - Q * kPrefillThreads;
+    const NamedSync<2 + Q, kPrefillThreads> sync;
+    uint8_t* smq = sm + Q * kPrepStride;
+    const uint32_t bars = smem_u32(smq + Q_OFF_MISC);
     const int items = ((p.T + kChunk - 1) / kChunk) * p.Hk;
-    uint32_t k = 0;
+    uint32_t phase[2] = {0, 0};
 #pragma unroll 1
-    for (int item = w; item < items; item += p.n_workers, ++k) {
-        const bool ok = prep_item(p, sm, tmem, bar, k & 1u, item / p.Hk, item % p.Hk, tid, sync);
+    for (int item = 2 * w + Q; item < items; item += 2 * p.n_workers) {
+        const bool ok = prep_item(p, smq, tmem + Q * kPrepTmemCols, bars, phase, item / p.Hk, item % p.Hk, tid, sync);
         __threadfence();  // this thread's record stores, before the flag
         sync();
         if (tid == 0 && ok) asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.ready + item), "r"(1) : "memory");
         if (!ok) break;
     }
+}
+
+__device__ __forceinline__ void prep_worker(const PrefillParams& p, uint8_t* sm, int w) {
+    const int tid = threadIdx.x;  // 0 .. 2 kPrefillThreads - 1
+    const NamedSync<1, 2 * kPrefillThreads> all;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Q_OFF_MISC + 16);
+    if ((tid >> 5) == 0) tmem_alloc(smem_u32(tmem_slot), 2 * kPrepTmemCols);
+    if (tid == 0) {
+        for (int q = 0; q < 2; ++q) {
+            uint8_t* smq = sm + q * kPrepStride;
+            mbar_init(smem_u32(smq + Q_OFF_MISC), 1);
+            mbar_init(smem_u32(smq + Q_OFF_MISC + 8), 1);
+            *reinterpret_cast<int*>(smq + Q_OFF_MISC + 20) = 0;
+        }
+    }
     fence_before_sync();
-    sync();
+    all();
     fence_after_sync();
-    if ((tid >> 5) == 0) tmem_dealloc(tmem, kPrepTmemCols);
+    const uint32_t tmem = *tmem_slot;
+    if (tid < kPrefillThreads) prep_pipeline<0>(p, sm, tmem, w);
+    else prep_pipeline<1>(p, sm, tmem, w);
+    fence_before_sync();
+    all();
+    fence_after_sync();
+    if ((tid >> 5) == 0) tmem_dealloc(tmem, 2 * kPrepTmemCols);
 }
 
 // Pre-pass and chain in one cooperative launch (every CTA resident at once, so
@@ -1292,7 +1405,7 @@ gdn_prefill_fused_kernel(const __grid_constant__ PrefillParams p) {
     extern __shared__ __align__(1024) uint8_t sm[];
     if ((int)blockIdx.x < p.Hv) {
         chain_body<true>(p, sm, blockIdx.x);
-    } else if ((int)threadIdx.x < kPrefillThreads) {
+    } else if ((int)threadIdx.x < 2 * kPrefillThreads) {
         prep_worker(p, sm, blockIdx.x - p.Hv);
     }
 }

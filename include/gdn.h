@@ -304,10 +304,10 @@ int gdn_commit_path(const gdn_shape* shape, int32_t N, const int32_t* parents,
  * gdn_prefill_workspace_bytes -- device workspace gdn_chunk_prefill needs for
  * T tokens in chunks of `chunk` (0 on a bad shape or chunk).  The workspace
  * holds the call's status word (int32 at offset 0, padded to 256 bytes) and,
- * for 128-wide heads, one 34,048-byte pre-pass record per (chunk, value
+ * for 128-wide heads, one 50,432-byte pre-pass record per (chunk, value
  * head) and one int32 ready flag per (chunk, key head), padded to 16 bytes:
- * 256 + ceil(T / 64) * (Hv * 34,048 + 4 * Hk) bytes, the flags rounded up to
- * 16 (209 MB at T = 8,192 with 48 value and 16 key heads).
+ * 256 + ceil(T / 64) * (Hv * 50,432 + 4 * Hk) bytes, the flags rounded up to
+ * 16 (310 MB at T = 8,192 with 48 value and 16 key heads).
  */
 size_t gdn_prefill_workspace_bytes(const gdn_shape* shape, int32_t T, int32_t chunk);
 
@@ -326,9 +326,10 @@ size_t gdn_prefill_workspace_bytes(const gdn_shape* shape, int32_t T, int32_t ch
  *              the results are invalid, as for GDN_ERR_TIMEOUT).
  * The chunk form runs for dk = dv = 128 (the 27B layer's heads); narrower
  * heads run the same recurrence token by token on the GPU.  A pre-pass
- * computes every chunk's state-independent part (the inverse
- * T = (I + L)^-1, the masked Q K^T and the per-token decays) into the
- * workspace, and a chain per value head walks the chunks in order.  Where the
+ * computes every chunk's state-independent part into the workspace: with
+ * T = (I + L)^-1, the state-update factor T^T diag(c) K, the output factor
+ * P T (P the masked, decayed Q K^T) and the per-token decays.  A chain per
+ * value head then walks the chunks in order.  Where the
  * GPU can hold one chain CTA per value head plus pre-pass workers at once, both
  * run in one cooperative launch (the chain of chunk c waits, bounded, for its
  * record's ready flag, so later chunks' pre-pass overlaps earlier chunks'

@@ -120,10 +120,12 @@ def test_prefill_then_decode_continues():
 
 
 @pytest.mark.parametrize("T", [64, 300, 1000])
-def test_prefill_prepass_equals_self_contained_bitwise(T):
-    """The pre-pass path (T, P and the per-token scalars computed for all
-    chunks in parallel, then read by the chain) and the self-contained chain
-    (the same chunk-local steps between the MMAs) give the same bits."""
+def test_prefill_prepass_and_self_contained_agree(T):
+    """The pre-pass path (T, the state-update factor T^T diag(c) K and the
+    output factor P T computed for all chunks in parallel, then read by the
+    chain) and the self-contained chain (which forms U = T X between its
+    MMAs) group the same algebra differently, so they round differently:
+    each must meet the oracle bars, and they must agree with each other."""
     import ctypes
     shape = gen.QWEN_27B
     d = gen.decode_inputs(90 + T, shape.with_batch(1), T, tag="prepass")
@@ -139,5 +141,10 @@ def test_prefill_prepass_equals_self_contained_bitwise(T):
                                               gdn.GDN_NORMALIZE_QK, P(torch.cuda.current_stream().cuda_stream))
     assert rc == 0, gdn.last_error()
     torch.cuda.synchronize()
-    assert torch.equal(out_a, out_b)
-    assert torch.equal(st_a, st_b)
+    out_ref, st_ref = oracle.prefill(d["qkv"], d["alpha"], d["beta"], d["state"], shape.Hk, shape.Hv,
+                                     shape.dk, shape.dv)
+    for out, st in ((out_a, st_a), (out_b, st_b)):
+        assert_out_close(host(out), out_ref[0])
+        assert_state_close(host(st), st_ref[0])
+    assert_out_close(host(out_a), host(out_b).astype(np.float64))
+    assert_state_close(host(st_a), host(st_b).astype(np.float64))
