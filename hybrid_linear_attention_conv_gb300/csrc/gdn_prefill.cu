@@ -94,8 +94,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 200000000ull;  // 0.2 s per tensor-core batch
 
 // Kernel parameters.  The two tensor maps describe the packed q/k/v rows
-// [T][C] (bf16) for the chain's TMA loads: 8 x 64 boxes (one 16-byte column
-// of 64 tokens) for K and Q, 128 x 64 boxes for V.
+// [T][C] (bf16) for the chain's TMA loads: 64 x 64 boxes with the 128-byte
+// swizzle (64 columns of 64 tokens) for K and Q, 128 x 64 plain boxes for V.
 struct alignas(64) PrefillParams {
     CUtensorMap tm_kq;
     CUtensorMap tm_v;
@@ -961,9 +961,10 @@ constexpr int kChainThreads = kEpiThreads + 32;  // and one warp that only issue
 constexpr uint32_t kRecStride = (kRecBytes + 1023) / 1024 * 1024;  // a record slot, padded to 1 KB
 
 // Inputs of a chunk are double-buffered by chunk parity and loaded by the
-// copy engine a whole chunk ahead.  [K;Q] is [16 column blocks][128 rows][8]
-// (K rows 0..63, Q rows 64..127): one TMA box per 16-byte column of K or Q,
-// i.e. K-major core matrices 2,048 B apart along K and 128 B apart along rows.
+// copy engine a whole chunk ahead.  [K;Q] is two 16 KB slabs (columns 0..63,
+// 64..127), each 128 rows of 128 B with the 128-byte swizzle (K rows 0..63,
+// then Q rows 64..127): four TMA boxes, read by the MMAs through swizzled
+// K-major descriptors.
 constexpr uint32_t C_OFF_KQ = 0;         // [K;Q] x 2   B of S [K;Q]^T
 constexpr uint32_t C_OFF_V = 65536;      // V     [64 t][128 i] x 2, plain row-major
 constexpr uint32_t C_OFF_REC = 98304;    // two record slots (W^T hi/lo, PT hi/lo, scalars)
@@ -1084,12 +1085,15 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
         const int t0 = cc * kChunk;
         if (lane == 0) mbar_arrive_expect_tx(b, kInputTx);
         __syncwarp();
-        const uint32_t kq = sbase + C_OFF_KQ + (uint32_t)(cc & 1) * kKqBytes;
-        const int kb = lane & 15;
-        const int x = (lane < 16 ? p.Hk * kD : 0) + g * kD + kb * 8;
-        tma_load_2d(kq + (uint32_t)kb * 2048u + (lane < 16 ? 0u : 1024u), &p.tm_kq, x, t0, b);
-        if (lane == 0)
+        // lanes 0..3: K slab 0, Q slab 0, K slab 1, Q slab 1; lane 4: V
+        if (lane < 4) {
+            const uint32_t kq = sbase + C_OFF_KQ + (uint32_t)(cc & 1) * kKqBytes;
+            const int is_q = lane & 1, slab = lane >> 1;
+            const int x = (is_q ? 0 : p.Hk * kD) + g * kD + slab * 64;
+            tma_load_2d(kq + (uint32_t)slab * 16384u + (uint32_t)is_q * 8192u, &p.tm_kq, x, t0, b);
+        } else if (lane == 4) {
             tma_load_2d(sbase + C_OFF_V + (uint32_t)(cc & 1) * kVBytes, &p.tm_v, 2 * p.Hk * kD + h * kD, t0, b);
+        }
     };
     // whether chunk cc's record is published (READY), without waiting
     auto record_ready = [&](int cc) -> bool {
@@ -1126,7 +1130,7 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
     // descriptor units, further on).  The issuing thread shares its SM
     // sub-partition with busy epilogue warps, so its instruction stream must
     // stay short for the tensor pipe to be fed at its own rate.
-    const uint64_t d_kq0 = smem_desc2(sbase + C_OFF_KQ, 2048, 128);  // [K;Q] of buffer 0
+    const uint64_t d_kq0 = smem_desc_sw128(sbase + C_OFF_KQ);  // [K;Q] of buffer 0
     constexpr uint64_t kKqDesc = kKqBytes >> 4;                    // buffer 1 vs buffer 0
     const uint64_t d_rec0 = smem_desc(sbase + C_OFF_REC, kChunk * 16);  // record slot 0, 64-wide K-major tiles
     constexpr uint64_t kRecDesc = kRecStride >> 4;  // slot 1 vs slot 0
@@ -1182,7 +1186,8 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
 #pragma unroll
                 for (int ks = 0; ks < kD / 16; ++ks)
                     mma_bf16_ts(tmem + d_col, tmem + (pass ? s_lo : T_SH) + ks * 8,
-                                d_kq0 + (uint64_t)(c & 1) * kKqDesc + 256 * ks, id, (pass > 0 || ks > 0));
+                                d_kq0 + (uint64_t)(c & 1) * kKqDesc + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2), id,
+                                (pass > 0 || ks > 0));
             mma_commit(bar_ks);
         }
         // the next chunk's [K;Q] and v, into the buffers chunk c - 1 used (its
@@ -1480,19 +1485,19 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
     return fn;
 }
 
-// The chain's tensor maps over the packed rows qkv [T][C] (bf16): 8 x 64
-// boxes for the K and Q columns, 128 x 64 for V.  Returns false if the driver
+// The chain's tensor maps over the packed rows qkv [T][C] (bf16): 64 x 64
+// boxes with the 128-byte swizzle for the K and Q columns, 128 x 64 for V.  Returns false if the driver
 // refuses them.
 bool encode_qkv_maps(PrefillParams& p, const void* qkv, int T, int C) {
     const PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
     if (enc == nullptr) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)T};
     const cuuint64_t strides[1] = {(cuuint64_t)C * 2};
-    const cuuint32_t box_kq[2] = {8, (cuuint32_t)kChunk}, box_v[2] = {(cuuint32_t)kD, (cuuint32_t)kChunk};
+    const cuuint32_t box_kq[2] = {64, (cuuint32_t)kChunk}, box_v[2] = {(cuuint32_t)kD, (cuuint32_t)kChunk};
     const cuuint32_t unit[2] = {1, 1};
     void* base = const_cast<void*>(qkv);
     return enc(&p.tm_kq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box_kq, unit,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
            enc(&p.tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box_v, unit,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,

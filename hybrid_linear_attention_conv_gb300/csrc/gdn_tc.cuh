@@ -37,14 +37,17 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo) {
     return d;
 }
 
-// The same with both offsets given: `lbo` between core matrices adjacent
-// along K, `sbo` between groups of 8 rows.
-__device__ __forceinline__ uint64_t smem_desc2(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// Shared-memory matrix descriptor of a K-major tile stored with the 128-byte
+// swizzle (as a TMA load with that swizzle leaves it): rows of 128 B (64
+// bf16), groups of 8 rows 1,024 B apart, layout type 2 in bits 61..63.  Step
+// k of K = 16 inside a 64-wide slab starts 32 B further on.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
     uint64_t d = 0;
     d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 16;              // leading byte offset (unused with this swizzle)
+    d |= (uint64_t)(1024u >> 4) << 32;   // stride byte offset
     d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
     return d;
 }
 
