@@ -198,7 +198,7 @@ int check_prefill_args(const gdn_shape* shape, int T, int chunk, const void* qkv
                        size_t workspace_bytes, uint32_t flags, bool records) {
     int rc;
     if ((rc = check_shape(shape, true)) != GDN_OK) return rc;
-    if ((rc = check_flags(flags)) != GDN_OK) return rc;
+    if ((rc = check_flags(flags & ~(records ? GDN_PREFILL_TWO_LAUNCH : 0u))) != GDN_OK) return rc;
     if (chunk != 64) return fail(GDN_ERR_INVALID_ARG, "chunk=%d, only 64 is supported", chunk);
     if (T < 0) return fail(GDN_ERR_INVALID_ARG, "T=%d < 0", T);
     if (T == 0) return GDN_OK;  // nothing to do; pointers may be NULL

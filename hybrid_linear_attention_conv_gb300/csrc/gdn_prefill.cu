@@ -1574,7 +1574,7 @@ int launch_prefill(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const
         // over all chunks, then the chain.
         const int resident = fused_capacity(dev);
         const int workers = std::min(resident - shape->Hv, nchunks * shape->Hk);
-        if (workers >= kMinWorkers) {
+        if (workers >= kMinWorkers && (flags & GDN_PREFILL_TWO_LAUNCH) == 0) {
             p.n_workers = workers;
             void* args[] = {&p};
             e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(gdn_prefill_fused_kernel),

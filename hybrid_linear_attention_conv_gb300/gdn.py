@@ -23,6 +23,7 @@ GDN_MAX_TREE_NODES = 64
 GDN_MAX_TREE_SLOTS = 8
 GDN_NORMALIZE_QK = 0x1
 GDN_OUT_BF16 = 0x2
+GDN_PREFILL_TWO_LAUNCH = 0x4
 
 STATUS = {
     0: "GDN_OK",
@@ -382,8 +383,9 @@ def prefill_workspace_bytes(T, Hk, Hv, dk, dv, chunk=64) -> int:
 
 
 def chunk_prefill(qkv, alpha, beta, state, Hk, Hv, dk, dv, out=None, workspace=None, chunk=64,
-                  q_scale=1.0, normalize=True, out_bf16=False) -> torch.Tensor:
-    """qkv bf16 [T,C], alpha/beta fp32 [T,Hv], state fp32 [Hv,dv,dk] (S_0 in, S_T out)."""
+                  q_scale=1.0, normalize=True, out_bf16=False, two_launch=False) -> torch.Tensor:
+    """qkv bf16 [T,C], alpha/beta fp32 [T,Hv], state fp32 [Hv,dv,dk] (S_0 in, S_T out).
+    two_launch: the pre-pass, then the chain, as two launches (GDN_PREFILL_TWO_LAUNCH)."""
     T = qkv.shape[0]
     if out is None:
         out = torch.empty((T, Hv, dv), dtype=torch.bfloat16 if out_bf16 else torch.float32,
@@ -400,7 +402,9 @@ def chunk_prefill(qkv, alpha, beta, state, Hk, Hv, dk, dv, out=None, workspace=N
                                   _dev(out, torch.bfloat16 if out_bf16 else torch.float32, "out",
                                        (T, Hv, dv)),
                                   _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
-                                  float(q_scale), _flags(normalize, out_bf16), _stream())
+                                  float(q_scale),
+                                  _flags(normalize, out_bf16) | (GDN_PREFILL_TWO_LAUNCH if two_launch else 0),
+                                  _stream())
     _check(rc, "gdn_chunk_prefill")
     return out
 

@@ -94,6 +94,10 @@ typedef enum gdn_status {
 /* flags */
 #define GDN_NORMALIZE_QK 0x1u  /* L2-normalise q and k per key head (eps 1e-6) */
 #define GDN_OUT_BF16 0x2u      /* outputs stored as bf16 (RNE) instead of fp32 */
+/* gdn_chunk_prefill only: run the pre-pass over all chunks, then the chain,
+ * as two launches, even where one cooperative launch would fit (the results
+ * are the same bits; for comparisons).  Other entry points refuse it. */
+#define GDN_PREFILL_TWO_LAUNCH 0x4u
 
 /* ABI version of the loaded library (GDN_ABI_VERSION it was built with). */
 int gdn_abi_version(void);

@@ -86,6 +86,10 @@ def test_decode_validation(lib, fn):
     rc = step(ctypes.byref(_sh()), 1, P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, 1.0,
                              0x80, None)
     assert rc == -1
+    # the prefill-only flag is unknown to the other entry points
+    rc = step(ctypes.byref(_sh()), 1, P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, 1.0,
+              gdn.GDN_NORMALIZE_QK | gdn.GDN_PREFILL_TWO_LAUNCH, None)
+    assert rc == -1
 
 
 def test_conv_validation(lib):

@@ -148,3 +148,20 @@ def test_prefill_prepass_and_self_contained_agree(T):
         assert_state_close(host(st), st_ref[0])
     assert_out_close(host(out_a), host(out_b).astype(np.float64))
     assert_state_close(host(st_a), host(st_b).astype(np.float64))
+
+
+@pytest.mark.parametrize("T", [300, 1000])
+def test_prefill_cooperative_equals_two_launch_bitwise(T):
+    """One cooperative launch (pre-pass workers beside the chains) and the
+    pre-pass over all chunks followed by the chain run the same code on the
+    same records: the same bits."""
+    shape = gen.QWEN_27B
+    d = gen.decode_inputs(110 + T, shape.with_batch(1), T, tag="forms")
+    qkv, al, be = bf16(d["qkv"][0]), f32(d["alpha"][0]), f32(d["beta"][0])
+    st_a, st_b = f32(d["state"][0]), f32(d["state"][0])
+    out_a = gdn.chunk_prefill(qkv, al, be, st_a, shape.Hk, shape.Hv, shape.dk, shape.dv)
+    out_b = gdn.chunk_prefill(qkv, al, be, st_b, shape.Hk, shape.Hv, shape.dk, shape.dv, two_launch=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out_a, out_b)
+    assert torch.equal(st_a, st_b)
+
