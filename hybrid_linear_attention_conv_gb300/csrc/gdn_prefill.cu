@@ -126,49 +126,42 @@ struct NamedSync {
     __device__ __forceinline__ void operator()() const { asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(N) : "memory"); }
 };
 
-// One block row BI of the blocked triangular inverse (T zero above its block
-// diagonal, blocks left of BI already final): with W = 16 BI,
-//   R = L[W:W+16][0:W] T[0:W][0:W],   T[W:W+16][0:W] = -T[W:W+16][W:W+16] R.
-// Trip counts are compile-time, so the sums unroll with independent chains.
-template <int BI, class Sync>
-__device__ __forceinline__ void block_row_solve(const float* sL, float* Tf, float* R, int tid, Sync sync) {
-    constexpr int W = 16 * BI;
-    constexpr int PER = 16 * W / kPrefillThreads;  // elements per thread
-    float acc[PER];
+// The blocks of T below its diagonal in column block J (16 J .. 16 J + 15),
+// one 8-column half per warp: for I = J + 1 .. 3 in turn,
+//   R = L[I][J:I] T[J:I][J],   T[I][J] = -T_II R.
+// Lane (column c, row group rg) keeps R[4 rg .. 4 rg + 3][c] in registers and
+// gathers the rest of column c from the lanes of the same column.  L comes
+// transposed (sLT[k][t] = L[t][k]) and T_II transposed (tiit[I][m][r]), so
+// that every shared-memory read of a warp is one contiguous run.
+template <int J>
+__device__ __forceinline__ void solve_column_block(const float* sLT, float* Tf, const float* tiit, int c, int rg,
+                                                   int lane) {
 #pragma unroll
-    for (int k = 0; k < PER; ++k) acc[k] = 0.f;
+    for (int I = J + 1; I < 4; ++I) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int q = 0; q < W; ++q) {
-#pragma unroll
-        for (int k = 0; k < PER; ++k) {
-            const int e = tid + k * kPrefillThreads;
-            const int r = e / W, cj = e % W;
-            acc[k] = __fmaf_rn(sL[(W + r) * kChunk + q], Tf[q * kChunk + cj], acc[k]);
+        for (int k = 16 * J; k < 16 * I; ++k) {
+            const float4 l4 = *reinterpret_cast<const float4*>(sLT + k * kChunk + 16 * I + 4 * rg);
+            const float tv = Tf[k * kChunk + c];
+            acc[0] = __fmaf_rn(l4.x, tv, acc[0]);
+            acc[1] = __fmaf_rn(l4.y, tv, acc[1]);
+            acc[2] = __fmaf_rn(l4.z, tv, acc[2]);
+            acc[3] = __fmaf_rn(l4.w, tv, acc[3]);
         }
-    }
+        float out[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int k = 0; k < PER; ++k) {
-        const int e = tid + k * kPrefillThreads;
-        R[(e / W) * 48 + e % W] = acc[k];
-    }
-    sync();
-#pragma unroll
-    for (int k = 0; k < PER; ++k) acc[k] = 0.f;
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-#pragma unroll
-        for (int k = 0; k < PER; ++k) {
-            const int e = tid + k * kPrefillThreads;
-            const int r = e / W, cj = e % W;
-            acc[k] = __fmaf_rn(Tf[(W + r) * kChunk + W + m], R[m * 48 + cj], acc[k]);
+        for (int m = 0; m < 16; ++m) {
+            const float rm = __shfl_sync(0xffffffffu, acc[m & 3], (m >> 2) * 8 + (lane & 7));
+            const float4 t4 = *reinterpret_cast<const float4*>(tiit + I * 256 + m * 16 + 4 * rg);
+            out[0] = __fmaf_rn(t4.x, rm, out[0]);
+            out[1] = __fmaf_rn(t4.y, rm, out[1]);
+            out[2] = __fmaf_rn(t4.z, rm, out[2]);
+            out[3] = __fmaf_rn(t4.w, rm, out[3]);
         }
-    }
 #pragma unroll
-    for (int k = 0; k < PER; ++k) {
-        const int e = tid + k * kPrefillThreads;
-        Tf[(W + e / W) * kChunk + e % W] = -acc[k];
+        for (int q = 0; q < 4; ++q) Tf[(16 * I + 4 * rg + q) * kChunk + c] = -out[q];
+        __syncwarp();  // the next block row reads this one's column c from the other lanes
     }
-    sync();
 }
 
 // ---------------------------------------------------------------------------
@@ -231,14 +224,14 @@ __device__ __forceinline__ void chunk_scalars(const float* s_lg, const float* s_
     }
 }
 
-// L (strictly lower, fp32 [64][64]) and P (lower with the diagonal, bf16 hi/lo
-// B-operand tiles) from the [K;Q] K^T accumulator: thread i_row holds row
-// i_row of it (K rows 0..63 give L, Q rows 64..127 give P); warpgroup wg takes
-// columns 32 wg .. 32 wg + 31.  P goes to fp32 rows at sP32 when that is
-// given, else to the bf16 hi/lo tiles.
+// L (strictly lower, fp32, stored transposed: sLT[s][t] = L[t][s]) and P
+// (lower with the diagonal, bf16 hi/lo tiles [t][s], K-major) from the
+// [K;Q] K^T accumulator: thread i_row holds row i_row of it (K rows 0..63 give
+// L, Q rows 64..127 give P); warpgroup wg takes columns 32 wg .. 32 wg + 31.
+// The transposed L makes a warp's stores (consecutive t) one contiguous run.
 __device__ __forceinline__ void form_l_p(uint32_t g_cols, int i_row, int wg, const float* s_lg, const float* s_brk,
-                                         const float* s_rq, const float* s_rk, float* sL, uint8_t* p_hi,
-                                         uint8_t* p_lo, float* sP32 = nullptr) {
+                                         const float* s_rq, const float* s_rk, float* sLT, uint8_t* p_hi,
+                                         uint8_t* p_lo) {
     const int t = i_row & 63;
     const bool krow = i_row < 64;
     const float lg_t = s_lg[t];
@@ -256,10 +249,9 @@ __device__ __forceinline__ void form_l_p(uint32_t g_cols, int i_row, int wg, con
             // L: strictly lower (rows of K); P: lower incl. diagonal (rows of Q)
             row[j] = (krow ? sj < t : sj <= t) ? v : 0.f;
         }
-        if (krow || sP32 != nullptr) {
-            float4* dst = reinterpret_cast<float4*>((krow ? sL : sP32) + t * kChunk + s0);
+        if (krow) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = make_float4(row[4 * q], row[4 * q + 1], row[4 * q + 2], row[4 * q + 3]);
+            for (int j = 0; j < 16; ++j) sLT[(s0 + j) * kChunk + t] = row[j];
         } else {
             store_split8(p_hi + core_off(t, s0, kChunk), p_lo + core_off(t, s0, kChunk), row);
             store_split8(p_hi + core_off(t, s0 + 8, kChunk), p_lo + core_off(t, s0 + 8, kChunk), row + 8);
@@ -267,42 +259,60 @@ __device__ __forceinline__ void form_l_p(uint32_t g_cols, int i_row, int wg, con
     }
 }
 
-// T = (I + L)^-1, blocked by 16, into Tf (fp32) and, when t_hi is given, bf16
-// hi/lo B-operand tiles (all kPrefillThreads threads; contains barriers).  R
-// is fp32 scratch.
+// T = (I + L)^-1 (L strictly lower, given transposed), blocked by 16, into Tf
+// (fp32 [64][64], zeros above the diagonal) and, when t_hi is given, bf16
+// hi/lo B-operand tiles [t][s].  tiit is 4 KB of fp32 scratch (the diagonal
+// blocks, transposed).  All kPrefillThreads threads; two barriers.
+//  1. Warp b < 4 inverts diagonal block b, lane = column: forward substitution
+//     in right-looking order (once x_q is final it enters every later row's
+//     sum, each sum still running over q in increasing order).  The other
+//     warps write the zero blocks above the diagonal.
+//  2. Warps 2 J and 2 J + 1 fill the blocks below the diagonal in column
+//     block J (solve_column_block): columns of T never mix, so no barrier
+//     between them.
+static_assert(kPrefillThreads == 256, "solve_t splits its work over exactly eight warps");
 template <class Sync>
-__device__ __forceinline__ void solve_t(const float* sL, float* Tf, float* R, uint8_t* t_hi, uint8_t* t_lo, int tid,
-                                        Sync sync) {
+__device__ __forceinline__ void solve_t(const float* sLT, float* Tf, float* tiit, uint8_t* t_hi, uint8_t* t_lo,
+                                        int tid, Sync sync) {
     const int warp = tid >> 5, lane = tid & 31;
-    // zero T, so every sum below can run over whole 16-blocks
-    {
-        float4* z = reinterpret_cast<float4*>(Tf);
+    if (warp < 4) {
+        if (lane < 16) {
+            const int b = warp * 16, cc = lane;
+            float x[16], acc[16];
 #pragma unroll
-        for (int q = 0; q < kChunk * kChunk / 4 / kPrefillThreads; ++q)
-            z[tid + q * kPrefillThreads] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    sync();
-    // diagonal blocks: warp w < 4 inverts block w column by column (lane = column)
-    if (warp < 4 && lane < 16) {
-        const int b = warp * 16, cc = lane;
-        float x[16];
+            for (int r = 0; r < 16; ++r) acc[r] = 0.f;
 #pragma unroll
-        for (int r = 0; r < 16; ++r) x[r] = (r == cc) ? 1.f : 0.f;
+            for (int q = 0; q < 16; ++q) {
+                x[q] = q == cc ? 1.f : (q > cc ? -acc[q] : 0.f);
 #pragma unroll
-        for (int r = 1; r < 16; ++r) {
-            float acc = 0.f;
+                for (int r = q + 1; r < 16; ++r) acc[r] = __fmaf_rn(sLT[(b + q) * kChunk + b + r], x[q], acc[r]);
+            }
 #pragma unroll
-            for (int q = 0; q < r; ++q) acc = __fmaf_rn(sL[(b + r) * kChunk + b + q], x[q], acc);
-            if (r > cc) x[r] = -acc;
+            for (int r = 0; r < 16; ++r) Tf[(b + r) * kChunk + b + cc] = x[r];
+            float4* dst = reinterpret_cast<float4*>(tiit + warp * 256 + cc * 16);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
         }
+    } else {
+        // the six 16 x 16 blocks (bi, bk) above the diagonal, in the order
+        // (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Tf[(b + r) * kChunk + b + cc] = x[r];
+        for (int k = 0; k < 3; ++k) {
+            const int idx = (tid - 128) + 128 * k;  // 0 .. 383: block, row, float4
+            const int blk = idx >> 6, r = (idx >> 2) & 15, f4 = idx & 3;
+            const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+            const int bk = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+            *reinterpret_cast<float4*>(Tf + (16 * bi + r) * kChunk + 16 * bk + 4 * f4) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
     sync();
-    // block rows 1..3: T[I][:I] = -T_II (L[I][:I] T[:I][:I])
-    block_row_solve<1>(sL, Tf, R, tid, sync);
-    block_row_solve<2>(sL, Tf, R, tid, sync);
-    block_row_solve<3>(sL, Tf, R, tid, sync);
+    if (warp < 6) {
+        const int c = 16 * (warp >> 1) + 8 * (warp & 1) + (lane & 7), rg = lane >> 3;
+        if (warp < 2) solve_column_block<0>(sLT, Tf, tiit, c, rg, lane);
+        else if (warp < 4) solve_column_block<1>(sLT, Tf, tiit, c, rg, lane);
+        else solve_column_block<2>(sLT, Tf, tiit, c, rg, lane);
+    }
+    sync();
     // T -> bf16 hi/lo B-operand tiles (rows t, K = s)
     for (int e = tid; t_hi != nullptr && e < kChunk * 8; e += kPrefillThreads) {
         const int t = e >> 3, s0 = (e & 7) * 8;
@@ -331,23 +341,23 @@ constexpr uint32_t kRecBytes = REC_SCAL + 5 * 64 * 4;
 constexpr uint32_t kRecBase = 256;       // records start after the status word
 
 // Shared memory of one pre-pass pipeline.  Regions whose contents are dead
-// are reused: once [K;Q] K^T and K^T are made, the [K;Q] tile holds P (fp32)
-// and then the P T tiles; once T is solved, L's region holds (diag(c) T)^T.
+// are reused: once [K;Q] K^T and K^T are made, the [K;Q] tile holds P and
+// T^T; once T is solved, L's region holds (diag(c) T)^T.
 constexpr uint32_t Q_OFF_KQ = 0;         // [K;Q] 32 KB (K-major core matrices, 128 rows)
-constexpr uint32_t Q_OFF_P = 0;          // P fp32 16 KB (after [K;Q] is consumed)
-constexpr uint32_t Q_OFF_PT = 16384;     // (P T) hi, lo [64 t][64 s] 2 x 8 KB (copied to the record)
+constexpr uint32_t Q_OFF_P = 0;          // P hi, lo [64 t][64 u] 2 x 8 KB, A of P T (after [K;Q] is consumed)
+constexpr uint32_t Q_OFF_TT = 16384;     // T^T hi, lo [64 s][64 u] 2 x 8 KB, B of P T
 constexpr uint32_t Q_OFF_KT = 32768;     // K^T [128 j][64 t] 16 KB, A of K^T (diag(c) T)
-constexpr uint32_t Q_OFF_L = 49152;      // L fp32 16 KB
+constexpr uint32_t Q_OFF_L = 49152;      // L^T fp32 16 KB
 constexpr uint32_t Q_OFF_CT = 49152;     // (diag(c) T)^T hi, lo [64 s][64 t] 2 x 8 KB (after the solve)
 constexpr uint32_t Q_OFF_TF = 65536;     // T fp32 16 KB
-constexpr uint32_t Q_OFF_R = 81920;      // block-solve scratch 3 KB
-constexpr uint32_t Q_OFF_SCAL = 84992;   // 9 x 64 fp32
+constexpr uint32_t Q_OFF_R = 81920;      // solve scratch 4 KB (the diagonal blocks of T, transposed)
+constexpr uint32_t Q_OFF_SCAL = 86016;   // 9 x 64 fp32
 constexpr uint32_t Q_OFF_AB = Q_OFF_SCAL + 9 * 64 * 4;  // alpha, beta of the group's heads: 2 x 64 x kMaxGroup fp32
 constexpr int kMaxGroup = 8;                             // value heads per key head staged at once
 constexpr uint32_t Q_OFF_MISC = Q_OFF_AB + 2 * 64 * kMaxGroup * 4;  // 2 mbarriers, TMEM base, abort flag
 constexpr uint32_t kPrepSmem = Q_OFF_MISC + 32;
 constexpr uint32_t kPrepStride = (kPrepSmem + 1023) / 1024 * 1024;  // one pipeline's share of a worker CTA
-constexpr uint32_t kPrepTmemCols = 128;  // [K;Q] K^T (64 columns), then W^T (64 columns)
+constexpr uint32_t kPrepTmemCols = 256;  // [K;Q] K^T, W^T and P T (64 columns each)
 
 // One pre-pass item: chunk c of key head g, giving the records of the key
 // head's value heads.  Per value head, from the chunk's own inputs:
@@ -356,9 +366,9 @@ constexpr uint32_t kPrepTmemCols = 128;  // [K;Q] K^T (64 columns), then W^T (64
 //        state-update factor: S_new = gamma_C S + X^T W;
 //   PT = P T (64 x 64), the output factor: O = diag(gamma r_q) Q S^T + PT X.
 // (With U = T X these are the chunk form's U^T diag(c) K and P U, regrouped
-// so that the chain never forms U.)  W^T = K^T (diag(c) T) runs on tcgen05
-// with K exact in bf16 and diag(c) T split hi + lo; P T runs on the CUDA cores
-// in fp32.  Runs on threads 0 .. kPrefillThreads - 1 of the CTA (tid), `sync`
+// so that the chain never forms U.)  Both run on tcgen05: W^T = K^T (diag(c) T)
+// with K exact in bf16 and diag(c) T split hi + lo (two passes), P T with
+// both factors split (three passes: hi hi, hi lo, lo hi).  Runs on threads 0 .. kPrefillThreads - 1 of the CTA (tid), `sync`
 // being a barrier over exactly those threads; `tmem` holds kPrepTmemCols
 // columns; `bars` are two mbarriers whose phases this CTA's MMAs complete in
 // turn (`*phase` counts them).  Returns false (after raising the status word)
@@ -440,8 +450,7 @@ __device__ bool prep_item(const PrefillParams& p, uint8_t* sm, uint32_t tmem, ui
     fence_after_sync();
     bool fine = *abort_flag == 0;
 
-    const float* sL = reinterpret_cast<const float*>(sm + Q_OFF_L);
-    float* sP = reinterpret_cast<float*>(sm + Q_OFF_P);
+    float* sLT = reinterpret_cast<float*>(sm + Q_OFF_L);
     float* Tf = reinterpret_cast<float*>(sm + Q_OFF_TF);
 #pragma unroll 1
     for (int j = 0; fine && j < p.group; ++j) {
@@ -461,19 +470,22 @@ __device__ bool prep_item(const PrefillParams& p, uint8_t* sm, uint32_t tmem, ui
         sync();
         chunk_scalars(s_lg, s_rk, s_rq, s_beta, s_gk, s_gq, s_ck, s_brk, tid);
         sync();
-        form_l_p(trow, i_row, wg, s_lg, s_brk, s_rq, s_rk, reinterpret_cast<float*>(sm + Q_OFF_L), nullptr, nullptr,
-                 sP);
+        form_l_p(trow, i_row, wg, s_lg, s_brk, s_rq, s_rk, sLT, sm + Q_OFF_P, sm + Q_OFF_P + 8192);
         sync();
-        solve_t(sL, Tf, reinterpret_cast<float*>(sm + Q_OFF_R), nullptr, nullptr, tid, sync);
-        sync();
-        // (diag(c) T)^T as the B operand [s][t] of K^T (diag(c) T), hi/lo (a
-        // warp's lanes take consecutive s: conflict-free column reads of T)
+        solve_t(sLT, Tf, reinterpret_cast<float*>(sm + Q_OFF_R), nullptr, nullptr, tid, sync);
+        // (diag(c) T)^T and T^T as the B operands [s][t] of K^T (diag(c) T) and
+        // P T, hi/lo (a warp's lanes take consecutive s: conflict-free column
+        // reads of T)
         for (int e = tid; e < kChunk * 8; e += kPrefillThreads) {
             const int sc = e & 63, tb = (e >> 6) * 8;
-            float v[8];
+            float v[8], w[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) v[q] = __fmul_rn(s_ck[tb + q], Tf[(tb + q) * kChunk + sc]);
+            for (int q = 0; q < 8; ++q) {
+                w[q] = Tf[(tb + q) * kChunk + sc];
+                v[q] = __fmul_rn(s_ck[tb + q], w[q]);
+            }
             store_split8(sm + Q_OFF_CT + core_off(sc, tb, kChunk), sm + Q_OFF_CT + 8192 + core_off(sc, tb, kChunk), v);
+            store_split8(sm + Q_OFF_TT + core_off(sc, tb, kChunk), sm + Q_OFF_TT + 8192 + core_off(sc, tb, kChunk), w);
         }
         fence_async_smem();
         fence_before_sync();
@@ -488,44 +500,23 @@ __device__ bool prep_item(const PrefillParams& p, uint8_t* sm, uint32_t tmem, ui
                     mma_bf16(tmem + 64, smem_desc(sbase + Q_OFF_KT + ks * 256, kChunk * 16),
                              smem_desc(sbase + Q_OFF_CT + (pass ? 8192 : 0) + ks * 256, kChunk * 16),
                              id_w, (pass > 0 || ks > 0));
+            // P T: (P hi, T hi), (P hi, T lo), (P lo, T hi); M = 64, so row t
+            // of the result sits in TMEM lane 32 (t / 16) + t % 16
+            constexpr uint32_t id_pt = idesc_bf16(64, 64);
+#pragma unroll
+            for (int pass = 0; pass < 3; ++pass)
+#pragma unroll
+                for (int ks = 0; ks < kChunk / 16; ++ks)
+                    mma_bf16(tmem + 128, smem_desc(sbase + Q_OFF_P + (pass == 2 ? 8192 : 0) + ks * 256, kChunk * 16),
+                             smem_desc(sbase + Q_OFF_TT + (pass == 1 ? 8192 : 0) + ks * 256, kChunk * 16),
+                             id_pt, (pass > 0 || ks > 0));
             mma_commit(bar_w);
         }
-        // meanwhile P T on the CUDA cores, a 4 x 4 block per thread, summed
-        // over u in order (the terms with u > t or u < s are exact zeros: P
-        // and T are lower triangular), into hi/lo tiles [t][s]
-        {
-            const int tb = (tid >> 4) * 4, sb = (tid & 15) * 4;
-            float acc[4][4];
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) acc[r][q] = 0.f;
-#pragma unroll 2
-            for (int u = 0; u < kChunk; u += 4) {
-                float4 pr[4], tr[4];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) pr[r] = *reinterpret_cast<const float4*>(sP + (tb + r) * kChunk + u);
-#pragma unroll
-                for (int r = 0; r < 4; ++r) tr[r] = *reinterpret_cast<const float4*>(Tf + (u + r) * kChunk + sb);
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const float pv[4] = {pr[r].x, pr[r].y, pr[r].z, pr[r].w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float tv[4] = {tr[k].x, tr[k].y, tr[k].z, tr[k].w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) acc[r][q] = __fmaf_rn(pv[k], tv[q], acc[r][q]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                uint32_t h0, l0, h1, l1;
-                split_pair(acc[r][0], acc[r][1], h0, l0);
-                split_pair(acc[r][2], acc[r][3], h1, l1);
-                *reinterpret_cast<uint2*>(sm + Q_OFF_PT + core_off(tb + r, sb, kChunk)) = make_uint2(h0, h1);
-                *reinterpret_cast<uint2*>(sm + Q_OFF_PT + 8192 + core_off(tb + r, sb, kChunk)) = make_uint2(l0, l1);
-            }
+        uint8_t* rec = reinterpret_cast<uint8_t*>(p.status) + kRecBase + ((size_t)c * p.Hv + h) * kRecBytes;
+        // meanwhile the per-token scalars
+        if (tid < 5 * 16) {
+            const float* src[5] = {s_beta, s_lg, s_gk, s_gq, s_ck};
+            reinterpret_cast<uint4*>(rec + REC_SCAL)[tid] = reinterpret_cast<const uint4*>(src[tid >> 4])[tid & 15];
         }
         wait_mma(bar_w, phase[1]++);
         sync();
@@ -534,9 +525,9 @@ __device__ bool prep_item(const PrefillParams& p, uint8_t* sm, uint32_t tmem, ui
             fine = false;
             break;
         }
-        // the record of (chunk c, value head h): W^T from TMEM (lane j, this
-        // warpgroup's 32 columns s) as hi/lo tiles, P T and the scalars
-        uint8_t* rec = reinterpret_cast<uint8_t*>(p.status) + kRecBase + ((size_t)c * p.Hv + h) * kRecBytes;
+        // the record of (chunk c, value head h): W^T (lane j, this warpgroup's
+        // 32 columns s) and P T (lanes 0..15 of each warp: row t, this
+        // warpgroup's 32 columns s) from TMEM as hi/lo tiles
         {
             float w[2][16];
             tmem_ld16(trow + 64 + wg * 32, w[0]);
@@ -549,12 +540,20 @@ __device__ bool prep_item(const PrefillParams& p, uint8_t* sm, uint32_t tmem, ui
                     store_split8(rec + REC_W_HI + core_off(i_row, sc, kChunk), rec + REC_W_LO + core_off(i_row, sc, kChunk),
                                  w[hh] + q * 8);
                 }
-        }
-        for (int v = tid; v < 16384 / 16; v += kPrefillThreads)
-            reinterpret_cast<uint4*>(rec + REC_PT_HI)[v] = reinterpret_cast<const uint4*>(sm + Q_OFF_PT)[v];
-        if (tid < 5 * 16) {
-            const float* src[5] = {s_beta, s_lg, s_gk, s_gq, s_ck};
-            reinterpret_cast<uint4*>(rec + REC_SCAL)[tid] = reinterpret_cast<const uint4*>(src[tid >> 4])[tid & 15];
+            float pt[2][16];
+            tmem_ld16(trow + 128 + wg * 32, pt[0]);
+            tmem_ld16(trow + 128 + wg * 32 + 16, pt[1]);
+            if (lane < 16) {
+                const int t = 16 * (warp & 3) + lane;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const int sc = wg * 32 + hh * 16 + q * 8;
+                        store_split8(rec + REC_PT_HI + core_off(t, sc, kChunk), rec + REC_PT_LO + core_off(t, sc, kChunk),
+                                     pt[hh] + q * 8);
+                    }
+            }
         }
         fence_before_sync();
         sync();  // every thread is past this head's TMEM reads and tiles
