@@ -368,8 +368,9 @@ constexpr uint32_t kPrepTmemCols = 256;  // [K;Q] K^T, W^T and P T (64 columns e
 // (With U = T X these are the chunk form's U^T diag(c) K and P U, regrouped
 // so that the chain never forms U.)  Both run on tcgen05: W^T = K^T (diag(c) T)
 // with K exact in bf16 and diag(c) T split hi + lo (two passes), P T with
-// both factors split (three passes: hi hi, hi lo, lo hi).  Runs on threads 0 .. kPrefillThreads - 1 of the CTA (tid), `sync`
-// being a barrier over exactly those threads; `tmem` holds kPrepTmemCols
+// both factors split (three passes: hi hi, hi lo, lo hi).  Runs on threads
+// 0 .. kPrefillThreads - 1 of the CTA (tid), `sync` being a barrier over
+// exactly those threads; `tmem` holds kPrepTmemCols
 // columns; `bars` are two mbarriers whose phases this CTA's MMAs complete in
 // turn (`*phase` counts them).  Returns false (after raising the status word)
 // when a tensor-core wait timed out.
@@ -956,7 +957,8 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
 // memory, so that chunk c's outputs are read out while chunk c + 1 runs.
 // ---------------------------------------------------------------------------
 constexpr int kEpiThreads = 512;    // four epilogue warpgroups over the 128 TMEM lanes
-constexpr int kChainThreads = kEpiThreads + 32;  // and one warp that only issues the MMAs
+constexpr int kLoopThreads = kEpiThreads + 32;   // and one warp that only issues the MMAs
+constexpr int kChainThreads = kLoopThreads + 32;  // and one warp that only requests the inputs
 constexpr uint32_t kRecStride = (kRecBytes + 1023) / 1024 * 1024;  // a record slot, padded to 1 KB
 
 // Inputs of a chunk are double-buffered by chunk parity and loaded by the
@@ -1013,21 +1015,30 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
     const int warp = tid >> 5;
     const bool issuer = tid == kEpiThreads;    // lane 0 of the MMA warp
     const bool epi = tid < kEpiThreads;        // an epilogue thread
+    const bool copier = tid >= kLoopThreads;   // the copy warp
     const int g = h / p.group;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C_OFF_MISC);  // 8 mbarriers
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C_OFF_MISC);  // 10 mbarriers
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C_OFF_MISC + 96);
+    // raised by the threads of the chunk loop before the barrier that closes
+    // a chunk, so that they all leave the loop together
     int* abort_flag = reinterpret_cast<int*>(sm + C_OFF_MISC + 100);
+    int* copy_fail = reinterpret_cast<int*>(sm + C_OFF_MISC + 104);  // the copy warp gave up
+    const NamedSync<1, kLoopThreads> loop_sync;  // the epilogue and MMA warps
     const uint32_t sbase = smem_u32(sm);
     const uint32_t bar_ks = smem_u32(bars + 0);    // S [K;Q]^T
+    const uint32_t bar_x = smem_u32(bars + 1);     // every epilogue warp has written its part of X^T
+    const uint32_t bar_qs = smem_u32(bars + 2);    // every epilogue warp has scaled its part of S Q^T
     const uint32_t bar_s = smem_u32(bars + 3);     // state update X^T W
     const uint32_t bar_o = smem_u32(bars + 4);     // outputs X^T PT^T
     const uint32_t bar_fin = smem_u32(bars + 5);   // every MMA issued, before TMEM is freed
     const uint32_t bar_in0 = smem_u32(bars + 6);   // a chunk's inputs landed in buffer 0 (bar_in0 + 8: buffer 1)
+    const uint32_t bar_free0 = smem_u32(bars + 8);  // buffer 0's chunk is done with it (bar_free0 + 8: buffer 1)
 
     if (warp == 0) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     if (tid == 0) {
-        for (int b = 0; b < 8; ++b) mbar_init(smem_u32(bars + b), 1);
+        for (int b = 0; b < 10; ++b) mbar_init(smem_u32(bars + b), (b == 1 || b == 2) ? kEpiThreads / 32 : 1);
         *abort_flag = 0;
+        *copy_fail = 0;
     }
     fence_before_sync();
     __syncthreads();
@@ -1071,17 +1082,26 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
 
     const int nchunks = (p.T + kChunk - 1) / kChunk;
     const int lane = tid & 31;
-    // The MMA warp loads chunk cc's inputs into buffer cc & 1 with the copy
-    // engine: 32 TMA boxes for [K;Q] (lane l: K column block l, or Q column
-    // block l - 16), one for V and one bulk copy of the record, all counted
-    // on that buffer's barrier.  Rows past the end of the prompt read as zeros.
-    // (The barrier expects all of a chunk's bytes when [K;Q] and V are
-    // requested; the record follows later, once its flag is set.)
-    int in_last = -1;  // MMA warp: the last chunk whose inputs it requested
-    auto issue_kqv = [&](int cc) {
-        in_last = cc;
+    // The copy warp loads chunk cc's inputs into buffer cc & 1 with the copy
+    // engine: four TMA boxes for [K;Q], one for V and one bulk copy of the
+    // record, all counted on that buffer's barrier.  Rows past the end of the
+    // prompt read as zeros.  (The barrier expects all of a chunk's bytes when
+    // [K;Q] and V are requested; the record follows once its flag is set.)
+    // Chunk cc's inputs, requested by the copy warp once chunk cc - 2, the
+    // previous user of buffer cc & 1, is done with it (its output MMAs, the
+    // last readers, committed that buffer's free barrier).  False when a wait
+    // gave up.
+    int in_last = -1;  // copy warp: the last chunk whose inputs it requested
+    auto issue_inputs = [&](int cc) -> bool {
         const uint32_t b = bar_in0 + 8u * (uint32_t)(cc & 1);
         const int t0 = cc * kChunk;
+        if (cc >= 2) {
+            int ok = 1;
+            if (lane == 0)
+                ok = mbar_wait(bar_free0 + 8u * (uint32_t)(cc & 1), (uint32_t)((cc - 2) >> 1) & 1u, kWaitLimitNs);
+            if (__shfl_sync(0xffffffffu, ok, 0) == 0) return false;
+        }
+        in_last = cc;
         if (lane == 0) mbar_arrive_expect_tx(b, kInputTx);
         __syncwarp();
         // lanes 0..3: K slab 0, Q slab 0, K slab 1, Q slab 1; lane 4: V
@@ -1093,28 +1113,18 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
         } else if (lane == 4) {
             tma_load_2d(sbase + C_OFF_V + (uint32_t)(cc & 1) * kVBytes, &p.tm_v, 2 * p.Hk * kD + h * kD, t0, b);
         }
-    };
-    // whether chunk cc's record is published (READY), without waiting
-    auto record_ready = [&](int cc) -> bool {
-        if (!READY) return true;
-        int v = 0;
-        if (lane == 0) asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p.ready + cc * p.Hk + g) : "memory");
-        return __shfl_sync(0xffffffffu, v, 0) != 0;
-    };
-    bool rec_pending = false;  // MMA warp: the next chunk's record is still to be requested
-    auto issue_record = [&](int cc) {
+        // the record, once its flag is set
+        int ok = 1;
         if (lane == 0) {
-            if (READY && !wait_ready(p.ready, cc * p.Hk + g)) atomicOr(abort_flag, 1);
-            fence_proxy_async_global();
-            const uint8_t* rec =
-                reinterpret_cast<const uint8_t*>(p.status) + kRecBase + ((size_t)cc * p.Hv + h) * kRecBytes;
-            bulk_g2s(sbase + C_OFF_REC + (uint32_t)(cc & 1) * kRecStride, rec, kRecBytes,
-                     bar_in0 + 8u * (uint32_t)(cc & 1));
+            ok = !READY || wait_ready(p.ready, cc * p.Hk + g);
+            if (ok) {
+                fence_proxy_async_global();
+                const uint8_t* rec =
+                    reinterpret_cast<const uint8_t*>(p.status) + kRecBase + ((size_t)cc * p.Hv + h) * kRecBytes;
+                bulk_g2s(sbase + C_OFF_REC + (uint32_t)(cc & 1) * kRecStride, rec, kRecBytes, b);
+            }
         }
-    };
-    auto issue_inputs = [&](int cc) {
-        issue_kqv(cc);
-        issue_record(cc);
+        return __shfl_sync(0xffffffffu, ok, 0) != 0;
     };
     // every thread that reads a buffer waits for its phase (chunk cc is the
     // (cc >> 1)-th use of buffer cc & 1)
@@ -1122,7 +1132,6 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
         if (!mbar_wait(bar_in0 + 8u * (uint32_t)(cc & 1), (uint32_t)(cc >> 1) & 1u, kWaitLimitNs))
             atomicOr(abort_flag, 1);
     };
-    if (!epi) issue_inputs(0);
 
     // Operand descriptors, computed once: an MMA issue is then a 64-bit add
     // and the instruction (step ks of a K-major tile starts 256 B, i.e. 16
@@ -1160,174 +1169,188 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
         }
     };
 
+    if (copier) {
+        // runs up to a chunk ahead of the chain, bounded by the two buffers
 #pragma unroll 1
-    for (int c = 0; c < nchunks; ++c) {
-        const uint32_t d_col = T_D + (uint32_t)(c & 1) * 128;  // S K^T here, O^T at + 64
-        const uint32_t s_lo = T_D + (uint32_t)((c + 1) & 1) * 128;  // this chunk's S lo operand
-        const uint8_t* rec = sm + C_OFF_REC + (uint32_t)(c & 1) * kRecStride;
-        const float* s_beta = reinterpret_cast<const float*>(rec + REC_SCAL);  // beta_t
-        const float* s_lg = s_beta + 64;   // log2 gamma_t
-        const float* s_gk = s_beta + 128;  // gamma_t r_k,t
-        const float* s_gq = s_beta + 192;  // gamma_t q_scale r_q,t
-        const uint64_t d_rec = d_rec0 + (uint64_t)(c & 1) * kRecDesc;
-
-        // ---- A: chunk c's inputs have landed
-        if (epi) wait_inputs(c);
-        fence_before_sync();
-        __syncthreads();
-
-        // ---- B: S [K;Q]^T (S hi, S lo from tensor memory) into this chunk's buffer
-        if (issuer) {
-            fence_after_sync();
-            constexpr uint32_t id = idesc_bf16(128, 128);
-#pragma unroll
-            for (int pass = 0; pass < 2; ++pass)
-#pragma unroll
-                for (int ks = 0; ks < kD / 16; ++ks)
-                    mma_bf16_ts(tmem + d_col, tmem + (pass ? s_lo : T_SH) + ks * 8,
-                                d_kq0 + (uint64_t)(c & 1) * kKqDesc + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2), id,
-                                (pass > 0 || ks > 0));
-            mma_commit(bar_ks);
-        }
-        // the next chunk's [K;Q] and v, into the buffers chunk c - 1 used (its
-        // record's PT tile is read by chunk c - 1's output MMA: wait for that
-        // first, since the record follows into that slot)
-        if (!epi && c + 1 < nchunks) {
-            if (c > 0 && lane == 0 && !mbar_wait(bar_o, (uint32_t)(c - 1) & 1u, kWaitLimitNs)) atomicOr(abort_flag, 1);
-            issue_kqv(c + 1);
-            // the record too if it is already published; else after this chunk's MMAs
-            rec_pending = !record_ready(c + 1);
-            if (!rec_pending) issue_record(c + 1);
-        }
-        if (epi) {
-            // in the shadow of S [K;Q]^T: S <- gamma_C S
-            {
-                const float gamma_c = exp2f(s_lg[kChunk - 1]);
-                const float2 g2 = make_float2(gamma_c, gamma_c);
-#pragma unroll 1
-                for (int cc = c0; cc < c0 + CS; cc += 16) {
-                    float sv[16];
-                    tmem_ld16(trow + T_S + cc, sv);
-#pragma unroll
-                    for (int j = 0; j < 16; j += 2) {
-                        const float2 r = __fmul2_rn(make_float2(sv[j], sv[j + 1]), g2);
-                        sv[j] = r.x;
-                        sv[j + 1] = r.y;
-                    }
-                    tmem_st16(trow + T_S + cc, sv);
-                }
-            }
-            wait_mma(bar_ks, c);
-
-            // ---- C: X^T[i][s] = beta_s (v_s[i] - gamma_s r_k,s (S k_s)[i]) as the A operand
-            // of both X^T W and X^T PT^T; S Q^T scaled by gamma_t q_scale r_q,t (the start of O^T)
-            {
-                const uint16_t* vcol = reinterpret_cast<const uint16_t*>(sm + C_OFF_V + (uint32_t)(c & 1) * kVBytes) + i;
-                float ks[16], x[16];
-                tmem_ld16(trow + d_col + s0, ks);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 b4 = reinterpret_cast<const float4*>(s_beta + s0)[q];
-                    const float4 g4 = reinterpret_cast<const float4*>(s_gk + s0)[q];
-                    const int sj = s0 + 4 * q;
-                    const float2 lo = __fmul2_rn(make_float2(b4.x, b4.y),
-                                                 __ffma2_rn(make_float2(-g4.x, -g4.y), make_float2(ks[4 * q], ks[4 * q + 1]),
-                                                            make_float2(bf16_to_f(vcol[sj * kD]), bf16_to_f(vcol[(sj + 1) * kD]))));
-                    const float2 hi = __fmul2_rn(make_float2(b4.z, b4.w),
-                                                 __ffma2_rn(make_float2(-g4.z, -g4.w), make_float2(ks[4 * q + 2], ks[4 * q + 3]),
-                                                            make_float2(bf16_to_f(vcol[(sj + 2) * kD]), bf16_to_f(vcol[(sj + 3) * kD]))));
-                    x[4 * q] = lo.x;
-                    x[4 * q + 1] = lo.y;
-                    x[4 * q + 2] = hi.x;
-                    x[4 * q + 3] = hi.y;
-                }
-                uint32_t hi[8], lo[8];
-                split_pack16(x, hi, lo);
-                tmem_st8(trow + T_XA + s0 / 2, hi);
-                tmem_st8(trow + T_XA + 32 + s0 / 2, lo);
-                float qs[16];
-                tmem_ld16(trow + d_col + 64 + s0, qs);
-                mul16(qs, s_gq + s0);
-                tmem_st16(trow + d_col + 64 + s0, qs);
-                tmem_wait_st();  // also covers the S rescale above
+        for (int cc = 0; cc < nchunks; ++cc) {
+            if (*reinterpret_cast<volatile int*>(abort_flag) != 0) break;
+            if (!issue_inputs(cc)) {
+                if (lane == 0) *copy_fail = 1;
+                break;
             }
         }
-        fence_before_sync();
-        __syncthreads();
-
-        // ---- G: S += X^T W (3 passes); then O^T += X^T PT^T (3 passes)
-        if (issuer) {
-            fence_after_sync();
-            constexpr uint32_t id_s = idesc_bf16(128, 128);
-            constexpr uint32_t id_o = idesc_bf16(128, 64);
-#pragma unroll
-            for (int pass = 0; pass < 3; ++pass)  // (X hi, W hi), (X hi, W lo), (X lo, W hi)
-#pragma unroll
-                for (int ks = 0; ks < kChunk / 16; ++ks)
-                    mma_bf16_ts(tmem + T_S, tmem + T_XA + (pass == 2 ? 32 : 0) + ks * 8,
-                                d_rec + (pass == 1 ? kWLo : kWHi) + 16 * ks, id_s, 1u);
-            mma_commit(bar_s);
-#pragma unroll
-            for (int pass = 0; pass < 3; ++pass)  // (X hi, PT hi), (X hi, PT lo), (X lo, PT hi)
-#pragma unroll
-                for (int ks = 0; ks < kChunk / 16; ++ks)
-                    mma_bf16_ts(tmem + d_col + 64, tmem + T_XA + (pass == 2 ? 32 : 0) + ks * 8,
-                                d_rec + (pass == 1 ? kPtLo : kPtHi) + 16 * ks, id_o, 1u);
-            mma_commit(bar_o);
-        }
-        // the next chunk's record, if it was not published in time above
-        if (!epi && rec_pending) {
-            issue_record(c + 1);
-            rec_pending = false;
-        }
-        if (epi) {
-            // in the shadow of the state update: the previous chunk's outputs
-            if (c > 0) {
-                wait_mma(bar_o, c - 1);
-                store_outputs(c - 1);
-            }
-            wait_mma(bar_s, c);
-
-            // ---- H: the next chunk's S operand (hi into T_SH; lo into this
-            // chunk's consumed S K^T half), or the final state
-            const bool last = (c == nchunks - 1);
-            float sv[2][16];
-            tmem_ld16(trow + T_S + c0, sv[0]);
-            tmem_ld16(trow + T_S + c0 + 16, sv[1]);
-            if (last) {
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        *reinterpret_cast<float4*>(srow + c0 + 16 * hh + 4 * q) =
-                            make_float4(sv[hh][4 * q], sv[hh][4 * q + 1], sv[hh][4 * q + 2], sv[hh][4 * q + 3]);
-            } else {
-                uint32_t hi[2][8], lo[2][8];
-                split_pack16(sv[0], hi[0], lo[0]);
-                split_pack16(sv[1], hi[1], lo[1]);
-                tmem_st8(trow + T_SH + c0 / 2, hi[0]);
-                tmem_st8(trow + T_SH + c0 / 2 + 8, hi[1]);
-                tmem_st8(trow + d_col + c0 / 2, lo[0]);
-                tmem_st8(trow + d_col + c0 / 2 + 8, lo[1]);
-                tmem_wait_st();
-            }
-        }
-        fence_before_sync();
-        __syncthreads();
-        if (*abort_flag != 0) break;
-    }
-
-    if (epi && *abort_flag == 0 && nchunks > 0) {
-        wait_mma(bar_o, nchunks - 1);
-        store_outputs(nchunks - 1);
-    }
-    if (!epi && lane == 0) {
         // no copy may still be writing shared memory at exit: wait for the
-        // last requested phase of each input buffer (a completed one returns
-        // at once)
-        for (int cc = in_last; cc >= 0 && cc > in_last - 2; --cc) {
-            if (!mbar_wait(bar_in0 + 8u * (uint32_t)(cc & 1), (uint32_t)(cc >> 1) & 1u, kWaitLimitNs))
-                atomicOr(abort_flag, 1);
+        // last requested phase of each input buffer
+        if (lane == 0)
+            for (int cc = in_last; cc >= 0 && cc > in_last - 2; --cc)
+                if (!mbar_wait(bar_in0 + 8u * (uint32_t)(cc & 1), (uint32_t)(cc >> 1) & 1u, kWaitLimitNs))
+                    *copy_fail = 1;
+    } else {
+        // the first chunk's MMAs read the operands of the prologue (later chunks'
+        // are ordered by the barrier that closes each chunk)
+        fence_before_sync();
+        loop_sync();
+#pragma unroll 1
+        for (int c = 0; c < nchunks; ++c) {
+            const uint32_t d_col = T_D + (uint32_t)(c & 1) * 128;  // S K^T here, O^T at + 64
+            const uint32_t s_lo = T_D + (uint32_t)((c + 1) & 1) * 128;  // this chunk's S lo operand
+            const uint8_t* rec = sm + C_OFF_REC + (uint32_t)(c & 1) * kRecStride;
+            const float* s_beta = reinterpret_cast<const float*>(rec + REC_SCAL);  // beta_t
+            const float* s_lg = s_beta + 64;   // log2 gamma_t
+            const float* s_gk = s_beta + 128;  // gamma_t r_k,t
+            const float* s_gq = s_beta + 192;  // gamma_t q_scale r_q,t
+            const uint64_t d_rec = d_rec0 + (uint64_t)(c & 1) * kRecDesc;
+
+            // ---- A: chunk c's inputs have landed (each thread that reads them
+            // waits on the barrier itself; the S operand is in place since the
+            // barrier that closed the previous chunk)
+            if (epi || issuer) wait_inputs(c);
+
+            // ---- B: S [K;Q]^T (S hi, S lo from tensor memory) into this chunk's buffer
+            if (issuer) {
+                fence_after_sync();
+                constexpr uint32_t id = idesc_bf16(128, 128);
+#pragma unroll
+                for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+                    for (int ks = 0; ks < kD / 16; ++ks)
+                        mma_bf16_ts(tmem + d_col, tmem + (pass ? s_lo : T_SH) + ks * 8,
+                                    d_kq0 + (uint64_t)(c & 1) * kKqDesc + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2), id,
+                                    (pass > 0 || ks > 0));
+                mma_commit(bar_ks);
+            }
+            if (epi) {
+                // in the shadow of S [K;Q]^T: S <- gamma_C S
+                {
+                    const float gamma_c = exp2f(s_lg[kChunk - 1]);
+                    const float2 g2 = make_float2(gamma_c, gamma_c);
+#pragma unroll 1
+                    for (int cc = c0; cc < c0 + CS; cc += 16) {
+                        float sv[16];
+                        tmem_ld16(trow + T_S + cc, sv);
+#pragma unroll
+                        for (int j = 0; j < 16; j += 2) {
+                            const float2 r = __fmul2_rn(make_float2(sv[j], sv[j + 1]), g2);
+                            sv[j] = r.x;
+                            sv[j + 1] = r.y;
+                        }
+                        tmem_st16(trow + T_S + cc, sv);
+                    }
+                }
+                wait_mma(bar_ks, c);
+
+                // ---- C: X^T[i][s] = beta_s (v_s[i] - gamma_s r_k,s (S k_s)[i]) as the A operand
+                // of both X^T W and X^T PT^T
+                {
+                    const uint16_t* vcol =
+                        reinterpret_cast<const uint16_t*>(sm + C_OFF_V + (uint32_t)(c & 1) * kVBytes) + i;
+                    float ks[16], x[16];
+                    tmem_ld16(trow + d_col + s0, ks);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 b4 = reinterpret_cast<const float4*>(s_beta + s0)[q];
+                        const float4 g4 = reinterpret_cast<const float4*>(s_gk + s0)[q];
+                        const int sj = s0 + 4 * q;
+                        const float2 v01 = make_float2(bf16_to_f(vcol[sj * kD]), bf16_to_f(vcol[(sj + 1) * kD]));
+                        const float2 v23 = make_float2(bf16_to_f(vcol[(sj + 2) * kD]), bf16_to_f(vcol[(sj + 3) * kD]));
+                        const float2 lo = __fmul2_rn(make_float2(b4.x, b4.y),
+                                                     __ffma2_rn(make_float2(-g4.x, -g4.y),
+                                                                make_float2(ks[4 * q], ks[4 * q + 1]), v01));
+                        const float2 hi = __fmul2_rn(make_float2(b4.z, b4.w),
+                                                     __ffma2_rn(make_float2(-g4.z, -g4.w),
+                                                                make_float2(ks[4 * q + 2], ks[4 * q + 3]), v23));
+                        x[4 * q] = lo.x;
+                        x[4 * q + 1] = lo.y;
+                        x[4 * q + 2] = hi.x;
+                        x[4 * q + 3] = hi.y;
+                    }
+                    uint32_t hi[8], lo[8];
+                    split_pack16(x, hi, lo);
+                    tmem_st8(trow + T_XA + s0 / 2, hi);
+                    tmem_st8(trow + T_XA + 32 + s0 / 2, lo);
+                    tmem_wait_st();  // also covers the S rescale above
+                }
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_x);
+            }
+
+            // ---- G: S += X^T W (3 passes); then O^T += X^T PT^T (3 passes)
+            if (issuer) {
+                if (!mbar_wait(bar_x, (uint32_t)c & 1u, kWaitLimitNs)) atomicOr(abort_flag, 1);
+                fence_after_sync();
+                constexpr uint32_t id_s = idesc_bf16(128, 128);
+                constexpr uint32_t id_o = idesc_bf16(128, 64);
+#pragma unroll
+                for (int pass = 0; pass < 3; ++pass)  // (X hi, W hi), (X hi, W lo), (X lo, W hi)
+#pragma unroll
+                    for (int ks = 0; ks < kChunk / 16; ++ks)
+                        mma_bf16_ts(tmem + T_S, tmem + T_XA + (pass == 2 ? 32 : 0) + ks * 8,
+                                    d_rec + (pass == 1 ? kWLo : kWHi) + 16 * ks, id_s, 1u);
+                mma_commit(bar_s);
+                // the output MMAs accumulate onto S Q^T once every epilogue warp has scaled its part
+                if (!mbar_wait(bar_qs, (uint32_t)c & 1u, kWaitLimitNs)) atomicOr(abort_flag, 1);
+                fence_after_sync();
+#pragma unroll
+                for (int pass = 0; pass < 3; ++pass)  // (X hi, PT hi), (X hi, PT lo), (X lo, PT hi)
+#pragma unroll
+                    for (int ks = 0; ks < kChunk / 16; ++ks)
+                        mma_bf16_ts(tmem + d_col + 64, tmem + T_XA + (pass == 2 ? 32 : 0) + ks * 8,
+                                    d_rec + (pass == 1 ? kPtLo : kPtHi) + 16 * ks, id_o, 1u);
+                mma_commit(bar_o);
+                mma_commit(bar_free0 + 8u * (uint32_t)(c & 1));  // the last readers of this chunk's buffers
+            }
+            if (epi) {
+                // in the shadow of the state update: S Q^T scaled by gamma_t q_scale r_q,t
+                // (the start of O^T), then the previous chunk's outputs
+                {
+                    float qs[16];
+                    tmem_ld16(trow + d_col + 64 + s0, qs);
+                    mul16(qs, s_gq + s0);
+                    tmem_st16(trow + d_col + 64 + s0, qs);
+                    tmem_wait_st();
+                }
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_qs);
+                if (c > 0) {
+                    wait_mma(bar_o, c - 1);
+                    store_outputs(c - 1);
+                }
+                wait_mma(bar_s, c);
+
+                // ---- H: the next chunk's S operand (hi into T_SH; lo into this
+                // chunk's consumed S K^T half), or the final state
+                const bool last = (c == nchunks - 1);
+                float sv[2][16];
+                tmem_ld16(trow + T_S + c0, sv[0]);
+                tmem_ld16(trow + T_S + c0 + 16, sv[1]);
+                if (last) {
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            *reinterpret_cast<float4*>(srow + c0 + 16 * hh + 4 * q) =
+                                make_float4(sv[hh][4 * q], sv[hh][4 * q + 1], sv[hh][4 * q + 2], sv[hh][4 * q + 3]);
+                } else {
+                    uint32_t hi[2][8], lo[2][8];
+                    split_pack16(sv[0], hi[0], lo[0]);
+                    split_pack16(sv[1], hi[1], lo[1]);
+                    tmem_st8(trow + T_SH + c0 / 2, hi[0]);
+                    tmem_st8(trow + T_SH + c0 / 2 + 8, hi[1]);
+                    tmem_st8(trow + d_col + c0 / 2, lo[0]);
+                    tmem_st8(trow + d_col + c0 / 2 + 8, lo[1]);
+                    tmem_wait_st();
+                }
+            }
+            fence_before_sync();
+            loop_sync();
+            if (*abort_flag != 0) break;
+        }
+
+        if (epi && *abort_flag == 0 && nchunks > 0) {
+            wait_mma(bar_o, nchunks - 1);
+            store_outputs(nchunks - 1);
         }
     }
     // every MMA this CTA issued has completed before TMEM is released
@@ -1341,7 +1364,7 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    if (*abort_flag != 0 && tid == 0) atomicExch(p.status, 1);
+    if ((*abort_flag != 0 || *copy_fail != 0) && tid == 0) atomicExch(p.status, 1);
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 

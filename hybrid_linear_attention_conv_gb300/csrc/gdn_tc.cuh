@@ -222,6 +222,11 @@ __device__ __forceinline__ void mul16(float (&x)[16], const float* f) {
 
 // Arrive once on `bar` and announce `bytes` of copy-engine data that will
 // complete on it (the phase completes when both have happened).
+// One arrival on an mbarrier (release at CTA scope).
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
