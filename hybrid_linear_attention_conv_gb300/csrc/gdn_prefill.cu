@@ -105,7 +105,7 @@ struct alignas(64) PrefillParams {
     float* state;
     void* out;
     int* status;
-    int* ready;         // per (chunk, key head): 1 once the pre-pass record is written (cooperative form)
+    int* ready;         // per (chunk, value head): 1 once the pre-pass record is written (cooperative form)
     int n_workers;      // pre-pass worker CTAs of the cooperative form
     int T, Hk, Hv, C, group;
     float q_scale;
@@ -376,7 +376,7 @@ constexpr uint32_t kPrepTmemCols = 256;  // [K;Q] K^T, W^T and P T (64 columns e
 // when a tensor-core wait timed out.
 template <class Sync>
 __device__ bool prep_item(const PrefillParams& p, uint8_t* sm, uint32_t tmem, uint32_t bars, uint32_t* phase, int c,
-                          int g, int tid, Sync sync) {
+                          int g, int j0, int j1, bool publish, int tid, Sync sync) {
     const int warp = tid >> 5, lane = tid & 31;
     float* s_alpha = reinterpret_cast<float*>(sm + Q_OFF_SCAL);
     float* s_beta = s_alpha + 64;
@@ -454,7 +454,7 @@ __device__ bool prep_item(const PrefillParams& p, uint8_t* sm, uint32_t tmem, ui
     float* sLT = reinterpret_cast<float*>(sm + Q_OFF_L);
     float* Tf = reinterpret_cast<float*>(sm + Q_OFF_TF);
 #pragma unroll 1
-    for (int j = 0; fine && j < p.group; ++j) {
+    for (int j = j0; fine && j < j1; ++j) {
         const int h = g * p.group + j;
         if (tid < kChunk) {
             const bool in = tid < n;
@@ -556,9 +556,12 @@ __device__ bool prep_item(const PrefillParams& p, uint8_t* sm, uint32_t tmem, ui
                     }
             }
         }
+        __threadfence();  // this thread's record stores, before the flag
         fence_before_sync();
-        sync();  // every thread is past this head's TMEM reads and tiles
+        sync();  // every thread is past this head's TMEM reads, tiles and record stores
         fence_after_sync();
+        if (publish && tid == 0)
+            asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.ready + (size_t)c * p.Hv + h), "r"(1) : "memory");
     }
     if (!fine && tid == 0) atomicExch(p.status, 1);
     fence_before_sync();
@@ -589,7 +592,7 @@ gdn_prefill_prep_kernel(const __grid_constant__ PrefillParams p) {
     const int tid = threadIdx.x;
     const uint32_t tmem = prep_setup(sm, tid, CtaSync{});
     uint32_t phase[2] = {0, 0};
-    prep_item(p, sm, tmem, smem_u32(sm + Q_OFF_MISC), phase, blockIdx.x, blockIdx.y, tid, CtaSync{});
+    prep_item(p, sm, tmem, smem_u32(sm + Q_OFF_MISC), phase, blockIdx.x, blockIdx.y, 0, p.group, false, tid, CtaSync{});
     if ((tid >> 5) == 0) tmem_dealloc(tmem, kPrepTmemCols);
 }
 
@@ -992,7 +995,7 @@ constexpr uint32_t T_D = 128;    // [S K^T | S Q^T -> O^T] [i][t], 2 x 128 (by c
 constexpr uint32_t T_SH = 384;   // S hi (the next chunk's operand)        64
 constexpr uint32_t T_XA = 448;   // X^T                    hi 32 + lo 32  64
 
-// Wait (bounded) until the pre-pass item `item` has been published.
+// Wait (bounded) until ready flag `item` (chunk * Hv + value head) is set.
 __device__ __forceinline__ bool wait_ready(const int* ready, int item) {
     const uint64_t t0 = global_ns();
     while (true) {
@@ -1095,8 +1098,11 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
     auto issue_inputs = [&](int cc) -> bool {
         const uint32_t b = bar_in0 + 8u * (uint32_t)(cc & 1);
         const int t0 = cc * kChunk;
+        // the record's ready flag first (no buffer needed for that)
+        int ok = 1;
+        if (READY && lane == 0) ok = wait_ready(p.ready, cc * p.Hv + h);
+        if (__shfl_sync(0xffffffffu, ok, 0) == 0) return false;
         if (cc >= 2) {
-            int ok = 1;
             if (lane == 0)
                 ok = mbar_wait(bar_free0 + 8u * (uint32_t)(cc & 1), (uint32_t)((cc - 2) >> 1) & 1u, kWaitLimitNs);
             if (__shfl_sync(0xffffffffu, ok, 0) == 0) return false;
@@ -1113,18 +1119,14 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
         } else if (lane == 4) {
             tma_load_2d(sbase + C_OFF_V + (uint32_t)(cc & 1) * kVBytes, &p.tm_v, 2 * p.Hk * kD + h * kD, t0, b);
         }
-        // the record, once its flag is set
-        int ok = 1;
+        // the record (published above)
         if (lane == 0) {
-            ok = !READY || wait_ready(p.ready, cc * p.Hk + g);
-            if (ok) {
-                fence_proxy_async_global();
-                const uint8_t* rec =
-                    reinterpret_cast<const uint8_t*>(p.status) + kRecBase + ((size_t)cc * p.Hv + h) * kRecBytes;
-                bulk_g2s(sbase + C_OFF_REC + (uint32_t)(cc & 1) * kRecStride, rec, kRecBytes, b);
-            }
+            fence_proxy_async_global();
+            const uint8_t* rec =
+                reinterpret_cast<const uint8_t*>(p.status) + kRecBase + ((size_t)cc * p.Hv + h) * kRecBytes;
+            bulk_g2s(sbase + C_OFF_REC + (uint32_t)(cc & 1) * kRecStride, rec, kRecBytes, b);
         }
-        return __shfl_sync(0xffffffffu, ok, 0) != 0;
+        return true;
     };
     // every thread that reads a buffer waits for its phase (chunk cc is the
     // (cc >> 1)-th use of buffer cc & 1)
@@ -1376,25 +1378,36 @@ gdn_prefill_chain_kernel(const __grid_constant__ PrefillParams p) {
 
 // Pre-pass worker w of the cooperative kernel: two independent pipelines of
 // kPrefillThreads threads (each with its own shared memory, named barrier and
-// 128 TMEM columns of one shared allocation), pipeline q taking the items
-// (chunk, key head) 2w + q, 2w + q + 2 n_workers, ... in chunk order.  Each
-// item is published with a release store of its flag once all of its records
-// are written.
+// kPrepTmemCols TMEM columns of one shared allocation), pipeline q taking the
+// items 2w + q, 2w + q + 2 n_workers, ... in chunk order.  The first chunk,
+// which every chain waits for before it can start, is split into one item per
+// value head; later chunks have one item per key head (its value heads share
+// [K;Q] K^T).  Each record is published with a release store of its ready
+// flag once it is written.
 template <int Q>
 __device__ __forceinline__ void prep_pipeline(const PrefillParams& p, uint8_t* sm, uint32_t tmem, int w) {
     const int tid = threadIdx.x - Q * kPrefillThreads;
     const NamedSync<2 + Q, kPrefillThreads> sync;
     uint8_t* smq = sm + Q * kPrepStride;
     const uint32_t bars = smem_u32(smq + Q_OFF_MISC);
-    const int items = ((p.T + kChunk - 1) / kChunk) * p.Hk;
+    const int nchunks = (p.T + kChunk - 1) / kChunk;
+    const int items = nchunks > 0 ? p.Hv + (nchunks - 1) * p.Hk : 0;
     uint32_t phase[2] = {0, 0};
 #pragma unroll 1
     for (int item = 2 * w + Q; item < items; item += 2 * p.n_workers) {
-        const bool ok = prep_item(p, smq, tmem + Q * kPrepTmemCols, bars, phase, item / p.Hk, item % p.Hk, tid, sync);
-        __threadfence();  // this thread's record stores, before the flag
-        sync();
-        if (tid == 0 && ok) asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.ready + item), "r"(1) : "memory");
-        if (!ok) break;
+        int c, g, j0, j1;
+        if (item < p.Hv) {  // chunk 0, value head `item`
+            c = 0;
+            g = item / p.group;
+            j0 = item % p.group;
+            j1 = j0 + 1;
+        } else {
+            c = 1 + (item - p.Hv) / p.Hk;
+            g = (item - p.Hv) % p.Hk;
+            j0 = 0;
+            j1 = p.group;
+        }
+        if (!prep_item(p, smq, tmem + Q * kPrepTmemCols, bars, phase, c, g, j0, j1, true, tid, sync)) break;
     }
 }
 
@@ -1447,7 +1460,7 @@ int launch_prefill(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const
                    float* state, void* out, void* workspace, float q_scale, uint32_t flags, cudaStream_t st,
                    bool prep);
 // bytes of the ready flags (one int32 per chunk and key head), padded to 16
-size_t ready_bytes(size_t nchunks, int Hk) { return (nchunks * (size_t)Hk * 4 + 15) / 16 * 16; }
+size_t ready_bytes(size_t nchunks, int Hv) { return (nchunks * (size_t)Hv * 4 + 15) / 16 * 16; }
 constexpr int kMinWorkers = 8;  // fewest pre-pass workers worth a cooperative launch
 // CTAs of the cooperative kernel the device holds at once (0: no cooperative launch)
 int fused_capacity(int dev);
@@ -1462,7 +1475,7 @@ size_t gdn_prefill_workspace_bytes(const gdn_shape* shape, int32_t T, int32_t ch
     // (chunk, key head)
     if (shape->dk != kD || shape->dv != kD || shape->Hv < 1) return kRecBase;
     const size_t nchunks = ((size_t)T + kChunk - 1) / kChunk;
-    return kRecBase + nchunks * (size_t)shape->Hv * kRecBytes + ready_bytes(nchunks, shape->Hk);
+    return kRecBase + nchunks * (size_t)shape->Hv * kRecBytes + ready_bytes(nchunks, shape->Hv);
 }
 
 int gdn_chunk_prefill(const gdn_shape* shape, int32_t T, int32_t chunk, const gdn_bf16* qkv,
@@ -1481,7 +1494,7 @@ int gdn_chunk_prefill(const gdn_shape* shape, int32_t T, int32_t chunk, const gd
     // the ready flags start at zero on every call
     const size_t nchunks = ((size_t)T + kChunk - 1) / kChunk;
     e = cudaMemsetAsync(static_cast<uint8_t*>(workspace) + kRecBase + nchunks * (size_t)shape->Hv * kRecBytes, 0,
-                        ready_bytes(nchunks, shape->Hk), st);
+                        ready_bytes(nchunks, shape->Hv), st);
     if (e != cudaSuccess) return cuda_error(e, "prefill flag reset");
     return launch_prefill(shape, T, qkv, alpha, beta, state, out, workspace, q_scale, flags, st, true);
 }
@@ -1595,7 +1608,8 @@ int launch_prefill(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const
         // and at least a few pre-pass workers at once; otherwise the pre-pass
         // over all chunks, then the chain.
         const int resident = fused_capacity(dev);
-        const int workers = std::min(resident - shape->Hv, nchunks * shape->Hk);
+        const int items = shape->Hv + (nchunks - 1) * shape->Hk;  // chunk 0 per value head, then per key head
+        const int workers = std::min(resident - shape->Hv, items);
         if (workers >= kMinWorkers && (flags & GDN_PREFILL_TWO_LAUNCH) == 0) {
             p.n_workers = workers;
             void* args[] = {&p};

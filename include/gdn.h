@@ -309,9 +309,9 @@ int gdn_commit_path(const gdn_shape* shape, int32_t N, const int32_t* parents,
  * T tokens in chunks of `chunk` (0 on a bad shape or chunk).  The workspace
  * holds the call's status word (int32 at offset 0, padded to 256 bytes) and,
  * for 128-wide heads, one 50,432-byte pre-pass record per (chunk, value
- * head) and one int32 ready flag per (chunk, key head), padded to 16 bytes:
- * 256 + ceil(T / 64) * (Hv * 50,432 + 4 * Hk) bytes, the flags rounded up to
- * 16 (310 MB at T = 8,192 with 48 value and 16 key heads).
+ * head) and one int32 ready flag per (chunk, value head), padded to 16
+ * bytes: 256 + ceil(T / 64) * Hv * (50,432 + 4) bytes, the flags rounded up
+ * to 16 (310 MB at T = 8,192 with 48 value heads).
  */
 size_t gdn_prefill_workspace_bytes(const gdn_shape* shape, int32_t T, int32_t chunk);
 

@@ -280,10 +280,10 @@ def test_prefill_workspace_holds_the_prepass_records(lib):
     P = ctypes.c_void_p
     sh = gdn.gdn_shape(1, 16, 48, 128, 128)
     # the status word, one 50,432-byte record per (chunk of 64, value head), then
-    # one int32 ready flag per (chunk, key head), padded to 16 bytes
-    assert gdn.prefill_workspace_bytes(8192, 16, 48, 128, 128) == 256 + 128 * 48 * 50432 + 128 * 16 * 4
-    assert gdn.prefill_workspace_bytes(65, 16, 48, 128, 128) == 256 + 2 * 48 * 50432 + 2 * 16 * 4
-    assert gdn.prefill_workspace_bytes(65, 1, 3, 128, 128) == 256 + 2 * 3 * 50432 + 16
+    # one int32 ready flag per (chunk, value head), padded to 16 bytes
+    assert gdn.prefill_workspace_bytes(8192, 16, 48, 128, 128) == 256 + 128 * 48 * 50432 + 128 * 48 * 4
+    assert gdn.prefill_workspace_bytes(65, 16, 48, 128, 128) == 256 + 2 * 48 * 50432 + 2 * 48 * 4
+    assert gdn.prefill_workspace_bytes(65, 1, 3, 128, 128) == 256 + 2 * 3 * 50432 + 32
     assert gdn.prefill_workspace_bytes(100, 2, 4, 32, 32) == 256     # narrow heads: no records
     rc = lib.gdn_chunk_prefill(ctypes.byref(sh), 64, 64, P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE * 256),
                                256, 1.0, 1, None)
