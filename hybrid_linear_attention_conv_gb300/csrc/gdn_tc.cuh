@@ -147,21 +147,29 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
-// Wait for phase `parity` of `bar` to complete; give up after `limit_ns`.
-// Each try_wait may suspend the thread (up to the hint) until the phase
-// completes, so waiting warps do not take issue slots from working ones.
+// One bounded try: true once phase `parity` of `bar` has completed.  The
+// thread may be suspended (up to the hint) until the phase completes, so
+// waiting warps do not take issue slots from working ones.
 constexpr uint32_t kSuspendHintNs = 20000;
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete; give up after `limit_ns`.  The
+// clock is read only once the first try has come back empty (reading it costs
+// more than a try on a completed phase).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     while (true) {
-        uint32_t ok;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}\n"
-            : "=r"(ok)
-            : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
-            : "memory");
-        if (ok) return true;
+        if (mbar_try(bar, parity)) return true;
         if (global_ns() - t0 > limit_ns) return false;
     }
 }
