@@ -744,6 +744,7 @@ class TreeBatch(Workload):
         self.launches_per_step = 1
         self.units_per_step = B * N * HV
         self.dominant = "gdn_tree_kernel"
+        self.traffic_key = "gdn_tree_kernel[batch8]"  # the 8-tree launch, not the 1-tree one
         self.dominant_sources = DECODE_SOURCES
         self.bound = "alu"
         self.dominant_work = B * N * HV * step_flops_per_head_token()
