@@ -18,26 +18,37 @@
 // agree mathematically but round differently ("Serving A Research Architecture
 // On CPU", third exactness layer).
 //
+// Substituting U = T X gives the form the pipelined chain runs, which never
+// forms U:
+//   S  <- gamma_C S + X^T W,                W  = T^T diag(c) K,  c_t = (gamma_C/gamma_t) r_k,t
+//   O^T = (S Q^T) diag(gamma r_q) + X^T PT^T, PT = P T
+// W and PT depend only on the chunk's own q, k, alpha and beta, so a pre-pass
+// computes them for every chunk in parallel and the chain per value head only
+// carries S [K;Q]^T -> X^T -> S += X^T W from chunk to chunk.
+//
 // A chain CTA owns one value head; thread i owns state row i, which is TMEM
 // lane i of every accumulator, so all products are written in the transposed
-// form (value rows as M = 128): S [K;Q]^T, X^T T^T, Uhat^T K and U^T P^T.  The
-// state stays in TMEM as an fp32 accumulator across all chunks and crosses HBM
-// once in and once out.  Operands that are not exact in bf16 (S, X, T, U, P)
-// are split into bf16 hi + lo and multiplied in 2 or 3 passes (hi.hi + hi.lo +
-// lo.hi) so the result keeps close to fp32 accuracy; q, k, v enter as the raw
-// bf16 inputs (exact) with the norms applied as fp32 scalings.  T is solved
-// on the CUDA cores by blocked forward substitution.
+// form (value rows as M = 128).  The state stays in TMEM as an fp32
+// accumulator across all chunks and crosses HBM once in and once out.
+// Operands that are not exact in bf16 (S, X, T, P, W, PT) are split into bf16
+// hi + lo and multiplied in 2 or 3 passes (hi.hi + hi.lo + lo.hi) so the
+// result keeps close to fp32 accuracy; q, k, v enter as the raw bf16 inputs
+// (exact) with the norms applied as fp32 scalings.  T is solved on the CUDA
+// cores by blocked forward substitution.
 //
 // The kernels in this file:
-//   gdn_prefill_prep_kernel   the pre-pass: T, P and the per-token scalars of
-//                             every (chunk, key head), written as records;
+//   gdn_prefill_prep_kernel   the pre-pass: W, PT and the per-token scalars of
+//                             every (chunk, value head), written as records;
 //   gdn_prefill_chain_kernel  the pipelined chain reading those records;
 //   gdn_prefill_fused_kernel  both in one cooperative launch, the pre-pass
 //                             workers running ahead of the chains (the form
 //                             gdn_chunk_prefill takes where the GPU holds it);
-//   gdn_prefill_tc_kernel     the self-contained chain computing each chunk's
-//                             T and P itself (gdn_chunk_prefill_noalloc).
-// All four use the same chunk-local arithmetic, so they give the same bits.
+//   gdn_prefill_tc_kernel     the self-contained chain in the U form, computing
+//                             each chunk's T and P itself
+//                             (gdn_chunk_prefill_noalloc).
+// The first three run the same code on the same records, so the cooperative
+// and two-launch forms give the same bits; the self-contained chain groups the
+// same algebra differently and agrees within rounding.
 //
 // Heads smaller than 128 run the same recurrence token by token with the
 // decode kernel (still on the GPU; the chunk form here is written for the
