@@ -343,6 +343,44 @@ class Workload:
     def e2e_copy(self, dst, src):
         dst.copy_(src, non_blocking=True)
 
+    def e2e_streams(self):
+        """Copy streams of the overlapped end-to-end step: host->device and
+        device->host copies run on their own streams, ordered against the
+        compute stream by events, so that piece p's inputs arrive while piece
+        p - 1 computes and its outputs leave while piece p + 1 computes."""
+        torch = self.torch
+        self.s_in = torch.cuda.Stream(device=self.device)
+        self.s_out = torch.cuda.Stream(device=self.device)
+
+    def e2e_pipeline(self, pieces, inputs, outputs, compute):
+        """One end-to-end step in pieces: for piece k, copy inputs(k) in on
+        s_in, run compute(k) on the current stream, copy outputs(k) out on
+        s_out.  The step ends on the current stream once the last copy out
+        has landed, so events on it bracket every copy."""
+        torch = self.torch
+        cs = torch.cuda.current_stream()
+        start = torch.cuda.Event()
+        start.record(cs)
+        self.s_in.wait_event(start)
+        self.s_out.wait_event(start)
+        for k in range(pieces):
+            with torch.cuda.stream(self.s_in):
+                for dst, src in inputs(k):
+                    dst.copy_(src, non_blocking=True)
+                ev_in = torch.cuda.Event()
+                ev_in.record(self.s_in)
+            cs.wait_event(ev_in)
+            compute(k)
+            ev_c = torch.cuda.Event()
+            ev_c.record(cs)
+            with torch.cuda.stream(self.s_out):
+                self.s_out.wait_event(ev_c)
+                for dst, src in outputs(k):
+                    dst.copy_(src, non_blocking=True)
+        done = torch.cuda.Event()
+        done.record(self.s_out)
+        cs.wait_event(done)
+
 
 class Batched(Workload):
     """48 GDN layers x 64 sequences, one token per sequence per layer."""
@@ -433,25 +471,57 @@ class Batched(Workload):
             return [ms / self.L for ms in rec.step_ms()]
         return rec.kernel_ms(self.dominant)
 
-    def e2e_setup(self):
+    E2E_PIECES = 8  # layer groups of the overlapped end-to-end step
+
+    def e2e_pairs(self):
+        """(device, pinned host) pairs of a step's inputs, and (host, device)
+        of its result; every tensor has the layer as its first dimension."""
         torch = self.torch
         self.h_x = self.x[0].cpu().pin_memory()
         self.h_a = self.alpha[0].cpu().pin_memory()
         self.h_b = self.beta[0].cpu().pin_memory()
         self.h_out = torch.empty(self.out.shape, dtype=torch.float32, pin_memory=True)
-        self.e2e_h2d = self.h_x.numel() * 2 + self.h_a.numel() * 4 + self.h_b.numel() * 4
-        self.e2e_d2h = self.h_out.numel() * 4
+        return [(self.x[0], self.h_x), (self.alpha[0], self.h_a), (self.beta[0], self.h_b)], \
+               [(self.h_out, self.out)]
+
+    def e2e_setup(self):
+        torch = self.torch
+        self.e2e_in, self.e2e_out = self.e2e_pairs()
+        self.e2e_h2d = sum(src.numel() * src.element_size() for _, src in self.e2e_in)
+        self.e2e_d2h = sum(dst.numel() * dst.element_size() for dst, _ in self.e2e_out)
+        self.e2e_streams()
+        n = self.E2E_PIECES
+        per = (self.L + n - 1) // n
+        self.e2e_groups = [(l0, min(l0 + per, self.L)) for l0 in range(0, self.L, per)]
+        # one CUDA graph per layer group (eager launches under --eager)
+        self.e2e_graphs = []
+        if getattr(self, "graphs", None):
+            for l0, l1 in self.e2e_groups:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    sp = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+                    for l in range(l0, l1):
+                        _call(self.fn, self._args(0, l, sp), self.gdn)
+                self.e2e_graphs.append(g)
+            torch.cuda.synchronize()
 
     def e2e_step(self, i: int):
-        self.e2e_copy(self.x[0], self.h_x)
-        self.e2e_copy(self.alpha[0], self.h_a)
-        self.e2e_copy(self.beta[0], self.h_b)
-        if getattr(self, "graphs", None):
-            self.graphs[0].replay()
-        else:
-            for args in self.args[0]:
-                _call(self.fn, args, self.gdn)
-        self.e2e_copy(self.h_out, self.out)
+        groups = self.e2e_groups
+
+        def compute(k):
+            if self.e2e_graphs:
+                self.e2e_graphs[k].replay()
+            else:
+                l0, l1 = groups[k]
+                for l in range(l0, l1):
+                    _call(self.fn, self.args[0][l], self.gdn)
+
+        self.e2e_pipeline(len(groups),
+                          lambda k: [(d[groups[k][0]:groups[k][1]], h[groups[k][0]:groups[k][1]])
+                                     for d, h in self.e2e_in],
+                          lambda k: [(h[groups[k][0]:groups[k][1]], d[groups[k][0]:groups[k][1]])
+                                     for h, d in self.e2e_out],
+                          compute)
 
     def config(self=None) -> dict:
         L = Batched.L if self is None else self.L
@@ -511,27 +581,15 @@ class LayerBatched(Batched):
                 P(self.dt_bias[l].data_ptr()), P(self.z[s, l].data_ptr()), P(self.norm_w[l].data_ptr()), 1e-6,
                 P(self.state[l].data_ptr()), None, P(self.y[l].data_ptr()), 1.0, self.gdn.GDN_NORMALIZE_QK, sp)
 
-    def e2e_setup(self):
+    def e2e_pairs(self):
         torch = self.torch
         self.h_x = self.x[0].cpu().pin_memory()
         self.h_a = self.a[0].cpu().pin_memory()
         self.h_b = self.b[0].cpu().pin_memory()
         self.h_z = self.z[0].cpu().pin_memory()
         self.h_y = torch.empty(self.y.shape, dtype=torch.bfloat16, pin_memory=True)
-        self.e2e_h2d = (self.h_x.numel() + self.h_a.numel() + self.h_b.numel() + self.h_z.numel()) * 2
-        self.e2e_d2h = self.h_y.numel() * 2
-
-    def e2e_step(self, i: int):
-        self.e2e_copy(self.x[0], self.h_x)
-        self.e2e_copy(self.a[0], self.h_a)
-        self.e2e_copy(self.b[0], self.h_b)
-        self.e2e_copy(self.z[0], self.h_z)
-        if getattr(self, "graphs", None):
-            self.graphs[0].replay()
-        else:
-            for args in self.args[0]:
-                _call(self.fn, args, self.gdn)
-        self.e2e_copy(self.h_y, self.y)
+        return [(self.x[0], self.h_x), (self.a[0], self.h_a), (self.b[0], self.h_b), (self.z[0], self.h_z)], \
+               [(self.h_y, self.y)]
 
     def config(self=None) -> dict:
         L = Batched.L if self is None else self.L
@@ -938,6 +996,8 @@ class Prefill(Workload):
         if st != 0:
             raise RuntimeError("prefill reported a tensor-core wait timeout")
 
+    E2E_PIECE = 2048  # tokens per piece of the overlapped end-to-end step (a multiple of the chunk)
+
     def e2e_setup(self):
         self.h_qkv = self.qkv.cpu().pin_memory()
         self.h_a = self.alpha.cpu().pin_memory()
@@ -945,13 +1005,29 @@ class Prefill(Workload):
         self.h_out = self.torch.empty(self.out.shape, dtype=self.torch.float32, pin_memory=True)
         self.e2e_h2d = self.h_qkv.numel() * 2 + self.h_a.numel() * 4 + self.h_b.numel() * 4
         self.e2e_d2h = self.h_out.numel() * 4
+        self.e2e_streams()
 
     def e2e_step(self, i: int):
-        self.e2e_copy(self.qkv, self.h_qkv)
-        self.e2e_copy(self.alpha, self.h_a)
-        self.e2e_copy(self.beta, self.h_b)
-        _call(self.lib.gdn_chunk_prefill, self._args(), self.gdn)
-        self.e2e_copy(self.h_out, self.out)
+        """The 8,192 tokens as four consecutive calls of 2,048 (the state
+        carries over; the chunk boundaries are the same, so the results are
+        the same), each piece's copies overlapping its neighbours' compute."""
+        P, n = ctypes.c_void_p, self.E2E_PIECE
+        pieces = (self.T + n - 1) // n
+        sl = lambda k: slice(k * n, min((k + 1) * n, self.T))
+
+        def compute(k):
+            t = sl(k)
+            args = (ctypes.byref(self.shape), t.stop - t.start, CHUNK, P(self.qkv[t].data_ptr()),
+                    P(self.alpha[t].data_ptr()), P(self.beta[t].data_ptr()), P(self.state.data_ptr()),
+                    P(self.out[t].data_ptr()), P(self.ws.data_ptr()), self.ws.numel(), 1.0,
+                    self.gdn.GDN_NORMALIZE_QK, ctypes.c_void_p(self.torch.cuda.current_stream().cuda_stream))
+            _call(self.lib.gdn_chunk_prefill, args, self.gdn)
+
+        self.e2e_pipeline(pieces,
+                          lambda k: [(self.qkv[sl(k)], self.h_qkv[sl(k)]), (self.alpha[sl(k)], self.h_a[sl(k)]),
+                                     (self.beta[sl(k)], self.h_b[sl(k)])],
+                          lambda k: [(self.h_out[sl(k)], self.out[sl(k)])],
+                          compute)
 
     @staticmethod
     def config() -> dict:
