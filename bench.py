@@ -343,6 +343,26 @@ class Workload:
     def e2e_copy(self, dst, src):
         dst.copy_(src, non_blocking=True)
 
+    def e2e_pack(self, hosts):
+        """The small per-step inputs `hosts` (CPU tensors) packed back to back,
+        each at a 16-byte boundary, into one pinned host buffer and one device
+        buffer, so that a step moves them with one copy instead of one per
+        tensor (for a few KB the copy's fixed cost dominates).  Returns the
+        device views, shaped and typed like `hosts`."""
+        torch = self.torch
+        offs, n = [], 0
+        for h in hosts:
+            offs.append(n)
+            n += (h.numel() * h.element_size() + 15) // 16 * 16
+        self.e2e_hbuf = torch.zeros(n, dtype=torch.uint8, pin_memory=True)
+        self.e2e_dbuf = torch.empty(n, dtype=torch.uint8, device=self.device)
+        views = []
+        for h, o in zip(hosts, offs):
+            nb = h.numel() * h.element_size()
+            self.e2e_hbuf[o:o + nb].copy_(h.contiguous().reshape(-1).view(torch.uint8))
+            views.append(self.e2e_dbuf[o:o + nb].view(h.dtype).view(h.shape))
+        return views
+
     def e2e_streams(self):
         """Copy streams of the overlapped end-to-end step: host->device and
         device->host copies run on their own streams, ordered against the
@@ -643,12 +663,15 @@ class Decode1(Workload):
         self.step_bytes = fused_bytes_per_launch(1)
         self.k = 0  # ping-pong position of the conv tail
 
-    def _args(self, s):
+    def _args(self, s, x=None, alpha=None, beta=None):
         P = ctypes.c_void_p
         tin, tout = self.tails[self.k % 2], self.tails[(self.k + 1) % 2]
         self.k += 1
-        return (ctypes.byref(self.shape), 1, P(self.x[s].data_ptr()), P(self.w.data_ptr()), P(tin.data_ptr()),
-                P(tout.data_ptr()), P(self.alpha[s].data_ptr()), P(self.beta[s].data_ptr()),
+        x = self.x[s] if x is None else x
+        alpha = self.alpha[s] if alpha is None else alpha
+        beta = self.beta[s] if beta is None else beta
+        return (ctypes.byref(self.shape), 1, P(x.data_ptr()), P(self.w.data_ptr()), P(tin.data_ptr()),
+                P(tout.data_ptr()), P(alpha.data_ptr()), P(beta.data_ptr()),
                 P(self.state.data_ptr()), P(self.out[s].data_ptr()), 1.0, self.gdn.GDN_NORMALIZE_QK, self.sp)
 
     def step(self, i: int, rec: Recorder | None = None):
@@ -660,18 +683,15 @@ class Decode1(Workload):
             rec.mark("gdn_conv_decode_kernel")
 
     def e2e_setup(self):
-        self.h_x = self.x[0].cpu().pin_memory()
-        self.h_a = self.alpha[0].cpu().pin_memory()
-        self.h_b = self.beta[0].cpu().pin_memory()
+        self.e2e_views = self.e2e_pack([self.x[0].cpu(), self.alpha[0].cpu(), self.beta[0].cpu()])
         self.h_out = self.torch.empty(self.out[0].shape, dtype=self.torch.float32, pin_memory=True)
-        self.e2e_h2d = self.h_x.numel() * 2 + self.h_a.numel() * 4 + self.h_b.numel() * 4
+        self.e2e_h2d = self.e2e_hbuf.numel()
         self.e2e_d2h = self.h_out.numel() * 4
 
     def e2e_step(self, i: int):
-        self.e2e_copy(self.x[0], self.h_x)
-        self.e2e_copy(self.alpha[0], self.h_a)
-        self.e2e_copy(self.beta[0], self.h_b)
-        _call(self.lib.gdn_conv_decode_step, self._args(0), self.gdn)
+        self.e2e_copy(self.e2e_dbuf, self.e2e_hbuf)  # x, alpha, beta in one copy
+        vx, va, vb = self.e2e_views
+        _call(self.lib.gdn_conv_decode_step, self._args(0, vx, va, vb), self.gdn)
         self.e2e_copy(self.h_out, self.out[0])
 
     @staticmethod
@@ -725,23 +745,24 @@ class Tree(Workload):
     def marks_per_step(self) -> int:
         return self.tree_marks
 
-    def _run(self, s, rec=None):
+    def _run(self, s, rec=None, inputs=None):
         P = ctypes.c_void_p
         lib, gdn = self.lib, self.gdn
         pp = self.parents.ctypes.data_as(P)
-        _call(lib.gdn_conv_step, (1, self.N, C_QKV, pp, P(self.x[s].data_ptr()), P(self.w.data_ptr()),
+        x, alpha, beta = (self.x[s], self.alpha[s], self.beta[s]) if inputs is None else inputs
+        _call(lib.gdn_conv_step, (1, self.N, C_QKV, pp, P(x.data_ptr()), P(self.w.data_ptr()),
                                   P(self.tail.data_ptr()), P(self.y.data_ptr()), 0, self.sp), gdn)
         if rec:
             rec.mark("gdn_conv_kernel")
         _call(lib.gdn_tree_verify, (ctypes.byref(self.shape), self.N, pp, P(self.y.data_ptr()),
-                                    P(self.alpha[s].data_ptr()), P(self.beta[s].data_ptr()),
+                                    P(alpha.data_ptr()), P(beta.data_ptr()),
                                     P(self.state.data_ptr()), P(self.out.data_ptr()), 1.0,
                                     gdn.GDN_NORMALIZE_QK, self.sp), gdn)
         if rec:
             rec.mark("gdn_tree_kernel")
         _call(lib.gdn_commit_path, (ctypes.byref(self.shape), self.N, pp, self.path.ctypes.data_as(P),
-                                    len(self.path), P(self.y.data_ptr()), P(self.alpha[s].data_ptr()),
-                                    P(self.beta[s].data_ptr()), P(self.x[s].data_ptr()),
+                                    len(self.path), P(self.y.data_ptr()), P(alpha.data_ptr()),
+                                    P(beta.data_ptr()), P(x.data_ptr()),
                                     P(self.state.data_ptr()), P(self.tail.data_ptr()),
                                     gdn.GDN_NORMALIZE_QK, self.sp), gdn)
         if rec:
@@ -753,18 +774,14 @@ class Tree(Workload):
         self._run(i % self.n_sets, rec)
 
     def e2e_setup(self):
-        self.h_x = self.x[0].cpu().pin_memory()
-        self.h_a = self.alpha[0].cpu().pin_memory()
-        self.h_b = self.beta[0].cpu().pin_memory()
+        self.e2e_views = self.e2e_pack([self.x[0].cpu(), self.alpha[0].cpu(), self.beta[0].cpu()])
         self.h_out = self.torch.empty(self.out.shape, dtype=self.torch.float32, pin_memory=True)
-        self.e2e_h2d = self.h_x.numel() * 2 + self.h_a.numel() * 4 + self.h_b.numel() * 4
+        self.e2e_h2d = self.e2e_hbuf.numel()
         self.e2e_d2h = self.h_out.numel() * 4
 
     def e2e_step(self, i: int):
-        self.e2e_copy(self.x[0], self.h_x)
-        self.e2e_copy(self.alpha[0], self.h_a)
-        self.e2e_copy(self.beta[0], self.h_b)
-        self._run(0)
+        self.e2e_copy(self.e2e_dbuf, self.e2e_hbuf)  # x, alpha, beta in one copy
+        self._run(0, inputs=self.e2e_views)
         self.e2e_copy(self.h_out, self.out)
 
     def config(self=None) -> dict:
@@ -808,10 +825,11 @@ class TreeBatch(Workload):
         self.dominant_work = B * N * HV * step_flops_per_head_token()
         self.step_bytes = B * (HV * DV * DK * 4 + N * (C_QKV * 2 + HV * 8 + HV * DV * 4))
 
-    def _args(self, s):
+    def _args(self, s, inputs=None):
         P = ctypes.c_void_p
+        qkv, alpha, beta = (self.qkv[s], self.alpha[s], self.beta[s]) if inputs is None else inputs
         return (ctypes.byref(self.shape), self.N, self.counts.ctypes.data_as(P), self.parents.ctypes.data_as(P),
-                P(self.qkv[s].data_ptr()), P(self.alpha[s].data_ptr()), P(self.beta[s].data_ptr()),
+                P(qkv.data_ptr()), P(alpha.data_ptr()), P(beta.data_ptr()),
                 P(self.state.data_ptr()), P(self.out.data_ptr()), 1.0, self.gdn.GDN_NORMALIZE_QK, self.sp)
 
     def step(self, i: int, rec: Recorder | None = None):
@@ -823,18 +841,14 @@ class TreeBatch(Workload):
             rec.mark("gdn_tree_kernel")
 
     def e2e_setup(self):
-        self.h_qkv = self.qkv[0].cpu().pin_memory()
-        self.h_a = self.alpha[0].cpu().pin_memory()
-        self.h_b = self.beta[0].cpu().pin_memory()
+        self.e2e_views = self.e2e_pack([self.qkv[0].cpu(), self.alpha[0].cpu(), self.beta[0].cpu()])
         self.h_out = self.torch.empty(self.out.shape, dtype=self.torch.float32, pin_memory=True)
-        self.e2e_h2d = self.h_qkv.numel() * 2 + self.h_a.numel() * 4 + self.h_b.numel() * 4
+        self.e2e_h2d = self.e2e_hbuf.numel()
         self.e2e_d2h = self.h_out.numel() * 4
 
     def e2e_step(self, i: int):
-        self.e2e_copy(self.qkv[0], self.h_qkv)
-        self.e2e_copy(self.alpha[0], self.h_a)
-        self.e2e_copy(self.beta[0], self.h_b)
-        _call(self.lib.gdn_tree_verify_batched, self._args(0), self.gdn)
+        self.e2e_copy(self.e2e_dbuf, self.e2e_hbuf)  # q/k/v, alpha, beta in one copy
+        _call(self.lib.gdn_tree_verify_batched, self._args(0, self.e2e_views), self.gdn)
         self.e2e_copy(self.h_out, self.out)
 
     @staticmethod
