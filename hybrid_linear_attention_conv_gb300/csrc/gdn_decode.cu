@@ -17,6 +17,8 @@
 // verified in one pass).
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "gdn_conv.cuh"
 #include "gdn_gates.cuh"
 #include "gdn_internal.h"
@@ -26,6 +28,7 @@ namespace gdn {
 
 constexpr int kThreads = 256;        // 8 warps = 32 row groups of 8 lanes
 constexpr int kRowsPerPass = 32;
+constexpr int kMaxSmemPerCta = 232448;  // the opt-in shared memory of one CTA (227 KB)
 
 // KDA selects a decay per key channel: alpha is then [B, Tsrc, Hv, dk].
 template <int DK, int R, bool GATHER, bool KDA>
@@ -100,8 +103,8 @@ gdn_decode_kernel(const __grid_constant__ DecodeParams p) {
 }
 
 // Shared-memory staging of the tree's inputs for one CTA (after the slots):
-// q and k of this CTA's key head for every node, this CTA's 32 rows of v, and
-// alpha/beta -- loaded once, all loads in flight together, before the walk.
+// q and k of this CTA's key head for every node, this CTA's 32 R rows of v,
+// and alpha/beta -- loaded once, all loads in flight together, before the walk.
 // Per node, the normalised k and q in the lane layout of TokenKQ plus k.q,
 // computed once per CTA (by one row group per node, with token_kq itself).
 template <int DK>
@@ -109,26 +112,32 @@ __host__ __device__ constexpr size_t tree_kq_bytes(int N) {
     return (size_t)N * (8 * 2 * (DK / 32) * 4 * 4 + 16);
 }
 
-template <int DK>
+template <int DK, int R>
 __host__ __device__ constexpr size_t tree_stage_bytes(int N) {
-    return tree_kq_bytes<DK>(N) + (size_t)N * (kRowsPerPass * 2 + 2 * 4 + sizeof(TreeStep));
+    return tree_kq_bytes<DK>(N) + (size_t)N * (kRowsPerPass * R * 2 + 2 * 4 + sizeof(TreeStep));
 }
 
-template <int DK, int MB>
+// The tree walk.  A thread keeps R rows of the state (rows rg + 32 r of this
+// CTA's 32 R), so that each node's k and q, fetched from shared memory once
+// per thread, serve R rows: the walk is bound by those fetches (every row of
+// every value head reads the whole record), and R rows per fetch divide that
+// traffic by R while giving each thread R independent row chains.
+template <int DK, int MB, int R>
 __global__ void __launch_bounds__(kThreads)
 gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     constexpr int V = DK / 32;
+    constexpr int ROWS = kRowsPerPass * R;  // rows of one value head per CTA
     const int tree = blockIdx.z;          // sequence b: its own tree and state
     const int N = p.N[tree];
     const uint16_t* qkv = p.qkv + (size_t)tree * p.Nmax * p.C;
     const float* alpha_b = p.alpha + (size_t)tree * p.Nmax * p.Hv;
     const float* beta_b = p.beta + (size_t)tree * p.Nmax * p.Hv;
     extern __shared__ float4 smem4[];
-    float4* slots = smem4;  // [n_slots][32 row groups][V][8 lanes]
-    uint8_t* stage = reinterpret_cast<uint8_t*>(smem4) + (size_t)p.n_slots * kRowsPerPass * DK * sizeof(float);
+    float4* slots = smem4;  // [n_slots][R][32 row groups][V][8 lanes]
+    uint8_t* stage = reinterpret_cast<uint8_t*>(smem4) + (size_t)p.n_slots * ROWS * DK * sizeof(float);
     float4* s_kq = reinterpret_cast<float4*>(stage);                                   // per-node records
-    uint16_t* s_v = reinterpret_cast<uint16_t*>(stage + tree_kq_bytes<DK>(p.Nmax));        // [N][32]
-    float* s_ab = reinterpret_cast<float*>(s_v + (size_t)p.Nmax * kRowsPerPass);            // [N][alpha, beta]
+    uint16_t* s_v = reinterpret_cast<uint16_t*>(stage + tree_kq_bytes<DK>(p.Nmax));        // [N][32 R]
+    float* s_ab = reinterpret_cast<float*>(s_v + (size_t)p.Nmax * ROWS);                    // [N][alpha, beta]
     // the walk's schedule, copied out of the parameter block (read once per
     // step on the walk's dependent chain)
     TreeStep* steps = reinterpret_cast<TreeStep*>(s_ab + 2 * (size_t)p.Nmax);
@@ -136,17 +145,16 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     const int rg = threadIdx.x >> 3;
     const int h = blockIdx.y;
     const int g = h / p.group;
-    const int row0 = blockIdx.x * kRowsPerPass;
-    const int row = row0 + rg;
+    const int row0 = blockIdx.x * ROWS;
+    const int row = row0 + rg;  // this thread's rows: row + 32 r
     // node n's record in s_kq: [V float4 of k, V float4 of q][8 lanes], then k.q
     constexpr int KQ_REC = 8 * 2 * V + 1;  // float4 units
 
     {
-        for (int idx = threadIdx.x; idx < N * (kRowsPerPass / 8); idx += kThreads) {
-            const int n = idx / (kRowsPerPass / 8), c = idx % (kRowsPerPass / 8);
+        for (int idx = threadIdx.x; idx < N * (ROWS / 8); idx += kThreads) {
+            const int n = idx / (ROWS / 8), c = idx % (ROWS / 8);
             const uint16_t* src = qkv + (size_t)n * p.C + (size_t)2 * p.Hk * DK + (size_t)h * p.dv + row0 + c * 8;
-            *reinterpret_cast<uint4*>(s_v + (size_t)n * kRowsPerPass + c * 8) =
-                __ldg(reinterpret_cast<const uint4*>(src));
+            *reinterpret_cast<uint4*>(s_v + (size_t)n * ROWS + c * 8) = __ldg(reinterpret_cast<const uint4*>(src));
         }
         for (int n = threadIdx.x; n < N; n += kThreads) {
             s_ab[2 * n] = alpha_b[(size_t)n * p.Hv + h];
@@ -155,9 +163,12 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
         }
     }
     const float* S = p.state + ((size_t)tree * p.Hv + h) * p.dv * DK + (size_t)row * DK;
-    float4 s[V];
+    float4 s[R][V];
 #pragma unroll
-    for (int m = 0; m < V; ++m) s[m] = __ldg(reinterpret_cast<const float4*>(S + 32 * m + 4 * lane8));
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < V; ++m)
+            s[r][m] = __ldg(reinterpret_cast<const float4*>(S + (size_t)kRowsPerPass * r * DK + 32 * m + 4 * lane8));
     __syncthreads();
 
     const bool normalize = p.normalize != 0;
@@ -199,22 +210,40 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     // one step of the walk on the node record `cur`, fetching the next
     // step's record into `nxt` (the loop below alternates the two, so no
     // record is copied between steps)
+    auto slot_at = [&](int slot, int r, int m) -> float4& {
+        return slots[(((slot * R + r) * kRowsPerPass + rg) * V + m) * 8 + lane8];
+    };
     auto walk_step = [&](int step, const TokenKQ<V>& cur, TokenKQ<V>& nxt) {
         const TreeStep st = steps[step];
         if (st.restore >= 0) {
 #pragma unroll
-            for (int m = 0; m < V; ++m) s[m] = slots[((st.restore * kRowsPerPass + rg) * V + m) * 8 + lane8];
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int m = 0; m < V; ++m) s[r][m] = slot_at(st.restore, r, m);
         }
         const int node = st.node;
         if (step + 1 < N) fetch(steps[step + 1].node, nxt);
         const float alpha = s_ab[2 * node];
         const float beta = s_ab[2 * node + 1];
-        const float v_i = __uint_as_float((uint32_t)s_v[(size_t)node * kRowsPerPass + rg] << 16);
-        const float o = row_step<V>(s, cur, v_i, alpha, beta);
-        if (lane8 == 0) store_out(p.out, (((size_t)tree * p.Nmax + node) * p.Hv + h) * p.dv + row, o, out_bf16);
+        float o[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float v_i = __uint_as_float((uint32_t)s_v[(size_t)node * ROWS + kRowsPerPass * r + rg] << 16);
+            o[r] = row_step<V>(s[r], cur, v_i, alpha, beta);
+        }
+        // lane r of a row group stores row r's output (every lane holds the same bits)
+        float my_o = o[0];
+#pragma unroll
+        for (int r = 1; r < R; ++r)
+            if (lane8 == r) my_o = o[r];
+        if (lane8 < R)
+            store_out(p.out, (((size_t)tree * p.Nmax + node) * p.Hv + h) * p.dv + row + kRowsPerPass * lane8, my_o,
+                      out_bf16);
         if (st.save >= 0) {
 #pragma unroll
-            for (int m = 0; m < V; ++m) slots[((st.save * kRowsPerPass + rg) * V + m) * 8 + lane8] = s[m];
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int m = 0; m < V; ++m) slot_at(st.save, r, m) = s[r][m];
         }
     };
     TokenKQ<V> ka, kb;
@@ -524,31 +553,43 @@ cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int g
                : launch_decode_k<false, false>(p, dk, rows_per_cta, s);
 }
 
-template <int DK, int MB>
+template <int DK, int MB, int R>
 static cudaError_t launch_tree_t(const TreeParamsT<MB>& p, cudaStream_t s) {
-    const size_t smem = (size_t)p.n_slots * kRowsPerPass * DK * sizeof(float) + tree_stage_bytes<DK>(p.Nmax);
+    constexpr int ROWS = kRowsPerPass * R;
+    const size_t smem = (size_t)p.n_slots * ROWS * DK * sizeof(float) + tree_stage_bytes<DK, R>(p.Nmax);
     static bool configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured[dev]) {
-        const int max_smem = GDN_MAX_TREE_SLOTS * kRowsPerPass * DK * (int)sizeof(float) +
-                             (int)tree_stage_bytes<DK>(GDN_MAX_TREE_NODES);
-        cudaError_t e = cudaFuncSetAttribute(gdn_tree_kernel<DK, MB>,
+        const int max_smem = std::min(GDN_MAX_TREE_SLOTS * ROWS * DK * (int)sizeof(float) +
+                                          (int)tree_stage_bytes<DK, R>(GDN_MAX_TREE_NODES),
+                                      kMaxSmemPerCta);
+        cudaError_t e = cudaFuncSetAttribute(gdn_tree_kernel<DK, MB, R>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    dim3 grid(p.dv / kRowsPerPass, p.Hv, p.B);
-    gdn_tree_kernel<DK, MB><<<grid, kThreads, smem, s>>>(p);
+    dim3 grid(p.dv / ROWS, p.Hv, p.B);
+    gdn_tree_kernel<DK, MB, R><<<grid, kThreads, smem, s>>>(p);
     return cudaGetLastError();
+}
+
+// Rows per thread: 2 when the value head has a multiple of 64 rows and the
+// slots for them fit in shared memory (each node's record then serves two
+// rows per fetch), else 1.
+template <int DK, int MB>
+static cudaError_t launch_tree_r(const TreeParamsT<MB>& p, cudaStream_t s) {
+    const size_t smem2 = (size_t)p.n_slots * 2 * kRowsPerPass * DK * sizeof(float) + tree_stage_bytes<DK, 2>(p.Nmax);
+    if (p.dv % (2 * kRowsPerPass) == 0 && smem2 <= (size_t)kMaxSmemPerCta) return launch_tree_t<DK, MB, 2>(p, s);
+    return launch_tree_t<DK, MB, 1>(p, s);
 }
 
 template <int MB>
 cudaError_t launch_tree(const TreeParamsT<MB>& p, int dk, cudaStream_t s) {
     switch (dk) {
-        case 32: return launch_tree_t<32, MB>(p, s);
-        case 64: return launch_tree_t<64, MB>(p, s);
-        case 128: return launch_tree_t<128, MB>(p, s);
+        case 32: return launch_tree_r<32, MB>(p, s);
+        case 64: return launch_tree_r<64, MB>(p, s);
+        case 128: return launch_tree_r<128, MB>(p, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -69,6 +69,37 @@ def test_tree_verify_outputs_equal_decode_bitwise():
         assert torch.equal(out[n], o[-1]), f"node {n}"
 
 
+def _binary_tree(n):
+    return np.array([-1] + [(i - 1) // 2 for i in range(1, n)], np.int32)
+
+
+def _caterpillar(n):
+    """A spine whose every node also has one leaf."""
+    parents = [-1]
+    spine = 0
+    while len(parents) < n:
+        parents.append(spine)
+        nxt = len(parents) - 1
+        if len(parents) < n:
+            parents.append(spine)
+        spine = nxt
+    return np.array(parents, np.int32)
+
+
+@pytest.mark.parametrize("parents", [_binary_tree(63), _caterpillar(17), gen.random_tree(11, 64, 8),
+                                     gen.random_tree(12, 48, 12), gen.random_tree(13, 64, 4)])
+def test_tree_walk_shapes_equal_decode_bitwise(parents):
+    """Whatever walk the host schedules (two nodes per step where the tree
+    allows, else the depth-first walk), every node's output is the bits of
+    the linear decode of its root path."""
+    shape = gen.QWEN_27B
+    _, d = _tree_case(shape, len(parents), 5, parents=parents)
+    out = _verify(shape, parents, d)
+    for n in range(len(parents)):
+        o, _ = _path_decode(shape, d, gdn.tree_root_path(parents, n))
+        assert torch.equal(out[n], o[-1]), f"node {n}"
+
+
 @pytest.mark.parametrize("parents", [
     np.array([-1], np.int32),                                  # a single node
     np.arange(-1, 63, dtype=np.int32),                         # a 64-long chain (no branch states)
