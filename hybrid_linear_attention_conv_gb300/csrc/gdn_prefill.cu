@@ -966,9 +966,12 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
 // X^T PT^T and the output stores) runs in the shadow of those MMAs.  X^T is
 // the A operand of both products, written by the epilogue threads straight
 // to tensor memory as bf16 pairs, as is the S operand of S [K;Q]^T.  A chunk's
-// inputs ([K;Q], v, the record) arrive by the copy engine a whole chunk ahead
-// into double buffers; the output accumulator is double-buffered in tensor
-// memory, so that chunk c's outputs are read out while chunk c + 1 runs.
+// inputs ([K;Q], v, the record) arrive by the copy engine into double
+// buffers, requested by a copy warp of their own up to a chunk ahead; the
+// output accumulator is double-buffered in tensor memory, so that chunk c's
+// outputs are read out while chunk c + 1 runs.  Per chunk the MMA warp learns
+// from mbarriers that X^T and the S Q^T scaling are in place; one barrier
+// over the epilogue and MMA warps closes the chunk (the next S operand).
 // ---------------------------------------------------------------------------
 constexpr int kEpiThreads = 512;    // four epilogue warpgroups over the 128 TMEM lanes
 constexpr int kLoopThreads = kEpiThreads + 32;   // and one warp that only issues the MMAs
@@ -1019,8 +1022,8 @@ __device__ __forceinline__ bool wait_ready(const int* ready, int item) {
 }
 
 // The chain of value head h.  READY: the records are produced concurrently
-// by the pre-pass workers of the cooperative kernel; the MMA warp waits for a
-// record's flag just before it requests the record, a chunk ahead of use.
+// by the pre-pass workers of the cooperative kernel; the copy warp waits for
+// a record's flag before it requests the record, up to a chunk ahead of use.
 template <bool READY>
 __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, int h) {
     constexpr int CW = kChunk / 4;  // columns of a 64-wide tile per warpgroup
