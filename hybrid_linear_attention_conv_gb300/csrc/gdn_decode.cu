@@ -293,6 +293,13 @@ gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
     const int row0 = rb * (kRowsPerPass * R) + rg;
     auto state_of = [&](int j) { return p.state + ((size_t)b * p.Hv + g * p.group + j) * (size_t)p.dv * DK; };
 
+    // Launched as a programmatic dependent of the previous kernel on the
+    // stream: this grid's CTAs may be placed while that kernel drains.  Each
+    // lets the next kernel launch in turn, then waits for the previous one to
+    // complete (and its writes to be visible) before it touches any memory.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
     // KDA: the group's decay vectors [T][group][DK] go to shared memory after
     // the conv outputs; the first kThreads float4s are loaded before the conv
     // so that their latency overlaps it.
@@ -466,8 +473,19 @@ static cudaError_t launch_conv_decode_t(const ConvDecodeParams& p, cudaStream_t 
     dim3 grid(p.Hk * p.head_parts * p.row_blocks, p.B, 1);
     const size_t smem = (size_t)p.T * p.CC * 2 + (KIND == 1 ? (size_t)p.T * p.group * DK * 4 : 0) +
                         (KIND == 2 ? (size_t)p.T * p.group * 8 : 0);
-    gdn_conv_decode_kernel<DK, R, KIND><<<grid, kThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    // a programmatic dependent launch (see the kernel): consecutive layer
+    // steps overlap one's start with the other's drain
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gdn_conv_decode_kernel<DK, R, KIND>, p);
 }
 
 template <int DK, int KIND>
