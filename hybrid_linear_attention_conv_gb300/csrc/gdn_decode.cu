@@ -30,6 +30,17 @@ constexpr int kThreads = 256;        // 8 warps = 32 row groups of 8 lanes
 constexpr int kRowsPerPass = 32;
 constexpr int kMaxSmemPerCta = 232448;  // the opt-in shared memory of one CTA (227 KB)
 
+// Fused step (plain and KDA), several value heads per CTA: each thread copies
+// its rows of the next head's state into shared memory (cp.async, its own
+// slots only) while it advances the current head, so the head loop does not
+// wait on DRAM between heads.  [R * V][kThreads] float4 (element-major: a warp's accesses
+// are contiguous).
+template <int DK, int R>
+__host__ __device__ constexpr size_t conv_decode_prefetch_bytes() {
+    return (size_t)R * (DK / 32) * kThreads * 16;
+}
+__host__ __device__ constexpr size_t align16(size_t n) { return (n + 15) / 16 * 16; }
+
 // KDA selects a decay per key channel: alpha is then [B, Tsrc, Hv, dk].
 template <int DK, int R, bool GATHER, bool KDA>
 __global__ void __launch_bounds__(kThreads, 2)
@@ -357,6 +368,26 @@ gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
             s_ab[idx] = make_float2(al, be);
         }
     }
+    // the next head's state rows, prefetched by each thread into its own slots
+    // (not in the layer step, whose per-head norm barrier already overlaps the
+    // next head's loads, and which measured slower with it)
+    const bool prefetch = !LAYER && nh > 1;
+    float4* s_pref = reinterpret_cast<float4*>(
+        reinterpret_cast<uint8_t*>(smem_y) +
+        align16((size_t)p.T * p.CC * 2 + (KDA ? (size_t)p.T * p.group * DK * 4 : 0) + (LAYER ? (size_t)p.T * p.group * 8 : 0)));
+    auto prefetch_head = [&](int j) {
+        const float* S = state_of(j);
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < V; ++m) {
+                const uint32_t dst = (uint32_t)__cvta_generic_to_shared(s_pref + (size_t)(r * V + m) * kThreads + threadIdx.x);
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
+                             "l"(S + (size_t)(row0 + kRowsPerPass * r) * DK + 32 * m + 4 * lane8)
+                             : "memory");
+            }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
     // the row this lane writes outputs for: lane l < R of a row group takes
     // row r = l (every lane of the group holds the same o bits)
     const int my_row = row0 + kRowsPerPass * (lane8 < R ? lane8 : 0);
@@ -393,12 +424,22 @@ gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
         const int h = g * p.group + j;
         float* S = state_of(j);
         float4 s[R][V];
+        if (prefetch && j > j0) {
+            // this thread's own copies of head j (issued during head j - 1)
+            asm volatile("cp.async.wait_all;" ::: "memory");
 #pragma unroll
-        for (int r = 0; r < R; ++r)
+            for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int m = 0; m < V; ++m)
-                s[r][m] = __ldcs(reinterpret_cast<const float4*>(
-                    S + (size_t)(row0 + kRowsPerPass * r) * DK + 32 * m + 4 * lane8));
+                for (int m = 0; m < V; ++m) s[r][m] = s_pref[(size_t)(r * V + m) * kThreads + threadIdx.x];
+        } else {
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int m = 0; m < V; ++m)
+                    s[r][m] = __ldcs(reinterpret_cast<const float4*>(
+                        S + (size_t)(row0 + kRowsPerPass * r) * DK + 32 * m + 4 * lane8));
+        }
+        if (prefetch && j + 1 < j0 + nh) prefetch_head(j + 1);
         if constexpr (LAYER) {
             if (pend) finish_pending();  // the previous head's last token, behind these loads
         }
@@ -471,8 +512,21 @@ gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
 template <int DK, int R, int KIND>
 static cudaError_t launch_conv_decode_t(const ConvDecodeParams& p, cudaStream_t s) {
     dim3 grid(p.Hk * p.head_parts * p.row_blocks, p.B, 1);
-    const size_t smem = (size_t)p.T * p.CC * 2 + (KIND == 1 ? (size_t)p.T * p.group * DK * 4 : 0) +
-                        (KIND == 2 ? (size_t)p.T * p.group * 8 : 0);
+    const bool prefetch = KIND != 2 && p.group / p.head_parts > 1;
+    const size_t smem = align16((size_t)p.T * p.CC * 2 + (KIND == 1 ? (size_t)p.T * p.group * DK * 4 : 0) +
+                                (KIND == 2 ? (size_t)p.T * p.group * 8 : 0)) +
+                        (prefetch ? conv_decode_prefetch_bytes<DK, R>() : 0);
+    // above 48 KB the kernel's dynamic shared memory must be opted into (to
+    // what this launch needs: the opt-in limit counts its static memory too)
+    static size_t opted[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (smem > 48 * 1024 && dev >= 0 && dev < 64 && smem > opted[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(gdn_conv_decode_kernel<DK, R, KIND>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        opted[dev] = smem;
+    }
     // a programmatic dependent launch (see the kernel): consecutive layer
     // steps overlap one's start with the other's drain
     cudaLaunchConfig_t cfg = {};
