@@ -169,6 +169,10 @@ int gdn_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv,
  *              buffer (ping-pong between calls) lets small batches spread
  *              each head's rows over more CTAs.  Partial overlap is refused.
  *   alpha, beta, state, out, q_scale, flags: as for gdn_decode_step.
+ * The launch is a programmatic dependent launch: its CTAs may be placed
+ * while the previous kernel on the stream drains, but they touch no memory
+ * before that kernel has completed, so stream order is kept (consecutive
+ * layer steps overlap one's start with the other's end).
  * Source: the per-layer decode step of "Architecture" (v0.14.2) section 8.1
  * (conv tail + recurrent state per layer) and section 8.3 (decode loop).
  */
