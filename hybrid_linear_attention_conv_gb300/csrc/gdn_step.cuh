@@ -150,13 +150,6 @@ __device__ __forceinline__ float row_step(float4 (&s)[V], const TokenKQ<V>& t, f
     return o;
 }
 
-// One KDA token on one state row (a decay per key channel, Kimi Delta
-// Attention): row i of S <- (S diag(g)) (I - beta k k^T) + beta v k^T, then
-// o = S q.  The decay comes first, s' = g o s; then on s'
-//   a = s'.k, c = s'.q,  u = beta * (v_i - a),  o_i = c + u * (k.q),
-//   s <- s' + u * k.
-// With g equal on every channel this is the same map as row_step; the
-// rounding order differs (the decay is applied before the dot products).
 // KDA (Kimi Delta Attention) replaces the scalar decay by one per key channel:
 // row i of S <- (S diag(g)) (I - beta k k^T) + beta v k^T, then o = S q.  The
 // decay comes first, s' = g o s (kda_decay, applied to all of a thread's rows
