@@ -107,7 +107,8 @@ constexpr uint64_t kWaitLimitNs = 200000000ull;  // 0.2 s per tensor-core batch
 // Kernel parameters.  The two tensor maps describe the packed q/k/v rows
 // [T][C] (bf16) for the chain's TMA loads: 64 x 64 boxes with the 128-byte
 // swizzle (64 columns of 64 tokens) for K and Q, 128 x 64 plain boxes for V.
-struct alignas(64) PrefillParams {
+// (CUtensorMap carries its own 128-byte alignment, and so the struct.)
+struct PrefillParams {
     CUtensorMap tm_kq;
     CUtensorMap tm_v;
     const uint16_t* qkv;
