@@ -2,10 +2,13 @@
 """Benchmark of the Gated DeltaNet mixer hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload batched|decode1|tree|treebatch|prefill]
+                    [--workload batched|decode1|tree|treebatch|prefill|...]
 
 Prints ONE JSON line (rank 0).  The metric is GDN state updates per second
 (head.tokens/s) with the achieved HBM bandwidth against the measured peak.
+With no --workload, the line is the batched decode (the headline) and, under
+the key "workloads", the other single-GPU configs measured in the same run:
+decode1, tree and prefill, each with its own roofline, e2e and CPU baseline.
 
 Workloads (27B head shape: 16 key heads, 48 value heads, d = 128):
   batched  (default) one step = conv + decode of one token for 64 sequences in
@@ -1135,46 +1138,94 @@ class OracleSample:
         return self.units
 
 
-def cpu_oracle_sample(workload: str, seconds: float) -> dict:
-    smp = OracleSample(workload)
-    n, units = 0, 0.0
+def host_info() -> dict:
+    """The host's core count and CPU model (the CPU baseline's machine)."""
+    model = ""
+    try:  # lscpu names Arm cores (e.g. Neoverse-V2) where /proc/cpuinfo has only part numbers
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                txt = f.read()
+            for key in ("model name", "Model Name", "CPU part"):
+                for line in txt.splitlines():
+                    if line.startswith(key):
+                        model = line.split(":", 1)[1].strip()
+                        break
+                if model:
+                    break
+        except OSError:
+            pass
+    import platform
+    return {"nproc": os.cpu_count() or 1, "cpu_model": model or "unknown", "machine": platform.machine()}
+
+
+def cpu_oracle_sample(workload: str, seconds: float, threads: int = 1) -> dict:
+    """The oracle as it stands on a bounded sample of the workload for about
+    `seconds`: one thread, or `threads` threads each running its own copy of
+    the sample (independent sequences: the C oracle runs with the GIL
+    released, so the threads take separate cores)."""
+    from concurrent.futures import ThreadPoolExecutor
+    samples = [OracleSample(workload) for _ in range(threads)]
     t0 = time.perf_counter()
-    while True:
-        units += smp.run_once()
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return {"value": units / el, "unit": getattr(WORKLOADS[workload], "unit", UNIT), "cores": 1, "kind": "oracle",
-            "sample": f"{n} x ({smp.desc}), 27B head shape, fp64 C oracle, single thread, {el:.1f} s"}
+
+    def loop(smp):
+        n, units = 0, 0.0
+        while True:
+            units += smp.run_once()
+            n += 1
+            if time.perf_counter() - t0 >= seconds:
+                return n, units
+
+    if threads == 1:
+        results = [loop(samples[0])]
+    else:
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            results = list(ex.map(loop, samples))
+    el = time.perf_counter() - t0
+    n = sum(r[0] for r in results)
+    units = sum(r[1] for r in results)
+    how = "single thread" if threads == 1 else f"{threads} threads (one independent sample each)"
+    return {"value": units / el, "unit": getattr(WORKLOADS[workload], "unit", UNIT), "cores": threads,
+            "kind": "oracle",
+            "sample": f"{n} x ({samples[0].desc}), 27B head shape, fp64 C oracle, {how}, {el:.1f} s"}
+
+
+def cpu_baselines(workload: str, seconds: float) -> dict:
+    """The single-thread oracle (the cpu_baseline) with, beside it, the same
+    sample on every host core and the host's description."""
+    one = cpu_oracle_sample(workload, seconds, 1)
+    info = host_info()
+    if info["nproc"] > 1:
+        one["all_cores"] = cpu_oracle_sample(workload, seconds, info["nproc"])
+    one["host"] = info
+    return one
 
 
 # ---------------------------------------------------------------------------
 # arms
 # ---------------------------------------------------------------------------
-def run_ours(args) -> dict | None:
+def measure(args, name: str, steps: int, warmup: int, device, peaks: dict, peaks_kind: str, cpu: bool) -> dict:
+    """One workload's timed steps, roofline, end-to-end run and CPU baseline:
+    the fields of a bench line (rank 0 gets the aggregate over ranks)."""
     import torch
     rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-
-    import __graft_entry__
-    __graft_entry__.build()
-
-    peaks, peaks_kind = load_peaks()
-    cls = WORKLOADS[args.workload]
+    cls = WORKLOADS[name]
     if issubclass(cls, Batched):
-        wl = cls(device, 1234 + rank, args.steps + args.warmup, layers=args.layers)
+        wl = cls(device, 1234 + rank, steps + warmup, layers=args.layers)
     elif cls is Snapshot:
-        wl = cls(device, 1234 + rank, args.steps + args.warmup, layers=args.layers, seqs=args.seqs)
+        wl = cls(device, 1234 + rank, steps + warmup, layers=args.layers, seqs=args.seqs)
     else:
-        wl = cls(device, 1234 + rank, args.steps + args.warmup)
+        wl = cls(device, 1234 + rank, steps + warmup)
     torch.cuda.synchronize()
 
-    for i in range(args.warmup):
+    for i in range(warmup):
         wl.pre_step()
         wl.step(i)
     torch.cuda.synchronize()
@@ -1183,15 +1234,15 @@ def run_ours(args) -> dict | None:
         wl.step(0)  # one replay before the timed region
         torch.cuda.synchronize()
 
-    rec = Recorder(torch, wl.stream, wl.marks_per_step, args.steps)
+    rec = Recorder(torch, wl.stream, wl.marks_per_step, steps)
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.2)
     barrier(world)
     torch.cuda.synchronize()
-    for i in range(args.steps):
+    for i in range(steps):
         wl.pre_step()
-        wl.step(args.warmup + i, rec)
+        wl.step(warmup + i, rec)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
@@ -1200,7 +1251,7 @@ def run_ours(args) -> dict | None:
     step_ms = rec.step_ms()
     total_s = sum(step_ms) / 1e3
     dom_ms = wl.dominant_ms(rec) if hasattr(wl, "dominant_ms") else rec.kernel_ms(wl.dominant)
-    agg = aggregate(wl.units_per_step * args.steps, total_s, world, device)
+    agg = aggregate(wl.units_per_step * steps, total_s, world, device)
 
     # end-to-end through the API with host buffers
     wl.e2e_setup()
@@ -1214,17 +1265,16 @@ def run_ours(args) -> dict | None:
     e2e_total = 0.0
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    for i in range(args.steps):
+    for i in range(steps):
         wl.pre_step()
         e0.record()
         wl.e2e_step(i)
         e1.record()
         e1.synchronize()
         e2e_total += e0.elapsed_time(e1) / 1e3
-    e2e = aggregate(wl.units_per_step * args.steps, e2e_total, world, device)
-
-    if rank != 0:
-        return None
+    e2e = aggregate(wl.units_per_step * steps, e2e_total, world, device)
+    if hasattr(wl, "check_status"):
+        wl.check_status()
 
     dom_avg_s = statistics.mean(dom_ms) / 1e3
     if wl.bound == "hbm":
@@ -1241,7 +1291,7 @@ def run_ours(args) -> dict | None:
         peak, unit = fp32_alu_peak_tflops(mhz), "TFLOP/s"
         peak_kind = f"derived fp32 FMA peak: {SMS} SMs x {FP32_LANES_PER_SM} lanes x 2 x {mhz:.0f} MHz"
     traffic = ncu_traffic(getattr(wl, "traffic_key", wl.dominant), wl.dominant_sources)
-    step_gbs = wl.step_bytes * args.steps / total_s / 1e9
+    step_gbs = wl.step_bytes * steps / total_s / 1e9
     roof = {"bound": wl.bound, "kernel": wl.dominant, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": achieved / peak, "peak_kind": peak_kind, "avg_launch_us": dom_avg_s * 1e6,
             "work_per_launch": wl.dominant_work,
@@ -1254,8 +1304,8 @@ def run_ours(args) -> dict | None:
         "value": agg["value"],
         "unit": unit_v,
         "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
+        "steps": steps,
+        "warmup": warmup,
         "ms_per_step": statistics.mean(step_ms),
         "higher_is_better": True,
         "scaling": "weak",
@@ -1268,11 +1318,46 @@ def run_ours(args) -> dict | None:
         "roofline": roof,
         "clocks": clk,
         "e2e": {"value": e2e["value"], "unit": unit_v, "h2d_bytes_per_step": wl.e2e_h2d,
-                "d2h_bytes_per_step": wl.e2e_d2h, "ms_per_step": e2e_total * 1e3 / args.steps},
-        "gpu_launches": wl.launches_per_step * args.steps,
+                "d2h_bytes_per_step": wl.e2e_d2h, "ms_per_step": e2e_total * 1e3 / steps},
+        "gpu_launches": wl.launches_per_step * steps,
     }
-    if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_oracle_sample(args.workload, args.cpu_seconds)
+    del wl, rec
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    if cpu and rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baselines(name, args.cpu_seconds)
+    return line
+
+
+# the other single-GPU configs measured beside the headline in a default run
+EXTRA_WORKLOADS = ("decode1", "tree", "prefill")
+
+
+def run_ours(args) -> dict | None:
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+
+    peaks, peaks_kind = load_peaks()
+    name = args.workload or "batched"
+    steps = args.steps if args.steps is not None else DEFAULT_STEPS[name]
+    line = measure(args, name, steps, args.warmup, device, peaks, peaks_kind, cpu=True)
+    if args.workload is None and world == 1 and not args.no_extras:
+        # the other configs, each at its own step count (decode1 1,000 steps
+        # as its config states; all of them finish in well under a second of
+        # GPU time)
+        line["workloads"] = {w: measure(args, w, DEFAULT_STEPS[w], args.warmup, device, peaks, peaks_kind,
+                                        cpu=True)
+                             for w in EXTRA_WORKLOADS}
+    if rank != 0:
+        return None
     return line
 
 
@@ -1280,26 +1365,29 @@ def run_reference(args) -> dict | None:
     rank, world, _ = dist_env()
     if rank != 0:
         return None
-    smp = OracleSample(args.workload)
+    name = args.workload or "batched"
+    steps = args.steps if args.steps is not None else DEFAULT_STEPS[name]
+    smp = OracleSample(name)
     for _ in range(args.warmup):
         smp.run_once()
     units = 0
     t0 = time.perf_counter()
-    for _ in range(args.steps):
+    for _ in range(steps):
         units += smp.run_once()
     el = time.perf_counter() - t0
     value = units / el
     sample = f"each step: {smp.desc}, 27B head shape, fp64 C oracle, single thread"
-    cls = WORKLOADS[args.workload]
+    cls = WORKLOADS[name]
     cfg = cls.config()
     metric, unit = getattr(cls, "metric", METRIC), getattr(cls, "unit", UNIT)
     return {
         "impl": "reference",
-        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
+        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": el * 1e3 / steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": getattr(cls, "dtype", "f64"), "data": "synthetic",
         "config": cfg,
-        "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle", "sample": sample,
+                         "host": host_info()},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -1310,7 +1398,11 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="batched")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=None,
+                    help="one workload alone (default: the batched decode, with decode1, tree and prefill "
+                         "measured beside it under \"workloads\")")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="with no --workload, measure the batched decode only")
     ap.add_argument("--layers", type=int, default=48,
                     help="GDN layers in the batched workload (48 = the 27B model; fewer only for "
                          "profiling small cases)")
@@ -1322,8 +1414,6 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
-    if args.steps is None:
-        args.steps = DEFAULT_STEPS[args.workload]
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line is not None:

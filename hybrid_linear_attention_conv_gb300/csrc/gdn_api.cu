@@ -6,6 +6,7 @@
 // Research Architecture On CPU").  Nothing here allocates device memory.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -57,9 +58,10 @@ int check_shape(const gdn_shape* s, bool need_single) {
 
 int packed_channels(const gdn_shape* s) { return 2 * s->Hk * s->dk + s->Hv * s->dv; }
 
-int check_flags(uint32_t flags) {
-    if (flags & ~(GDN_NORMALIZE_QK | GDN_OUT_BF16))
-        return fail(GDN_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
+// `extra`: flag bits this call accepts beyond the common two.
+int check_flags(uint32_t flags, uint32_t extra = 0) {
+    if (flags & ~(GDN_NORMALIZE_QK | GDN_OUT_BF16 | extra))
+        return fail(GDN_ERR_INVALID_ARG, "unknown flag bits 0x%x for this call", flags);
     return GDN_OK;
 }
 
@@ -149,15 +151,16 @@ int check_path(int N, const int32_t* parents, const int32_t* path, int L) {
 }
 
 int sm_count() {
-    static int cached[64] = {};
+    // relaxed atomics: host threads may race to fill an entry, all with the same value
+    static std::atomic<int> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (cached[dev] == 0) {
-        int n = 0;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-        cached[dev] = n;
+        cached[dev].store(n, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return n;
 }
 
 // Rows of one head per CTA for decode: the widest (fewest CTAs, most loads in
@@ -241,10 +244,12 @@ int gdn_tree_root_path(int32_t N, const int32_t* parents, int32_t node, int32_t*
     return len;
 }
 
-int gdn_conv_step(int32_t B, int32_t T, int32_t C, const int32_t* parents, const gdn_bf16* x,
-                  const gdn_bf16* w, gdn_bf16* tail, gdn_bf16* y, uint32_t flags, void* stream) {
+int gdn_conv_step(int32_t B, int32_t T, int32_t C, const int32_t* parents, const void* x, const void* w,
+                  void* tail, void* y, uint32_t flags, void* stream) {
     int rc;
-    if ((rc = check_flags(flags)) != GDN_OK) return rc;
+    if ((rc = check_flags(flags, GDN_IN_F32)) != GDN_OK) return rc;
+    if (flags & (GDN_NORMALIZE_QK | GDN_OUT_BF16))
+        return fail(GDN_ERR_INVALID_ARG, "the conv takes only GDN_IN_F32 (flags 0x%x)", flags);
     if (B < 0 || T < 0 || C < 0) return fail(GDN_ERR_INVALID_ARG, "negative size B=%d T=%d C=%d", B, T, C);
     if (C % 8 != 0) return fail(GDN_ERR_UNSUPPORTED_SHAPE, "channels C=%d not a multiple of 8", C);
     if (B > 65535) return fail(GDN_ERR_UNSUPPORTED_SHAPE, "B=%d exceeds 65535", B);
@@ -261,6 +266,7 @@ int gdn_conv_step(int32_t B, int32_t T, int32_t C, const int32_t* parents, const
     p.B = B;
     p.T = T;
     p.C = C;
+    p.f32 = (flags & GDN_IN_F32) != 0;
     p.tree = parents != nullptr;
     if (p.tree) {
         for (int n = 0; n < T; ++n) {
@@ -281,19 +287,20 @@ int gdn_conv_step(int32_t B, int32_t T, int32_t C, const int32_t* parents, const
 }
 
 // The decode step with a decay per head (kda = false) or per key channel.
-static int decode_impl(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const float* alpha,
+static int decode_impl(const gdn_shape* shape, int32_t T, const void* qkv, const float* alpha,
                        const float* beta, float* state, void* out, float q_scale, uint32_t flags,
                        void* stream, bool kda) {
     int rc;
     if ((rc = check_shape(shape, false)) != GDN_OK) return rc;
-    if ((rc = check_flags(flags)) != GDN_OK) return rc;
+    if ((rc = check_flags(flags, kda ? 0u : GDN_IN_F32)) != GDN_OK) return rc;
     if (T < 0) return fail(GDN_ERR_INVALID_ARG, "T=%d < 0", T);
     if (shape->B == 0 || T == 0) return GDN_OK;  // nothing to do; pointers may be NULL
     if ((rc = check_ptr(qkv, "qkv")) || (rc = check_ptr(alpha, "alpha")) || (rc = check_ptr(beta, "beta")) ||
         (rc = check_ptr(state, "state")) || (rc = check_ptr(out, "out", false)))
         return rc;
+    const bool in_f32 = (flags & GDN_IN_F32) != 0;
     DecodeParams p{};
-    p.qkv = qkv;
+    p.qkv = static_cast<const uint16_t*>(qkv);
     p.alpha = alpha;
     p.beta = beta;
     p.state = state;
@@ -310,11 +317,11 @@ static int decode_impl(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, c
     p.normalize = (flags & GDN_NORMALIZE_QK) != 0;
     p.out_bf16 = (flags & GDN_OUT_BF16) != 0;
     const int rows = decode_rows_per_cta(shape->B, shape->Hv, shape->dv);
-    cudaError_t e = launch_decode(p, shape->dk, rows, 0, kda, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_decode(p, shape->dk, rows, 0, kda, in_f32, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, kda ? "KDA decode launch" : "decode launch");
 }
 
-int gdn_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const float* alpha,
+int gdn_decode_step(const gdn_shape* shape, int32_t T, const void* qkv, const float* alpha,
                     const float* beta, float* state, void* out, float q_scale, uint32_t flags,
                     void* stream) {
     return decode_impl(shape, T, qkv, alpha, beta, state, out, q_scale, flags, stream, false);
@@ -584,7 +591,7 @@ int gdn_commit_path(const gdn_shape* shape, int32_t N, const int32_t* parents, c
     p.out_bf16 = 0;
     for (int i = 0; i < L; ++i) p.tok[i] = path[i];
     const int rows = decode_rows_per_cta(1, shape->Hv, shape->dv);
-    cudaError_t e = launch_decode(p, shape->dk, rows, 1, false, st);
+    cudaError_t e = launch_decode(p, shape->dk, rows, 1, false, false, st);
     if (e != cudaSuccess) return cuda_fail(e, "commit launch");
     if (x_tree != nullptr) {
         TailParams tp{};

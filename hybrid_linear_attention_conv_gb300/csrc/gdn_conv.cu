@@ -18,18 +18,21 @@ namespace gdn {
 constexpr int kConvThreads = 128;
 constexpr int kConvTok = 16;  // tokens per thread in a linear run
 
+// E is the element type of x, w, tail and y: uint16_t (bf16 bits; y rounded
+// to bf16) or float (the fp32-activation conv; y kept in fp32).
+template <typename E>
 __global__ void __launch_bounds__(kConvThreads) gdn_conv_kernel(const __grid_constant__ ConvParams p) {
     const int cv = blockIdx.x * kConvThreads + threadIdx.x;
     const int c0 = cv * 8;
     if (c0 >= p.C) return;
     const int b = blockIdx.z;
     const size_t C = (size_t)p.C;
-    const uint16_t* xb = p.x + (size_t)b * p.T * C + c0;
-    uint16_t* yb = p.y + (size_t)b * p.T * C + c0;
-    uint16_t* tb = p.tail + (size_t)b * GDN_CONV_W * C + c0;
+    const E* xb = static_cast<const E*>(p.x) + (size_t)b * p.T * C + c0;
+    E* yb = static_cast<E*>(p.y) + (size_t)b * p.T * C + c0;
+    E* tb = static_cast<E*>(p.tail) + (size_t)b * GDN_CONV_W * C + c0;
 
     float w[8][4];
-    load_taps8(p.w + (size_t)c0 * GDN_CONV_W, w);
+    load_taps8(static_cast<const E*>(p.w) + (size_t)c0 * GDN_CONV_W, w);
 
     if (!p.tree && gridDim.y == 1) {
         // The whole run in one pass (T <= kConvTok, e.g. a decode step): a
@@ -70,16 +73,20 @@ __global__ void __launch_bounds__(kConvThreads) gdn_conv_kernel(const __grid_con
         if (blockIdx.y == 0) {
             // New tail = the last four of (tail ++ x).  Only this thread touches
             // these channels of the tail, and it has finished reading it.
-            uint4 nt[GDN_CONV_W];
+            // (raw 16-byte words: the bytes are copied as they are)
+            constexpr int W16 = (int)sizeof(E) / 2;  // 16-byte words per 8 channels
+            uint4 nt[GDN_CONV_W][W16];
 #pragma unroll
             for (int j = 0; j < GDN_CONV_W; ++j) {
                 const int pos = p.T + j;  // index into tail ++ x
-                const uint16_t* src = pos < GDN_CONV_W ? tb + (size_t)pos * C
-                                                       : xb + (size_t)(pos - GDN_CONV_W) * C;
-                nt[j] = *reinterpret_cast<const uint4*>(src);
+                const E* src = pos < GDN_CONV_W ? tb + (size_t)pos * C : xb + (size_t)(pos - GDN_CONV_W) * C;
+#pragma unroll
+                for (int q = 0; q < W16; ++q) nt[j][q] = reinterpret_cast<const uint4*>(src)[q];
             }
 #pragma unroll
-            for (int j = 0; j < GDN_CONV_W; ++j) *reinterpret_cast<uint4*>(tb + (size_t)j * C) = nt[j];
+            for (int j = 0; j < GDN_CONV_W; ++j)
+#pragma unroll
+                for (int q = 0; q < W16; ++q) reinterpret_cast<uint4*>(tb + (size_t)j * C)[q] = nt[j][q];
         }
     } else {
         const int n = blockIdx.y;
@@ -115,7 +122,8 @@ cudaError_t launch_conv(const ConvParams& p, cudaStream_t s) {
     const int cvecs = p.C / 8;
     const int gy = p.tree ? p.T : (p.T + kConvTok - 1) / kConvTok;
     dim3 grid((cvecs + kConvThreads - 1) / kConvThreads, gy, p.B);
-    gdn_conv_kernel<<<grid, kConvThreads, 0, s>>>(p);
+    if (p.f32) gdn_conv_kernel<float><<<grid, kConvThreads, 0, s>>>(p);
+    else gdn_conv_kernel<uint16_t><<<grid, kConvThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 

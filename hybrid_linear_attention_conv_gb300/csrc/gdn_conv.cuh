@@ -28,6 +28,22 @@ __device__ __forceinline__ Vec8 load8(const uint16_t* p) {
     return r;
 }
 
+// 8 consecutive fp32 channels (the fp32-activation conv).
+__device__ __forceinline__ Vec8 load8(const float* p) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 b = *reinterpret_cast<const float4*>(p + 4);
+    Vec8 r;
+    r.v[0] = a.x;
+    r.v[1] = a.y;
+    r.v[2] = a.z;
+    r.v[3] = a.w;
+    r.v[4] = b.x;
+    r.v[5] = b.y;
+    r.v[6] = b.z;
+    r.v[7] = b.w;
+    return r;
+}
+
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
     const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(a));
     const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(b));
@@ -57,6 +73,29 @@ __device__ __forceinline__ void store_y(uint16_t* dst, const float (&w)[8][4], c
     *reinterpret_cast<uint4*>(dst) = out;
 }
 
+// The same 8 outputs kept in fp32 (the fp32-activation conv stores no bf16).
+__device__ __forceinline__ void store_y(float* dst, const float (&w)[8][4], const Vec8& u0, const Vec8& u1,
+                                        const Vec8& u2, const Vec8& u3) {
+    float y[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) y[c] = conv_silu(w[c], u0.v[c], u1.v[c], u2.v[c], u3.v[c]);
+    *reinterpret_cast<float4*>(dst) = make_float4(y[0], y[1], y[2], y[3]);
+    *reinterpret_cast<float4*>(dst + 4) = make_float4(y[4], y[5], y[6], y[7]);
+}
+
+// Taps of 8 consecutive channels, fp32 [C][4].
+__device__ __forceinline__ void load_taps8(const float* wp, float (&w)[8][4]) {
+    const float4* w4 = reinterpret_cast<const float4*>(wp);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const float4 t = w4[c];
+        w[c][0] = t.x;
+        w[c][1] = t.y;
+        w[c][2] = t.z;
+        w[c][3] = t.w;
+    }
+}
+
 // Taps of 8 consecutive channels (w is [C][4] bf16, channel-major).
 __device__ __forceinline__ void load_taps8(const uint16_t* wp, float (&w)[8][4]) {
     const uint4* w4 = reinterpret_cast<const uint4*>(wp);
@@ -72,6 +111,12 @@ __device__ __forceinline__ void load_taps8(const uint16_t* wp, float (&w)[8][4])
         w[2 * q + 1][2] = bf16_lo(raw.w);
         w[2 * q + 1][3] = bf16_hi(raw.w);
     }
+}
+
+// Store 8 fp32 inputs as they are (the fp32-activation tail).
+__device__ __forceinline__ void put8(float* dst, const Vec8& v) {
+    *reinterpret_cast<float4*>(dst) = make_float4(v.v[0], v.v[1], v.v[2], v.v[3]);
+    *reinterpret_cast<float4*>(dst + 4) = make_float4(v.v[4], v.v[5], v.v[6], v.v[7]);
 }
 
 // Store 8 values that are exact in bf16 (a window of inputs) as bf16.

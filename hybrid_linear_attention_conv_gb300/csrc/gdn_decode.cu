@@ -18,6 +18,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "gdn_conv.cuh"
 #include "gdn_gates.cuh"
@@ -42,10 +43,12 @@ __host__ __device__ constexpr size_t conv_decode_prefetch_bytes() {
 __host__ __device__ constexpr size_t align16(size_t n) { return (n + 15) / 16 * 16; }
 
 // KDA selects a decay per key channel: alpha is then [B, Tsrc, Hv, dk].
-template <int DK, int R, bool GATHER, bool KDA>
+// In is the activations' element type: uint16_t (bf16 bits) or float.
+template <int DK, int R, bool GATHER, bool KDA, typename In>
 __global__ void __launch_bounds__(kThreads, 2)
 gdn_decode_kernel(const __grid_constant__ DecodeParams p) {
     constexpr int V = DK / 32;
+    const In* qkv = reinterpret_cast<const In*>(p.qkv);
     const int lane8 = threadIdx.x & 7;
     const int rg = threadIdx.x >> 3;
     const int h = blockIdx.y;
@@ -76,14 +79,14 @@ gdn_decode_kernel(const __grid_constant__ DecodeParams p) {
                     __ldg(reinterpret_cast<const float4*>(p.alpha + (trow * p.Hv + h) * DK) + threadIdx.x);
             __syncthreads();
         }
-        const uint16_t* row = p.qkv + trow * (size_t)p.C;
+        const In* row = qkv + trow * (size_t)p.C;
         TokenKQ<V> kq;
         token_kq<V>(row + g * DK, row + (size_t)p.Hk * DK + g * DK, lane8, p.q_scale,
                     normalize, kq);
         float alpha = 0.0f;
         if constexpr (!KDA) alpha = p.alpha[trow * p.Hv + h];
         const float beta = p.beta[trow * p.Hv + h];
-        const uint16_t* vrow = row + (size_t)2 * p.Hk * DK + (size_t)h * p.dv;
+        const In* vrow = row + (size_t)2 * p.Hk * DK + (size_t)h * p.dv;
         if constexpr (KDA) {
             float4 g[V];
             load_gate_smem<V>(s_gate[t & 1], lane8, g);
@@ -94,7 +97,7 @@ gdn_decode_kernel(const __grid_constant__ DecodeParams p) {
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const int i = row0 + kRowsPerPass * r;
-            const float v_i = __uint_as_float((uint32_t)vrow[i] << 16);
+            const float v_i = act_f(vrow[i]);
             float o;
             if constexpr (KDA) o = delta_row_step<V>(s[r], kq, v_i, beta);
             else o = row_step<V>(s[r], kq, v_i, alpha, beta);
@@ -517,15 +520,22 @@ static cudaError_t launch_conv_decode_t(const ConvDecodeParams& p, cudaStream_t 
                                 (KIND == 2 ? (size_t)p.T * p.group * 8 : 0)) +
                         (prefetch ? conv_decode_prefetch_bytes<DK, R>() : 0);
     // above 48 KB the kernel's dynamic shared memory must be opted into (to
-    // what this launch needs: the opt-in limit counts its static memory too)
-    static size_t opted[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (smem > 48 * 1024 && dev >= 0 && dev < 64 && smem > opted[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(gdn_conv_decode_kernel<DK, R, KIND>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // what this launch needs: the opt-in limit counts its static memory too);
+    // the per-device record of what was opted into is shared by host threads
+    if (smem > 48 * 1024) {
+        static std::mutex mu;
+        static size_t opted[64] = {};
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
-        opted[dev] = smem;
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        std::lock_guard<std::mutex> lock(mu);
+        if (smem > opted[dev]) {
+            e = cudaFuncSetAttribute(gdn_conv_decode_kernel<DK, R, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem);
+            if (e != cudaSuccess) return e;
+            opted[dev] = smem;
+        }
     }
     // a programmatic dependent launch (see the kernel): consecutive layer
     // steps overlap one's start with the other's drain
@@ -589,35 +599,37 @@ cudaError_t launch_gates(const GatesParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <int DK, int R, bool GATHER, bool KDA>
+template <int DK, int R, bool GATHER, bool KDA, typename In>
 static cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
     dim3 grid(p.dv / (kRowsPerPass * R), p.Hv, p.B);
-    gdn_decode_kernel<DK, R, GATHER, KDA><<<grid, kThreads, 0, s>>>(p);
+    gdn_decode_kernel<DK, R, GATHER, KDA, In><<<grid, kThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 
-template <int DK, bool GATHER, bool KDA>
+template <int DK, bool GATHER, bool KDA, typename In>
 static cudaError_t launch_decode_r(const DecodeParams& p, int rows_per_cta, cudaStream_t s) {
     switch (rows_per_cta) {
-        case 32: return launch_decode_t<DK, 1, GATHER, KDA>(p, s);
-        case 64: return launch_decode_t<DK, 2, GATHER, KDA>(p, s);
-        case 128: return launch_decode_t<DK, 4, GATHER, KDA>(p, s);
+        case 32: return launch_decode_t<DK, 1, GATHER, KDA, In>(p, s);
+        case 64: return launch_decode_t<DK, 2, GATHER, KDA, In>(p, s);
+        case 128: return launch_decode_t<DK, 4, GATHER, KDA, In>(p, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
-template <bool GATHER, bool KDA>
+template <bool GATHER, bool KDA, typename In = uint16_t>
 static cudaError_t launch_decode_k(const DecodeParams& p, int dk, int rows_per_cta, cudaStream_t s) {
     switch (dk) {
-        case 32: return launch_decode_r<32, GATHER, KDA>(p, rows_per_cta, s);
-        case 64: return launch_decode_r<64, GATHER, KDA>(p, rows_per_cta, s);
-        case 128: return launch_decode_r<128, GATHER, KDA>(p, rows_per_cta, s);
+        case 32: return launch_decode_r<32, GATHER, KDA, In>(p, rows_per_cta, s);
+        case 64: return launch_decode_r<64, GATHER, KDA, In>(p, rows_per_cta, s);
+        case 128: return launch_decode_r<128, GATHER, KDA, In>(p, rows_per_cta, s);
     }
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int gather, bool kda,
+cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int gather, bool kda, bool in_f32,
                           cudaStream_t s) {
+    // fp32 activations: the plain step only (the host refuses other combinations)
+    if (in_f32) return (gather || kda) ? cudaErrorInvalidValue : launch_decode_k<false, false, float>(p, dk, rows_per_cta, s);
     // commit (gather) replays short paths: one row pass per CTA keeps the grid wide
     if (gather) return kda ? launch_decode_k<true, true>(p, dk, rows_per_cta, s)
                            : launch_decode_k<true, false>(p, dk, rows_per_cta, s);
@@ -629,18 +641,21 @@ template <int DK, int MB, int R>
 static cudaError_t launch_tree_t(const TreeParamsT<MB>& p, cudaStream_t s) {
     constexpr int ROWS = kRowsPerPass * R;
     const size_t smem = (size_t)p.n_slots * ROWS * DK * sizeof(float) + tree_stage_bytes<DK, R>(p.Nmax);
-    static bool configured[64] = {};
+    // the shared-memory opt-in, once per device whatever the host threads
+    static std::once_flag once[64];
+    static cudaError_t setup_err[64];
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::call_once(once[dev], [dev] {
         const int max_smem = std::min(GDN_MAX_TREE_SLOTS * ROWS * DK * (int)sizeof(float) +
                                           (int)tree_stage_bytes<DK, R>(GDN_MAX_TREE_NODES),
                                       kMaxSmemPerCta);
-        cudaError_t e = cudaFuncSetAttribute(gdn_tree_kernel<DK, MB, R>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-        if (e != cudaSuccess) return e;
-        configured[dev] = true;
-    }
+        setup_err[dev] = cudaFuncSetAttribute(gdn_tree_kernel<DK, MB, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              max_smem);
+    });
+    if (setup_err[dev] != cudaSuccess) return setup_err[dev];
     dim3 grid(p.dv / ROWS, p.Hv, p.B);
     gdn_tree_kernel<DK, MB, R><<<grid, kThreads, smem, s>>>(p);
     return cudaGetLastError();

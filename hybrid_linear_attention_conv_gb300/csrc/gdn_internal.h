@@ -13,7 +13,7 @@ namespace gdn {
 // Decode / commit: T sequential tokens per sequence, optionally gathered
 // through an index map (commit replays a tree path).
 struct DecodeParams {
-    const uint16_t* qkv;   // bf16 [B, Tsrc, C]
+    const uint16_t* qkv;   // bf16 [B, Tsrc, C] (fp32 for the fp32-activation step, cast by the kernel)
     const float* alpha;    // [B, Tsrc, Hv], or [B, Tsrc, Hv, dk] for KDA
     const float* beta;     // [B, Tsrc, Hv]
     float* state;          // [B, Hv, dv, dk]
@@ -55,10 +55,12 @@ using TreeParams = TreeParamsT<1>;
 using TreeParamsBatch = TreeParamsT<kMaxTreeBatch>;
 
 struct ConvParams {
-    const uint16_t* x;     // [B, T, C]
-    const uint16_t* w;     // [C, 4]
-    uint16_t* tail;        // [B, 4, C]
-    uint16_t* y;           // [B, T, C]
+    // bf16 bits, or fp32 for the fp32-activation conv (f32 = 1; cast by the kernel)
+    const void* x;         // [B, T, C]
+    const void* w;         // [C, 4]
+    void* tail;            // [B, 4, C]
+    void* y;               // [B, T, C]
+    int f32;
     int B, T, C;
     int tree;              // 0: linear run, 1: tree (ancestor table below)
     // tree mode: for node n, source of its m-th earlier input (m = 1..3):
@@ -129,7 +131,8 @@ int device_sm_count();                                        // SMs of the curr
 
 // Launchers (return the cudaError_t of the launch).
 // kda: a decay per key channel (alpha [.., Hv, dk]) instead of one per head.
-cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int gather, bool kda,
+// in_f32: the activations (qkv) are fp32 instead of bf16 (plain step only).
+cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int gather, bool kda, bool in_f32,
                           cudaStream_t s);
 template <int MB>
 cudaError_t launch_tree(const TreeParamsT<MB>& p, int dk, cudaStream_t s);

@@ -58,6 +58,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <mutex>
 
@@ -102,7 +103,12 @@ constexpr uint32_t COL_U = 256;   // U^T [i][t]               64 columns
 constexpr uint32_t COL_G = 320;   // [K;Q] K^T [t'][s]        64 columns
 constexpr uint32_t kTmemCols = 512;
 
-constexpr uint64_t kWaitLimitNs = 200000000ull;  // 0.2 s per tensor-core batch
+// Bounded waits.  A wait for the tensor cores, a copy or another CTA's record
+// gives up after PrefillParams::wait_ns (0.2 s unless the caller set another
+// limit; 0 gives up at the first empty probe).  After a wait gave up, the
+// kernel still lets the work it started finish before it frees tensor memory
+// or exits (the drain), with this fixed limit.
+constexpr uint64_t kDrainLimitNs = 200000000ull;
 
 // Kernel parameters.  The two tensor maps describe the packed q/k/v rows
 // [T][C] (bf16) for the chain's TMA loads: 64 x 64 boxes with the 128-byte
@@ -117,6 +123,7 @@ struct PrefillParams {
     float* state;
     void* out;
     int* status;
+    uint64_t wait_ns;   // limit of each bounded wait (see kDrainLimitNs)
     int* ready;         // per (chunk, value head): 1 once the pre-pass record is written (cooperative form)
     int n_workers;      // pre-pass worker CTAs of the cooperative form
     int T, Hk, Hv, C, group;
@@ -405,9 +412,13 @@ __device__ bool prep_item(const PrefillParams& p, uint8_t* sm, uint32_t tmem, ui
     const int n = min(kChunk, p.T - t0);
     const size_t C = (size_t)p.C;
     const uint32_t bar_g = bars, bar_w = bars + 8;
-    // a bounded wait for the next phase of one of the two barriers
+    // a bounded wait for the next phase of one of the two barriers; if it gives
+    // up, the MMAs are still let finish (drain) before TMEM is reused or freed
     auto wait_mma = [&](uint32_t b, uint32_t ph) {
-        if (!mbar_wait(b, ph & 1u, kWaitLimitNs)) atomicOr(abort_flag, 1);
+        if (!mbar_wait(b, ph & 1u, p.wait_ns)) {
+            atomicOr(abort_flag, 1);
+            mbar_wait(b, ph & 1u, kDrainLimitNs);
+        }
     };
 
     // [K;Q] rows of the chunk (zero-filled past the last token)
@@ -660,13 +671,14 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
     uint32_t parity = 0, parity_g = 0;
 
     // wait for the tensor cores; on a timeout every thread leaves the chunk loop
+    // with the same phase kept (every thread's), to drain it below
     auto wait_on = [&](uint32_t b, uint32_t& par) -> bool {
-        const bool ok = mbar_wait(b, par, kWaitLimitNs);
-        if (ok) par ^= 1u;  // on a timeout keep the phase, to drain it below
-        else atomicOr(abort_flag, 1);
+        if (!mbar_wait(b, par, p.wait_ns)) atomicOr(abort_flag, 1);
         __syncthreads();
         fence_after_sync();
-        return *abort_flag == 0;
+        if (*abort_flag != 0) return false;
+        par ^= 1u;
+        return true;
     };
 
     // ---- prologue: state row i -> TMEM lane i and the bf16 hi/lo operand tiles
@@ -947,8 +959,9 @@ gdn_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
     cp_async_wait_all();  // no prefetch may still be writing shared memory at exit
     if (*abort_flag != 0) {
         if (tid == 0) atomicExch(p.status, 1);
-        // give in-flight tensor-core work one more bounded chance to drain
-        mbar_wait(bar, parity, kWaitLimitNs);
+        // let in-flight tensor-core work drain (the last commit covers every
+        // MMA issued before it) before TMEM is freed
+        mbar_wait(bar, parity, kDrainLimitNs);
     }
     fence_before_sync();
     __syncthreads();
@@ -1010,14 +1023,15 @@ constexpr uint32_t T_D = 128;    // [S K^T | S Q^T -> O^T] [i][t], 2 x 128 (by c
 constexpr uint32_t T_SH = 384;   // S hi (the next chunk's operand)        64
 constexpr uint32_t T_XA = 448;   // X^T                    hi 32 + lo 32  64
 
-// Wait (bounded) until ready flag `item` (chunk * Hv + value head) is set.
-__device__ __forceinline__ bool wait_ready(const int* ready, int item) {
+// Wait (bounded by limit_ns) until ready flag `item` (chunk * Hv + value
+// head) is set.
+__device__ __forceinline__ bool wait_ready(const int* ready, int item, uint64_t limit_ns) {
     const uint64_t t0 = global_ns();
     while (true) {
         int v;
         asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ready + item) : "memory");
         if (v != 0) return true;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 >= limit_ns) return false;
         __nanosleep(100);
     }
 }
@@ -1072,7 +1086,7 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
     // chunk); a timeout only raises the flag, which every thread checks at the
     // end of the chunk, so no thread leaves a barrier the others still reach
     auto wait_mma = [&](uint32_t b, int chunk) {
-        if (!mbar_wait(b, (uint32_t)chunk & 1u, kWaitLimitNs)) atomicOr(abort_flag, 1);
+        if (!mbar_wait(b, (uint32_t)chunk & 1u, p.wait_ns)) atomicOr(abort_flag, 1);
         __syncwarp();  // the tcgen05.ld that follow are warp-collective
         fence_after_sync();
     };
@@ -1115,11 +1129,11 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
         const int t0 = cc * kChunk;
         // the record's ready flag first (no buffer needed for that)
         int ok = 1;
-        if (READY && lane == 0) ok = wait_ready(p.ready, cc * p.Hv + h);
+        if (READY && lane == 0) ok = wait_ready(p.ready, cc * p.Hv + h, p.wait_ns);
         if (__shfl_sync(0xffffffffu, ok, 0) == 0) return false;
         if (cc >= 2) {
             if (lane == 0)
-                ok = mbar_wait(bar_free0 + 8u * (uint32_t)(cc & 1), (uint32_t)((cc - 2) >> 1) & 1u, kWaitLimitNs);
+                ok = mbar_wait(bar_free0 + 8u * (uint32_t)(cc & 1), (uint32_t)((cc - 2) >> 1) & 1u, p.wait_ns);
             if (__shfl_sync(0xffffffffu, ok, 0) == 0) return false;
         }
         in_last = cc;
@@ -1146,7 +1160,7 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
     // every thread that reads a buffer waits for its phase (chunk cc is the
     // (cc >> 1)-th use of buffer cc & 1)
     auto wait_inputs = [&](int cc) {
-        if (!mbar_wait(bar_in0 + 8u * (uint32_t)(cc & 1), (uint32_t)(cc >> 1) & 1u, kWaitLimitNs))
+        if (!mbar_wait(bar_in0 + 8u * (uint32_t)(cc & 1), (uint32_t)(cc >> 1) & 1u, p.wait_ns))
             atomicOr(abort_flag, 1);
     };
 
@@ -1200,7 +1214,7 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
         // last requested phase of each input buffer
         if (lane == 0)
             for (int cc = in_last; cc >= 0 && cc > in_last - 2; --cc)
-                if (!mbar_wait(bar_in0 + 8u * (uint32_t)(cc & 1), (uint32_t)(cc >> 1) & 1u, kWaitLimitNs))
+                if (!mbar_wait(bar_in0 + 8u * (uint32_t)(cc & 1), (uint32_t)(cc >> 1) & 1u, kDrainLimitNs))
                     *copy_fail = 1;
     } else {
         // the first chunk's MMAs read the operands of the prologue (later chunks'
@@ -1294,7 +1308,7 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
 
             // ---- G: S += X^T W (3 passes); then O^T += X^T PT^T (3 passes)
             if (issuer) {
-                if (!mbar_wait(bar_x, (uint32_t)c & 1u, kWaitLimitNs)) atomicOr(abort_flag, 1);
+                if (!mbar_wait(bar_x, (uint32_t)c & 1u, p.wait_ns)) atomicOr(abort_flag, 1);
                 fence_after_sync();
                 constexpr uint32_t id_s = idesc_bf16(128, 128);
                 constexpr uint32_t id_o = idesc_bf16(128, 64);
@@ -1306,7 +1320,7 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
                                     d_rec + (pass == 1 ? kWLo : kWHi) + 16 * ks, id_s, 1u);
                 mma_commit(bar_s);
                 // the output MMAs accumulate onto S Q^T once every epilogue warp has scaled its part
-                if (!mbar_wait(bar_qs, (uint32_t)c & 1u, kWaitLimitNs)) atomicOr(abort_flag, 1);
+                if (!mbar_wait(bar_qs, (uint32_t)c & 1u, p.wait_ns)) atomicOr(abort_flag, 1);
                 fence_after_sync();
 #pragma unroll
                 for (int pass = 0; pass < 3; ++pass)  // (X hi, PT hi), (X hi, PT lo), (X lo, PT hi)
@@ -1377,7 +1391,7 @@ __device__ __forceinline__ void chain_body(const PrefillParams& p, uint8_t* sm, 
         fence_after_sync();
         mma_commit(bar_fin);
     }
-    if (!mbar_wait(bar_fin, 0, kWaitLimitNs)) atomicOr(abort_flag, 1);
+    if (!mbar_wait(bar_fin, 0, kDrainLimitNs)) atomicOr(abort_flag, 1);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -1477,11 +1491,41 @@ int launch_prefill(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const
 // bytes of the ready flags (one int32 per chunk and key head), padded to 16
 size_t ready_bytes(size_t nchunks, int Hv) { return (nchunks * (size_t)Hv * 4 + 15) / 16 * 16; }
 constexpr int kMinWorkers = 8;  // fewest pre-pass workers worth a cooperative launch
-// CTAs of the cooperative kernel the device holds at once (0: no cooperative launch)
-int fused_capacity(int dev);
+
+// Limit of each bounded device wait of the prefill kernels, read at every launch.
+constexpr uint64_t kDefaultWaitNs = 200000000ull;   // 0.2 s
+constexpr uint64_t kMaxWaitNs = 10000000000ull;     // 10 s
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+
+// Copy a prefill status word (int32 in device memory) to the host once the
+// stream has reached it: GDN_OK (0), GDN_ERR_TIMEOUT (non-zero) or GDN_ERR_CUDA.
+int read_status_word(const void* word, void* stream, int32_t* status) {
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, word, sizeof v, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_error(e, "reading the prefill status word");
+    if (status != nullptr) *status = v;
+    if (v != 0)
+        return report_error(GDN_ERR_TIMEOUT, "a bounded device wait of the prefill gave up (status %d): its outputs "
+                            "and state are not valid", v);
+    return GDN_OK;
+}
 }  // namespace
 
 extern "C" {
+
+uint64_t gdn_set_wait_limit_ns(uint64_t ns) {
+    if (ns > kMaxWaitNs) ns = kMaxWaitNs;
+    return g_wait_ns.exchange(ns);
+}
+
+int gdn_prefill_status(const void* workspace, void* stream, int32_t* status) {
+    if (workspace == nullptr) return report_error(GDN_ERR_INVALID_ARG, "workspace is NULL");
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return report_error(GDN_ERR_MISALIGNED, "workspace (%p) is not 256-byte aligned", workspace);
+    return read_status_word(workspace, stream, status);
+}
 
 size_t gdn_prefill_workspace_bytes(const gdn_shape* shape, int32_t T, int32_t chunk) {
     if (shape == nullptr || T < 0 || chunk != kChunk) return 0;
@@ -1554,38 +1598,23 @@ bool encode_qkv_maps(PrefillParams& p, const void* qkv, int T, int C) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int fused_capacity(int dev) {
-    static int cached[64];
-    static bool known[64];
-    if (dev < 0 || dev >= 64) return 0;
-    if (!known[dev]) {
-        int coop = 0, sms = 0, per_sm = 0;
-        if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess) coop = 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gdn_prefill_fused_kernel, kChainThreads,
-                                                          kChainSmem) != cudaSuccess)
-            per_sm = 0;
-        (void)cudaGetLastError();
-        cached[dev] = coop ? sms * per_sm : 0;
-        known[dev] = true;
-    }
-    return cached[dev];
-}
+// Per-device set-up of the prefill kernels, done once per device (with that
+// device current) however many host threads make their first call at once:
+// the shared-memory opt-ins, then the number of cooperative-kernel CTAs the
+// device holds at once (0: no cooperative launch).
+struct PrefillDevice {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    int capacity = 0;
+};
+PrefillDevice g_prefill_dev[64];
 
-// The chunk-form launch(es): with `prep`, the pre-pass and the chain reading
-// its records (the workspace holds them), as one cooperative kernel where the
-// device allows it; without, the self-contained chain (the workspace holds
-// only the status word).
-int launch_prefill(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const float* alpha, const float* beta,
-                   float* state, void* out, void* workspace, float q_scale, uint32_t flags, cudaStream_t st,
-                   bool prep) {
-    static bool configured[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaError_t e;
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
-        e = cudaFuncSetAttribute(gdn_prefill_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kChainSmem);
+const PrefillDevice* prefill_device(int dev) {
+    if (dev < 0 || dev >= 64) return nullptr;
+    PrefillDevice& d = g_prefill_dev[dev];
+    std::call_once(d.once, [&d, dev] {
+        cudaError_t e = cudaFuncSetAttribute(gdn_prefill_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kChainSmem);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(gdn_prefill_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kChainSmem);
@@ -1595,9 +1624,33 @@ int launch_prefill(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(gdn_prefill_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kPrepSmem);
-        if (e != cudaSuccess) return cuda_error(e, "prefill smem attribute");
-        configured[dev] = true;
-    }
+        d.err = e;
+        if (e != cudaSuccess) return;
+        int coop = 0, sms = 0, per_sm = 0;
+        if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess) coop = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gdn_prefill_fused_kernel, kChainThreads,
+                                                          kChainSmem) != cudaSuccess)
+            per_sm = 0;
+        (void)cudaGetLastError();
+        d.capacity = coop ? sms * per_sm : 0;
+    });
+    return &d;
+}
+
+// The chunk-form launch(es): with `prep`, the pre-pass and the chain reading
+// its records (the workspace holds them), as one cooperative kernel where the
+// device allows it; without, the self-contained chain (the workspace holds
+// only the status word).
+int launch_prefill(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const float* alpha, const float* beta,
+                   float* state, void* out, void* workspace, float q_scale, uint32_t flags, cudaStream_t st,
+                   bool prep) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_error(e, "prefill device");
+    const PrefillDevice* pd = prefill_device(dev);
+    if (pd == nullptr) return report_error(GDN_ERR_CUDA, "device %d outside the 64 this library tracks", dev);
+    if (pd->err != cudaSuccess) return cuda_error(pd->err, "prefill smem attribute");
     PrefillParams p{};
     p.qkv = qkv;
     p.alpha = alpha;
@@ -1605,6 +1658,7 @@ int launch_prefill(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const
     p.state = state;
     p.out = out;
     p.status = static_cast<int*>(workspace);
+    p.wait_ns = g_wait_ns.load();
     p.T = T;
     p.Hk = shape->Hk;
     p.Hv = shape->Hv;
@@ -1622,7 +1676,7 @@ int launch_prefill(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv, const
         // The cooperative form when the GPU holds a chain CTA per value head
         // and at least a few pre-pass workers at once; otherwise the pre-pass
         // over all chunks, then the chain.
-        const int resident = fused_capacity(dev);
+        const int resident = pd->capacity;
         const int items = shape->Hv + (nchunks - 1) * shape->Hk;  // chunk 0 per value head, then per key head
         const int workers = std::min(resident - shape->Hv, items);
         if (workers >= kMinWorkers && (flags & GDN_PREFILL_TWO_LAUNCH) == 0) {
@@ -1684,6 +1738,13 @@ cudaError_t noalloc_scratch(void** ptr) {
 }
 
 }  // namespace
+
+extern "C" int gdn_chunk_prefill_noalloc_status(void* stream, int32_t* status) {
+    void* scratch = nullptr;
+    cudaError_t e = noalloc_scratch(&scratch);
+    if (e != cudaSuccess) return cuda_error(e, "locating the built-in prefill scratch");
+    return read_status_word(scratch, stream, status);
+}
 
 extern "C" int gdn_chunk_prefill_noalloc(const gdn_shape* shape, int32_t T, int32_t chunk, const gdn_bf16* qkv,
                                          const float* alpha, const float* beta, float* state, void* out,

@@ -39,6 +39,10 @@ __device__ __forceinline__ float group_sum8(float x) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// One activation as fp32: a bf16 bit pattern widened exactly, or an fp32 value.
+__device__ __forceinline__ float act_f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+__device__ __forceinline__ float act_f(float f) { return f; }
+
 // This lane's V*4 elements of a dk-long bf16 head vector.
 template <int V>
 __device__ __forceinline__ void load_head_vec(const uint16_t* head, int lane8, float (&x)[V][4]) {
@@ -49,6 +53,19 @@ __device__ __forceinline__ void load_head_vec(const uint16_t* head, int lane8, f
         x[m][1] = bf16_hi(raw.x);
         x[m][2] = bf16_lo(raw.y);
         x[m][3] = bf16_hi(raw.y);
+    }
+}
+
+// The same for an fp32 head vector (the fp32-activation decode).
+template <int V>
+__device__ __forceinline__ void load_head_vec(const float* head, int lane8, float (&x)[V][4]) {
+#pragma unroll
+    for (int m = 0; m < V; ++m) {
+        const float4 f = *reinterpret_cast<const float4*>(head + 32 * m + 4 * lane8);
+        x[m][0] = f.x;
+        x[m][1] = f.y;
+        x[m][2] = f.z;
+        x[m][3] = f.w;
     }
 }
 
@@ -115,8 +132,8 @@ struct TokenKQ {
     float kq;
 };
 
-template <int V>
-__device__ __forceinline__ void token_kq(const uint16_t* q_head, const uint16_t* k_head,
+template <int V, typename In>
+__device__ __forceinline__ void token_kq(const In* q_head, const In* k_head,
                                          int lane8, float q_scale, bool normalize,
                                          TokenKQ<V>& t) {
     load_head_vec<V>(k_head, lane8, t.k);

@@ -162,10 +162,25 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// One probe that never suspends the thread: true if phase `parity` of `bar`
+// has already completed.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for phase `parity` of `bar` to complete; give up after `limit_ns`.  The
 // clock is read only once the first try has come back empty (reading it costs
-// more than a try on a completed phase).
+// more than a try on a completed phase).  A limit of 0 gives up at once unless
+// the phase has already completed (one probe, no suspension).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (limit_ns == 0) return mbar_test(bar, parity);
     if (mbar_try(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     while (true) {

@@ -24,6 +24,7 @@ GDN_MAX_TREE_SLOTS = 8
 GDN_NORMALIZE_QK = 0x1
 GDN_OUT_BF16 = 0x2
 GDN_PREFILL_TWO_LAUNCH = 0x4
+GDN_IN_F32 = 0x8
 
 STATUS = {
     0: "GDN_OK",
@@ -56,7 +57,10 @@ EXPORTS = [
     "gdn_commit_path",
     "gdn_prefill_workspace_bytes",
     "gdn_chunk_prefill",
+    "gdn_prefill_status",
+    "gdn_set_wait_limit_ns",
     "gdn_chunk_prefill_noalloc",
+    "gdn_chunk_prefill_noalloc_status",
     "gdn_snapshot_bytes",
     "gdn_snapshot_signature",
     "gdn_snapshot_save",
@@ -111,7 +115,10 @@ def load(path: str = LIB_PATH):
             "gdn_commit_path": (ctypes.c_int, [SH, I32, P, P, I32, P, P, P, P, P, P, U32, P]),
             "gdn_prefill_workspace_bytes": (SZ, [SH, I32, I32]),
             "gdn_chunk_prefill": (ctypes.c_int, [SH, I32, I32, P, P, P, P, P, P, SZ, F, U32, P]),
+            "gdn_prefill_status": (ctypes.c_int, [P, P, ctypes.POINTER(I32)]),
+            "gdn_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
             "gdn_chunk_prefill_noalloc": (ctypes.c_int, [SH, I32, I32, P, P, P, P, P, F, U32, P]),
+            "gdn_chunk_prefill_noalloc_status": (ctypes.c_int, [P, ctypes.POINTER(I32)]),
             "gdn_snapshot_bytes": (SZ, [SH, I32]),
             "gdn_snapshot_signature": (ctypes.c_uint64, [SH, I32]),
             "gdn_snapshot_save": (ctypes.c_int, [SH, I32, I32, P, I64, P, I64, P, SZ, P, SZ, P]),
@@ -196,15 +203,18 @@ def tree_root_path(parents, node: int) -> np.ndarray:
 
 def conv_step(x: torch.Tensor, w: torch.Tensor, tail: torch.Tensor, y: torch.Tensor | None = None,
               parents=None) -> torch.Tensor:
-    """x bf16 [B,T,C], w bf16 [C,4], tail bf16 [B,4,C] (updated in place in linear mode)."""
+    """x bf16 [B,T,C], w bf16 [C,4], tail bf16 [B,4,C] (updated in place in linear mode).
+    With fp32 x, every tensor is fp32 (GDN_IN_F32: y is not rounded to bf16)."""
     B, T, C = x.shape
+    dt = torch.float32 if x.dtype == torch.float32 else torch.bfloat16
     if y is None:
         y = torch.empty_like(x)
     par, pp = _host_i32(parents, "parents")
-    rc = load().gdn_conv_step(B, T, C, pp, _dev(x, torch.bfloat16, "x"),
-                              _dev(w, torch.bfloat16, "w", (C, GDN_CONV_W)),
-                              _dev(tail, torch.bfloat16, "tail", (B, GDN_CONV_W, C)),
-                              _dev(y, torch.bfloat16, "y", (B, T, C)), 0, _stream())
+    rc = load().gdn_conv_step(B, T, C, pp, _dev(x, dt, "x"),
+                              _dev(w, dt, "w", (C, GDN_CONV_W)),
+                              _dev(tail, dt, "tail", (B, GDN_CONV_W, C)),
+                              _dev(y, dt, "y", (B, T, C)), GDN_IN_F32 if dt == torch.float32 else 0,
+                              _stream())
     _check(rc, "gdn_conv_step")
     return y
 
@@ -215,20 +225,24 @@ def _decode(fn, qkv, alpha, beta, state, Hk, Hv, dk, dv, out, q_scale, normalize
         out = torch.empty((B, T, Hv, dv), dtype=torch.bfloat16 if out_bf16 else torch.float32,
                           device=qkv.device)
     sh = _shape(B, Hk, Hv, dk, dv)
+    in_f32 = qkv.dtype == torch.float32  # GDN_IN_F32 (the library refuses it where unsupported)
     rc = getattr(load(), fn)(ctypes.byref(sh), T,
-                             _dev(qkv, torch.bfloat16, "qkv", (B, T, packed_channels(Hk, Hv, dk, dv))),
+                             _dev(qkv, torch.float32 if in_f32 else torch.bfloat16, "qkv",
+                                  (B, T, packed_channels(Hk, Hv, dk, dv))),
                              _dev(alpha, torch.float32, "alpha", gate_shape(B, T)),
                              _dev(beta, torch.float32, "beta", (B, T, Hv)),
                              _dev(state, torch.float32, "state", (B, Hv, dv, dk)),
                              _dev(out, torch.bfloat16 if out_bf16 else torch.float32, "out", (B, T, Hv, dv)),
-                             float(q_scale), _flags(normalize, out_bf16), _stream())
+                             float(q_scale), _flags(normalize, out_bf16) | (GDN_IN_F32 if in_f32 else 0),
+                             _stream())
     _check(rc, fn)
     return out
 
 
 def decode_step(qkv, alpha, beta, state, Hk, Hv, dk, dv, out=None, q_scale=1.0, normalize=True,
                 out_bf16=False) -> torch.Tensor:
-    """qkv bf16 [B,T,C], alpha/beta fp32 [B,T,Hv], state fp32 [B,Hv,dv,dk] (in place)."""
+    """qkv bf16 [B,T,C] (or fp32: GDN_IN_F32), alpha/beta fp32 [B,T,Hv], state fp32
+    [B,Hv,dv,dk] (in place)."""
     return _decode("gdn_decode_step", qkv, alpha, beta, state, Hk, Hv, dk, dv, out, q_scale, normalize,
                    out_bf16, lambda B, T: (B, T, Hv))
 
@@ -407,6 +421,53 @@ def chunk_prefill(qkv, alpha, beta, state, Hk, Hv, dk, dv, out=None, workspace=N
                                   _stream())
     _check(rc, "gdn_chunk_prefill")
     return out
+
+
+def prefill_status(workspace: torch.Tensor) -> int:
+    """Synchronise the current stream and return the status word of the last
+    gdn_chunk_prefill call that used `workspace` (0: the results are valid;
+    non-zero: a bounded device wait gave up)."""
+    st = ctypes.c_int32(0)
+    rc = load().gdn_prefill_status(_dev(workspace, torch.uint8, "workspace"), _stream(), ctypes.byref(st))
+    if rc not in (0, -8):
+        _check(rc, "gdn_prefill_status")
+    return int(st.value)
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    """Limit of every bounded device wait of the prefill kernels (process-wide,
+    read at each later launch); returns the previous limit."""
+    return int(load().gdn_set_wait_limit_ns(int(ns)))
+
+
+def chunk_prefill_noalloc(qkv, alpha, beta, state, Hk, Hv, dk, dv, out=None, chunk=64, q_scale=1.0,
+                          normalize=True, out_bf16=False) -> torch.Tensor:
+    """gdn_chunk_prefill_noalloc: chunk_prefill without a workspace (its
+    scratch lives in the library).  Same arguments and layouts."""
+    T = qkv.shape[0]
+    if out is None:
+        out = torch.empty((T, Hv, dv), dtype=torch.bfloat16 if out_bf16 else torch.float32, device=qkv.device)
+    sh = _shape(1, Hk, Hv, dk, dv)
+    rc = load().gdn_chunk_prefill_noalloc(ctypes.byref(sh), T, int(chunk),
+                                          _dev(qkv, torch.bfloat16, "qkv", (T, packed_channels(Hk, Hv, dk, dv))),
+                                          _dev(alpha, torch.float32, "alpha", (T, Hv)),
+                                          _dev(beta, torch.float32, "beta", (T, Hv)),
+                                          _dev(state, torch.float32, "state", (Hv, dv, dk)),
+                                          _dev(out, torch.bfloat16 if out_bf16 else torch.float32, "out",
+                                               (T, Hv, dv)),
+                                          float(q_scale), _flags(normalize, out_bf16), _stream())
+    _check(rc, "gdn_chunk_prefill_noalloc")
+    return out
+
+
+def chunk_prefill_noalloc_status() -> int:
+    """Synchronise the current stream and return the status word the last
+    gdn_chunk_prefill_noalloc call on this device left (0: valid results)."""
+    st = ctypes.c_int32(0)
+    rc = load().gdn_chunk_prefill_noalloc_status(_stream(), ctypes.byref(st))
+    if rc not in (0, -8):
+        _check(rc, "gdn_chunk_prefill_noalloc_status")
+    return int(st.value)
 
 
 # ---------------------------------------------------------------------------

@@ -149,6 +149,23 @@ def conv_inputs(seed: int, B: int, T: int, C: int, tag: str = "conv", zero_tail:
     return {"x": x, "w": w, "tail": tail}
 
 
+def decode_inputs_f32(seed: int, shape: Shape, T: int, tag: str = "decode_f32") -> dict:
+    """As decode_inputs, with the packed activations qkv [B,T,C] drawn and kept
+    in fp32 (~N(0, 1), never rounded to bf16)."""
+    d = decode_inputs(seed, shape, T, tag=tag)
+    d["qkv"] = normal_f32(seed, tag + ".qkv32", (shape.B, T, shape.C))
+    return d
+
+
+def conv_inputs_f32(seed: int, B: int, T: int, C: int, tag: str = "conv_f32", zero_tail: bool = True) -> dict:
+    """Pre-conv x fp32 [B,T,C] ~ N(0, 1), taps w fp32 [C,4] ~ N(0, 0.5^2), tail
+    fp32 [B,4,C] (zeros: the start of a sequence, unless zero_tail is False)."""
+    x = normal_f32(seed, tag + ".x", (B, T, C))
+    w = normal_f32(seed, tag + ".w", (C, CONV_W), 0.5)
+    tail = np.zeros((B, CONV_W, C), np.float32) if zero_tail else normal_f32(seed, tag + ".tail", (B, CONV_W, C))
+    return {"x": x, "w": w, "tail": tail}
+
+
 def random_tree(seed: int, N: int = 32, max_depth: int = 8, branch=(1, 4)) -> np.ndarray:
     """Draft-tree parent array: node 0 is the root (parent -1); nodes are added
     in breadth-first order, each visited node drawing U{branch} children, never

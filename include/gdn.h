@@ -98,6 +98,11 @@ typedef enum gdn_status {
  * as two launches, even where one cooperative launch would fit (the results
  * are the same bits; for comparisons).  Other entry points refuse it. */
 #define GDN_PREFILL_TWO_LAUNCH 0x4u
+/* gdn_conv_step and gdn_decode_step only: the activations are fp32 instead
+ * of bf16 (conv: x, w, tail and y; decode: qkv), for inputs drawn or kept in
+ * fp32.  The arithmetic is the same; nothing is rounded to bf16 on the way.
+ * Other entry points refuse it. */
+#define GDN_IN_F32 0x8u
 
 /* ABI version of the loaded library (GDN_ABI_VERSION it was built with). */
 int gdn_abi_version(void);
@@ -129,12 +134,15 @@ int gdn_tree_root_path(int32_t N, const int32_t* parents, int32_t node, int32_t*
  *   tail      bf16 [B, 4, C]  the last four inputs, oldest first (in/out in
  *                             linear mode, read-only in tree mode).
  *   y         bf16 [B, T, C]  output (fp32 math, rounded to nearest even).
+ *   flags     0, or GDN_IN_F32: x, w, tail and y are all fp32 (y not rounded).
+ * The conv takes its sizes as (B, T, C) rather than a gdn_shape: it is a
+ * per-channel operation, and C need not be a packed q/k/v row (C % 8 == 0).
  * Source: the per-layer 4-wide convolution tail, "Architecture" (v0.14.2)
  * section 8.1; short convolution rings carried between steps, "Serving A
  * Research Architecture On CPU" (engine design).
  */
 int gdn_conv_step(int32_t B, int32_t T, int32_t C, const int32_t* parents,
-                  const gdn_bf16* x, const gdn_bf16* w, gdn_bf16* tail, gdn_bf16* y,
+                  const void* x, const void* w, void* tail, void* y,
                   uint32_t flags, void* stream);
 
 /*
@@ -143,14 +151,15 @@ int gdn_conv_step(int32_t B, int32_t T, int32_t C, const int32_t* parents,
  *   q^ = q_scale * q / |q|,  k^ = k / |k|   (if GDN_NORMALIZE_QK),
  *   S_h <- alpha S_h (I - beta k^ k^T) + beta v k^T,   out = S_h q^.
  * The state is read from HBM once and written once per call, whatever T.
- *   qkv     bf16 [B, T, C_qkv]   packed post-conv activations.
+ *   qkv     bf16 [B, T, C_qkv]   packed post-conv activations (fp32 with
+ *                                GDN_IN_F32).
  *   alpha   fp32 [B, T, Hv]      decay, beta fp32 [B, T, Hv] write strength.
  *   state   fp32 [B, Hv, dv, dk] in/out.
  *   out     [B, T, Hv, dv] fp32, or bf16 with GDN_OUT_BF16; may be NULL.
  * Source: "Architecture" (v0.11.1) "The parts" (one token, a block);
  * "Architecture" (v0.14.2) section 8.3 (decode without speculation).
  */
-int gdn_decode_step(const gdn_shape* shape, int32_t T, const gdn_bf16* qkv,
+int gdn_decode_step(const gdn_shape* shape, int32_t T, const void* qkv,
                     const float* alpha, const float* beta, float* state, void* out,
                     float q_scale, uint32_t flags, void* stream);
 
@@ -329,9 +338,9 @@ size_t gdn_prefill_workspace_bytes(const gdn_shape* shape, int32_t T, int32_t ch
  *   state fp32 [Hv, dv, dk] in: S_0, out: S_T;  out [T, Hv, dv] fp32 / bf16.
  *   workspace  device, >= gdn_prefill_workspace_bytes(), 256-byte aligned,
  *              caller-owned.  Its int32 at offset 0 is reset to 0 by the call
- *              and set non-zero on the device if a bounded tensor-core wait gave
- *              up (read it after the stream has synchronised; non-zero means
- *              the results are invalid, as for GDN_ERR_TIMEOUT).
+ *              and set non-zero on the device if a bounded wait (for the
+ *              tensor cores, a copy, or a pre-pass record) gave up; the
+ *              results are then invalid.  gdn_prefill_status() reads it.
  * The chunk form runs for dk = dv = 128 (the 27B layer's heads); narrower
  * heads run the same recurrence token by token on the GPU.  A pre-pass
  * computes every chunk's state-independent part into the workspace: with
@@ -355,27 +364,63 @@ int gdn_chunk_prefill(const gdn_shape* shape, int32_t T, int32_t chunk,
                       float q_scale, uint32_t flags, void* stream);
 
 /*
+ * gdn_prefill_status -- the status word of a gdn_chunk_prefill call: waits
+ * for `stream` to reach this point (cudaStreamSynchronize), copies the int32
+ * at offset 0 of `workspace` to *status (if status != NULL) and returns
+ * GDN_OK when it is 0, GDN_ERR_TIMEOUT when a bounded device wait of the call
+ * gave up (its outputs and state are then not valid), GDN_ERR_CUDA if the
+ * copy failed.  Source: failing loudly rather than handing back corrupt
+ * results, "Serving A Research Architecture On CPU" (the head-size bug).
+ */
+int gdn_prefill_status(const void* workspace, void* stream, int32_t* status);
+
+/*
+ * gdn_set_wait_limit_ns -- the limit, in nanoseconds, of every bounded device
+ * wait of the prefill kernels (for the tensor cores, a copy, or another CTA's
+ * pre-pass record), read at each later launch; returns the previous limit.
+ * Default 200,000,000 (0.2 s); values above 10 s are clamped to 10 s; 0 makes
+ * a wait give up at once unless what it waits for has already happened (for
+ * tests of the timeout path).  A wait that gives up sets the call's status
+ * word; the kernel still lets the work it started finish before it returns.
+ * Process-wide; launches already enqueued keep the limit they were given.
+ */
+uint64_t gdn_set_wait_limit_ns(uint64_t ns);
+
+/*
  * gdn_chunk_prefill_noalloc -- gdn_chunk_prefill for callers that cannot
  * allocate device memory, e.g. a serving loop whose device footprint is fixed
  * at start-up and must not grow while it serves, or a host whose device memory
  * is owned by another allocator.  (The pages describe no such call; it exists
  * for those callers.)
- *   Arguments and results as gdn_chunk_prefill (the same bits), without the
- *   workspace: it runs the single-launch form of the chain that computes each
- *   chunk's state-independent part itself, so the only scratch it needs is
- *   the status word, in a 256-byte array inside this library, which every GPU
+ *   Arguments as gdn_chunk_prefill, without the workspace.  It runs the
+ *   single-launch form of the chain that computes each chunk's
+ *   state-independent part itself, so its results agree with
+ *   gdn_chunk_prefill's within the parity tolerances (max abs error 1e-3 on
+ *   the outputs, relative Frobenius error 1e-4 on the state), not bit for bit:
+ *   the same algebra is grouped differently.  The only scratch it needs is the
+ *   status word, in a 256-byte array inside this library, which every GPU
  *   that loads the library keeps until the process exits.  Returns
  *   GDN_ERR_WORKSPACE if the call would need more scratch than that.
  *   The first call on a device looks up the array's device address (once per
  *   device, with that device current); make that first call before any stream
  *   capture.  Every call on a device shares the one array and clears the part
  *   that must start at zero; calls that overlap on the GPU (different streams,
- *   no ordering between them) race on it.  The kernel's status word lives in
- *   that shared array and is not returned to the caller.
+ *   no ordering between them) race on it.  The status word of the last call
+ *   is read with gdn_chunk_prefill_noalloc_status().
  */
 int gdn_chunk_prefill_noalloc(const gdn_shape* shape, int32_t T, int32_t chunk, const gdn_bf16* qkv,
                               const float* alpha, const float* beta, float* state, void* out,
                               float q_scale, uint32_t flags, void* stream);
+
+/*
+ * gdn_chunk_prefill_noalloc_status -- the status word that the last
+ * gdn_chunk_prefill_noalloc call on the current device left in the library's
+ * array, read as gdn_prefill_status() reads a workspace's (it synchronises
+ * `stream`, which should be the stream of that call): GDN_OK, or
+ * GDN_ERR_TIMEOUT when a bounded device wait of the call gave up and its
+ * outputs and state are not valid.  Allocates nothing.
+ */
+int gdn_chunk_prefill_noalloc_status(void* stream, int32_t* status);
 
 /*
  * ---- Snapshot and restore of one sequence's recurrent sections -------------

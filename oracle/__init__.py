@@ -55,6 +55,8 @@ def _load():
             "orc_silu": (D, [D]),
             "orc_conv_linear": (None, [I, I, I, I, P, P, P, P]),
             "orc_conv_tree": (None, [I, I, I, P, P, P, P, P]),
+            "orc_conv_linear_f32": (None, [I, I, I, I, P, P, P, P]),
+            "orc_decode_f32": (None, [I, I, I, I, I, I, P, P, P, P, P, D, I]),
             "orc_tree_check": (I, [I, P, P]),
             "orc_root_path": (I, [I, P, I, P]),
             "orc_path_check": (I, [I, P, P, I]),
@@ -135,6 +137,18 @@ def conv_linear(x, w, tail):
     return y, tail
 
 
+def conv_linear_f32(x, w, tail):
+    """conv_linear over fp32 x [B,T,C], w [C,4], tail [B,4,C] -> (y f64, new fp32 tail)."""
+    x = _c(x, np.float32)
+    w = _c(w, np.float32)
+    tail = _c(tail, np.float32).copy()
+    B, T, C = x.shape
+    W = w.shape[1]
+    y = np.empty((B, T, C), np.float64)
+    _load().orc_conv_linear_f32(B, T, C, W, _ptr(x), _ptr(w), _ptr(tail), _ptr(y))
+    return y, tail
+
+
 def conv_tree(parents, x, w, tail):
     """x bf16 [N,C], tail bf16 [4,C] (read only) -> y f64 [N,C]."""
     parents = _c(parents, np.int32)
@@ -208,6 +222,21 @@ def decode(qkv, alpha, beta, state, Hk, Hv, dk, dv, q_scale=1.0, normalize=True)
     out = np.empty((B, T, Hv, dv), np.float64)
     _load().orc_decode(B, T, Hk, Hv, dk, dv, _ptr(qkv), _ptr(alpha), _ptr(beta), _ptr(st),
                        _ptr(out), float(q_scale), int(bool(normalize)))
+    return out, st
+
+
+def decode_f32(qkv, alpha, beta, state, Hk, Hv, dk, dv, q_scale=1.0, normalize=True):
+    """decode() over fp32 activations qkv [B,T,C] (no bf16 rounding anywhere)."""
+    qkv = _c(qkv, np.float32)
+    alpha = _c(alpha, np.float32)
+    beta = _c(beta, np.float32)
+    st = _c(state, np.float64).copy()
+    B, T = qkv.shape[0], qkv.shape[1]
+    assert qkv.shape[2] == 2 * Hk * dk + Hv * dv
+    assert st.shape == (B, Hv, dv, dk)
+    out = np.empty((B, T, Hv, dv), np.float64)
+    _load().orc_decode_f32(B, T, Hk, Hv, dk, dv, _ptr(qkv), _ptr(alpha), _ptr(beta), _ptr(st),
+                           _ptr(out), float(q_scale), int(bool(normalize)))
     return out, st
 
 

@@ -98,6 +98,31 @@ void orc_conv_linear(int B, int T, int C, int W, const uint16_t* x,
     free(u);
 }
 
+/* The same linear run over fp32 activations and taps (widened exactly to fp64;
+ * nothing is rounded to bf16). */
+void orc_conv_linear_f32(int B, int T, int C, int W, const float* x, const float* w,
+                         float* tail, double* y) {
+    double* u = (double*)malloc(sizeof(double) * (size_t)W);
+    float* hist = (float*)malloc(sizeof(float) * (size_t)(W + T));
+    for (int b = 0; b < B; ++b) {
+        for (int c = 0; c < C; ++c) {
+            for (int j = 0; j < W; ++j) hist[j] = tail[((size_t)b * W + j) * C + c];
+            for (int t = 0; t < T; ++t) hist[W + t] = x[((size_t)b * T + t) * C + c];
+            for (int t = 0; t < T; ++t) {
+                double acc = 0.0;
+                for (int j = 0; j < W; ++j) {
+                    u[j] = (double)hist[t + 1 + j];
+                    acc += (double)w[(size_t)c * W + j] * u[j];
+                }
+                y[((size_t)b * T + t) * C + c] = orc_silu(acc);
+            }
+            for (int j = 0; j < W; ++j) tail[((size_t)b * W + j) * C + c] = hist[T + j];
+        }
+    }
+    free(hist);
+    free(u);
+}
+
 void orc_conv_tree(int N, int C, int W, const int32_t* parents, const uint16_t* x,
                    const uint16_t* w, const uint16_t* tail, double* y) {
     double* u = (double*)malloc(sizeof(double) * (size_t)W);
@@ -251,6 +276,40 @@ void orc_decode(int B, int T, int Hk, int Hv, int dk, int dv, const uint16_t* qk
     free(v);
     free(k);
     free(q);
+}
+
+/* orc_decode over fp32 activations: each token's q, k, v widened exactly to
+ * fp64, then the same normalisation and row-form step. */
+void orc_decode_f32(int B, int T, int Hk, int Hv, int dk, int dv, const float* qkv,
+                    const float* alpha, const float* beta, double* state, double* out,
+                    double q_scale, int normalize) {
+    const size_t C = (size_t)2 * Hk * dk + (size_t)Hv * dv;
+    const int group = Hv / Hk;
+    double* raw = (double*)malloc(sizeof(double) * (size_t)dk);
+    double* q = (double*)malloc(sizeof(double) * (size_t)dk);
+    double* k = (double*)malloc(sizeof(double) * (size_t)dk);
+    double* v = (double*)malloc(sizeof(double) * (size_t)dv);
+    for (int b = 0; b < B; ++b)
+        for (int t = 0; t < T; ++t) {
+            const size_t tok = (size_t)b * T + t;
+            const float* row = qkv + tok * C;
+            for (int h = 0; h < Hv; ++h) {
+                const int g = h / group;
+                for (int j = 0; j < dk; ++j) raw[j] = (double)row[(size_t)g * dk + j];
+                if (normalize) orc_l2norm(raw, dk, 1e-6, q); else memcpy(q, raw, sizeof(double) * dk);
+                for (int j = 0; j < dk; ++j) q[j] *= q_scale;
+                for (int j = 0; j < dk; ++j) raw[j] = (double)row[(size_t)Hk * dk + (size_t)g * dk + j];
+                if (normalize) orc_l2norm(raw, dk, 1e-6, k); else memcpy(k, raw, sizeof(double) * dk);
+                for (int i = 0; i < dv; ++i) v[i] = (double)row[(size_t)2 * Hk * dk + (size_t)h * dv + i];
+                double* S = state + ((size_t)b * Hv + h) * (size_t)dv * dk;
+                orc_delta_token(dk, dv, S, k, v, q, (double)alpha[tok * Hv + h],
+                                (double)beta[tok * Hv + h], out + (tok * Hv + h) * dv);
+            }
+        }
+    free(v);
+    free(k);
+    free(q);
+    free(raw);
 }
 
 void orc_tree_verify(int N, int Hk, int Hv, int dk, int dv, const int32_t* parents,

@@ -64,6 +64,10 @@ double orc_silu(double z);
 void orc_conv_linear(int B, int T, int C, int W, const uint16_t* x,
                      const uint16_t* w, uint16_t* tail, double* y);
 
+/* The linear run over fp32 x, w and tail (widened exactly; tail stays fp32). */
+void orc_conv_linear_f32(int B, int T, int C, int W, const float* x, const float* w,
+                         float* tail, double* y);
+
 /* Tree run (one sequence): node n's earlier inputs are its ancestors' inputs,
  * nearest first, and then the committed tail.  tail is not modified. */
 void orc_conv_tree(int N, int C, int W, const int32_t* parents, const uint16_t* x,
@@ -102,6 +106,11 @@ void orc_delta_token_matrix(int dk, int dv, double* S, const double* k,
 void orc_decode(int B, int T, int Hk, int Hv, int dk, int dv, const uint16_t* qkv,
                 const float* alpha, const float* beta, double* state, double* out,
                 double q_scale, int normalize);
+
+/* orc_decode over fp32 activations qkv [B,T,C_qkv] (widened exactly). */
+void orc_decode_f32(int B, int T, int Hk, int Hv, int dk, int dv, const float* qkv,
+                    const float* alpha, const float* beta, double* state, double* out,
+                    double q_scale, int normalize);
 
 /* Tree verify (one sequence): node n's state is the committed state advanced
  * through the root..n path; out[n] is that node's output.  Computed by replaying

@@ -60,5 +60,46 @@ def oracle_conv_then_round(x, w, tail):
     return oracle.f64_to_bf16(y), tail2
 
 
+def _key_head_slice(qkv, shape, g):
+    """Packed rows of key head g and its value heads, as an Hk = 1 problem."""
+    Hk, dk, dv = shape.Hk, shape.dk, shape.dv
+    grp = shape.Hv // Hk
+    q = qkv[..., g * dk:(g + 1) * dk]
+    k = qkv[..., Hk * dk + g * dk: Hk * dk + (g + 1) * dk]
+    v = qkv[..., 2 * Hk * dk + g * grp * dv: 2 * Hk * dk + (g + 1) * grp * dv]
+    return np.ascontiguousarray(np.concatenate([q, k, v], axis=-1)), slice(g * grp, (g + 1) * grp)
+
+
+def oracle_decode_parallel(qkv, alpha, beta, state, shape, q_scale=1.0, normalize=True, keys=None):
+    """The oracle's sequential decode, run per key head on all host cores.
+
+    qkv [B,T,C] bf16 bits, alpha/beta [B,T,Hv], state [B,Hv,dv,dk].  Key heads
+    are independent problems (each value head reads only its own key head), so
+    each is the oracle on that head's slice; ctypes releases the GIL during the
+    C call, so the slices run on separate cores.  `keys` picks key heads
+    (default all); returns (out [B,T,Hv,dv], state [B,Hv,dv,dk]) with only the
+    picked heads filled (NaN elsewhere)."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    B, T = qkv.shape[0], qkv.shape[1]
+    grp = shape.Hv // shape.Hk
+    keys = list(range(shape.Hk)) if keys is None else list(keys)
+    out = np.full((B, T, shape.Hv, shape.dv), np.nan)
+    st = np.full((B, shape.Hv, shape.dv, shape.dk), np.nan)
+
+    def one(g):
+        q_g, hs = _key_head_slice(qkv, shape, g)
+        o, s_ = oracle.decode(q_g, alpha[..., hs], beta[..., hs], state[:, hs], 1, grp, shape.dk, shape.dv,
+                              q_scale=q_scale, normalize=normalize)
+        return hs, o, s_
+
+    with ThreadPoolExecutor(max_workers=min(len(keys), os.cpu_count() or 1)) as ex:
+        for hs, o, s_ in ex.map(one, keys):
+            out[:, :, hs] = o
+            st[:, hs] = s_
+    return out, st
+
+
 __all__ = ["OUT_ATOL", "STATE_RTOL_F", "rel_frob", "f32", "bf16", "host", "assert_out_close",
-           "assert_state_close", "bf16_ulp_diff", "oracle_conv_then_round", "gen", "gdn", "oracle"]
+           "assert_state_close", "bf16_ulp_diff", "oracle_conv_then_round", "oracle_decode_parallel", "gen", "gdn",
+           "oracle"]

@@ -288,3 +288,47 @@ def test_prefill_workspace_holds_the_prepass_records(lib):
     rc = lib.gdn_chunk_prefill(ctypes.byref(sh), 64, 64, P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE * 256),
                                256, 1.0, 1, None)
     assert rc == -9 and "needed" in gdn.last_error()
+
+
+def test_fp32_activation_flag_validation(lib):
+    """GDN_IN_F32 is accepted by the conv and the plain decode, refused by the
+    other entry points; the conv refuses the decode-only flags."""
+    P = ctypes.c_void_p
+    F32 = gdn.GDN_IN_F32
+    rc = lib.gdn_kda_decode_step(ctypes.byref(_sh()), 1, P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, 1.0, 1 | F32, None)
+    assert rc == -1 and "flag" in gdn.last_error()
+    rc = lib.gdn_conv_decode_step(ctypes.byref(_sh()), 1, P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                                  P(FAKE), None, 1.0, 1 | F32, None)
+    assert rc == -1
+    rc = _tree_call_flags(lib, 1 | F32)
+    assert rc == -1
+    # the flag passes the decode's flag check: the (misaligned) qkv is what fails
+    rc = lib.gdn_decode_step(ctypes.byref(_sh()), 1, P(FAKE + 4), P(FAKE), P(FAKE), P(FAKE), None, 1.0, 1 | F32,
+                             None)
+    assert rc == -6
+    assert lib.gdn_conv_step(1, 1, 128, None, P(FAKE), P(FAKE + 8), P(FAKE), P(FAKE), F32, None) == -6
+    assert lib.gdn_conv_step(1, 1, 128, None, P(FAKE), P(FAKE), P(FAKE), P(FAKE), gdn.GDN_NORMALIZE_QK, None) == -1
+
+
+def _tree_call_flags(lib, flags):
+    P = ctypes.c_void_p
+    par = np.array([-1, 0], np.int32)
+    return lib.gdn_tree_verify(ctypes.byref(_sh()), 2, par.ctypes.data_as(P), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                               P(FAKE), 1.0, flags, None)
+
+
+def test_wait_limit_setter_and_status_validation(lib):
+    """The wait-limit setter returns the previous limit and clamps at 10 s; the
+    status readers refuse a missing or misaligned workspace before touching
+    the device."""
+    prev = gdn.set_wait_limit_ns(12345)
+    try:
+        assert prev == 200_000_000
+        assert gdn.set_wait_limit_ns(10**12) == 12345
+        assert gdn.set_wait_limit_ns(0) == 10_000_000_000
+    finally:
+        gdn.set_wait_limit_ns(prev)
+    word = ctypes.c_int32(7)
+    assert lib.gdn_prefill_status(None, None, ctypes.byref(word)) == -1
+    assert lib.gdn_prefill_status(ctypes.c_void_p(FAKE + 16), None, ctypes.byref(word)) == -6
+    assert word.value == 7

@@ -113,3 +113,23 @@ def test_reference_arm_nonzero_rank_is_silent():
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
                           "--steps", "1"], capture_output=True, text=True, timeout=120, env=env, check=True)
     assert out.stdout.strip() == ""
+
+
+def test_reference_arm_default_is_the_headline():
+    """With no --workload the reference arm times the headline (batched) config."""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2",
+                          "--warmup", "3"], capture_output=True, text=True, timeout=300, check=True).stdout
+    d = json.loads(out.strip().splitlines()[-1])
+    assert d["config"]["workload"].startswith("batched decode")
+    assert d["cpu_baseline"]["host"]["nproc"] >= 1
+
+
+def test_cpu_baselines_single_and_all_cores():
+    """The CPU baseline: one thread, and the same sample on every core, with the
+    host's core count and CPU model."""
+    b = bench.cpu_baselines("decode1", 0.2)
+    assert b["cores"] == 1 and b["value"] > 0 and b["kind"] == "oracle"
+    assert b["host"]["nproc"] == (os.cpu_count() or 1) and b["host"]["cpu_model"]
+    if b["host"]["nproc"] > 1:
+        allc = b["all_cores"]
+        assert allc["cores"] == b["host"]["nproc"] and allc["value"] > 0

@@ -5,7 +5,7 @@ import pytest
 import torch
 
 from gdn_testutil import (assert_out_close, assert_state_close, bf16, bf16_ulp_diff, f32, gdn, gen,
-                          host, oracle, oracle_conv_then_round)
+                          host, oracle, oracle_conv_then_round, oracle_decode_parallel)
 
 pytestmark = pytest.mark.gpu
 
@@ -101,10 +101,59 @@ def _run_decode(shape, T, seed, q_scale=1.0, normalize=True, out_bf16=False, tag
 
 
 def test_decode_tiny_config():
-    """1 sequence, 2 key / 4 value heads of 32, 16 sequential tokens, seed 0."""
+    """1 sequence, 2 key / 4 value heads of 32, 16 sequential tokens, seed 0
+    (bf16 activations, as every other workload stores them)."""
     _, out, st, out_ref, st_ref = _run_decode(gen.TINY, 16, 0)
     assert_out_close(host(out), out_ref)
     assert_state_close(host(st), st_ref)
+
+
+@pytest.mark.parametrize("conv_channels", [256, 128])
+def test_tiny_config_fp32_activations(conv_channels):
+    """The tiny config as stated: q, k, v drawn ~N(0, 1) in fp32 and kept in
+    fp32 (GDN_IN_F32), conv taps ~N(0, 0.5^2), a zero conv tail (the start of
+    the sequence), 16 sequential tokens, seed 0.  256 channels: the conv runs
+    over every q/k/v channel and feeds the decode; 128 channels: the conv alone
+    at the config's stated width.  Against the oracle's fp32-input conv and
+    decode (no bf16 rounding anywhere)."""
+    s = gen.TINY
+    T = 16
+    c = gen.conv_inputs_f32(0, 1, T, conv_channels)
+    x, w, tail = f32(c["x"]), f32(c["w"]), f32(c["tail"])
+    y = gdn.conv_step(x, w, tail)
+    torch.cuda.synchronize()
+    y_ref, tail_ref = oracle.conv_linear_f32(c["x"], c["w"], c["tail"])
+    assert np.array_equal(host(tail), tail_ref)
+    # fp32 conv vs fp64: a few fp32 roundings of values of order 1
+    assert np.abs(host(y) - y_ref).max() <= 1e-5
+    if conv_channels != s.C:
+        return
+    d = gen.decode_inputs(0, s, T, tag="tiny_f32")
+    st = f32(d["state"])
+    out = gdn.decode_step(y, f32(d["alpha"]), f32(d["beta"]), st, s.Hk, s.Hv, s.dk, s.dv)
+    torch.cuda.synchronize()
+    out_ref, st_ref = oracle.decode_f32(y_ref.astype(np.float32), d["alpha"], d["beta"], d["state"], s.Hk, s.Hv,
+                                        s.dk, s.dv)
+    assert_out_close(host(out), out_ref)
+    assert_state_close(host(st), st_ref)
+    # the decode alone on the oracle's own fp32 conv outputs, and with fp32 draws of q, k, v directly
+    d32 = gen.decode_inputs_f32(0, s, T)
+    st = f32(d32["state"])
+    out = gdn.decode_step(f32(d32["qkv"]), f32(d32["alpha"]), f32(d32["beta"]), st, s.Hk, s.Hv, s.dk, s.dv)
+    torch.cuda.synchronize()
+    out_ref, st_ref = oracle.decode_f32(d32["qkv"], d32["alpha"], d32["beta"], d32["state"], s.Hk, s.Hv, s.dk,
+                                        s.dv)
+    assert_out_close(host(out), out_ref)
+    assert_state_close(host(st), st_ref)
+
+
+def test_fp32_activation_flag_is_refused_elsewhere():
+    """GDN_IN_F32 belongs to the conv and the plain decode only."""
+    s = gen.TINY
+    d = gen.decode_inputs_f32(1, s, 2)
+    with pytest.raises(gdn.GdnError):
+        gdn.kda_decode_step(f32(d["qkv"]), f32(np.ones((1, 2, s.Hv, s.dk), np.float32)), f32(d["beta"]),
+                            f32(d["state"]), s.Hk, s.Hv, s.dk, s.dv)
 
 
 @pytest.mark.parametrize("shape,T", [
@@ -133,6 +182,64 @@ def test_decode_options():
     got = gen.bf16_bits_to_f32(host(out)).astype(np.float64)
     # bf16 outputs: within one bf16 rounding of the oracle (RNE), plus the fp32 slack
     assert np.all(np.abs(got - out_ref) <= np.abs(out_ref) * 2.0 ** -8 + 1e-3)
+
+
+def test_decode_27b_single_layer_1000_steps():
+    """The 27B single-layer decode config at its full length: batch 1, bf16
+    inputs, 1,000 single-token steps with the state carried.  Every output of
+    every step and the final state against the oracle's sequential decode on
+    the same bf16 inputs."""
+    s = gen.QWEN_27B
+    steps = 1000
+    d = gen.decode_inputs(0, s, steps, tag="d1000")
+    qkv, al, be = bf16(d["qkv"]), f32(d["alpha"]), f32(d["beta"])
+    st = f32(d["state"])
+    out = torch.empty((1, steps, s.Hv, s.dv), dtype=torch.float32, device="cuda")
+    for t in range(steps):
+        gdn.decode_step(qkv[:, t:t + 1], al[:, t:t + 1], be[:, t:t + 1], st, s.Hk, s.Hv, s.dk, s.dv,
+                        out=out[:, t:t + 1])
+    torch.cuda.synchronize()
+    out_ref, st_ref = oracle_decode_parallel(d["qkv"], d["alpha"], d["beta"], d["state"], s)
+    assert_out_close(host(out), out_ref)
+    assert_state_close(host(st), st_ref)
+
+
+def test_fused_decode_27b_1000_steps_equals_conv_then_decode():
+    """The same config through the fused conv + step, as a decode loop runs it
+    (the 4-tap conv over all 10,240 channels, ping-pong tails): 1,000 steps
+    equal gdn_conv_step followed by gdn_decode_step bit for bit, in every
+    output, the final state and the tail, and every step's conv output is
+    within one bf16 rounding of the oracle's conv.  (The conv output is
+    rounded to bf16, a decision the kernel takes in fp32 and the oracle in
+    fp64; about 0.5 % of values sit close enough to a rounding midpoint to
+    land one ulp apart, which perturbs the decode's inputs, so the decode's
+    parity with the oracle is checked above on identical bf16 inputs.)"""
+    s = gen.QWEN_27B
+    steps = 1000
+    c = gen.conv_inputs(0, 1, steps, s.C, tag="d1000", zero_tail=True)
+    d = gen.decode_inputs(0, s, steps, tag="d1000")
+    x, w = bf16(c["x"]), bf16(c["w"])
+    tails = [bf16(c["tail"]), bf16(c["tail"])]
+    al, be = f32(d["alpha"]), f32(d["beta"])
+    st_a, st_b = f32(d["state"]), f32(d["state"])
+    out_a = torch.empty((1, steps, s.Hv, s.dv), dtype=torch.float32, device="cuda")
+    out_b = torch.empty_like(out_a)
+    tail_u = bf16(c["tail"])
+    ys = torch.empty((1, steps, s.C), dtype=torch.bfloat16, device="cuda")
+    for t in range(steps):
+        gdn.conv_decode_step(x[:, t:t + 1], w, tails[t % 2], al[:, t:t + 1], be[:, t:t + 1], st_a, s.Hk, s.Hv,
+                             s.dk, s.dv, tail_out=tails[(t + 1) % 2], out=out_a[:, t:t + 1])
+        gdn.conv_step(x[:, t:t + 1], w, tail_u, y=ys[:, t:t + 1])
+        gdn.decode_step(ys[:, t:t + 1], al[:, t:t + 1], be[:, t:t + 1], st_b, s.Hk, s.Hv, s.dk, s.dv,
+                        out=out_b[:, t:t + 1])
+    torch.cuda.synchronize()
+    assert torch.equal(out_a, out_b)
+    assert torch.equal(st_a, st_b)
+    assert torch.equal(tails[steps % 2], tail_u)
+    y_ref, tail_ref = oracle_conv_then_round(c["x"], c["w"], c["tail"])
+    assert np.array_equal(host(tail_u), tail_ref)
+    ulp = bf16_ulp_diff(host(ys), y_ref)
+    assert ulp.max() <= 1 and (ulp == 0).mean() > 0.99
 
 
 def test_decode_27b_single_layer_steps():

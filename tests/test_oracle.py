@@ -273,9 +273,11 @@ def test_l2norm():
 
 
 def _decode_textbook(d, shape, T, q_scale=1.0, normalize=True):
-    """Independent numpy decode: matrix form, numpy norms, explicit head map."""
+    """Independent numpy decode: matrix form, numpy norms, explicit head map
+    (qkv as bf16 bits, or as fp32 values)."""
     B, Hk, Hv, dk, dv = shape.B, shape.Hk, shape.Hv, shape.dk, shape.dv
-    qkv = gen.bf16_bits_to_f32(d["qkv"]).astype(np.float64)
+    qkv = d["qkv"].astype(np.float64) if d["qkv"].dtype == np.float32 else \
+        gen.bf16_bits_to_f32(d["qkv"]).astype(np.float64)
     S = d["state"].astype(np.float64).copy()
     out = np.zeros((B, T, Hv, dv))
     for b in range(B):
@@ -308,6 +310,51 @@ def test_decode_vs_textbook(shape):
                             shape.dk, shape.dv, normalize=False)
     out_t, st_t = _decode_textbook(d, shape, T, normalize=False)
     np.testing.assert_allclose(out, out_t, rtol=1e-12, atol=1e-10)
+
+
+@pytest.mark.parametrize("shape", [gen.Shape(2, 2, 4, 8, 6), gen.TINY])
+def test_decode_f32_vs_textbook(shape):
+    """The fp32-activation decode against the independent numpy decode on fp32
+    draws (values that bf16 cannot hold, so a stray rounding would show)."""
+    T = 6
+    d = gen.decode_inputs_f32(22, shape, T)
+    assert not np.array_equal(gen.bf16_bits_to_f32(gen.f32_to_bf16_bits(d["qkv"])), d["qkv"])
+    out, st = oracle.decode_f32(d["qkv"], d["alpha"], d["beta"], d["state"], shape.Hk, shape.Hv,
+                                shape.dk, shape.dv, q_scale=0.75)
+    out_t, st_t = _decode_textbook(d, shape, T, q_scale=0.75)
+    np.testing.assert_allclose(out, out_t, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(st, st_t, rtol=0, atol=1e-12)
+
+
+def test_decode_f32_equals_bf16_decode_on_bf16_values():
+    """Widening is exact, so fp32 inputs that bf16 holds exactly give the bf16
+    decode's results bit for bit."""
+    s = gen.Shape(2, 2, 4, 16, 8)
+    d = gen.decode_inputs(23, s, 4)
+    out, st = oracle.decode(d["qkv"], d["alpha"], d["beta"], d["state"], s.Hk, s.Hv, s.dk, s.dv)
+    out32, st32 = oracle.decode_f32(gen.bf16_bits_to_f32(d["qkv"]), d["alpha"], d["beta"], d["state"], s.Hk,
+                                    s.Hv, s.dk, s.dv)
+    assert np.array_equal(out, out32) and np.array_equal(st, st32)
+
+
+def test_conv_f32_matches_numpy_correlate_and_bf16_conv():
+    """The fp32 conv: numpy's cross-correlation of (tail ++ x) with the taps,
+    then SiLU; the new tail is the last four inputs; on bf16-held values it is
+    the bf16 conv exactly."""
+    B, T, C = 2, 9, 16
+    d = gen.conv_inputs_f32(6, B, T, C, zero_tail=False)
+    y, tail2 = oracle.conv_linear_f32(d["x"], d["w"], d["tail"])
+    for b in range(B):
+        for c in range(C):
+            hist = np.concatenate([d["tail"][b, :, c], d["x"][b, :, c]]).astype(np.float64)
+            z = np.correlate(hist, d["w"][c].astype(np.float64), mode="valid")[1:]
+            np.testing.assert_allclose(y[b, :, c], z / (1.0 + np.exp(-z)), rtol=1e-13, atol=1e-15)
+    assert np.array_equal(tail2, np.concatenate([d["tail"], d["x"]], axis=1)[:, -4:, :])
+    h = gen.conv_inputs(7, B, T, C)
+    y16, t16 = oracle.conv_linear(h["x"], h["w"], h["tail"])
+    y32, t32 = oracle.conv_linear_f32(gen.bf16_bits_to_f32(h["x"]), gen.bf16_bits_to_f32(h["w"]),
+                                      gen.bf16_bits_to_f32(h["tail"]))
+    assert np.array_equal(y16, y32) and np.array_equal(gen.bf16_bits_to_f32(t16), t32)
 
 
 def test_decode_key_head_map():
@@ -694,3 +741,16 @@ def test_layer_decode_is_conv_gates_decode_norm():
                                                                                 d["norm_w"]))
     # the gates the recipe draws decay (some heads strongly: A up to 16, dt up to 0.1)
     assert 0.0 < al.min() and al.max() < 1.0
+
+
+def test_parallel_key_head_oracle_equals_serial():
+    """The test helper that runs the oracle per key head on all cores gives the
+    serial oracle's results bit for bit (key heads are independent problems)."""
+    from gdn_testutil import oracle_decode_parallel
+    s = gen.Shape(2, 3, 6, 8, 8)
+    d = gen.decode_inputs(24, s, 5)
+    out, st = oracle.decode(d["qkv"], d["alpha"], d["beta"], d["state"], s.Hk, s.Hv, s.dk, s.dv)
+    out_p, st_p = oracle_decode_parallel(d["qkv"], d["alpha"], d["beta"], d["state"], s)
+    assert np.array_equal(out, out_p) and np.array_equal(st, st_p)
+    out_k, _ = oracle_decode_parallel(d["qkv"], d["alpha"], d["beta"], d["state"], s, keys=[1])
+    assert np.array_equal(out_k[:, :, 2:4], out[:, :, 2:4]) and np.isnan(out_k[:, :, :2]).all()
