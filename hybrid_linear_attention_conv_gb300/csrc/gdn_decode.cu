@@ -314,6 +314,18 @@ gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
+    // Small batches (one row per thread): the first value head's state rows
+    // are requested before the conv, so that their DRAM round trip overlaps the
+    // conv inputs' instead of following it.
+    constexpr bool kEarlyState = R == 1;
+    float4 s_first[kEarlyState ? 1 : R][V];
+    if constexpr (kEarlyState) {
+        const float* S = state_of(j0);
+#pragma unroll
+        for (int m = 0; m < V; ++m)
+            s_first[0][m] = __ldcs(reinterpret_cast<const float4*>(S + (size_t)row0 * DK + 32 * m + 4 * lane8));
+    }
+
     // KDA: the group's decay vectors [T][group][DK] go to shared memory after
     // the conv outputs; the first kThreads float4s are loaded before the conv
     // so that their latency overlaps it.
@@ -427,7 +439,10 @@ gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
         const int h = g * p.group + j;
         float* S = state_of(j);
         float4 s[R][V];
-        if (prefetch && j > j0) {
+        if (kEarlyState && j == j0) {
+#pragma unroll
+            for (int m = 0; m < V; ++m) s[0][m] = s_first[0][m];
+        } else if (prefetch && j > j0) {
             // this thread's own copies of head j (issued during head j - 1)
             asm volatile("cp.async.wait_all;" ::: "memory");
 #pragma unroll
