@@ -606,4 +606,69 @@ int gdn_commit_path(const gdn_shape* shape, int32_t N, const int32_t* parents, c
     return GDN_OK;
 }
 
+int gdn_commit_path_batched(const gdn_shape* shape, int32_t N, const int32_t* counts, const int32_t* parents,
+                            const int32_t* paths, const int32_t* lengths, const gdn_bf16* qkv, const float* alpha,
+                            const float* beta, const gdn_bf16* x_tree, float* state, gdn_bf16* tail, uint32_t flags,
+                            void* stream) {
+    int rc;
+    if ((rc = check_shape(shape, false)) != GDN_OK) return rc;
+    if (flags & GDN_OUT_BF16) return fail(GDN_ERR_INVALID_ARG, "commit writes no output; GDN_OUT_BF16 not allowed");
+    if ((rc = check_flags(flags)) != GDN_OK) return rc;
+    if (shape->B < 1 || shape->B > kMaxTreeBatch)
+        return fail(GDN_ERR_UNSUPPORTED_SHAPE, "B=%d trees, one call commits 1 .. %d", shape->B, kMaxTreeBatch);
+    if (N < 1 || N > GDN_MAX_TREE_NODES)
+        return fail(GDN_ERR_BAD_PARENTS, "node capacity N=%d outside [1, %d]", N, GDN_MAX_TREE_NODES);
+    if (counts == nullptr || parents == nullptr || lengths == nullptr)
+        return fail(GDN_ERR_INVALID_ARG, "counts / parents / lengths is NULL");
+    static thread_local CommitBatchParams p;  // 2 KB of paths: kept off the stack
+    p = CommitBatchParams{};
+    int total = 0;
+    for (int b = 0; b < shape->B; ++b) {
+        if (counts[b] < 1 || counts[b] > N)
+            return fail(GDN_ERR_BAD_PARENTS, "tree %d has %d nodes, need 1 .. %d", b, counts[b], N);
+        const int32_t* par = parents + (size_t)b * N;
+        if ((rc = check_parents(counts[b], par)) != GDN_OK) {
+            const std::string why = t_error;
+            return fail(rc, "tree %d: %s", b, why.c_str());
+        }
+        const int L = lengths[b];
+        if (L > 0 && paths == nullptr) return fail(GDN_ERR_INVALID_ARG, "paths is NULL");
+        if ((rc = check_path(counts[b], par, L > 0 ? paths + (size_t)b * N : nullptr, L)) != GDN_OK) {
+            const std::string why = t_error;
+            return fail(rc, "tree %d: %s", b, why.c_str());
+        }
+        p.L[b] = L;
+        for (int i = 0; i < L; ++i) p.path[b][i] = (int8_t)paths[(size_t)b * N + i];
+        total += L;
+    }
+    if ((rc = check_ptr(qkv, "qkv")) || (rc = check_ptr(alpha, "alpha")) || (rc = check_ptr(beta, "beta")) ||
+        (rc = check_ptr(state, "state")) || (rc = check_ptr(x_tree, "x_tree", false)))
+        return rc;
+    if (x_tree != nullptr && (rc = check_ptr(tail, "tail")) != GDN_OK) return rc;
+    if (total == 0) return GDN_OK;  // no sequence accepted anything
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    p.qkv = qkv;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.state = state;
+    p.x_tree = x_tree;
+    p.tail = tail;
+    p.B = shape->B;
+    p.N = N;
+    p.Hk = shape->Hk;
+    p.Hv = shape->Hv;
+    p.dv = shape->dv;
+    p.group = shape->Hv / shape->Hk;
+    p.C = packed_channels(shape);
+    p.normalize = (flags & GDN_NORMALIZE_QK) != 0;
+    const int rows = decode_rows_per_cta(shape->B, shape->Hv, shape->dv);
+    cudaError_t e = launch_commit_batched(p, shape->dk, rows, st);
+    if (e != cudaSuccess) return cuda_fail(e, "batched commit launch");
+    if (x_tree != nullptr) {
+        e = launch_commit_tail_batched(p, st);
+        if (e != cudaSuccess) return cuda_fail(e, "batched commit tail launch");
+    }
+    return GDN_OK;
+}
+
 }  // extern "C"

@@ -116,6 +116,80 @@ gdn_decode_kernel(const __grid_constant__ DecodeParams p) {
                    s[r][m]);
 }
 
+// Commit of several sequences' accepted paths in one launch.  A CTA owns 32 R
+// rows of one value head of one sequence and replays that sequence's path
+// through the shared step, exactly as gdn_decode_kernel does with a gather
+// map (the same functions in the same order), so each sequence's result is the
+// bits of gdn_commit_path on its tree alone.
+template <int DK, int R>
+__global__ void __launch_bounds__(kThreads, 2)
+gdn_commit_batched_kernel(const __grid_constant__ CommitBatchParams p) {
+    constexpr int V = DK / 32;
+    const int lane8 = threadIdx.x & 7;
+    const int rg = threadIdx.x >> 3;
+    const int h = blockIdx.y;
+    const int b = blockIdx.z;
+    const int L = p.L[b];
+    if (L == 0) return;  // nothing accepted for this sequence
+    const int g = h / p.group;
+    const int row0 = blockIdx.x * (kRowsPerPass * R) + rg;
+    float* S = p.state + ((size_t)b * p.Hv + h) * (size_t)p.dv * DK;
+    float4 s[R][V];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < V; ++m)
+            s[r][m] = __ldcs(reinterpret_cast<const float4*>(S + (size_t)(row0 + kRowsPerPass * r) * DK + 32 * m +
+                                                             4 * lane8));
+    const bool normalize = p.normalize != 0;
+    for (int t = 0; t < L; ++t) {
+        const size_t trow = (size_t)b * p.N + p.path[b][t];
+        const uint16_t* row = p.qkv + trow * (size_t)p.C;
+        TokenKQ<V> kq;
+        token_kq<V>(row + g * DK, row + (size_t)p.Hk * DK + g * DK, lane8, 1.0f, normalize, kq);
+        const float alpha = p.alpha[trow * p.Hv + h];
+        const float beta = p.beta[trow * p.Hv + h];
+        const uint16_t* vrow = row + (size_t)2 * p.Hk * DK + (size_t)h * p.dv;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float v_i = act_f(vrow[row0 + kRowsPerPass * r]);
+            row_step<V>(s[r], kq, v_i, alpha, beta);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < V; ++m)
+            __stcs(reinterpret_cast<float4*>(S + (size_t)(row0 + kRowsPerPass * r) * DK + 32 * m + 4 * lane8),
+                   s[r][m]);
+}
+
+template <int DK, int R>
+static cudaError_t launch_commit_batched_t(const CommitBatchParams& p, cudaStream_t s) {
+    dim3 grid(p.dv / (kRowsPerPass * R), p.Hv, p.B);
+    gdn_commit_batched_kernel<DK, R><<<grid, kThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <int DK>
+static cudaError_t launch_commit_batched_r(const CommitBatchParams& p, int rows_per_cta, cudaStream_t s) {
+    switch (rows_per_cta) {
+        case 32: return launch_commit_batched_t<DK, 1>(p, s);
+        case 64: return launch_commit_batched_t<DK, 2>(p, s);
+        case 128: return launch_commit_batched_t<DK, 4>(p, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_commit_batched(const CommitBatchParams& p, int dk, int rows_per_cta, cudaStream_t s) {
+    switch (dk) {
+        case 32: return launch_commit_batched_r<32>(p, rows_per_cta, s);
+        case 64: return launch_commit_batched_r<64>(p, rows_per_cta, s);
+        case 128: return launch_commit_batched_r<128>(p, rows_per_cta, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
 // Shared-memory staging of the tree's inputs for one CTA (after the slots):
 // q and k of this CTA's key head for every node, this CTA's 32 R rows of v,
 // and alpha/beta -- loaded once, all loads in flight together, before the walk.

@@ -111,6 +111,22 @@ struct ConvDecodeParams {
     LayerParams layer;        // the layer step only (gates from projections, gated-norm output)
 };
 
+// Commit of the accepted paths of up to kMaxTreeBatch sequences (a joint
+// verify's trees) in one launch: sequence b replays path[b][0 .. L[b] - 1] of
+// its own tree, and its tail takes the last four inputs of (tail ++ x_tree[path]).
+struct CommitBatchParams {
+    const uint16_t* qkv;     // bf16 [B, N, C] the trees' inputs (post-conv)
+    const float* alpha;      // [B, N, Hv]
+    const float* beta;       // [B, N, Hv]
+    float* state;            // [B, Hv, dv, dk] in place
+    const uint16_t* x_tree;  // bf16 [B, N, C] pre-conv inputs, or nullptr (tails untouched)
+    uint16_t* tail;          // bf16 [B, 4, C]
+    int B, N, Hk, Hv, dv, group, C;
+    int normalize;
+    int32_t L[32];                         // path length of sequence b (0: nothing to commit)
+    int8_t path[32][GDN_MAX_TREE_NODES];   // its path, root first (node indices)
+};
+
 struct TailParams {
     const uint16_t* x_tree;  // [N, C]
     uint16_t* tail;          // [4, C]
@@ -143,5 +159,7 @@ constexpr int kFusedMaxTokens = 16;
 constexpr int kFusedMaxSmem = 48 * 1024;
 cudaError_t launch_conv(const ConvParams& p, cudaStream_t s);
 cudaError_t launch_commit_tail(const TailParams& p, cudaStream_t s);
+cudaError_t launch_commit_batched(const CommitBatchParams& p, int dk, int rows_per_cta, cudaStream_t s);
+cudaError_t launch_commit_tail_batched(const CommitBatchParams& p, cudaStream_t s);
 
 }  // namespace gdn

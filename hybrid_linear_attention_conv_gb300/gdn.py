@@ -55,6 +55,7 @@ EXPORTS = [
     "gdn_tree_verify",
     "gdn_tree_verify_batched",
     "gdn_commit_path",
+    "gdn_commit_path_batched",
     "gdn_prefill_workspace_bytes",
     "gdn_chunk_prefill",
     "gdn_prefill_status",
@@ -113,6 +114,7 @@ def load(path: str = LIB_PATH):
             "gdn_tree_verify": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, F, U32, P]),
             "gdn_tree_verify_batched": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, F, U32, P]),
             "gdn_commit_path": (ctypes.c_int, [SH, I32, P, P, I32, P, P, P, P, P, P, U32, P]),
+            "gdn_commit_path_batched": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, P, P, P, U32, P]),
             "gdn_prefill_workspace_bytes": (SZ, [SH, I32, I32]),
             "gdn_chunk_prefill": (ctypes.c_int, [SH, I32, I32, P, P, P, P, P, P, SZ, F, U32, P]),
             "gdn_prefill_status": (ctypes.c_int, [P, P, ctypes.POINTER(I32)]),
@@ -389,6 +391,27 @@ def commit_path(parents, path, qkv, alpha, beta, state, Hk, Hv, dk, dv, x_tree=N
                                 _dev(tail, torch.bfloat16, "tail", (GDN_CONV_W, packed_channels(Hk, Hv, dk, dv))), _flags(normalize, False),
                                 _stream())
     _check(rc, "gdn_commit_path")
+
+
+def commit_path_batched(counts, parents, paths, lengths, qkv, alpha, beta, state, Hk, Hv, dk, dv, x_tree=None,
+                        tail=None, normalize=True) -> None:
+    """B sequences' accepted paths in one launch.  counts [B], parents [B,N],
+    paths [B,N] (first lengths[b] entries used), lengths [B] (host); qkv bf16
+    [B,N,C], alpha/beta fp32 [B,N,Hv], x_tree bf16 [B,N,C] or None; state fp32
+    [B,Hv,dv,dk] and tail bf16 [B,4,C] updated in place."""
+    cnt, pc = _host_i32(counts, "counts")
+    par, pp = _host_i32(parents, "parents")
+    pth, ppth = _host_i32(paths, "paths")
+    ln, pl = _host_i32(lengths, "lengths")
+    B, N = par.shape
+    C = packed_channels(Hk, Hv, dk, dv)
+    rc = load().gdn_commit_path_batched(
+        ctypes.byref(_shape(B, Hk, Hv, dk, dv)), N, pc, pp, ppth, pl,
+        _dev(qkv, torch.bfloat16, "qkv", (B, N, C)), _dev(alpha, torch.float32, "alpha", (B, N, Hv)),
+        _dev(beta, torch.float32, "beta", (B, N, Hv)), _dev(x_tree, torch.bfloat16, "x_tree", (B, N, C)),
+        _dev(state, torch.float32, "state", (B, Hv, dv, dk)), _dev(tail, torch.bfloat16, "tail", (B, GDN_CONV_W, C)),
+        _flags(normalize, False), _stream())
+    _check(rc, "gdn_commit_path_batched")
 
 
 def prefill_workspace_bytes(T, Hk, Hv, dk, dv, chunk=64) -> int:

@@ -318,6 +318,39 @@ int gdn_commit_path(const gdn_shape* shape, int32_t N, const int32_t* parents,
                     float* state, gdn_bf16* tail, uint32_t flags, void* stream);
 
 /*
+ * gdn_commit_path_batched -- gdn_commit_path for B sequences in one launch
+ * (after a joint gdn_tree_verify_batched): sequence b replays its accepted
+ * path through the step in place, and its tail takes the path's inputs.  Each
+ * sequence's state and tail equal, bit for bit, gdn_commit_path on its tree
+ * alone.
+ *   shape->B  trees, 1 .. 32.   N  node capacity per tree, 1 .. 64.
+ *   counts    host int32 [B]: nodes of tree b, 1 .. N.
+ *   parents   host int32 [B, N]: tree b's parent array (as for
+ *             gdn_tree_verify_batched).
+ *   paths     host int32 [B, N]: tree b's accepted root-to-node path in
+ *             paths[b*N .. b*N + lengths[b] - 1]; may be NULL when every
+ *             length is 0.
+ *   lengths   host int32 [B]: path lengths, 0 .. counts[b] (0: sequence b
+ *             keeps its state and tail).
+ *   qkv, alpha, beta  the trees' inputs as given to the joint verify:
+ *             bf16 [B, N, C_qkv], fp32 [B, N, Hv].
+ *   x_tree    bf16 [B, N, C_qkv] the trees' pre-conv inputs, or NULL.
+ *   state     fp32 [B, Hv, dv, dk] in/out.
+ *   tail      bf16 [B, 4, C_qkv]: when x_tree != NULL, sequence b's tail is
+ *             replaced by the last four inputs of (tail ++ x_tree[b][path]).
+ *   flags     GDN_NORMALIZE_QK only.
+ * A tree or path that fails validation refuses the whole call (nothing is
+ * enqueued).  Source: "Architecture" (v0.14.2) section 8.5 (several requests'
+ * trees verified in one joint pass) and section 8.3 (commit the state of the
+ * accepted path).
+ */
+int gdn_commit_path_batched(const gdn_shape* shape, int32_t N, const int32_t* counts,
+                            const int32_t* parents, const int32_t* paths, const int32_t* lengths,
+                            const gdn_bf16* qkv, const float* alpha, const float* beta,
+                            const gdn_bf16* x_tree, float* state, gdn_bf16* tail, uint32_t flags,
+                            void* stream);
+
+/*
  * gdn_prefill_workspace_bytes -- device workspace gdn_chunk_prefill needs for
  * T tokens in chunks of `chunk` (0 on a bad shape or chunk).  The workspace
  * holds the call's status word (int32 at offset 0, padded to 256 bytes) and,

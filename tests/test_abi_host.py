@@ -332,3 +332,33 @@ def test_wait_limit_setter_and_status_validation(lib):
     assert lib.gdn_prefill_status(None, None, ctypes.byref(word)) == -1
     assert lib.gdn_prefill_status(ctypes.c_void_p(FAKE + 16), None, ctypes.byref(word)) == -6
     assert word.value == 7
+
+
+def test_commit_batched_validation(lib):
+    """Every tree and path is checked before anything is enqueued; a call in
+    which no sequence accepted anything is a no-op."""
+    P = ctypes.c_void_p
+    N = 5
+    parents = np.array([[-1, 0, 0, 1, 3], [-1, 0, 1, -7, -7]], np.int32)
+    counts = np.array([5, 3], np.int32)
+
+    def call(paths, lengths, sh=None, flags=1, cnt=counts, par=parents):
+        pa = np.ascontiguousarray(paths, np.int32)
+        ln = np.ascontiguousarray(lengths, np.int32)
+        return lib.gdn_commit_path_batched(ctypes.byref(sh or _sh(B=2)), N, cnt.ctypes.data_as(P),
+                                           par.ctypes.data_as(P), pa.ctypes.data_as(P), ln.ctypes.data_as(P),
+                                           P(FAKE), P(FAKE), P(FAKE), None, P(FAKE), None, flags, None)
+
+    ok = [[0, 1, 3, 4, 0], [0, 1, 2, 0, 0]]
+    assert call(ok, [0, 0]) == 0                       # nothing accepted: a no-op
+    assert call([[1, 3, 0, 0, 0], [0, 0, 0, 0, 0]], [2, 0]) == -4   # does not start at the root
+    assert call([[0, 1, 3, 0, 0], [0, 2, 0, 0, 0]], [3, 2]) == -4   # 2 is not a child of 0 in tree 1
+    assert call(ok, [4, 4]) == -4                      # tree 1 has 3 nodes
+    assert call(ok, [4, 3], sh=_sh(B=0)) == -2
+    assert call(ok, [4, 3], sh=_sh(B=33)) == -2
+    assert call(ok, [4, 3], flags=1 | gdn.GDN_OUT_BF16) == -1
+    assert call(ok, [4, 3], cnt=np.array([5, 6], np.int32)) == -3
+    bad = parents.copy()
+    bad[1, 1] = 2
+    assert call(ok, [4, 3], par=bad) == -3
+    assert "tree 1" in gdn.last_error()

@@ -270,3 +270,50 @@ def test_tree_verify_batched_equals_single_and_oracle(shape):
         ref = oracle.tree_verify(t, d["qkv"][b, :n], d["alpha"][b, :n], d["beta"][b, :n], d["state"][b], shape.Hk,
                                  shape.Hv, shape.dk, shape.dv)
         assert_out_close(host(out[b, :n]), ref)
+
+
+@pytest.mark.parametrize("shape", [gen.QWEN_27B, gen.Shape(1, 2, 4, 64, 64)])
+def test_commit_path_batched_equals_single_commits_and_oracle(shape):
+    """A joint verify's sequences commit their accepted paths in one launch:
+    each sequence's state and tail equal gdn_commit_path on its tree alone, bit
+    for bit, and the oracle's commit within the bars; a sequence that accepts
+    nothing keeps its state and tail."""
+    N = 32
+    trees = [gen.random_tree(50, 32, 8), np.array([-1], np.int32), gen.random_tree(51, 13, 5),
+             gen.random_tree(52, 20, 8), np.arange(-1, 6, dtype=np.int32)]
+    B = len(trees)
+    counts = np.array([len(t) for t in trees], np.int32)
+    parents = _pad_parents(trees, N)
+    paths = np.full((B, N), -9, np.int32)
+    lengths = np.zeros(B, np.int32)
+    for b, t in enumerate(trees):
+        if b == 3:
+            continue  # nothing accepted
+        p = gdn.tree_root_path(t, gen.random_leaf(60 + b, t))
+        paths[b, :len(p)] = p
+        lengths[b] = len(p)
+    d = gen.decode_inputs(53, shape.with_batch(B), N, tag="commitb")
+    c = gen.conv_inputs(54, B, N, shape.C, tag="commitb")
+    qkv, al, be, xt = bf16(d["qkv"]), f32(d["alpha"]), f32(d["beta"]), bf16(c["x"])
+    st = f32(d["state"])
+    tail = bf16(c["tail"])
+    gdn.commit_path_batched(counts, parents, paths, lengths, qkv, al, be, st, shape.Hk, shape.Hv, shape.dk,
+                            shape.dv, x_tree=xt, tail=tail)
+    torch.cuda.synchronize()
+    for b, t in enumerate(trees):
+        n, L = len(t), int(lengths[b])
+        st_1 = f32(d["state"][b])
+        tail_1 = bf16(c["tail"][b])
+        gdn.commit_path(t, paths[b, :L], qkv[b, :n].contiguous(), al[b, :n].contiguous(), be[b, :n].contiguous(),
+                        st_1, shape.Hk, shape.Hv, shape.dk, shape.dv, x_tree=xt[b, :n].contiguous(), tail=tail_1)
+        torch.cuda.synchronize()
+        assert torch.equal(st[b], st_1), f"sequence {b}: state"
+        assert torch.equal(tail[b], tail_1), f"sequence {b}: tail"
+        if L == 0:
+            assert np.array_equal(host(st[b]), d["state"][b]) and np.array_equal(host(tail[b]), c["tail"][b])
+            continue
+        st_ref, tail_ref = oracle.commit(t, paths[b, :L], d["qkv"][b, :n], d["alpha"][b, :n], d["beta"][b, :n],
+                                         d["state"][b], shape.Hk, shape.Hv, shape.dk, shape.dv,
+                                         x_tree=c["x"][b, :n], tail=c["tail"][b])
+        assert_state_close(host(st[b]), st_ref)
+        assert np.array_equal(host(tail[b]), tail_ref)
