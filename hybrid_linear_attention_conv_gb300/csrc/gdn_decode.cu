@@ -388,10 +388,36 @@ gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    // Small batches (one row per thread): the first value head's state rows
-    // are requested before the conv, so that their DRAM round trip overlaps the
-    // conv inputs' instead of following it.
+    // the next head's state rows, prefetched by each thread into its own slots
+    // (not in the layer step, whose per-head norm barrier already overlaps the
+    // next head's loads, and which measured slower with it)
+    const bool prefetch = !LAYER && nh > 1;
+    float4* s_pref = reinterpret_cast<float4*>(
+        reinterpret_cast<uint8_t*>(smem_y) +
+        align16((size_t)p.T * p.CC * 2 + (KDA ? (size_t)p.T * p.group * DK * 4 : 0) + (LAYER ? (size_t)p.T * p.group * 8 : 0)));
+    auto prefetch_head = [&](int j) {
+        const float* S = state_of(j);
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < V; ++m) {
+                const uint32_t dst = (uint32_t)__cvta_generic_to_shared(s_pref + (size_t)(r * V + m) * kThreads + threadIdx.x);
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
+                             "l"(S + (size_t)(row0 + kRowsPerPass * r) * DK + 32 * m + 4 * lane8)
+                             : "memory");
+            }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+
+    // The first value head's state rows are requested before the conv, so that
+    // their DRAM round trip overlaps the conv inputs' instead of following it:
+    // into registers with one row per thread (small batches), else, for the
+    // plain step, into the prefetch slots (several heads per CTA: no registers
+    // held across the conv; batch 64: 69.28 -> 68.97 us a layer; the KDA step,
+    // whose decay vectors are also loaded before the conv, measured no gain).
     constexpr bool kEarlyState = R == 1;
+    const bool early_slots = !kEarlyState && KIND == 0 && prefetch;
+    if (early_slots) prefetch_head(j0);
     float4 s_first[kEarlyState ? 1 : R][V];
     if constexpr (kEarlyState) {
         const float* S = state_of(j0);
@@ -457,26 +483,6 @@ gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
             s_ab[idx] = make_float2(al, be);
         }
     }
-    // the next head's state rows, prefetched by each thread into its own slots
-    // (not in the layer step, whose per-head norm barrier already overlaps the
-    // next head's loads, and which measured slower with it)
-    const bool prefetch = !LAYER && nh > 1;
-    float4* s_pref = reinterpret_cast<float4*>(
-        reinterpret_cast<uint8_t*>(smem_y) +
-        align16((size_t)p.T * p.CC * 2 + (KDA ? (size_t)p.T * p.group * DK * 4 : 0) + (LAYER ? (size_t)p.T * p.group * 8 : 0)));
-    auto prefetch_head = [&](int j) {
-        const float* S = state_of(j);
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int m = 0; m < V; ++m) {
-                const uint32_t dst = (uint32_t)__cvta_generic_to_shared(s_pref + (size_t)(r * V + m) * kThreads + threadIdx.x);
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
-                             "l"(S + (size_t)(row0 + kRowsPerPass * r) * DK + 32 * m + 4 * lane8)
-                             : "memory");
-            }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-    };
     // the row this lane writes outputs for: lane l < R of a row group takes
     // row r = l (every lane of the group holds the same o bits)
     const int my_row = row0 + kRowsPerPass * (lane8 < R ? lane8 : 0);
@@ -516,8 +522,9 @@ gdn_conv_decode_kernel(const __grid_constant__ ConvDecodeParams p) {
         if (kEarlyState && j == j0) {
 #pragma unroll
             for (int m = 0; m < V; ++m) s[0][m] = s_first[0][m];
-        } else if (prefetch && j > j0) {
-            // this thread's own copies of head j (issued during head j - 1)
+        } else if (prefetch && (j > j0 || early_slots)) {
+            // this thread's own copies of head j (issued during head j - 1, or
+            // before the conv for the first head)
             asm volatile("cp.async.wait_all;" ::: "memory");
 #pragma unroll
             for (int r = 0; r < R; ++r)
