@@ -767,8 +767,8 @@ class Tree(Workload):
         self.y = torch.empty((1, N, C_QKV), dtype=bf, device=device)
         self.out = torch.empty((N, HV, DV), dtype=torch.float32, device=device)
         self.shape = gdn.gdn_shape(1, HK, HV, DK, DV)
-        self.launches_per_step = 4  # tree conv, verify, commit replay, commit tail
-        self.tree_marks = 3          # conv, verify, commit (its two launches together)
+        self.launches_per_step = 3  # tree conv, verify, commit (replay + conv-tail update in one launch)
+        self.tree_marks = 3          # conv, verify, commit
         self.units_per_step = (N + len(self.path)) * HV
         self.dominant = "gdn_tree_kernel"
         self.dominant_sources = DECODE_SOURCES
@@ -802,7 +802,7 @@ class Tree(Workload):
                                     P(self.state.data_ptr()), P(self.tail.data_ptr()),
                                     gdn.GDN_NORMALIZE_QK, self.sp), gdn)
         if rec:
-            rec.mark("commit")  # replay + tail update (two launches)
+            rec.mark("commit")  # replay + tail update (one launch)
 
     def step(self, i: int, rec: Recorder | None = None):
         if rec:

@@ -590,19 +590,11 @@ int gdn_commit_path(const gdn_shape* shape, int32_t N, const int32_t* parents, c
     p.normalize = (flags & GDN_NORMALIZE_QK) != 0;
     p.out_bf16 = 0;
     for (int i = 0; i < L; ++i) p.tok[i] = path[i];
+    p.x_tree = x_tree;  // the conv tail is updated by the same launch
+    p.tail = x_tree != nullptr ? tail : nullptr;
     const int rows = decode_rows_per_cta(1, shape->Hv, shape->dv);
     cudaError_t e = launch_decode(p, shape->dk, rows, 1, false, false, st);
     if (e != cudaSuccess) return cuda_fail(e, "commit launch");
-    if (x_tree != nullptr) {
-        TailParams tp{};
-        tp.x_tree = x_tree;
-        tp.tail = tail;
-        tp.C = p.C;
-        tp.L = L;
-        for (int i = 0; i < L; ++i) tp.path[i] = path[i];
-        e = launch_commit_tail(tp, st);
-        if (e != cudaSuccess) return cuda_fail(e, "commit tail launch");
-    }
     return GDN_OK;
 }
 
@@ -662,12 +654,8 @@ int gdn_commit_path_batched(const gdn_shape* shape, int32_t N, const int32_t* co
     p.C = packed_channels(shape);
     p.normalize = (flags & GDN_NORMALIZE_QK) != 0;
     const int rows = decode_rows_per_cta(shape->B, shape->Hv, shape->dv);
-    cudaError_t e = launch_commit_batched(p, shape->dk, rows, st);
+    cudaError_t e = launch_commit_batched(p, shape->dk, rows, st);  // the tails too, when x_tree is given
     if (e != cudaSuccess) return cuda_fail(e, "batched commit launch");
-    if (x_tree != nullptr) {
-        e = launch_commit_tail_batched(p, st);
-        if (e != cudaSuccess) return cuda_fail(e, "batched commit tail launch");
-    }
     return GDN_OK;
 }
 

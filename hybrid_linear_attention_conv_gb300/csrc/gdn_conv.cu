@@ -1,5 +1,4 @@
-// gdn_conv.cu -- 4-tap causal depthwise convolution + SiLU, and the conv-tail
-// update of a commit (sm_103a).
+// gdn_conv.cu -- 4-tap causal depthwise convolution + SiLU (sm_103a).
 //
 // The layer keeps, per sequence, the last four pre-conv inputs of every q/k/v
 // channel (TandemLLM "Architecture" v0.14.2 section 8.1: a 4-wide convolution
@@ -101,53 +100,6 @@ __global__ void __launch_bounds__(kConvThreads) gdn_conv_kernel(const __grid_con
     }
 }
 
-__global__ void __launch_bounds__(kConvThreads)
-gdn_commit_tail_kernel(const __grid_constant__ TailParams p) {
-    const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * 8;
-    if (c0 >= p.C) return;
-    const size_t C = (size_t)p.C;
-    uint4 nt[GDN_CONV_W];
-#pragma unroll
-    for (int j = 0; j < GDN_CONV_W; ++j) {
-        const int pos = p.L + j;  // index into tail ++ x_tree[path]
-        const uint16_t* src = pos < GDN_CONV_W ? p.tail + (size_t)pos * C + c0
-                                               : p.x_tree + (size_t)p.path[pos - GDN_CONV_W] * C + c0;
-        nt[j] = *reinterpret_cast<const uint4*>(src);
-    }
-#pragma unroll
-    for (int j = 0; j < GDN_CONV_W; ++j) *reinterpret_cast<uint4*>(p.tail + (size_t)j * C + c0) = nt[j];
-}
-
-// The tails of a batched commit: sequence b (blockIdx.y) takes the last four
-// inputs of (tail[b] ++ x_tree[b][path[b][0]] ++ ...), as gdn_commit_tail_kernel.
-__global__ void __launch_bounds__(kConvThreads)
-gdn_commit_tail_batched_kernel(const __grid_constant__ CommitBatchParams p) {
-    const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * 8;
-    const int b = blockIdx.y;
-    const int L = p.L[b];
-    if (c0 >= p.C || L == 0) return;
-    const size_t C = (size_t)p.C;
-    uint16_t* tail = p.tail + (size_t)b * GDN_CONV_W * C;
-    const uint16_t* xb = p.x_tree + (size_t)b * p.N * C;
-    uint4 nt[GDN_CONV_W];
-#pragma unroll
-    for (int j = 0; j < GDN_CONV_W; ++j) {
-        const int pos = L + j;  // index into tail ++ x_tree[path]
-        const uint16_t* src = pos < GDN_CONV_W ? tail + (size_t)pos * C + c0
-                                               : xb + (size_t)p.path[b][pos - GDN_CONV_W] * C + c0;
-        nt[j] = *reinterpret_cast<const uint4*>(src);
-    }
-#pragma unroll
-    for (int j = 0; j < GDN_CONV_W; ++j) *reinterpret_cast<uint4*>(tail + (size_t)j * C + c0) = nt[j];
-}
-
-cudaError_t launch_commit_tail_batched(const CommitBatchParams& p, cudaStream_t s) {
-    const int cvecs = p.C / 8;
-    dim3 grid((cvecs + kConvThreads - 1) / kConvThreads, p.B, 1);
-    gdn_commit_tail_batched_kernel<<<grid, kConvThreads, 0, s>>>(p);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_conv(const ConvParams& p, cudaStream_t s) {
     const int cvecs = p.C / 8;
     const int gy = p.tree ? p.T : (p.T + kConvTok - 1) / kConvTok;
@@ -157,11 +109,6 @@ cudaError_t launch_conv(const ConvParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_commit_tail(const TailParams& p, cudaStream_t s) {
-    const int cvecs = p.C / 8;
-    dim3 grid((cvecs + kConvThreads - 1) / kConvThreads, 1, 1);
-    gdn_commit_tail_kernel<<<grid, kConvThreads, 0, s>>>(p);
-    return cudaGetLastError();
-}
+
 
 }  // namespace gdn

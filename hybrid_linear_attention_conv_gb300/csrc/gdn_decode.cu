@@ -42,6 +42,39 @@ __host__ __device__ constexpr size_t conv_decode_prefetch_bytes() {
 }
 __host__ __device__ constexpr size_t align16(size_t n) { return (n + 15) / 16 * 16; }
 
+// The conv-tail update of a commit, done by the commit's own launch: the
+// tail becomes the last four inputs of (tail ++ x_tree[path[0]] ++ ...), 8
+// channels (one 16-byte vector) per thread of the grid, copied as they are.
+// Each vector is read and written by one thread only.  The loads are issued
+// with the state loads and the stores made at the end, so that the tail adds
+// no DRAM round trip to the commit.
+struct CommitTail {
+    uint4 v[GDN_CONV_W];
+    size_t c0;
+    bool mine;
+};
+
+template <typename PathIndex>
+__device__ __forceinline__ void commit_tail_load(CommitTail& t, const uint16_t* x_tree, const uint16_t* tail, int C,
+                                                 int L, const PathIndex* path, long long gi) {
+    t.mine = gi < C / 8;
+    if (!t.mine) return;
+    t.c0 = (size_t)gi * 8;
+#pragma unroll
+    for (int j = 0; j < GDN_CONV_W; ++j) {
+        const int pos = L + j;  // index into tail ++ x_tree[path]
+        const uint16_t* src = pos < GDN_CONV_W ? tail + (size_t)pos * C + t.c0
+                                               : x_tree + (size_t)path[pos - GDN_CONV_W] * C + t.c0;
+        t.v[j] = *reinterpret_cast<const uint4*>(src);
+    }
+}
+
+__device__ __forceinline__ void commit_tail_store(const CommitTail& t, uint16_t* tail, int C) {
+    if (!t.mine) return;
+#pragma unroll
+    for (int j = 0; j < GDN_CONV_W; ++j) *reinterpret_cast<uint4*>(tail + (size_t)j * C + t.c0) = t.v[j];
+}
+
 // KDA selects a decay per key channel: alpha is then [B, Tsrc, Hv, dk].
 // In is the activations' element type: uint16_t (bf16 bits) or float.
 template <int DK, int R, bool GATHER, bool KDA, typename In>
@@ -56,6 +89,13 @@ gdn_decode_kernel(const __grid_constant__ DecodeParams p) {
     const int g = h / p.group;
     const int row0 = blockIdx.x * (kRowsPerPass * R) + rg;
     float* S = p.state + ((size_t)b * p.Hv + h) * (size_t)p.dv * DK;
+
+    CommitTail ct;  // commit: the conv tail too (one sequence); the grid has far more threads than C / 8
+    ct.mine = false;
+    if (GATHER && p.x_tree != nullptr)
+        commit_tail_load(ct, p.x_tree, p.tail, p.C, p.T, p.tok,
+                         (((long long)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x) * kThreads +
+                             threadIdx.x);
 
     float4 s[R][V];
 #pragma unroll
@@ -114,6 +154,7 @@ gdn_decode_kernel(const __grid_constant__ DecodeParams p) {
             __stcs(reinterpret_cast<float4*>(S + (size_t)(row0 + kRowsPerPass * r) * DK + 32 * m +
                                              4 * lane8),
                    s[r][m]);
+    if (GATHER) commit_tail_store(ct, p.tail, p.C);
 }
 
 // Commit of several sequences' accepted paths in one launch.  A CTA owns 32 R
@@ -131,6 +172,11 @@ gdn_commit_batched_kernel(const __grid_constant__ CommitBatchParams p) {
     const int b = blockIdx.z;
     const int L = p.L[b];
     if (L == 0) return;  // nothing accepted for this sequence
+    CommitTail ct;  // sequence b's conv tail, by sequence b's CTAs (far more threads than C / 8)
+    ct.mine = false;
+    if (p.x_tree != nullptr)
+        commit_tail_load(ct, p.x_tree + (size_t)b * p.N * p.C, p.tail + (size_t)b * GDN_CONV_W * p.C, p.C, L,
+                         p.path[b], ((long long)blockIdx.y * gridDim.x + blockIdx.x) * kThreads + threadIdx.x);
     const int g = h / p.group;
     const int row0 = blockIdx.x * (kRowsPerPass * R) + rg;
     float* S = p.state + ((size_t)b * p.Hv + h) * (size_t)p.dv * DK;
@@ -162,6 +208,7 @@ gdn_commit_batched_kernel(const __grid_constant__ CommitBatchParams p) {
         for (int m = 0; m < V; ++m)
             __stcs(reinterpret_cast<float4*>(S + (size_t)(row0 + kRowsPerPass * r) * DK + 32 * m + 4 * lane8),
                    s[r][m]);
+    commit_tail_store(ct, p.tail + (size_t)b * GDN_CONV_W * p.C, p.C);
 }
 
 template <int DK, int R>

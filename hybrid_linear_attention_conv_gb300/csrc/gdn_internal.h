@@ -24,6 +24,10 @@ struct DecodeParams {
     int normalize;
     int out_bf16;
     int32_t tok[GDN_MAX_TREE_NODES];  // gather map when used (commit)
+    // commit only: the tree's pre-conv inputs [Tsrc, C] and the conv tail
+    // [4, C] to update from them (nullptr: the tail is left alone)
+    const uint16_t* x_tree;
+    uint16_t* tail;
 };
 
 // One step of the tree walk, computed on the host (depth-first preorder).
@@ -127,12 +131,6 @@ struct CommitBatchParams {
     int8_t path[32][GDN_MAX_TREE_NODES];   // its path, root first (node indices)
 };
 
-struct TailParams {
-    const uint16_t* x_tree;  // [N, C]
-    uint16_t* tail;          // [4, C]
-    int C, L;
-    int32_t path[GDN_MAX_TREE_NODES];
-};
 
 // Host validation shared by the entry points (gdn_api.cu).  Both record a
 // message for gdn_last_error() and return a gdn_status.
@@ -158,8 +156,6 @@ cudaError_t launch_gates(const GatesParams& p, cudaStream_t s);
 constexpr int kFusedMaxTokens = 16;
 constexpr int kFusedMaxSmem = 48 * 1024;
 cudaError_t launch_conv(const ConvParams& p, cudaStream_t s);
-cudaError_t launch_commit_tail(const TailParams& p, cudaStream_t s);
 cudaError_t launch_commit_batched(const CommitBatchParams& p, int dk, int rows_per_cta, cudaStream_t s);
-cudaError_t launch_commit_tail_batched(const CommitBatchParams& p, cudaStream_t s);
 
 }  // namespace gdn
