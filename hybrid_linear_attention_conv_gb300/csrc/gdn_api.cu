@@ -150,6 +150,30 @@ int check_path(int N, const int32_t* parents, const int32_t* path, int L) {
     return GDN_OK;
 }
 
+// The tree conv's ancestor table: node n's m-th earlier input (m = 0 .. 2,
+// nearest first) is its m+1-th ancestor, or, past the root, the tail's slots
+// from the newest down (-1 - slot).
+void conv_ancestors(int N, const int32_t* parents, int8_t (*anc)[3]) {
+    for (int n = 0; n < N; ++n) {
+        int a = n, tail_slot = GDN_CONV_W - 1;
+        for (int m = 0; m < GDN_CONV_W - 1; ++m) {
+            if (a >= 0) a = parents[a];
+            if (a >= 0) {
+                anc[n][m] = (int8_t)a;
+            } else {
+                anc[n][m] = (int8_t)(-1 - tail_slot);
+                tail_slot -= 1;
+            }
+        }
+    }
+}
+
+// true when [a, a + n) and [b, b + n) share a byte
+bool overlaps(const void* a, const void* b, size_t n) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + n && y < x + n;
+}
+
 int sm_count() {
     // relaxed atomics: host threads may race to fill an entry, all with the same value
     static std::atomic<int> cached[64];
@@ -268,20 +292,7 @@ int gdn_conv_step(int32_t B, int32_t T, int32_t C, const int32_t* parents, const
     p.C = C;
     p.f32 = (flags & GDN_IN_F32) != 0;
     p.tree = parents != nullptr;
-    if (p.tree) {
-        for (int n = 0; n < T; ++n) {
-            int a = n, tail_slot = GDN_CONV_W - 1;
-            for (int m = 0; m < GDN_CONV_W - 1; ++m) {
-                if (a >= 0) a = parents[a];
-                if (a >= 0) {
-                    p.anc[n][m] = (int8_t)a;
-                } else {
-                    p.anc[n][m] = (int8_t)(-1 - tail_slot);
-                    tail_slot -= 1;
-                }
-            }
-        }
-    }
+    if (p.tree) conv_ancestors(T, parents, p.anc);
     cudaError_t e = launch_conv(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "conv launch");
 }
@@ -474,19 +485,37 @@ int gdn_gates(int64_t n, int32_t Hv, const gdn_bf16* a, const gdn_bf16* b, const
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gates launch");
 }
 
-int gdn_tree_verify(const gdn_shape* shape, int32_t N, const int32_t* parents, const gdn_bf16* qkv,
-                    const float* alpha, const float* beta, const float* state, void* out,
-                    float q_scale, uint32_t flags, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Tree verify of one tree (conv == false: post-conv qkv) or with the tree
+// conv fused in (x, w, tail: pre-conv inputs).
+int tree_verify_impl(const gdn_shape* shape, int32_t N, const int32_t* parents, const gdn_bf16* qkv,
+                     const gdn_bf16* x, const gdn_bf16* w, const gdn_bf16* tail, bool conv, const float* alpha,
+                     const float* beta, const float* state, void* out, float q_scale, uint32_t flags,
+                     void* stream) {
     int rc;
     if ((rc = check_shape(shape, true)) != GDN_OK) return rc;
     if ((rc = check_flags(flags)) != GDN_OK) return rc;
     if ((rc = check_parents(N, parents)) != GDN_OK) return rc;
-    if ((rc = check_ptr(qkv, "qkv")) || (rc = check_ptr(alpha, "alpha")) || (rc = check_ptr(beta, "beta")) ||
-        (rc = check_ptr(state, "state")) || (rc = check_ptr(out, "out")))
+    if (conv) {
+        if ((rc = check_ptr(x, "x")) || (rc = check_ptr(w, "w")) || (rc = check_ptr(tail, "tail"))) return rc;
+    } else if ((rc = check_ptr(qkv, "qkv")) != GDN_OK) {
+        return rc;
+    }
+    if ((rc = check_ptr(alpha, "alpha")) || (rc = check_ptr(beta, "beta")) || (rc = check_ptr(state, "state")) ||
+        (rc = check_ptr(out, "out")))
         return rc;
     TreeParams p{};
     if ((rc = schedule_tree(N, parents, p.steps[0], &p.n_slots)) != GDN_OK) return rc;
     p.qkv = qkv;
+    if (conv) {
+        p.x = x;
+        p.w = w;
+        p.tail = tail;
+        conv_ancestors(N, parents, p.anc[0]);
+    }
     p.alpha = alpha;
     p.beta = beta;
     p.state = state;
@@ -503,12 +532,13 @@ int gdn_tree_verify(const gdn_shape* shape, int32_t N, const int32_t* parents, c
     p.normalize = (flags & GDN_NORMALIZE_QK) != 0;
     p.out_bf16 = (flags & GDN_OUT_BF16) != 0;
     cudaError_t e = launch_tree(p, shape->dk, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "tree verify launch");
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, conv ? "conv + tree verify launch" : "tree verify launch");
 }
 
-int gdn_tree_verify_batched(const gdn_shape* shape, int32_t N, const int32_t* counts, const int32_t* parents,
-                            const gdn_bf16* qkv, const float* alpha, const float* beta, const float* state,
-                            void* out, float q_scale, uint32_t flags, void* stream) {
+int tree_verify_batched_impl(const gdn_shape* shape, int32_t N, const int32_t* counts, const int32_t* parents,
+                             const gdn_bf16* qkv, const gdn_bf16* x, const gdn_bf16* w, const gdn_bf16* tail,
+                             bool conv, const float* alpha, const float* beta, const float* state, void* out,
+                             float q_scale, uint32_t flags, void* stream) {
     int rc;
     if ((rc = check_shape(shape, false)) != GDN_OK) return rc;
     if ((rc = check_flags(flags)) != GDN_OK) return rc;
@@ -517,10 +547,15 @@ int gdn_tree_verify_batched(const gdn_shape* shape, int32_t N, const int32_t* co
     if (N < 1 || N > GDN_MAX_TREE_NODES)
         return fail(GDN_ERR_BAD_PARENTS, "node capacity N=%d outside [1, %d]", N, GDN_MAX_TREE_NODES);
     if (counts == nullptr || parents == nullptr) return fail(GDN_ERR_INVALID_ARG, "counts / parents is NULL");
-    if ((rc = check_ptr(qkv, "qkv")) || (rc = check_ptr(alpha, "alpha")) || (rc = check_ptr(beta, "beta")) ||
-        (rc = check_ptr(state, "state")) || (rc = check_ptr(out, "out")))
+    if (conv) {
+        if ((rc = check_ptr(x, "x")) || (rc = check_ptr(w, "w")) || (rc = check_ptr(tail, "tail"))) return rc;
+    } else if ((rc = check_ptr(qkv, "qkv")) != GDN_OK) {
         return rc;
-    static thread_local TreeParamsBatch p;  // 8 KB of schedules: kept off the stack
+    }
+    if ((rc = check_ptr(alpha, "alpha")) || (rc = check_ptr(beta, "beta")) || (rc = check_ptr(state, "state")) ||
+        (rc = check_ptr(out, "out")))
+        return rc;
+    static thread_local TreeParamsBatch p;  // 14 KB of schedules and ancestor tables: kept off the stack
     p = TreeParamsBatch{};
     for (int b = 0; b < shape->B; ++b) {
         if (counts[b] < 1 || counts[b] > N)
@@ -534,10 +569,16 @@ int gdn_tree_verify_batched(const gdn_shape* shape, int32_t N, const int32_t* co
             const std::string why = t_error;
             return fail(rc, "tree %d: %s", b, why.c_str());
         }
+        if (conv) conv_ancestors(counts[b], parents + (size_t)b * N, p.anc[b]);
         p.N[b] = counts[b];
         if (slots > p.n_slots) p.n_slots = slots;
     }
     p.qkv = qkv;
+    if (conv) {
+        p.x = x;
+        p.w = w;
+        p.tail = tail;
+    }
     p.alpha = alpha;
     p.beta = beta;
     p.state = state;
@@ -553,7 +594,118 @@ int gdn_tree_verify_batched(const gdn_shape* shape, int32_t N, const int32_t* co
     p.normalize = (flags & GDN_NORMALIZE_QK) != 0;
     p.out_bf16 = (flags & GDN_OUT_BF16) != 0;
     cudaError_t e = launch_tree(p, shape->dk, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "batched tree verify launch");
+    return e == cudaSuccess ? GDN_OK
+                            : cuda_fail(e, conv ? "batched conv + tree verify launch" : "batched tree verify launch");
+}
+
+// Commit of B sequences' paths through the batched kernel.  Fused conv when
+// w != nullptr: x_tree and tail_in required, tail_out written for every
+// sequence (distinct from tail_in); else qkv required and tail updated in
+// place when x_tree is given.
+int commit_batched_impl(const gdn_shape* shape, int32_t N, const int32_t* counts, const int32_t* parents,
+                        const int32_t* paths, const int32_t* lengths, const gdn_bf16* qkv, const float* alpha,
+                        const float* beta, const gdn_bf16* x_tree, float* state, gdn_bf16* tail,
+                        const gdn_bf16* w, const gdn_bf16* tail_in, uint32_t flags, void* stream) {
+    const bool conv = w != nullptr;
+    int rc;
+    if ((rc = check_shape(shape, false)) != GDN_OK) return rc;
+    if (flags & GDN_OUT_BF16) return fail(GDN_ERR_INVALID_ARG, "commit writes no output; GDN_OUT_BF16 not allowed");
+    if ((rc = check_flags(flags)) != GDN_OK) return rc;
+    if (shape->B < 1 || shape->B > kMaxTreeBatch)
+        return fail(GDN_ERR_UNSUPPORTED_SHAPE, "B=%d trees, one call commits 1 .. %d", shape->B, kMaxTreeBatch);
+    if (N < 1 || N > GDN_MAX_TREE_NODES)
+        return fail(GDN_ERR_BAD_PARENTS, "node capacity N=%d outside [1, %d]", N, GDN_MAX_TREE_NODES);
+    if (counts == nullptr || parents == nullptr || lengths == nullptr)
+        return fail(GDN_ERR_INVALID_ARG, "counts / parents / lengths is NULL");
+    static thread_local CommitBatchParams p;  // 2 KB of paths: kept off the stack
+    p = CommitBatchParams{};
+    int total = 0;
+    for (int b = 0; b < shape->B; ++b) {
+        if (counts[b] < 1 || counts[b] > N)
+            return fail(GDN_ERR_BAD_PARENTS, "tree %d has %d nodes, need 1 .. %d", b, counts[b], N);
+        const int32_t* par = parents + (size_t)b * N;
+        if ((rc = check_parents(counts[b], par)) != GDN_OK) {
+            const std::string why = t_error;
+            return fail(rc, "tree %d: %s", b, why.c_str());
+        }
+        const int L = lengths[b];
+        if (L > 0 && paths == nullptr) return fail(GDN_ERR_INVALID_ARG, "paths is NULL");
+        if ((rc = check_path(counts[b], par, L > 0 ? paths + (size_t)b * N : nullptr, L)) != GDN_OK) {
+            const std::string why = t_error;
+            return fail(rc, "tree %d: %s", b, why.c_str());
+        }
+        p.L[b] = L;
+        for (int i = 0; i < L; ++i) p.path[b][i] = (int8_t)paths[(size_t)b * N + i];
+        total += L;
+    }
+    if (conv) {
+        if ((rc = check_ptr(x_tree, "x")) || (rc = check_ptr(tail_in, "tail_in")) ||
+            (rc = check_ptr(tail, "tail_out")))
+            return rc;
+        const size_t tail_bytes = (size_t)shape->B * GDN_CONV_W * packed_channels(shape) * sizeof(gdn_bf16);
+        if (overlaps(tail_in, tail, tail_bytes))
+            return fail(GDN_ERR_INVALID_ARG, "tail_in and tail_out overlap (they must be distinct buffers)");
+    } else {
+        if ((rc = check_ptr(qkv, "qkv")) || (rc = check_ptr(x_tree, "x_tree", false))) return rc;
+        if (x_tree != nullptr && (rc = check_ptr(tail, "tail")) != GDN_OK) return rc;
+    }
+    if ((rc = check_ptr(alpha, "alpha")) || (rc = check_ptr(beta, "beta")) || (rc = check_ptr(state, "state")))
+        return rc;
+    if (total == 0 && !conv) return GDN_OK;  // no sequence accepted anything (the fused conv still moves the tails)
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    p.qkv = conv ? nullptr : qkv;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.state = state;
+    p.x_tree = x_tree;
+    p.tail = tail;
+    p.w = w;
+    p.tail_in = conv ? tail_in : nullptr;
+    p.B = shape->B;
+    p.N = N;
+    p.Hk = shape->Hk;
+    p.Hv = shape->Hv;
+    p.dv = shape->dv;
+    p.group = shape->Hv / shape->Hk;
+    p.C = packed_channels(shape);
+    p.normalize = (flags & GDN_NORMALIZE_QK) != 0;
+    const int rows = decode_rows_per_cta(shape->B, shape->Hv, shape->dv);
+    cudaError_t e = launch_commit_batched(p, shape->dk, rows, st);  // the tails too, when x_tree is given
+    if (e != cudaSuccess) return cuda_fail(e, conv ? "conv + commit launch" : "batched commit launch");
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_tree_verify(const gdn_shape* shape, int32_t N, const int32_t* parents, const gdn_bf16* qkv,
+                    const float* alpha, const float* beta, const float* state, void* out,
+                    float q_scale, uint32_t flags, void* stream) {
+    return tree_verify_impl(shape, N, parents, qkv, nullptr, nullptr, nullptr, false, alpha, beta, state, out,
+                            q_scale, flags, stream);
+}
+
+int gdn_conv_tree_verify(const gdn_shape* shape, int32_t N, const int32_t* parents, const gdn_bf16* x,
+                         const gdn_bf16* w, const gdn_bf16* tail, const float* alpha, const float* beta,
+                         const float* state, void* out, float q_scale, uint32_t flags, void* stream) {
+    return tree_verify_impl(shape, N, parents, nullptr, x, w, tail, true, alpha, beta, state, out, q_scale, flags,
+                            stream);
+}
+
+int gdn_tree_verify_batched(const gdn_shape* shape, int32_t N, const int32_t* counts, const int32_t* parents,
+                            const gdn_bf16* qkv, const float* alpha, const float* beta, const float* state,
+                            void* out, float q_scale, uint32_t flags, void* stream) {
+    return tree_verify_batched_impl(shape, N, counts, parents, qkv, nullptr, nullptr, nullptr, false, alpha, beta,
+                                    state, out, q_scale, flags, stream);
+}
+
+int gdn_conv_tree_verify_batched(const gdn_shape* shape, int32_t N, const int32_t* counts, const int32_t* parents,
+                                 const gdn_bf16* x, const gdn_bf16* w, const gdn_bf16* tail, const float* alpha,
+                                 const float* beta, const float* state, void* out, float q_scale, uint32_t flags,
+                                 void* stream) {
+    return tree_verify_batched_impl(shape, N, counts, parents, nullptr, x, w, tail, true, alpha, beta, state, out,
+                                    q_scale, flags, stream);
 }
 
 int gdn_commit_path(const gdn_shape* shape, int32_t N, const int32_t* parents, const int32_t* path,
@@ -602,61 +754,31 @@ int gdn_commit_path_batched(const gdn_shape* shape, int32_t N, const int32_t* co
                             const int32_t* paths, const int32_t* lengths, const gdn_bf16* qkv, const float* alpha,
                             const float* beta, const gdn_bf16* x_tree, float* state, gdn_bf16* tail, uint32_t flags,
                             void* stream) {
+    return commit_batched_impl(shape, N, counts, parents, paths, lengths, qkv, alpha, beta, x_tree, state, tail,
+                               nullptr, nullptr, flags, stream);
+}
+
+int gdn_conv_commit_path(const gdn_shape* shape, int32_t N, const int32_t* parents, const int32_t* path, int32_t L,
+                         const gdn_bf16* x, const gdn_bf16* w, const gdn_bf16* tail_in, gdn_bf16* tail_out,
+                         const float* alpha, const float* beta, float* state, uint32_t flags, void* stream) {
     int rc;
-    if ((rc = check_shape(shape, false)) != GDN_OK) return rc;
-    if (flags & GDN_OUT_BF16) return fail(GDN_ERR_INVALID_ARG, "commit writes no output; GDN_OUT_BF16 not allowed");
-    if ((rc = check_flags(flags)) != GDN_OK) return rc;
-    if (shape->B < 1 || shape->B > kMaxTreeBatch)
-        return fail(GDN_ERR_UNSUPPORTED_SHAPE, "B=%d trees, one call commits 1 .. %d", shape->B, kMaxTreeBatch);
+    if ((rc = check_shape(shape, true)) != GDN_OK) return rc;
+    if ((rc = check_ptr(w, "w")) != GDN_OK) return rc;
     if (N < 1 || N > GDN_MAX_TREE_NODES)
-        return fail(GDN_ERR_BAD_PARENTS, "node capacity N=%d outside [1, %d]", N, GDN_MAX_TREE_NODES);
-    if (counts == nullptr || parents == nullptr || lengths == nullptr)
-        return fail(GDN_ERR_INVALID_ARG, "counts / parents / lengths is NULL");
-    static thread_local CommitBatchParams p;  // 2 KB of paths: kept off the stack
-    p = CommitBatchParams{};
-    int total = 0;
-    for (int b = 0; b < shape->B; ++b) {
-        if (counts[b] < 1 || counts[b] > N)
-            return fail(GDN_ERR_BAD_PARENTS, "tree %d has %d nodes, need 1 .. %d", b, counts[b], N);
-        const int32_t* par = parents + (size_t)b * N;
-        if ((rc = check_parents(counts[b], par)) != GDN_OK) {
-            const std::string why = t_error;
-            return fail(rc, "tree %d: %s", b, why.c_str());
-        }
-        const int L = lengths[b];
-        if (L > 0 && paths == nullptr) return fail(GDN_ERR_INVALID_ARG, "paths is NULL");
-        if ((rc = check_path(counts[b], par, L > 0 ? paths + (size_t)b * N : nullptr, L)) != GDN_OK) {
-            const std::string why = t_error;
-            return fail(rc, "tree %d: %s", b, why.c_str());
-        }
-        p.L[b] = L;
-        for (int i = 0; i < L; ++i) p.path[b][i] = (int8_t)paths[(size_t)b * N + i];
-        total += L;
-    }
-    if ((rc = check_ptr(qkv, "qkv")) || (rc = check_ptr(alpha, "alpha")) || (rc = check_ptr(beta, "beta")) ||
-        (rc = check_ptr(state, "state")) || (rc = check_ptr(x_tree, "x_tree", false)))
-        return rc;
-    if (x_tree != nullptr && (rc = check_ptr(tail, "tail")) != GDN_OK) return rc;
-    if (total == 0) return GDN_OK;  // no sequence accepted anything
-    const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    p.qkv = qkv;
-    p.alpha = alpha;
-    p.beta = beta;
-    p.state = state;
-    p.x_tree = x_tree;
-    p.tail = tail;
-    p.B = shape->B;
-    p.N = N;
-    p.Hk = shape->Hk;
-    p.Hv = shape->Hv;
-    p.dv = shape->dv;
-    p.group = shape->Hv / shape->Hk;
-    p.C = packed_channels(shape);
-    p.normalize = (flags & GDN_NORMALIZE_QK) != 0;
-    const int rows = decode_rows_per_cta(shape->B, shape->Hv, shape->dv);
-    cudaError_t e = launch_commit_batched(p, shape->dk, rows, st);  // the tails too, when x_tree is given
-    if (e != cudaSuccess) return cuda_fail(e, "batched commit launch");
-    return GDN_OK;
+        return fail(GDN_ERR_BAD_PARENTS, "tree size N=%d outside [1, %d]", N, GDN_MAX_TREE_NODES);
+    const int32_t counts[1] = {N}, lengths[1] = {L};
+    return commit_batched_impl(shape, N, counts, parents, path, lengths, nullptr, alpha, beta, x, state, tail_out,
+                               w, tail_in, flags, stream);
+}
+
+int gdn_conv_commit_path_batched(const gdn_shape* shape, int32_t N, const int32_t* counts, const int32_t* parents,
+                                 const int32_t* paths, const int32_t* lengths, const gdn_bf16* x, const gdn_bf16* w,
+                                 const gdn_bf16* tail_in, gdn_bf16* tail_out, const float* alpha, const float* beta,
+                                 float* state, uint32_t flags, void* stream) {
+    int rc;
+    if ((rc = check_ptr(w, "w")) != GDN_OK) return rc;
+    return commit_batched_impl(shape, N, counts, parents, paths, lengths, nullptr, alpha, beta, x, state, tail_out,
+                               w, tail_in, flags, stream);
 }
 
 }  // extern "C"

@@ -42,6 +42,12 @@ __host__ __device__ constexpr size_t conv_decode_prefetch_bytes() {
 }
 __host__ __device__ constexpr size_t align16(size_t n) { return (n + 15) / 16 * 16; }
 
+// One 16-byte global -> shared copy (cp.async, L2 only); both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+    const uint32_t dst = (uint32_t)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(gsrc) : "memory");
+}
+
 // The conv-tail update of a commit, done by the commit's own launch: the
 // tail becomes the last four inputs of (tail ++ x_tree[path[0]] ++ ...), 8
 // channels (one 16-byte vector) per thread of the grid, copied as they are.
@@ -162,43 +168,101 @@ gdn_decode_kernel(const __grid_constant__ DecodeParams p) {
 // through the shared step, exactly as gdn_decode_kernel does with a gather
 // map (the same functions in the same order), so each sequence's result is the
 // bits of gdn_commit_path on its tree alone.
+//
+// Fused conv (p.w set): before the replay, the CTA computes the conv outputs
+// of the path's tokens for the channels it reads (q and k of its key head, v
+// of its own rows) into shared memory, [L][2 DK + 32 R] bf16, with the
+// arithmetic and rounding of gdn_conv_step.  The path is a root path, so the
+// inputs before token t are path[t-1], path[t-2], ... then the tail's newest
+// entries: the tree conv of node path[t].
+template <int DK, int R>
+__host__ __device__ constexpr size_t commit_conv_bytes(int L) {
+    return (size_t)L * (2 * DK + kRowsPerPass * R) * 2;
+}
+
 template <int DK, int R>
 __global__ void __launch_bounds__(kThreads, 2)
 gdn_commit_batched_kernel(const __grid_constant__ CommitBatchParams p) {
     constexpr int V = DK / 32;
+    constexpr int ROWS = kRowsPerPass * R;
+    constexpr int YW = 2 * DK + ROWS;  // one token's conv outputs in shared memory
     const int lane8 = threadIdx.x & 7;
     const int rg = threadIdx.x >> 3;
     const int h = blockIdx.y;
     const int b = blockIdx.z;
     const int L = p.L[b];
-    if (L == 0) return;  // nothing accepted for this sequence
+    const bool conv = p.w != nullptr;
+    if (L == 0 && !conv) return;  // nothing accepted for this sequence
     CommitTail ct;  // sequence b's conv tail, by sequence b's CTAs (far more threads than C / 8)
     ct.mine = false;
     if (p.x_tree != nullptr)
-        commit_tail_load(ct, p.x_tree + (size_t)b * p.N * p.C, p.tail + (size_t)b * GDN_CONV_W * p.C, p.C, L,
-                         p.path[b], ((long long)blockIdx.y * gridDim.x + blockIdx.x) * kThreads + threadIdx.x);
+        commit_tail_load(ct, p.x_tree + (size_t)b * p.N * p.C,
+                         (conv ? p.tail_in : p.tail) + (size_t)b * GDN_CONV_W * p.C, p.C, L, p.path[b],
+                         ((long long)blockIdx.y * gridDim.x + blockIdx.x) * kThreads + threadIdx.x);
+    if (L == 0) {  // the fused conv: the tail is carried over to the output buffer as it is
+        commit_tail_store(ct, p.tail + (size_t)b * GDN_CONV_W * p.C, p.C);
+        return;
+    }
     const int g = h / p.group;
-    const int row0 = blockIdx.x * (kRowsPerPass * R) + rg;
+    const int row0 = blockIdx.x * ROWS + rg;
     float* S = p.state + ((size_t)b * p.Hv + h) * (size_t)p.dv * DK;
     float4 s[R][V];
+    auto load_state = [&]() {
 #pragma unroll
-    for (int r = 0; r < R; ++r)
+        for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int m = 0; m < V; ++m)
-            s[r][m] = __ldcs(reinterpret_cast<const float4*>(S + (size_t)(row0 + kRowsPerPass * r) * DK + 32 * m +
-                                                             4 * lane8));
+            for (int m = 0; m < V; ++m)
+                s[r][m] = __ldcs(reinterpret_cast<const float4*>(S + (size_t)(row0 + kRowsPerPass * r) * DK +
+                                                                 32 * m + 4 * lane8));
+    };
+    // The state rows are requested before the fused conv's loads, so that the
+    // two DRAM round trips overlap -- except with four rows per thread, where
+    // the 64 state registers and the conv's taps and windows would not fit
+    // together in the register budget of two CTAs per SM.
+    constexpr bool kStateFirst = R < 4;
+    if (kStateFirst || !conv) load_state();
+    extern __shared__ uint4 smem_commit[];
+    uint16_t* ys = reinterpret_cast<uint16_t*>(smem_commit);  // the fused conv's outputs, [L][YW]
+    if (conv) {
+        const uint16_t* xb = p.x_tree + (size_t)b * p.N * p.C;
+        const uint16_t* tb = p.tail_in + (size_t)b * GDN_CONV_W * p.C;
+        const int8_t* path = p.path[b];
+        constexpr int QK8 = 2 * DK / 8, PER = YW / 8;
+        for (int idx = threadIdx.x; idx < L * PER; idx += kThreads) {
+            const int t = idx / PER, c = idx % PER;
+            const int gc = c < DK / 8 ? g * DK + 8 * c
+                         : c < QK8    ? p.Hk * DK + g * DK + 8 * (c - DK / 8)
+                                      : 2 * p.Hk * DK + h * p.dv + blockIdx.x * ROWS + 8 * (c - QK8);
+            float w[8][4];
+            load_taps8(p.w + (size_t)gc * GDN_CONV_W, w);
+            // input j of (tail ++ x_tree[path]) counted from the path's start: j < 0 is tail slot 4 + j
+            auto in = [&](int j) -> Vec8 {
+                return j >= 0 ? load8(xb + (size_t)path[j] * p.C + gc) : load8(tb + (size_t)(GDN_CONV_W + j) * p.C + gc);
+            };
+            store_y(ys + (size_t)t * YW + 8 * c, w, in(t - 3), in(t - 2), in(t - 1), in(t));
+        }
+        if (!kStateFirst) load_state();
+        __syncthreads();
+    }
     const bool normalize = p.normalize != 0;
     for (int t = 0; t < L; ++t) {
         const size_t trow = (size_t)b * p.N + p.path[b][t];
-        const uint16_t* row = p.qkv + trow * (size_t)p.C;
         TokenKQ<V> kq;
-        token_kq<V>(row + g * DK, row + (size_t)p.Hk * DK + g * DK, lane8, 1.0f, normalize, kq);
+        const uint16_t* vrow;  // v of this CTA's row r at vrow[kRowsPerPass * r]
+        if (conv) {
+            const uint16_t* yt = ys + (size_t)t * YW;
+            token_kq<V>(yt, yt + DK, lane8, 1.0f, normalize, kq);
+            vrow = yt + 2 * DK + rg;
+        } else {
+            const uint16_t* row = p.qkv + trow * (size_t)p.C;
+            token_kq<V>(row + g * DK, row + (size_t)p.Hk * DK + g * DK, lane8, 1.0f, normalize, kq);
+            vrow = row + (size_t)2 * p.Hk * DK + (size_t)h * p.dv + row0;
+        }
         const float alpha = p.alpha[trow * p.Hv + h];
         const float beta = p.beta[trow * p.Hv + h];
-        const uint16_t* vrow = row + (size_t)2 * p.Hk * DK + (size_t)h * p.dv;
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const float v_i = act_f(vrow[row0 + kRowsPerPass * r]);
+            const float v_i = act_f(vrow[kRowsPerPass * r]);
             row_step<V>(s[r], kq, v_i, alpha, beta);
         }
     }
@@ -214,7 +278,12 @@ gdn_commit_batched_kernel(const __grid_constant__ CommitBatchParams p) {
 template <int DK, int R>
 static cudaError_t launch_commit_batched_t(const CommitBatchParams& p, cudaStream_t s) {
     dim3 grid(p.dv / (kRowsPerPass * R), p.Hv, p.B);
-    gdn_commit_batched_kernel<DK, R><<<grid, kThreads, 0, s>>>(p);
+    int lmax = 0;
+    for (int b = 0; b < p.B; ++b) lmax = std::max(lmax, (int)p.L[b]);
+    const size_t smem = p.w != nullptr ? commit_conv_bytes<DK, R>(lmax) : 0;
+    // at most 64 tokens x (2 x 128 + 128) channels x 2 bytes = 48 KB: no opt-in needed
+    if (smem > 48 * 1024) return cudaErrorInvalidValue;
+    gdn_commit_batched_kernel<DK, R><<<grid, kThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 
@@ -252,6 +321,24 @@ __host__ __device__ constexpr size_t tree_stage_bytes(int N) {
     return tree_kq_bytes<DK>(N) + (size_t)N * (kRowsPerPass * R * 2 + 2 * 4 + sizeof(TreeStep));
 }
 
+// The region in front of the staging: the walk's branch slots, which the
+// fused conv uses first (it is done before the walk writes its first slot):
+//   y_qk  [N][2 DK] bf16      the conv outputs of the key head's q and k
+//   xs    [N + 3][2 DK + 32 R] bf16  the conv inputs of the CTA's channels:
+//         tail slots 1..3, then the N nodes
+//   ws    [2 DK + 32 R][4] bf16      their taps
+template <int DK, int R>
+__host__ __device__ constexpr size_t tree_conv_bytes(int N) {
+    return (size_t)N * 2 * DK * 2 + ((size_t)N + 3 + 4) * (2 * DK + kRowsPerPass * R) * 2;
+}
+
+template <int DK, int R>
+__host__ __device__ constexpr size_t tree_slot_bytes(int n_slots, int N, bool conv) {
+    const size_t slots = (size_t)n_slots * kRowsPerPass * R * DK * sizeof(float);
+    const size_t c = conv ? tree_conv_bytes<DK, R>(N) : 0;
+    return slots > c ? slots : c;
+}
+
 // The tree walk.  A thread keeps R rows of the state (rows rg + 32 r of this
 // CTA's 32 R), so that each node's k and q, fetched from shared memory once
 // per thread, serve R rows: the walk is bound by those fetches (every row of
@@ -267,9 +354,10 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     const uint16_t* qkv = p.qkv + (size_t)tree * p.Nmax * p.C;
     const float* alpha_b = p.alpha + (size_t)tree * p.Nmax * p.Hv;
     const float* beta_b = p.beta + (size_t)tree * p.Nmax * p.Hv;
+    const bool conv = p.x != nullptr;  // pre-conv inputs: the tree conv runs here
     extern __shared__ float4 smem4[];
     float4* slots = smem4;  // [n_slots][R][32 row groups][V][8 lanes]
-    uint8_t* stage = reinterpret_cast<uint8_t*>(smem4) + (size_t)p.n_slots * ROWS * DK * sizeof(float);
+    uint8_t* stage = reinterpret_cast<uint8_t*>(smem4) + tree_slot_bytes<DK, R>(p.n_slots, p.Nmax, conv);
     float4* s_kq = reinterpret_cast<float4*>(stage);                                   // per-node records
     uint16_t* s_v = reinterpret_cast<uint16_t*>(stage + tree_kq_bytes<DK>(p.Nmax));        // [N][32 R]
     float* s_ab = reinterpret_cast<float*>(s_v + (size_t)p.Nmax * ROWS);                    // [N][alpha, beta]
@@ -285,18 +373,8 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     // node n's record in s_kq: [V float4 of k, V float4 of q][8 lanes], then k.q
     constexpr int KQ_REC = 8 * 2 * V + 1;  // float4 units
 
-    {
-        for (int idx = threadIdx.x; idx < N * (ROWS / 8); idx += kThreads) {
-            const int n = idx / (ROWS / 8), c = idx % (ROWS / 8);
-            const uint16_t* src = qkv + (size_t)n * p.C + (size_t)2 * p.Hk * DK + (size_t)h * p.dv + row0 + c * 8;
-            *reinterpret_cast<uint4*>(s_v + (size_t)n * ROWS + c * 8) = __ldg(reinterpret_cast<const uint4*>(src));
-        }
-        for (int n = threadIdx.x; n < N; n += kThreads) {
-            s_ab[2 * n] = alpha_b[(size_t)n * p.Hv + h];
-            s_ab[2 * n + 1] = beta_b[(size_t)n * p.Hv + h];
-            steps[n] = p.steps[tree][n];
-        }
-    }
+    // this thread's rows of the committed state, requested before the staging
+    // loads so that the two DRAM round trips overlap
     const float* S = p.state + ((size_t)tree * p.Hv + h) * p.dv * DK + (size_t)row * DK;
     float4 s[R][V];
 #pragma unroll
@@ -304,6 +382,67 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
 #pragma unroll
         for (int m = 0; m < V; ++m)
             s[r][m] = __ldg(reinterpret_cast<const float4*>(S + (size_t)kRowsPerPass * r * DK + 32 * m + 4 * lane8));
+
+    // conv: node n's q and k of key head g, [N][2 DK] bf16, in the slot region
+    uint16_t* y_qk = reinterpret_cast<uint16_t*>(smem4);
+    if (conv) {
+        // The tree conv of every node, for the channels this CTA reads: q and
+        // k of key head g and its own rows of v (the arithmetic and bf16
+        // rounding of gdn_conv_step in tree mode).  A node's earlier inputs are
+        // its nearest ancestors, then the tail.  First every input row and the
+        // taps of these channels are copied to shared memory, all copies in
+        // flight together (one DRAM round trip, beside the state loads above);
+        // then each task (a node and 8 channels) computes from there.
+        constexpr int QK8 = 2 * DK / 8, PER = QK8 + ROWS / 8, CW = 8 * PER;
+        uint16_t* xs = y_qk + (size_t)p.Nmax * 2 * DK;   // [N + 3][CW]
+        uint16_t* ws = xs + ((size_t)p.Nmax + 3) * CW;   // [CW][4]
+        const uint16_t* xb = p.x + (size_t)tree * p.Nmax * p.C;
+        const uint16_t* tb = p.tail + (size_t)tree * GDN_CONV_W * p.C;
+        auto chan = [&](int c) {  // the packed channel of this CTA's vector c
+            return c < DK / 8 ? g * DK + 8 * c
+                 : c < QK8    ? p.Hk * DK + g * DK + 8 * (c - DK / 8)
+                              : 2 * p.Hk * DK + h * p.dv + row0 + 8 * (c - QK8);
+        };
+        for (int idx = threadIdx.x; idx < (N + 3) * PER; idx += kThreads) {
+            const int r = idx / PER, c = idx % PER;
+            const uint16_t* src = r < 3 ? tb + (size_t)(r + 1) * p.C + chan(c) : xb + (size_t)(r - 3) * p.C + chan(c);
+            cp_async16(xs + (size_t)r * CW + 8 * c, src);
+        }
+        for (int idx = threadIdx.x; idx < PER * 4; idx += kThreads) {  // 8 channels x 4 taps = 4 x 16 bytes
+            const int c = idx >> 2, q = idx & 3;
+            cp_async16(ws + (size_t)c * 32 + 8 * q, p.w + (size_t)chan(c) * GDN_CONV_W + 8 * q);
+        }
+        asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+        __syncthreads();
+        // staged row of input a: a node (a >= 0) or tail slot -1 - a (1 .. 3)
+        auto row_of = [&](int a) { return a >= 0 ? a + 3 : -2 - a; };
+        for (int idx = threadIdx.x; idx < N * PER; idx += kThreads) {
+            const int n = idx / PER, c = idx % PER;
+            float w[8][4];
+            load_taps8(ws + (size_t)c * 32, w);
+            const int8_t* anc = p.anc[tree][n];
+            const uint16_t* xc = xs + 8 * c;
+            const Vec8 u3 = load8(xc + (size_t)(n + 3) * CW);
+            const Vec8 u2 = load8(xc + (size_t)row_of(anc[0]) * CW);
+            const Vec8 u1 = load8(xc + (size_t)row_of(anc[1]) * CW);
+            const Vec8 u0 = load8(xc + (size_t)row_of(anc[2]) * CW);
+            store_y(c < QK8 ? y_qk + (size_t)n * 2 * DK + 8 * c : s_v + (size_t)n * ROWS + 8 * (c - QK8), w, u0, u1,
+                    u2, u3);
+        }
+    } else {
+        for (int idx = threadIdx.x; idx < N * (ROWS / 8); idx += kThreads) {
+            const int n = idx / (ROWS / 8), c = idx % (ROWS / 8);
+            const uint16_t* src = qkv + (size_t)n * p.C + (size_t)2 * p.Hk * DK + (size_t)h * p.dv + row0 + c * 8;
+            *reinterpret_cast<uint4*>(s_v + (size_t)n * ROWS + c * 8) = __ldg(reinterpret_cast<const uint4*>(src));
+        }
+    }
+    {
+        for (int n = threadIdx.x; n < N; n += kThreads) {
+            s_ab[2 * n] = alpha_b[(size_t)n * p.Hv + h];
+            s_ab[2 * n + 1] = beta_b[(size_t)n * p.Hv + h];
+            steps[n] = p.steps[tree][n];
+        }
+    }
     __syncthreads();
 
     const bool normalize = p.normalize != 0;
@@ -318,9 +457,15 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
         const int n = n0 + (rg & 3);
         const bool real = n < N;
         TokenKQ<V> t;
-        const uint16_t* qkv_row = qkv + (size_t)(real ? n : N - 1) * p.C;
-        token_kq<V>(qkv_row + (size_t)g * DK, qkv_row + (size_t)p.Hk * DK + (size_t)g * DK, lane8, p.q_scale,
-                    normalize, t);
+        const int nc = real ? n : N - 1;
+        if (conv) {
+            const uint16_t* yn = y_qk + (size_t)nc * 2 * DK;
+            token_kq<V>(yn, yn + DK, lane8, p.q_scale, normalize, t);
+        } else {
+            const uint16_t* qkv_row = qkv + (size_t)nc * p.C;
+            token_kq<V>(qkv_row + (size_t)g * DK, qkv_row + (size_t)p.Hk * DK + (size_t)g * DK, lane8, p.q_scale,
+                        normalize, t);
+        }
         if (real) {
             float4* rec = s_kq + (size_t)n * KQ_REC + lane8;
 #pragma unroll
@@ -783,7 +928,7 @@ cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int g
 template <int DK, int MB, int R>
 static cudaError_t launch_tree_t(const TreeParamsT<MB>& p, cudaStream_t s) {
     constexpr int ROWS = kRowsPerPass * R;
-    const size_t smem = (size_t)p.n_slots * ROWS * DK * sizeof(float) + tree_stage_bytes<DK, R>(p.Nmax);
+    const size_t smem = tree_slot_bytes<DK, R>(p.n_slots, p.Nmax, p.x != nullptr) + tree_stage_bytes<DK, R>(p.Nmax);
     // the shared-memory opt-in, once per device whatever the host threads
     static std::once_flag once[64];
     static cudaError_t setup_err[64];
@@ -792,8 +937,8 @@ static cudaError_t launch_tree_t(const TreeParamsT<MB>& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::call_once(once[dev], [dev] {
-        const int max_smem = std::min(GDN_MAX_TREE_SLOTS * ROWS * DK * (int)sizeof(float) +
-                                          (int)tree_stage_bytes<DK, R>(GDN_MAX_TREE_NODES),
+        const int max_smem = std::min((int)(tree_slot_bytes<DK, R>(GDN_MAX_TREE_SLOTS, GDN_MAX_TREE_NODES, true) +
+                                            tree_stage_bytes<DK, R>(GDN_MAX_TREE_NODES)),
                                       kMaxSmemPerCta);
         setup_err[dev] = cudaFuncSetAttribute(gdn_tree_kernel<DK, MB, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               max_smem);
@@ -809,7 +954,7 @@ static cudaError_t launch_tree_t(const TreeParamsT<MB>& p, cudaStream_t s) {
 // rows per fetch), else 1.
 template <int DK, int MB>
 static cudaError_t launch_tree_r(const TreeParamsT<MB>& p, cudaStream_t s) {
-    const size_t smem2 = (size_t)p.n_slots * 2 * kRowsPerPass * DK * sizeof(float) + tree_stage_bytes<DK, 2>(p.Nmax);
+    const size_t smem2 = tree_slot_bytes<DK, 2>(p.n_slots, p.Nmax, p.x != nullptr) + tree_stage_bytes<DK, 2>(p.Nmax);
     if (p.dv % (2 * kRowsPerPass) == 0 && smem2 <= (size_t)kMaxSmemPerCta) return launch_tree_t<DK, MB, 2>(p, s);
     return launch_tree_t<DK, MB, 1>(p, s);
 }

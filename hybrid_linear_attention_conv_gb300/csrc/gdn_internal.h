@@ -53,6 +53,12 @@ struct TreeParamsT {
     int n_slots;           // largest number of branch states any tree needs
     int N[MB];             // nodes of tree b
     TreeStep steps[MB][GDN_MAX_TREE_NODES];
+    // Fused conv (x != nullptr; qkv unused): the tree conv of the pre-conv
+    // inputs runs in the kernel.  anc as in ConvParams, per tree.
+    const uint16_t* x;     // bf16 [B, Nmax, C] pre-conv inputs
+    const uint16_t* w;     // bf16 [C, 4]
+    const uint16_t* tail;  // bf16 [B, 4, C] read only
+    int8_t anc[MB][GDN_MAX_TREE_NODES][3];
 };
 constexpr int kMaxTreeBatch = 32;
 using TreeParams = TreeParamsT<1>;
@@ -118,13 +124,18 @@ struct ConvDecodeParams {
 // Commit of the accepted paths of up to kMaxTreeBatch sequences (a joint
 // verify's trees) in one launch: sequence b replays path[b][0 .. L[b] - 1] of
 // its own tree, and its tail takes the last four inputs of (tail ++ x_tree[path]).
+// With w set (the fused conv), the path's conv outputs are computed in the
+// kernel from x_tree and tail_in, qkv is unused, and the new tail goes to
+// `tail`, a buffer distinct from tail_in (every sequence's, L[b] == 0 too).
 struct CommitBatchParams {
     const uint16_t* qkv;     // bf16 [B, N, C] the trees' inputs (post-conv)
     const float* alpha;      // [B, N, Hv]
     const float* beta;       // [B, N, Hv]
     float* state;            // [B, Hv, dv, dk] in place
     const uint16_t* x_tree;  // bf16 [B, N, C] pre-conv inputs, or nullptr (tails untouched)
-    uint16_t* tail;          // bf16 [B, 4, C]
+    uint16_t* tail;          // bf16 [B, 4, C] (in place; the fused conv: written only)
+    const uint16_t* w;       // bf16 [C, 4] the fused conv's taps, or nullptr
+    const uint16_t* tail_in; // bf16 [B, 4, C] the fused conv's tail before the commit
     int B, N, Hk, Hv, dv, group, C;
     int normalize;
     int32_t L[32];                         // path length of sequence b (0: nothing to commit)

@@ -56,6 +56,10 @@ EXPORTS = [
     "gdn_tree_verify_batched",
     "gdn_commit_path",
     "gdn_commit_path_batched",
+    "gdn_conv_tree_verify",
+    "gdn_conv_tree_verify_batched",
+    "gdn_conv_commit_path",
+    "gdn_conv_commit_path_batched",
     "gdn_prefill_workspace_bytes",
     "gdn_chunk_prefill",
     "gdn_prefill_status",
@@ -115,6 +119,10 @@ def load(path: str = LIB_PATH):
             "gdn_tree_verify_batched": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, F, U32, P]),
             "gdn_commit_path": (ctypes.c_int, [SH, I32, P, P, I32, P, P, P, P, P, P, U32, P]),
             "gdn_commit_path_batched": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, P, P, P, U32, P]),
+            "gdn_conv_tree_verify": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, P, F, U32, P]),
+            "gdn_conv_tree_verify_batched": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, P, P, F, U32, P]),
+            "gdn_conv_commit_path": (ctypes.c_int, [SH, I32, P, P, I32, P, P, P, P, P, P, P, U32, P]),
+            "gdn_conv_commit_path_batched": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, P, P, P, P, U32, P]),
             "gdn_prefill_workspace_bytes": (SZ, [SH, I32, I32]),
             "gdn_chunk_prefill": (ctypes.c_int, [SH, I32, I32, P, P, P, P, P, P, SZ, F, U32, P]),
             "gdn_prefill_status": (ctypes.c_int, [P, P, ctypes.POINTER(I32)]),
@@ -412,6 +420,86 @@ def commit_path_batched(counts, parents, paths, lengths, qkv, alpha, beta, state
         _dev(state, torch.float32, "state", (B, Hv, dv, dk)), _dev(tail, torch.bfloat16, "tail", (B, GDN_CONV_W, C)),
         _flags(normalize, False), _stream())
     _check(rc, "gdn_commit_path_batched")
+
+
+def conv_tree_verify(parents, x, w, tail, alpha, beta, state, Hk, Hv, dk, dv, out=None, q_scale=1.0,
+                     normalize=True, out_bf16=False) -> torch.Tensor:
+    """The tree conv and verify in one launch.  x bf16 [N,C] pre-conv, w bf16 [C,4],
+    tail bf16 [4,C] (read only), alpha/beta fp32 [N,Hv], state fp32 [Hv,dv,dk] (read only)."""
+    par, pp = _host_i32(parents, "parents")
+    N = len(par)
+    C = packed_channels(Hk, Hv, dk, dv)
+    if out is None:
+        out = torch.empty((N, Hv, dv), dtype=torch.bfloat16 if out_bf16 else torch.float32, device=x.device)
+    rc = load().gdn_conv_tree_verify(
+        ctypes.byref(_shape(1, Hk, Hv, dk, dv)), N, pp, _dev(x, torch.bfloat16, "x", (N, C)),
+        _dev(w, torch.bfloat16, "w", (C, GDN_CONV_W)), _dev(tail, torch.bfloat16, "tail", (GDN_CONV_W, C)),
+        _dev(alpha, torch.float32, "alpha", (N, Hv)), _dev(beta, torch.float32, "beta", (N, Hv)),
+        _dev(state, torch.float32, "state", (Hv, dv, dk)),
+        _dev(out, torch.bfloat16 if out_bf16 else torch.float32, "out", (N, Hv, dv)),
+        float(q_scale), _flags(normalize, out_bf16), _stream())
+    _check(rc, "gdn_conv_tree_verify")
+    return out
+
+
+def conv_tree_verify_batched(counts, parents, x, w, tail, alpha, beta, state, Hk, Hv, dk, dv, out=None,
+                             q_scale=1.0, normalize=True, out_bf16=False) -> torch.Tensor:
+    """B trees' conv and joint verify in one launch.  counts [B], parents [B,N] (host),
+    x bf16 [B,N,C], w bf16 [C,4], tail bf16 [B,4,C] (read only), alpha/beta fp32 [B,N,Hv],
+    state fp32 [B,Hv,dv,dk] (read only) -> out [B,N,Hv,dv]."""
+    cnt, pc = _host_i32(counts, "counts")
+    par, pp = _host_i32(parents, "parents")
+    B, N = par.shape
+    C = packed_channels(Hk, Hv, dk, dv)
+    if out is None:
+        out = torch.empty((B, N, Hv, dv), dtype=torch.bfloat16 if out_bf16 else torch.float32, device=x.device)
+    rc = load().gdn_conv_tree_verify_batched(
+        ctypes.byref(_shape(B, Hk, Hv, dk, dv)), N, pc, pp, _dev(x, torch.bfloat16, "x", (B, N, C)),
+        _dev(w, torch.bfloat16, "w", (C, GDN_CONV_W)), _dev(tail, torch.bfloat16, "tail", (B, GDN_CONV_W, C)),
+        _dev(alpha, torch.float32, "alpha", (B, N, Hv)), _dev(beta, torch.float32, "beta", (B, N, Hv)),
+        _dev(state, torch.float32, "state", (B, Hv, dv, dk)),
+        _dev(out, torch.bfloat16 if out_bf16 else torch.float32, "out", (B, N, Hv, dv)),
+        float(q_scale), _flags(normalize, out_bf16), _stream())
+    _check(rc, "gdn_conv_tree_verify_batched")
+    return out
+
+
+def conv_commit_path(parents, path, x, w, tail_in, tail_out, alpha, beta, state, Hk, Hv, dk, dv,
+                     normalize=True) -> None:
+    """The commit from pre-conv inputs: x bf16 [N,C], w bf16 [C,4]; tail_in bf16 [4,C] read,
+    tail_out bf16 [4,C] written (a distinct buffer); state fp32 [Hv,dv,dk] in place."""
+    par, pp = _host_i32(parents, "parents")
+    pa, ppa = _host_i32(path, "path")
+    N = len(par)
+    C = packed_channels(Hk, Hv, dk, dv)
+    rc = load().gdn_conv_commit_path(
+        ctypes.byref(_shape(1, Hk, Hv, dk, dv)), N, pp, ppa, len(pa), _dev(x, torch.bfloat16, "x", (N, C)),
+        _dev(w, torch.bfloat16, "w", (C, GDN_CONV_W)), _dev(tail_in, torch.bfloat16, "tail_in", (GDN_CONV_W, C)),
+        _dev(tail_out, torch.bfloat16, "tail_out", (GDN_CONV_W, C)),
+        _dev(alpha, torch.float32, "alpha", (N, Hv)), _dev(beta, torch.float32, "beta", (N, Hv)),
+        _dev(state, torch.float32, "state", (Hv, dv, dk)), _flags(normalize, False), _stream())
+    _check(rc, "gdn_conv_commit_path")
+
+
+def conv_commit_path_batched(counts, parents, paths, lengths, x, w, tail_in, tail_out, alpha, beta, state,
+                             Hk, Hv, dk, dv, normalize=True) -> None:
+    """B sequences' commits from pre-conv inputs in one launch.  counts [B], parents [B,N],
+    paths [B,N], lengths [B] (host); x bf16 [B,N,C], w bf16 [C,4]; tail_in bf16 [B,4,C] read,
+    tail_out bf16 [B,4,C] written for every sequence; state fp32 [B,Hv,dv,dk] in place."""
+    cnt, pc = _host_i32(counts, "counts")
+    par, pp = _host_i32(parents, "parents")
+    pth, ppth = _host_i32(paths, "paths")
+    ln, pl = _host_i32(lengths, "lengths")
+    B, N = par.shape
+    C = packed_channels(Hk, Hv, dk, dv)
+    rc = load().gdn_conv_commit_path_batched(
+        ctypes.byref(_shape(B, Hk, Hv, dk, dv)), N, pc, pp, ppth, pl, _dev(x, torch.bfloat16, "x", (B, N, C)),
+        _dev(w, torch.bfloat16, "w", (C, GDN_CONV_W)),
+        _dev(tail_in, torch.bfloat16, "tail_in", (B, GDN_CONV_W, C)),
+        _dev(tail_out, torch.bfloat16, "tail_out", (B, GDN_CONV_W, C)),
+        _dev(alpha, torch.float32, "alpha", (B, N, Hv)), _dev(beta, torch.float32, "beta", (B, N, Hv)),
+        _dev(state, torch.float32, "state", (B, Hv, dv, dk)), _flags(normalize, False), _stream())
+    _check(rc, "gdn_conv_commit_path_batched")
 
 
 def prefill_workspace_bytes(T, Hk, Hv, dk, dv, chunk=64) -> int:

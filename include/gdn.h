@@ -351,6 +351,86 @@ int gdn_commit_path_batched(const gdn_shape* shape, int32_t N, const int32_t* co
                             void* stream);
 
 /*
+ * The speculative round with the conv fused in.  A round is a tree conv, the
+ * verify and the commit; these entry points take the tree's PRE-conv inputs
+ * and run the 4-tap conv + SiLU inside the verify and commit kernels, so the
+ * conv outputs never reach HBM and the round is two launches instead of three.
+ * Each CTA computes the conv of the channels it reads (its key head's q and k,
+ * its own rows of v) with the arithmetic and bf16 rounding of gdn_conv_step,
+ * so the results are the same bits as the unfused calls.
+ *
+ * gdn_conv_tree_verify -- gdn_conv_step in tree mode (x -> y) followed by
+ * gdn_tree_verify on y, in one launch.  out equals that pair's, bit for bit.
+ *   x       bf16 [N, C_qkv] the nodes' pre-conv inputs (packed [q | k | v]).
+ *   w       bf16 [C_qkv, 4] conv taps (as for gdn_conv_step).
+ *   tail    bf16 [4, C_qkv] the committed conv tail, read only.
+ *   the other arguments as for gdn_tree_verify.
+ * Source: the rule run over "a tree" ("Architecture" v0.11.1, "The parts")
+ * with the per-layer conv tail of v0.14.2 section 8.1; verify the whole tree
+ * in one pass (v0.14.2 section 8.3).
+ */
+int gdn_conv_tree_verify(const gdn_shape* shape, int32_t N, const int32_t* parents,
+                         const gdn_bf16* x, const gdn_bf16* w, const gdn_bf16* tail,
+                         const float* alpha, const float* beta, const float* state, void* out,
+                         float q_scale, uint32_t flags, void* stream);
+
+/*
+ * gdn_conv_tree_verify_batched -- gdn_conv_tree_verify for B sequences in one
+ * launch (the joint verify of gdn_tree_verify_batched with the conv fused in).
+ *   x     bf16 [B, N, C_qkv];  tail  bf16 [B, 4, C_qkv] read only;
+ *   w     bf16 [C_qkv, 4] (one layer's taps, shared by the sequences);
+ *   the other arguments as for gdn_tree_verify_batched.
+ * Each tree's outputs equal, bit for bit, gdn_conv_tree_verify of that tree
+ * alone.  Source: "Architecture" (v0.14.2) section 8.5 (joint verify).
+ */
+int gdn_conv_tree_verify_batched(const gdn_shape* shape, int32_t N, const int32_t* counts,
+                                 const int32_t* parents, const gdn_bf16* x, const gdn_bf16* w,
+                                 const gdn_bf16* tail, const float* alpha, const float* beta,
+                                 const float* state, void* out, float q_scale, uint32_t flags,
+                                 void* stream);
+
+/*
+ * gdn_conv_commit_path -- the commit of the accepted path from the tree's
+ * pre-conv inputs: the path's conv outputs are computed in the kernel, the
+ * state is replayed in place, and the new tail -- the last four inputs of
+ * (tail_in ++ x[path[0]] ++ ... ++ x[path[L-1]]) -- is written to tail_out.
+ * state and tail_out equal, bit for bit, gdn_conv_step (tree mode) followed by
+ * gdn_commit_path with x_tree = x.
+ *   shape->B must be 1.  parents, path, L as for gdn_commit_path; L == 0
+ *             leaves the state unchanged and copies tail_in to tail_out.
+ *   x         bf16 [N, C_qkv] pre-conv inputs;  w  bf16 [C_qkv, 4].
+ *   tail_in   bf16 [4, C_qkv] read;  tail_out  bf16 [4, C_qkv] written.  The
+ *             two must not overlap (GDN_ERR_INVALID_ARG): every CTA reads
+ *             tail_in for the conv while others write the new tail, so the
+ *             caller alternates two tail buffers between rounds.
+ *   alpha, beta, state, flags  as for gdn_commit_path.
+ * Source: "Architecture" (v0.14.2) section 8.3 (commit the state of the
+ * accepted path) and section 8.1 (the per-layer conv tail).
+ */
+int gdn_conv_commit_path(const gdn_shape* shape, int32_t N, const int32_t* parents,
+                         const int32_t* path, int32_t L, const gdn_bf16* x, const gdn_bf16* w,
+                         const gdn_bf16* tail_in, gdn_bf16* tail_out, const float* alpha,
+                         const float* beta, float* state, uint32_t flags, void* stream);
+
+/*
+ * gdn_conv_commit_path_batched -- gdn_conv_commit_path for B sequences in one
+ * launch (after gdn_conv_tree_verify_batched).
+ *   counts, parents, paths, lengths  as for gdn_commit_path_batched.
+ *   x         bf16 [B, N, C_qkv];  w  bf16 [C_qkv, 4].
+ *   tail_in   bf16 [B, 4, C_qkv] read;  tail_out  bf16 [B, 4, C_qkv] written
+ *             for every sequence (a sequence with lengths[b] == 0 gets its
+ *             tail_in copied); the two must not overlap.
+ *   alpha, beta fp32 [B, N, Hv];  state fp32 [B, Hv, dv, dk] in/out.
+ * Each sequence's state and tail equal, bit for bit, gdn_conv_commit_path on
+ * its tree alone.  Source: "Architecture" (v0.14.2) sections 8.3 and 8.5.
+ */
+int gdn_conv_commit_path_batched(const gdn_shape* shape, int32_t N, const int32_t* counts,
+                                 const int32_t* parents, const int32_t* paths,
+                                 const int32_t* lengths, const gdn_bf16* x, const gdn_bf16* w,
+                                 const gdn_bf16* tail_in, gdn_bf16* tail_out, const float* alpha,
+                                 const float* beta, float* state, uint32_t flags, void* stream);
+
+/*
  * gdn_prefill_workspace_bytes -- device workspace gdn_chunk_prefill needs for
  * T tokens in chunks of `chunk` (0 on a bad shape or chunk).  The workspace
  * holds the call's status word (int32 at offset 0, padded to 256 bytes) and,

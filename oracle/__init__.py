@@ -56,6 +56,8 @@ def _load():
             "orc_conv_linear": (None, [I, I, I, I, P, P, P, P]),
             "orc_conv_tree": (None, [I, I, I, P, P, P, P, P]),
             "orc_conv_linear_f32": (None, [I, I, I, I, P, P, P, P]),
+            "orc_conv_linear_r32": (None, [I, I, I, I, P, P, P, P]),
+            "orc_conv_tree_r32": (None, [I, I, I, P, P, P, P, P]),
             "orc_decode_f32": (None, [I, I, I, I, I, I, P, P, P, P, P, D, I]),
             "orc_tree_check": (I, [I, P, P]),
             "orc_root_path": (I, [I, P, I, P]),
@@ -158,6 +160,30 @@ def conv_tree(parents, x, w, tail):
     N, C = x.shape
     y = np.empty((N, C), np.float64)
     _load().orc_conv_tree(N, C, w.shape[1], _ptr(parents), _ptr(x), _ptr(w), _ptr(tail), _ptr(y))
+    return y
+
+
+def conv_linear_r32(x, w, tail):
+    """conv_linear with the outputs as bf16 bits, rounded from binary32 (the
+    precision the CUDA conv rounds in) -> (y bf16 [B,T,C], new tail)."""
+    x = _c(x, np.uint16)
+    w = _c(w, np.uint16)
+    tail = _c(tail, np.uint16).copy()
+    B, T, C = x.shape
+    y = np.empty((B, T, C), np.uint16)
+    _load().orc_conv_linear_r32(B, T, C, w.shape[1], _ptr(x), _ptr(w), _ptr(tail), _ptr(y))
+    return y, tail
+
+
+def conv_tree_r32(parents, x, w, tail):
+    """conv_tree with the outputs as bf16 bits, rounded from binary32 -> y bf16 [N,C]."""
+    parents = _c(parents, np.int32)
+    x = _c(x, np.uint16)
+    w = _c(w, np.uint16)
+    tail = _c(tail, np.uint16)
+    N, C = x.shape
+    y = np.empty((N, C), np.uint16)
+    _load().orc_conv_tree_r32(N, C, w.shape[1], _ptr(parents), _ptr(x), _ptr(w), _ptr(tail), _ptr(y))
     return y
 
 

@@ -77,8 +77,22 @@ static double conv_channel(int W, const uint16_t* wc, const double* u) {
     return orc_silu(acc);
 }
 
-void orc_conv_linear(int B, int T, int C, int W, const uint16_t* x,
-                     const uint16_t* w, uint16_t* tail, double* y) {
+/* The same channel where the output is stored as bf16 and the rounding is
+ * decided in binary32, the precision of the CUDA conv: the sum over the taps in
+ * binary32 in tap order (the first product is exact, each further term one
+ * fused multiply-add), SiLU(z) = z / (1 + e^-z) in binary32 with the host
+ * libm's expf, then round to the nearest bf16, ties to even.  Rounding a conv
+ * output to bf16 is a quantisation, so both sides take it in one precision. */
+static uint16_t conv_channel_r32(int W, const uint16_t* wc, const double* u) {
+    float acc = (float)orc_bf16_to_f64(wc[0]) * (float)u[0];
+    for (int j = 1; j < W; ++j) acc = fmaf((float)orc_bf16_to_f64(wc[j]), (float)u[j], acc);
+    const float z = acc / (1.0f + expf(-acc));
+    return orc_f64_to_bf16((double)z); /* exact widening, then one rounding */
+}
+
+/* y64 != NULL: fp64 outputs; else y16 gets the bf16 outputs decided in binary32 */
+static void conv_linear_impl(int B, int T, int C, int W, const uint16_t* x, const uint16_t* w, uint16_t* tail,
+                             double* y64, uint16_t* y16) {
     /* history per sequence: W tail inputs followed by the T new inputs */
     double* u = (double*)malloc(sizeof(double) * (size_t)W);
     uint16_t* hist = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(W + T));
@@ -89,13 +103,25 @@ void orc_conv_linear(int B, int T, int C, int W, const uint16_t* x,
             for (int t = 0; t < T; ++t) {
                 /* inputs x_{t-W+1} .. x_t sit at hist[t+1 .. t+W] */
                 for (int j = 0; j < W; ++j) u[j] = orc_bf16_to_f64(hist[t + 1 + j]);
-                y[((size_t)b * T + t) * C + c] = conv_channel(W, w + (size_t)c * W, u);
+                const size_t at = ((size_t)b * T + t) * C + c;
+                if (y64) y64[at] = conv_channel(W, w + (size_t)c * W, u);
+                else y16[at] = conv_channel_r32(W, w + (size_t)c * W, u);
             }
             for (int j = 0; j < W; ++j) tail[((size_t)b * W + j) * C + c] = hist[T + j];
         }
     }
     free(hist);
     free(u);
+}
+
+void orc_conv_linear(int B, int T, int C, int W, const uint16_t* x,
+                     const uint16_t* w, uint16_t* tail, double* y) {
+    conv_linear_impl(B, T, C, W, x, w, tail, y, NULL);
+}
+
+void orc_conv_linear_r32(int B, int T, int C, int W, const uint16_t* x,
+                         const uint16_t* w, uint16_t* tail, uint16_t* y) {
+    conv_linear_impl(B, T, C, W, x, w, tail, NULL, y);
 }
 
 /* The same linear run over fp32 activations and taps (widened exactly to fp64;
@@ -123,8 +149,8 @@ void orc_conv_linear_f32(int B, int T, int C, int W, const float* x, const float
     free(u);
 }
 
-void orc_conv_tree(int N, int C, int W, const int32_t* parents, const uint16_t* x,
-                   const uint16_t* w, const uint16_t* tail, double* y) {
+static void conv_tree_impl(int N, int C, int W, const int32_t* parents, const uint16_t* x, const uint16_t* w,
+                           const uint16_t* tail, double* y64, uint16_t* y16) {
     double* u = (double*)malloc(sizeof(double) * (size_t)W);
     for (int n = 0; n < N; ++n) {
         for (int c = 0; c < C; ++c) {
@@ -140,10 +166,21 @@ void orc_conv_tree(int N, int C, int W, const int32_t* parents, const uint16_t* 
                     tail_pos -= 1;
                 }
             }
-            y[(size_t)n * C + c] = conv_channel(W, w + (size_t)c * W, u);
+            if (y64) y64[(size_t)n * C + c] = conv_channel(W, w + (size_t)c * W, u);
+            else y16[(size_t)n * C + c] = conv_channel_r32(W, w + (size_t)c * W, u);
         }
     }
     free(u);
+}
+
+void orc_conv_tree(int N, int C, int W, const int32_t* parents, const uint16_t* x,
+                   const uint16_t* w, const uint16_t* tail, double* y) {
+    conv_tree_impl(N, C, W, parents, x, w, tail, y, NULL);
+}
+
+void orc_conv_tree_r32(int N, int C, int W, const int32_t* parents, const uint16_t* x,
+                       const uint16_t* w, const uint16_t* tail, uint16_t* y) {
+    conv_tree_impl(N, C, W, parents, x, w, tail, NULL, y);
 }
 
 /* ------------------------------------------------------------------------ */

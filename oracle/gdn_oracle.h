@@ -73,6 +73,16 @@ void orc_conv_linear_f32(int B, int T, int C, int W, const float* x, const float
 void orc_conv_tree(int N, int C, int W, const int32_t* parents, const uint16_t* x,
                    const uint16_t* w, const uint16_t* tail, double* y);
 
+/* The linear and tree runs with the output stored as bf16 and its rounding
+ * decided in binary32 (the tap sum in tap order, SiLU, then one rounding to
+ * bf16, ties to even), the precision the CUDA conv decides it in: where a
+ * floating-point value is quantised, both sides quantise the same-precision
+ * value.  Within one bf16 ulp of rounding the fp64 output. */
+void orc_conv_linear_r32(int B, int T, int C, int W, const uint16_t* x,
+                         const uint16_t* w, uint16_t* tail, uint16_t* y);
+void orc_conv_tree_r32(int N, int C, int W, const int32_t* parents, const uint16_t* x,
+                       const uint16_t* w, const uint16_t* tail, uint16_t* y);
+
 /* ---- tree bookkeeping ---------------------------------------------------- */
 /* 0 if parents[] describes one tree rooted at node 0 (parents[0] == -1 and
  * 0 <= parents[i] < i for i > 0); negative otherwise.  depth[n] (optional)

@@ -362,3 +362,73 @@ def test_commit_batched_validation(lib):
     bad[1, 1] = 2
     assert call(ok, [4, 3], par=bad) == -3
     assert "tree 1" in gdn.last_error()
+
+
+def test_conv_fused_round_validation(lib):
+    """The verify and commit with the conv fused in refuse what the unfused
+    calls refuse, plus missing conv inputs and overlapping tails.  Every call
+    fails validation (the last argument checked is a misaligned state), so
+    nothing is launched."""
+    P = ctypes.c_void_p
+    parents = np.array([-1, 0, 0, 1, 3], np.int32)
+    far = FAKE + (1 << 20)  # a second buffer, clear of the first tail
+
+    def verify(x=FAKE, w=FAKE, tail=FAKE, sh=None, par=parents, flags=1, state=FAKE + 4):
+        return lib.gdn_conv_tree_verify(ctypes.byref(sh or _sh()), len(par), par.ctypes.data_as(P), P(x), P(w),
+                                        P(tail), P(FAKE), P(FAKE), P(state), P(FAKE), 1.0, flags, None)
+
+    assert verify(x=None) == -1
+    assert verify(w=None) == -1
+    assert verify(tail=None) == -1
+    assert verify(x=FAKE + 2) == -6
+    assert verify(par=np.array([0, 0], np.int32)) == -3
+    assert verify(sh=_sh(B=2)) == -2
+    assert verify(flags=0x40) == -1
+    assert verify() == -6 and "state" in gdn.last_error()
+
+    def commit(path=(0, 1, 3), w=FAKE, tin=FAKE, tout=far, sh=None, flags=1, state=FAKE + 4):
+        pa = np.ascontiguousarray(path, np.int32)
+        return lib.gdn_conv_commit_path(ctypes.byref(sh or _sh()), len(parents), parents.ctypes.data_as(P),
+                                        pa.ctypes.data_as(P) if pa.size else None, len(pa), P(FAKE), P(w), P(tin),
+                                        P(tout), P(FAKE), P(FAKE), P(state), flags, None)
+
+    assert commit(w=None) == -1
+    assert commit(tin=None) == -1
+    assert commit(tout=None) == -1
+    assert commit(tout=FAKE + 16) == -1 and "overlap" in gdn.last_error()
+    assert commit(tout=FAKE + 8) == -6
+    assert commit(path=(1, 3)) == -4
+    assert commit(flags=1 | gdn.GDN_OUT_BF16) == -1
+    assert commit(sh=_sh(B=2)) == -2
+    assert commit() == -6 and "state" in gdn.last_error()
+    assert commit(path=()) == -6  # nothing accepted still validates everything (the tail is still copied)
+
+    N = 5
+    par2 = np.array([[-1, 0, 0, 1, 3], [-1, 0, 1, -7, -7]], np.int32)
+    counts = np.array([5, 3], np.int32)
+
+    def vbatch(x=FAKE, sh=None, par=par2, state=FAKE + 4):
+        return lib.gdn_conv_tree_verify_batched(ctypes.byref(sh or _sh(B=2)), N, counts.ctypes.data_as(P),
+                                                par.ctypes.data_as(P), P(x), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                                                P(state), P(FAKE), 1.0, 1, None)
+
+    assert vbatch(x=None) == -1
+    assert vbatch(sh=_sh(B=33)) == -2
+    bad = par2.copy()
+    bad[1, 2] = 2
+    assert vbatch(par=bad, state=FAKE) == -3 and "tree 1" in gdn.last_error()  # pointers pass, the tree does not
+    assert vbatch() == -6
+
+    def cbatch(lengths=(3, 2), tout=far, w=FAKE, state=FAKE + 4):
+        paths = np.array([[0, 1, 3, 0, 0], [0, 1, 2, 0, 0]], np.int32)
+        ln = np.ascontiguousarray(lengths, np.int32)
+        return lib.gdn_conv_commit_path_batched(ctypes.byref(_sh(B=2)), N, counts.ctypes.data_as(P),
+                                                par2.ctypes.data_as(P), paths.ctypes.data_as(P),
+                                                ln.ctypes.data_as(P), P(FAKE), P(w), P(FAKE), P(tout), P(FAKE),
+                                                P(FAKE), P(state), 1, None)
+
+    assert cbatch(w=None) == -1
+    assert cbatch(tout=FAKE + 2 * 4 * 10240 * 2 - 16) == -1  # overlaps the last sequence's tail_in
+    assert cbatch(lengths=(3, 4)) == -4
+    assert cbatch() == -6
+    assert cbatch(lengths=(0, 0)) == -6  # no sequence accepted anything: still validated

@@ -213,7 +213,7 @@ def test_speculative_round_end_to_end():
                     x_tree=x_tree[0], tail=tail[0])
     torch.cuda.synchronize()
 
-    y_ref = oracle.f64_to_bf16(oracle.conv_tree(parents, c["x"][0], c["w"], c["tail"][0]))
+    y_ref = oracle.conv_tree_r32(parents, c["x"][0], c["w"], c["tail"][0])  # bf16 rounding decided in binary32
     out_ref = oracle.tree_verify(parents, y_ref, d["alpha"][0], d["beta"][0], d["state"][0], shape.Hk,
                                  shape.Hv, shape.dk, shape.dv)
     st_ref, tail_ref = oracle.commit(parents, path, y_ref, d["alpha"][0], d["beta"][0], d["state"][0],
@@ -317,3 +317,175 @@ def test_commit_path_batched_equals_single_commits_and_oracle(shape):
                                          x_tree=c["x"][b, :n], tail=c["tail"][b])
         assert_state_close(host(st[b]), st_ref)
         assert np.array_equal(host(tail[b]), tail_ref)
+
+
+# ---------------------------------------------------------------------------
+# the round with the conv fused into verify and commit (pre-conv inputs)
+# ---------------------------------------------------------------------------
+_FUSED_TREES = {
+    "random32": gen.random_tree(70, 32, 8),
+    "chain64": np.arange(-1, 63, dtype=np.int32),   # no branch states: the conv outputs alone size the slot region
+    "binary63": _binary_tree(63),                    # several branch states
+    "single": np.array([-1], np.int32),
+    "random13": np.array([-1, 0, 0, 1, 1, 2, 3, 3, 4, 6, 6, 9, 10], np.int32),
+}
+
+
+def _conv_case(shape, N, seed, B=1, tag="fused"):
+    c = gen.conv_inputs(seed, B, N, shape.C, tag=tag)
+    d = gen.decode_inputs(seed + 1, shape.with_batch(B), N, tag=tag)
+    return c, d
+
+
+@pytest.mark.parametrize("shape", [gen.TINY, gen.QWEN_27B, gen.Shape(1, 2, 4, 64, 64)])
+@pytest.mark.parametrize("tree", sorted(_FUSED_TREES))
+def test_conv_tree_verify_equals_conv_then_verify(shape, tree):
+    """gdn_conv_tree_verify == gdn_conv_step (tree mode) + gdn_tree_verify, bit
+    for bit; the committed state and the tail are left untouched."""
+    parents = _FUSED_TREES[tree]
+    N = len(parents)
+    c, d = _conv_case(shape, N, 72)
+    x, w, tail = bf16(c["x"][0]), bf16(c["w"]), bf16(c["tail"][0])
+    al, be, st = f32(d["alpha"][0]), f32(d["beta"][0]), f32(d["state"][0])
+    y = gdn.conv_step(x[None], w, tail[None].clone(), parents=parents)[0]
+    ref = gdn.tree_verify(parents, y, al, be, st, shape.Hk, shape.Hv, shape.dk, shape.dv)
+    out = gdn.conv_tree_verify(parents, x, w, tail, al, be, st, shape.Hk, shape.Hv, shape.dk, shape.dv)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    assert np.array_equal(host(st), d["state"][0]) and np.array_equal(host(tail), c["tail"][0])
+
+
+@pytest.mark.parametrize("shape", [gen.TINY, gen.QWEN_27B])
+def test_conv_commit_equals_conv_then_commit_every_prefix(shape):
+    """gdn_conv_commit_path == gdn_conv_step (tree mode) + gdn_commit_path with
+    x_tree, bit for bit, for every prefix of a root-to-leaf path (L = 0
+    included: the state stays and tail_in is copied to tail_out)."""
+    parents = gen.random_tree(74, 32, 8)
+    path = gdn.tree_root_path(parents, gen.random_leaf(74, parents))
+    N = len(parents)
+    c, d = _conv_case(shape, N, 75)
+    x, w = bf16(c["x"][0]), bf16(c["w"])
+    al, be = f32(d["alpha"][0]), f32(d["beta"][0])
+    y = gdn.conv_step(x[None], w, bf16(c["tail"]), parents=parents)[0]
+    for L in range(len(path) + 1):
+        st1, tail1 = f32(d["state"][0]), bf16(c["tail"][0])
+        gdn.commit_path(parents, path[:L], y, al, be, st1, shape.Hk, shape.Hv, shape.dk, shape.dv, x_tree=x,
+                        tail=tail1)
+        st2, tail_in = f32(d["state"][0]), bf16(c["tail"][0])
+        tail_out = torch.full_like(tail_in, 0x7FC0)  # junk: every entry must be written
+        gdn.conv_commit_path(parents, path[:L], x, w, tail_in, tail_out, al, be, st2, shape.Hk, shape.Hv, shape.dk,
+                             shape.dv)
+        torch.cuda.synchronize()
+        assert torch.equal(st1, st2), f"L={L}: state"
+        assert torch.equal(tail1, tail_out), f"L={L}: tail"
+        assert np.array_equal(host(tail_in), c["tail"][0]), "tail_in is read only"
+
+
+def test_conv_commit_long_path():
+    """A 64-node chain accepted whole: the longest path (64 tokens of conv
+    outputs in shared memory)."""
+    shape = gen.QWEN_27B
+    parents = np.arange(-1, 63, dtype=np.int32)
+    path = np.arange(64, dtype=np.int32)
+    c, d = _conv_case(shape, 64, 76)
+    x, w = bf16(c["x"][0]), bf16(c["w"])
+    al, be = f32(d["alpha"][0]), f32(d["beta"][0])
+    y = gdn.conv_step(x[None], w, bf16(c["tail"]), parents=parents)[0]
+    st1, tail1 = f32(d["state"][0]), bf16(c["tail"][0])
+    gdn.commit_path(parents, path, y, al, be, st1, shape.Hk, shape.Hv, shape.dk, shape.dv, x_tree=x, tail=tail1)
+    st2, tail_out = f32(d["state"][0]), torch.empty_like(tail1)
+    gdn.conv_commit_path(parents, path, x, w, bf16(c["tail"][0]), tail_out, al, be, st2, shape.Hk, shape.Hv,
+                         shape.dk, shape.dv)
+    torch.cuda.synchronize()
+    assert torch.equal(st1, st2) and torch.equal(tail1, tail_out)
+
+
+def test_fused_rounds_vs_oracle_and_unfused():
+    """Two speculative rounds at the 27B shape with the conv fused in (tails
+    alternating between two buffers): each round's outputs, the state and the
+    tail equal the three-launch round bit for bit, and the oracle's conv +
+    verify + commit within the bars.  The oracle's conv rounds its outputs to
+    bf16 from binary32, as the kernels do: from fp64, the rare outputs within
+    an ulp or two of a bf16 midpoint land one bf16 ulp apart, and a single
+    such v input moves a node's output by about 1e-3."""
+    shape = gen.QWEN_27B
+    N = 32
+    c, d = _conv_case(shape, N, 78, B=2, tag="rounds")
+    w = bf16(c["w"])
+    st_f, st_u = f32(d["state"][0]), f32(d["state"][0])
+    tails = [bf16(c["tail"][0]), torch.empty_like(bf16(c["tail"][0]))]
+    tail_u = bf16(c["tail"][0])
+    st_ref, tail_ref = d["state"][0], c["tail"][0]
+    for r in range(2):
+        parents = gen.random_tree(80 + r, N, 8)
+        path = gdn.tree_root_path(parents, gen.random_leaf(80 + r, parents))
+        x = bf16(c["x"][r])
+        al, be = f32(d["alpha"][r]), f32(d["beta"][r])
+        tin, tout = tails[r % 2], tails[(r + 1) % 2]
+        out_f = gdn.conv_tree_verify(parents, x, w, tin, al, be, st_f, shape.Hk, shape.Hv, shape.dk, shape.dv)
+        gdn.conv_commit_path(parents, path, x, w, tin, tout, al, be, st_f, shape.Hk, shape.Hv, shape.dk, shape.dv)
+        y = gdn.conv_step(x[None], w, tail_u[None].clone(), parents=parents)[0]
+        out_u = gdn.tree_verify(parents, y, al, be, st_u, shape.Hk, shape.Hv, shape.dk, shape.dv)
+        gdn.commit_path(parents, path, y, al, be, st_u, shape.Hk, shape.Hv, shape.dk, shape.dv, x_tree=x,
+                        tail=tail_u)
+        torch.cuda.synchronize()
+        assert torch.equal(out_f, out_u), f"round {r}: outputs"
+        assert torch.equal(st_f, st_u), f"round {r}: state"
+        assert torch.equal(tout, tail_u), f"round {r}: tail"
+        # the conv outputs' bf16 rounding decided in binary32 on both sides
+        y_ref = oracle.conv_tree_r32(parents, c["x"][r], c["w"], tail_ref)
+        out_ref = oracle.tree_verify(parents, y_ref, d["alpha"][r], d["beta"][r], st_ref, shape.Hk, shape.Hv,
+                                     shape.dk, shape.dv)
+        st_ref, tail_ref = oracle.commit(parents, path, y_ref, d["alpha"][r], d["beta"][r], st_ref, shape.Hk,
+                                         shape.Hv, shape.dk, shape.dv, x_tree=c["x"][r], tail=tail_ref)
+        assert_out_close(host(out_f), out_ref)
+        assert_state_close(host(st_f), st_ref)
+        assert np.array_equal(host(tout), tail_ref)
+
+
+@pytest.mark.parametrize("B", [5, 8, 14])  # one, two and four rows per thread in the commit at the 27B shape
+def test_conv_round_batched_equals_single(B):
+    """The joint verify and the batched commit with the conv fused in equal
+    the single-sequence fused calls bit for bit (sequence 1 accepts nothing:
+    its state stays and its tail is copied)."""
+    shape = gen.QWEN_27B
+    N = 32
+    base = [gen.random_tree(90, 32, 8), np.array([-1], np.int32), gen.random_tree(91, 13, 5),
+            gen.random_tree(92, 20, 8), np.arange(-1, 6, dtype=np.int32)]
+    trees = [base[b % len(base)] if b < len(base) else gen.random_tree(93 + b, 32, 8) for b in range(B)]
+    counts = np.array([len(t) for t in trees], np.int32)
+    parents = _pad_parents(trees, N)
+    paths = np.full((B, N), -9, np.int32)
+    lengths = np.zeros(B, np.int32)
+    for b, t in enumerate(trees):
+        if b == 1:
+            continue
+        p = gdn.tree_root_path(t, gen.random_leaf(100 + b, t))
+        paths[b, :len(p)] = p
+        lengths[b] = len(p)
+    c, d = _conv_case(shape, N, 95, B=B, tag="roundb")
+    x, w, tail = bf16(c["x"]), bf16(c["w"]), bf16(c["tail"])
+    al, be, st = f32(d["alpha"]), f32(d["beta"]), f32(d["state"])
+    out = torch.full((B, N, shape.Hv, shape.dv), float("nan"), device="cuda")
+    gdn.conv_tree_verify_batched(counts, parents, x, w, tail, al, be, st, shape.Hk, shape.Hv, shape.dk, shape.dv,
+                                 out=out)
+    tail_out = torch.full_like(tail, 0x7FC0)
+    gdn.conv_commit_path_batched(counts, parents, paths, lengths, x, w, tail, tail_out, al, be, st, shape.Hk,
+                                 shape.Hv, shape.dk, shape.dv)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(tail), c["tail"]), "tail_in is read only"
+    for b, t in enumerate(trees):
+        n, L = len(t), int(lengths[b])
+        xb = x[b, :n].contiguous()
+        alb, beb = al[b, :n].contiguous(), be[b, :n].contiguous()
+        st1 = f32(d["state"][b])
+        o1 = gdn.conv_tree_verify(t, xb, w, tail[b], alb, beb, st1, shape.Hk, shape.Hv, shape.dk, shape.dv)
+        t1 = torch.empty_like(tail[b])
+        gdn.conv_commit_path(t, paths[b, :L], xb, w, tail[b], t1, alb, beb, st1, shape.Hk, shape.Hv, shape.dk,
+                             shape.dv)
+        torch.cuda.synchronize()
+        assert torch.equal(out[b, :n], o1), f"sequence {b}: outputs"
+        assert torch.isnan(out[b, n:]).all(), f"sequence {b}: rows past the tree"
+        assert torch.equal(st[b], st1), f"sequence {b}: state"
+        assert torch.equal(tail_out[b], t1), f"sequence {b}: tail"
+    assert np.array_equal(host(st[1]), d["state"][1]) and np.array_equal(host(tail_out[1]), c["tail"][1])

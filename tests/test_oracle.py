@@ -151,6 +151,53 @@ def test_conv_tree_chain_and_replay():
         assert np.array_equal(y_tree[n], y_path[0, -1])
 
 
+def test_conv_r32_closed_forms():
+    """The binary32-decided conv on inputs whose outputs are known in closed
+    form: SiLU(1) = 1/(1+e^-1) = 0.7310586 -> bf16 0.73046875 (0x3F3B),
+    SiLU(-1) = -0.2689414 -> -0.26953125 (0xBE8A), SiLU(1+2) = 2.857722 ->
+    2.859375 (0x4037), SiLU(0) = 0."""
+    one, two = 0x3F80, 0x4000
+    w = np.array([[0, 0, 0, one], [0, 0, 0, one], [0, 0, one, one], [one, one, one, one]], np.uint16)
+    tail = np.zeros((1, 4, 4), np.uint16)
+    tail[0, 3, 2] = one  # the newest tail input of channel 2
+    x = np.array([[[one, 0xBF80, two, 0]]], np.uint16)  # 1, -1, 2, 0
+    y, new_tail = oracle.conv_linear_r32(x, w, tail)
+    assert y[0, 0].tolist() == [0x3F3B, 0xBE8A, 0x4037, 0]
+    assert new_tail[0, 3].tolist() == x[0, 0].tolist()
+
+
+def test_conv_r32_within_one_ulp_of_fp64():
+    """Deciding the bf16 rounding in binary32 moves an output by at most one
+    bf16 ulp from rounding the fp64 conv, and almost never (the binary32 value
+    is within a few of its ulps of the exact one, and a bf16 midpoint lies
+    between the two only rarely); the tail is the same."""
+    d = gen.conv_inputs(12, 2, 48, 1024, tag="r32")
+    y64, t64 = oracle.conv_linear(d["x"], d["w"], d["tail"])
+    y16, t16 = oracle.conv_linear_r32(d["x"], d["w"], d["tail"])
+    ref = oracle.f64_to_bf16(y64)
+    key = lambda b: np.where(b.astype(np.int32) & 0x8000, -(b.astype(np.int32) & 0x7FFF), b.astype(np.int32))
+    ulp = np.abs(key(ref) - key(y16))
+    assert ulp.max() <= 1
+    assert (ulp == 0).mean() > 0.999
+    assert np.array_equal(t64, t16)
+
+
+def test_conv_tree_r32_chain_and_root_paths():
+    """The binary32-decided tree conv: a chain is the linear run, and every
+    node of a random tree is the linear run over its root path."""
+    C = 24
+    d = gen.conv_inputs(5, 1, 12, C, tag="r32t")
+    chain = np.arange(-1, 11, dtype=np.int32)
+    y_lin, _ = oracle.conv_linear_r32(d["x"], d["w"], d["tail"])
+    assert np.array_equal(oracle.conv_tree_r32(chain, d["x"][0], d["w"], d["tail"][0]), y_lin[0])
+    parents = gen.random_tree(12, 12, 5)
+    y_tree = oracle.conv_tree_r32(parents, d["x"][0], d["w"], d["tail"][0])
+    for n in range(12):
+        p = oracle.root_path(parents, n)
+        y_path, _ = oracle.conv_linear_r32(d["x"][:, p], d["w"], d["tail"])
+        assert np.array_equal(y_tree[n], y_path[0, -1])
+
+
 # ---------------------------------------------------------------------------
 # tree bookkeeping: brute force over every tree of up to 7 nodes
 # ---------------------------------------------------------------------------
