@@ -1106,6 +1106,31 @@ class Prefill(Workload):
         if st != 0:
             raise RuntimeError("prefill reported a tensor-core wait timeout")
 
+    def extra_measures(self) -> dict:
+        """The prompt's conv ahead of the prefill (gdn_conv_step, linear mode,
+        8,192 tokens x 10,240 channels): what producing the prefill's qkv input
+        from the pre-conv projections costs.  Its 168 MB in and 168 MB out are
+        larger than L2; calls enqueued back to back, median of 10."""
+        torch, P = self.torch, ctypes.c_void_p
+        T, n = self.T, 13
+        x = self.randn((1, T, C_QKV), 1.0, torch.bfloat16)
+        w = self.randn((C_QKV, 4), 0.5, torch.bfloat16)
+        tail = self.randn((1, 4, C_QKV), 1.0, torch.bfloat16)
+        y = torch.empty_like(x)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for i in range(n):
+            ev[i][0].record(self.stream)
+            _call(self.lib.gdn_conv_step, (1, T, C_QKV, None, P(x.data_ptr()), P(w.data_ptr()), P(tail.data_ptr()),
+                                           P(y.data_ptr()), 0, self.sp), self.gdn)
+            ev[i][1].record(self.stream)
+        torch.cuda.synchronize()
+        us = statistics.median(e[0].elapsed_time(e[1]) * 1e3 for e in ev[3:])
+        nbytes = 2 * T * C_QKV * 2  # x read + y written (bf16); taps and tail are negligible
+        return {"conv": {"us": us, "gbs": nbytes / (us * 1e-6) / 1e9, "bytes": nbytes, "tokens": T,
+                         "channels": C_QKV,
+                         "how": "gdn_conv_step over the prompt (linear mode), bf16 in and out, median of 10, "
+                                "calls enqueued back to back"}}
+
     E2E_PIECE = 2048  # tokens per piece of the overlapped end-to-end step (a multiple of the chunk)
 
     def e2e_setup(self):
@@ -1414,7 +1439,7 @@ def measure(args, name: str, steps: int, warmup: int, device, peaks: dict, peaks
                 "d2h_bytes_per_step": wl.e2e_d2h, "ms_per_step": e2e_total * 1e3 / steps},
         "gpu_launches": wl.launches_per_step * steps,
     }
-    if hasattr(wl, "extra_measures"):
+    if hasattr(wl, "extra_measures") and not args.no_extras:
         line.update(wl.extra_measures())
     del wl, rec
     torch.cuda.synchronize()
@@ -1497,7 +1522,8 @@ def main(argv=None):
                     help="one workload alone (default: the batched decode, with decode1, tree and prefill "
                          "measured beside it under \"workloads\")")
     ap.add_argument("--no-extras", action="store_true",
-                    help="with no --workload, measure the batched decode only")
+                    help="measure the named workload (default: the batched decode) only, without the other "
+                         "configs or the extra measurements beside it (for profiling runs)")
     ap.add_argument("--layers", type=int, default=48,
                     help="GDN layers in the batched workload (48 = the 27B model; fewer only for "
                          "profiling small cases)")
