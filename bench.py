@@ -786,7 +786,7 @@ class Tree(Workload):
         self.tree_marks = 2
         self.units_per_step = (N + len(self.path)) * HV
         self.dominant = "gdn_tree_kernel"
-        self.dominant_sources = DECODE_SOURCES
+        self.dominant_sources = FUSED_SOURCES  # the fused verify runs the conv arithmetic too
         self.bound = "alu"
         self.dominant_work = N * HV * step_flops_per_head_token()
         self.step_bytes = (2 * conv_bytes_per_launch(1, N) + HV * DV * DK * 4 +

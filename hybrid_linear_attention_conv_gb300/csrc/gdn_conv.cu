@@ -15,7 +15,42 @@
 namespace gdn {
 
 constexpr int kConvThreads = 128;
-constexpr int kConvTok = 16;  // tokens per thread in a linear run
+constexpr int kConvTok = 16;  // tokens per thread in a single-pass linear run
+
+// Tokens per thread when a long linear run is split over blocks: every input
+// of a thread's tokens is loaded before any is used, held as raw 16-byte
+// words (16 tokens of bf16, 8 of fp32: 19 or 11 loads of one or two words).
+template <typename E>
+__host__ __device__ constexpr int conv_split_tok() {
+    return sizeof(E) == 2 ? 16 : 8;
+}
+
+// 8 channels from their raw 16-byte words: one word of bf16, two of fp32.
+__device__ __forceinline__ Vec8 vec8_of(const uint4 (&r)[1]) {
+    Vec8 v;
+    v.v[0] = bf16_lo(r[0].x);
+    v.v[1] = bf16_hi(r[0].x);
+    v.v[2] = bf16_lo(r[0].y);
+    v.v[3] = bf16_hi(r[0].y);
+    v.v[4] = bf16_lo(r[0].z);
+    v.v[5] = bf16_hi(r[0].z);
+    v.v[6] = bf16_lo(r[0].w);
+    v.v[7] = bf16_hi(r[0].w);
+    return v;
+}
+
+__device__ __forceinline__ Vec8 vec8_of(const uint4 (&r)[2]) {
+    Vec8 v;
+    v.v[0] = __uint_as_float(r[0].x);
+    v.v[1] = __uint_as_float(r[0].y);
+    v.v[2] = __uint_as_float(r[0].z);
+    v.v[3] = __uint_as_float(r[0].w);
+    v.v[4] = __uint_as_float(r[1].x);
+    v.v[5] = __uint_as_float(r[1].y);
+    v.v[6] = __uint_as_float(r[1].z);
+    v.v[7] = __uint_as_float(r[1].w);
+    return v;
+}
 
 // E is the element type of x, w, tail and y: uint16_t (bf16 bits; y rounded
 // to bf16) or float (the fp32-activation conv; y kept in fp32).
@@ -55,19 +90,33 @@ __global__ void __launch_bounds__(kConvThreads) gdn_conv_kernel(const __grid_con
         put8(tb + 2 * C, h2);
         put8(tb + 3 * C, h3);
     } else if (!p.tree) {
-        // inputs before token t0: t < 0 reads tail slot 4 + t
-        const int t0 = blockIdx.y * kConvTok;
-        const int t1 = min(p.T, t0 + kConvTok);
-        auto in = [&](int t) -> Vec8 {
-            return t >= 0 ? load8(xb + (size_t)t * C) : load8(tb + (size_t)(GDN_CONV_W + t) * C);
-        };
-        Vec8 u0 = in(t0 - 3), u1 = in(t0 - 2), u2 = in(t0 - 1);
-        for (int t = t0; t < t1; ++t) {
-            const Vec8 u3 = load8(xb + (size_t)t * C);
-            store_y(yb + (size_t)t * C, w, u0, u1, u2, u3);
-            u0 = u1;
-            u1 = u2;
-            u2 = u3;
+        // A block of TOK tokens: the three inputs before it (t < 0 reads tail
+        // slot 4 + t) and its own, all requested before the first is used, so
+        // that a thread waits for one DRAM round trip, not one per token.
+        constexpr int TOK = conv_split_tok<E>();
+        constexpr int W16 = (int)sizeof(E) / 2;  // 16-byte words per 8 channels
+        const int t0 = blockIdx.y * TOK;
+        const int n = min(p.T - t0, TOK);
+        uint4 raw[3 + TOK][W16];
+#pragma unroll
+        for (int j = 0; j < 3 + TOK; ++j) {
+            const int t = t0 - 3 + j;
+            if (j < 3 + n) {
+                const E* src = t >= 0 ? xb + (size_t)t * C : tb + (size_t)(GDN_CONV_W + t) * C;
+#pragma unroll
+                for (int q = 0; q < W16; ++q) raw[j][q] = reinterpret_cast<const uint4*>(src)[q];
+            }
+        }
+        Vec8 u0 = vec8_of(raw[0]), u1 = vec8_of(raw[1]), u2 = vec8_of(raw[2]);
+#pragma unroll
+        for (int i = 0; i < TOK; ++i) {
+            if (i < n) {
+                const Vec8 u3 = vec8_of(raw[3 + i]);
+                store_y(yb + (size_t)(t0 + i) * C, w, u0, u1, u2, u3);
+                u0 = u1;
+                u1 = u2;
+                u2 = u3;
+            }
         }
         if (blockIdx.y == 0) {
             // New tail = the last four of (tail ++ x).  Only this thread touches
@@ -102,7 +151,10 @@ __global__ void __launch_bounds__(kConvThreads) gdn_conv_kernel(const __grid_con
 
 cudaError_t launch_conv(const ConvParams& p, cudaStream_t s) {
     const int cvecs = p.C / 8;
-    const int gy = p.tree ? p.T : (p.T + kConvTok - 1) / kConvTok;
+    // a linear run of up to kConvTok tokens is one pass per thread; a longer
+    // one is split into blocks of conv_split_tok tokens along grid y
+    const int tok = p.f32 ? conv_split_tok<float>() : conv_split_tok<uint16_t>();
+    const int gy = p.tree ? p.T : p.T <= kConvTok ? 1 : (p.T + tok - 1) / tok;
     dim3 grid((cvecs + kConvThreads - 1) / kConvThreads, gy, p.B);
     if (p.f32) gdn_conv_kernel<float><<<grid, kConvThreads, 0, s>>>(p);
     else gdn_conv_kernel<uint16_t><<<grid, kConvThreads, 0, s>>>(p);

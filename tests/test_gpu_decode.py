@@ -41,6 +41,52 @@ def test_conv_linear_vs_oracle(B, T, C):
     assert ulp32.max() <= 1 and (ulp32 == 0).mean() > 0.9999, (int((ulp32 != 0).sum()), ulp32.size)
 
 
+def test_conv_prompt_8192_tokens_sampled_channels():
+    """The prompt-length conv (8,192 tokens x 10,240 channels, the prefill
+    config's width): blocks of 16 tokens per thread with every input loaded up
+    front.  The conv is per channel, so the oracle (rounding decided in
+    binary32, as the kernel decides it) runs on three slices of channels; the
+    new tail is checked whole, and the run equals two halves of 4,096 tokens
+    with the tail carried, bit for bit."""
+    T, C = 8192, 10240
+    d = gen.conv_inputs(812, 1, T, C, tag="prompt")
+    x, w = bf16(d["x"]), bf16(d["w"])
+    tail = bf16(d["tail"])
+    y = gdn.conv_step(x, w, tail)
+    tail2 = bf16(d["tail"])
+    y_a = gdn.conv_step(x[:, :T // 2].contiguous(), w, tail2)
+    y_b = gdn.conv_step(x[:, T // 2:].contiguous(), w, tail2)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat([y_a, y_b], dim=1), y) and torch.equal(tail2, tail)
+    assert np.array_equal(host(tail), d["x"][:, T - 4:])
+    yh = host(y)
+    for lo in (0, 5120 - 128, C - 256):
+        sl = slice(lo, lo + 256)
+        y32, _ = oracle.conv_linear_r32(np.ascontiguousarray(d["x"][:, :, sl]), np.ascontiguousarray(d["w"][sl]),
+                                        np.ascontiguousarray(d["tail"][:, :, sl]))
+        ulp = bf16_ulp_diff(yh[:, :, sl], y32)
+        assert ulp.max() <= 1 and (ulp == 0).mean() > 0.9999, (lo, int((ulp != 0).sum()))
+
+
+@pytest.mark.parametrize("T", [17, 41])
+def test_conv_f32_split_blocks(T):
+    """fp32 activations past one pass (blocks of 8 tokens per thread, a
+    ragged last block, a non-zero tail): the oracle's fp32-input conv, the
+    exact new tail, and token-by-token calls bit for bit."""
+    C = 256
+    c = gen.conv_inputs_f32(70 + T, 1, T, C, zero_tail=False)
+    w = f32(c["w"])
+    tail = f32(c["tail"])
+    y = gdn.conv_step(f32(c["x"]), w, tail)
+    tail1 = f32(c["tail"])
+    ys = [gdn.conv_step(f32(c["x"][:, t:t + 1]), w, tail1) for t in range(T)]
+    torch.cuda.synchronize()
+    y_ref, tail_ref = oracle.conv_linear_f32(c["x"], c["w"], c["tail"])
+    assert np.array_equal(host(tail), tail_ref) and torch.equal(tail1, tail)
+    assert np.abs(host(y) - y_ref).max() <= 1e-5
+    assert torch.equal(torch.cat(ys, dim=1), y)
+
+
 def test_conv_zero_tokens_is_noop():
     d = gen.conv_inputs(1, 2, 0, 128)
     tail = bf16(gen.conv_inputs(1, 2, 1, 128)["tail"])
