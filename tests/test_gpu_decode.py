@@ -43,7 +43,7 @@ def test_conv_linear_vs_oracle(B, T, C):
 
 def test_conv_prompt_8192_tokens_sampled_channels():
     """The prompt-length conv (8,192 tokens x 10,240 channels, the prefill
-    config's width): blocks of 16 tokens per thread with every input loaded up
+    config's width): blocks of 8 tokens per thread with every input loaded up
     front.  The conv is per channel, so the oracle (rounding decided in
     binary32, as the kernel decides it) runs on three slices of channels; the
     new tail is checked whole, and the run equals two halves of 4,096 tokens
