@@ -60,8 +60,9 @@ __device__ __forceinline__ float conv_silu(const float (&w)[4], float u0, float 
     return __fdiv_rn(acc, __fadd_rn(1.0f, expf(-acc)));
 }
 
-__device__ __forceinline__ void store_y(uint16_t* dst, const float (&w)[8][4], const Vec8& u0,
-                                        const Vec8& u1, const Vec8& u2, const Vec8& u3) {
+// 8 conv outputs rounded to bf16, packed as they are stored.
+__device__ __forceinline__ uint4 conv8_bf16(const float (&w)[8][4], const Vec8& u0, const Vec8& u1, const Vec8& u2,
+                                            const Vec8& u3) {
     float y[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) y[c] = conv_silu(w[c], u0.v[c], u1.v[c], u2.v[c], u3.v[c]);
@@ -70,7 +71,12 @@ __device__ __forceinline__ void store_y(uint16_t* dst, const float (&w)[8][4], c
     out.y = pack2(y[2], y[3]);
     out.z = pack2(y[4], y[5]);
     out.w = pack2(y[6], y[7]);
-    *reinterpret_cast<uint4*>(dst) = out;
+    return out;
+}
+
+__device__ __forceinline__ void store_y(uint16_t* dst, const float (&w)[8][4], const Vec8& u0,
+                                        const Vec8& u1, const Vec8& u2, const Vec8& u3) {
+    *reinterpret_cast<uint4*>(dst) = conv8_bf16(w, u0, u1, u2, u3);
 }
 
 // The same 8 outputs kept in fp32 (the fp32-activation conv stores no bf16).

@@ -48,6 +48,29 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(gsrc) : "memory");
 }
 
+// Thread-block cluster helpers (the fused verify's shared q/k conv).
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster: shared-memory writes before it,
+// local or remote, are visible to all of them after it.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Store 16 bytes at the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ void st_cluster16(const void* local, uint32_t rank, uint4 v) {
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(local);
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
 // The conv-tail update of a commit, done by the commit's own launch: the
 // tail becomes the last four inputs of (tail ++ x_tree[path[0]] ++ ...), 8
 // channels (one 16-byte vector) per thread of the grid, copied as they are.
@@ -413,11 +436,19 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
             cp_async16(ws + (size_t)c * 32 + 8 * q, p.w + (size_t)chan(c) * GDN_CONV_W + 8 * q);
         }
         asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
-        __syncthreads();
+        // With a cluster (the CTAs of one key head: its value heads' row
+        // blocks), the q/k outputs are computed once per cluster: task j goes
+        // to CTA j mod csize, which stores the result into every CTA's y_qk.
+        // The first cluster barrier also makes sure every CTA of the cluster
+        // is running before any remote store.
+        const int csize = p.cluster;
+        const uint32_t rank = csize > 1 ? cluster_rank() : 0u;
+        if (csize > 1) cluster_sync_all();
+        else __syncthreads();
         // staged row of input a: a node (a >= 0) or tail slot -1 - a (1 .. 3)
         auto row_of = [&](int a) { return a >= 0 ? a + 3 : -2 - a; };
-        for (int idx = threadIdx.x; idx < N * PER; idx += kThreads) {
-            const int n = idx / PER, c = idx % PER;
+        // vector c of node n: c < QK8 a q/k vector, else one of this CTA's v vectors
+        auto conv_task = [&](int n, int c) -> uint4 {
             float w[8][4];
             load_taps8(ws + (size_t)c * 32, w);
             const int8_t* anc = p.anc[tree][n];
@@ -426,9 +457,27 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
             const Vec8 u2 = load8(xc + (size_t)row_of(anc[0]) * CW);
             const Vec8 u1 = load8(xc + (size_t)row_of(anc[1]) * CW);
             const Vec8 u0 = load8(xc + (size_t)row_of(anc[2]) * CW);
-            store_y(c < QK8 ? y_qk + (size_t)n * 2 * DK + 8 * c : s_v + (size_t)n * ROWS + 8 * (c - QK8), w, u0, u1,
-                    u2, u3);
+            return conv8_bf16(w, u0, u1, u2, u3);
+        };
+        const int n_qk = N * QK8;  // q/k tasks of the tree
+        for (int t = threadIdx.x; t * csize + (int)rank < n_qk; t += kThreads) {
+            const int j = t * csize + (int)rank;
+            const int n = j / QK8, c = j % QK8;
+            const uint4 y = conv_task(n, c);
+            uint16_t* dst = y_qk + (size_t)n * 2 * DK + 8 * c;
+            if (csize > 1) {
+                for (int r = 0; r < csize; ++r) st_cluster16(dst, (uint32_t)r, y);
+            } else {
+                *reinterpret_cast<uint4*>(dst) = y;
+            }
         }
+        for (int idx = threadIdx.x; idx < N * (ROWS / 8); idx += kThreads) {
+            const int n = idx / (ROWS / 8), c = idx % (ROWS / 8);
+            *reinterpret_cast<uint4*>(s_v + (size_t)n * ROWS + 8 * c) = conv_task(n, QK8 + c);
+        }
+        // every CTA's y_qk is complete (and no remote store is still to come:
+        // a CTA may leave the cluster only after this point)
+        if (csize > 1) cluster_sync_all();
     } else {
         for (int idx = threadIdx.x; idx < N * (ROWS / 8); idx += kThreads) {
             const int n = idx / (ROWS / 8), c = idx % (ROWS / 8);
@@ -926,7 +975,7 @@ cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int g
 }
 
 template <int DK, int MB, int R>
-static cudaError_t launch_tree_t(const TreeParamsT<MB>& p, cudaStream_t s) {
+static cudaError_t launch_tree_t(TreeParamsT<MB>& p, cudaStream_t s) {
     constexpr int ROWS = kRowsPerPass * R;
     const size_t smem = tree_slot_bytes<DK, R>(p.n_slots, p.Nmax, p.x != nullptr) + tree_stage_bytes<DK, R>(p.Nmax);
     // the shared-memory opt-in, once per device whatever the host threads
@@ -945,6 +994,29 @@ static cudaError_t launch_tree_t(const TreeParamsT<MB>& p, cudaStream_t s) {
     });
     if (setup_err[dev] != cudaSuccess) return setup_err[dev];
     dim3 grid(p.dv / ROWS, p.Hv, p.B);
+    // The fused conv shares each key head's q/k conv among the CTAs that read
+    // it -- the row blocks of its value heads, adjacent in the grid -- as one
+    // thread-block cluster (at most the portable 8 CTAs).  If the cluster
+    // cannot be placed, the launch falls back to one CTA per cluster.
+    const int csize = (p.dv / ROWS) * p.group;
+    if (p.x != nullptr && csize > 1 && csize <= 8) {
+        p.cluster = csize;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)(p.dv / ROWS);
+        attr[0].val.clusterDim.y = (unsigned)p.group;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, gdn_tree_kernel<DK, MB, R>, p) == cudaSuccess) return cudaSuccess;
+        (void)cudaGetLastError();  // a configuration error, not sticky: take the plain launch
+    }
+    p.cluster = 1;
     gdn_tree_kernel<DK, MB, R><<<grid, kThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
@@ -953,14 +1025,14 @@ static cudaError_t launch_tree_t(const TreeParamsT<MB>& p, cudaStream_t s) {
 // slots for them fit in shared memory (each node's record then serves two
 // rows per fetch), else 1.
 template <int DK, int MB>
-static cudaError_t launch_tree_r(const TreeParamsT<MB>& p, cudaStream_t s) {
+static cudaError_t launch_tree_r(TreeParamsT<MB>& p, cudaStream_t s) {
     const size_t smem2 = tree_slot_bytes<DK, 2>(p.n_slots, p.Nmax, p.x != nullptr) + tree_stage_bytes<DK, 2>(p.Nmax);
     if (p.dv % (2 * kRowsPerPass) == 0 && smem2 <= (size_t)kMaxSmemPerCta) return launch_tree_t<DK, MB, 2>(p, s);
     return launch_tree_t<DK, MB, 1>(p, s);
 }
 
 template <int MB>
-cudaError_t launch_tree(const TreeParamsT<MB>& p, int dk, cudaStream_t s) {
+cudaError_t launch_tree(TreeParamsT<MB>& p, int dk, cudaStream_t s) {
     switch (dk) {
         case 32: return launch_tree_r<32, MB>(p, s);
         case 64: return launch_tree_r<64, MB>(p, s);
@@ -968,7 +1040,7 @@ cudaError_t launch_tree(const TreeParamsT<MB>& p, int dk, cudaStream_t s) {
     }
     return cudaErrorInvalidValue;
 }
-template cudaError_t launch_tree<1>(const TreeParamsT<1>&, int, cudaStream_t);
-template cudaError_t launch_tree<kMaxTreeBatch>(const TreeParamsT<kMaxTreeBatch>&, int, cudaStream_t);
+template cudaError_t launch_tree<1>(TreeParamsT<1>&, int, cudaStream_t);
+template cudaError_t launch_tree<kMaxTreeBatch>(TreeParamsT<kMaxTreeBatch>&, int, cudaStream_t);
 
 }  // namespace gdn

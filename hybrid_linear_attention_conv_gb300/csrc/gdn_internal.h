@@ -59,6 +59,7 @@ struct TreeParamsT {
     const uint16_t* w;     // bf16 [C, 4]
     const uint16_t* tail;  // bf16 [B, 4, C] read only
     int8_t anc[MB][GDN_MAX_TREE_NODES][3];
+    int cluster;           // CTAs per thread-block cluster sharing the q/k conv (1: no cluster; set by the launcher)
 };
 constexpr int kMaxTreeBatch = 32;
 using TreeParams = TreeParamsT<1>;
@@ -160,7 +161,7 @@ int device_sm_count();                                        // SMs of the curr
 cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int gather, bool kda, bool in_f32,
                           cudaStream_t s);
 template <int MB>
-cudaError_t launch_tree(const TreeParamsT<MB>& p, int dk, cudaStream_t s);
+cudaError_t launch_tree(TreeParamsT<MB>& p, int dk, cudaStream_t s);  // sets p.cluster
 // kind: 0 the plain step, 1 KDA, 2 the layer step (gates in front, gated norm after)
 cudaError_t launch_conv_decode(const ConvDecodeParams& p, int dk, int rows_per_cta, int kind, cudaStream_t s);
 cudaError_t launch_gates(const GatesParams& p, cudaStream_t s);
