@@ -48,6 +48,12 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(gsrc) : "memory");
 }
 
+// One 4-byte global -> shared copy (cp.async); both addresses 4-byte aligned.
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gsrc) {
+    const uint32_t dst = (uint32_t)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(gsrc) : "memory");
+}
+
 // Thread-block cluster helpers (the fused verify's shared q/k conv).
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -341,7 +347,8 @@ __host__ __device__ constexpr size_t tree_kq_bytes(int N) {
 
 template <int DK, int R>
 __host__ __device__ constexpr size_t tree_stage_bytes(int N) {
-    return tree_kq_bytes<DK>(N) + (size_t)N * (kRowsPerPass * R * 2 + 2 * 4 + sizeof(TreeStep));
+    // per node: the record, v, alpha/beta, the schedule step and (fused conv) its 3 ancestors + pad
+    return tree_kq_bytes<DK>(N) + (size_t)N * (kRowsPerPass * R * 2 + 2 * 4 + sizeof(TreeStep) + 4);
 }
 
 // The region in front of the staging: the walk's branch slots, which the
@@ -387,6 +394,8 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     // the walk's schedule, copied out of the parameter block (read once per
     // step on the walk's dependent chain)
     TreeStep* steps = reinterpret_cast<TreeStep*>(s_ab + 2 * (size_t)p.Nmax);
+    // the fused conv's ancestor table, [N] x (3 ancestors + pad), copied out of the parameters
+    char4* s_anc = reinterpret_cast<char4*>(steps + p.Nmax);
     const int lane8 = threadIdx.x & 7;
     const int rg = threadIdx.x >> 3;
     const int h = blockIdx.y;
@@ -435,6 +444,17 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
             const int c = idx >> 2, q = idx & 3;
             cp_async16(ws + (size_t)c * 32 + 8 * q, p.w + (size_t)chan(c) * GDN_CONV_W + 8 * q);
         }
+        // the gates too, in the same round trip (after the conv they would cost another);
+        // and the per-node tables read with a per-node index out of the
+        // parameters (constant-cache misses), while the copies are in flight
+        for (int n = threadIdx.x; n < N; n += kThreads) {
+            cp_async4(s_ab + 2 * n, alpha_b + (size_t)n * p.Hv + h);
+            cp_async4(s_ab + 2 * n + 1, beta_b + (size_t)n * p.Hv + h);
+        }
+        for (int n = threadIdx.x; n < N; n += kThreads) {
+            steps[n] = p.steps[tree][n];
+            s_anc[n] = make_char4(p.anc[tree][n][0], p.anc[tree][n][1], p.anc[tree][n][2], 0);
+        }
         asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
         // With a cluster (the CTAs of one key head: its value heads' row
         // blocks), the q/k outputs are computed once per cluster: task j goes
@@ -451,7 +471,8 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
         auto conv_task = [&](int n, int c) -> uint4 {
             float w[8][4];
             load_taps8(ws + (size_t)c * 32, w);
-            const int8_t* anc = p.anc[tree][n];
+            const char4 a4 = s_anc[n];
+            const int anc[3] = {a4.x, a4.y, a4.z};
             const uint16_t* xc = xs + 8 * c;
             const Vec8 u3 = load8(xc + (size_t)(n + 3) * CW);
             const Vec8 u2 = load8(xc + (size_t)row_of(anc[0]) * CW);
@@ -485,7 +506,7 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
             *reinterpret_cast<uint4*>(s_v + (size_t)n * ROWS + c * 8) = __ldg(reinterpret_cast<const uint4*>(src));
         }
     }
-    {
+    if (!conv) {  // (the fused conv staged these with its inputs)
         for (int n = threadIdx.x; n < N; n += kThreads) {
             s_ab[2 * n] = alpha_b[(size_t)n * p.Hv + h];
             s_ab[2 * n + 1] = beta_b[(size_t)n * p.Hv + h];
