@@ -936,6 +936,33 @@ class TreeBatch(Workload):
         if rec:
             rec.mark("gdn_tree_kernel")
 
+    def extra_measures(self) -> dict:
+        """The same joint verify from pre-conv inputs: gdn_conv_tree_verify_batched
+        (each tree's conv inside the verify, the q/k conv of a key head shared by
+        its CTAs as one cluster).  L2 flushed before each, calls enqueued back to
+        back, median of 50."""
+        torch, P = self.torch, ctypes.c_void_p
+        B, N = self.B, self.N
+        x = self.randn((B, N, C_QKV), 1.0, torch.bfloat16)
+        w = self.randn((C_QKV, 4), 0.5, torch.bfloat16)
+        tails = self.randn((B, 4, C_QKV), 1.0, torch.bfloat16)
+        n = 53
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for i in range(n):
+            self.pre_step()
+            ev[i][0].record(self.stream)
+            _call(self.lib.gdn_conv_tree_verify_batched,
+                  (ctypes.byref(self.shape), N, self.counts.ctypes.data_as(P), self.parents.ctypes.data_as(P),
+                   P(x.data_ptr()), P(w.data_ptr()), P(tails.data_ptr()), P(self.alpha[0].data_ptr()),
+                   P(self.beta[0].data_ptr()), P(self.state.data_ptr()), P(self.out.data_ptr()), 1.0,
+                   self.gdn.GDN_NORMALIZE_QK, self.sp), self.gdn)
+            ev[i][1].record(self.stream)
+        torch.cuda.synchronize()
+        us = statistics.median(e[0].elapsed_time(e[1]) * 1e3 for e in ev[3:])
+        return {"conv_fused": {"us_per_step": us, "value": self.units_per_step / (us * 1e-6), "unit": UNIT,
+                               "how": "gdn_conv_tree_verify_batched on pre-conv inputs (8 trees x 32 nodes), L2 "
+                                      "flushed before each call, median of 50"}}
+
     def e2e_setup(self):
         self.e2e_views = self.e2e_pack([self.qkv[0].cpu(), self.alpha[0].cpu(), self.beta[0].cpu()])
         self.h_out = self.torch.empty(self.out.shape, dtype=self.torch.float32, pin_memory=True)

@@ -355,6 +355,67 @@ def test_conv_tree_verify_equals_conv_then_verify(shape, tree):
     assert np.array_equal(host(st), d["state"][0]) and np.array_equal(host(tail), c["tail"][0])
 
 
+@pytest.mark.parametrize("out_bf16,q_scale", [(True, 1.0), (False, 0.0884), (True, 0.0884)])
+def test_conv_tree_verify_flags_equal_unfused(out_bf16, q_scale):
+    """bf16 outputs and a q scale (1/sqrt(128)) through the fused verify: the
+    bits of conv + unfused verify with the same flags, on the 27B shape."""
+    shape = gen.QWEN_27B
+    parents = _FUSED_TREES["random32"]
+    N = len(parents)
+    c, d = _conv_case(shape, N, 73)
+    x, w, tail = bf16(c["x"][0]), bf16(c["w"]), bf16(c["tail"][0])
+    al, be, st = f32(d["alpha"][0]), f32(d["beta"][0]), f32(d["state"][0])
+    y = gdn.conv_step(x[None], w, tail[None].clone(), parents=parents)[0]
+    ref = gdn.tree_verify(parents, y, al, be, st, shape.Hk, shape.Hv, shape.dk, shape.dv, q_scale=q_scale,
+                          out_bf16=out_bf16)
+    out = gdn.conv_tree_verify(parents, x, w, tail, al, be, st, shape.Hk, shape.Hv, shape.dk, shape.dv,
+                               q_scale=q_scale, out_bf16=out_bf16)
+    torch.cuda.synchronize()
+    assert out.dtype == (torch.bfloat16 if out_bf16 else torch.float32)
+    assert torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("shape", [gen.TINY, gen.Shape(1, 2, 4, 64, 64)])
+def test_conv_round_batched_small_shapes(shape):
+    """The joint fused verify and batched fused commit at the small head
+    shapes (clusters of two CTAs): equal to the per-sequence fused calls."""
+    N = 20
+    trees = [gen.random_tree(120, 20, 6), gen.random_tree(121, 7, 4), np.array([-1], np.int32)]
+    B = len(trees)
+    counts = np.array([len(t) for t in trees], np.int32)
+    parents = _pad_parents(trees, N)
+    paths = np.full((B, N), -9, np.int32)
+    lengths = np.zeros(B, np.int32)
+    for b, t in enumerate(trees):
+        p = gdn.tree_root_path(t, gen.random_leaf(130 + b, t))
+        paths[b, :len(p)] = p
+        lengths[b] = len(p)
+    c, d = _conv_case(shape, N, 131, B=B, tag="roundsmall")
+    x, w, tail = bf16(c["x"]), bf16(c["w"]), bf16(c["tail"])
+    al, be, st = f32(d["alpha"]), f32(d["beta"]), f32(d["state"])
+    out = gdn.conv_tree_verify_batched(counts, parents, x, w, tail, al, be, st, shape.Hk, shape.Hv, shape.dk,
+                                       shape.dv)
+    tail_out = torch.empty_like(tail)
+    gdn.conv_commit_path_batched(counts, parents, paths, lengths, x, w, tail, tail_out, al, be, st, shape.Hk,
+                                 shape.Hv, shape.dk, shape.dv)
+    torch.cuda.synchronize()
+    for b, t in enumerate(trees):
+        n, L = len(t), int(lengths[b])
+        xb, alb, beb = x[b, :n].contiguous(), al[b, :n].contiguous(), be[b, :n].contiguous()
+        st1 = f32(d["state"][b])
+        o1 = gdn.conv_tree_verify(t, xb, w, tail[b], alb, beb, st1, shape.Hk, shape.Hv, shape.dk, shape.dv)
+        t1 = torch.empty_like(tail[b])
+        gdn.conv_commit_path(t, paths[b, :L], xb, w, tail[b], t1, alb, beb, st1, shape.Hk, shape.Hv, shape.dk,
+                             shape.dv)
+        torch.cuda.synchronize()
+        assert torch.equal(out[b, :n], o1) and torch.equal(st[b], st1) and torch.equal(tail_out[b], t1), b
+        # and the oracle (conv outputs rounded from binary32, as the kernels round them)
+        y_ref = oracle.conv_tree_r32(t, c["x"][b, :n], c["w"], c["tail"][b])
+        out_ref = oracle.tree_verify(t, y_ref, d["alpha"][b, :n], d["beta"][b, :n], d["state"][b], shape.Hk,
+                                     shape.Hv, shape.dk, shape.dv)
+        assert_out_close(host(o1), out_ref)
+
+
 @pytest.mark.parametrize("shape", [gen.TINY, gen.QWEN_27B])
 def test_conv_commit_equals_conv_then_commit_every_prefix(shape):
     """gdn_conv_commit_path == gdn_conv_step (tree mode) + gdn_commit_path with
