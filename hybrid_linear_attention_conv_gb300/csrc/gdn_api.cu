@@ -494,7 +494,7 @@ namespace {
 int tree_verify_impl(const gdn_shape* shape, int32_t N, const int32_t* parents, const gdn_bf16* qkv,
                      const gdn_bf16* x, const gdn_bf16* w, const gdn_bf16* tail, bool conv, const float* alpha,
                      const float* beta, const float* state, void* out, float q_scale, uint32_t flags,
-                     void* stream) {
+                     void* stream, bool kda = false) {
     int rc;
     if ((rc = check_shape(shape, true)) != GDN_OK) return rc;
     if ((rc = check_flags(flags)) != GDN_OK) return rc;
@@ -531,8 +531,11 @@ int tree_verify_impl(const gdn_shape* shape, int32_t N, const int32_t* parents, 
     p.q_scale = q_scale;
     p.normalize = (flags & GDN_NORMALIZE_QK) != 0;
     p.out_bf16 = (flags & GDN_OUT_BF16) != 0;
+    p.kda = kda;
     cudaError_t e = launch_tree(p, shape->dk, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? GDN_OK : cuda_fail(e, conv ? "conv + tree verify launch" : "tree verify launch");
+    return e == cudaSuccess ? GDN_OK
+                            : cuda_fail(e, kda ? "KDA tree verify launch"
+                                               : conv ? "conv + tree verify launch" : "tree verify launch");
 }
 
 int tree_verify_batched_impl(const gdn_shape* shape, int32_t N, const int32_t* counts, const int32_t* parents,
@@ -686,6 +689,13 @@ int gdn_tree_verify(const gdn_shape* shape, int32_t N, const int32_t* parents, c
                             q_scale, flags, stream);
 }
 
+int gdn_kda_tree_verify(const gdn_shape* shape, int32_t N, const int32_t* parents, const gdn_bf16* qkv,
+                        const float* alpha, const float* beta, const float* state, void* out, float q_scale,
+                        uint32_t flags, void* stream) {
+    return tree_verify_impl(shape, N, parents, qkv, nullptr, nullptr, nullptr, false, alpha, beta, state, out,
+                            q_scale, flags, stream, true);
+}
+
 int gdn_conv_tree_verify(const gdn_shape* shape, int32_t N, const int32_t* parents, const gdn_bf16* x,
                          const gdn_bf16* w, const gdn_bf16* tail, const float* alpha, const float* beta,
                          const float* state, void* out, float q_scale, uint32_t flags, void* stream) {
@@ -708,10 +718,14 @@ int gdn_conv_tree_verify_batched(const gdn_shape* shape, int32_t N, const int32_
                                     q_scale, flags, stream);
 }
 
-int gdn_commit_path(const gdn_shape* shape, int32_t N, const int32_t* parents, const int32_t* path,
-                    int32_t L, const gdn_bf16* qkv, const float* alpha, const float* beta,
-                    const gdn_bf16* x_tree, float* state, gdn_bf16* tail, uint32_t flags,
-                    void* stream) {
+}  // extern "C"
+
+// The single-sequence commit through the decode kernel's gather path (kda:
+// a decay per key channel, alpha [N, Hv, dk]).
+static int commit_path_impl(const gdn_shape* shape, int32_t N, const int32_t* parents, const int32_t* path,
+                            int32_t L, const gdn_bf16* qkv, const float* alpha, const float* beta,
+                            const gdn_bf16* x_tree, float* state, gdn_bf16* tail, uint32_t flags, void* stream,
+                            bool kda) {
     int rc;
     if ((rc = check_shape(shape, true)) != GDN_OK) return rc;
     if (flags & GDN_OUT_BF16) return fail(GDN_ERR_INVALID_ARG, "commit writes no output; GDN_OUT_BF16 not allowed");
@@ -745,10 +759,25 @@ int gdn_commit_path(const gdn_shape* shape, int32_t N, const int32_t* parents, c
     p.x_tree = x_tree;  // the conv tail is updated by the same launch
     p.tail = x_tree != nullptr ? tail : nullptr;
     const int rows = decode_rows_per_cta(1, shape->Hv, shape->dv);
-    cudaError_t e = launch_decode(p, shape->dk, rows, 1, false, false, st);
-    if (e != cudaSuccess) return cuda_fail(e, "commit launch");
+    cudaError_t e = launch_decode(p, shape->dk, rows, 1, kda, false, st);
+    if (e != cudaSuccess) return cuda_fail(e, kda ? "KDA commit launch" : "commit launch");
     return GDN_OK;
 }
+
+extern "C" {
+
+int gdn_commit_path(const gdn_shape* shape, int32_t N, const int32_t* parents, const int32_t* path, int32_t L,
+                    const gdn_bf16* qkv, const float* alpha, const float* beta, const gdn_bf16* x_tree, float* state,
+                    gdn_bf16* tail, uint32_t flags, void* stream) {
+    return commit_path_impl(shape, N, parents, path, L, qkv, alpha, beta, x_tree, state, tail, flags, stream, false);
+}
+
+int gdn_kda_commit_path(const gdn_shape* shape, int32_t N, const int32_t* parents, const int32_t* path, int32_t L,
+                        const gdn_bf16* qkv, const float* alpha, const float* beta, const gdn_bf16* x_tree,
+                        float* state, gdn_bf16* tail, uint32_t flags, void* stream) {
+    return commit_path_impl(shape, N, parents, path, L, qkv, alpha, beta, x_tree, state, tail, flags, stream, true);
+}
+
 
 int gdn_commit_path_batched(const gdn_shape* shape, int32_t N, const int32_t* counts, const int32_t* parents,
                             const int32_t* paths, const int32_t* lengths, const gdn_bf16* qkv, const float* alpha,

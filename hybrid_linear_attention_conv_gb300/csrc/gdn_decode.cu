@@ -374,7 +374,11 @@ __host__ __device__ constexpr size_t tree_slot_bytes(int n_slots, int N, bool co
 // per thread, serve R rows: the walk is bound by those fetches (every row of
 // every value head reads the whole record), and R rows per fetch divide that
 // traffic by R while giving each thread R independent row chains.
-template <int DK, int MB, int R>
+// KDA: a decay vector per node and head (alpha [B, Nmax, Hv, dk]) staged after
+// the other inputs, [N][dk] fp32; each step applies kda_decay and the delta
+// step of the KDA decode, so a node's output is the bits of gdn_kda_decode_step
+// over its root path.
+template <int DK, int MB, int R, bool KDA>
 __global__ void __launch_bounds__(kThreads)
 gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     constexpr int V = DK / 32;
@@ -396,6 +400,8 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     TreeStep* steps = reinterpret_cast<TreeStep*>(s_ab + 2 * (size_t)p.Nmax);
     // the fused conv's ancestor table, [N] x (3 ancestors + pad), copied out of the parameters
     char4* s_anc = reinterpret_cast<char4*>(steps + p.Nmax);
+    // KDA: the nodes' decay vectors for head h, [N][DK / 4] float4, after the staging
+    float4* s_gate = reinterpret_cast<float4*>(stage + tree_stage_bytes<DK, R>(p.Nmax));
     const int lane8 = threadIdx.x & 7;
     const int rg = threadIdx.x >> 3;
     const int h = blockIdx.y;
@@ -448,8 +454,14 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
         // and the per-node tables read with a per-node index out of the
         // parameters (constant-cache misses), while the copies are in flight
         for (int n = threadIdx.x; n < N; n += kThreads) {
-            cp_async4(s_ab + 2 * n, alpha_b + (size_t)n * p.Hv + h);
+            if (!KDA) cp_async4(s_ab + 2 * n, alpha_b + (size_t)n * p.Hv + h);
             cp_async4(s_ab + 2 * n + 1, beta_b + (size_t)n * p.Hv + h);
+        }
+        if constexpr (KDA) {
+            for (int idx = threadIdx.x; idx < N * (DK / 4); idx += kThreads) {
+                const int n = idx / (DK / 4), c4 = idx % (DK / 4);
+                cp_async16(s_gate + idx, p.alpha + (((size_t)tree * p.Nmax + n) * p.Hv + h) * DK + 4 * c4);
+            }
         }
         for (int n = threadIdx.x; n < N; n += kThreads) {
             steps[n] = p.steps[tree][n];
@@ -508,9 +520,16 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     }
     if (!conv) {  // (the fused conv staged these with its inputs)
         for (int n = threadIdx.x; n < N; n += kThreads) {
-            s_ab[2 * n] = alpha_b[(size_t)n * p.Hv + h];
+            if (!KDA) s_ab[2 * n] = alpha_b[(size_t)n * p.Hv + h];
             s_ab[2 * n + 1] = beta_b[(size_t)n * p.Hv + h];
             steps[n] = p.steps[tree][n];
+        }
+        if constexpr (KDA) {
+            for (int idx = threadIdx.x; idx < N * (DK / 4); idx += kThreads) {
+                const int n = idx / (DK / 4), c4 = idx % (DK / 4);
+                s_gate[idx] = __ldg(reinterpret_cast<const float4*>(
+                    p.alpha + (((size_t)tree * p.Nmax + n) * p.Hv + h) * DK + 4 * c4));
+            }
         }
     }
     __syncthreads();
@@ -573,13 +592,25 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
         }
         const int node = st.node;
         if (step + 1 < N) fetch(steps[step + 1].node, nxt);
-        const float alpha = s_ab[2 * node];
         const float beta = s_ab[2 * node + 1];
         float o[R];
+        if constexpr (KDA) {
+            float4 gv[V];
+            load_gate_smem<V>(s_gate + (size_t)node * (DK / 4), lane8, gv);
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const float v_i = __uint_as_float((uint32_t)s_v[(size_t)node * ROWS + kRowsPerPass * r + rg] << 16);
-            o[r] = row_step<V>(s[r], cur, v_i, alpha, beta);
+            for (int r = 0; r < R; ++r) kda_decay<V>(s[r], gv);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const float v_i = __uint_as_float((uint32_t)s_v[(size_t)node * ROWS + kRowsPerPass * r + rg] << 16);
+                o[r] = delta_row_step<V>(s[r], cur, v_i, beta);
+            }
+        } else {
+            const float alpha = s_ab[2 * node];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const float v_i = __uint_as_float((uint32_t)s_v[(size_t)node * ROWS + kRowsPerPass * r + rg] << 16);
+                o[r] = row_step<V>(s[r], cur, v_i, alpha, beta);
+            }
         }
         // lane r of a row group stores row r's output (every lane holds the same bits)
         float my_o = o[0];
@@ -995,10 +1026,15 @@ cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int g
                : launch_decode_k<false, false>(p, dk, rows_per_cta, s);
 }
 
-template <int DK, int MB, int R>
+template <int DK, int R>
+static size_t tree_smem_bytes(int n_slots, int N, bool conv, bool kda) {
+    return tree_slot_bytes<DK, R>(n_slots, N, conv) + tree_stage_bytes<DK, R>(N) + (kda ? (size_t)N * DK * 4 : 0);
+}
+
+template <int DK, int MB, int R, bool KDA>
 static cudaError_t launch_tree_t(TreeParamsT<MB>& p, cudaStream_t s) {
     constexpr int ROWS = kRowsPerPass * R;
-    const size_t smem = tree_slot_bytes<DK, R>(p.n_slots, p.Nmax, p.x != nullptr) + tree_stage_bytes<DK, R>(p.Nmax);
+    const size_t smem = tree_smem_bytes<DK, R>(p.n_slots, p.Nmax, p.x != nullptr, KDA);
     // the shared-memory opt-in, once per device whatever the host threads
     static std::once_flag once[64];
     static cudaError_t setup_err[64];
@@ -1007,11 +1043,10 @@ static cudaError_t launch_tree_t(TreeParamsT<MB>& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::call_once(once[dev], [dev] {
-        const int max_smem = std::min((int)(tree_slot_bytes<DK, R>(GDN_MAX_TREE_SLOTS, GDN_MAX_TREE_NODES, true) +
-                                            tree_stage_bytes<DK, R>(GDN_MAX_TREE_NODES)),
+        const int max_smem = std::min((int)tree_smem_bytes<DK, R>(GDN_MAX_TREE_SLOTS, GDN_MAX_TREE_NODES, true, KDA),
                                       kMaxSmemPerCta);
-        setup_err[dev] = cudaFuncSetAttribute(gdn_tree_kernel<DK, MB, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              max_smem);
+        setup_err[dev] = cudaFuncSetAttribute(gdn_tree_kernel<DK, MB, R, KDA>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     });
     if (setup_err[dev] != cudaSuccess) return setup_err[dev];
     dim3 grid(p.dv / ROWS, p.Hv, p.B);
@@ -1034,30 +1069,43 @@ static cudaError_t launch_tree_t(TreeParamsT<MB>& p, cudaStream_t s) {
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, gdn_tree_kernel<DK, MB, R>, p) == cudaSuccess) return cudaSuccess;
+        if (cudaLaunchKernelEx(&cfg, gdn_tree_kernel<DK, MB, R, KDA>, p) == cudaSuccess) return cudaSuccess;
         (void)cudaGetLastError();  // a configuration error, not sticky: take the plain launch
     }
     p.cluster = 1;
-    gdn_tree_kernel<DK, MB, R><<<grid, kThreads, smem, s>>>(p);
+    gdn_tree_kernel<DK, MB, R, KDA><<<grid, kThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 
 // Rows per thread: 2 when the value head has a multiple of 64 rows and the
 // slots for them fit in shared memory (each node's record then serves two
 // rows per fetch), else 1.
-template <int DK, int MB>
+template <int DK, int MB, bool KDA>
 static cudaError_t launch_tree_r(TreeParamsT<MB>& p, cudaStream_t s) {
-    const size_t smem2 = tree_slot_bytes<DK, 2>(p.n_slots, p.Nmax, p.x != nullptr) + tree_stage_bytes<DK, 2>(p.Nmax);
-    if (p.dv % (2 * kRowsPerPass) == 0 && smem2 <= (size_t)kMaxSmemPerCta) return launch_tree_t<DK, MB, 2>(p, s);
-    return launch_tree_t<DK, MB, 1>(p, s);
+    const size_t smem2 = tree_smem_bytes<DK, 2>(p.n_slots, p.Nmax, p.x != nullptr, KDA);
+    if (p.dv % (2 * kRowsPerPass) == 0 && smem2 <= (size_t)kMaxSmemPerCta) return launch_tree_t<DK, MB, 2, KDA>(p, s);
+    return launch_tree_t<DK, MB, 1, KDA>(p, s);
 }
 
+// KDA: single trees only (the host refuses a joint KDA verify)
 template <int MB>
 cudaError_t launch_tree(TreeParamsT<MB>& p, int dk, cudaStream_t s) {
+    if (p.kda) {
+        if constexpr (MB != 1) {
+            return cudaErrorInvalidValue;
+        } else {
+            switch (dk) {
+                case 32: return launch_tree_r<32, MB, true>(p, s);
+                case 64: return launch_tree_r<64, MB, true>(p, s);
+                case 128: return launch_tree_r<128, MB, true>(p, s);
+            }
+            return cudaErrorInvalidValue;
+        }
+    }
     switch (dk) {
-        case 32: return launch_tree_r<32, MB>(p, s);
-        case 64: return launch_tree_r<64, MB>(p, s);
-        case 128: return launch_tree_r<128, MB>(p, s);
+        case 32: return launch_tree_r<32, MB, false>(p, s);
+        case 64: return launch_tree_r<64, MB, false>(p, s);
+        case 128: return launch_tree_r<128, MB, false>(p, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -56,6 +56,8 @@ EXPORTS = [
     "gdn_tree_verify_batched",
     "gdn_commit_path",
     "gdn_commit_path_batched",
+    "gdn_kda_tree_verify",
+    "gdn_kda_commit_path",
     "gdn_conv_tree_verify",
     "gdn_conv_tree_verify_batched",
     "gdn_conv_commit_path",
@@ -119,6 +121,8 @@ def load(path: str = LIB_PATH):
             "gdn_tree_verify_batched": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, F, U32, P]),
             "gdn_commit_path": (ctypes.c_int, [SH, I32, P, P, I32, P, P, P, P, P, P, U32, P]),
             "gdn_commit_path_batched": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, P, P, P, U32, P]),
+            "gdn_kda_tree_verify": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, F, U32, P]),
+            "gdn_kda_commit_path": (ctypes.c_int, [SH, I32, P, P, I32, P, P, P, P, P, P, U32, P]),
             "gdn_conv_tree_verify": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, P, F, U32, P]),
             "gdn_conv_tree_verify_batched": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, P, P, F, U32, P]),
             "gdn_conv_commit_path": (ctypes.c_int, [SH, I32, P, P, I32, P, P, P, P, P, P, P, U32, P]),
@@ -420,6 +424,40 @@ def commit_path_batched(counts, parents, paths, lengths, qkv, alpha, beta, state
         _dev(state, torch.float32, "state", (B, Hv, dv, dk)), _dev(tail, torch.bfloat16, "tail", (B, GDN_CONV_W, C)),
         _flags(normalize, False), _stream())
     _check(rc, "gdn_commit_path_batched")
+
+
+def kda_tree_verify(parents, qkv, alpha, beta, state, Hk, Hv, dk, dv, out=None, q_scale=1.0,
+                    normalize=True, out_bf16=False) -> torch.Tensor:
+    """The KDA tree verify.  qkv bf16 [N,C], alpha fp32 [N,Hv,dk], beta fp32 [N,Hv],
+    state fp32 [Hv,dv,dk] (read only) -> out [N,Hv,dv]."""
+    par, pp = _host_i32(parents, "parents")
+    N = len(par)
+    if out is None:
+        out = torch.empty((N, Hv, dv), dtype=torch.bfloat16 if out_bf16 else torch.float32, device=qkv.device)
+    rc = load().gdn_kda_tree_verify(
+        ctypes.byref(_shape(1, Hk, Hv, dk, dv)), N, pp,
+        _dev(qkv, torch.bfloat16, "qkv", (N, packed_channels(Hk, Hv, dk, dv))),
+        _dev(alpha, torch.float32, "alpha", (N, Hv, dk)), _dev(beta, torch.float32, "beta", (N, Hv)),
+        _dev(state, torch.float32, "state", (Hv, dv, dk)),
+        _dev(out, torch.bfloat16 if out_bf16 else torch.float32, "out", (N, Hv, dv)),
+        float(q_scale), _flags(normalize, out_bf16), _stream())
+    _check(rc, "gdn_kda_tree_verify")
+    return out
+
+
+def kda_commit_path(parents, path, qkv, alpha, beta, state, Hk, Hv, dk, dv, x_tree=None, tail=None,
+                    normalize=True) -> None:
+    """The KDA commit: replays `path` in place on state [Hv,dv,dk]; alpha fp32 [N,Hv,dk]; updates tail [4,C]."""
+    par, pp = _host_i32(parents, "parents")
+    pa, ppa = _host_i32(path, "path")
+    N = len(par)
+    C = packed_channels(Hk, Hv, dk, dv)
+    rc = load().gdn_kda_commit_path(
+        ctypes.byref(_shape(1, Hk, Hv, dk, dv)), N, pp, ppa, len(pa), _dev(qkv, torch.bfloat16, "qkv", (N, C)),
+        _dev(alpha, torch.float32, "alpha", (N, Hv, dk)), _dev(beta, torch.float32, "beta", (N, Hv)),
+        _dev(x_tree, torch.bfloat16, "x_tree", (N, C)), _dev(state, torch.float32, "state", (Hv, dv, dk)),
+        _dev(tail, torch.bfloat16, "tail", (GDN_CONV_W, C)), _flags(normalize, False), _stream())
+    _check(rc, "gdn_kda_commit_path")
 
 
 def conv_tree_verify(parents, x, w, tail, alpha, beta, state, Hk, Hv, dk, dv, out=None, q_scale=1.0,

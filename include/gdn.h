@@ -351,6 +351,37 @@ int gdn_commit_path_batched(const gdn_shape* shape, int32_t N, const int32_t* co
                             void* stream);
 
 /*
+ * gdn_kda_tree_verify -- gdn_tree_verify with the KDA step of
+ * gdn_kda_decode_step (a decay per key channel): node n's state is the
+ * committed state advanced through the root..n path by
+ *   S <- (S diag(a_t)) (I - beta_t k^_t k^_t^T) + beta_t v_t k^_t^T,
+ * and out[n] = S_n q^_n.  Each node's output equals, bit for bit, the output
+ * gdn_kda_decode_step gives for the last token of that node's root path.
+ *   alpha  fp32 [N, Hv, dk] (node n's decay vector for head h at
+ *          alpha[(n * Hv + h) * dk]); every other argument as for
+ *          gdn_tree_verify.
+ * Source: the KDA mixer of the metrale_model_arch API page (see
+ * gdn_kda_decode_step) run over "a tree" ("Architecture" v0.11.1, "The parts";
+ * v0.14.2 section 8.3).
+ */
+int gdn_kda_tree_verify(const gdn_shape* shape, int32_t N, const int32_t* parents,
+                        const gdn_bf16* qkv, const float* alpha, const float* beta,
+                        const float* state, void* out, float q_scale, uint32_t flags,
+                        void* stream);
+
+/*
+ * gdn_kda_commit_path -- gdn_commit_path with the KDA step: replays the
+ * accepted path through gdn_kda_decode_step's arithmetic in place (bit for
+ * bit the KDA decode of the path's gathered inputs), and updates the conv
+ * tail as gdn_commit_path does.
+ *   alpha  fp32 [N, Hv, dk]; every other argument as for gdn_commit_path.
+ */
+int gdn_kda_commit_path(const gdn_shape* shape, int32_t N, const int32_t* parents,
+                        const int32_t* path, int32_t L, const gdn_bf16* qkv,
+                        const float* alpha, const float* beta, const gdn_bf16* x_tree,
+                        float* state, gdn_bf16* tail, uint32_t flags, void* stream);
+
+/*
  * The speculative round with the conv fused in.  A round is a tree conv, the
  * verify and the commit; these entry points take the tree's PRE-conv inputs
  * and run the 4-tap conv + SiLU inside the verify and commit kernels, so the

@@ -432,3 +432,29 @@ def test_conv_fused_round_validation(lib):
     assert cbatch(lengths=(3, 4)) == -4
     assert cbatch() == -6
     assert cbatch(lengths=(0, 0)) == -6  # no sequence accepted anything: still validated
+
+
+def test_kda_round_validation(lib):
+    """The KDA tree verify and commit validate like the plain ones; nothing is launched."""
+    P = ctypes.c_void_p
+    parents = np.array([-1, 0, 0, 1, 3], np.int32)
+
+    def verify(alpha=FAKE, sh=None, par=parents, state=FAKE + 4):
+        return lib.gdn_kda_tree_verify(ctypes.byref(sh or _sh()), len(par), par.ctypes.data_as(P), P(FAKE),
+                                       P(alpha), P(FAKE), P(state), P(FAKE), 1.0, 1, None)
+
+    assert verify(alpha=None) == -1
+    assert verify(alpha=FAKE + 4) == -6
+    assert verify(sh=_sh(B=2)) == -2
+    assert verify(par=np.array([-1, 1], np.int32)) == -3
+    assert verify() == -6 and "state" in gdn.last_error()
+
+    def commit(path=(0, 1, 3), state=FAKE + 4, flags=1):
+        pa = np.ascontiguousarray(path, np.int32)
+        return lib.gdn_kda_commit_path(ctypes.byref(_sh()), len(parents), parents.ctypes.data_as(P),
+                                       pa.ctypes.data_as(P) if pa.size else None, len(pa), P(FAKE), P(FAKE),
+                                       P(FAKE), None, P(state), None, flags, None)
+
+    assert commit(path=(1, 3)) == -4
+    assert commit(flags=1 | gdn.GDN_OUT_BF16) == -1
+    assert commit() == -6

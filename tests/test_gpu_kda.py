@@ -163,3 +163,75 @@ def test_kda_conv_decode_fused_vs_oracle_27b():
     assert np.array_equal(host(tail), tail_ref)
     assert_out_close(host(out), out_ref)
     assert_state_close(host(st), st_ref)
+
+
+# ---------------------------------------------------------------------------
+# the speculative round with the KDA step: tree verify and commit
+# ---------------------------------------------------------------------------
+def _kda_tree_case(shape, N, seed, tag="kdatree"):
+    d = gen.kda_inputs(seed, shape.with_batch(1), N, tag=tag)
+    return {"qkv": d["qkv"][0], "alpha": d["alpha"][0], "beta": d["beta"][0], "state": d["state"][0]}
+
+
+def _kda_path_decode(shape, d, path):
+    st = f32(d["state"][None])
+    out = gdn.kda_decode_step(bf16(d["qkv"][None, path]), f32(d["alpha"][None, path]), f32(d["beta"][None, path]),
+                              st, shape.Hk, shape.Hv, shape.dk, shape.dv)
+    torch.cuda.synchronize()
+    return out[0], st[0]
+
+
+@pytest.mark.parametrize("shape,parents", [
+    (gen.QWEN_27B, gen.random_tree(150, 32, 8)),
+    (gen.TINY, gen.random_tree(151, 20, 6)),
+    (gen.Shape(1, 2, 4, 64, 64), np.array([-1] + [0] * 15, np.int32)),      # a star
+    (gen.Shape(1, 2, 4, 64, 64), np.arange(-1, 40, dtype=np.int32)),        # a 41-long chain
+])
+def test_kda_tree_verify_equals_kda_decode_of_root_paths(shape, parents):
+    """Every node's output is the bits of the KDA decode of its root path; the
+    committed state is untouched; and the outputs agree with the oracle's KDA
+    decode of the root paths (a sample of nodes at the 27B shape)."""
+    N = len(parents)
+    d = _kda_tree_case(shape, N, 152)
+    st = f32(d["state"])
+    out = gdn.kda_tree_verify(parents, bf16(d["qkv"]), f32(d["alpha"]), f32(d["beta"]), st, shape.Hk, shape.Hv,
+                              shape.dk, shape.dv)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(st), d["state"]), "verify must not write the committed state"
+    nodes = range(N) if shape is not gen.QWEN_27B else [0, 1, 7, 15, N - 1]
+    for n in range(N):
+        path = gdn.tree_root_path(parents, n)
+        o, _ = _kda_path_decode(shape, d, path)
+        assert torch.equal(out[n], o[-1]), f"node {n}"
+        if n in nodes:
+            o_ref, _ = oracle.kda_decode(d["qkv"][None, path], d["alpha"][None, path], d["beta"][None, path],
+                                         d["state"][None], shape.Hk, shape.Hv, shape.dk, shape.dv)
+            assert_out_close(host(out[n]), o_ref[0, -1])
+
+
+@pytest.mark.parametrize("shape", [gen.QWEN_27B, gen.TINY])
+def test_kda_commit_equals_kda_decode_every_prefix(shape):
+    """The KDA commit of every prefix of a root-to-leaf path: the bits of the
+    KDA decode of the gathered path, the tail the last four inputs, and the
+    state within the oracle's bar."""
+    N = 32
+    parents = gen.random_tree(153, N, 8)
+    path = gdn.tree_root_path(parents, gen.random_leaf(153, parents))
+    d = _kda_tree_case(shape, N, 154)
+    c = gen.conv_inputs(155, 1, N, shape.C, tag="kdacommit")
+    for L in range(len(path) + 1):
+        st = f32(d["state"])
+        tail = bf16(c["tail"][0])
+        gdn.kda_commit_path(parents, path[:L], bf16(d["qkv"]), f32(d["alpha"]), f32(d["beta"]), st, shape.Hk,
+                            shape.Hv, shape.dk, shape.dv, x_tree=bf16(c["x"][0]), tail=tail)
+        torch.cuda.synchronize()
+        hist = np.concatenate([c["tail"][0], c["x"][0][path[:L]]], axis=0)
+        assert np.array_equal(host(tail), hist[-4:]), f"L={L}: tail"
+        if L == 0:
+            assert np.array_equal(host(st), d["state"])
+            continue
+        _, st_dec = _kda_path_decode(shape, d, path[:L])
+        assert torch.equal(st, st_dec), f"L={L}: state"
+    _, st_ref = oracle.kda_decode(d["qkv"][None, path], d["alpha"][None, path], d["beta"][None, path],
+                                  d["state"][None], shape.Hk, shape.Hv, shape.dk, shape.dv)
+    assert_state_close(host(st), st_ref[0])
