@@ -799,8 +799,9 @@ class Tree(Workload):
     def marks_per_step(self) -> int:
         return self.tree_marks
 
-    def _run(self, s, rec=None, inputs=None, i=0):
-        """The fused round: step i reads tail buffer i % 2 and writes the other."""
+    def _run(self, s, rec=None, inputs=None, i=0, between=None):
+        """The fused round: step i reads tail buffer i % 2 and writes the other.
+        `between` runs after the verify is enqueued and before the commit."""
         P = ctypes.c_void_p
         lib, gdn = self.lib, self.gdn
         pp = self.parents.ctypes.data_as(P)
@@ -812,6 +813,8 @@ class Tree(Workload):
                                          gdn.GDN_NORMALIZE_QK, self.sp), gdn)
         if rec:
             rec.mark("gdn_tree_kernel")
+        if between is not None:
+            between()
         _call(lib.gdn_conv_commit_path, (ctypes.byref(self.shape), self.N, pp, self.path.ctypes.data_as(P),
                                          len(self.path), P(x.data_ptr()), P(self.w.data_ptr()),
                                          P(t_in.data_ptr()), P(t_out.data_ptr()), P(alpha.data_ptr()),
@@ -877,11 +880,27 @@ class Tree(Workload):
         self.h_out = self.torch.empty(self.out.shape, dtype=self.torch.float32, pin_memory=True)
         self.e2e_h2d = self.e2e_hbuf.numel()
         self.e2e_d2h = self.h_out.numel() * 4
+        self.e2e_streams()
 
     def e2e_step(self, i: int):
+        """Inputs in (one packed copy), the verify, then the verify's outputs
+        back to the host on their own stream while the commit runs; the step
+        ends once both are done."""
+        torch = self.torch
+        cs = torch.cuda.current_stream()
         self.e2e_copy(self.e2e_dbuf, self.e2e_hbuf)  # x, alpha, beta in one copy
-        self._run(0, inputs=self.e2e_views, i=i)
-        self.e2e_copy(self.h_out, self.out)
+
+        def out_back():
+            ev = torch.cuda.Event()
+            ev.record(cs)
+            with torch.cuda.stream(self.s_out):
+                self.s_out.wait_event(ev)
+                self.h_out.copy_(self.out, non_blocking=True)
+
+        self._run(0, inputs=self.e2e_views, i=i, between=out_back)
+        done = torch.cuda.Event()
+        done.record(self.s_out)
+        cs.wait_event(done)
 
     def config(self=None) -> dict:
         L = None if self is None else len(self.path)

@@ -8,13 +8,15 @@
 // stores use the streaming cache hint, since a batched decode touches each
 // state exactly once per step and it should not evict the activations from L2.
 //
-// Tree verify: one CTA owns 32 rows of one value head and walks the draft
+// Tree verify: one CTA owns 32 R rows of one value head and walks the draft
 // tree depth-first.  The current node's rows stay in registers; the rows of a
 // node with two or more children are parked in shared memory until its last
 // child starts (host-computed slots).  The committed state is read once and
 // node states never reach HBM (TandemLLM "Architecture" v0.14.2 section 8.3:
 // each draft node's state branches from its parent's and the whole tree is
-// verified in one pass).
+// verified in one pass).  Given pre-conv inputs, the CTA also runs the tree
+// conv of the channels it reads (a key head's CTAs share its q/k conv as one
+// thread-block cluster); a KDA variant applies a decay per key channel.
 #include <cuda_runtime.h>
 
 #include <algorithm>
