@@ -267,3 +267,28 @@ def test_prefill_wait_timeout_is_reported_and_recovers(two_launch):
     out_ref, st_ref = oracle_decode_parallel(d["qkv"], d["alpha"], d["beta"], d["state"], shape)
     assert_out_close(host(out), out_ref[0])
     assert_state_close(host(st), st_ref[0])
+
+
+def test_prefill_long_prompt_split_calls_and_sampled_heads():
+    """32,768 tokens (four times the config's prompt) at the 27B shape, in one
+    call and as four calls of 8,192 with the state carried (chunk boundaries
+    unchanged, so the same bits); key heads 0 and 15 -- all their value heads,
+    every output and the final state -- against the oracle (key heads are
+    independent problems, run on two host cores)."""
+    shape = gen.QWEN_27B
+    T, P = 32768, 8192
+    d = gen.decode_inputs(32, shape.with_batch(1), T, tag="prefill-long")
+    qkv, al, be = bf16(d["qkv"][0]), f32(d["alpha"][0]), f32(d["beta"][0])
+    st = f32(d["state"][0])
+    out = gdn.chunk_prefill(qkv, al, be, st, shape.Hk, shape.Hv, shape.dk, shape.dv)
+    st2 = f32(d["state"][0])
+    outs = [gdn.chunk_prefill(qkv[i:i + P], al[i:i + P], be[i:i + P], st2, shape.Hk, shape.Hv, shape.dk,
+                              shape.dv) for i in range(0, T, P)]
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat(outs, 0), out) and torch.equal(st2, st)
+    keys = [0, shape.Hk - 1]
+    out_ref, st_ref = oracle_decode_parallel(d["qkv"], d["alpha"], d["beta"], d["state"], shape, keys=keys)
+    grp = shape.Hv // shape.Hk
+    heads = np.concatenate([np.arange(g * grp, (g + 1) * grp) for g in keys])
+    assert_out_close(host(out)[:, heads], out_ref[0][:, heads])
+    assert_state_close(host(st)[heads], st_ref[0][heads])

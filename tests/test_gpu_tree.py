@@ -550,3 +550,32 @@ def test_conv_round_batched_equals_single(B):
         assert torch.equal(st[b], st1), f"sequence {b}: state"
         assert torch.equal(tail_out[b], t1), f"sequence {b}: tail"
     assert np.array_equal(host(st[1]), d["state"][1]) and np.array_equal(host(tail_out[1]), c["tail"][1])
+
+
+def test_tree_verify_batched_at_the_maximum():
+    """The joint verify at its limits: 32 sequences, node capacity 64, trees of
+    1 to 64 nodes with branching states up to the slot limit; each tree equals
+    its single-tree verify bit for bit, and three of them the oracle."""
+    shape = gen.QWEN_27B
+    B, N = 32, 64
+    trees = [gen.random_tree(200 + b, 1 + (b * 37) % 64, 2 + b % 7) for b in range(B)]
+    trees[0] = np.arange(-1, 63, dtype=np.int32)  # the longest chain
+    counts = np.array([len(t) for t in trees], np.int32)
+    parents = _pad_parents(trees, N)
+    d = gen.decode_inputs(240, shape.with_batch(B), N, tag="treemax")
+    st = f32(d["state"])
+    out = torch.full((B, N, shape.Hv, shape.dv), float("nan"), device="cuda")
+    gdn.tree_verify_batched(counts, parents, bf16(d["qkv"]), f32(d["alpha"]), f32(d["beta"]), st, shape.Hk,
+                            shape.Hv, shape.dk, shape.dv, out=out)
+    torch.cuda.synchronize()
+    for b, t in enumerate(trees):
+        n = len(t)
+        single = gdn.tree_verify(t, bf16(d["qkv"][b, :n]), f32(d["alpha"][b, :n]), f32(d["beta"][b, :n]),
+                                 f32(d["state"][b]), shape.Hk, shape.Hv, shape.dk, shape.dv)
+        torch.cuda.synchronize()
+        assert torch.equal(out[b, :n], single), f"tree {b}"
+        assert torch.isnan(out[b, n:]).all()
+        if b in (0, 13, 31):
+            ref = oracle.tree_verify(t, d["qkv"][b, :n], d["alpha"][b, :n], d["beta"][b, :n], d["state"][b],
+                                     shape.Hk, shape.Hv, shape.dk, shape.dv)
+            assert_out_close(host(out[b, :n]), ref)
