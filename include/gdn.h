@@ -386,9 +386,10 @@ int gdn_kda_commit_path(const gdn_shape* shape, int32_t N, const int32_t* parent
  * verify and the commit; these entry points take the tree's PRE-conv inputs
  * and run the 4-tap conv + SiLU inside the verify and commit kernels, so the
  * conv outputs never reach HBM and the round is two launches instead of three.
- * Each CTA computes the conv of the channels it reads (its key head's q and k,
- * its own rows of v) with the arithmetic and bf16 rounding of gdn_conv_step,
- * so the results are the same bits as the unfused calls.
+ * The kernels compute the conv outputs they read (a key head's q and k, shared
+ * by the CTAs that read them, and each CTA's own rows of v) with the
+ * arithmetic and bf16 rounding of gdn_conv_step, so the results are the same
+ * bits as the unfused calls.
  *
  * gdn_conv_tree_verify -- gdn_conv_step in tree mode (x -> y) followed by
  * gdn_tree_verify on y, in one launch.  out equals that pair's, bit for bit.
