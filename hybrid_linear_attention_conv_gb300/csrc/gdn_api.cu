@@ -541,7 +541,7 @@ int tree_verify_impl(const gdn_shape* shape, int32_t N, const int32_t* parents, 
 int tree_verify_batched_impl(const gdn_shape* shape, int32_t N, const int32_t* counts, const int32_t* parents,
                              const gdn_bf16* qkv, const gdn_bf16* x, const gdn_bf16* w, const gdn_bf16* tail,
                              bool conv, const float* alpha, const float* beta, const float* state, void* out,
-                             float q_scale, uint32_t flags, void* stream) {
+                             float q_scale, uint32_t flags, void* stream, bool kda = false) {
     int rc;
     if ((rc = check_shape(shape, false)) != GDN_OK) return rc;
     if ((rc = check_flags(flags)) != GDN_OK) return rc;
@@ -596,9 +596,11 @@ int tree_verify_batched_impl(const gdn_shape* shape, int32_t N, const int32_t* c
     p.q_scale = q_scale;
     p.normalize = (flags & GDN_NORMALIZE_QK) != 0;
     p.out_bf16 = (flags & GDN_OUT_BF16) != 0;
+    p.kda = kda;
     cudaError_t e = launch_tree(p, shape->dk, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GDN_OK
-                            : cuda_fail(e, conv ? "batched conv + tree verify launch" : "batched tree verify launch");
+                            : cuda_fail(e, kda ? "batched KDA tree verify launch"
+                                               : conv ? "batched conv + tree verify launch" : "batched tree verify launch");
 }
 
 // Commit of B sequences' paths through the batched kernel.  Fused conv when
@@ -708,6 +710,13 @@ int gdn_tree_verify_batched(const gdn_shape* shape, int32_t N, const int32_t* co
                             void* out, float q_scale, uint32_t flags, void* stream) {
     return tree_verify_batched_impl(shape, N, counts, parents, qkv, nullptr, nullptr, nullptr, false, alpha, beta,
                                     state, out, q_scale, flags, stream);
+}
+
+int gdn_kda_tree_verify_batched(const gdn_shape* shape, int32_t N, const int32_t* counts, const int32_t* parents,
+                                const gdn_bf16* qkv, const float* alpha, const float* beta, const float* state,
+                                void* out, float q_scale, uint32_t flags, void* stream) {
+    return tree_verify_batched_impl(shape, N, counts, parents, qkv, nullptr, nullptr, nullptr, false, alpha, beta,
+                                    state, out, q_scale, flags, stream, true);
 }
 
 int gdn_conv_tree_verify_batched(const gdn_shape* shape, int32_t N, const int32_t* counts, const int32_t* parents,

@@ -1089,20 +1089,15 @@ static cudaError_t launch_tree_r(TreeParamsT<MB>& p, cudaStream_t s) {
     return launch_tree_t<DK, MB, 1, KDA>(p, s);
 }
 
-// KDA: single trees only (the host refuses a joint KDA verify)
 template <int MB>
 cudaError_t launch_tree(TreeParamsT<MB>& p, int dk, cudaStream_t s) {
     if (p.kda) {
-        if constexpr (MB != 1) {
-            return cudaErrorInvalidValue;
-        } else {
-            switch (dk) {
-                case 32: return launch_tree_r<32, MB, true>(p, s);
-                case 64: return launch_tree_r<64, MB, true>(p, s);
-                case 128: return launch_tree_r<128, MB, true>(p, s);
-            }
-            return cudaErrorInvalidValue;
+        switch (dk) {
+            case 32: return launch_tree_r<32, MB, true>(p, s);
+            case 64: return launch_tree_r<64, MB, true>(p, s);
+            case 128: return launch_tree_r<128, MB, true>(p, s);
         }
+        return cudaErrorInvalidValue;
     }
     switch (dk) {
         case 32: return launch_tree_r<32, MB, false>(p, s);

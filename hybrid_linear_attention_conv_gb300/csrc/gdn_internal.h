@@ -60,7 +60,7 @@ struct TreeParamsT {
     const uint16_t* tail;  // bf16 [B, 4, C] read only
     int8_t anc[MB][GDN_MAX_TREE_NODES][3];
     int cluster;           // CTAs per thread-block cluster sharing the q/k conv (1: no cluster; set by the launcher)
-    int kda;               // a decay per key channel: alpha is [B, Nmax, Hv, dk] (single trees only)
+    int kda;               // a decay per key channel: alpha is [B, Nmax, Hv, dk]
 };
 constexpr int kMaxTreeBatch = 32;
 using TreeParams = TreeParamsT<1>;

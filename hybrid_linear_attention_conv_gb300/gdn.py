@@ -57,6 +57,7 @@ EXPORTS = [
     "gdn_commit_path",
     "gdn_commit_path_batched",
     "gdn_kda_tree_verify",
+    "gdn_kda_tree_verify_batched",
     "gdn_kda_commit_path",
     "gdn_conv_tree_verify",
     "gdn_conv_tree_verify_batched",
@@ -122,6 +123,7 @@ def load(path: str = LIB_PATH):
             "gdn_commit_path": (ctypes.c_int, [SH, I32, P, P, I32, P, P, P, P, P, P, U32, P]),
             "gdn_commit_path_batched": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, P, P, P, U32, P]),
             "gdn_kda_tree_verify": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, F, U32, P]),
+            "gdn_kda_tree_verify_batched": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, F, U32, P]),
             "gdn_kda_commit_path": (ctypes.c_int, [SH, I32, P, P, I32, P, P, P, P, P, P, U32, P]),
             "gdn_conv_tree_verify": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, P, F, U32, P]),
             "gdn_conv_tree_verify_batched": (ctypes.c_int, [SH, I32, P, P, P, P, P, P, P, P, P, F, U32, P]),
@@ -442,6 +444,26 @@ def kda_tree_verify(parents, qkv, alpha, beta, state, Hk, Hv, dk, dv, out=None, 
         _dev(out, torch.bfloat16 if out_bf16 else torch.float32, "out", (N, Hv, dv)),
         float(q_scale), _flags(normalize, out_bf16), _stream())
     _check(rc, "gdn_kda_tree_verify")
+    return out
+
+
+def kda_tree_verify_batched(counts, parents, qkv, alpha, beta, state, Hk, Hv, dk, dv, out=None, q_scale=1.0,
+                            normalize=True, out_bf16=False) -> torch.Tensor:
+    """B trees' KDA verify in one launch.  counts [B], parents [B,N] (host), qkv bf16 [B,N,C],
+    alpha fp32 [B,N,Hv,dk], beta fp32 [B,N,Hv], state fp32 [B,Hv,dv,dk] (read only) -> out [B,N,Hv,dv]."""
+    cnt, pc = _host_i32(counts, "counts")
+    par, pp = _host_i32(parents, "parents")
+    B, N = par.shape
+    if out is None:
+        out = torch.empty((B, N, Hv, dv), dtype=torch.bfloat16 if out_bf16 else torch.float32, device=qkv.device)
+    rc = load().gdn_kda_tree_verify_batched(
+        ctypes.byref(_shape(B, Hk, Hv, dk, dv)), N, pc, pp,
+        _dev(qkv, torch.bfloat16, "qkv", (B, N, packed_channels(Hk, Hv, dk, dv))),
+        _dev(alpha, torch.float32, "alpha", (B, N, Hv, dk)), _dev(beta, torch.float32, "beta", (B, N, Hv)),
+        _dev(state, torch.float32, "state", (B, Hv, dv, dk)),
+        _dev(out, torch.bfloat16 if out_bf16 else torch.float32, "out", (B, N, Hv, dv)),
+        float(q_scale), _flags(normalize, out_bf16), _stream())
+    _check(rc, "gdn_kda_tree_verify_batched")
     return out
 
 

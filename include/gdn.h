@@ -370,6 +370,20 @@ int gdn_kda_tree_verify(const gdn_shape* shape, int32_t N, const int32_t* parent
                         void* stream);
 
 /*
+ * gdn_kda_tree_verify_batched -- gdn_kda_tree_verify for B sequences in one
+ * launch (the joint verify of gdn_tree_verify_batched with the KDA step).
+ *   alpha  fp32 [B, N, Hv, dk]; every other argument as for
+ *          gdn_tree_verify_batched.
+ * Each tree's outputs equal, bit for bit, gdn_kda_tree_verify of that tree
+ * alone.  Source: "Architecture" (v0.14.2) section 8.5 (joint verify) with the
+ * KDA mixer of gdn_kda_decode_step.
+ */
+int gdn_kda_tree_verify_batched(const gdn_shape* shape, int32_t N, const int32_t* counts,
+                                const int32_t* parents, const gdn_bf16* qkv, const float* alpha,
+                                const float* beta, const float* state, void* out, float q_scale,
+                                uint32_t flags, void* stream);
+
+/*
  * gdn_kda_commit_path -- gdn_commit_path with the KDA step: replays the
  * accepted path through gdn_kda_decode_step's arithmetic in place (bit for
  * bit the KDA decode of the path's gathered inputs), and updates the conv

@@ -449,6 +449,21 @@ def test_kda_round_validation(lib):
     assert verify(par=np.array([-1, 1], np.int32)) == -3
     assert verify() == -6 and "state" in gdn.last_error()
 
+    par2 = np.array([[-1, 0, 0, 1, 3], [-1, 0, 1, -7, -7]], np.int32)
+    counts = np.array([5, 3], np.int32)
+
+    def vbatch(sh=None, alpha=FAKE, state=FAKE + 4, par=par2):
+        return lib.gdn_kda_tree_verify_batched(ctypes.byref(sh or _sh(B=2)), 5, counts.ctypes.data_as(P),
+                                               par.ctypes.data_as(P), P(FAKE), P(alpha), P(FAKE), P(state), P(FAKE),
+                                               1.0, 1, None)
+
+    assert vbatch(sh=_sh(B=33)) == -2
+    assert vbatch(alpha=None) == -1
+    bad = par2.copy()
+    bad[1, 2] = 2
+    assert vbatch(par=bad, state=FAKE) == -3
+    assert vbatch() == -6
+
     def commit(path=(0, 1, 3), state=FAKE + 4, flags=1):
         pa = np.ascontiguousarray(path, np.int32)
         return lib.gdn_kda_commit_path(ctypes.byref(_sh()), len(parents), parents.ctypes.data_as(P),

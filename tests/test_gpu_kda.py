@@ -235,3 +235,32 @@ def test_kda_commit_equals_kda_decode_every_prefix(shape):
     _, st_ref = oracle.kda_decode(d["qkv"][None, path], d["alpha"][None, path], d["beta"][None, path],
                                   d["state"][None], shape.Hk, shape.Hv, shape.dk, shape.dv)
     assert_state_close(host(st), st_ref[0])
+
+
+def test_kda_tree_verify_batched_equals_single():
+    """The joint KDA verify (trees of 32, 1, 13 and 20 nodes; capacity 32):
+    each tree equals gdn_kda_tree_verify of that tree alone, bit for bit; rows
+    past a tree's size are not written; the states are untouched."""
+    shape = gen.QWEN_27B
+    N = 32
+    trees = [gen.random_tree(160, 32, 8), np.array([-1], np.int32), gen.random_tree(161, 13, 5),
+             gen.random_tree(162, 20, 8)]
+    B = len(trees)
+    counts = np.array([len(t) for t in trees], np.int32)
+    parents = np.full((B, N), -7, np.int32)
+    for b, t in enumerate(trees):
+        parents[b, :len(t)] = t
+    d = gen.kda_inputs(163, shape.with_batch(B), N, tag="kdajoint")
+    st = f32(d["state"])
+    out = torch.full((B, N, shape.Hv, shape.dv), float("nan"), device="cuda")
+    gdn.kda_tree_verify_batched(counts, parents, bf16(d["qkv"]), f32(d["alpha"]), f32(d["beta"]), st, shape.Hk,
+                                shape.Hv, shape.dk, shape.dv, out=out)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(st), d["state"])
+    for b, t in enumerate(trees):
+        n = len(t)
+        single = gdn.kda_tree_verify(t, bf16(d["qkv"][b, :n]), f32(d["alpha"][b, :n]), f32(d["beta"][b, :n]),
+                                     f32(d["state"][b]), shape.Hk, shape.Hv, shape.dk, shape.dv)
+        torch.cuda.synchronize()
+        assert torch.equal(out[b, :n], single), f"tree {b}"
+        assert torch.isnan(out[b, n:]).all()
