@@ -6,6 +6,7 @@
 // Research Architecture On CPU").  Nothing here allocates device memory.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -129,11 +130,114 @@ int schedule_tree(int N, const int32_t* parents, TreeStep* steps, int* n_slots) 
         steps[k].node = (int8_t)n;
         steps[k].restore = (int8_t)restore;
         steps[k].save = (int8_t)save;
-        steps[k].pad = 0;
+        steps[k].store = 1;
         prev = n;
     }
     *n_slots = max_depth;
     return GDN_OK;
+}
+
+// The walk of one of two walkers: a depth-first preorder over `member` (a
+// set of nodes closed under taking parents, so a subtree holding the root),
+// writing the outputs of the nodes in `own`.  The children of a node are
+// visited in increasing order of the branch slots their own subtrees need,
+// so that the parent's slot is released before the most demanding child
+// (the fewest slots any preorder can use); slots are numbered from `base`.
+// Returns the steps taken; *n_slots gets the slots used.
+int schedule_walker(int N, const int32_t* parents, const char* member, const char* own, int base, TreeStep* steps,
+                    int* n_slots) {
+    // children lists in fixed arrays (N <= GDN_MAX_TREE_NODES): kids[n][0 .. nk[n])
+    int8_t kids[GDN_MAX_TREE_NODES][GDN_MAX_TREE_NODES];
+    int nk[GDN_MAX_TREE_NODES] = {};
+    for (int i = 1; i < N; ++i)
+        if (member[i]) kids[parents[i]][nk[parents[i]]++] = (int8_t)i;
+    // slots a subtree needs (children in increasing order of need): the
+    // parent's slot is held through every child but the last
+    int need[GDN_MAX_TREE_NODES] = {};
+    for (int n = N - 1; n >= 0; --n) {  // children have larger indices than their parent
+        if (!member[n]) continue;
+        int8_t* c = kids[n];
+        for (int a = 1; a < nk[n]; ++a)  // stable insertion sort by need
+            for (int b = a; b > 0 && need[c[b - 1]] > need[c[b]]; --b) std::swap(c[b - 1], c[b]);
+        if (nk[n] == 1) need[n] = need[c[0]];
+        else if (nk[n] >= 2) need[n] = std::max(need[c[nk[n] - 1]], need[c[nk[n] - 2]] + 1);
+    }
+    int slot_of[GDN_MAX_TREE_NODES];
+    int stack[GDN_MAX_TREE_NODES];
+    int sp = 0, k = 0, depth = 0, max_depth = 0, prev = -1;
+    stack[sp++] = 0;
+    while (sp > 0) {
+        const int n = stack[--sp];
+        for (int c = nk[n] - 1; c >= 0; --c) stack[sp++] = kids[n][c];
+        slot_of[n] = -1;
+        int restore = -1;
+        if (n != 0) {
+            const int par = parents[n];
+            if (prev != par) restore = slot_of[par];
+            if (slot_of[par] >= 0 && n == kids[par][nk[par] - 1]) depth -= 1;  // the last child frees the slot
+        }
+        int save = -1;
+        if (nk[n] >= 2) {
+            save = base + depth++;
+            slot_of[n] = save;
+            max_depth = std::max(max_depth, depth);
+        }
+        steps[k].node = (int8_t)n;
+        steps[k].restore = (int8_t)restore;
+        steps[k].save = (int8_t)save;
+        steps[k].store = own[n] ? 1 : 0;
+        prev = n;
+        ++k;
+    }
+    *n_slots = max_depth;
+    return k;
+}
+
+// Two walkers for one tree: the preorder (children by slot need) cut in two
+// at the point that minimises the longer walk.  Walker 0 takes the nodes
+// before the cut (a set closed under parents); walker 1 the nodes from the
+// cut on, replaying their ancestors before the cut without storing them.
+// Each node's output is written by exactly one walker, with the arithmetic
+// and operand order of the single walk, so the bits are the same.  Left at
+// walkers = 1 when the longer walk would not be at least a quarter shorter
+// than the single one (chains, small trees).
+void split_walkers(int N, const int32_t* parents, TreeParams& p) {
+    p.walkers = 1;
+    if (N < 8) return;
+    char all[GDN_MAX_TREE_NODES];
+    memset(all, 1, sizeof all);
+    TreeStep order_steps[GDN_MAX_TREE_NODES];
+    int slots = 0;
+    schedule_walker(N, parents, all, all, 0, order_steps, &slots);
+    int order[GDN_MAX_TREE_NODES];
+    for (int k = 0; k < N; ++k) order[k] = order_steps[k].node;
+    // walker 1's walk for cut k: the nodes from k on and their ancestors, a
+    // set that grows as k moves down (one pass from the end of the preorder)
+    int best_k = -1, best_len = N, len = 0;
+    char m[GDN_MAX_TREE_NODES] = {};
+    for (int k = N - 1; k >= 1; --k) {
+        for (int a = order[k]; a >= 0 && !m[a]; a = parents[a]) {
+            m[a] = 1;
+            ++len;
+        }
+        const int longer = std::max(k, len);
+        if (longer < best_len) {
+            best_len = longer;
+            best_k = k;
+        }
+    }
+    if (best_k < 0 || 4 * best_len > 3 * N) return;
+    char m0[GDN_MAX_TREE_NODES] = {}, m1[GDN_MAX_TREE_NODES] = {}, own1[GDN_MAX_TREE_NODES] = {};
+    for (int j = 0; j < best_k; ++j) m0[order[j]] = 1;
+    for (int j = best_k; j < N; ++j) {
+        own1[order[j]] = 1;
+        for (int a = order[j]; a >= 0 && !m1[a]; a = parents[a]) m1[a] = 1;
+    }
+    int s0 = 0, s1 = 0;
+    p.walk_n[0] = schedule_walker(N, parents, m0, m0, 0, p.walk[0], &s0);
+    p.walk_n[1] = schedule_walker(N, parents, m1, own1, s0, p.walk[1], &s1);
+    p.walk_slots = s0 + s1;
+    p.walkers = 2;
 }
 
 int check_path(int N, const int32_t* parents, const int32_t* path, int L) {
@@ -509,6 +613,7 @@ int tree_verify_impl(const gdn_shape* shape, int32_t N, const int32_t* parents, 
         return rc;
     TreeParams p{};
     if ((rc = schedule_tree(N, parents, p.steps[0], &p.n_slots)) != GDN_OK) return rc;
+    split_walkers(N, parents, p);
     p.qkv = qkv;
     if (conv) {
         p.x = x;

@@ -347,10 +347,11 @@ __host__ __device__ constexpr size_t tree_kq_bytes(int N) {
     return (size_t)N * (8 * 2 * (DK / 32) * 4 * 4 + 16);
 }
 
-template <int DK, int R>
+template <int DK, int R, int G>
 __host__ __device__ constexpr size_t tree_stage_bytes(int N) {
-    // per node: the record, v, alpha/beta, the schedule step and (fused conv) its 3 ancestors + pad
-    return tree_kq_bytes<DK>(N) + (size_t)N * (kRowsPerPass * R * 2 + 2 * 4 + sizeof(TreeStep) + 4);
+    // per node: the record, v, alpha/beta, each walker's schedule step and
+    // (fused conv) its 3 ancestors + pad
+    return tree_kq_bytes<DK>(N) + (size_t)N * (kRowsPerPass * R * 2 + 2 * 4 + G * sizeof(TreeStep) + 4);
 }
 
 // The region in front of the staging: the walk's branch slots, which the
@@ -380,11 +381,17 @@ __host__ __device__ constexpr size_t tree_slot_bytes(int n_slots, int N, bool co
 // the other inputs, [N][dk] fp32; each step applies kda_decay and the delta
 // step of the KDA decode, so a node's output is the bits of gdn_kda_decode_step
 // over its root path.
-template <int DK, int MB, int R, bool KDA>
-__global__ void __launch_bounds__(kThreads)
+// G walkers: G groups of 256 threads, each holding all of the CTA's rows and
+// walking its own part of the tree (walk[g]; G = 2 for one tree, when the
+// split shortens the longer walk).  Each walk is a dependent chain of node
+// steps, so two half-length chains on one SM finish in about the time of one;
+// both walkers share the staged inputs and the per-node records.
+template <int DK, int MB, int R, bool KDA, int G>
+__global__ void __launch_bounds__(kThreads * G)
 gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     constexpr int V = DK / 32;
     constexpr int ROWS = kRowsPerPass * R;  // rows of one value head per CTA
+    constexpr int NT = kThreads * G;        // threads of the CTA
     const int tree = blockIdx.z;          // sequence b: its own tree and state
     const int N = p.N[tree];
     const uint16_t* qkv = p.qkv + (size_t)tree * p.Nmax * p.C;
@@ -393,19 +400,20 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     const bool conv = p.x != nullptr;  // pre-conv inputs: the tree conv runs here
     extern __shared__ float4 smem4[];
     float4* slots = smem4;  // [n_slots][R][32 row groups][V][8 lanes]
-    uint8_t* stage = reinterpret_cast<uint8_t*>(smem4) + tree_slot_bytes<DK, R>(p.n_slots, p.Nmax, conv);
+    uint8_t* stage = reinterpret_cast<uint8_t*>(smem4) + tree_slot_bytes<DK, R>(G == 1 ? p.n_slots : p.walk_slots,
+                                                                                   p.Nmax, conv);
     float4* s_kq = reinterpret_cast<float4*>(stage);                                   // per-node records
     uint16_t* s_v = reinterpret_cast<uint16_t*>(stage + tree_kq_bytes<DK>(p.Nmax));        // [N][32 R]
     float* s_ab = reinterpret_cast<float*>(s_v + (size_t)p.Nmax * ROWS);                    // [N][alpha, beta]
-    // the walk's schedule, copied out of the parameter block (read once per
-    // step on the walk's dependent chain)
+    // the walks' schedules, walker g's at steps + g Nmax (staged below)
     TreeStep* steps = reinterpret_cast<TreeStep*>(s_ab + 2 * (size_t)p.Nmax);
     // the fused conv's ancestor table, [N] x (3 ancestors + pad), copied out of the parameters
-    char4* s_anc = reinterpret_cast<char4*>(steps + p.Nmax);
+    char4* s_anc = reinterpret_cast<char4*>(steps + G * p.Nmax);
     // KDA: the nodes' decay vectors for head h, [N][DK / 4] float4, after the staging
-    float4* s_gate = reinterpret_cast<float4*>(stage + tree_stage_bytes<DK, R>(p.Nmax));
+    float4* s_gate = reinterpret_cast<float4*>(stage + tree_stage_bytes<DK, R, G>(p.Nmax));
     const int lane8 = threadIdx.x & 7;
-    const int rg = threadIdx.x >> 3;
+    const int walker = G == 1 ? 0 : (int)threadIdx.x / kThreads;
+    const int rg = (threadIdx.x % kThreads) >> 3;  // row group within the walker
     const int h = blockIdx.y;
     const int g = h / p.group;
     const int row0 = blockIdx.x * ROWS;
@@ -422,6 +430,19 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
 #pragma unroll
         for (int m = 0; m < V; ++m)
             s[r][m] = __ldg(reinterpret_cast<const float4*>(S + (size_t)kRowsPerPass * r * DK + 32 * m + 4 * lane8));
+
+    // the walks' schedules, copied out of the parameter block (read once per
+    // step on the walk's dependent chain)
+    auto stage_steps = [&] {
+        if constexpr (G == 1) {
+            for (int n = threadIdx.x; n < N; n += NT) steps[n] = p.steps[tree][n];
+        } else {
+            for (int i = threadIdx.x; i < G * p.Nmax; i += NT) {
+                const int g = i / p.Nmax, k = i % p.Nmax;
+                if (k < p.walk_n[g]) steps[i] = p.walk[MB == 1 ? g : 0][MB == 1 ? k : 0];
+            }
+        }
+    };
 
     // conv: node n's q and k of key head g, [N][2 DK] bf16, in the slot region
     uint16_t* y_qk = reinterpret_cast<uint16_t*>(smem4);
@@ -443,32 +464,31 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
                  : c < QK8    ? p.Hk * DK + g * DK + 8 * (c - DK / 8)
                               : 2 * p.Hk * DK + h * p.dv + row0 + 8 * (c - QK8);
         };
-        for (int idx = threadIdx.x; idx < (N + 3) * PER; idx += kThreads) {
+        for (int idx = threadIdx.x; idx < (N + 3) * PER; idx += NT) {
             const int r = idx / PER, c = idx % PER;
             const uint16_t* src = r < 3 ? tb + (size_t)(r + 1) * p.C + chan(c) : xb + (size_t)(r - 3) * p.C + chan(c);
             cp_async16(xs + (size_t)r * CW + 8 * c, src);
         }
-        for (int idx = threadIdx.x; idx < PER * 4; idx += kThreads) {  // 8 channels x 4 taps = 4 x 16 bytes
+        for (int idx = threadIdx.x; idx < PER * 4; idx += NT) {  // 8 channels x 4 taps = 4 x 16 bytes
             const int c = idx >> 2, q = idx & 3;
             cp_async16(ws + (size_t)c * 32 + 8 * q, p.w + (size_t)chan(c) * GDN_CONV_W + 8 * q);
         }
         // the gates too, in the same round trip (after the conv they would cost another);
         // and the per-node tables read with a per-node index out of the
         // parameters (constant-cache misses), while the copies are in flight
-        for (int n = threadIdx.x; n < N; n += kThreads) {
+        for (int n = threadIdx.x; n < N; n += NT) {
             if (!KDA) cp_async4(s_ab + 2 * n, alpha_b + (size_t)n * p.Hv + h);
             cp_async4(s_ab + 2 * n + 1, beta_b + (size_t)n * p.Hv + h);
         }
         if constexpr (KDA) {
-            for (int idx = threadIdx.x; idx < N * (DK / 4); idx += kThreads) {
+            for (int idx = threadIdx.x; idx < N * (DK / 4); idx += NT) {
                 const int n = idx / (DK / 4), c4 = idx % (DK / 4);
                 cp_async16(s_gate + idx, p.alpha + (((size_t)tree * p.Nmax + n) * p.Hv + h) * DK + 4 * c4);
             }
         }
-        for (int n = threadIdx.x; n < N; n += kThreads) {
-            steps[n] = p.steps[tree][n];
+        for (int n = threadIdx.x; n < N; n += NT)
             s_anc[n] = make_char4(p.anc[tree][n][0], p.anc[tree][n][1], p.anc[tree][n][2], 0);
-        }
+        stage_steps();
         asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
         // With a cluster (the CTAs of one key head: its value heads' row
         // blocks), the q/k outputs are computed once per cluster: task j goes
@@ -495,7 +515,7 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
             return conv8_bf16(w, u0, u1, u2, u3);
         };
         const int n_qk = N * QK8;  // q/k tasks of the tree
-        for (int t = threadIdx.x; t * csize + (int)rank < n_qk; t += kThreads) {
+        for (int t = threadIdx.x; t * csize + (int)rank < n_qk; t += NT) {
             const int j = t * csize + (int)rank;
             const int n = j / QK8, c = j % QK8;
             const uint4 y = conv_task(n, c);
@@ -506,7 +526,7 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
                 *reinterpret_cast<uint4*>(dst) = y;
             }
         }
-        for (int idx = threadIdx.x; idx < N * (ROWS / 8); idx += kThreads) {
+        for (int idx = threadIdx.x; idx < N * (ROWS / 8); idx += NT) {
             const int n = idx / (ROWS / 8), c = idx % (ROWS / 8);
             *reinterpret_cast<uint4*>(s_v + (size_t)n * ROWS + 8 * c) = conv_task(n, QK8 + c);
         }
@@ -514,26 +534,26 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
         // a CTA may leave the cluster only after this point)
         if (csize > 1) cluster_sync_all();
     } else {
-        for (int idx = threadIdx.x; idx < N * (ROWS / 8); idx += kThreads) {
+        for (int idx = threadIdx.x; idx < N * (ROWS / 8); idx += NT) {
             const int n = idx / (ROWS / 8), c = idx % (ROWS / 8);
             const uint16_t* src = qkv + (size_t)n * p.C + (size_t)2 * p.Hk * DK + (size_t)h * p.dv + row0 + c * 8;
             *reinterpret_cast<uint4*>(s_v + (size_t)n * ROWS + c * 8) = __ldg(reinterpret_cast<const uint4*>(src));
         }
     }
     if (!conv) {  // (the fused conv staged these with its inputs)
-        for (int n = threadIdx.x; n < N; n += kThreads) {
+        for (int n = threadIdx.x; n < N; n += NT) {
             if (!KDA) s_ab[2 * n] = alpha_b[(size_t)n * p.Hv + h];
             s_ab[2 * n + 1] = beta_b[(size_t)n * p.Hv + h];
-            steps[n] = p.steps[tree][n];
         }
         if constexpr (KDA) {
-            for (int idx = threadIdx.x; idx < N * (DK / 4); idx += kThreads) {
+            for (int idx = threadIdx.x; idx < N * (DK / 4); idx += NT) {
                 const int n = idx / (DK / 4), c4 = idx % (DK / 4);
                 s_gate[idx] = __ldg(reinterpret_cast<const float4*>(
                     p.alpha + (((size_t)tree * p.Nmax + n) * p.Hv + h) * DK + 4 * c4));
             }
         }
     }
+    if (!conv) stage_steps();
     __syncthreads();
 
     const bool normalize = p.normalize != 0;
@@ -544,8 +564,9 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     // token_kq reduces with full-warp shuffles, so the loop is warp-uniform:
     // all four row groups of a warp iterate together (on a clamped node when
     // they run past N) and only the groups with a real node write.
-    for (int n0 = rg & ~3; n0 < N; n0 += kRowsPerPass) {
-        const int n = n0 + (rg & 3);
+    const int rgc = threadIdx.x >> 3;  // row group within the CTA
+    for (int n0 = rgc & ~3; n0 < N; n0 += NT / 8) {
+        const int n = n0 + (rgc & 3);
         const bool real = n < N;
         TokenKQ<V> t;
         const int nc = real ? n : N - 1;
@@ -584,8 +605,10 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     auto slot_at = [&](int slot, int r, int m) -> float4& {
         return slots[(((slot * R + r) * kRowsPerPass + rg) * V + m) * 8 + lane8];
     };
+    const TreeStep* my_steps = steps + walker * p.Nmax;
+    const int NS = G == 1 ? N : p.walk_n[walker];  // steps of this walker
     auto walk_step = [&](int step, const TokenKQ<V>& cur, TokenKQ<V>& nxt) {
-        const TreeStep st = steps[step];
+        const TreeStep st = my_steps[step];
         if (st.restore >= 0) {
 #pragma unroll
             for (int r = 0; r < R; ++r)
@@ -593,7 +616,7 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
                 for (int m = 0; m < V; ++m) s[r][m] = slot_at(st.restore, r, m);
         }
         const int node = st.node;
-        if (step + 1 < N) fetch(steps[step + 1].node, nxt);
+        if (step + 1 < NS) fetch(my_steps[step + 1].node, nxt);
         const float beta = s_ab[2 * node + 1];
         float o[R];
         if constexpr (KDA) {
@@ -619,7 +642,7 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
 #pragma unroll
         for (int r = 1; r < R; ++r)
             if (lane8 == r) my_o = o[r];
-        if (lane8 < R)
+        if (lane8 < R && st.store)
             store_out(p.out, (((size_t)tree * p.Nmax + node) * p.Hv + h) * p.dv + row + kRowsPerPass * lane8, my_o,
                       out_bf16);
         if (st.save >= 0) {
@@ -630,10 +653,10 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
         }
     };
     TokenKQ<V> ka, kb;
-    fetch(steps[0].node, ka);
-    for (int step = 0; step < N; step += 2) {
+    fetch(my_steps[0].node, ka);
+    for (int step = 0; step < NS; step += 2) {
         walk_step(step, ka, kb);
-        if (step + 1 < N) walk_step(step + 1, kb, ka);
+        if (step + 1 < NS) walk_step(step + 1, kb, ka);
     }
 }
 
@@ -1028,15 +1051,15 @@ cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int g
                : launch_decode_k<false, false>(p, dk, rows_per_cta, s);
 }
 
-template <int DK, int R>
+template <int DK, int R, int G = 1>
 static size_t tree_smem_bytes(int n_slots, int N, bool conv, bool kda) {
-    return tree_slot_bytes<DK, R>(n_slots, N, conv) + tree_stage_bytes<DK, R>(N) + (kda ? (size_t)N * DK * 4 : 0);
+    return tree_slot_bytes<DK, R>(n_slots, N, conv) + tree_stage_bytes<DK, R, G>(N) + (kda ? (size_t)N * DK * 4 : 0);
 }
 
-template <int DK, int MB, int R, bool KDA>
+template <int DK, int MB, int R, bool KDA, int G = 1>
 static cudaError_t launch_tree_t(TreeParamsT<MB>& p, cudaStream_t s) {
     constexpr int ROWS = kRowsPerPass * R;
-    const size_t smem = tree_smem_bytes<DK, R>(p.n_slots, p.Nmax, p.x != nullptr, KDA);
+    const size_t smem = tree_smem_bytes<DK, R, G>(G == 1 ? p.n_slots : p.walk_slots, p.Nmax, p.x != nullptr, KDA);
     // the shared-memory opt-in, once per device whatever the host threads
     static std::once_flag once[64];
     static cudaError_t setup_err[64];
@@ -1045,9 +1068,9 @@ static cudaError_t launch_tree_t(TreeParamsT<MB>& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::call_once(once[dev], [dev] {
-        const int max_smem = std::min((int)tree_smem_bytes<DK, R>(GDN_MAX_TREE_SLOTS, GDN_MAX_TREE_NODES, true, KDA),
-                                      kMaxSmemPerCta);
-        setup_err[dev] = cudaFuncSetAttribute(gdn_tree_kernel<DK, MB, R, KDA>,
+        const int max_smem = std::min(
+            (int)tree_smem_bytes<DK, R, G>(G * GDN_MAX_TREE_SLOTS, GDN_MAX_TREE_NODES, true, KDA), kMaxSmemPerCta);
+        setup_err[dev] = cudaFuncSetAttribute(gdn_tree_kernel<DK, MB, R, KDA, G>,
                                               cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     });
     if (setup_err[dev] != cudaSuccess) return setup_err[dev];
@@ -1061,7 +1084,7 @@ static cudaError_t launch_tree_t(TreeParamsT<MB>& p, cudaStream_t s) {
         p.cluster = csize;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;
-        cfg.blockDim = dim3(kThreads);
+        cfg.blockDim = dim3(kThreads * G);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = s;
         cudaLaunchAttribute attr[1];
@@ -1071,19 +1094,29 @@ static cudaError_t launch_tree_t(TreeParamsT<MB>& p, cudaStream_t s) {
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, gdn_tree_kernel<DK, MB, R, KDA>, p) == cudaSuccess) return cudaSuccess;
+        if (cudaLaunchKernelEx(&cfg, gdn_tree_kernel<DK, MB, R, KDA, G>, p) == cudaSuccess) return cudaSuccess;
         (void)cudaGetLastError();  // a configuration error, not sticky: take the plain launch
     }
     p.cluster = 1;
-    gdn_tree_kernel<DK, MB, R, KDA><<<grid, kThreads, smem, s>>>(p);
+    gdn_tree_kernel<DK, MB, R, KDA, G><<<grid, kThreads * G, smem, s>>>(p);
     return cudaGetLastError();
 }
 
 // Rows per thread: 2 when the value head has a multiple of 64 rows and the
 // slots for them fit in shared memory (each node's record then serves two
 // rows per fetch), else 1.
+// Two walkers (one tree, the scalar-gated step): when the host split the
+// tree, the value head has a multiple of 64 rows, both walkers' slots fit,
+// and the grid leaves every CTA an SM of its own (a 512-thread CTA of this
+// kernel takes most of an SM's registers).
 template <int DK, int MB, bool KDA>
 static cudaError_t launch_tree_r(TreeParamsT<MB>& p, cudaStream_t s) {
+    if constexpr (MB == 1 && !KDA) {
+        if (p.walkers == 2 && p.dv % (2 * kRowsPerPass) == 0 &&
+            (p.dv / (2 * kRowsPerPass)) * p.Hv <= device_sm_count() &&
+            tree_smem_bytes<DK, 2, 2>(p.walk_slots, p.Nmax, p.x != nullptr, false) <= (size_t)kMaxSmemPerCta)
+            return launch_tree_t<DK, MB, 2, false, 2>(p, s);
+    }
     const size_t smem2 = tree_smem_bytes<DK, 2>(p.n_slots, p.Nmax, p.x != nullptr, KDA);
     if (p.dv % (2 * kRowsPerPass) == 0 && smem2 <= (size_t)kMaxSmemPerCta) return launch_tree_t<DK, MB, 2, KDA>(p, s);
     return launch_tree_t<DK, MB, 1, KDA>(p, s);

@@ -35,7 +35,8 @@ struct TreeStep {
     int8_t node;      // node processed at this step
     int8_t restore;   // slot holding the parent's state, or -1 (registers)
     int8_t save;      // slot to keep this node's state in, or -1
-    int8_t pad;
+    int8_t store;     // 1: write the node's output; 0: an ancestor replayed
+                      // by the second walker, whose output the first writes
 };
 
 // Tree verify over up to MB trees (one per sequence) in one launch.
@@ -61,6 +62,14 @@ struct TreeParamsT {
     int8_t anc[MB][GDN_MAX_TREE_NODES][3];
     int cluster;           // CTAs per thread-block cluster sharing the q/k conv (1: no cluster; set by the launcher)
     int kda;               // a decay per key channel: alpha is [B, Nmax, Hv, dk]
+    // Two walkers per CTA (one tree, walkers == 2): the tree's preorder split
+    // in two, walker g running walk[g][0 .. walk_n[g] - 1] over the same rows
+    // with its own branch slots (walk_slots in all).  The launcher takes this
+    // schedule instead of steps[0] when the second walker fits.
+    TreeStep walk[MB == 1 ? 2 : 1][MB == 1 ? GDN_MAX_TREE_NODES : 1];
+    int walk_n[2];
+    int walk_slots;
+    int walkers;           // 2 when walk[] holds a split schedule, else 1
 };
 constexpr int kMaxTreeBatch = 32;
 using TreeParams = TreeParamsT<1>;

@@ -89,15 +89,43 @@ def _caterpillar(n):
 @pytest.mark.parametrize("parents", [_binary_tree(63), _caterpillar(17), gen.random_tree(11, 64, 8),
                                      gen.random_tree(12, 48, 12), gen.random_tree(13, 64, 4)])
 def test_tree_walk_shapes_equal_decode_bitwise(parents):
-    """Whatever walk the host schedules (two nodes per step where the tree
-    allows, else the depth-first walk), every node's output is the bits of
-    the linear decode of its root path."""
+    """Whatever walk the host schedules (the tree split between two walkers
+    where that shortens the walk and their branch states fit, else one
+    depth-first walk), every node's output is the bits of the linear decode
+    of its root path."""
     shape = gen.QWEN_27B
     _, d = _tree_case(shape, len(parents), 5, parents=parents)
     out = _verify(shape, parents, d)
     for n in range(len(parents)):
         o, _ = _path_decode(shape, d, gdn.tree_root_path(parents, n))
         assert torch.equal(out[n], o[-1]), f"node {n}"
+
+
+@pytest.mark.parametrize("parents", [gen.random_tree(1234, 32, 8), gen.random_tree(0, 32, 8), _caterpillar(17),
+                                     gen.random_tree(12, 48, 12), gen.random_tree(3, 8, 8), _binary_tree(63),
+                                     np.arange(-1, 31, dtype=np.int32)])
+def test_two_walkers_equal_one_walker_bitwise(parents):
+    """A single tree's verify splits the tree between two walkers when that
+    shortens the walk; the joint verify (one tree here) always walks it
+    whole.  Both give the same bits, with post-conv and pre-conv inputs."""
+    shape = gen.QWEN_27B
+    N = len(parents)
+    _, d = _tree_case(shape, N, 21, parents=parents)
+    out = _verify(shape, parents, d)
+    joint = gdn.tree_verify_batched(np.array([N], np.int32), parents[None], bf16(d["qkv"][None]),
+                                    f32(d["alpha"][None]), f32(d["beta"][None]), f32(d["state"][None]),
+                                    shape.Hk, shape.Hv, shape.dk, shape.dv)
+    torch.cuda.synchronize()
+    assert torch.equal(out, joint[0])
+    c = gen.conv_inputs(22, 1, N, shape.C, tag="walkers")
+    w = bf16(c["w"])
+    fused = gdn.conv_tree_verify(parents, bf16(c["x"][0]), w, bf16(c["tail"][0]), f32(d["alpha"]),
+                                 f32(d["beta"]), f32(d["state"]), shape.Hk, shape.Hv, shape.dk, shape.dv)
+    fused_joint = gdn.conv_tree_verify_batched(np.array([N], np.int32), parents[None], bf16(c["x"]), w,
+                                               bf16(c["tail"]), f32(d["alpha"][None]), f32(d["beta"][None]),
+                                               f32(d["state"][None]), shape.Hk, shape.Hv, shape.dk, shape.dv)
+    torch.cuda.synchronize()
+    assert torch.equal(fused, fused_joint[0])
 
 
 @pytest.mark.parametrize("parents", [
