@@ -193,17 +193,19 @@ int schedule_walker(int N, const int32_t* parents, const char* member, const cha
     return k;
 }
 
-// Two walkers for one tree: the preorder (children by slot need) cut in two
-// at the point that minimises the longer walk.  Walker 0 takes the nodes
-// before the cut (a set closed under parents); walker 1 the nodes from the
-// cut on, replaying their ancestors before the cut without storing them.
-// Each node's output is written by exactly one walker, with the arithmetic
-// and operand order of the single walk, so the bits are the same.  Left at
-// walkers = 1 when the longer walk would not be at least a quarter shorter
-// than the single one (chains, small trees).
-void split_walkers(int N, const int32_t* parents, TreeParams& p) {
+// Walkers for one tree: the preorder (children by slot need) cut into P
+// contiguous ranges, walker w taking range w and replaying, without storing
+// them, the ancestors of its nodes that lie before the range.  Each node's
+// output is written by exactly one walker, with the arithmetic and operand
+// order of the single walk, so the bits are the same.  The cuts minimise the
+// longest walk: for a bound L, ranges taken greedily as long as their walks
+// stay within L (a walk only grows as its range does) cover the tree iff any
+// cuts do, and L rises from N / P until they do.  Left at walkers = 1 when
+// the longest walk would not be at least a quarter shorter than the single
+// walk (chains, small trees).
+void split_walkers(int N, const int32_t* parents, int P, TreeParams& p) {
     p.walkers = 1;
-    if (N < 8) return;
+    if (P < 2 || N < 8) return;
     char all[GDN_MAX_TREE_NODES];
     memset(all, 1, sizeof all);
     TreeStep order_steps[GDN_MAX_TREE_NODES];
@@ -211,33 +213,47 @@ void split_walkers(int N, const int32_t* parents, TreeParams& p) {
     schedule_walker(N, parents, all, all, 0, order_steps, &slots);
     int order[GDN_MAX_TREE_NODES];
     for (int k = 0; k < N; ++k) order[k] = order_steps[k].node;
-    // walker 1's walk for cut k: the nodes from k on and their ancestors, a
-    // set that grows as k moves down (one pass from the end of the preorder)
-    int best_k = -1, best_len = N, len = 0;
-    char m[GDN_MAX_TREE_NODES] = {};
-    for (int k = N - 1; k >= 1; --k) {
-        for (int a = order[k]; a >= 0 && !m[a]; a = parents[a]) {
-            m[a] = 1;
-            ++len;
+    // a walk is at least as long as its deepest node's root path
+    int depth[GDN_MAX_TREE_NODES], max_depth = 1;
+    depth[0] = 1;
+    for (int n = 1; n < N; ++n) max_depth = std::max(max_depth, depth[n] = depth[parents[n]] + 1);
+    int cut[kMaxWalkers + 1] = {};
+    int best = N;
+    for (int L = std::max((N + P - 1) / P, max_depth); 4 * L <= 3 * N; ++L) {
+        int k = 0, w = 0;
+        for (; w < P && k < N; ++w) {
+            char m[GDN_MAX_TREE_NODES] = {};
+            int len = 0;
+            cut[w] = k;
+            for (; k < N; ++k) {
+                int add = 0;
+                for (int a = order[k]; a >= 0 && !m[a]; a = parents[a]) ++add;
+                if (len + add > L) break;
+                for (int a = order[k]; a >= 0 && !m[a]; a = parents[a]) m[a] = 1;
+                len += add;
+            }
         }
-        const int longer = std::max(k, len);
-        if (longer < best_len) {
-            best_len = longer;
-            best_k = k;
+        if (k == N) {
+            best = L;
+            P = w;  // the walkers the cuts use
+            cut[P] = N;
+            break;
         }
     }
-    if (best_k < 0 || 4 * best_len > 3 * N) return;
-    char m0[GDN_MAX_TREE_NODES] = {}, m1[GDN_MAX_TREE_NODES] = {}, own1[GDN_MAX_TREE_NODES] = {};
-    for (int j = 0; j < best_k; ++j) m0[order[j]] = 1;
-    for (int j = best_k; j < N; ++j) {
-        own1[order[j]] = 1;
-        for (int a = order[j]; a >= 0 && !m1[a]; a = parents[a]) m1[a] = 1;
+    if (P < 2 || 4 * best > 3 * N) return;
+    int s_max = 0;
+    for (int w = 0; w < P; ++w) {
+        char mw[GDN_MAX_TREE_NODES] = {}, own[GDN_MAX_TREE_NODES] = {};
+        for (int j = cut[w]; j < cut[w + 1]; ++j) {
+            own[order[j]] = 1;
+            for (int a = order[j]; a >= 0 && !mw[a]; a = parents[a]) mw[a] = 1;
+        }
+        int sw = 0;
+        p.walk_n[w] = schedule_walker(N, parents, mw, own, 0, p.walk[w], &sw);
+        s_max = std::max(s_max, sw);
     }
-    int s0 = 0, s1 = 0;
-    p.walk_n[0] = schedule_walker(N, parents, m0, m0, 0, p.walk[0], &s0);
-    p.walk_n[1] = schedule_walker(N, parents, m1, own1, s0, p.walk[1], &s1);
-    p.walk_slots = s0 + s1;
-    p.walkers = 2;
+    p.walk_slots = s_max;
+    p.walkers = P;
 }
 
 int check_path(int N, const int32_t* parents, const int32_t* path, int L) {
@@ -613,7 +629,11 @@ int tree_verify_impl(const gdn_shape* shape, int32_t N, const int32_t* parents, 
         return rc;
     TreeParams p{};
     if ((rc = schedule_tree(N, parents, p.steps[0], &p.n_slots)) != GDN_OK) return rc;
-    split_walkers(N, parents, p);
+    // As many walkers (up to kMaxWalkers) as keep the grid -- walkers x row
+    // blocks of 64 x value heads -- within two CTAs per SM.
+    int walkers = kMaxWalkers;
+    while (walkers > 1 && (long)walkers * (shape->dv / 64) * shape->Hv > 2L * sm_count()) --walkers;
+    split_walkers(N, parents, walkers, p);
     p.qkv = qkv;
     if (conv) {
         p.x = x;

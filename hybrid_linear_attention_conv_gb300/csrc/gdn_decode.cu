@@ -32,6 +32,7 @@ namespace gdn {
 constexpr int kThreads = 256;        // 8 warps = 32 row groups of 8 lanes
 constexpr int kRowsPerPass = 32;
 constexpr int kMaxSmemPerCta = 232448;  // the opt-in shared memory of one CTA (227 KB)
+constexpr size_t kSmemTwoCtas = 233472 / 2 - 1024;  // two CTAs on one SM (228 KB, 1 KB reserved per CTA)
 
 // Fused step (plain and KDA), several value heads per CTA: each thread copies
 // its rows of the next head's state into shared memory (cp.async, its own
@@ -347,11 +348,10 @@ __host__ __device__ constexpr size_t tree_kq_bytes(int N) {
     return (size_t)N * (8 * 2 * (DK / 32) * 4 * 4 + 16);
 }
 
-template <int DK, int R, int G>
+template <int DK, int R>
 __host__ __device__ constexpr size_t tree_stage_bytes(int N) {
-    // per node: the record, v, alpha/beta, each walker's schedule step and
-    // (fused conv) its 3 ancestors + pad
-    return tree_kq_bytes<DK>(N) + (size_t)N * (kRowsPerPass * R * 2 + 2 * 4 + G * sizeof(TreeStep) + 4);
+    // per node: the record, v, alpha/beta, the schedule step and (fused conv) its 3 ancestors + pad
+    return tree_kq_bytes<DK>(N) + (size_t)N * (kRowsPerPass * R * 2 + 2 * 4 + sizeof(TreeStep) + 4);
 }
 
 // The region in front of the staging: the walk's branch slots, which the
@@ -381,18 +381,19 @@ __host__ __device__ constexpr size_t tree_slot_bytes(int n_slots, int N, bool co
 // the other inputs, [N][dk] fp32; each step applies kda_decay and the delta
 // step of the KDA decode, so a node's output is the bits of gdn_kda_decode_step
 // over its root path.
-// G walkers: G groups of 256 threads, each holding all of the CTA's rows and
-// walking its own part of the tree (walk[g]; G = 2 for one tree, when the
-// split shortens the longer walk).  Each walk is a dependent chain of node
-// steps, so two half-length chains on one SM finish in about the time of one;
-// both walkers share the staged inputs and the per-node records.
-template <int DK, int MB, int R, bool KDA, int G>
-__global__ void __launch_bounds__(kThreads * G)
+// Walkers: with p.walkers = W > 1 (one tree), W CTAs hold the same rows and
+// each walks its own part of the tree (walk[w]), the host having cut the
+// tree's preorder into W ranges.  Each walk is a dependent chain of node
+// steps, so W shorter chains in parallel (two CTAs to an SM) end sooner than
+// one long one; every CTA stages the inputs and records it reads.
+template <int DK, int MB, int R, bool KDA>
+__global__ void __launch_bounds__(kThreads, 2)
 gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     constexpr int V = DK / 32;
     constexpr int ROWS = kRowsPerPass * R;  // rows of one value head per CTA
-    constexpr int NT = kThreads * G;        // threads of the CTA
-    const int tree = blockIdx.z;          // sequence b: its own tree and state
+    constexpr int NT = kThreads;
+    // z: the sequence b (its own tree and state), or with one tree the walker
+    const int tree = MB == 1 ? 0 : (int)blockIdx.z;
     const int N = p.N[tree];
     const uint16_t* qkv = p.qkv + (size_t)tree * p.Nmax * p.C;
     const float* alpha_b = p.alpha + (size_t)tree * p.Nmax * p.Hv;
@@ -400,20 +401,21 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     const bool conv = p.x != nullptr;  // pre-conv inputs: the tree conv runs here
     extern __shared__ float4 smem4[];
     float4* slots = smem4;  // [n_slots][R][32 row groups][V][8 lanes]
-    uint8_t* stage = reinterpret_cast<uint8_t*>(smem4) + tree_slot_bytes<DK, R>(G == 1 ? p.n_slots : p.walk_slots,
+    const int W = MB == 1 ? p.walkers : 1;   // walkers (CTAs) per row block
+    const int walker = MB == 1 ? (int)blockIdx.z : 0;
+    uint8_t* stage = reinterpret_cast<uint8_t*>(smem4) + tree_slot_bytes<DK, R>(W == 1 ? p.n_slots : p.walk_slots,
                                                                                    p.Nmax, conv);
     float4* s_kq = reinterpret_cast<float4*>(stage);                                   // per-node records
     uint16_t* s_v = reinterpret_cast<uint16_t*>(stage + tree_kq_bytes<DK>(p.Nmax));        // [N][32 R]
     float* s_ab = reinterpret_cast<float*>(s_v + (size_t)p.Nmax * ROWS);                    // [N][alpha, beta]
-    // the walks' schedules, walker g's at steps + g Nmax (staged below)
+    // the walk's schedule (this walker's), staged from the parameters below
     TreeStep* steps = reinterpret_cast<TreeStep*>(s_ab + 2 * (size_t)p.Nmax);
     // the fused conv's ancestor table, [N] x (3 ancestors + pad), copied out of the parameters
-    char4* s_anc = reinterpret_cast<char4*>(steps + G * p.Nmax);
+    char4* s_anc = reinterpret_cast<char4*>(steps + p.Nmax);
     // KDA: the nodes' decay vectors for head h, [N][DK / 4] float4, after the staging
-    float4* s_gate = reinterpret_cast<float4*>(stage + tree_stage_bytes<DK, R, G>(p.Nmax));
+    float4* s_gate = reinterpret_cast<float4*>(stage + tree_stage_bytes<DK, R>(p.Nmax));
     const int lane8 = threadIdx.x & 7;
-    const int walker = G == 1 ? 0 : (int)threadIdx.x / kThreads;
-    const int rg = (threadIdx.x % kThreads) >> 3;  // row group within the walker
+    const int rg = threadIdx.x >> 3;
     const int h = blockIdx.y;
     const int g = h / p.group;
     const int row0 = blockIdx.x * ROWS;
@@ -433,14 +435,12 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
 
     // the walks' schedules, copied out of the parameter block (read once per
     // step on the walk's dependent chain)
+    const int NS = W == 1 ? N : p.walk_n[walker];  // steps of this walk
     auto stage_steps = [&] {
-        if constexpr (G == 1) {
+        if (W == 1) {
             for (int n = threadIdx.x; n < N; n += NT) steps[n] = p.steps[tree][n];
         } else {
-            for (int i = threadIdx.x; i < G * p.Nmax; i += NT) {
-                const int g = i / p.Nmax, k = i % p.Nmax;
-                if (k < p.walk_n[g]) steps[i] = p.walk[MB == 1 ? g : 0][MB == 1 ? k : 0];
-            }
+            for (int k = threadIdx.x; k < NS; k += NT) steps[k] = p.walk[MB == 1 ? walker : 0][MB == 1 ? k : 0];
         }
     };
 
@@ -526,9 +526,18 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
                 *reinterpret_cast<uint4*>(dst) = y;
             }
         }
-        for (int idx = threadIdx.x; idx < N * (ROWS / 8); idx += NT) {
-            const int n = idx / (ROWS / 8), c = idx % (ROWS / 8);
-            *reinterpret_cast<uint4*>(s_v + (size_t)n * ROWS + 8 * c) = conv_task(n, QK8 + c);
+        if (p.cluster_rows) {  // the cluster's CTAs hold the same rows: split the v tasks too
+            for (int t = threadIdx.x; t * csize + (int)rank < N * (ROWS / 8); t += NT) {
+                const int j = t * csize + (int)rank;
+                const int n = j / (ROWS / 8), c = j % (ROWS / 8);
+                const uint4 y = conv_task(n, QK8 + c);
+                for (int r = 0; r < csize; ++r) st_cluster16(s_v + (size_t)n * ROWS + 8 * c, (uint32_t)r, y);
+            }
+        } else {
+            for (int idx = threadIdx.x; idx < N * (ROWS / 8); idx += NT) {
+                const int n = idx / (ROWS / 8), c = idx % (ROWS / 8);
+                *reinterpret_cast<uint4*>(s_v + (size_t)n * ROWS + 8 * c) = conv_task(n, QK8 + c);
+            }
         }
         // every CTA's y_qk is complete (and no remote store is still to come:
         // a CTA may leave the cluster only after this point)
@@ -564,9 +573,8 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     // token_kq reduces with full-warp shuffles, so the loop is warp-uniform:
     // all four row groups of a warp iterate together (on a clamped node when
     // they run past N) and only the groups with a real node write.
-    const int rgc = threadIdx.x >> 3;  // row group within the CTA
-    for (int n0 = rgc & ~3; n0 < N; n0 += NT / 8) {
-        const int n = n0 + (rgc & 3);
+    for (int n0 = rg & ~3; n0 < N; n0 += kRowsPerPass) {
+        const int n = n0 + (rg & 3);
         const bool real = n < N;
         TokenKQ<V> t;
         const int nc = real ? n : N - 1;
@@ -605,8 +613,7 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     auto slot_at = [&](int slot, int r, int m) -> float4& {
         return slots[(((slot * R + r) * kRowsPerPass + rg) * V + m) * 8 + lane8];
     };
-    const TreeStep* my_steps = steps + walker * p.Nmax;
-    const int NS = G == 1 ? N : p.walk_n[walker];  // steps of this walker
+    const TreeStep* my_steps = steps;
     auto walk_step = [&](int step, const TokenKQ<V>& cur, TokenKQ<V>& nxt) {
         const TreeStep st = my_steps[step];
         if (st.restore >= 0) {
@@ -1051,15 +1058,16 @@ cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int g
                : launch_decode_k<false, false>(p, dk, rows_per_cta, s);
 }
 
-template <int DK, int R, int G = 1>
+template <int DK, int R>
 static size_t tree_smem_bytes(int n_slots, int N, bool conv, bool kda) {
-    return tree_slot_bytes<DK, R>(n_slots, N, conv) + tree_stage_bytes<DK, R, G>(N) + (kda ? (size_t)N * DK * 4 : 0);
+    return tree_slot_bytes<DK, R>(n_slots, N, conv) + tree_stage_bytes<DK, R>(N) + (kda ? (size_t)N * DK * 4 : 0);
 }
 
-template <int DK, int MB, int R, bool KDA, int G = 1>
+template <int DK, int MB, int R, bool KDA>
 static cudaError_t launch_tree_t(TreeParamsT<MB>& p, cudaStream_t s) {
     constexpr int ROWS = kRowsPerPass * R;
-    const size_t smem = tree_smem_bytes<DK, R, G>(G == 1 ? p.n_slots : p.walk_slots, p.Nmax, p.x != nullptr, KDA);
+    const int W = MB == 1 ? p.walkers : 1;
+    const size_t smem = tree_smem_bytes<DK, R>(W == 1 ? p.n_slots : p.walk_slots, p.Nmax, p.x != nullptr, KDA);
     // the shared-memory opt-in, once per device whatever the host threads
     static std::once_flag once[64];
     static cudaError_t setup_err[64];
@@ -1068,54 +1076,63 @@ static cudaError_t launch_tree_t(TreeParamsT<MB>& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::call_once(once[dev], [dev] {
-        const int max_smem = std::min(
-            (int)tree_smem_bytes<DK, R, G>(G * GDN_MAX_TREE_SLOTS, GDN_MAX_TREE_NODES, true, KDA), kMaxSmemPerCta);
-        setup_err[dev] = cudaFuncSetAttribute(gdn_tree_kernel<DK, MB, R, KDA, G>,
+        const int max_smem = std::min((int)tree_smem_bytes<DK, R>(GDN_MAX_TREE_SLOTS, GDN_MAX_TREE_NODES, true, KDA),
+                                      kMaxSmemPerCta);
+        setup_err[dev] = cudaFuncSetAttribute(gdn_tree_kernel<DK, MB, R, KDA>,
                                               cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     });
     if (setup_err[dev] != cudaSuccess) return setup_err[dev];
-    dim3 grid(p.dv / ROWS, p.Hv, p.B);
+    dim3 grid(p.dv / ROWS, p.Hv, MB == 1 ? W : p.B);
     // The fused conv shares each key head's q/k conv among the CTAs that read
-    // it -- the row blocks of its value heads, adjacent in the grid -- as one
-    // thread-block cluster (at most the portable 8 CTAs).  If the cluster
-    // cannot be placed, the launch falls back to one CTA per cluster.
-    const int csize = (p.dv / ROWS) * p.group;
+    // it as one thread-block cluster (at most the portable 8 CTAs): the row
+    // blocks of its value heads, adjacent in the grid; or, with walkers, the
+    // walkers of one row block, which share the v conv as well (clusters of
+    // three place far more easily than of six with two CTAs to an SM).  If
+    // the cluster cannot be placed, the launch falls back to one CTA per
+    // cluster.
+    const int cx = W == 1 ? p.dv / ROWS : 1, cy = W == 1 ? p.group : 1, cz = W;
+    const int csize = cx * cy * cz;
+    p.cluster_rows = W > 1;
     if (p.x != nullptr && csize > 1 && csize <= 8) {
         p.cluster = csize;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;
-        cfg.blockDim = dim3(kThreads * G);
+        cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = s;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)(p.dv / ROWS);
-        attr[0].val.clusterDim.y = (unsigned)p.group;
-        attr[0].val.clusterDim.z = 1;
+        attr[0].val.clusterDim.x = (unsigned)cx;
+        attr[0].val.clusterDim.y = (unsigned)cy;
+        attr[0].val.clusterDim.z = (unsigned)cz;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, gdn_tree_kernel<DK, MB, R, KDA, G>, p) == cudaSuccess) return cudaSuccess;
+        if (cudaLaunchKernelEx(&cfg, gdn_tree_kernel<DK, MB, R, KDA>, p) == cudaSuccess) return cudaSuccess;
         (void)cudaGetLastError();  // a configuration error, not sticky: take the plain launch
     }
     p.cluster = 1;
-    gdn_tree_kernel<DK, MB, R, KDA, G><<<grid, kThreads * G, smem, s>>>(p);
+    p.cluster_rows = 0;
+    gdn_tree_kernel<DK, MB, R, KDA><<<grid, kThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 
 // Rows per thread: 2 when the value head has a multiple of 64 rows and the
 // slots for them fit in shared memory (each node's record then serves two
 // rows per fetch), else 1.
-// Two walkers (one tree, the scalar-gated step): when the host split the
-// tree, the value head has a multiple of 64 rows, both walkers' slots fit,
-// and the grid leaves every CTA an SM of its own (a 512-thread CTA of this
-// kernel takes most of an SM's registers).
+// Walkers (one tree): when the host split the tree, the value head has a
+// multiple of 64 rows, and two CTAs fit on an SM (registers: the launch
+// bounds; shared memory: the walkers' slots and staging), so that the grid
+// of W x row blocks x heads CTAs runs in one wave.
 template <int DK, int MB, bool KDA>
 static cudaError_t launch_tree_r(TreeParamsT<MB>& p, cudaStream_t s) {
-    if constexpr (MB == 1 && !KDA) {
-        if (p.walkers == 2 && p.dv % (2 * kRowsPerPass) == 0 &&
-            (p.dv / (2 * kRowsPerPass)) * p.Hv <= device_sm_count() &&
-            tree_smem_bytes<DK, 2, 2>(p.walk_slots, p.Nmax, p.x != nullptr, false) <= (size_t)kMaxSmemPerCta)
-            return launch_tree_t<DK, MB, 2, false, 2>(p, s);
+    if constexpr (MB == 1) {
+        if (p.walkers > 1) {
+            const bool fits = p.dv % (2 * kRowsPerPass) == 0 &&
+                              (p.dv / (2 * kRowsPerPass)) * p.Hv * p.walkers <= 2 * device_sm_count() &&
+                              tree_smem_bytes<DK, 2>(p.walk_slots, p.Nmax, p.x != nullptr, KDA) <= kSmemTwoCtas;
+            if (fits) return launch_tree_t<DK, MB, 2, KDA>(p, s);
+            p.walkers = 1;
+        }
     }
     const size_t smem2 = tree_smem_bytes<DK, 2>(p.n_slots, p.Nmax, p.x != nullptr, KDA);
     if (p.dv % (2 * kRowsPerPass) == 0 && smem2 <= (size_t)kMaxSmemPerCta) return launch_tree_t<DK, MB, 2, KDA>(p, s);

@@ -39,6 +39,8 @@ struct TreeStep {
                       // by the second walker, whose output the first writes
 };
 
+constexpr int kMaxWalkers = 3;
+
 // Tree verify over up to MB trees (one per sequence) in one launch.
 template <int MB>
 struct TreeParamsT {
@@ -61,15 +63,17 @@ struct TreeParamsT {
     const uint16_t* tail;  // bf16 [B, 4, C] read only
     int8_t anc[MB][GDN_MAX_TREE_NODES][3];
     int cluster;           // CTAs per thread-block cluster sharing the q/k conv (1: no cluster; set by the launcher)
+    int cluster_rows;      // 1: the cluster's CTAs hold the same rows (a row block's walkers), so they share the v conv too
     int kda;               // a decay per key channel: alpha is [B, Nmax, Hv, dk]
-    // Two walkers per CTA (one tree, walkers == 2): the tree's preorder split
-    // in two, walker g running walk[g][0 .. walk_n[g] - 1] over the same rows
-    // with its own branch slots (walk_slots in all).  The launcher takes this
-    // schedule instead of steps[0] when the second walker fits.
-    TreeStep walk[MB == 1 ? 2 : 1][MB == 1 ? GDN_MAX_TREE_NODES : 1];
-    int walk_n[2];
+    // Walkers (one tree, walkers > 1): the tree's preorder cut into
+    // `walkers` ranges, walker w's CTAs running walk[w][0 .. walk_n[w] - 1]
+    // over their rows with branch slots 0 .. walk_slots - 1 of their own.  The
+    // launcher takes this schedule instead of steps[0] when the walkers fit
+    // (and sets walkers back to 1 when they do not).
+    TreeStep walk[MB == 1 ? kMaxWalkers : 1][MB == 1 ? GDN_MAX_TREE_NODES : 1];
+    int walk_n[kMaxWalkers];
     int walk_slots;
-    int walkers;           // 2 when walk[] holds a split schedule, else 1
+    int walkers;           // CTAs walking one row block's part of the tree (1 .. kMaxWalkers)
 };
 constexpr int kMaxTreeBatch = 32;
 using TreeParams = TreeParamsT<1>;

@@ -89,10 +89,10 @@ def _caterpillar(n):
 @pytest.mark.parametrize("parents", [_binary_tree(63), _caterpillar(17), gen.random_tree(11, 64, 8),
                                      gen.random_tree(12, 48, 12), gen.random_tree(13, 64, 4)])
 def test_tree_walk_shapes_equal_decode_bitwise(parents):
-    """Whatever walk the host schedules (the tree split between two walkers
-    where that shortens the walk and their branch states fit, else one
-    depth-first walk), every node's output is the bits of the linear decode
-    of its root path."""
+    """Whatever walk the host schedules (the tree split between walkers where
+    that shortens the walk and their branch states fit, else one depth-first
+    walk), every node's output is the bits of the linear decode of its root
+    path."""
     shape = gen.QWEN_27B
     _, d = _tree_case(shape, len(parents), 5, parents=parents)
     out = _verify(shape, parents, d)
@@ -104,10 +104,11 @@ def test_tree_walk_shapes_equal_decode_bitwise(parents):
 @pytest.mark.parametrize("parents", [gen.random_tree(1234, 32, 8), gen.random_tree(0, 32, 8), _caterpillar(17),
                                      gen.random_tree(12, 48, 12), gen.random_tree(3, 8, 8), _binary_tree(63),
                                      np.arange(-1, 31, dtype=np.int32)])
-def test_two_walkers_equal_one_walker_bitwise(parents):
-    """A single tree's verify splits the tree between two walkers when that
-    shortens the walk; the joint verify (one tree here) always walks it
-    whole.  Both give the same bits, with post-conv and pre-conv inputs."""
+def test_walkers_equal_one_walker_bitwise(parents):
+    """A single tree's verify splits the tree between up to three walkers
+    (CTAs holding the same rows, each walking part of the tree) when that
+    shortens the walk; the joint verify (one tree here) always walks it whole.
+    Both give the same bits, with post-conv and pre-conv inputs."""
     shape = gen.QWEN_27B
     N = len(parents)
     _, d = _tree_case(shape, N, 21, parents=parents)
