@@ -80,6 +80,35 @@ __device__ __forceinline__ void st_cluster16(const void* local, uint32_t rank, u
                  : "memory");
 }
 
+// Tensor memory as the tree walk's branch slots.  A thread's rows of one slot
+// (R V float4) sit in its own TMEM lane, 4 R V consecutive columns: warp w
+// uses the lanes of quarter w mod 4 and the columns of half w / 4, so a slot
+// takes 8 R V columns.  Loads and stores are exact 32-bit moves, and they
+// leave the shared-memory pipe to the walk's record fetches.
+template <int R, int V>
+__device__ __forceinline__ void tmem_put_rows(uint32_t taddr, const float4 (&s)[R][V]) {
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < V; ++m)
+            asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             taddr + (uint32_t)(4 * (r * V + m))),
+                         "f"(s[r][m].x), "f"(s[r][m].y), "f"(s[r][m].z), "f"(s[r][m].w)
+                         : "memory");
+}
+template <int R, int V>
+__device__ __forceinline__ void tmem_get_rows(uint32_t taddr, float4 (&s)[R][V]) {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");  // this thread's earlier saves
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < V; ++m)
+            asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(s[r][m].x), "=f"(s[r][m].y), "=f"(s[r][m].z), "=f"(s[r][m].w)
+                         : "r"(taddr + (uint32_t)(4 * (r * V + m))));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 // The conv-tail update of a commit, done by the commit's own launch: the
 // tail becomes the last four inputs of (tail ++ x_tree[path[0]] ++ ...), 8
 // channels (one 16-byte vector) per thread of the grid, copied as they are.
@@ -403,8 +432,8 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     float4* slots = smem4;  // [n_slots][R][32 row groups][V][8 lanes]
     const int W = MB == 1 ? p.walkers : 1;   // walkers (CTAs) per row block
     const int walker = MB == 1 ? (int)blockIdx.z : 0;
-    uint8_t* stage = reinterpret_cast<uint8_t*>(smem4) + tree_slot_bytes<DK, R>(W == 1 ? p.n_slots : p.walk_slots,
-                                                                                   p.Nmax, conv);
+    uint8_t* stage = reinterpret_cast<uint8_t*>(smem4) +
+                     tree_slot_bytes<DK, R>(p.tmem_cols > 0 ? 0 : W == 1 ? p.n_slots : p.walk_slots, p.Nmax, conv);
     float4* s_kq = reinterpret_cast<float4*>(stage);                                   // per-node records
     uint16_t* s_v = reinterpret_cast<uint16_t*>(stage + tree_kq_bytes<DK>(p.Nmax));        // [N][32 R]
     float* s_ab = reinterpret_cast<float*>(s_v + (size_t)p.Nmax * ROWS);                    // [N][alpha, beta]
@@ -422,6 +451,21 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     const int row = row0 + rg;  // this thread's rows: row + 32 r
     // node n's record in s_kq: [V float4 of k, V float4 of q][8 lanes], then k.q
     constexpr int KQ_REC = 8 * 2 * V + 1;  // float4 units
+
+    // branch slots in tensor memory (p.tmem_cols columns, at most half of an
+    // SM's, so that two CTAs fit), allocated by warp 0 before the staging; the
+    // allocation's address goes to the last word of the dynamic shared memory
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(stage + tree_stage_bytes<DK, R>(p.Nmax) +
+                                                   (KDA ? (size_t)p.Nmax * DK * 4 : 0));
+    const bool tm = p.tmem_cols > 0;
+    if (tm && threadIdx.x < 32) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         (uint32_t)__cvta_generic_to_shared(s_tmem)),
+                     "r"((uint32_t)p.tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    }
 
     // this thread's rows of the committed state, requested before the staging
     // loads so that the two DRAM round trips overlap
@@ -613,14 +657,25 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     auto slot_at = [&](int slot, int r, int m) -> float4& {
         return slots[(((slot * R + r) * kRowsPerPass + rg) * V + m) * 8 + lane8];
     };
+    uint32_t tm_warp = 0;  // this warp's first slot column block (lane quarter, column half)
+    if (tm) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const int warp = threadIdx.x >> 5;
+        tm_warp = *s_tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)((warp >> 2) * 4 * R * V);
+    }
+    constexpr uint32_t kSlotCols = 8 * R * V;
     const TreeStep* my_steps = steps;
     auto walk_step = [&](int step, const TokenKQ<V>& cur, TokenKQ<V>& nxt) {
         const TreeStep st = my_steps[step];
         if (st.restore >= 0) {
+            if (tm) {
+                tmem_get_rows<R, V>(tm_warp + (uint32_t)st.restore * kSlotCols, s);
+            } else {
 #pragma unroll
-            for (int r = 0; r < R; ++r)
+                for (int r = 0; r < R; ++r)
 #pragma unroll
-                for (int m = 0; m < V; ++m) s[r][m] = slot_at(st.restore, r, m);
+                    for (int m = 0; m < V; ++m) s[r][m] = slot_at(st.restore, r, m);
+            }
         }
         const int node = st.node;
         if (step + 1 < NS) fetch(my_steps[step + 1].node, nxt);
@@ -653,10 +708,14 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
             store_out(p.out, (((size_t)tree * p.Nmax + node) * p.Hv + h) * p.dv + row + kRowsPerPass * lane8, my_o,
                       out_bf16);
         if (st.save >= 0) {
+            if (tm) {
+                tmem_put_rows<R, V>(tm_warp + (uint32_t)st.save * kSlotCols, s);
+            } else {
 #pragma unroll
-            for (int r = 0; r < R; ++r)
+                for (int r = 0; r < R; ++r)
 #pragma unroll
-                for (int m = 0; m < V; ++m) slot_at(st.save, r, m) = s[r][m];
+                    for (int m = 0; m < V; ++m) slot_at(st.save, r, m) = s[r][m];
+            }
         }
     };
     TokenKQ<V> ka, kb;
@@ -664,6 +723,15 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     for (int step = 0; step < NS; step += 2) {
         walk_step(step, ka, kb);
         if (step + 1 < NS) walk_step(step + 1, kb, ka);
+    }
+    if (tm) {  // every thread's TMEM stores done, then warp 0 frees the columns
+        asm volatile("tcgen05.wait::st.sync.aligned;\n\ttcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(*s_tmem), "r"((uint32_t)p.tmem_cols)
+                         : "memory");
+        }
     }
 }
 
@@ -1060,14 +1128,35 @@ cudaError_t launch_decode(const DecodeParams& p, int dk, int rows_per_cta, int g
 
 template <int DK, int R>
 static size_t tree_smem_bytes(int n_slots, int N, bool conv, bool kda) {
-    return tree_slot_bytes<DK, R>(n_slots, N, conv) + tree_stage_bytes<DK, R>(N) + (kda ? (size_t)N * DK * 4 : 0);
+    // + the word for the tensor-memory address
+    return tree_slot_bytes<DK, R>(n_slots, N, conv) + tree_stage_bytes<DK, R>(N) + (kda ? (size_t)N * DK * 4 : 0) + 16;
+}
+
+// Tensor-memory columns for n_slots branch slots (8 R V each, allocated in a
+// power of two of at least 32), or 0 to keep them in shared memory: more
+// than 256 columns would leave no room for a second CTA on the SM.
+template <int DK, int R>
+static int tree_tmem_cols(int n_slots) {
+    if (n_slots <= 0) return 0;
+    const int need = n_slots * 8 * R * (DK / 32);
+    int cols = 32;
+    while (cols < need) cols *= 2;
+    return cols <= 256 ? cols : 0;
+}
+
+// Shared memory of a launch whose slots go to tensor memory when they fit.
+template <int DK, int R>
+static size_t tree_smem_bytes_tm(int n_slots, int N, bool conv, bool kda) {
+    return tree_smem_bytes<DK, R>(tree_tmem_cols<DK, R>(n_slots) > 0 ? 0 : n_slots, N, conv, kda);
 }
 
 template <int DK, int MB, int R, bool KDA>
 static cudaError_t launch_tree_t(TreeParamsT<MB>& p, cudaStream_t s) {
     constexpr int ROWS = kRowsPerPass * R;
     const int W = MB == 1 ? p.walkers : 1;
-    const size_t smem = tree_smem_bytes<DK, R>(W == 1 ? p.n_slots : p.walk_slots, p.Nmax, p.x != nullptr, KDA);
+    const int n_slots = W == 1 ? p.n_slots : p.walk_slots;
+    p.tmem_cols = tree_tmem_cols<DK, R>(n_slots);
+    const size_t smem = tree_smem_bytes_tm<DK, R>(n_slots, p.Nmax, p.x != nullptr, KDA);
     // the shared-memory opt-in, once per device whatever the host threads
     static std::once_flag once[64];
     static cudaError_t setup_err[64];
@@ -1129,12 +1218,12 @@ static cudaError_t launch_tree_r(TreeParamsT<MB>& p, cudaStream_t s) {
         if (p.walkers > 1) {
             const bool fits = p.dv % (2 * kRowsPerPass) == 0 &&
                               (p.dv / (2 * kRowsPerPass)) * p.Hv * p.walkers <= 2 * device_sm_count() &&
-                              tree_smem_bytes<DK, 2>(p.walk_slots, p.Nmax, p.x != nullptr, KDA) <= kSmemTwoCtas;
+                              tree_smem_bytes_tm<DK, 2>(p.walk_slots, p.Nmax, p.x != nullptr, KDA) <= kSmemTwoCtas;
             if (fits) return launch_tree_t<DK, MB, 2, KDA>(p, s);
             p.walkers = 1;
         }
     }
-    const size_t smem2 = tree_smem_bytes<DK, 2>(p.n_slots, p.Nmax, p.x != nullptr, KDA);
+    const size_t smem2 = tree_smem_bytes_tm<DK, 2>(p.n_slots, p.Nmax, p.x != nullptr, KDA);
     if (p.dv % (2 * kRowsPerPass) == 0 && smem2 <= (size_t)kMaxSmemPerCta) return launch_tree_t<DK, MB, 2, KDA>(p, s);
     return launch_tree_t<DK, MB, 1, KDA>(p, s);
 }

@@ -74,6 +74,7 @@ struct TreeParamsT {
     int walk_n[kMaxWalkers];
     int walk_slots;
     int walkers;           // CTAs walking one row block's part of the tree (1 .. kMaxWalkers)
+    int tmem_cols;         // > 0: the branch slots live in this many tensor-memory columns (set by the launcher)
 };
 constexpr int kMaxTreeBatch = 32;
 using TreeParams = TreeParamsT<1>;
