@@ -10,12 +10,15 @@
 //
 // Tree verify: one CTA owns 32 R rows of one value head and walks the draft
 // tree depth-first.  The current node's rows stay in registers; the rows of a
-// node with two or more children are parked in shared memory until its last
-// child starts (host-computed slots).  The committed state is read once and
-// node states never reach HBM (TandemLLM "Architecture" v0.14.2 section 8.3:
-// each draft node's state branches from its parent's and the whole tree is
-// verified in one pass).  Given pre-conv inputs, the CTA also runs the tree
-// conv of the channels it reads (a key head's CTAs share its q/k conv as one
+// node with two or more children are parked in tensor memory (or, for deep
+// nests, shared memory) until its last child starts (host-computed slots).
+// A single tree's preorder is cut into up to three walks, each run by its own
+// CTA over the same rows, so that the dependent chain of node steps is
+// shorter.  The committed state is read once and node states never reach HBM
+// (TandemLLM "Architecture" v0.14.2 section 8.3: each draft node's state
+// branches from its parent's and the whole tree is verified in one pass).
+// Given pre-conv inputs, the CTA also runs the tree conv of the channels it
+// reads (the CTAs that need the same conv outputs share the work as one
 // thread-block cluster); a KDA variant applies a decay per key channel.
 #include <cuda_runtime.h>
 
@@ -396,8 +399,9 @@ __host__ __device__ constexpr size_t tree_conv_bytes(int N) {
 
 template <int DK, int R>
 __host__ __device__ constexpr size_t tree_slot_bytes(int n_slots, int N, bool conv) {
+    // without the conv the region still holds y_qk, the staged q and k rows
     const size_t slots = (size_t)n_slots * kRowsPerPass * R * DK * sizeof(float);
-    const size_t c = conv ? tree_conv_bytes<DK, R>(N) : 0;
+    const size_t c = conv ? tree_conv_bytes<DK, R>(N) : (size_t)N * 2 * DK * 2;
     return slots > c ? slots : c;
 }
 
@@ -535,10 +539,11 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
         stage_steps();
         asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
         // With a cluster (the CTAs of one key head: its value heads' row
-        // blocks), the q/k outputs are computed once per cluster: task j goes
-        // to CTA j mod csize, which stores the result into every CTA's y_qk.
-        // The first cluster barrier also makes sure every CTA of the cluster
-        // is running before any remote store.
+        // blocks; or a row block's walkers), the q/k outputs are computed
+        // once per cluster: task j goes to CTA j mod csize, which stores the
+        // result into every CTA's y_qk (and, for walkers, which hold the same
+        // rows, the v outputs likewise).  The first cluster barrier also makes
+        // sure every CTA of the cluster is running before any remote store.
         const int csize = p.cluster;
         const uint32_t rank = csize > 1 ? cluster_rank() : 0u;
         if (csize > 1) cluster_sync_all();
@@ -587,26 +592,34 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
         // a CTA may leave the cluster only after this point)
         if (csize > 1) cluster_sync_all();
     } else {
+        // Post-conv inputs: the key head's q and k rows of every node (into
+        // y_qk, as the fused conv leaves them), this CTA's v rows, the gates
+        // and (KDA) the decay vectors, all copies in flight together beside
+        // the state loads: one DRAM round trip before the records.
+        constexpr int QK8 = 2 * DK / 8;
+        for (int idx = threadIdx.x; idx < N * QK8; idx += NT) {
+            const int n = idx / QK8, c = idx % QK8;
+            const size_t ch = c < DK / 8 ? (size_t)g * DK + 8 * c : (size_t)p.Hk * DK + g * DK + 8 * (c - DK / 8);
+            cp_async16(y_qk + (size_t)n * 2 * DK + 8 * c, qkv + (size_t)n * p.C + ch);
+        }
         for (int idx = threadIdx.x; idx < N * (ROWS / 8); idx += NT) {
             const int n = idx / (ROWS / 8), c = idx % (ROWS / 8);
-            const uint16_t* src = qkv + (size_t)n * p.C + (size_t)2 * p.Hk * DK + (size_t)h * p.dv + row0 + c * 8;
-            *reinterpret_cast<uint4*>(s_v + (size_t)n * ROWS + c * 8) = __ldg(reinterpret_cast<const uint4*>(src));
+            cp_async16(s_v + (size_t)n * ROWS + c * 8,
+                       qkv + (size_t)n * p.C + (size_t)2 * p.Hk * DK + (size_t)h * p.dv + row0 + c * 8);
         }
-    }
-    if (!conv) {  // (the fused conv staged these with its inputs)
         for (int n = threadIdx.x; n < N; n += NT) {
-            if (!KDA) s_ab[2 * n] = alpha_b[(size_t)n * p.Hv + h];
-            s_ab[2 * n + 1] = beta_b[(size_t)n * p.Hv + h];
+            if (!KDA) cp_async4(s_ab + 2 * n, alpha_b + (size_t)n * p.Hv + h);
+            cp_async4(s_ab + 2 * n + 1, beta_b + (size_t)n * p.Hv + h);
         }
         if constexpr (KDA) {
             for (int idx = threadIdx.x; idx < N * (DK / 4); idx += NT) {
                 const int n = idx / (DK / 4), c4 = idx % (DK / 4);
-                s_gate[idx] = __ldg(reinterpret_cast<const float4*>(
-                    p.alpha + (((size_t)tree * p.Nmax + n) * p.Hv + h) * DK + 4 * c4));
+                cp_async16(s_gate + idx, p.alpha + (((size_t)tree * p.Nmax + n) * p.Hv + h) * DK + 4 * c4);
             }
         }
+        stage_steps();
+        asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
     }
-    if (!conv) stage_steps();
     __syncthreads();
 
     const bool normalize = p.normalize != 0;
@@ -622,14 +635,8 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
         const bool real = n < N;
         TokenKQ<V> t;
         const int nc = real ? n : N - 1;
-        if (conv) {
-            const uint16_t* yn = y_qk + (size_t)nc * 2 * DK;
-            token_kq<V>(yn, yn + DK, lane8, p.q_scale, normalize, t);
-        } else {
-            const uint16_t* qkv_row = qkv + (size_t)nc * p.C;
-            token_kq<V>(qkv_row + (size_t)g * DK, qkv_row + (size_t)p.Hk * DK + (size_t)g * DK, lane8, p.q_scale,
-                        normalize, t);
-        }
+        const uint16_t* yn = y_qk + (size_t)nc * 2 * DK;
+        token_kq<V>(yn, yn + DK, lane8, p.q_scale, normalize, t);
         if (real) {
             float4* rec = s_kq + (size_t)n * KQ_REC + lane8;
 #pragma unroll
