@@ -18,8 +18,9 @@
 // (TandemLLM "Architecture" v0.14.2 section 8.3: each draft node's state
 // branches from its parent's and the whole tree is verified in one pass).
 // Given pre-conv inputs, the CTA also runs the tree conv of the channels it
-// reads (the CTAs that need the same conv outputs share the work as one
-// thread-block cluster); a KDA variant applies a decay per key channel.
+// reads (a key head's CTAs share its q/k conv as one thread-block cluster; a
+// walker convolves its own walk's nodes); a KDA variant applies a decay per
+// key channel.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -539,11 +540,11 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
         stage_steps();
         asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
         // With a cluster (the CTAs of one key head: its value heads' row
-        // blocks; or a row block's walkers), the q/k outputs are computed
-        // once per cluster: task j goes to CTA j mod csize, which stores the
-        // result into every CTA's y_qk (and, for walkers, which hold the same
-        // rows, the v outputs likewise).  The first cluster barrier also makes
-        // sure every CTA of the cluster is running before any remote store.
+        // blocks), the q/k outputs are computed once per cluster: task j goes
+        // to CTA j mod csize, which stores the result into every CTA's y_qk.
+        // The first cluster barrier also makes sure every CTA of the cluster
+        // is running before any remote store.  A walker (no cluster) computes
+        // the outputs of its own walk's nodes only.
         const int csize = p.cluster;
         const uint32_t rank = csize > 1 ? cluster_rank() : 0u;
         if (csize > 1) cluster_sync_all();
@@ -563,7 +564,18 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
             const Vec8 u0 = load8(xc + (size_t)row_of(anc[2]) * CW);
             return conv8_bf16(w, u0, u1, u2, u3);
         };
-        const int n_qk = N * QK8;  // q/k tasks of the tree
+        if (W > 1) {
+            // a walker needs the conv outputs of its own walk's nodes only:
+            // its range and the ancestors it replays
+            for (int idx = threadIdx.x; idx < NS * PER; idx += NT) {
+                const int i = idx / PER, c = idx % PER;
+                const int n = steps[i].node;
+                const uint4 y = conv_task(n, c);
+                if (c < QK8) *reinterpret_cast<uint4*>(y_qk + (size_t)n * 2 * DK + 8 * c) = y;
+                else *reinterpret_cast<uint4*>(s_v + (size_t)n * ROWS + 8 * (c - QK8)) = y;
+            }
+        }
+        const int n_qk = W > 1 ? 0 : N * QK8;  // q/k tasks of the tree
         for (int t = threadIdx.x; t * csize + (int)rank < n_qk; t += NT) {
             const int j = t * csize + (int)rank;
             const int n = j / QK8, c = j % QK8;
@@ -575,14 +587,7 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
                 *reinterpret_cast<uint4*>(dst) = y;
             }
         }
-        if (p.cluster_rows) {  // the cluster's CTAs hold the same rows: split the v tasks too
-            for (int t = threadIdx.x; t * csize + (int)rank < N * (ROWS / 8); t += NT) {
-                const int j = t * csize + (int)rank;
-                const int n = j / (ROWS / 8), c = j % (ROWS / 8);
-                const uint4 y = conv_task(n, QK8 + c);
-                for (int r = 0; r < csize; ++r) st_cluster16(s_v + (size_t)n * ROWS + 8 * c, (uint32_t)r, y);
-            }
-        } else {
+        if (W == 1) {
             for (int idx = threadIdx.x; idx < N * (ROWS / 8); idx += NT) {
                 const int n = idx / (ROWS / 8), c = idx % (ROWS / 8);
                 *reinterpret_cast<uint4*>(s_v + (size_t)n * ROWS + 8 * c) = conv_task(n, QK8 + c);
@@ -630,12 +635,15 @@ gdn_tree_kernel(const __grid_constant__ TreeParamsT<MB> p) {
     // token_kq reduces with full-warp shuffles, so the loop is warp-uniform:
     // all four row groups of a warp iterate together (on a clamped node when
     // they run past N) and only the groups with a real node write.
-    for (int n0 = rg & ~3; n0 < N; n0 += kRowsPerPass) {
-        const int n = n0 + (rg & 3);
-        const bool real = n < N;
+    // (a walker: the records of its own walk's nodes only)
+    const int NR = W > 1 ? NS : N;
+    for (int i0 = rg & ~3; i0 < NR; i0 += kRowsPerPass) {
+        const int i = i0 + (rg & 3);
+        const bool real = i < NR;
         TokenKQ<V> t;
-        const int nc = real ? n : N - 1;
-        const uint16_t* yn = y_qk + (size_t)nc * 2 * DK;
+        const int ic = real ? i : NR - 1;
+        const int n = W > 1 ? (int)steps[ic].node : ic;
+        const uint16_t* yn = y_qk + (size_t)n * 2 * DK;
         token_kq<V>(yn, yn + DK, lane8, p.q_scale, normalize, t);
         if (real) {
             float4* rec = s_kq + (size_t)n * KQ_REC + lane8;
@@ -1180,16 +1188,15 @@ static cudaError_t launch_tree_t(TreeParamsT<MB>& p, cudaStream_t s) {
     if (setup_err[dev] != cudaSuccess) return setup_err[dev];
     dim3 grid(p.dv / ROWS, p.Hv, MB == 1 ? W : p.B);
     // The fused conv shares each key head's q/k conv among the CTAs that read
-    // it as one thread-block cluster (at most the portable 8 CTAs): the row
-    // blocks of its value heads, adjacent in the grid; or, with walkers, the
-    // walkers of one row block, which share the v conv as well (clusters of
-    // three place far more easily than of six with two CTAs to an SM).  If
+    // it -- the row blocks of its value heads, adjacent in the grid -- as one
+    // thread-block cluster (at most the portable 8 CTAs).  Walkers run
+    // without one: each computes only its own walk's nodes, which measured
+    // faster than sharing all of a row block's conv in clusters of three.  If
     // the cluster cannot be placed, the launch falls back to one CTA per
     // cluster.
-    const int cx = W == 1 ? p.dv / ROWS : 1, cy = W == 1 ? p.group : 1, cz = W;
-    const int csize = cx * cy * cz;
-    p.cluster_rows = W > 1;
-    if (p.x != nullptr && csize > 1 && csize <= 8) {
+    const int cx = p.dv / ROWS, cy = p.group;
+    const int csize = cx * cy;
+    if (p.x != nullptr && csize > 1 && csize <= 8 && W == 1) {
         p.cluster = csize;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;
@@ -1200,14 +1207,13 @@ static cudaError_t launch_tree_t(TreeParamsT<MB>& p, cudaStream_t s) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = (unsigned)cx;
         attr[0].val.clusterDim.y = (unsigned)cy;
-        attr[0].val.clusterDim.z = (unsigned)cz;
+        attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         if (cudaLaunchKernelEx(&cfg, gdn_tree_kernel<DK, MB, R, KDA>, p) == cudaSuccess) return cudaSuccess;
         (void)cudaGetLastError();  // a configuration error, not sticky: take the plain launch
     }
     p.cluster = 1;
-    p.cluster_rows = 0;
     gdn_tree_kernel<DK, MB, R, KDA><<<grid, kThreads, smem, s>>>(p);
     return cudaGetLastError();
 }

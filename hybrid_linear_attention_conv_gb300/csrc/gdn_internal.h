@@ -63,7 +63,6 @@ struct TreeParamsT {
     const uint16_t* tail;  // bf16 [B, 4, C] read only
     int8_t anc[MB][GDN_MAX_TREE_NODES][3];
     int cluster;           // CTAs per thread-block cluster sharing the q/k conv (1: no cluster; set by the launcher)
-    int cluster_rows;      // 1: the cluster's CTAs hold the same rows (a row block's walkers), so they share the v conv too
     int kda;               // a decay per key channel: alpha is [B, Nmax, Hv, dk]
     // Walkers (one tree, walkers > 1): the tree's preorder cut into
     // `walkers` ranges, walker w's CTAs running walk[w][0 .. walk_n[w] - 1]
