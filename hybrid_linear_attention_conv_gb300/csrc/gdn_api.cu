@@ -137,7 +137,7 @@ int schedule_tree(int N, const int32_t* parents, TreeStep* steps, int* n_slots) 
     return GDN_OK;
 }
 
-// The walk of one of two walkers: a depth-first preorder over `member` (a
+// The walk of one walker: a depth-first preorder over `member` (a
 // set of nodes closed under taking parents, so a subtree holding the root),
 // writing the outputs of the nodes in `own`.  The children of a node are
 // visited in increasing order of the branch slots their own subtrees need,
