@@ -401,9 +401,9 @@ int gdn_kda_commit_path(const gdn_shape* shape, int32_t N, const int32_t* parent
  * and run the 4-tap conv + SiLU inside the verify and commit kernels, so the
  * conv outputs never reach HBM and the round is two launches instead of three.
  * The kernels compute the conv outputs they read (a key head's q and k, shared
- * by the CTAs that read them, and each CTA's own rows of v) with the
- * arithmetic and bf16 rounding of gdn_conv_step, so the results are the same
- * bits as the unfused calls.
+ * by the CTAs that read them or computed for just the nodes a CTA walks, and
+ * each CTA's own rows of v) with the arithmetic and bf16 rounding of
+ * gdn_conv_step, so the results are the same bits as the unfused calls.
  *
  * gdn_conv_tree_verify -- gdn_conv_step in tree mode (x -> y) followed by
  * gdn_tree_verify on y, in one launch.  out equals that pair's, bit for bit.
